@@ -1,0 +1,180 @@
+"""ctypes wrapper around the fp64 CPU oracle in loglinear_oracle.c.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, by ``__graft_entry__.smoke()``
+and by the CPU-baseline leg of ``bench.py``; never by the product path.  It
+shares no code with the CUDA path: it takes numpy arrays (already rounded to
+the dtype the GPU consumes) and returns fp64 numpy arrays.
+
+What each function computes, and the passage it follows, is stated in the C
+file's header and above each C function.  Summary:
+
+* ``level(t, s)``           Fenwick level of key s for query t (page 1 of the
+                            sources, 特殊结构：树划分).
+* ``prefix_buckets(n)``     binary-indexed-tree segments of the prefix [0, n).
+* ``form_q``                quadratic masked form (QKᵀ ⊙ M^S ⊙ M^H) V.
+* ``form_q_points``         the same at chosen query positions of one head.
+* ``form_r``                recurrent per-bucket-state form, optional export
+                            of the bucket states at position T.
+* ``form_r_head``           one head, capturing states at chosen positions.
+* ``brute``                 dense masks built by explicit loops (small T).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "loglinear_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libloglinear_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_L = ctypes.POINTER(ctypes.c_long)
+_l = ctypes.c_long
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP) into oracle/_build/."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_level.restype = ctypes.c_int
+            lib.oracle_level.argtypes = [_l, _l]
+            lib.oracle_prefix_buckets.restype = ctypes.c_int
+            lib.oracle_prefix_buckets.argtypes = [_l, _L, _L, ctypes.c_int]
+            lib.oracle_num_threads.restype = ctypes.c_int
+            six = [_l] * 7
+            lib.oracle_form_q.argtypes = six + [_D] * 6
+            lib.oracle_brute.argtypes = six + [_D] * 6
+            lib.oracle_form_r.argtypes = six + [_D] * 7 + [_l]
+            lib.oracle_form_q_points.argtypes = [_l] * 4 + [_D] * 5 + [_L, _l, _D]
+            lib.oracle_form_r_head.argtypes = [_l] * 4 + [_D] * 6 + [_l, _l, _L, _D]
+            for f in ("oracle_form_q", "oracle_brute", "oracle_form_r", "oracle_form_q_points",
+                      "oracle_form_r_head"):
+                getattr(lib, f).restype = None
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def _d(x: np.ndarray):
+    return x.ctypes.data_as(_D)
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _bitlen(x: int) -> int:
+    return int(x).bit_length()
+
+
+def level(t: int, s: int) -> int:
+    return int(_load().oracle_level(int(t), int(s)))
+
+
+def prefix_buckets(n: int):
+    """Segments (start, length) of the prefix [0, n), nearest first."""
+    lo = (ctypes.c_long * 64)()
+    ln = (ctypes.c_long * 64)()
+    c = _load().oracle_prefix_buckets(int(n), lo, ln, 64)
+    return [(int(lo[i]), int(ln[i])) for i in range(c)]
+
+
+def _check(q, k, v, a, lam):
+    q, k, v, a, lam = (_f64(x) for x in (q, k, v, a, lam))
+    B, T, G, dk = q.shape
+    H, dv = v.shape[2], v.shape[3]
+    L = lam.shape[3]
+    assert k.shape == q.shape and v.shape[:2] == (B, T) and a.shape == (B, T, H)
+    assert lam.shape[:3] == (B, T, H) and H % G == 0
+    if T > 0:
+        assert L >= _bitlen(T - 1) + 1, "lambda needs bit_length(T-1)+1 levels"
+    return q, k, v, a, lam, (B, T, H, H // G, dk, dv, L)
+
+
+def form_q(q, k, v, a, lam) -> np.ndarray:
+    q, k, v, a, lam, shp = _check(q, k, v, a, lam)
+    B, T, H, _, _, dv, _ = shp
+    o = np.zeros((B, T, H, dv), dtype=np.float64)
+    _load().oracle_form_q(*shp, _d(q), _d(k), _d(v), _d(a), _d(lam), _d(o))
+    return o
+
+
+def brute(q, k, v, a, lam) -> np.ndarray:
+    q, k, v, a, lam, shp = _check(q, k, v, a, lam)
+    B, T, H, _, _, dv, _ = shp
+    assert T <= 256, "brute force is for small T"
+    o = np.zeros((B, T, H, dv), dtype=np.float64)
+    _load().oracle_brute(*shp, _d(q), _d(k), _d(v), _d(a), _d(lam), _d(o))
+    return o
+
+
+def form_r(q, k, v, a, lam, export_levels: int | None = None):
+    """Returns o, and the bucket states at position T when export_levels is given
+    (shape (B, H, export_levels, dk, dv))."""
+    q, k, v, a, lam, shp = _check(q, k, v, a, lam)
+    B, T, H, _, dk, dv, L = shp
+    Ls = max(L, _bitlen(T) + 1)
+    if export_levels is not None:
+        assert export_levels >= _bitlen(T) + 1
+        Ls = max(Ls, export_levels)
+    o = np.zeros((B, T, H, dv), dtype=np.float64)
+    st = np.zeros((B, H, Ls, dk, dv), dtype=np.float64) if export_levels is not None else None
+    _load().oracle_form_r(*shp, _d(q), _d(k), _d(v), _d(a), _d(lam), _d(o),
+                          _d(st) if st is not None else None, Ls)
+    if st is None:
+        return o
+    return o, st[:, :, :export_levels]
+
+
+def form_q_points(q, k, v, a, lam_pts, ts) -> np.ndarray:
+    """One head: q, k (T', dk), v (T', dv), a (T'), lam_pts (n, L) for the
+    queries ts (n); positions are 0-based and ts < T'.  Returns (n, dv)."""
+    q, k, v, a, lam_pts = (_f64(x) for x in (q, k, v, a, lam_pts))
+    ts = np.ascontiguousarray(np.asarray(ts, dtype=np.int64))
+    T, dk = q.shape
+    dv = v.shape[1]
+    n, L = lam_pts.shape
+    assert ts.shape == (n,) and (n == 0 or (ts.min() >= 0 and ts.max() < T))
+    assert n == 0 or L >= _bitlen(int(ts.max())) + 1
+    o = np.zeros((n, dv), dtype=np.float64)
+    _load().oracle_form_q_points(T, dk, dv, L, _d(q), _d(k), _d(v), _d(a), _d(lam_pts),
+                                 ts.ctypes.data_as(_L), n, _d(o))
+    return o
+
+
+def form_r_head(q, k, v, a, lam, cap_pos, levels: int):
+    """One head over T tokens: returns o (T, dv) and states (len(cap_pos),
+    levels, dk, dv) captured at each position in cap_pos (ascending, <= T)."""
+    q, k, v, a, lam = (_f64(x) for x in (q, k, v, a, lam))
+    T, dk = q.shape
+    dv = v.shape[1]
+    L = lam.shape[1]
+    cap = np.ascontiguousarray(np.asarray(cap_pos, dtype=np.int64))
+    assert np.all(np.diff(cap) >= 0) and (cap.size == 0 or cap.max() <= T)
+    assert levels >= _bitlen(T) + 1 and L >= _bitlen(max(T - 1, 0)) + 1
+    o = np.zeros((T, dv), dtype=np.float64)
+    st = np.zeros((cap.size, levels, dk, dv), dtype=np.float64)
+    _load().oracle_form_r_head(T, dk, dv, L, _d(q), _d(k), _d(v), _d(a), _d(lam), _d(o),
+                               levels, cap.size, cap.ctypes.data_as(_L), _d(st))
+    return o, st
