@@ -1,0 +1,192 @@
+/*
+ * loglinear.h — C ABI of the log-linear Mamba-2 forward and decode step
+ * (sm_103a, one GPU).
+ *
+ * What is computed.  For every batch b, head h and query position t
+ * (0-indexed), with group g = h / heads_per_group:
+ *
+ *     o[b,t,h,:] = sum_{s <= t} lambda[b,t,h, l(t,s)] * M^S(t,s) * (q[b,t,g,:] . k[b,s,g,:]) * v[b,s,h,:]
+ *
+ *   M^S(t,s) = a[b,s+1,h] * ... * a[b,t,h]   (Mamba-2 scalar-decay, 1-semiseparable mask;
+ *              state-space-duality article http://biyoush.com/article/202409/463109.htm,
+ *              section 狀態空間對偶性)
+ *   l(t,s)   = 0 if s == t, else the bit length of (t xor s): the level of the Fenwick-tree
+ *              bucket of t that holds s; buckets have power-of-two sizes and are finer near t
+ *              (log-linear attention write-up https://www.yoousoft.com/industry/3746.html,
+ *              section 特殊结构：树划分; the mask M^H(t,s) = lambda_t^{l(t,s)} and its
+ *              composition with M^S, section 对Mamba-2和门控的对数线性推广).
+ *
+ * The forward uses the chunkwise algorithm of the write-up (section 高效训练算法):
+ * dense masked products inside aligned chunks and a hierarchical state pass
+ * across chunks.  The result does not depend on the chunk length; it is an exact
+ * re-association of the sum above.
+ *
+ * Conventions shared by all entry points.
+ *  - Every tensor is row-major and contiguous, and is owned by the caller.  Device
+ *    pointers must be 16-byte aligned (LL_ERR_ALIGN otherwise).
+ *  - q, k, v, o share ll_shape.dtype (fp32 or bf16); a, lambda and the states are fp32.
+ *  - All work is enqueued on the caller's CUDA stream (`stream`, a cudaStream_t, may be
+ *    NULL for the legacy default stream).  The library allocates no device memory, frees
+ *    nothing and does not synchronise, except where a function says so.
+ *  - Arguments are validated on the host before any launch; a failed check returns its
+ *    code and enqueues nothing.  A launch error returns LL_ERR_CUDA.  Errors detected on
+ *    the device (a bounded wait that ran out) are recorded in a device status word and
+ *    reported by loglinear_check_status().  No C++ exception crosses this boundary.
+ */
+#ifndef LOGLINEAR_H
+#define LOGLINEAR_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LL_OK = 0,
+  LL_ERR_NULL = 1,          /* a required pointer is NULL */
+  LL_ERR_SHAPE = 2,         /* sizes out of the supported range or inconsistent */
+  LL_ERR_DTYPE = 3,         /* unsupported dtype */
+  LL_ERR_ALIGN = 4,         /* a pointer is not 16-byte aligned */
+  LL_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than the query says */
+  LL_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed */
+  LL_ERR_TIMEOUT = 7,       /* a bounded device-side wait ran out (see check_status) */
+  LL_ERR_UNIMPLEMENTED = 8  /* valid request that this build does not cover */
+} ll_status;
+
+typedef enum { LL_F32 = 0, LL_BF16 = 1 } ll_dtype;
+
+/*
+ * Problem shape.
+ *   batch            B >= 1
+ *   T                sequence length, T >= 1 and T % chunk == 0 (forward); unused by decode
+ *   heads            H >= 1, H % heads_per_group == 0
+ *   heads_per_group  heads sharing one q/k group (MVA); G = H / heads_per_group groups
+ *   d_k              16, 32, 64 or 128 (q/k width, the state's row count)
+ *   d_v              16, 32 or 64 (v/o width, the state's column count)
+ *   chunk            C in {16, 32, 64, 128}
+ *   levels           L: lambda holds L weights per (b, t, h); forward needs
+ *                    L >= bit_length(T-1) + 1 (every level a query below T can see);
+ *                    decode uses L as the number of state slots too
+ *   dtype            dtype of q, k, v and o
+ */
+typedef struct {
+  int batch;
+  int T;
+  int heads;
+  int heads_per_group;
+  int d_k;
+  int d_v;
+  int chunk;
+  int levels;
+  ll_dtype dtype;
+} ll_shape;
+
+/* Bytes of device workspace loglinear_fwd needs for this shape (0 if the shape is
+ * invalid).  The workspace holds per-chunk decays, chunk states and the Fenwick block
+ * states of the inter-chunk pass (write-up section 高效训练算法). */
+size_t loglinear_fwd_workspace_bytes(const ll_shape* shape);
+
+/*
+ * Forward over the whole sequence (write-up sections 高效训练算法 and
+ * 对Mamba-2和门控的对数线性推广, Algorithm 1 / Fig. 3).
+ *   q, k      (B, T, G, d_k)     dtype
+ *   v         (B, T, H, d_v)     dtype
+ *   a         (B, T, H)          fp32, each in (0, 1]; a <= 0 gives undefined results
+ *   lambda    (B, T, H, L)       fp32
+ *   o         (B, T, H, d_v)     dtype, written
+ *   workspace device buffer of at least loglinear_fwd_workspace_bytes(shape) bytes,
+ *             16-byte aligned; its contents on entry do not matter
+ *   states_out        NULL, or (B, H, state_levels, d_k, d_v) fp32: the Fenwick bucket
+ *                     states at position T, i.e. the memory a decode step at position T
+ *                     starts from.  Level l holds sum over the level-l bucket of T of
+ *                     M^S(T-1, s) k_s v_sᵀ; levels that are not live at T are zero.
+ *   state_logscale_out NULL, or (B, H, state_levels) fp32, written as zeros (the decay
+ *                     is folded into states_out).
+ *   state_levels      slots in states_out; must be >= bit_length(T) + 1 when states_out
+ *                     is given, ignored otherwise.
+ */
+ll_status loglinear_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
+                        const float* a, const float* lambda, void* o, void* workspace,
+                        size_t workspace_bytes, float* states_out, float* state_logscale_out,
+                        int state_levels, void* stream);
+
+/*
+ * One decode step at position `pos` for every (b, h) (write-up section 特殊结构：树划分:
+ * O(log T) time and memory per decoded token).  shape->T is ignored;
+ * shape->levels = L is the number of state slots and of lambda weights.
+ *   q_t, k_t   (B, G, d_k)   dtype
+ *   v_t        (B, H, d_v)   dtype
+ *   a_t        (B, H)        fp32 in (0, 1]
+ *   lambda_t   (B, H, L)     fp32
+ *   o_t        (B, H, d_v)   dtype, written
+ *   states     (B, H, L, d_k, d_v) fp32, read and updated in place
+ *   state_logscale (B, H, L) fp32, read and updated in place
+ * The bucket memory of level l is exp(state_logscale[l]) * states[l]; level l >= 1 is
+ * live at position pos when bit l-1 of pos is set; slots of levels that are not live
+ * hold unspecified values.  The step decays the live levels by a_t (in the log-scale),
+ * forms o_t = lambda^0 (q.k) v + sum over live l of lambda^l q^T S^l, then merges the
+ * token and the levels 1..m (m = trailing ones of pos) into level m+1 of pos+1.
+ * Requires pos >= 0 and L >= bit_length(pos + 1) + 1.  A state exported by
+ * loglinear_fwd at T continues with pos = T.
+ */
+ll_status loglinear_decode_step(const ll_shape* shape, long long pos, const void* q_t,
+                                const void* k_t, const void* v_t, const float* a_t,
+                                const float* lambda_t, void* o_t, float* states,
+                                float* state_logscale, void* stream);
+
+/*
+ * End-to-end forward from HOST buffers: copies q, k, v, a, lambda (host, same layouts
+ * as loglinear_fwd; pinned memory lets the copies run asynchronously) into
+ * `device_arena`, runs loglinear_fwd and copies o back to the host buffer o_host, all
+ * enqueued on `stream`.  The host buffers must stay valid until the stream reaches that
+ * point; the caller synchronises.  `device_arena` must hold at least
+ * loglinear_fwd_host_arena_bytes(shape) bytes (16-byte aligned).
+ */
+size_t loglinear_fwd_host_arena_bytes(const ll_shape* shape);
+ll_status loglinear_fwd_host(const ll_shape* shape, const void* q_host, const void* k_host,
+                             const void* v_host, const float* a_host, const float* lambda_host,
+                             void* o_host, void* device_arena, size_t arena_bytes, void* stream);
+
+/* ---- diagnostics -------------------------------------------------------------------- */
+
+/* Same as loglinear_fwd, and records CUDA events on `stream` around its kernels:
+ * events[0] before the first kernel and events[i + 1] right after kernel i, for as many
+ * as n_events allows (events are cudaEvent_t handles created by the caller).  The kernel
+ * order is the one loglinear_fwd_kernel_names() lists. */
+ll_status loglinear_fwd_profiled(const ll_shape* shape, const void* q, const void* k,
+                                 const void* v, const float* a, const float* lambda, void* o,
+                                 void* workspace, size_t workspace_bytes, float* states_out,
+                                 float* state_logscale_out, int state_levels, void* stream,
+                                 void** events, int n_events);
+
+/* Comma-separated names of the kernels loglinear_fwd launches for this shape, in launch
+ * order (with_export != 0: states_out is given).  Empty string for an invalid shape. */
+const char* loglinear_fwd_kernel_names(const ll_shape* shape, int with_export);
+
+/* Number of kernels this library has launched in this process so far (all devices). */
+unsigned long long loglinear_launch_count(void);
+
+/* Synchronises `stream`, then reads and clears the device status word of the current
+ * device.  Returns LL_OK, LL_ERR_TIMEOUT when a bounded device-side wait ran out since
+ * the last check (the launch returned early; its outputs are undefined), or
+ * LL_ERR_CUDA when the synchronisation itself failed. */
+ll_status loglinear_check_status(void* stream);
+
+/* Self-test of the bounded-wait path: launches one block that waits on a barrier that
+ * nothing completes, giving up after about `spins` polls, which records LL_ERR_TIMEOUT
+ * in the status word.  Faults nothing; the context stays usable. */
+ll_status loglinear_selftest_wait_timeout(long long spins, void* stream);
+
+/* Static description of a status code. */
+const char* loglinear_status_string(ll_status status);
+
+/* Which kernels loglinear_fwd would launch for this shape: 0 = invalid shape,
+ * 1 = generic CUDA-core path, 2 = tensor-core (tcgen05) path. */
+int loglinear_fwd_path(const ll_shape* shape);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOGLINEAR_H */

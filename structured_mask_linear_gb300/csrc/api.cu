@@ -1,0 +1,263 @@
+// C ABI of the log-linear Mamba-2 library: argument validation, workspace sizing,
+// dispatch to the kernels, device status word.  Declarations and contracts are in
+// include/loglinear.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "ll_internal.cuh"
+
+namespace {
+
+std::atomic<unsigned long long> g_launches{0};
+
+__device__ unsigned g_ll_status;  // device-side error word (0 = ok)
+
+std::mutex g_mu;
+unsigned* g_status_addr[128];  // per-device address of g_ll_status
+
+unsigned* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ll_status) != cudaSuccess) return nullptr;
+    g_status_addr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_addr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pow2_in(int x, int lo, int hi) { return x >= lo && x <= hi && (x & (x - 1)) == 0; }
+
+ll_status check_common(const ll_shape* s) {
+  if (!s) return LL_ERR_NULL;
+  if (s->dtype != LL_F32 && s->dtype != LL_BF16) return LL_ERR_DTYPE;
+  if (s->batch < 1 || s->heads < 1 || s->heads_per_group < 1) return LL_ERR_SHAPE;
+  if (s->heads % s->heads_per_group) return LL_ERR_SHAPE;
+  if (!pow2_in(s->d_k, 16, 128) || !pow2_in(s->d_v, 16, 64)) return LL_ERR_SHAPE;
+  if ((long long)s->batch * s->heads > 65535) return LL_ERR_SHAPE;
+  return LL_OK;
+}
+
+ll_status check_fwd_shape(const ll_shape* s) {
+  ll_status st = check_common(s);
+  if (st != LL_OK) return st;
+  if (s->T < 1 || !pow2_in(s->chunk, 16, 128) || s->T % s->chunk) return LL_ERR_SHAPE;
+  if (s->levels < ll::bit_length(s->T - 1) + 1 || s->levels > 32) return LL_ERR_SHAPE;
+  return LL_OK;
+}
+
+size_t esize(const ll_shape* s) { return s->dtype == LL_BF16 ? 2 : 4; }
+
+size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+ll_status fwd_impl(const ll_shape* s, const void* q, const void* k, const void* v, const float* a,
+                   const float* lambda, void* o, void* workspace, size_t workspace_bytes,
+                   float* states_out, float* state_logscale_out, int state_levels, void* stream,
+                   void** events, int n_events);
+
+}  // namespace
+
+namespace ll {
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void note_launch(const FwdArgs& a, int i, cudaStream_t st) {
+  note_launch();
+  if (a.events && i + 1 < a.n_events && a.events[i + 1])
+    cudaEventRecord(static_cast<cudaEvent_t>(a.events[i + 1]), st);
+}
+}  // namespace ll
+
+extern "C" {
+
+const char* loglinear_status_string(ll_status s) {
+  switch (s) {
+    case LL_OK: return "ok";
+    case LL_ERR_NULL: return "required pointer is NULL";
+    case LL_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case LL_ERR_DTYPE: return "unsupported dtype";
+    case LL_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case LL_ERR_WORKSPACE: return "workspace missing or too small";
+    case LL_ERR_CUDA: return "CUDA runtime error";
+    case LL_ERR_TIMEOUT: return "bounded device wait ran out";
+    case LL_ERR_UNIMPLEMENTED: return "not implemented for this shape";
+  }
+  return "unknown status";
+}
+
+int loglinear_fwd_path(const ll_shape* s) {
+  if (check_fwd_shape(s) != LL_OK) return 0;
+  return ll::tc_supported(*s) ? 2 : 1;
+}
+
+size_t loglinear_fwd_workspace_bytes(const ll_shape* s) {
+  if (check_fwd_shape(s) != LL_OK) return 0;
+  if (ll::tc_supported(*s)) {
+    ll::TcPlan tp;
+    return ll::make_tc_plan(*s, &tp) ? tp.bytes : 0;
+  }
+  ll::GenPlan p;
+  if (!ll::make_gen_plan(*s, &p)) return 0;
+  return p.bytes;
+}
+
+ll_status loglinear_fwd(const ll_shape* s, const void* q, const void* k, const void* v,
+                        const float* a, const float* lambda, void* o, void* workspace,
+                        size_t workspace_bytes, float* states_out, float* state_logscale_out,
+                        int state_levels, void* stream) {
+  return fwd_impl(s, q, k, v, a, lambda, o, workspace, workspace_bytes, states_out,
+                  state_logscale_out, state_levels, stream, nullptr, 0);
+}
+
+ll_status loglinear_fwd_profiled(const ll_shape* s, const void* q, const void* k, const void* v,
+                                 const float* a, const float* lambda, void* o, void* workspace,
+                                 size_t workspace_bytes, float* states_out,
+                                 float* state_logscale_out, int state_levels, void* stream,
+                                 void** events, int n_events) {
+  return fwd_impl(s, q, k, v, a, lambda, o, workspace, workspace_bytes, states_out,
+                  state_logscale_out, state_levels, stream, events, n_events);
+}
+
+const char* loglinear_fwd_kernel_names(const ll_shape* s, int with_export) {
+  if (check_fwd_shape(s) != LL_OK) return "";
+  if (ll::tc_supported(*s)) return ll::tc_kernel_names(with_export != 0);
+  return with_export ? "gen_chunk_state,gen_blocks,gen_output,gen_export"
+                     : "gen_chunk_state,gen_blocks,gen_output";
+}
+
+unsigned long long loglinear_launch_count(void) {
+  return g_launches.load(std::memory_order_relaxed);
+}
+
+ll_status loglinear_decode_step(const ll_shape* s, long long pos, const void* q_t, const void* k_t,
+                                const void* v_t, const float* a_t, const float* lambda_t,
+                                void* o_t, float* states, float* state_logscale, void* stream) {
+  ll_status st = check_common(s);
+  if (st != LL_OK) return st;
+  if (pos < 0 || pos >= (1LL << 62)) return LL_ERR_SHAPE;
+  if (s->levels < ll::bit_length(pos + 1) + 1 || s->levels > 64) return LL_ERR_SHAPE;
+  if (!q_t || !k_t || !v_t || !a_t || !lambda_t || !o_t || !states || !state_logscale)
+    return LL_ERR_NULL;
+  if (!aligned16(q_t) || !aligned16(k_t) || !aligned16(v_t) || !aligned16(o_t) ||
+      !aligned16(states))
+    return LL_ERR_ALIGN;
+  ll::DecodeArgs d{s->batch, s->heads, s->heads_per_group, s->heads / s->heads_per_group,
+                   s->d_k, s->d_v, s->levels, pos, q_t, k_t, v_t, a_t, lambda_t, o_t,
+                   states, state_logscale};
+  cudaError_t e = ll::launch_decode(d, s->dtype == LL_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
+size_t loglinear_fwd_host_arena_bytes(const ll_shape* s) {
+  if (check_fwd_shape(s) != LL_OK) return 0;
+  const size_t B = s->batch, T = s->T, H = s->heads, G = s->heads / s->heads_per_group;
+  const size_t es = esize(s);
+  size_t n = 0;
+  n += 2 * a256(B * T * G * s->d_k * es);   // q, k
+  n += 2 * a256(B * T * H * s->d_v * es);   // v, o
+  n += a256(B * T * H * 4);                 // a
+  n += a256(B * T * H * s->levels * 4);     // lambda
+  n += a256(loglinear_fwd_workspace_bytes(s));
+  return n;
+}
+
+ll_status loglinear_fwd_host(const ll_shape* s, const void* q_host, const void* k_host,
+                             const void* v_host, const float* a_host, const float* lambda_host,
+                             void* o_host, void* device_arena, size_t arena_bytes, void* stream) {
+  ll_status st = check_fwd_shape(s);
+  if (st != LL_OK) return st;
+  if (!q_host || !k_host || !v_host || !a_host || !lambda_host || !o_host) return LL_ERR_NULL;
+  const size_t need = loglinear_fwd_host_arena_bytes(s);
+  if (!device_arena || arena_bytes < need) return LL_ERR_WORKSPACE;
+  if (!aligned16(device_arena)) return LL_ERR_ALIGN;
+  const size_t B = s->batch, T = s->T, H = s->heads, G = s->heads / s->heads_per_group;
+  const size_t es = esize(s);
+  const size_t bq = B * T * G * s->d_k * es, bv = B * T * H * s->d_v * es, ba = B * T * H * 4,
+               bl = B * T * H * s->levels * 4;
+  char* p = static_cast<char*>(device_arena);
+  char* dq = p; p += a256(bq);
+  char* dk = p; p += a256(bq);
+  char* dv = p; p += a256(bv);
+  char* dout = p; p += a256(bv);
+  char* da = p; p += a256(ba);
+  char* dl = p; p += a256(bl);
+  char* dws = p;
+  const size_t wsb = loglinear_fwd_workspace_bytes(s);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dq, q_host, bq, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k_host, bq, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v_host, bv, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(da, a_host, ba, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(dl, lambda_host, bl, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return LL_ERR_CUDA;
+  st = loglinear_fwd(s, dq, dk, dv, reinterpret_cast<float*>(da), reinterpret_cast<float*>(dl),
+                     dout, dws, wsb, nullptr, nullptr, 0, stream);
+  if (st != LL_OK) return st;
+  if (cudaMemcpyAsync(o_host, dout, bv, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+    return LL_ERR_CUDA;
+  return LL_OK;
+}
+
+ll_status loglinear_check_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LL_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_ll_status, sizeof(v)) != cudaSuccess) return LL_ERR_CUDA;
+  if (v != 0 && cudaMemcpyToSymbol(g_ll_status, &zero, sizeof(zero)) != cudaSuccess)
+    return LL_ERR_CUDA;
+  if (v == 0) return LL_OK;
+  return v == LL_ERR_TIMEOUT ? LL_ERR_TIMEOUT : LL_ERR_CUDA;
+}
+
+ll_status loglinear_selftest_wait_timeout(long long spins, void* stream) {
+  if (spins < 0) return LL_ERR_SHAPE;
+  unsigned* sw = status_word();
+  if (!sw) return LL_ERR_CUDA;
+  cudaError_t e = ll::launch_wait_selftest(sw, spins, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+ll_status fwd_impl(const ll_shape* s, const void* q, const void* k, const void* v, const float* a,
+                   const float* lambda, void* o, void* workspace, size_t workspace_bytes,
+                   float* states_out, float* state_logscale_out, int state_levels, void* stream,
+                   void** events, int n_events) {
+  ll_status st = check_fwd_shape(s);
+  if (st != LL_OK) return st;
+  if (!q || !k || !v || !a || !lambda || !o) return LL_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) || !aligned16(lambda) ||
+      !aligned16(o))
+    return LL_ERR_ALIGN;
+  if (states_out) {
+    if (state_levels < ll::bit_length(s->T) + 1 || state_levels > 64) return LL_ERR_SHAPE;
+    if (!aligned16(states_out)) return LL_ERR_ALIGN;
+  }
+  const size_t need = loglinear_fwd_workspace_bytes(s);
+  if (!workspace || workspace_bytes < need) return LL_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return LL_ERR_ALIGN;
+  unsigned* sw = status_word();
+  if (!sw) return LL_ERR_CUDA;
+  ll::FwdArgs fa{q, k, v, a, lambda, o, static_cast<char*>(workspace), states_out,
+                 state_logscale_out, state_levels, sw, events, n_events};
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (events && n_events > 0 && events[0])
+    cudaEventRecord(static_cast<cudaEvent_t>(events[0]), cs);
+  cudaError_t e;
+  if (ll::tc_supported(*s)) {
+    ll::TcPlan tp;
+    if (!ll::make_tc_plan(*s, &tp)) return LL_ERR_SHAPE;
+    e = ll::launch_tc_fwd(tp, fa, cs);
+  } else {
+    ll::GenPlan p;
+    if (!ll::make_gen_plan(*s, &p)) return LL_ERR_SHAPE;
+    e = ll::launch_generic_fwd(p, s->dtype == LL_BF16, fa, cs);
+  }
+  return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
+}  // namespace

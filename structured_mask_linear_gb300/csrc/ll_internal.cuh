@@ -1,0 +1,100 @@
+// Internal declarations shared by the CUDA translation units of the library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/loglinear.h"
+
+namespace ll {
+
+// Device status word values (mirror ll_status).
+constexpr unsigned kStatusTimeout = LL_ERR_TIMEOUT;
+
+// Chunk / block bookkeeping for the generic path.
+struct GenPlan {
+  int B, T, H, hpg, G, dk, dv, C, clog, L, N;  // N = T / C chunks
+  int M;                                       // chunk levels: bit_length(N)
+  int nblk;                                    // Fenwick block states per (b, h)
+  int blk_off[32];                             // first block of chunk level m
+  size_t off_g, off_gamma, off_H, off_blk, off_blkG, bytes;
+};
+
+bool make_gen_plan(const ll_shape& s, GenPlan* p);
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* a;
+  const float* lam;
+  void* o;
+  char* ws;
+  float* states_out;
+  float* logscale_out;
+  int state_levels;
+  unsigned* status;
+  void** events;  // optional: events[0] before the first kernel, events[i+1] after kernel i
+  int n_events;
+};
+
+// Counts a kernel launch and records the profiling event that follows kernel `i`.
+void note_launch(const FwdArgs& a, int i, cudaStream_t st);
+void note_launch();
+
+
+cudaError_t launch_generic_fwd(const GenPlan& p, bool bf16, const FwdArgs& a, cudaStream_t st);
+
+struct DecodeArgs {
+  int B, H, hpg, G, dk, dv, L;
+  long long pos;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* a;
+  const float* lam;
+  void* o;
+  float* states;
+  float* logscale;
+};
+
+cudaError_t launch_decode(const DecodeArgs& d, bool bf16, cudaStream_t st);
+
+cudaError_t launch_wait_selftest(unsigned* status, long long spins, cudaStream_t st);
+
+// ---- tensor-core path (tcgen05) --------------------------------------------
+struct TcPlan {
+  int B, T, H, hpg, G, L;
+  int NT;           // 128-token tiles
+  int nnodes;       // Fenwick tree nodes per (b, h)
+  int node_off[32]; // first node of tile level m
+  int MT;           // tile levels (bit_length(NT))
+  size_t off_gam, off_nodeG, off_cnt, off_node32, off_node16, cnt_bytes, bytes;
+};
+
+bool tc_supported(const ll_shape& s);
+bool make_tc_plan(const ll_shape& s, TcPlan* p);
+cudaError_t launch_tc_fwd(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
+const char* tc_kernel_names(bool with_export);
+
+__host__ __device__ inline int bit_length(long long x) {
+  int l = 0;
+  while (x > 0) {
+    l++;
+    x >>= 1;
+  }
+  return l;
+}
+
+}  // namespace ll
+
+// ---- small device helpers -----------------------------------------------------
+__device__ __forceinline__ float ll_load(const float* p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ll_load(const __nv_bfloat16* p, size_t i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void ll_store(float* p, size_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void ll_store(__nv_bfloat16* p, size_t i, float x) {
+  p[i] = __float2bfloat16_rn(x);
+}
