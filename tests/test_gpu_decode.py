@@ -55,12 +55,12 @@ def test_decode_matches_recurrent_form(sml, cfg):
     ref_o, ref_st = oracle.form_r(*(to_numpy64(t) for t in (x.q, x.k, x.v, x.a, x.lam)),
                                   export_levels=L)
     for i in range(steps):
-        assert_parity(o[:, i].double().cpu().numpy(), ref_o[:, T0 + i], f"step {T0 + i}")
+        assert_parity(o[:, i].double().cpu().numpy(), ref_o[:, T0 + i], f"step {T0 + i}", o.dtype)
     # final states: exp(logscale) * states on the live levels of position T
     got = (torch.exp(lsc)[..., None, None] * st).double().cpu().numpy()
     for lvl in range(1, L):
         if (T >> (lvl - 1)) & 1:
-            assert_parity(got[:, :, lvl], ref_st[:, :, lvl], f"state level {lvl}")
+            assert_parity(got[:, :, lvl], ref_st[:, :, lvl], f"state level {lvl}", "f32")
 
 
 def test_decode_workload_sampled(sml):
@@ -79,8 +79,8 @@ def test_decode_workload_sampled(sml):
         ref_o, ref_st = oracle.form_r_head(
             to_numpy64(x.q[b, :, g]), to_numpy64(x.k[b, :, g]), to_numpy64(x.v[b, :, h]),
             to_numpy64(x.a[b, :, h]), to_numpy64(x.lam[b, :, h]), [T], levels=L)
-        assert_parity(o[b, :, h].double().cpu().numpy(), ref_o[T0:], f"b={b} h={h}")
+        assert_parity(o[b, :, h].double().cpu().numpy(), ref_o[T0:], f"b={b} h={h}", o.dtype)
         got = (torch.exp(lsc[b, h])[:, None, None] * st[b, h]).double().cpu().numpy()
         for lvl in range(1, L):
             if (T >> (lvl - 1)) & 1:
-                assert_parity(got[lvl], ref_st[0, lvl], f"b={b} h={h} level {lvl}")
+                assert_parity(got[lvl], ref_st[0, lvl], f"b={b} h={h} level {lvl}", "f32")

@@ -32,18 +32,28 @@ def _np(x):
     return tuple(to_numpy64(t) for t in (x.q, x.k, x.v, x.a, x.lam))
 
 
+@pytest.mark.parametrize("name,T,path", [("small", 2048, 2), ("pages", 8192, 2), ("long", 131072, 2),
+                                         ("small", 64 * 37, 1), ("tiny", 256, 1)])
+def test_path_selection(sml, name, T, path):
+    """bf16 with d_k = 128, d_v = 64 and T % 128 == 0 runs the tensor-core kernels."""
+    w = workload(name, T=T, levels=levels_for(T))
+    shape = sml.make_shape(w.batch, T, w.heads, w.heads_per_group, w.d_k, w.d_v, w.chunk,
+                           w.levels, w.dtype)
+    assert sml.loglinear_fwd_path(shape) == path
+
+
 def test_tiny_workload_full(sml):
     w = workload("tiny")
     x = make_inputs(w, "cpu", seed=0)
     o = _run(sml, x, w.chunk)
-    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), "tiny")
+    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), "tiny", o.dtype)
 
 
 def test_small_workload_full(sml):
     w = workload("small")
     x = make_inputs(w, "cpu", seed=0)
     o = _run(sml, x, w.chunk)
-    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), "small")
+    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), "small", o.dtype)
 
 
 @pytest.mark.parametrize("T", [64, 128, 192, 64 * 37])
@@ -52,7 +62,7 @@ def test_ragged_chunk_counts(sml, T):
     w = workload("small", batch=1, heads=4, T=T, levels=levels_for(T))
     x = make_inputs(w, "cpu", seed=3)
     o = _run(sml, x, 64)
-    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), f"T={T}")
+    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), f"T={T}", o.dtype)
 
 
 @pytest.mark.parametrize("chunk", [16, 32, 64, 128])
@@ -61,7 +71,7 @@ def test_chunk_invariance(sml, chunk):
     w = workload("small", batch=1, heads=2, d_k=64, d_v=32, T=1024, levels=levels_for(1024))
     x = make_inputs(w, "cpu", seed=5)
     o = _run(sml, x, chunk)
-    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), f"chunk={chunk}")
+    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), f"chunk={chunk}", o.dtype)
 
 
 @pytest.mark.parametrize("decay", ["ones", "slow"])
@@ -72,16 +82,18 @@ def test_slow_decay_keeps_far_levels_live(sml, name, decay):
         w = workload(name, decay=decay, batch=1, heads=4)
     x = make_inputs(w, "cpu", seed=11)
     o = _run(sml, x, w.chunk)
-    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), f"{name}/{decay}")
+    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), f"{name}/{decay}", o.dtype)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_level_isolation(sml, dtype):
-    """lambda^l = [l == j] for each level j, slow decay: each level checked alone."""
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.float32, 64, 32), (torch.bfloat16, 64, 32),
+                                         (torch.bfloat16, 128, 64)])
+def test_level_isolation(sml, dtype, dk, dv):
+    """lambda^l = [l == j] for each level j, slow decay: each level checked alone (the
+    bf16 128/64 case runs the tensor-core path)."""
     T = 1024
     L = levels_for(T)
     w = workload("small", batch=1, heads=2, heads_per_group=2, T=T, levels=L, decay="slow",
-                 dtype=dtype, d_k=64, d_v=32)
+                 dtype=dtype, d_k=dk, d_v=dv)
     x = make_inputs(w, "cpu", seed=2)
     for j in range(L):
         lam = torch.zeros_like(x.lam)
@@ -92,7 +104,7 @@ def test_level_isolation(sml, dtype):
         if np.linalg.norm(ref) == 0:
             assert float(o.abs().max()) == 0.0
         else:
-            assert_parity(o.double().cpu().numpy(), ref, f"level {j}")
+            assert_parity(o.double().cpu().numpy(), ref, f"level {j}", o.dtype)
 
 
 def _probe_inputs(T, H, hpg, dk, dv, L, dtype, v):
@@ -160,7 +172,7 @@ def test_state_export(sml, T, decay):
     lsc = torch.full((1, 4, SL), float("nan"), device=DEV)
     o = _run(sml, x, 64, states_out=st, state_logscale_out=lsc, state_levels=SL)
     ref_o, ref_st = oracle.form_r(*_np(x), export_levels=SL)
-    assert_parity(o.double().cpu().numpy(), ref_o, "o")
+    assert_parity(o.double().cpu().numpy(), ref_o, "o", o.dtype)
     assert torch.all(lsc == 0)
     got = st.double().cpu().numpy()
     live = [lvl for lvl in range(SL) if lvl >= 1 and (T >> (lvl - 1)) & 1]
@@ -168,8 +180,8 @@ def test_state_export(sml, T, decay):
         if lvl not in live:
             assert np.all(got[:, :, lvl] == 0)
         elif decay == "slow":
-            assert_parity(got[:, :, lvl], ref_st[:, :, lvl], f"state level {lvl}")
-    assert_parity(got[:, :, live], ref_st[:, :, live], "live levels")
+            assert_parity(got[:, :, lvl], ref_st[:, :, lvl], f"state level {lvl}", "f32")
+    assert_parity(got[:, :, live], ref_st[:, :, live], "live levels", "f32")
 
 
 def test_many_heads_ungrouped(sml):
@@ -177,7 +189,7 @@ def test_many_heads_ungrouped(sml):
                  levels=levels_for(256), dtype=torch.float32)
     x = make_inputs(w, "cpu", seed=4)
     o = _run(sml, x, 32)
-    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), "ungrouped")
+    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), "ungrouped", o.dtype)
 
 
 def test_timeout_selftest_reports_and_recovers(sml):
@@ -187,7 +199,7 @@ def test_timeout_selftest_reports_and_recovers(sml):
     w = workload("tiny")
     x = make_inputs(w, "cpu", seed=0)
     o = _run(sml, x, w.chunk)  # the context is still usable
-    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), "after timeout")
+    assert_parity(o.double().cpu().numpy(), oracle.form_q(*_np(x)), "after timeout", o.dtype)
 
 
 # --- full-size workloads, sampled outputs ------------------------------------
@@ -213,7 +225,7 @@ def _sampled_check(sml, name, n_pairs, n_t, seed=0):
                                    to_numpy64(x.v[b, :tm, h]), to_numpy64(x.a[b, :tm, h]),
                                    to_numpy64(x.lam[b, torch.as_tensor(ts, device=DEV), h]), ts)
         got = o[b, torch.as_tensor(ts, device=DEV), h].double().cpu().numpy()
-        assert_parity(got, ref, f"{name} b={b} h={h}")
+        assert_parity(got, ref, f"{name} b={b} h={h}", o.dtype)
 
 
 def test_pages_workload_sampled(sml):
