@@ -148,6 +148,33 @@ ll_status loglinear_fwd_host(const ll_shape* shape, const void* q_host, const vo
                              const void* v_host, const float* a_host, const float* lambda_host,
                              void* o_host, void* device_arena, size_t arena_bytes, void* stream);
 
+/*
+ * Forward for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for code that is not allowed to call
+ * cudaMalloc or any other allocator while it runs (for example a plugin whose host owns
+ * every device allocation, or code sharing the context with an allocator it must not
+ * disturb), and for callers that cannot size or keep a workspace between calls.
+ *
+ * Same arguments and results as loglinear_fwd, without the workspace: the library uses
+ * a fixed device array of LOGLINEAR_STATIC_WORKSPACE_BYTES (32 MiB) that each GPU loading
+ * the library holds until the process exits.  The call allocates nothing and frees
+ * nothing.
+ *   - Shapes whose loglinear_fwd_workspace_bytes() exceeds LOGLINEAR_STATIC_WORKSPACE_BYTES
+ *     are rejected with LL_ERR_WORKSPACE before anything is enqueued (for example
+ *     B*H = 16 heads of T = 2048 at d_k = 128, d_v = 64 fit; the pages workload does not).
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture begins.
+ *   - Every call on a device shares the one array and leaves its contents behind; parts
+ *     that must start at zero are cleared on the stream by each call.  Calls whose work
+ *     overlaps on the GPU (other streams, other threads) race on the array: serialise
+ *     them, e.g. on one stream.
+ */
+#define LOGLINEAR_STATIC_WORKSPACE_BYTES (32u << 20)
+ll_status loglinear_fwd_static_workspace(const ll_shape* shape, const void* q, const void* k,
+                                         const void* v, const float* a, const float* lambda,
+                                         void* o, float* states_out, float* state_logscale_out,
+                                         int state_levels, void* stream);
+
 /* ---- diagnostics -------------------------------------------------------------------- */
 
 /* Same as loglinear_fwd, and records CUDA events on `stream` around its kernels:

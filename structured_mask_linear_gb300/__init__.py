@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
                                                   ctypes.c_int])
             L.loglinear_fwd_kernel_names.restype = ctypes.c_char_p
             L.loglinear_fwd_kernel_names.argtypes = [_SP, ctypes.c_int]
+            L.loglinear_fwd_static_workspace.restype = ctypes.c_int
+            L.loglinear_fwd_static_workspace.argtypes = [_SP] + [_vp] * 8 + [ctypes.c_int, _vp]
             L.loglinear_launch_count.restype = ctypes.c_ulonglong
             L.loglinear_launch_count.argtypes = []
             _lib = L
@@ -175,6 +177,25 @@ def loglinear_fwd_profiled(q, k, v, a, lam, events, chunk: int = 64, o=None, wor
                                       _ptr(states_out), _ptr(state_logscale_out),
                                       int(state_levels), _stream_ptr(stream), arr, len(events))
     _check(st, "loglinear_fwd_profiled")
+    return o
+
+
+STATIC_WORKSPACE_BYTES = 32 << 20
+
+
+def loglinear_fwd_static_workspace(q, k, v, a, lam, chunk: int = 64, o=None, states_out=None,
+                                   state_logscale_out=None, state_levels: int = 0, stream=None):
+    """loglinear_fwd without a workspace argument, for callers that cannot allocate device
+    memory: the library's own fixed 32 MiB device array is used instead (shapes needing
+    more are rejected).  Only `o` is allocated here, and only when it is not given."""
+    shape = fwd_shape(q, v, lam, chunk)
+    if o is None:
+        o = torch.empty_like(v)
+    st = lib().loglinear_fwd_static_workspace(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                              _ptr(a), _ptr(lam), _ptr(o), _ptr(states_out),
+                                              _ptr(state_logscale_out), int(state_levels),
+                                              _stream_ptr(stream))
+    _check(st, "loglinear_fwd_static_workspace")
     return o
 
 
