@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the long/decode/e2e extras")
+    ap.add_argument("--ncu-case", action="store_true",
+                    help="profiling case: 3 forwards of the pages workload at batch 1 "
+                         "(inputs 225 MB > L2), no timing, no JSON")
     return ap.parse_args()
 
 
@@ -219,8 +222,28 @@ def run_reference(args):
 
 
 # ---- GPU arm --------------------------------------------------------------------------
+def ncu_case():
+    import torch
+
+    import structured_mask_linear_gb300 as sml
+    from structured_mask_linear_gb300.inputs import make_inputs, workload
+
+    sml.lib()
+    w = workload("pages", batch=1)
+    x = make_inputs(w, "cuda", seed=0)
+    st = torch.empty((1, w.heads, w.T.bit_length() + 1, w.d_k, w.d_v), device="cuda")
+    for _ in range(3):
+        sml.loglinear_fwd(x.q, x.k, x.v, x.a, x.lam, chunk=w.chunk, states_out=st,
+                          state_levels=w.T.bit_length() + 1)
+    torch.cuda.synchronize()
+    assert sml.loglinear_check_status() == 0
+
+
 def main():
     args = parse()
+    if args.ncu_case:
+        ncu_case()
+        return
     if args.impl == "reference":
         run_reference(args)
         return
