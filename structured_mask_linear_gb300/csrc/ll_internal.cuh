@@ -70,7 +70,9 @@ struct TcPlan {
   int nnodes;       // Fenwick tree nodes per (b, h)
   int node_off[32]; // first node of tile level m
   int MT;           // tile levels (bit_length(NT))
-  size_t off_gam, off_nodeG, off_cnt, off_node32, off_node16, cnt_bytes, bytes;
+  size_t off_img;   // fp16 node images, 16 KB each
+  size_t off_meta;  // per node: arrivals, scale exponent, log2 decay, spare
+  size_t meta_bytes, bytes;
 };
 
 bool tc_supported(const ll_shape& s);

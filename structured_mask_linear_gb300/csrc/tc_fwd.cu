@@ -9,25 +9,27 @@
 //  tc_state   one CTA per (b, h, tile u): chunk-local log2 decay cumsum g, tile decay
 //             gamma_u, tile state H_u = K_uᵀ diag(2^(gamma_u - g)) V_u on the tensor
 //             cores (M = d_k, N = d_v, K = tokens).  Then the Fenwick tree over tiles is
-//             built without any waiting: the CTA stores its node and climbs while it is
-//             the second of two siblings to arrive (atomic counter per parent), merging
-//             Node_{m+1}[i] = 2^(Gamma(right)) Node_m[2i] + Node_m[2i+1].  Even nodes also
-//             get a bf16 hi/lo image in the UMMA operand layout for tc_output.
-//  tc_output  one CTA per (b, h, tile u): S = Q Kᵀ on the tensor cores; for every set
-//             bit m of u one MMA Y = Q · Node_m[(u >> m) - 1] whose rows are added with
-//             weight lambda_t^(8+m) 2^(g_t + D_m), D_m the decay of the nearer buckets
-//             (write-up section 特殊结构：树划分: one memory per bucket level); then
-//             P = S ⊙ lambda^l ⊙ 2^(g_t - g_s) ⊙ [s <= t] written to shared memory and
-//             O = P V.
+//             built without any waiting: the CTA publishes its node and climbs while it
+//             is the second of two siblings to arrive (one atomic counter per parent),
+//             merging Node_{m+1}[i] = 2^(Gamma(right)) Node_m[2i] + Node_m[2i+1].  Nodes
+//             are published as fp16 images in the UMMA operand layout with a power-of-two
+//             scale and their total log2 decay.
+//  tc_output  one CTA per (b, h, tile u): S = Q Kᵀ on the tensor cores; P = S ⊙ lambda^l
+//             ⊙ 2^(g_t - g_s) ⊙ [s <= t] (levels 0..7) written to shared memory as fp16 with
+//             a power-of-two row scale; O = P V; then for every set bit m of u one more MMA
+//             Y = Q · Node_m[(u >> m) - 1], its rows added with weight
+//             lambda_t^(8+m) 2^(g_t + D_m), D_m the decay of the nearer buckets (write-up
+//             section 特殊结构：树划分: one memory per bucket level); one write of o.
+//  tc_export  bucket states at position T from the published nodes (decode hand-off).
 //
-// Operands the kernels form themselves (decayed V, P, node images) are stored as a bf16
-// hi part plus a bf16 lo part (the rounding remainder) and multiplied by both, so the
-// products keep about 16 significant bits while q, k, v enter exactly.
-//  tc_export  bucket states at position T from the fp32 nodes (decode hand-off).
+// Operands formed inside the kernels are fp16 with exact power-of-two scales chosen from
+// their maxima (fp16 keeps 11 significant bits, bf16 only 8); the decayed V of the state
+// product is split into a bf16 hi part and a bf16 lo part.  q, k, v enter exactly.
 //
-// Every mbarrier wait is bounded; a wait that runs out records LL_ERR_TIMEOUT in the
-// status word and the CTA skips the rest of its work.
+// Every mbarrier wait is bounded by 2 s of %globaltimer; a wait that runs out records
+// LL_ERR_TIMEOUT in the status word and the CTA skips the rest of its work.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
@@ -40,13 +42,23 @@ namespace ll {
 
 namespace {
 
-constexpr int kTile = 128;         // tokens per tile
-constexpr int kDk = 128, kDv = 64;  // supported head dims
-constexpr int kLevIntra = 8;        // levels 0..7 live inside a 128-token tile
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
-constexpr int kNodeF = kDk * kDv;   // floats per fp32 node
-constexpr int kImgHalf = kDk * kDv * 2;    // bytes of one bf16 d_k x d_v image
-constexpr int kImgBytes = 2 * kImgHalf;    // node image: hi part then lo part
+constexpr int kTile = 128;                   // tokens per tile
+constexpr int kDk = 128, kDv = 64;            // supported head dims
+constexpr int kLevIntra = 8;                  // levels 0..7 live inside a 128-token tile
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
+constexpr int kImgBytes = kDk * kDv * 2;      // fp16 node image, 128 rows x 128 bytes
+constexpr int kMeta = 4;  // u32 per node: arrivals, scale exponent, log2 decay (f32 bits), spare
+
+struct TcParams {
+  int B, T, H, hpg, G, L, NT, nnodes, MT;
+  int node_off[32];
+  const float* a;
+  const float* lam;
+  __nv_bfloat16* o;
+  uint8_t* img;    // (B*H, nnodes, 16 KB) fp16 node images
+  unsigned* meta;  // (B*H, nnodes, 4)
+  unsigned* status;
+};
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -58,33 +70,62 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
   }
 }
 
-struct TcParams {
-  int B, T, H, hpg, G, L, NT, nnodes, MT;
-  int node_off[32];
-  const float* a;
-  const float* lam;
-  __nv_bfloat16* o;
-  float* node32;  // (B*H, nnodes, d_k, d_v)
-  float* nodeG;   // (B*H, nnodes) total log2 decay of each node
-  unsigned* cnt;  // (B*H, nnodes) arrival counters (zeroed before tc_state)
-  uint8_t* img;   // (B*H, nnodes, 32 KB) bf16 hi/lo images of even nodes
-  unsigned* status;
-};
+// 2^e as an exact float, e in [-126, 127].
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+// 2^e for a sum of two exponents (|e| <= 252): product of two exact powers of two.
+__device__ __forceinline__ float pow2s(int e) {
+  const int h = e / 2;
+  return pow2i(h) * pow2i(e - h);
+}
+
+// Exponent e with m * 2^-e in [2^14, 2^15): scaling by 2^-e keeps fp16 away from
+// overflow (max 65504) and keeps 29 binades below the maximum in fp16's normal range.
+__device__ __forceinline__ int f16_exp(float m) {
+  if (!(m > 0.f)) return 0;
+  int eb = ((__float_as_int(m) >> 23) & 0xff) - 127;
+  if (eb < -126) eb = -126;
+  int e = eb - 14;
+  return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
 
 // Block-wide inclusive prefix sum over 128 threads (one value each).
-__device__ __forceinline__ float block_scan128(float x, float* s_warp) {
+__device__ __forceinline__ float block_scan128(float x, float* s_red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     float y = __shfl_up_sync(0xffffffffu, x, off);
     if (lane >= off) x += y;
   }
-  if (lane == 31) s_warp[warp] = x;
+  if (lane == 31) s_red[warp] = x;
   __syncthreads();
   float add = 0.f;
-  for (int w = 0; w < warp; ++w) add += s_warp[w];
+  for (int w = 0; w < warp; ++w) add += s_red[w];
   __syncthreads();
   return x + add;
+}
+
+// Block-wide max of two values (128 threads).
+__device__ __forceinline__ float2 block_max2(float2 v, float2* s_red2) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, off));
+    v.y = fmaxf(v.y, __shfl_xor_sync(0xffffffffu, v.y, off));
+  }
+  if (lane == 0) s_red2[warp] = v;
+  __syncthreads();
+  float2 r = s_red2[0];
+  for (int w = 1; w < 4; ++w) {
+    r.x = fmaxf(r.x, s_red2[w].x);
+    r.y = fmaxf(r.y, s_red2[w].y);
+  }
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -92,14 +133,38 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// (a, b) -> bf16 pair hi = round(a, b) and lo = round((a, b) - hi): hi + lo carries about
-// 16 significant bits, which a pair of MMAs accumulating in fp32 preserves.
-__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  float2 r = __bfloat1622float2(h);
-  __nv_bfloat162 l = __floats2bfloat162_rn(a - r.x, b - r.y);
-  hi = *reinterpret_cast<uint32_t*>(&h);
-  lo = *reinterpret_cast<uint32_t*>(&l);
+// Max |x| over the 8 bf16 chunks (128 bytes) of one shared-memory row.  Threads visit
+// the chunks in the order c ^ (row & 7) so that a warp's accesses spread over the banks.
+__device__ __forceinline__ float row_absmax_bf16(const uint8_t* row, int rot) {
+  float m = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 x = *reinterpret_cast<const uint4*>(row + ((c ^ rot) << 4));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float2 f = __bfloat1622float2(h[e]);
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+  return m;
+}
+
+// In place: one 128-byte row of bf16 -> fp16, each value times s (same chunk slots).
+__device__ __forceinline__ void row_bf16_to_f16(uint8_t* row, int rot, float s) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4* q = reinterpret_cast<uint4*>(row + ((c ^ rot) << 4));
+    uint4 x = *q, y;
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+    __half2* o = reinterpret_cast<__half2*>(&y);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float2 f = __bfloat1622float2(h[e]);
+      o[e] = __floats2half2_rn(f.x * s, f.y * s);
+    }
+    *q = y;
+  }
 }
 
 // ---------------------------------------------------------------------------------
@@ -110,15 +175,16 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
                                                        TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = smem;            // 32 KB: two 64-wide d_k boxes of 128 tokens (SW128)
-  uint8_t* sV = smem + 32768;    // 32 KB: Ṽ hi part (the TMA box) then Ṽ lo part
+  uint8_t* sK = smem;          // 32 KB: K (bf16, two 64-wide d_k boxes); later node staging
+  uint8_t* sV = smem + 32768;  // 32 KB: Ṽ hi part (the TMA box) then Ṽ lo part
   __shared__ __align__(8) uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_warp[4];
+  __shared__ float s_red[4];
+  __shared__ float2 s_red2[4];
   __shared__ float s_gamma;
   __shared__ unsigned s_flag;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, rot = tid & 7;
   const int lin = blockIdx.x;
   const int h = lin % p.H;
   const int u = (lin / p.H) % p.NT;
@@ -126,45 +192,40 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   const int g = h / p.hpg;
   const int bh = b * p.H + h;
   const long long t0 = (long long)u * kTile;
+  const float la = log2f(p.a[((size_t)b * p.T + t0 + tid) * p.H + h]);
 
   if (tid == 0) {
     ptx::mbar_init(&bar_ld, 1);
     ptx::mbar_init(&bar_mma, 1);
     ptx::fence_mbar_init();
-  }
-  if (warp == 0) {
-    ptx::tmem_alloc(&tmem_base, 128);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tbase = tmem_base;
-
-  if (tid == 0) {
     ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
     ptx::tma_load_4d(sK, &mapK, &bar_ld, 0, g, (int)t0, b);
     ptx::tma_load_4d(sK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
     ptx::tma_load_4d(sV, &mapV, &bar_ld, 0, h, (int)t0, b);
   }
-  // decay of token t0 + tid: chunk-local log2 cumsum
-  const float la = log2f(p.a[((size_t)b * p.T + t0 + tid) * p.H + h]);
-  const float gi = block_scan128(la, s_warp);
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_base, 128);
+    ptx::tmem_relinquish();
+  }
+  // decay of token t0 + tid: chunk-local log2 cumsum (the scan also publishes tmem_base)
+  ptx::tc_fence_before();
+  const float gi = block_scan128(la, s_red);
+  ptx::tc_fence_after();
+  const uint32_t tbase = tmem_base;
   if (tid == kTile - 1) s_gamma = gi;
   bool ok = wait_bar(&bar_ld, 0);
   if (!ok) atomicExch(p.status, kStatusTimeout);
   ok = __syncthreads_and(ok);
   const float gamma = s_gamma;
   if (ok) {
-    // Ṽ row tid = 2^(gamma - g_tid) v_tid, split into a bf16 hi part (in place) and a
-    // bf16 lo part (the rounding remainder) so that Kᵀ(Ṽhi + Ṽlo) keeps ~16 bits.  The
-    // 128-byte swizzle permutes 16-byte chunks inside a row only, so rows map in place.
+    // Ṽ row tid = 2^(gamma - g_tid) v_tid as a bf16 hi part (in place) plus a bf16 lo
+    // part (the rounding remainder), so that Kᵀ(Ṽhi + Ṽlo) keeps ~16 bits.  The 128-byte
+    // swizzle permutes 16-byte chunks inside a row only, so rows map in place.
     const float w = exp2f(gamma - gi);
-    uint4* vrow = reinterpret_cast<uint4*>(sV + tid * 128);
-    uint4* vlo = reinterpret_cast<uint4*>(sV + 16384 + tid * 128);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      uint4 x = vrow[c], y;
+      const int off = tid * 128 + ((c ^ rot) << 4);
+      uint4 x = *reinterpret_cast<uint4*>(sV + off), y;
       __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
       __nv_bfloat162* hy = reinterpret_cast<__nv_bfloat162*>(&y);
 #pragma unroll
@@ -176,8 +237,8 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
         float2 r = __bfloat1622float2(hx[e]);
         hy[e] = __floats2bfloat162_rn(f.x - r.x, f.y - r.y);
       }
-      vrow[c] = x;
-      vlo[c] = y;
+      *reinterpret_cast<uint4*>(sV + off) = x;
+      *reinterpret_cast<uint4*>(sV + 16384 + off) = y;
     }
     ptx::fence_proxy_async_smem();
   }
@@ -221,77 +282,85 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   if (warp == 0) ptx::tmem_dealloc(tbase, 128);
   if (!ok) return;
 
-  // Fenwick tree climb.  Row `tid` of every node is owned by thread tid.
+  // Fenwick tree climb.  Row `tid` of every node is owned by thread tid.  Node images
+  // go through shared memory (sK, free now) so that global stores and loads coalesce.
+  uint8_t* stage = sK;             // 16 KB: outgoing image
+  uint8_t* stage_in = sK + 16384;  // 16 KB: sibling image
   float Gcur = gamma;
   int k = 0, idx = u;
   const size_t nbase = (size_t)bh * p.nnodes;
   while (true) {
     const size_t node = nbase + p.node_off[k] + idx;
-    float4* dst = reinterpret_cast<float4*>(p.node32 + node * kNodeF + tid * kDv);
+    {  // publish: fp16 image with scale 2^e, row tid at chunk slots c ^ (tid & 7)
+      float m = 0.f;
 #pragma unroll
-    for (int c = 0; c < kDv / 4; ++c)
-      dst[c] = make_float4(cur[4 * c], cur[4 * c + 1], cur[4 * c + 2], cur[4 * c + 3]);
-    if ((idx & 1) == 0) {
-      // bf16 image, hi part then lo part (rounding remainder): row tid (d_k index) holds
-      // 64 d_v values; 16-byte chunk c sits at c ^ (tid & 7) (128-byte swizzle).
-      uint8_t* img = p.img + node * kImgBytes + tid * 128;
+      for (int j = 0; j < kDv; ++j) m = fmaxf(m, fabsf(cur[j]));
+      const int e = f16_exp(block_max2(make_float2(m, 0.f), s_red2).x);
+      const float s = pow2i(-e);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        uint32_t hw[4], lw[4];
+        const int cc = c ^ rot;
+        *reinterpret_cast<uint4*>(stage + tid * 128 + (cc << 4)) =
+            make_uint4(pack_h2(cur[8 * c] * s, cur[8 * c + 1] * s),
+                       pack_h2(cur[8 * c + 2] * s, cur[8 * c + 3] * s),
+                       pack_h2(cur[8 * c + 4] * s, cur[8 * c + 5] * s),
+                       pack_h2(cur[8 * c + 6] * s, cur[8 * c + 7] * s));
+      }
+      __syncthreads();
+      uint4* dst = reinterpret_cast<uint4*>(p.img + node * kImgBytes);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_bf16(cur[8 * c + 2 * e], cur[8 * c + 2 * e + 1], hw[e], lw[e]);
-        *reinterpret_cast<uint4*>(img + ((c ^ (tid & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(img + kImgHalf + ((c ^ (tid & 7)) << 4)) =
-            make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      for (int r = 0; r < kImgBytes / 16 / 128; ++r)
+        dst[r * 128 + tid] = reinterpret_cast<const uint4*>(stage)[r * 128 + tid];
+      if (tid == 0) {
+        p.meta[node * kMeta + 1] = (unsigned)e;
+        p.meta[node * kMeta + 2] = __float_as_uint(Gcur);
       }
     }
-    if (tid == 0) p.nodeG[node] = Gcur;
     // parent exists only if both children are complete nodes
     if ((idx >> 1) >= (p.NT >> (k + 1))) break;
-    __threadfence();
+    __syncthreads();  // every thread's stores precede thread 0's release below
+    if (tid == 0) {
+      __threadfence();
+      s_flag = atomicAdd(p.meta + (nbase + p.node_off[k + 1] + (idx >> 1)) * kMeta, 1u);
+      __threadfence();
+    }
     __syncthreads();
-    if (tid == 0) s_flag = atomicAdd(p.cnt + nbase + p.node_off[k + 1] + (idx >> 1), 1u);
-    __syncthreads();
-    const unsigned first = (s_flag == 0u);
-    if (first) break;  // first of the two siblings: the other one merges
-    __threadfence();
+    if (s_flag == 0u) break;  // first of the two siblings: the other one merges
     const size_t sib = nbase + p.node_off[k] + (idx ^ 1);
-    const float Gs = __ldcg(p.nodeG + sib);
-    const float4* src = reinterpret_cast<const float4*>(p.node32 + sib * kNodeF + tid * kDv);
-    if (idx & 1) {  // sibling is the left (earlier) block: decay it across ours
-      const float d = exp2f(Gcur);
 #pragma unroll
-      for (int c = 0; c < kDv / 4; ++c) {
-        float4 s4 = __ldcg(src + c);
-        cur[4 * c] += d * s4.x;
-        cur[4 * c + 1] += d * s4.y;
-        cur[4 * c + 2] += d * s4.z;
-        cur[4 * c + 3] += d * s4.w;
-      }
-    } else {  // sibling is the right block: decay ours across it
-      const float d = exp2f(Gs);
+    for (int r = 0; r < kImgBytes / 16 / 128; ++r)
+      reinterpret_cast<uint4*>(stage_in)[r * 128 + tid] =
+          __ldcg(reinterpret_cast<const uint4*>(p.img + sib * kImgBytes) + r * 128 + tid);
+    const float ss = pow2i((int)__ldcg(p.meta + sib * kMeta + 1));
+    const float Gs = __uint_as_float(__ldcg(p.meta + sib * kMeta + 2));
+    __syncthreads();
+    const bool left_sib = (idx & 1) != 0;  // sibling is the earlier block
+    const float dcur = left_sib ? 1.f : exp2f(Gs);
+    const float dsib = (left_sib ? exp2f(Gcur) : 1.f) * ss;
 #pragma unroll
-      for (int c = 0; c < kDv / 4; ++c) {
-        float4 s4 = __ldcg(src + c);
-        cur[4 * c] = d * cur[4 * c] + s4.x;
-        cur[4 * c + 1] = d * cur[4 * c + 1] + s4.y;
-        cur[4 * c + 2] = d * cur[4 * c + 2] + s4.z;
-        cur[4 * c + 3] = d * cur[4 * c + 3] + s4.w;
+    for (int c = 0; c < 8; ++c) {
+      uint4 v4 = *reinterpret_cast<const uint4*>(stage_in + tid * 128 + ((c ^ rot) << 4));
+      const __half2* hv = reinterpret_cast<const __half2*>(&v4);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 f = __half22float2(hv[e]);
+        cur[8 * c + 2 * e] = dcur * cur[8 * c + 2 * e] + dsib * f.x;
+        cur[8 * c + 2 * e + 1] = dcur * cur[8 * c + 2 * e + 1] + dsib * f.y;
       }
     }
     Gcur += Gs;
     ++k;
     idx >>= 1;
-    __syncthreads();  // s_flag is rewritten next round
+    __syncthreads();  // staging buffers and s_flag are reused next round
   }
 }
 
 // ---------------------------------------------------------------------------------
-// tc_output: level-fused inter-tile buckets, then intra-tile masked attention.
+// tc_output: intra-tile masked attention + level-fused inter-tile buckets.
 //
-// Shared memory (2 CTAs per SM): R1 = Q, later the lo part of P; R2 = K, later the hi
-// part of P; R3 = the current node image [hi | lo], later V.  TMEM (256 columns):
-// S = Q Kᵀ in columns 0..127; Y = Q [Ehi | Elo] in 128..255, later O = P V in 128..191.
+// Shared memory (2 CTAs per SM): RQ = Q (bf16, then fp16 in place after S); RK = K
+// (bf16), then P (fp16); RV = V (bf16, then fp16 in place); RE = one node image.
+// TMEM (256 columns): S in 0..127, O in 128..191, Y in 192..255.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                         const __grid_constant__ CUtensorMap mapK,
@@ -299,17 +368,19 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
                                                         TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* R1 = smem;             // 32 KB
-  uint8_t* R2 = smem + 32768;     // 32 KB
-  uint8_t* R3 = smem + 65536;     // 32 KB
-  float* sG = reinterpret_cast<float*>(smem + 98304);    // 128 floats: g
-  float* sLam = reinterpret_cast<float*>(smem + 98816);  // 128 x 9 floats: lambda^0..7
-  __shared__ __align__(8) uint64_t bar_qk, bar_s, bar_e, bar_y, bar_v, bar_o;
+  uint8_t* RQ = smem;           // 32 KB (two d_k blocks of 64)
+  uint8_t* RK = smem + 32768;   // 32 KB
+  uint8_t* RV = smem + 65536;   // 16 KB
+  uint8_t* RE = smem + 81920;   // 16 KB
+  float* sG = reinterpret_cast<float*>(smem + 98304);  // 128 floats: g
+  float* sB = reinterpret_cast<float*>(smem + 98816);  // 128 floats: 2^(g_end(group) - g_s)
+  __shared__ __align__(8) uint64_t bar_ld, bar_s, bar_o, bar_e, bar_y;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_warp[4];
+  __shared__ float s_red[4];
+  __shared__ float2 s_red2[4];
   __shared__ int s_ok;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, rot = tid & 7;
   const int lin = blockIdx.x;
   const int h = lin % p.H;
   const int u = (lin / p.H) % p.NT;
@@ -318,56 +389,58 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
   const int bh = b * p.H + h;
   const long long t0 = (long long)u * kTile;
   const size_t nbase = (size_t)bh * p.nnodes;
+  const size_t row = (size_t)b * p.T + t0 + tid;  // token of this thread's query row
+  const float* lrow = p.lam + (row * p.H + h) * p.L;
+  const float la = log2f(p.a[row * p.H + h]);
+  float lam8[kLevIntra];
+#pragma unroll
+  for (int l = 0; l < kLevIntra; ++l) lam8[l] = lrow[l];
 
+  const int mlow = (u == 0) ? -1 : __ffs(u) - 1;  // nearest inter-tile level, if any
   if (tid == 0) {
-    ptx::mbar_init(&bar_qk, 1);
+    ptx::mbar_init(&bar_ld, 1);
     ptx::mbar_init(&bar_s, 1);
+    ptx::mbar_init(&bar_o, 1);
     ptx::mbar_init(&bar_e, 1);
     ptx::mbar_init(&bar_y, 1);
-    ptx::mbar_init(&bar_v, 1);
-    ptx::mbar_init(&bar_o, 1);
     ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 * 2 + 16384);
+    ptx::tma_load_4d(RQ, &mapQ, &bar_ld, 0, g, (int)t0, b);
+    ptx::tma_load_4d(RQ + 16384, &mapQ, &bar_ld, 64, g, (int)t0, b);
+    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
+    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
+    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
+    if (mlow >= 0) {
+      const size_t node = nbase + p.node_off[mlow] + ((u >> mlow) - 1);
+      ptx::mbar_arrive_expect_tx(&bar_e, kImgBytes);
+      ptx::bulk_load(RE, p.img + node * kImgBytes, kImgBytes, &bar_e);
+    }
   }
   if (warp == 0) {
     ptx::tmem_alloc(&tmem_base, 256);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  const float gt = block_scan128(la, s_red);  // also publishes tmem_base
   ptx::tc_fence_after();
   const uint32_t tbase = tmem_base;
-  const uint32_t tS = tbase, tY = tbase + 128, tO = tbase + 128;
+  const uint32_t tS = tbase, tO = tbase + 128, tY = tbase + 192;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-
-  const int mlow = (u == 0) ? -1 : __ffs(u) - 1;  // nearest inter-tile level, if any
-  if (tid == 0) {
-    ptx::mbar_arrive_expect_tx(&bar_qk, 32768 * 2);
-    ptx::tma_load_4d(R1, &mapQ, &bar_qk, 0, g, (int)t0, b);
-    ptx::tma_load_4d(R1 + 16384, &mapQ, &bar_qk, 64, g, (int)t0, b);
-    ptx::tma_load_4d(R2, &mapK, &bar_qk, 0, g, (int)t0, b);
-    ptx::tma_load_4d(R2 + 16384, &mapK, &bar_qk, 64, g, (int)t0, b);
-    if (mlow >= 0) {
-      const size_t node = nbase + p.node_off[mlow] + ((u >> mlow) - 1);
-      ptx::mbar_arrive_expect_tx(&bar_e, kImgBytes);
-      ptx::bulk_load(R3, p.img + node * kImgBytes, kImgBytes, &bar_e);
-    }
-  }
-  const size_t row = (size_t)b * p.T + t0 + tid;  // token of this thread's query row
-  const float la = log2f(p.a[row * p.H + h]);
-  const float gt = block_scan128(la, s_warp);
   sG[tid] = gt;
-  const float* lrow = p.lam + (row * p.H + h) * p.L;
+  float lmax = 0.f;
 #pragma unroll
-  for (int l = 0; l < kLevIntra; ++l) sLam[tid * 9 + l] = lrow[l];
-  bool ok = wait_bar(&bar_qk, 0);
+  for (int l = 0; l < kLevIntra; ++l) lmax = fmaxf(lmax, fabsf(lam8[l]));
+  __syncthreads();
+  sB[tid] = exp2f(sG[tid | 31] - gt);  // decay from key tid to the end of its 32-key group
+  bool ok = wait_bar(&bar_ld, 0);
   if (!ok) atomicExch(p.status, kStatusTimeout);
   ok = __syncthreads_and(ok);
 
-  // S = Q Kᵀ (M = 128 queries, N = 128 keys, K = 128 d_k), both K-major.
+  // S = Q Kᵀ (M = 128 queries, N = 128 keys, K = 128 d_k), bf16, both K-major.
   if (ok && tid == 0) {
     ptx::tc_fence_after();
     const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 0);
-    const uint32_t q0 = ptx::smem_u32(R1), k0 = ptx::smem_u32(R2);
+    const uint32_t q0 = ptx::smem_u32(RQ), k0 = ptx::smem_u32(RK);
 #pragma unroll
     for (int kk = 0; kk < kDk / 16; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -376,9 +449,115 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
     }
     ptx::umma_commit(&bar_s);
   }
+  // tile scales of Q and V (reading bf16 while the MMA reads Q is fine); V -> fp16 now
+  int eq = 0, ev = 0;
+  if (ok) {
+    float2 m2;
+    m2.x = fmaxf(row_absmax_bf16(RQ + tid * 128, rot), row_absmax_bf16(RQ + 16384 + tid * 128, rot));
+    m2.y = row_absmax_bf16(RV + tid * 128, rot);
+    m2 = block_max2(m2, s_red2);
+    eq = f16_exp(m2.x);
+    ev = f16_exp(m2.y);
+    row_bf16_to_f16(RV + tid * 128, rot, pow2i(-ev));
+    ok = wait_bar(&bar_s, 0);
+    if (!ok) atomicExch(p.status, kStatusTimeout);
+  }
+  ok = __syncthreads_and(ok);
+  if (ok) {
+    // S has been computed: Q -> fp16 in place for the node MMAs
+    row_bf16_to_f16(RQ + tid * 128, rot, pow2i(-eq));
+    row_bf16_to_f16(RQ + 16384 + tid * 128, rot, pow2i(-eq));
+  }
 
-  // inter-tile levels, nearest first: Y = Q [Ehi | Elo] (N = 128: two 64-wide MN atoms of
-  // the node image, 16 KB apart), rows weighted by lambda_t^(8+m) 2^(g_t + D).
+  // P row t = tid in fp16 with row scale 2^-ep, written over K (consumed by S).
+  int ep = 0;
+  if (ok) {
+    ptx::tc_fence_after();
+    const int t = tid;
+    float smax = 0.f;
+#pragma unroll 1
+    for (int cg = 0; cg <= warp; ++cg) {  // warp-uniform bound: tcgen05.ld is collective
+      float sv[32];
+      ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (cg * 32 + j <= t) smax = fmaxf(smax, fabsf(sv[j]));
+    }
+    ep = f16_exp(smax * lmax);  // |P| <= max|S| * max lambda (decays are <= 1)
+    const float coef = pow2i(-ep);
+#pragma unroll 1
+    for (int cg = 0; cg < 4; ++cg) {
+      uint32_t pk[16];
+      if (cg < warp) {
+        // keys of an earlier 32-group: one level (6 or 7) and a factored decay
+        float sv[32];
+        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+        ptx::tmem_ld_wait();
+        const int l = 5 + (32 - __clz(warp ^ cg));
+        const float cA = coef * (l == 6 ? lam8[6] : lam8[7]) * exp2f(gt - sG[cg * 32 + 31]);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2)
+          pk[j >> 1] = pack_h2(sv[j] * cA * sB[cg * 32 + j], sv[j + 1] * cA * sB[cg * 32 + j + 1]);
+      } else if (cg == warp) {
+        // the diagonal 32-group: levels 0..5 and the decay per key
+        float sv[32];
+        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float v[2];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int s = cg * 32 + j + q;
+            float val = 0.f;
+            if (s <= t) {
+              const int l = (s == t) ? 0 : 32 - __clz(t ^ s);
+              float lv = lam8[0];
+              lv = (l == 1) ? lam8[1] : lv;
+              lv = (l == 2) ? lam8[2] : lv;
+              lv = (l == 3) ? lam8[3] : lv;
+              lv = (l == 4) ? lam8[4] : lv;
+              lv = (l == 5) ? lam8[5] : lv;
+              val = sv[j + q] * coef * lv * exp2f(gt - sG[s]);
+            }
+            v[q] = val;
+          }
+          pk[j >> 1] = pack_h2(v[0], v[1]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+      }
+      // 4 chunks of 8 keys: key block cg / 2, chunk index (cg % 2) * 4 + qd
+      uint8_t* prow = RK + (cg >> 1) * 16384 + t * 128;
+#pragma unroll
+      for (int qd = 0; qd < 4; ++qd) {
+        const int c = (cg & 1) * 4 + qd;
+        *reinterpret_cast<uint4*>(prow + ((c ^ rot) << 4)) =
+            make_uint4(pk[4 * qd], pk[4 * qd + 1], pk[4 * qd + 2], pk[4 * qd + 3]);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  // O = P V (M = 128, N = 64, K = 128 keys): P K-major, V MN-major, fp16.
+  if (ok && tid == 0) {
+    ptx::tc_fence_after();
+    const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
+    const uint32_t p0 = ptx::smem_u32(RK), v0 = ptx::smem_u32(RV);
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk) {
+      const uint32_t offp = (kk >> 2) * 16384 + (kk & 3) * 32;
+      ptx::umma_f16(tO, ptx::smem_desc_sw128(p0 + offp, 16, 1024),
+                    ptx::smem_desc_sw128(v0 + kk * 2048, 1024, 1024), idesc, kk > 0);
+    }
+    ptx::umma_commit(&bar_o);
+  }
+
+  // inter-tile levels, nearest first: Y = Q · Node (fp16, Node MN-major), rows weighted by
+  // lambda_t^(8+m) 2^(g_t + D) and the two scales.
   float acc[kDv];
 #pragma unroll
   for (int j = 0; j < kDv; ++j) acc[j] = 0.f;
@@ -391,25 +570,25 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
       bool okw = wait_bar(&bar_e, it & 1);
       if (okw) {
         ptx::tc_fence_after();
-        const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 1);
-        const uint32_t q0 = ptx::smem_u32(R1), e0 = ptx::smem_u32(R3);
+        const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
+        const uint32_t q0 = ptx::smem_u32(RQ), e0 = ptx::smem_u32(RE);
 #pragma unroll
         for (int kk = 0; kk < kDk / 16; ++kk) {
           const uint32_t offq = (kk >> 2) * 16384 + (kk & 3) * 32;
           ptx::umma_f16(tY, ptx::smem_desc_sw128(q0 + offq, 16, 1024),
-                        ptx::smem_desc_sw128(e0 + kk * 2048, kImgHalf, 1024), idesc, kk > 0);
+                        ptx::smem_desc_sw128(e0 + kk * 2048, 1024, 1024), idesc, kk > 0);
         }
         ptx::umma_commit(&bar_y);
         okw = wait_bar(&bar_y, it & 1);
       }
       if (!okw) atomicExch(p.status, kStatusTimeout);
-      // next level's image (the MMA reading R3 has completed)
+      // next level's image (the MMA reading RE has completed)
       int mn = m + 1;
       while (mn < 31 && (u >> mn) > 0 && !((u >> mn) & 1)) ++mn;
       if (okw && mn < 31 && (u >> mn) > 0) {
         const size_t nn = nbase + p.node_off[mn] + ((u >> mn) - 1);
         ptx::mbar_arrive_expect_tx(&bar_e, kImgBytes);
-        ptx::bulk_load(R3, p.img + nn * kImgBytes, kImgBytes, &bar_e);
+        ptx::bulk_load(RE, p.img + nn * kImgBytes, kImgBytes, &bar_e);
       }
       s_ok = okw ? 1 : 0;
     }
@@ -417,98 +596,22 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
     ok = s_ok != 0;
     if (!ok) break;
     ptx::tc_fence_after();
-    const float w = lrow[kLevIntra + m] * exp2f(gt + D);
+    const int en = (int)p.meta[node * kMeta + 1];
+    const float wy = lrow[kLevIntra + m] * exp2f(gt + D) * pow2s(eq + en);
+    float y[32];
+    ptx::tmem_ld32(tY + lane_off, y);
+    ptx::tmem_ld_wait();
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float yh[32], yl[32];
-      ptx::tmem_ld32(tY + lane_off + half * 32, yh);
-      ptx::tmem_ld32(tY + lane_off + 64 + half * 32, yl);
-      ptx::tmem_ld_wait();
+    for (int j = 0; j < 32; ++j) acc[j] += wy * y[j];
+    ptx::tmem_ld32(tY + lane_off + 32, y);
+    ptx::tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[half * 32 + j] += w * (yh[j] + yl[j]);
-    }
-    D += __ldcg(p.nodeG + node);
+    for (int j = 0; j < 32; ++j) acc[32 + j] += wy * y[j];
+    D += __uint_as_float(p.meta[node * kMeta + 2]);
     ++it;
     ptx::tc_fence_before();
     __syncthreads();  // Y is rewritten by the next level's MMA
   }
-  // every MMA reading Q or the node image has completed: R3 takes V
-  if (ok && tid == 0) {
-    ptx::mbar_arrive_expect_tx(&bar_v, 16384);
-    ptx::tma_load_4d(R3, &mapV, &bar_v, 0, h, (int)t0, b);
-  }
-  if (ok) {
-    ok = wait_bar(&bar_s, 0);
-    if (!ok) atomicExch(p.status, kStatusTimeout);
-  }
-  ok = __syncthreads_and(ok);
-  if (ok) {
-    ptx::tc_fence_after();
-    // P row t = tid, keys in 32-column groups; groups above the diagonal are zero.
-    // hi part -> R2 (K is consumed), lo part -> R1 (Q is consumed).
-    const int t = tid;
-#pragma unroll 1
-    for (int cg = 0; cg < 4; ++cg) {
-      float sv[32];
-      // tcgen05.ld is warp-collective: the whole warp loads when any lane needs it
-      const bool warp_any = cg <= warp;
-      if (warp_any) {
-        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
-        ptx::tmem_ld_wait();
-      }
-      uint32_t ph[16], pl[16];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        float v0 = 0.f, v1 = 0.f;
-        const int s0 = cg * 32 + j, s1 = s0 + 1;
-        if (warp_any && s0 <= t) {
-          const int l0 = (s0 == t) ? 0 : 32 - __clz(t ^ s0);
-          v0 = sv[j] * sLam[t * 9 + l0] * exp2f(gt - sG[s0]);
-        }
-        if (warp_any && s1 <= t) {
-          const int l1 = (s1 == t) ? 0 : 32 - __clz(t ^ s1);
-          v1 = sv[j + 1] * sLam[t * 9 + l1] * exp2f(gt - sG[s1]);
-        }
-        split_bf16(v0, v1, ph[j >> 1], pl[j >> 1]);
-      }
-      // 4 chunks of 8 keys: key block kb = cg / 2, chunk index c = (cg % 2) * 4 + qd
-      const int off = (cg >> 1) * 16384 + t * 128;
-#pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {
-        const int c = (cg & 1) * 4 + qd;
-        const int o16 = off + ((c ^ (t & 7)) << 4);
-        *reinterpret_cast<uint4*>(R2 + o16) =
-            make_uint4(ph[4 * qd], ph[4 * qd + 1], ph[4 * qd + 2], ph[4 * qd + 3]);
-        *reinterpret_cast<uint4*>(R1 + o16) =
-            make_uint4(pl[4 * qd], pl[4 * qd + 1], pl[4 * qd + 2], pl[4 * qd + 3]);
-      }
-    }
-    ptx::fence_proxy_async_smem();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  // O = (Phi + Plo) V (M = 128, N = 64, K = 128 keys): P K-major, V MN-major.
-  if (ok && tid == 0) {
-    bool okv = wait_bar(&bar_v, 0);
-    if (okv) {
-      ptx::tc_fence_after();
-      const uint32_t idesc = ptx::idesc_bf16_f32(128, 64, 0, 1);
-      const uint32_t ph0 = ptx::smem_u32(R2), pl0 = ptx::smem_u32(R1), v0 = ptx::smem_u32(R3);
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint32_t offp = (kk >> 2) * 16384 + (kk & 3) * 32;
-        const uint64_t dv = ptx::smem_desc_sw128(v0 + kk * 2048, 1024, 1024);
-        ptx::umma_f16(tO, ptx::smem_desc_sw128(ph0 + offp, 16, 1024), dv, idesc, kk > 0);
-        ptx::umma_f16(tO, ptx::smem_desc_sw128(pl0 + offp, 16, 1024), dv, idesc, 1);
-      }
-      ptx::umma_commit(&bar_o);
-    } else {
-      atomicExch(p.status, kStatusTimeout);
-    }
-    s_ok = okv ? 1 : 0;
-  }
-  __syncthreads();
-  if (ok) ok = s_ok != 0;
   if (ok) {
     ok = wait_bar(&bar_o, 0);
     if (!ok) atomicExch(p.status, kStatusTimeout);
@@ -516,6 +619,7 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
   ok = __syncthreads_and(ok);
   if (ok) {
     ptx::tc_fence_after();
+    const float so = pow2s(ep + ev);
     __nv_bfloat16* orow = p.o + (row * p.H + h) * kDv;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -525,7 +629,7 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2)
-        pk[j >> 1] = pack_bf16(y[j] + acc[half * 32 + j], y[j + 1] + acc[half * 32 + j + 1]);
+        pk[j >> 1] = pack_bf16(y[j] * so + acc[half * 32 + j], y[j + 1] * so + acc[half * 32 + j + 1]);
       uint4* dst = reinterpret_cast<uint4*>(orow + half * 32);
 #pragma unroll
       for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
@@ -541,21 +645,43 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) tc_export_kernel(TcParams p, int SL, float* st, float* lsc) {
   const int lvl = blockIdx.x, bh = blockIdx.y;
-  float* dst = st + ((size_t)bh * SL + lvl) * kNodeF;
+  float* dst = st + ((size_t)bh * SL + lvl) * (kDk * kDv);
   const bool live = lvl >= 1 && ((((long long)p.T) >> (lvl - 1)) & 1);
   float scale = 0.f;
-  const float* src = nullptr;
+  const uint8_t* img = nullptr;
   if (live) {
     const int m = lvl - kLevIntra;
     const size_t nbase = (size_t)bh * p.nnodes;
     float D = 0.f;
     for (int mm = 0; mm < m; ++mm)
-      if ((p.NT >> mm) & 1) D += p.nodeG[nbase + p.node_off[mm] + ((p.NT >> mm) - 1)];
-    scale = exp2f(D);
-    src = p.node32 + (nbase + p.node_off[m] + ((p.NT >> m) - 1)) * kNodeF;
+      if ((p.NT >> mm) & 1)
+        D += __uint_as_float(p.meta[(nbase + p.node_off[mm] + ((p.NT >> mm) - 1)) * kMeta + 2]);
+    const size_t node = nbase + p.node_off[m] + ((p.NT >> m) - 1);
+    scale = exp2f(D) * pow2i((int)p.meta[node * kMeta + 1]);
+    img = p.img + node * kImgBytes;
   }
-  for (int e = threadIdx.x; e < kNodeF; e += 256) dst[e] = live ? scale * src[e] : 0.f;
+  for (int e = threadIdx.x; e < kDk * kDv; e += 256) {
+    float v = 0.f;
+    if (live) {
+      const int i = e / kDv, j = e % kDv, c = j >> 3;
+      const __half x = *reinterpret_cast<const __half*>(img + i * 128 + ((c ^ (i & 7)) << 4) + (j & 7) * 2);
+      v = scale * __half2float(x);
+    }
+    dst[e] = v;
+  }
   if (lsc && threadIdx.x == 0) lsc[(size_t)bh * SL + lvl] = 0.f;
+}
+
+__global__ void wait_selftest_kernel(unsigned* status, long long spins) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!ptx::mbar_wait(&bar, 0, spins)) atomicExch(status, kStatusTimeout);
+  }
 }
 
 // ---------------------------------------------------------------------------------
@@ -592,19 +718,7 @@ bool make_map(CUtensorMap* m, const void* base, int inner, int count, int T, int
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int kSmemState = 32768 + 32768 + 1024;
-constexpr int kSmemOutput = 98816 + 128 * 9 * 4 + 1024;
-
-__global__ void wait_selftest_kernel(unsigned* status, long long spins) {
-  __shared__ __align__(8) uint64_t bar;
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(&bar, 1);
-    ptx::fence_mbar_init();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    if (!ptx::mbar_wait(&bar, 0, spins)) atomicExch(status, kStatusTimeout);
-  }
-}
+constexpr int kSmemOutput = 98816 + 512 + 1024;
 
 }  // namespace
 
@@ -635,16 +749,11 @@ bool make_tc_plan(const ll_shape& s, TcPlan* p) {
   p->nnodes = off;
   const size_t BH = (size_t)p->B * p->H;
   size_t o = 0;
-  p->off_node32 = o;
-  o = a256(o + sizeof(float) * BH * p->nnodes * kNodeF);
-  p->off_node16 = o;
+  p->off_img = o;
   o = a256(o + BH * p->nnodes * (size_t)kImgBytes);
-  p->off_nodeG = o;
-  o = a256(o + sizeof(float) * BH * p->nnodes);
-  p->off_cnt = o;
-  p->cnt_bytes = sizeof(unsigned) * BH * p->nnodes;
-  o = a256(o + p->cnt_bytes);
-  p->off_gam = 0;
+  p->off_meta = o;
+  p->meta_bytes = sizeof(unsigned) * BH * p->nnodes * kMeta;
+  o = a256(o + p->meta_bytes);
   p->bytes = o;
   return true;
 }
@@ -668,12 +777,10 @@ cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   p.a = a.a;
   p.lam = a.lam;
   p.o = static_cast<__nv_bfloat16*>(a.o);
-  p.node32 = reinterpret_cast<float*>(a.ws + tp.off_node32);
-  p.img = reinterpret_cast<uint8_t*>(a.ws + tp.off_node16);
-  p.nodeG = reinterpret_cast<float*>(a.ws + tp.off_nodeG);
-  p.cnt = reinterpret_cast<unsigned*>(a.ws + tp.off_cnt);
+  p.img = reinterpret_cast<uint8_t*>(a.ws + tp.off_img);
+  p.meta = reinterpret_cast<unsigned*>(a.ws + tp.off_meta);
   p.status = a.status;
-  cudaError_t e = cudaMemsetAsync(p.cnt, 0, tp.cnt_bytes, st);
+  cudaError_t e = cudaMemsetAsync(p.meta, 0, tp.meta_bytes, st);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((size_t)tp.B * tp.NT * tp.H);
   e = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemState);
