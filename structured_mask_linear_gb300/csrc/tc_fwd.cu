@@ -115,7 +115,7 @@ __device__ __forceinline__ float2 block_max2(float2 v, float2* s_red2) {
   if (lane == 0) s_red2[warp] = v;
   __syncthreads();
   float2 r = s_red2[0];
-  for (int w = 1; w < 4; ++w) {
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
     r.x = fmaxf(r.x, s_red2[w].x);
     r.y = fmaxf(r.y, s_red2[w].y);
   }
@@ -319,11 +319,8 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
     // parent exists only if both children are complete nodes
     if ((idx >> 1) >= (p.NT >> (k + 1))) break;
     __syncthreads();  // every thread's stores precede thread 0's release below
-    if (tid == 0) {
-      __threadfence();
-      s_flag = atomicAdd(p.meta + (nbase + p.node_off[k + 1] + (idx >> 1)) * kMeta, 1u);
-      __threadfence();
-    }
+    if (tid == 0)
+      s_flag = ptx::atom_add_acq_rel_gpu(p.meta + (nbase + p.node_off[k + 1] + (idx >> 1)) * kMeta, 1u);
     __syncthreads();
     if (s_flag == 0u) break;  // first of the two siblings: the other one merges
     const size_t sib = nbase + p.node_off[k] + (idx ^ 1);
@@ -358,14 +355,17 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
 // ---------------------------------------------------------------------------------
 // tc_output: intra-tile masked attention + level-fused inter-tile buckets.
 //
+// 256 threads in two roles after a common prologue: warps 0-3 form P (row = thread) and
+// issue O = P V; warps 4-7 run the inter-tile levels at the same time and finally write
+// o.  Both roles see every TMEM lane through warp % 4.
 // Shared memory (2 CTAs per SM): RQ = Q (bf16, then fp16 in place after S); RK = K
 // (bf16), then P (fp16); RV = V (bf16, then fp16 in place); RE = one node image.
 // TMEM (256 columns): S in 0..127, O in 128..191, Y in 192..255.
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ CUtensorMap mapQ,
-                                                        const __grid_constant__ CUtensorMap mapK,
-                                                        const __grid_constant__ CUtensorMap mapV,
-                                                        TcParams p) {
+__global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant__ CUtensorMap mapQ,
+                                                           const __grid_constant__ CUtensorMap mapK,
+                                                           const __grid_constant__ CUtensorMap mapV,
+                                                           TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* RQ = smem;           // 32 KB (two d_k blocks of 64)
@@ -374,13 +374,18 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
   uint8_t* RE = smem + 81920;   // 16 KB
   float* sG = reinterpret_cast<float*>(smem + 98304);  // 128 floats: g
   float* sB = reinterpret_cast<float*>(smem + 98816);  // 128 floats: 2^(g_end(group) - g_s)
+  int* sEp = reinterpret_cast<int*>(smem + 99328);     // 128 ints: P row scale exponents
   __shared__ __align__(8) uint64_t bar_ld, bar_s, bar_o, bar_e, bar_y;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_red[4];
-  __shared__ float2 s_red2[4];
+  __shared__ float s_red[8];
+  __shared__ float2 s_red2[8];
   __shared__ int s_ok;
 
-  const int tid = threadIdx.x, warp = tid >> 5, rot = tid & 7;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & 127;             // query row (tile-local token)
+  const int quad = warp & 3;           // TMEM lane quadrant of this warp
+  const bool role_b = warp >= 4;       // inter-tile levels and the final write
+  const int rot = r & 7;
   const int lin = blockIdx.x;
   const int h = lin % p.H;
   const int u = (lin / p.H) % p.NT;
@@ -389,7 +394,7 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
   const int bh = b * p.H + h;
   const long long t0 = (long long)u * kTile;
   const size_t nbase = (size_t)bh * p.nnodes;
-  const size_t row = (size_t)b * p.T + t0 + tid;  // token of this thread's query row
+  const size_t row = (size_t)b * p.T + t0 + r;  // token of this thread's query row
   const float* lrow = p.lam + (row * p.H + h) * p.L;
   const float la = log2f(p.a[row * p.H + h]);
   float lam8[kLevIntra];
@@ -420,18 +425,27 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
     ptx::tmem_alloc(&tmem_base, 256);
     ptx::tmem_relinquish();
   }
+  // chunk-local log2 decay cumsum over the 128 rows (both roles compute it)
+  float gt = la;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, gt, off);
+    if (lane >= off) gt += y;
+  }
+  if (lane == 31) s_red[warp] = gt;
   ptx::tc_fence_before();
-  const float gt = block_scan128(la, s_red);  // also publishes tmem_base
+  __syncthreads();
   ptx::tc_fence_after();
+  for (int w = 0; w < quad; ++w) gt += s_red[w];
   const uint32_t tbase = tmem_base;
   const uint32_t tS = tbase, tO = tbase + 128, tY = tbase + 192;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  sG[tid] = gt;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  if (!role_b) sG[r] = gt;
   float lmax = 0.f;
 #pragma unroll
   for (int l = 0; l < kLevIntra; ++l) lmax = fmaxf(lmax, fabsf(lam8[l]));
   __syncthreads();
-  sB[tid] = exp2f(sG[tid | 31] - gt);  // decay from key tid to the end of its 32-key group
+  if (!role_b) sB[r] = exp2f(sG[r | 31] - gt);  // decay from key r to the end of its 32-group
   bool ok = wait_bar(&bar_ld, 0);
   if (!ok) atomicExch(p.status, kStatusTimeout);
   ok = __syncthreads_and(ok);
@@ -449,190 +463,221 @@ __global__ void __launch_bounds__(128) tc_output_kernel(const __grid_constant__ 
     }
     ptx::umma_commit(&bar_s);
   }
-  // tile scales of Q and V (reading bf16 while the MMA reads Q is fine); V -> fp16 now
+  // tile scales of Q and V (reading bf16 while the MMA reads Q is fine); V -> fp16 now.
+  // Q: role a takes d_k block 0 of its row, role b block 1; V: each takes half the chunks.
+  uint8_t* qrow = RQ + (role_b ? 16384 : 0) + r * 128;
+  uint8_t* vrow = RV + r * 128;
+  const int vc0 = role_b ? 4 : 0;
   int eq = 0, ev = 0;
   if (ok) {
-    float2 m2;
-    m2.x = fmaxf(row_absmax_bf16(RQ + tid * 128, rot), row_absmax_bf16(RQ + 16384 + tid * 128, rot));
-    m2.y = row_absmax_bf16(RV + tid * 128, rot);
+    float2 m2 = make_float2(row_absmax_bf16(qrow, rot), 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 x = *reinterpret_cast<const uint4*>(vrow + (((vc0 + i) ^ rot) << 4));
+      const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 f = __bfloat1622float2(hx[e]);
+        m2.y = fmaxf(m2.y, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
     m2 = block_max2(m2, s_red2);
     eq = f16_exp(m2.x);
     ev = f16_exp(m2.y);
-    row_bf16_to_f16(RV + tid * 128, rot, pow2i(-ev));
+    const float sv_ = pow2i(-ev);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4* qv = reinterpret_cast<uint4*>(vrow + (((vc0 + i) ^ rot) << 4));
+      uint4 x = *qv, y;
+      const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&x);
+      __half2* hy = reinterpret_cast<__half2*>(&y);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 f = __bfloat1622float2(hx[e]);
+        hy[e] = __floats2half2_rn(f.x * sv_, f.y * sv_);
+      }
+      *qv = y;
+    }
     ok = wait_bar(&bar_s, 0);
     if (!ok) atomicExch(p.status, kStatusTimeout);
   }
   ok = __syncthreads_and(ok);
   if (ok) {
-    // S has been computed: Q -> fp16 in place for the node MMAs
-    row_bf16_to_f16(RQ + tid * 128, rot, pow2i(-eq));
-    row_bf16_to_f16(RQ + 16384 + tid * 128, rot, pow2i(-eq));
-  }
-
-  // P row t = tid in fp16 with row scale 2^-ep, written over K (consumed by S).
-  int ep = 0;
-  if (ok) {
-    ptx::tc_fence_after();
-    const int t = tid;
-    float smax = 0.f;
-#pragma unroll 1
-    for (int cg = 0; cg <= warp; ++cg) {  // warp-uniform bound: tcgen05.ld is collective
-      float sv[32];
-      ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (cg * 32 + j <= t) smax = fmaxf(smax, fabsf(sv[j]));
-    }
-    ep = f16_exp(smax * lmax);  // |P| <= max|S| * max lambda (decays are <= 1)
-    const float coef = pow2i(-ep);
-#pragma unroll 1
-    for (int cg = 0; cg < 4; ++cg) {
-      uint32_t pk[16];
-      if (cg < warp) {
-        // keys of an earlier 32-group: one level (6 or 7) and a factored decay
-        float sv[32];
-        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
-        ptx::tmem_ld_wait();
-        const int l = 5 + (32 - __clz(warp ^ cg));
-        const float cA = coef * (l == 6 ? lam8[6] : lam8[7]) * exp2f(gt - sG[cg * 32 + 31]);
-#pragma unroll
-        for (int j = 0; j < 32; j += 2)
-          pk[j >> 1] = pack_h2(sv[j] * cA * sB[cg * 32 + j], sv[j + 1] * cA * sB[cg * 32 + j + 1]);
-      } else if (cg == warp) {
-        // the diagonal 32-group: levels 0..5 and the decay per key
-        float sv[32];
-        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float v[2];
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int s = cg * 32 + j + q;
-            float val = 0.f;
-            if (s <= t) {
-              const int l = (s == t) ? 0 : 32 - __clz(t ^ s);
-              float lv = lam8[0];
-              lv = (l == 1) ? lam8[1] : lv;
-              lv = (l == 2) ? lam8[2] : lv;
-              lv = (l == 3) ? lam8[3] : lv;
-              lv = (l == 4) ? lam8[4] : lv;
-              lv = (l == 5) ? lam8[5] : lv;
-              val = sv[j + q] * coef * lv * exp2f(gt - sG[s]);
-            }
-            v[q] = val;
-          }
-          pk[j >> 1] = pack_h2(v[0], v[1]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) pk[j] = 0u;
-      }
-      // 4 chunks of 8 keys: key block cg / 2, chunk index (cg % 2) * 4 + qd
-      uint8_t* prow = RK + (cg >> 1) * 16384 + t * 128;
-#pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {
-        const int c = (cg & 1) * 4 + qd;
-        *reinterpret_cast<uint4*>(prow + ((c ^ rot) << 4)) =
-            make_uint4(pk[4 * qd], pk[4 * qd + 1], pk[4 * qd + 2], pk[4 * qd + 3]);
-      }
-    }
+    row_bf16_to_f16(qrow, rot, pow2i(-eq));  // S is done: Q -> fp16 for the node MMAs
     ptx::fence_proxy_async_smem();
   }
   ptx::tc_fence_before();
   __syncthreads();
-  // O = P V (M = 128, N = 64, K = 128 keys): P K-major, V MN-major, fp16.
-  if (ok && tid == 0) {
-    ptx::tc_fence_after();
-    const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
-    const uint32_t p0 = ptx::smem_u32(RK), v0 = ptx::smem_u32(RV);
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk) {
-      const uint32_t offp = (kk >> 2) * 16384 + (kk & 3) * 32;
-      ptx::umma_f16(tO, ptx::smem_desc_sw128(p0 + offp, 16, 1024),
-                    ptx::smem_desc_sw128(v0 + kk * 2048, 1024, 1024), idesc, kk > 0);
-    }
-    ptx::umma_commit(&bar_o);
-  }
 
-  // inter-tile levels, nearest first: Y = Q · Node (fp16, Node MN-major), rows weighted by
-  // lambda_t^(8+m) 2^(g_t + D) and the two scales.
-  float acc[kDv];
+  if (!role_b) {
+    // ---- role a: P row t = r in fp16 with row scale 2^-ep, over K; then O = P V -------
+    int ep = 0;
+    if (ok) {
+      ptx::tc_fence_after();
+      const int t = r;
+      float smax = 0.f;
+#pragma unroll 1
+      for (int cg = 0; cg <= quad; ++cg) {  // warp-uniform bound: tcgen05.ld is collective
+        float sv[32];
+        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+        ptx::tmem_ld_wait();
 #pragma unroll
-  for (int j = 0; j < kDv; ++j) acc[j] = 0.f;
-  float D = 0.f;
-  int it = 0;
-  for (int m = mlow; ok && m >= 0 && m < 31 && (u >> m) > 0; ++m) {
-    if (!((u >> m) & 1)) continue;
-    const size_t node = nbase + p.node_off[m] + ((u >> m) - 1);
-    if (tid == 0) {
-      bool okw = wait_bar(&bar_e, it & 1);
-      if (okw) {
-        ptx::tc_fence_after();
-        const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
-        const uint32_t q0 = ptx::smem_u32(RQ), e0 = ptx::smem_u32(RE);
+        for (int j = 0; j < 32; ++j)
+          if (cg * 32 + j <= t) smax = fmaxf(smax, fabsf(sv[j]));
+      }
+      ep = f16_exp(smax * lmax);  // |P| <= max|S| * max lambda (decays are <= 1)
+      sEp[t] = ep;
+      const float coef = pow2i(-ep);
+#pragma unroll 1
+      for (int cg = 0; cg < 4; ++cg) {
+        uint32_t pk[16];
+        if (cg < quad) {
+          // keys of an earlier 32-group: one level (6 or 7) and a factored decay
+          float sv[32];
+          ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+          ptx::tmem_ld_wait();
+          const int l = 5 + (32 - __clz(quad ^ cg));
+          const float cA = coef * (l == 6 ? lam8[6] : lam8[7]) * exp2f(gt - sG[cg * 32 + 31]);
 #pragma unroll
-        for (int kk = 0; kk < kDk / 16; ++kk) {
-          const uint32_t offq = (kk >> 2) * 16384 + (kk & 3) * 32;
-          ptx::umma_f16(tY, ptx::smem_desc_sw128(q0 + offq, 16, 1024),
-                        ptx::smem_desc_sw128(e0 + kk * 2048, 1024, 1024), idesc, kk > 0);
+          for (int j = 0; j < 32; j += 2)
+            pk[j >> 1] = pack_h2(sv[j] * cA * sB[cg * 32 + j], sv[j + 1] * cA * sB[cg * 32 + j + 1]);
+        } else if (cg == quad) {
+          // the diagonal 32-group: levels 0..5 and the decay per key
+          float sv[32];
+          ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float v[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int s = cg * 32 + j + q;
+              float val = 0.f;
+              if (s <= t) {
+                const int l = (s == t) ? 0 : 32 - __clz(t ^ s);
+                float lv = lam8[0];
+                lv = (l == 1) ? lam8[1] : lv;
+                lv = (l == 2) ? lam8[2] : lv;
+                lv = (l == 3) ? lam8[3] : lv;
+                lv = (l == 4) ? lam8[4] : lv;
+                lv = (l == 5) ? lam8[5] : lv;
+                val = sv[j + q] * coef * lv * exp2f(gt - sG[s]);
+              }
+              v[q] = val;
+            }
+            pk[j >> 1] = pack_h2(v[0], v[1]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = 0u;
         }
-        ptx::umma_commit(&bar_y);
-        okw = wait_bar(&bar_y, it & 1);
+        // 4 chunks of 8 keys: key block cg / 2, chunk index (cg % 2) * 4 + qd
+        uint8_t* prow = RK + (cg >> 1) * 16384 + t * 128;
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+          const int c = (cg & 1) * 4 + qd;
+          *reinterpret_cast<uint4*>(prow + ((c ^ rot) << 4)) =
+              make_uint4(pk[4 * qd], pk[4 * qd + 1], pk[4 * qd + 2], pk[4 * qd + 3]);
+        }
       }
-      if (!okw) atomicExch(p.status, kStatusTimeout);
-      // next level's image (the MMA reading RE has completed)
-      int mn = m + 1;
-      while (mn < 31 && (u >> mn) > 0 && !((u >> mn) & 1)) ++mn;
-      if (okw && mn < 31 && (u >> mn) > 0) {
-        const size_t nn = nbase + p.node_off[mn] + ((u >> mn) - 1);
-        ptx::mbar_arrive_expect_tx(&bar_e, kImgBytes);
-        ptx::bulk_load(RE, p.img + nn * kImgBytes, kImgBytes, &bar_e);
-      }
-      s_ok = okw ? 1 : 0;
+      ptx::fence_proxy_async_smem();
     }
-    __syncthreads();
-    ok = s_ok != 0;
-    if (!ok) break;
-    ptx::tc_fence_after();
-    const int en = (int)p.meta[node * kMeta + 1];
-    const float wy = lrow[kLevIntra + m] * exp2f(gt + D) * pow2s(eq + en);
-    float y[32];
-    ptx::tmem_ld32(tY + lane_off, y);
-    ptx::tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] += wy * y[j];
-    ptx::tmem_ld32(tY + lane_off + 32, y);
-    ptx::tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc[32 + j] += wy * y[j];
-    D += __uint_as_float(p.meta[node * kMeta + 2]);
-    ++it;
     ptx::tc_fence_before();
-    __syncthreads();  // Y is rewritten by the next level's MMA
-  }
-  if (ok) {
-    ok = wait_bar(&bar_o, 0);
-    if (!ok) atomicExch(p.status, kStatusTimeout);
-  }
-  ok = __syncthreads_and(ok);
-  if (ok) {
-    ptx::tc_fence_after();
-    const float so = pow2s(ep + ev);
-    __nv_bfloat16* orow = p.o + (row * p.H + h) * kDv;
+    ptx::named_bar_sync(1, 128);
+    // O = P V (M = 128, N = 64, K = 128 keys): P K-major, V MN-major, fp16.
+    if (ok && tid == 0) {
+      ptx::tc_fence_after();
+      const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
+      const uint32_t p0 = ptx::smem_u32(RK), v0 = ptx::smem_u32(RV);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const uint32_t offp = (kk >> 2) * 16384 + (kk & 3) * 32;
+        ptx::umma_f16(tO, ptx::smem_desc_sw128(p0 + offp, 16, 1024),
+                      ptx::smem_desc_sw128(v0 + kk * 2048, 1024, 1024), idesc, kk > 0);
+      }
+      ptx::umma_commit(&bar_o);
+    }
+    __syncthreads();  // join (role b waits here after its levels)
+  } else {
+    // ---- role b: inter-tile levels, nearest first: Y = Q · Node (fp16, Node MN-major),
+    // rows weighted by lambda_t^(8+m) 2^(g_t + D) and the two scales ----------------------
+    float acc[kDv];
+#pragma unroll
+    for (int j = 0; j < kDv; ++j) acc[j] = 0.f;
+    float D = 0.f;
+    int it = 0;
+    const bool driver = tid == 128;
+    for (int m = mlow; ok && m >= 0 && m < 31 && (u >> m) > 0; ++m) {
+      if (!((u >> m) & 1)) continue;
+      const size_t node = nbase + p.node_off[m] + ((u >> m) - 1);
+      if (driver) {
+        bool okw = wait_bar(&bar_e, it & 1);
+        if (okw) {
+          ptx::tc_fence_after();
+          const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
+          const uint32_t q0 = ptx::smem_u32(RQ), e0 = ptx::smem_u32(RE);
+#pragma unroll
+          for (int kk = 0; kk < kDk / 16; ++kk) {
+            const uint32_t offq = (kk >> 2) * 16384 + (kk & 3) * 32;
+            ptx::umma_f16(tY, ptx::smem_desc_sw128(q0 + offq, 16, 1024),
+                          ptx::smem_desc_sw128(e0 + kk * 2048, 1024, 1024), idesc, kk > 0);
+          }
+          ptx::umma_commit(&bar_y);
+          okw = wait_bar(&bar_y, it & 1);
+        }
+        if (!okw) atomicExch(p.status, kStatusTimeout);
+        // next level's image (the MMA reading RE has completed)
+        int mn = m + 1;
+        while (mn < 31 && (u >> mn) > 0 && !((u >> mn) & 1)) ++mn;
+        if (okw && mn < 31 && (u >> mn) > 0) {
+          const size_t nn = nbase + p.node_off[mn] + ((u >> mn) - 1);
+          ptx::mbar_arrive_expect_tx(&bar_e, kImgBytes);
+          ptx::bulk_load(RE, p.img + nn * kImgBytes, kImgBytes, &bar_e);
+        }
+        s_ok = okw ? 1 : 0;
+      }
+      ptx::named_bar_sync(2, 128);
+      ok = s_ok != 0;
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int en = (int)p.meta[node * kMeta + 1];
+      const float wy = lrow[kLevIntra + m] * exp2f(gt + D) * pow2s(eq + en);
       float y[32];
-      ptx::tmem_ld32(tO + lane_off + half * 32, y);
+      ptx::tmem_ld32(tY + lane_off, y);
       ptx::tmem_ld_wait();
-      uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2)
-        pk[j >> 1] = pack_bf16(y[j] * so + acc[half * 32 + j], y[j + 1] * so + acc[half * 32 + j + 1]);
-      uint4* dst = reinterpret_cast<uint4*>(orow + half * 32);
+      for (int j = 0; j < 32; ++j) acc[j] += wy * y[j];
+      ptx::tmem_ld32(tY + lane_off + 32, y);
+      ptx::tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int j = 0; j < 32; ++j) acc[32 + j] += wy * y[j];
+      D += __uint_as_float(p.meta[node * kMeta + 2]);
+      ++it;
+      ptx::tc_fence_before();
+      ptx::named_bar_sync(2, 128);  // Y is rewritten by the next level's MMA
+    }
+    __syncthreads();  // join: P, its row scales and the O MMA have been issued
+    if (ok) {
+      ok = wait_bar(&bar_o, 0);
+      if (!ok) atomicExch(p.status, kStatusTimeout);
+    }
+    if (ok) {
+      ptx::tc_fence_after();
+      const float so = pow2s(sEp[r] + ev);
+      __nv_bfloat16* orow = p.o + (row * p.H + h) * kDv;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float y[32];
+        ptx::tmem_ld32(tO + lane_off + half * 32, y);
+        ptx::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2)
+          pk[j >> 1] = pack_bf16(y[j] * so + acc[half * 32 + j], y[j + 1] * so + acc[half * 32 + j + 1]);
+        uint4* dst = reinterpret_cast<uint4*>(orow + half * 32);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
     }
   }
   ptx::tc_fence_before();
@@ -718,7 +763,7 @@ bool make_map(CUtensorMap* m, const void* base, int inner, int count, int T, int
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int kSmemState = 32768 + 32768 + 1024;
-constexpr int kSmemOutput = 98816 + 512 + 1024;
+constexpr int kSmemOutput = 99328 + 512 + 1024;
 
 }  // namespace
 
@@ -790,7 +835,7 @@ cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   note_launch(a, 0, st);
   e = cudaFuncSetAttribute(tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
   if (e != cudaSuccess) return e;
-  tc_output_kernel<<<grid, 128, kSmemOutput, st>>>(mQ, mK, mV, p);
+  tc_output_kernel<<<grid, 256, kSmemOutput, st>>>(mQ, mK, mV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch(a, 1, st);
   if (a.states_out) {
