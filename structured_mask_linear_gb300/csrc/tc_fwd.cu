@@ -15,8 +15,9 @@
 //             are published as fp16 images in the UMMA operand layout with a power-of-two
 //             scale and their total log2 decay.
 //  tc_output  one CTA per (b, h, tile u): S = Q Kᵀ on the tensor cores; P = S ⊙ lambda^l
-//             ⊙ 2^(g_t - g_s) ⊙ [s <= t] (levels 0..7) written to shared memory as fp16 with
-//             a power-of-two row scale; O = P V; then for every set bit m of u one more MMA
+//             ⊙ 2^(g_t - g_s) ⊙ [s <= t] (levels 0..7) written to tensor memory as fp16
+//             with a power-of-two row scale; O = P V with P as the tensor-memory operand;
+//             then for every set bit m of u one more MMA
 //             Y = Q · Node_m[(u >> m) - 1], its rows added with weight
 //             lambda_t^(8+m) 2^(g_t + D_m), D_m the decay of the nearer buckets (write-up
 //             section 特殊结构：树划分: one memory per bucket level); one write of o.
@@ -64,6 +65,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
+#pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (ptx::mbar_try_wait(bar, parity)) return true;
     if (ptx::globaltimer_ns() - t0 > kWaitNs) return false;
@@ -131,40 +133,6 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Max |x| over the 8 bf16 chunks (128 bytes) of one shared-memory row.  Threads visit
-// the chunks in the order c ^ (row & 7) so that a warp's accesses spread over the banks.
-__device__ __forceinline__ float row_absmax_bf16(const uint8_t* row, int rot) {
-  float m = 0.f;
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint4 x = *reinterpret_cast<const uint4*>(row + ((c ^ rot) << 4));
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float2 f = __bfloat1622float2(h[e]);
-      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-    }
-  }
-  return m;
-}
-
-// In place: one 128-byte row of bf16 -> fp16, each value times s (same chunk slots).
-__device__ __forceinline__ void row_bf16_to_f16(uint8_t* row, int rot, float s) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint4* q = reinterpret_cast<uint4*>(row + ((c ^ rot) << 4));
-    uint4 x = *q, y;
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
-    __half2* o = reinterpret_cast<__half2*>(&y);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float2 f = __bfloat1622float2(h[e]);
-      o[e] = __floats2half2_rn(f.x * s, f.y * s);
-    }
-    *q = y;
-  }
 }
 
 // ---------------------------------------------------------------------------------
@@ -355,13 +323,59 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
 // ---------------------------------------------------------------------------------
 // tc_output: intra-tile masked attention + level-fused inter-tile buckets.
 //
-// 256 threads in two roles after a common prologue: warps 0-3 form P (row = thread) and
-// issue O = P V; warps 4-7 run the inter-tile levels at the same time and finally write
-// o.  Both roles see every TMEM lane through warp % 4.
-// Shared memory (2 CTAs per SM): RQ = Q (bf16, then fp16 in place after S); RK = K
-// (bf16), then P (fp16); RV = V (bf16, then fp16 in place); RE = one node image.
-// TMEM (256 columns): S in 0..127, O in 128..191, Y in 192..255.
+// 256 threads in two roles after a common prologue (loads, decay cumsum):
+//  role a (warps 0-3): V tile scale and V -> fp16 in place; P row t = thread, written as
+//          fp16 into tensor memory over the columns of S it has consumed; O = P V with P
+//          as the tensor-memory A operand.
+//  role b (warps 4-7): issues S = Q Kᵀ; Q row t -> fp16 with a power-of-two scale of its
+//          own (undone in the row weight) in place once S has read Q; the inter-tile
+//          levels, nearest first, with up to three node images in flight and two Y
+//          accumulators, so that the MMA of one level overlaps the read-out of the last;
+//          then the write of o.
+// Both roles see every TMEM lane through warp % 4.
+// Shared memory (2 CTAs per SM): RQ = Q (bf16, then fp16 in place); RK = K (bf16) until
+// S completes, then node image buffers 1 and 2; RV = V (bf16, then fp16 in place);
+// RE = node image buffer 0.  The image of level index i (i-th set bit of u from the
+// bottom) goes to buffer i % 3, completing phase (i / 3) & 1 of bar_e[i % 3].
+// lambda rows and the node scalars are copied into shared memory at the start
+// (asynchronously), so that no global load sits on the path of P or of a level.
+// TMEM (256 columns): S in 0..127; once role a has consumed S, P in 0..63 and O in
+// 64..127; Y0 in 192..255 and Y1 in 128..191 (free from the start).
 // ---------------------------------------------------------------------------------
+constexpr int kOutFixed = 104704;  // shared bytes in front of the inter-level lambda table
+constexpr int kMaxInter = 19;      // inter-tile levels per tile supported (NT <= 2^19)
+__host__ __device__ constexpr int out_smem_bytes(int ninter) {
+  return kOutFixed + 512 * (ninter > 0 ? ninter : 1) + 1024;
+}
+
+__device__ __forceinline__ int nth_set_bit(unsigned x, int i) {
+  for (int j = 0; j < i; ++j) x &= x - 1;
+  return __ffs(x) - 1;
+}
+// |.|-max of two bf16 pairs, halfwise (the sign of the result is meaningless)
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t w) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(acc), "r"(w));
+  return d;
+}
+__device__ __forceinline__ float bf16x2_maxhalf(uint32_t w) {
+  return fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xffff0000u)));
+}
+__device__ __forceinline__ uint32_t absmax_u4(uint32_t acc, const uint4& x) {
+  return bf16x2_absmax(bf16x2_absmax(acc, x.x), bf16x2_absmax(x.y, bf16x2_absmax(x.z, x.w)));
+}
+// bf16 pair -> fp16 pair, both times s2 (an exact power of two, so the bf16 product is exact)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, __nv_bfloat162 s2) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&w);
+  x = __hmul2(x, s2);
+  const uint32_t y = *reinterpret_cast<uint32_t*>(&x);
+  return pack_h2(__uint_as_float(y << 16), __uint_as_float(y & 0xffff0000u));
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& x, __nv_bfloat162 s2) {
+  return make_uint4(bf16x2_to_f16x2(x.x, s2), bf16x2_to_f16x2(x.y, s2), bf16x2_to_f16x2(x.z, s2),
+                    bf16x2_to_f16x2(x.w, s2));
+}
+
 __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                            const __grid_constant__ CUtensorMap mapK,
                                                            const __grid_constant__ CUtensorMap mapV,
@@ -372,19 +386,22 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   uint8_t* RK = smem + 32768;   // 32 KB
   uint8_t* RV = smem + 65536;   // 16 KB
   uint8_t* RE = smem + 81920;   // 16 KB
-  float* sG = reinterpret_cast<float*>(smem + 98304);  // 128 floats: g
-  float* sB = reinterpret_cast<float*>(smem + 98816);  // 128 floats: 2^(g_end(group) - g_s)
-  int* sEp = reinterpret_cast<int*>(smem + 99328);     // 128 ints: P row scale exponents
-  __shared__ __align__(8) uint64_t bar_ld, bar_s, bar_o, bar_e, bar_y;
+  float* sG = reinterpret_cast<float*>(smem + 98304);      // 128: g
+  float* sB8 = reinterpret_cast<float*>(smem + 98816);     // 128: 2^(g_end8(s) - g_s)
+  int* sEp = reinterpret_cast<int*>(smem + 99328);         // 128: P row + V scale exponents
+  float* sLam8 = reinterpret_cast<float*>(smem + 99840);   // 128 x 9: lambda levels 0..7 of row r
+  float* sNode = reinterpret_cast<float*>(smem + 104448);  // 32 x 2: node scale exp. (bits), log2 decay
+  float* sLamI = reinterpret_cast<float*>(smem + kOutFixed);  // [level index][row]: lambda_t^(8+m)
+  __shared__ __align__(8) uint64_t bar_ld, bar_s, bar_o, bar_e[3], bar_y[2], bar_yf[2];
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[8];
-  __shared__ float2 s_red2[8];
-  __shared__ int s_ok;
+  __shared__ int s_oi;  // role a -> all: the O MMA was issued
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = tid & 127;             // query row (tile-local token)
   const int quad = warp & 3;           // TMEM lane quadrant of this warp
-  const bool role_b = warp >= 4;       // inter-tile levels and the final write
+  const bool role_b = warp >= 4;       // S, inter-tile levels and the final write
+  const bool driver = tid == 128;      // role b's MMA and image-load issuer
   const int rot = r & 7;
   const int lin = blockIdx.x;
   const int h = lin % p.H;
@@ -396,18 +413,23 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   const size_t nbase = (size_t)bh * p.nnodes;
   const size_t row = (size_t)b * p.T + t0 + r;  // token of this thread's query row
   const float* lrow = p.lam + (row * p.H + h) * p.L;
-  const float la = log2f(p.a[row * p.H + h]);
-  float lam8[kLevIntra];
-#pragma unroll
-  for (int l = 0; l < kLevIntra; ++l) lam8[l] = lrow[l];
+  const int nlev = __popc((unsigned)u);         // inter-tile levels of this tile
+  auto ebuf = [&](int k) { return k == 0 ? RE : RK + (k - 1) * 16384; };  // image buffer k
+  auto node_of = [&](int i) {                   // node read by level index i
+    const int m = nth_set_bit((unsigned)u, i);
+    return nbase + p.node_off[m] + ((u >> m) - 1);
+  };
 
-  const int mlow = (u == 0) ? -1 : __ffs(u) - 1;  // nearest inter-tile level, if any
   if (tid == 0) {
+    s_oi = 0;
     ptx::mbar_init(&bar_ld, 1);
     ptx::mbar_init(&bar_s, 1);
     ptx::mbar_init(&bar_o, 1);
-    ptx::mbar_init(&bar_e, 1);
-    ptx::mbar_init(&bar_y, 1);
+    for (int i = 0; i < 3; ++i) ptx::mbar_init(&bar_e[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bar_y[i], 1);
+      ptx::mbar_init(&bar_yf[i], 128);
+    }
     ptx::fence_mbar_init();
     ptx::mbar_arrive_expect_tx(&bar_ld, 32768 * 2 + 16384);
     ptx::tma_load_4d(RQ, &mapQ, &bar_ld, 0, g, (int)t0, b);
@@ -415,18 +437,35 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
     ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
     ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
-    if (mlow >= 0) {
-      const size_t node = nbase + p.node_off[mlow] + ((u >> mlow) - 1);
-      ptx::mbar_arrive_expect_tx(&bar_e, kImgBytes);
-      ptx::bulk_load(RE, p.img + node * kImgBytes, kImgBytes, &bar_e);
+    if (nlev > 0) {
+      ptx::mbar_arrive_expect_tx(&bar_e[0], kImgBytes);
+      ptx::bulk_load(RE, p.img + node_of(0) * kImgBytes, kImgBytes, &bar_e[0]);
     }
   }
   if (warp == 0) {
     ptx::tmem_alloc(&tmem_base, 256);
     ptx::tmem_relinquish();
   }
+  // lambda of this row (levels 0..7 for role a, the tile's inter levels for role b) and
+  // the node scalars of the tile's levels, copied asynchronously
+  if (!role_b) {
+#pragma unroll
+    for (int l = 0; l < kLevIntra; ++l) ptx::cp_async4(sLam8 + r * 9 + l, lrow + l);
+  } else {
+    unsigned rest = (unsigned)u;
+    for (int i = 0; rest; ++i) {
+      const int m = __ffs(rest) - 1;
+      rest &= rest - 1;
+      ptx::cp_async4(sLamI + i * 128 + r, lrow + kLevIntra + m);
+    }
+    if (r < nlev) {
+      const size_t node = node_of(r);
+      ptx::cp_async4(sNode + 2 * r, p.meta + node * kMeta + 1);
+      ptx::cp_async4(sNode + 2 * r + 1, p.meta + node * kMeta + 2);
+    }
+  }
   // chunk-local log2 decay cumsum over the 128 rows (both roles compute it)
-  float gt = la;
+  float gt = log2f(p.a[row * p.H + h]);
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const float y = __shfl_up_sync(0xffffffffu, gt, off);
@@ -438,20 +477,17 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   ptx::tc_fence_after();
   for (int w = 0; w < quad; ++w) gt += s_red[w];
   const uint32_t tbase = tmem_base;
-  const uint32_t tS = tbase, tO = tbase + 128, tY = tbase + 192;
+  const uint32_t tS = tbase, tO = tbase + 64;
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   if (!role_b) sG[r] = gt;
-  float lmax = 0.f;
-#pragma unroll
-  for (int l = 0; l < kLevIntra; ++l) lmax = fmaxf(lmax, fabsf(lam8[l]));
-  __syncthreads();
-  if (!role_b) sB[r] = exp2f(sG[r | 31] - gt);  // decay from key r to the end of its 32-group
+  __syncthreads();  // sG complete; s_red free again
+  if (!role_b) sB8[r] = exp2f(sG[r | 7] - gt);  // decay from key r to the end of its 8-block
   bool ok = wait_bar(&bar_ld, 0);
   if (!ok) atomicExch(p.status, kStatusTimeout);
   ok = __syncthreads_and(ok);
 
   // S = Q Kᵀ (M = 128 queries, N = 128 keys, K = 128 d_k), bf16, both K-major.
-  if (ok && tid == 0) {
+  if (ok && driver) {
     ptx::tc_fence_after();
     const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 0);
     const uint32_t q0 = ptx::smem_u32(RQ), k0 = ptx::smem_u32(RK);
@@ -463,207 +499,274 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     }
     ptx::umma_commit(&bar_s);
   }
-  // tile scales of Q and V (reading bf16 while the MMA reads Q is fine); V -> fp16 now.
-  // Q: role a takes d_k block 0 of its row, role b block 1; V: each takes half the chunks.
-  uint8_t* qrow = RQ + (role_b ? 16384 : 0) + r * 128;
-  uint8_t* vrow = RV + r * 128;
-  const int vc0 = role_b ? 4 : 0;
-  int eq = 0, ev = 0;
-  if (ok) {
-    float2 m2 = make_float2(row_absmax_bf16(qrow, rot), 0.f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 x = *reinterpret_cast<const uint4*>(vrow + (((vc0 + i) ^ rot) << 4));
-      const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float2 f = __bfloat1622float2(hx[e]);
-        m2.y = fmaxf(m2.y, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
-    }
-    m2 = block_max2(m2, s_red2);
-    eq = f16_exp(m2.x);
-    ev = f16_exp(m2.y);
-    const float sv_ = pow2i(-ev);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4* qv = reinterpret_cast<uint4*>(vrow + (((vc0 + i) ^ rot) << 4));
-      uint4 x = *qv, y;
-      const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&x);
-      __half2* hy = reinterpret_cast<__half2*>(&y);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float2 f = __bfloat1622float2(hx[e]);
-        hy[e] = __floats2half2_rn(f.x * sv_, f.y * sv_);
-      }
-      *qv = y;
-    }
-    ok = wait_bar(&bar_s, 0);
-    if (!ok) atomicExch(p.status, kStatusTimeout);
-  }
-  ok = __syncthreads_and(ok);
-  if (ok) {
-    row_bf16_to_f16(qrow, rot, pow2i(-eq));  // S is done: Q -> fp16 for the node MMAs
-    ptx::fence_proxy_async_smem();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
+  const bool s_issued = ok;
 
   if (!role_b) {
-    // ---- role a: P row t = r in fp16 with row scale 2^-ep, over K; then O = P V -------
-    int ep = 0;
+    // ---- role a -----------------------------------------------------------------------
+    // V tile scale (V is not an operand of S) and V -> fp16 in place.
+    uint8_t* vrow = RV + r * 128;
+    uint4 vv[8];
+    int ev = 0;
+    if (ok) {
+      uint32_t mx = 0u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        vv[c] = *reinterpret_cast<const uint4*>(vrow + ((c ^ rot) << 4));
+        mx = absmax_u4(mx, vv[c]);
+      }
+      float mv = bf16x2_maxhalf(mx);
+#pragma unroll
+      for (int off = 16; off; off >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+      if (lane == 0) s_red[warp] = mv;
+    }
+    ptx::named_bar_sync(1, 128);
+    if (ok) {
+      ev = f16_exp(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
+      const float sv_ = pow2i(-ev);
+      const __nv_bfloat162 s2 = __floats2bfloat162_rn(sv_, sv_);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(vrow + ((c ^ rot) << 4)) = bf16x8_to_f16x8(vv[c], s2);
+      ptx::fence_proxy_async_smem();
+      ok = wait_bar(&bar_s, 0);
+      if (!ok) atomicExch(p.status, kStatusTimeout);
+    }
+    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld / st below are warp-collective
+    // P row t = r in fp16 with row scale 2^-ep, into TMEM columns 0..63 over S.
     if (ok) {
       ptx::tc_fence_after();
-      const int t = r;
+      ptx::cp_async_wait_all();
+      const float* lamr = sLam8 + r * 9;
+      const int t = r, tl = t & 31;
+      float lmax = 0.f;
+#pragma unroll
+      for (int l = 0; l < kLevIntra; ++l) lmax = fmaxf(lmax, fabsf(lamr[l]));
       float smax = 0.f;
 #pragma unroll 1
-      for (int cg = 0; cg <= quad; ++cg) {  // warp-uniform bound: tcgen05.ld is collective
+      for (int cg = 0; cg < quad; ++cg) {  // warp-uniform bound
         float sv[32];
         ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (cg * 32 + j <= t) smax = fmaxf(smax, fabsf(sv[j]));
+        for (int j = 0; j < 32; ++j) smax = fmaxf(smax, fabsf(sv[j]));
       }
-      ep = f16_exp(smax * lmax);  // |P| <= max|S| * max lambda (decays are <= 1)
-      sEp[t] = ep;
+      {
+        float sv[32];
+        ptx::tmem_ld32(tS + lane_off + quad * 32, sv);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j <= tl) smax = fmaxf(smax, fabsf(sv[j]));
+      }
+      const int ep = f16_exp(smax * lmax);  // |P| <= max|S| * max lambda (decays are <= 1)
+      sEp[t] = ep + ev;
       const float coef = pow2i(-ep);
+      // Decay 2^(g_t - g_s) = A_kb B8[s], with A_kb = 2^(g_t - g_end8(kb)) per row and
+      // 8-key block kb and B8[s] = 2^(g_end8(s) - g_s) per key; both are <= 1 for keys of
+      // blocks before t's.  In t's own block A_kb >= 1, bounded by 2^(block span): when no
+      // block of the diagonal group spans more than 60 the factored form stays inside
+      // fp32's range; otherwise each key of that group takes its own exp2 (warp-uniform).
+      const float* gq = sG + quad * 32;
+      const float span8 = fmaxf(fmaxf(gq[0] - gq[7], gq[8] - gq[15]), fmaxf(gq[16] - gq[23], gq[24] - gq[31]));
+      const bool fastd = span8 <= 60.f;
+      // Keys cg*32 .. cg*32+31 become packed columns cg*16 .. cg*16+15: those columns held
+      // S of keys below cg*32, all read before (the loop runs upward).
 #pragma unroll 1
       for (int cg = 0; cg < 4; ++cg) {
         uint32_t pk[16];
         if (cg < quad) {
-          // keys of an earlier 32-group: one level (6 or 7) and a factored decay
+          // keys of an earlier 32-group: one level (6 or 7) and the factored decay
           float sv[32];
           ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
           ptx::tmem_ld_wait();
-          const int l = 5 + (32 - __clz(quad ^ cg));
-          const float cA = coef * (l == 6 ? lam8[6] : lam8[7]) * exp2f(gt - sG[cg * 32 + 31]);
+          const float cl = coef * lamr[(quad ^ cg) >= 2 ? 7 : 6];
+          float ak[4];
 #pragma unroll
-          for (int j = 0; j < 32; j += 2)
-            pk[j >> 1] = pack_h2(sv[j] * cA * sB[cg * 32 + j], sv[j + 1] * cA * sB[cg * 32 + j + 1]);
-        } else if (cg == quad) {
-          // the diagonal 32-group: levels 0..5 and the decay per key
-          float sv[32];
-          ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
-          ptx::tmem_ld_wait();
+          for (int kb = 0; kb < 4; ++kb) ak[kb] = cl * exp2f(gt - sG[cg * 32 + kb * 8 + 7]);
+          const float4* b4 = reinterpret_cast<const float4*>(sB8 + cg * 32);
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float v[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int s = cg * 32 + j + q;
-              float val = 0.f;
-              if (s <= t) {
-                const int l = (s == t) ? 0 : 32 - __clz(t ^ s);
-                float lv = lam8[0];
-                lv = (l == 1) ? lam8[1] : lv;
-                lv = (l == 2) ? lam8[2] : lv;
-                lv = (l == 3) ? lam8[3] : lv;
-                lv = (l == 4) ? lam8[4] : lv;
-                lv = (l == 5) ? lam8[5] : lv;
-                val = sv[j + q] * coef * lv * exp2f(gt - sG[s]);
-              }
-              v[q] = val;
-            }
-            pk[j >> 1] = pack_h2(v[0], v[1]);
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 bb = b4[j4];
+            const float a = ak[j4 >> 1];
+            pk[2 * j4] = pack_h2(sv[4 * j4] * a * bb.x, sv[4 * j4 + 1] * a * bb.y);
+            pk[2 * j4 + 1] = pack_h2(sv[4 * j4 + 2] * a * bb.z, sv[4 * j4 + 3] * a * bb.w);
           }
+        } else if (cg == quad) {
+          // the diagonal 32-group: levels 0..5 (level of key j: bit length of tl ^ j)
+          float sv[32];
+          ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+          ptx::tmem_ld_wait();
+          float v[32];
+          if (fastd) {
+            // blocks after t's may give A = inf; their keys are masked by the select
+            float ak[4];
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) ak[kb] = exp2f(gt - gq[kb * 8 + 7]);
+            const float4* b4 = reinterpret_cast<const float4*>(sB8 + cg * 32);
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 bb = b4[j4];
+              const float bj[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 4 * j4 + e;
+                const float x = (sv[j] * coef) * lamr[32 - __clz(tl ^ j)] * (ak[j >> 3] * bj[e]);
+                v[j] = j <= tl ? x : 0.f;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float x = sv[j] * coef * lamr[32 - __clz(tl ^ j)] * exp2f(gt - gq[j]);
+              v[j] = j <= tl ? x : 0.f;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = pack_h2(v[2 * j], v[2 * j + 1]);
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) pk[j] = 0u;
         }
-        // 4 chunks of 8 keys: key block cg / 2, chunk index (cg % 2) * 4 + qd
-        uint8_t* prow = RK + (cg >> 1) * 16384 + t * 128;
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
-          const int c = (cg & 1) * 4 + qd;
-          *reinterpret_cast<uint4*>(prow + ((c ^ rot) << 4)) =
-              make_uint4(pk[4 * qd], pk[4 * qd + 1], pk[4 * qd + 2], pk[4 * qd + 3]);
-        }
+        ptx::tmem_st16(tS + lane_off + cg * 16, pk);
       }
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_st_wait();
     }
     ptx::tc_fence_before();
-    ptx::named_bar_sync(1, 128);
-    // O = P V (M = 128, N = 64, K = 128 keys): P K-major, V MN-major, fp16.
-    if (ok && tid == 0) {
+    const bool ok_a = ptx::named_bar_and(1, 128, ok);
+    // O = P V (M = 128, N = 64, K = 128 keys): P from TMEM, V fp16 MN-major, into the
+    // S columns 64..127 that every role-a thread has finished reading.
+    if (tid == 0 && ok_a) {
       ptx::tc_fence_after();
       const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
-      const uint32_t p0 = ptx::smem_u32(RK), v0 = ptx::smem_u32(RV);
+      const uint32_t v0 = ptx::smem_u32(RV);
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint32_t offp = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::umma_f16(tO, ptx::smem_desc_sw128(p0 + offp, 16, 1024),
-                      ptx::smem_desc_sw128(v0 + kk * 2048, 1024, 1024), idesc, kk > 0);
-      }
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        ptx::umma_f16_tmem_a(tO, tS + kk * 8, ptx::smem_desc_sw128(v0 + kk * 2048, 1024, 1024),
+                             idesc, kk > 0);
       ptx::umma_commit(&bar_o);
+      s_oi = 1;
     }
     __syncthreads();  // join (role b waits here after its levels)
   } else {
-    // ---- role b: inter-tile levels, nearest first: Y = Q · Node (fp16, Node MN-major),
-    // rows weighted by lambda_t^(8+m) 2^(g_t + D) and the two scales ----------------------
+    // ---- role b -----------------------------------------------------------------------
+    // Q row r -> fp16 with scale 2^-eq of its own: read and converted while S runs,
+    // stored back once S has completed.  Then images 1 and 2 go into RK.
+    uint8_t* qrow0 = RQ + r * 128;
+    uint8_t* qrow1 = RQ + 16384 + r * 128;
+    int eq = 0;
+    int issued = nlev > 0 ? 1 : 0;  // image loads issued (level 0 by thread 0)
+    int consumed = 0;               // image loads waited for by the driver
+    int y_issued = 0, y_seen = 0;   // Y MMAs issued / seen complete by the driver
+    if (ok) {
+      uint4 qv[16];
+      uint32_t mx = 0u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        qv[c] = *reinterpret_cast<const uint4*>(qrow0 + ((c ^ rot) << 4));
+        qv[8 + c] = *reinterpret_cast<const uint4*>(qrow1 + ((c ^ rot) << 4));
+        mx = absmax_u4(absmax_u4(mx, qv[c]), qv[8 + c]);
+      }
+      eq = f16_exp(bf16x2_maxhalf(mx));
+      const float sq = pow2i(-eq);
+      const __nv_bfloat162 s2 = __floats2bfloat162_rn(sq, sq);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) qv[c] = bf16x8_to_f16x8(qv[c], s2);
+      ok = wait_bar(&bar_s, 0);
+      if (!ok) atomicExch(p.status, kStatusTimeout);
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(qrow0 + ((c ^ rot) << 4)) = qv[c];
+          *reinterpret_cast<uint4*>(qrow1 + ((c ^ rot) << 4)) = qv[8 + c];
+        }
+        ptx::fence_proxy_async_smem();
+      }
+    }
+    if (ok && driver) {
+      for (int i = 1; i < 3 && i < nlev; ++i) {  // K has been read by S: RK is free
+        ptx::mbar_arrive_expect_tx(&bar_e[i], kImgBytes);
+        ptx::bulk_load(ebuf(i), p.img + node_of(i) * kImgBytes, kImgBytes, &bar_e[i]);
+        ++issued;
+      }
+    }
+    ptx::cp_async_wait_all();
+    ok = ptx::named_bar_and(2, 128, ok);  // Q fp16 in place; sLamI, sNode complete
+
+    // Levels, nearest first: Y_i = Q · Node_i (fp16, Node MN-major) into Y buffer i & 1;
+    // its rows are added with weight lambda_t^(8+m) 2^(g_t + D) and the two scales.
+    // The driver issues level i + 1 before it reads level i.
+    auto issue_y = [&](int i) -> bool {
+      if (i >= 2 && !wait_bar(&bar_yf[i & 1], ((i - 2) >> 1) & 1)) return false;  // Y buffer read
+      if (!wait_bar(&bar_e[i % 3], (i / 3) & 1)) return false;                   // image landed
+      ++consumed;
+      ptx::tc_fence_after();
+      const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
+      const uint32_t q0 = ptx::smem_u32(RQ), e0 = ptx::smem_u32(ebuf(i % 3));
+      const uint32_t ty = tbase + ((i & 1) ? 128 : 192);
+#pragma unroll
+      for (int kk = 0; kk < kDk / 16; ++kk) {
+        const uint32_t offq = (kk >> 2) * 16384 + (kk & 3) * 32;
+        ptx::umma_f16(ty, ptx::smem_desc_sw128(q0 + offq, 16, 1024),
+                      ptx::smem_desc_sw128(e0 + kk * 2048, 1024, 1024), idesc, kk > 0);
+      }
+      ptx::umma_commit(&bar_y[i & 1]);
+      ++y_issued;
+      return true;
+    };
     float acc[kDv];
 #pragma unroll
     for (int j = 0; j < kDv; ++j) acc[j] = 0.f;
     float D = 0.f;
-    int it = 0;
-    const bool driver = tid == 128;
-    for (int m = mlow; ok && m >= 0 && m < 31 && (u >> m) > 0; ++m) {
-      if (!((u >> m) & 1)) continue;
-      const size_t node = nbase + p.node_off[m] + ((u >> m) - 1);
-      if (driver) {
-        bool okw = wait_bar(&bar_e, it & 1);
-        if (okw) {
-          ptx::tc_fence_after();
-          const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
-          const uint32_t q0 = ptx::smem_u32(RQ), e0 = ptx::smem_u32(RE);
-#pragma unroll
-          for (int kk = 0; kk < kDk / 16; ++kk) {
-            const uint32_t offq = (kk >> 2) * 16384 + (kk & 3) * 32;
-            ptx::umma_f16(tY, ptx::smem_desc_sw128(q0 + offq, 16, 1024),
-                          ptx::smem_desc_sw128(e0 + kk * 2048, 1024, 1024), idesc, kk > 0);
-          }
-          ptx::umma_commit(&bar_y);
-          okw = wait_bar(&bar_y, it & 1);
-        }
-        if (!okw) atomicExch(p.status, kStatusTimeout);
-        // next level's image (the MMA reading RE has completed)
-        int mn = m + 1;
-        while (mn < 31 && (u >> mn) > 0 && !((u >> mn) & 1)) ++mn;
-        if (okw && mn < 31 && (u >> mn) > 0) {
-          const size_t nn = nbase + p.node_off[mn] + ((u >> mn) - 1);
-          ptx::mbar_arrive_expect_tx(&bar_e, kImgBytes);
-          ptx::bulk_load(RE, p.img + nn * kImgBytes, kImgBytes, &bar_e);
-        }
-        s_ok = okw ? 1 : 0;
+    bool okd = true;
+    if (ok && driver && nlev > 0) okd = issue_y(0);
+    for (int i = 0; ok && i < nlev; ++i) {
+      if (driver && okd && i + 1 < nlev) okd = issue_y(i + 1);  // level i + 1 ahead
+      if (driver && !okd) atomicExch(p.status, kStatusTimeout);
+      bool okw = wait_bar(&bar_y[i & 1], (i >> 1) & 1);
+      if (!okw) atomicExch(p.status, kStatusTimeout);
+      okw = __all_sync(0xffffffffu, okw);
+      if (!okw) {
+        ok = false;
+        break;
       }
-      ptx::named_bar_sync(2, 128);
-      ok = s_ok != 0;
-      if (!ok) break;
+      if (driver) {
+        ++y_seen;
+        if (i + 3 < nlev) {  // the image buffer of level i is free again
+          ptx::mbar_arrive_expect_tx(&bar_e[i % 3], kImgBytes);
+          ptx::bulk_load(ebuf(i % 3), p.img + node_of(i + 3) * kImgBytes, kImgBytes, &bar_e[i % 3]);
+          ++issued;
+        }
+      }
       ptx::tc_fence_after();
-      const int en = (int)p.meta[node * kMeta + 1];
-      const float wy = lrow[kLevIntra + m] * exp2f(gt + D) * pow2s(eq + en);
+      const uint32_t ty = tbase + ((i & 1) ? 128 : 192) + lane_off;
+      const float wy = sLamI[i * 128 + r] * exp2f(gt + D) * pow2s(eq + __float_as_int(sNode[2 * i]));
       float y[32];
-      ptx::tmem_ld32(tY + lane_off, y);
+      ptx::tmem_ld32(ty, y);
       ptx::tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 32; ++j) acc[j] += wy * y[j];
-      ptx::tmem_ld32(tY + lane_off + 32, y);
+      ptx::tmem_ld32(ty + 32, y);
       ptx::tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 32; ++j) acc[32 + j] += wy * y[j];
-      D += __uint_as_float(p.meta[node * kMeta + 2]);
-      ++it;
+      D += sNode[2 * i + 1];
       ptx::tc_fence_before();
-      ptx::named_bar_sync(2, 128);  // Y is rewritten by the next level's MMA
+      ptx::mbar_arrive(&bar_yf[i & 1]);
+    }
+    if (driver) {
+      // after a failed wait: let this CTA's own copies and MMAs land (bounded) before exit
+      for (int j = consumed; j < issued; ++j) wait_bar(&bar_e[j % 3], (j / 3) & 1);
+      for (int j = y_seen; j < y_issued; ++j) wait_bar(&bar_y[j & 1], (j >> 1) & 1);
+      if (s_issued) wait_bar(&bar_s, 0);
     }
     __syncthreads();  // join: P, its row scales and the O MMA have been issued
-    if (ok) {
-      ok = wait_bar(&bar_o, 0);
-      if (!ok) atomicExch(p.status, kStatusTimeout);
-    }
+    const bool o_issued = s_oi != 0;
+    ok = ok && o_issued && wait_bar(&bar_o, 0);
+    if (!ok && o_issued) atomicExch(p.status, kStatusTimeout);
+    ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       ptx::tc_fence_after();
-      const float so = pow2s(sEp[r] + ev);
+      const float so = pow2s(sEp[r]);
       __nv_bfloat16* orow = p.o + (row * p.H + h) * kDv;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -679,6 +782,11 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       }
     }
+  }
+  if (tid == 0) {
+    // bounded: return at once when complete; otherwise let them land before TMEM goes
+    wait_bar(&bar_ld, 0);
+    if (s_oi) wait_bar(&bar_o, 0);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -763,13 +871,12 @@ bool make_map(CUtensorMap* m, const void* base, int inner, int count, int T, int
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int kSmemState = 32768 + 32768 + 1024;
-constexpr int kSmemOutput = 99328 + 512 + 1024;
 
 }  // namespace
 
 bool tc_supported(const ll_shape& s) {
   return s.dtype == LL_BF16 && s.d_k == kDk && s.d_v == kDv && s.T % kTile == 0 &&
-         s.levels <= 32 && encode_fn() != nullptr;
+         s.levels <= 32 && bit_length(s.T / kTile - 1) <= kMaxInter && encode_fn() != nullptr;
 }
 
 const char* tc_kernel_names(bool with_export) {
@@ -833,9 +940,10 @@ cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   tc_state_kernel<<<grid, 128, kSmemState, st>>>(mK, mV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch(a, 0, st);
-  e = cudaFuncSetAttribute(tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
+  const int smem_out = out_smem_bytes(bit_length(tp.NT - 1));
+  e = cudaFuncSetAttribute(tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_out);
   if (e != cudaSuccess) return e;
-  tc_output_kernel<<<grid, 256, kSmemOutput, st>>>(mQ, mK, mV, p);
+  tc_output_kernel<<<grid, 256, smem_out, st>>>(mQ, mK, mV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch(a, 1, st);
   if (a.states_out) {
