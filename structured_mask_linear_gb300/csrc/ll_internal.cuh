@@ -71,7 +71,7 @@ struct TcPlan {
   int node_off[32]; // first node of tile level m
   int MT;           // tile levels (bit_length(NT))
   size_t off_img;   // fp16 node images, 16 KB each
-  size_t off_meta;  // per node: arrivals, scale exponent, log2 decay, spare
+  size_t off_meta;  // per node: spare, scale exponent, log2 decay, spare
   size_t meta_bytes, bytes;
 };
 

@@ -54,8 +54,8 @@ extern "C" ll_status loglinear_fwd_static_workspace(const ll_shape* shape, const
   void* ws = nullptr;
   ll_status st = static_workspace(&ws);
   if (st != LL_OK) return st;
-  // loglinear_fwd clears, on the stream, every part of the workspace that must start at
-  // zero (the tree's arrival counters); everything else is written before it is read.
+  // Nothing in the workspace needs to start at zero: every word is written before it is
+  // read within one call.
   return loglinear_fwd(shape, q, k, v, a, lambda, o, ws, (size_t)LOGLINEAR_STATIC_WORKSPACE_BYTES,
                        states_out, state_logscale_out, state_levels, stream);
 }

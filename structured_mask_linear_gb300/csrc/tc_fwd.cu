@@ -8,12 +8,11 @@
 //
 //  tc_state   one CTA per (b, h, tile u): chunk-local log2 decay cumsum g, tile decay
 //             gamma_u, tile state H_u = K_uᵀ diag(2^(gamma_u - g)) V_u on the tensor
-//             cores (M = d_k, N = d_v, K = tokens).  Then the Fenwick tree over tiles is
-//             built without any waiting: the CTA publishes its node and climbs while it
-//             is the second of two siblings to arrive (one atomic counter per parent),
-//             merging Node_{m+1}[i] = 2^(Gamma(right)) Node_m[2i] + Node_m[2i+1].  Nodes
-//             are published as fp16 images in the UMMA operand layout with a power-of-two
-//             scale and their total log2 decay.
+//             cores (M = d_k, N = d_v, K = tokens), published as node (0, u) of the
+//             Fenwick tree over tiles.  Nodes are fp16 images in the UMMA operand layout
+//             with a power-of-two scale and their total log2 decay.
+//  tc_tree    two tree levels per launch, Node_{m+1}[i] = 2^(Gamma(right)) Node_m[2i] +
+//             Node_m[2i+1], from the images of the level below (no CTA waits for another).
 //  tc_output  one CTA per (b, h, tile u): S = Q Kᵀ on the tensor cores; P = S ⊙ lambda^l
 //             ⊙ 2^(g_t - g_s) ⊙ [s <= t] (levels 0..7) written to tensor memory as fp16
 //             with a power-of-two row scale; O = P V with P as the tensor-memory operand;
@@ -48,7 +47,7 @@ constexpr int kDk = 128, kDv = 64;            // supported head dims
 constexpr int kLevIntra = 8;                  // levels 0..7 live inside a 128-token tile
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
 constexpr int kImgBytes = kDk * kDv * 2;      // fp16 node image, 128 rows x 128 bytes
-constexpr int kMeta = 4;  // u32 per node: arrivals, scale exponent, log2 decay (f32 bits), spare
+constexpr int kMeta = 4;  // u32 per node: spare, scale exponent, log2 decay (f32 bits), spare
 
 struct TcParams {
   int B, T, H, hpg, G, L, NT, nnodes, MT;
@@ -135,8 +134,39 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Publishes one tree node from 128 threads, thread tid holding row tid (d_k index) of the
+// d_k x d_v fp32 state in cur: an fp16 image with a power-of-two scale 2^e (maximum in
+// [2^14, 2^15)), row tid at chunk slots c ^ (tid & 7), staged through `stage` (16 KB of
+// shared memory whose row tid only this thread uses before the call) so that the global
+// stores coalesce; then the scale exponent and the node's log2 decay G into meta.
+__device__ __forceinline__ void publish_node(const float (&cur)[kDv], uint8_t* stage, size_t node,
+                                             float G, float2* s_red2, const TcParams& p) {
+  const int tid = threadIdx.x, rot = tid & 7;
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < kDv; ++j) m = fmaxf(m, fabsf(cur[j]));
+  const int e = f16_exp(block_max2(make_float2(m, 0.f), s_red2).x);
+  const float s = pow2i(-e);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int cc = c ^ rot;
+    *reinterpret_cast<uint4*>(stage + tid * 128 + (cc << 4)) =
+        make_uint4(pack_h2(cur[8 * c] * s, cur[8 * c + 1] * s), pack_h2(cur[8 * c + 2] * s, cur[8 * c + 3] * s),
+                   pack_h2(cur[8 * c + 4] * s, cur[8 * c + 5] * s), pack_h2(cur[8 * c + 6] * s, cur[8 * c + 7] * s));
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(p.img + node * kImgBytes);
+#pragma unroll
+  for (int r = 0; r < kImgBytes / 16 / 128; ++r)
+    dst[r * 128 + tid] = reinterpret_cast<const uint4*>(stage)[r * 128 + tid];
+  if (tid == 0) {
+    p.meta[node * kMeta + 1] = (unsigned)e;
+    p.meta[node * kMeta + 2] = __float_as_uint(G);
+  }
+}
+
 // ---------------------------------------------------------------------------------
-// tc_state: tile states and the Fenwick tree over tiles.
+// tc_state: tile states (level 0 of the Fenwick tree over tiles).
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ CUtensorMap mapK,
                                                        const __grid_constant__ CUtensorMap mapV,
@@ -150,7 +180,6 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   __shared__ float s_red[4];
   __shared__ float2 s_red2[4];
   __shared__ float s_gamma;
-  __shared__ unsigned s_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, rot = tid & 7;
   const int lin = blockIdx.x;
@@ -250,74 +279,87 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   if (warp == 0) ptx::tmem_dealloc(tbase, 128);
   if (!ok) return;
 
-  // Fenwick tree climb.  Row `tid` of every node is owned by thread tid.  Node images
-  // go through shared memory (sK, free now) so that global stores and loads coalesce.
-  uint8_t* stage = sK;             // 16 KB: outgoing image
-  uint8_t* stage_in = sK + 16384;  // 16 KB: sibling image
-  float Gcur = gamma;
-  int k = 0, idx = u;
+  // the tile's node (level 0; node_off[0] == 0), staged in sK (free now)
+  publish_node(cur, sK, (size_t)bh * p.nnodes + u, gamma, s_red2, p);
+}
+
+// ---------------------------------------------------------------------------------
+// tc_tree: levels m0 and m0 + 1 of the Fenwick tree over tiles, from the published
+// images of level m0 - 1.  Node_{m+1}[i] = 2^(Gamma(Node_m[2i+1])) Node_m[2i] +
+// Node_m[2i+1].  One CTA per pair of level-m0 nodes (2i, 2i+1): it loads their four
+// children with bulk copies, merges each pair in fp32 (thread tid owns row tid),
+// publishes both, and the parent Node_{m0+1}[i] from the fp32 sums when it exists.  No
+// CTA waits for another: the launches before it on the stream produced its inputs.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar_ld;
+  __shared__ float2 s_red2[4];
+  const int tid = threadIdx.x, rot = tid & 7;
+  const int n0 = p.NT >> m0;         // nodes at level m0
+  const int ni = (n0 + 1) >> 1;      // CTAs per (b, h)
+  const int bh = blockIdx.x / ni, i = blockIdx.x % ni;
+  const int nj = (2 * i + 1 < n0) ? 2 : 1;  // level-m0 nodes built here
   const size_t nbase = (size_t)bh * p.nnodes;
-  while (true) {
-    const size_t node = nbase + p.node_off[k] + idx;
-    {  // publish: fp16 image with scale 2^e, row tid at chunk slots c ^ (tid & 7)
-      float m = 0.f;
+  const size_t child0 = nbase + p.node_off[m0 - 1] + 4 * i;
+  if (tid == 0) {
+    ptx::mbar_init(&bar_ld, 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(&bar_ld, 2 * nj * kImgBytes);
+    for (int c = 0; c < 2 * nj; ++c)
+      ptx::bulk_load(smem + c * kImgBytes, p.img + (child0 + c) * kImgBytes, kImgBytes, &bar_ld);
+  }
+  float sc[4], gm[4];
 #pragma unroll
-      for (int j = 0; j < kDv; ++j) m = fmaxf(m, fabsf(cur[j]));
-      const int e = f16_exp(block_max2(make_float2(m, 0.f), s_red2).x);
-      const float s = pow2i(-e);
+  for (int c = 0; c < 4; ++c) {
+    sc[c] = c < 2 * nj ? pow2i((int)p.meta[(child0 + c) * kMeta + 1]) : 0.f;
+    gm[c] = c < 2 * nj ? __uint_as_float(p.meta[(child0 + c) * kMeta + 2]) : 0.f;
+  }
+  __syncthreads();  // barrier initialised
+  bool ok = wait_bar(&bar_ld, 0);
+  if (!ok) atomicExch(p.status, kStatusTimeout);
+  ok = __syncthreads_and(ok);
+  if (!ok) {
+    if (tid == 0) wait_bar(&bar_ld, 0);  // bounded: let the copies land before exit
+    return;
+  }
+  float par[kDv], cur[kDv];
+  float G0 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int cc = c ^ rot;
-        *reinterpret_cast<uint4*>(stage + tid * 128 + (cc << 4)) =
-            make_uint4(pack_h2(cur[8 * c] * s, cur[8 * c + 1] * s),
-                       pack_h2(cur[8 * c + 2] * s, cur[8 * c + 3] * s),
-                       pack_h2(cur[8 * c + 4] * s, cur[8 * c + 5] * s),
-                       pack_h2(cur[8 * c + 6] * s, cur[8 * c + 7] * s));
-      }
-      __syncthreads();
-      uint4* dst = reinterpret_cast<uint4*>(p.img + node * kImgBytes);
-#pragma unroll
-      for (int r = 0; r < kImgBytes / 16 / 128; ++r)
-        dst[r * 128 + tid] = reinterpret_cast<const uint4*>(stage)[r * 128 + tid];
-      if (tid == 0) {
-        p.meta[node * kMeta + 1] = (unsigned)e;
-        p.meta[node * kMeta + 2] = __float_as_uint(Gcur);
-      }
-    }
-    // parent exists only if both children are complete nodes
-    if ((idx >> 1) >= (p.NT >> (k + 1))) break;
-    __syncthreads();  // every thread's stores precede thread 0's release below
-    if (tid == 0)
-      s_flag = ptx::atom_add_acq_rel_gpu(p.meta + (nbase + p.node_off[k + 1] + (idx >> 1)) * kMeta, 1u);
-    __syncthreads();
-    if (s_flag == 0u) break;  // first of the two siblings: the other one merges
-    const size_t sib = nbase + p.node_off[k] + (idx ^ 1);
-#pragma unroll
-    for (int r = 0; r < kImgBytes / 16 / 128; ++r)
-      reinterpret_cast<uint4*>(stage_in)[r * 128 + tid] =
-          __ldcg(reinterpret_cast<const uint4*>(p.img + sib * kImgBytes) + r * 128 + tid);
-    const float ss = pow2i((int)__ldcg(p.meta + sib * kMeta + 1));
-    const float Gs = __uint_as_float(__ldcg(p.meta + sib * kMeta + 2));
-    __syncthreads();
-    const bool left_sib = (idx & 1) != 0;  // sibling is the earlier block
-    const float dcur = left_sib ? 1.f : exp2f(Gs);
-    const float dsib = (left_sib ? exp2f(Gcur) : 1.f) * ss;
+  for (int jj = 0; jj < 2; ++jj) {
+    if (jj >= nj) break;
+    const uint8_t* L = smem + (2 * jj) * kImgBytes + tid * 128;
+    const uint8_t* R = L + kImgBytes;
+    const float wl = exp2f(gm[2 * jj + 1]) * sc[2 * jj], wr = sc[2 * jj + 1];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      uint4 v4 = *reinterpret_cast<const uint4*>(stage_in + tid * 128 + ((c ^ rot) << 4));
-      const __half2* hv = reinterpret_cast<const __half2*>(&v4);
+      const uint4 l4 = *reinterpret_cast<const uint4*>(L + ((c ^ rot) << 4));
+      const uint4 r4 = *reinterpret_cast<const uint4*>(R + ((c ^ rot) << 4));
+      const __half2* hl = reinterpret_cast<const __half2*>(&l4);
+      const __half2* hr = reinterpret_cast<const __half2*>(&r4);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float2 f = __half22float2(hv[e]);
-        cur[8 * c + 2 * e] = dcur * cur[8 * c + 2 * e] + dsib * f.x;
-        cur[8 * c + 2 * e + 1] = dcur * cur[8 * c + 2 * e + 1] + dsib * f.y;
+        const float2 fl = __half22float2(hl[e]), fr = __half22float2(hr[e]);
+        cur[8 * c + 2 * e] = wl * fl.x + wr * fr.x;
+        cur[8 * c + 2 * e + 1] = wl * fl.y + wr * fr.y;
       }
     }
-    Gcur += Gs;
-    ++k;
-    idx >>= 1;
-    __syncthreads();  // staging buffers and s_flag are reused next round
+    const float G = gm[2 * jj] + gm[2 * jj + 1];
+    // staged over the left child, whose row tid only this thread has read
+    publish_node(cur, smem + (2 * jj) * kImgBytes, nbase + p.node_off[m0] + 2 * i + jj, G, s_red2, p);
+    if (jj == 0) {
+      G0 = G;
+#pragma unroll
+      for (int j = 0; j < kDv; ++j) par[j] = cur[j];
+    } else {
+      const float d = exp2f(G);
+#pragma unroll
+      for (int j = 0; j < kDv; ++j) par[j] = d * par[j] + cur[j];
+    }
   }
+  if (nj == 2)  // then i < NT >> (m0 + 1): the parent exists
+    publish_node(par, smem + kImgBytes, nbase + p.node_off[m0 + 1] + i, G0 + gm[2] + gm[3], s_red2, p);
 }
 
 // ---------------------------------------------------------------------------------
@@ -871,6 +913,7 @@ bool make_map(CUtensorMap* m, const void* base, int inner, int count, int T, int
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int kSmemState = 32768 + 32768 + 1024;
+constexpr int kSmemTree = 4 * kImgBytes + 1024;
 
 }  // namespace
 
@@ -880,7 +923,7 @@ bool tc_supported(const ll_shape& s) {
 }
 
 const char* tc_kernel_names(bool with_export) {
-  return with_export ? "tc_state,tc_output,tc_export" : "tc_state,tc_output";
+  return with_export ? "tc_state,tc_tree,tc_output,tc_export" : "tc_state,tc_tree,tc_output";
 }
 
 bool make_tc_plan(const ll_shape& s, TcPlan* p) {
@@ -932,25 +975,35 @@ cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   p.img = reinterpret_cast<uint8_t*>(a.ws + tp.off_img);
   p.meta = reinterpret_cast<unsigned*>(a.ws + tp.off_meta);
   p.status = a.status;
-  cudaError_t e = cudaMemsetAsync(p.meta, 0, tp.meta_bytes, st);
-  if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((size_t)tp.B * tp.NT * tp.H);
-  e = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemState);
+  cudaError_t e = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemState);
   if (e != cudaSuccess) return e;
   tc_state_kernel<<<grid, 128, kSmemState, st>>>(mK, mV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch(a, 0, st);
+  // tree levels 1.. two per launch; the profiling event of slot 1 follows the last one
+  e = cudaFuncSetAttribute(tc_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTree);
+  if (e != cudaSuccess) return e;
+  for (int m0 = 1; m0 < tp.MT; m0 += 2) {
+    const unsigned gt = (unsigned)((size_t)tp.B * tp.H * (((tp.NT >> m0) + 1) >> 1));
+    tc_tree_kernel<<<gt, 128, kSmemTree, st>>>(p, m0);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (m0 + 2 < tp.MT) note_launch();
+    else note_launch(a, 1, st);
+  }
+  if (tp.MT <= 1 && a.events && 2 < a.n_events && a.events[2])  // no tree level above tiles
+    cudaEventRecord(static_cast<cudaEvent_t>(a.events[2]), st);
   const int smem_out = out_smem_bytes(bit_length(tp.NT - 1));
   e = cudaFuncSetAttribute(tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_out);
   if (e != cudaSuccess) return e;
   tc_output_kernel<<<grid, 256, smem_out, st>>>(mQ, mK, mV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch(a, 1, st);
+  note_launch(a, 2, st);
   if (a.states_out) {
     tc_export_kernel<<<dim3(a.state_levels, tp.B * tp.H), 256, 0, st>>>(p, a.state_levels, a.states_out,
                                                                         a.logscale_out);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    note_launch(a, 2, st);
+    note_launch(a, 3, st);
   }
   return cudaSuccess;
 }
