@@ -18,6 +18,7 @@ CPU oracle (recurrent form) timed on this host's cores on a bounded sample.  Wit
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -349,6 +350,7 @@ def main():
         line["e2e"] = e2e_measure(sml, torch, x, w, dev, min(args.steps, 20))
         line["long"] = long_measure(sml, torch, dev)
         line["decode"] = decode_measure(sml, torch, dev, hbm_peak)
+        line["comparators"] = comparators_measure(sml, torch, x, w, ms)
     else:
         line["e2e"] = e2e_measure(sml, torch, x, w, dev, min(args.steps, 10))
         if world > 1:
@@ -385,6 +387,44 @@ def e2e_measure(sml, torch, x, w, dev, steps):
     return {"value": w.batch * w.T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps,
             "api": "loglinear_fwd_host (pinned host buffers)"}
+
+
+def comparators_measure(sml, torch, x, w, fused_ms, steps=5):
+    """The same workload through the two comparators: the forward without level fusion
+    (one output pass per level) and the lambda-constant special case (Mamba-2 SSD, with a
+    sequential state pass over tiles).  CUDA events around whole calls, inputs in HBM."""
+    res = {"fused_ms": fused_ms}
+    shape = sml.fwd_shape(x.q, x.v, x.lam, w.chunk)
+    dev = x.q.device
+    o = torch.empty_like(x.v)
+    ws_n = torch.empty(sml.lib().loglinear_fwd_naive_workspace_bytes(ctypes.byref(shape)),
+                       dtype=torch.uint8, device=dev)
+    ws_s = torch.empty(sml.lib().ssd_fwd_workspace_bytes(ctypes.byref(shape)), dtype=torch.uint8,
+                       device=dev)
+    for key, call in (("naive_per_level_ms",
+                       lambda: sml.loglinear_fwd_naive(x.q, x.k, x.v, x.a, x.lam, chunk=w.chunk, o=o,
+                                                       workspace=ws_n)),
+                      ("ssd_ms", lambda: sml.ssd_fwd(x.q, x.k, x.v, x.a, chunk=w.chunk, o=o,
+                                                     workspace=ws_s))):
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        res[key] = e0.elapsed_time(e1) / steps
+    if sml.loglinear_check_status() != 0:
+        raise RuntimeError("device status error in the comparators")
+    res["level_fusion_speedup"] = res["naive_per_level_ms"] / fused_ms
+    res["loglinear_over_ssd_time"] = fused_ms / res["ssd_ms"]
+    res["note"] = (f"workspaces and outputs allocated before timing; steps={steps}; fused_ms is "
+                   "the main line's ms_per_step")
+    del o, ws_n, ws_s
+    torch.cuda.empty_cache()
+    return res
 
 
 def long_measure(sml, torch, dev, steps=5):

@@ -164,8 +164,9 @@ ll_status loglinear_fwd_host(const ll_shape* shape, const void* q_host, const vo
  *     B*H = 16 heads of T = 2048 at d_k = 128, d_v = 64 fit; the pages workload does not).
  *   - The first call on each device looks up the array's device address (with that
  *     device current); make that first call before any stream capture begins.
- *   - Every call on a device shares the one array and leaves its contents behind; parts
- *     that must start at zero are cleared on the stream by each call.  Calls whose work
+ *   - Every call on a device shares the one array and leaves its contents behind;
+ *     nothing in it needs to start at zero, since every call writes each word before
+ *     reading it.  Calls whose work
  *     overlaps on the GPU (other streams, other threads) race on the array: serialise
  *     them, e.g. on one stream.
  */
@@ -174,6 +175,41 @@ ll_status loglinear_fwd_static_workspace(const ll_shape* shape, const void* q, c
                                          const void* v, const float* a, const float* lambda,
                                          void* o, float* states_out, float* state_logscale_out,
                                          int state_levels, void* stream);
+
+/* ---- comparators ---------------------------------------------------------------------
+ * Two other ways to compute on the tensor-core shape (bf16, d_k = 128, d_v = 64,
+ * T % 128 == 0), kept to measure the level-fused forward against.  Any other shape
+ * returns LL_ERR_UNIMPLEMENTED.  Same layouts, alignment and stream rules as
+ * loglinear_fwd; outputs written, workspace contents on entry do not matter.
+ */
+
+/* Bytes of workspace loglinear_fwd_naive needs (0: invalid or unsupported shape). */
+size_t loglinear_fwd_naive_workspace_bytes(const ll_shape* shape);
+
+/*
+ * The same output as loglinear_fwd, computed without level fusion: after the tile
+ * states and the Fenwick tree, one output pass per level (the intra-tile levels 0..7,
+ * then each inter-tile level), each re-reading its inputs and adding its level's term
+ * to an fp32 sum in the workspace.  This mirrors the write-up's naive variant, which
+ * re-runs an existing Mamba-2 computation once per level (section
+ * 对Mamba-2和门控的对数线性推广, Fig. 4).
+ */
+ll_status loglinear_fwd_naive(const ll_shape* shape, const void* q, const void* k, const void* v,
+                              const float* a, const float* lambda, void* o, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace ssd_fwd needs (0: invalid or unsupported shape). */
+size_t ssd_fwd_workspace_bytes(const ll_shape* shape);
+
+/*
+ * The lambda-constant special case, i.e. Mamba-2's SSD (state-space-duality article,
+ * section 狀態空間對偶性): o_t = sum over s <= t of M^S(t, s) (q_t . k_s) v_s.  It runs
+ * the Mamba-2 structure: chunk states, a sequential state pass over tiles, then one
+ * chunk output pass with a single prefix state per tile.  Same as loglinear_fwd with
+ * lambda = 1 everywhere, up to rounding.  shape->levels is ignored.
+ */
+ll_status ssd_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
+                  const float* a, void* o, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- diagnostics -------------------------------------------------------------------- */
 

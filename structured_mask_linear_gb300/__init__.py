@@ -87,6 +87,14 @@ def lib() -> ctypes.CDLL:
             L.loglinear_fwd_static_workspace.argtypes = [_SP] + [_vp] * 8 + [ctypes.c_int, _vp]
             L.loglinear_launch_count.restype = ctypes.c_ulonglong
             L.loglinear_launch_count.argtypes = []
+            L.loglinear_fwd_naive_workspace_bytes.restype = ctypes.c_size_t
+            L.loglinear_fwd_naive_workspace_bytes.argtypes = [_SP]
+            L.loglinear_fwd_naive.restype = ctypes.c_int
+            L.loglinear_fwd_naive.argtypes = [_SP] + [_vp] * 7 + [ctypes.c_size_t, _vp]
+            L.ssd_fwd_workspace_bytes.restype = ctypes.c_size_t
+            L.ssd_fwd_workspace_bytes.argtypes = [_SP]
+            L.ssd_fwd.restype = ctypes.c_int
+            L.ssd_fwd.argtypes = [_SP] + [_vp] * 6 + [ctypes.c_size_t, _vp]
             _lib = L
     return _lib
 
@@ -196,6 +204,39 @@ def loglinear_fwd_static_workspace(q, k, v, a, lam, chunk: int = 64, o=None, sta
                                               _ptr(state_logscale_out), int(state_levels),
                                               _stream_ptr(stream))
     _check(st, "loglinear_fwd_static_workspace")
+    return o
+
+
+def loglinear_fwd_naive(q, k, v, a, lam, chunk: int = 64, o=None, workspace=None, stream=None):
+    """Comparator: the same output as loglinear_fwd, one output pass per level (no level
+    fusion).  Tensor-core shape only."""
+    shape = fwd_shape(q, v, lam, chunk)
+    if o is None:
+        o = torch.empty_like(v)
+    nb = int(lib().loglinear_fwd_naive_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None:
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
+    st = lib().loglinear_fwd_naive(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                   _ptr(lam), _ptr(o), _ptr(workspace), workspace.numel(),
+                                   _stream_ptr(stream))
+    _check(st, "loglinear_fwd_naive")
+    return o
+
+
+def ssd_fwd(q, k, v, a, chunk: int = 64, o=None, workspace=None, stream=None):
+    """Comparator: the lambda-constant special case (Mamba-2 SSD) with a sequential state
+    pass over tiles.  Tensor-core shape only."""
+    B, T, G, dk = q.shape
+    H, dv = v.shape[2], v.shape[3]
+    shape = make_shape(B, T, H, H // G, dk, dv, chunk, max(1, (T - 1).bit_length() + 1), q.dtype)
+    if o is None:
+        o = torch.empty_like(v)
+    nb = int(lib().ssd_fwd_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None:
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
+    st = lib().ssd_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o),
+                       _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(st, "ssd_fwd")
     return o
 
 

@@ -55,6 +55,14 @@ size_t esize(const ll_shape* s) { return s->dtype == LL_BF16 ? 2 : 4; }
 
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The SSD comparator takes no lambda; its plan uses the smallest valid level count.
+bool ssd_shape(const ll_shape* s, ll_shape* out) {
+  if (!s) return false;
+  *out = *s;
+  if (out->T >= 1) out->levels = ll::bit_length(out->T - 1) + 1;
+  return true;
+}
+
 ll_status fwd_impl(const ll_shape* s, const void* q, const void* k, const void* v, const float* a,
                    const float* lambda, void* o, void* workspace, size_t workspace_bytes,
                    float* states_out, float* state_logscale_out, int state_levels, void* stream,
@@ -199,6 +207,61 @@ ll_status loglinear_fwd_host(const ll_shape* s, const void* q_host, const void* 
   if (cudaMemcpyAsync(o_host, dout, bv, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
     return LL_ERR_CUDA;
   return LL_OK;
+}
+
+size_t loglinear_fwd_naive_workspace_bytes(const ll_shape* s) {
+  if (check_fwd_shape(s) != LL_OK || !ll::tc_supported(*s)) return 0;
+  ll::TcPlan tp;
+  return ll::make_tc_plan(*s, &tp) ? ll::tc_naive_bytes(tp) : 0;
+}
+
+ll_status loglinear_fwd_naive(const ll_shape* s, const void* q, const void* k, const void* v,
+                              const float* a, const float* lambda, void* o, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  ll_status st = check_fwd_shape(s);
+  if (st != LL_OK) return st;
+  if (!ll::tc_supported(*s)) return LL_ERR_UNIMPLEMENTED;
+  if (!q || !k || !v || !a || !lambda || !o) return LL_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) || !aligned16(lambda) ||
+      !aligned16(o) || !aligned16(workspace))
+    return LL_ERR_ALIGN;
+  ll::TcPlan tp;
+  if (!ll::make_tc_plan(*s, &tp)) return LL_ERR_SHAPE;
+  if (!workspace || workspace_bytes < ll::tc_naive_bytes(tp)) return LL_ERR_WORKSPACE;
+  unsigned* sw = status_word();
+  if (!sw) return LL_ERR_CUDA;
+  ll::FwdArgs fa{q, k, v, a, lambda, o, static_cast<char*>(workspace), nullptr, nullptr, 0, sw,
+                 nullptr, 0};
+  return ll::launch_tc_naive(tp, fa, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LL_OK
+                                                                                       : LL_ERR_CUDA;
+}
+
+size_t ssd_fwd_workspace_bytes(const ll_shape* s) {
+  ll_shape t;
+  if (!ssd_shape(s, &t) || check_fwd_shape(&t) != LL_OK || !ll::tc_supported(t)) return 0;
+  ll::TcPlan tp;
+  return ll::make_tc_plan(t, &tp) ? ll::tc_ssd_bytes(tp) : 0;
+}
+
+ll_status ssd_fwd(const ll_shape* s, const void* q, const void* k, const void* v, const float* a,
+                  void* o, void* workspace, size_t workspace_bytes, void* stream) {
+  ll_shape t;
+  if (!ssd_shape(s, &t)) return LL_ERR_NULL;
+  ll_status st = check_fwd_shape(&t);
+  if (st != LL_OK) return st;
+  if (!ll::tc_supported(t)) return LL_ERR_UNIMPLEMENTED;
+  if (!q || !k || !v || !a || !o) return LL_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) || !aligned16(o) ||
+      !aligned16(workspace))
+    return LL_ERR_ALIGN;
+  ll::TcPlan tp;
+  if (!ll::make_tc_plan(t, &tp)) return LL_ERR_SHAPE;
+  if (!workspace || workspace_bytes < ll::tc_ssd_bytes(tp)) return LL_ERR_WORKSPACE;
+  unsigned* sw = status_word();
+  if (!sw) return LL_ERR_CUDA;
+  ll::FwdArgs fa{q, k, v, a, nullptr, o, static_cast<char*>(workspace), nullptr, nullptr, 0, sw,
+                 nullptr, 0};
+  return ll::launch_tc_ssd(tp, fa, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
 ll_status loglinear_check_status(void* stream) {

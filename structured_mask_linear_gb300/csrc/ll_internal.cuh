@@ -78,6 +78,12 @@ struct TcPlan {
 bool tc_supported(const ll_shape& s);
 bool make_tc_plan(const ll_shape& s, TcPlan* p);
 cudaError_t launch_tc_fwd(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
+// Comparators on the tensor-core shape (not the product path): the forward with one
+// output pass per level (no level fusion), and the lambda-constant special case (SSD).
+size_t tc_naive_bytes(const TcPlan& p);
+cudaError_t launch_tc_naive(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
+size_t tc_ssd_bytes(const TcPlan& p);
+cudaError_t launch_tc_ssd(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
 const char* tc_kernel_names(bool with_export);
 
 __host__ __device__ inline int bit_length(long long x) {

@@ -58,6 +58,12 @@ struct TcParams {
   uint8_t* img;    // (B*H, nnodes, 16 KB) fp16 node images
   unsigned* meta;  // (B*H, nnodes, 4)
   unsigned* status;
+  // comparators only (single-level and SSD output modes)
+  float* o32;      // (B, T, H, d_v) fp32 running sum of the single-level passes
+  int lsel;        // the one level of a single-level pass
+  int lflags;      // bit 0: first pass (store), bit 1: last pass (write o)
+  uint8_t* pimg;   // (B*H, NT, 16 KB) SSD prefix-state images
+  unsigned* pmeta; // (B*H, NT, 4)
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
@@ -140,7 +146,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // shared memory whose row tid only this thread uses before the call) so that the global
 // stores coalesce; then the scale exponent and the node's log2 decay G into meta.
 __device__ __forceinline__ void publish_node(const float (&cur)[kDv], uint8_t* stage, size_t node,
-                                             float G, float2* s_red2, const TcParams& p) {
+                                             float G, float2* s_red2, uint8_t* img, unsigned* meta) {
   const int tid = threadIdx.x, rot = tid & 7;
   float m = 0.f;
 #pragma unroll
@@ -155,13 +161,13 @@ __device__ __forceinline__ void publish_node(const float (&cur)[kDv], uint8_t* s
                    pack_h2(cur[8 * c + 4] * s, cur[8 * c + 5] * s), pack_h2(cur[8 * c + 6] * s, cur[8 * c + 7] * s));
   }
   __syncthreads();
-  uint4* dst = reinterpret_cast<uint4*>(p.img + node * kImgBytes);
+  uint4* dst = reinterpret_cast<uint4*>(img + node * kImgBytes);
 #pragma unroll
   for (int r = 0; r < kImgBytes / 16 / 128; ++r)
     dst[r * 128 + tid] = reinterpret_cast<const uint4*>(stage)[r * 128 + tid];
   if (tid == 0) {
-    p.meta[node * kMeta + 1] = (unsigned)e;
-    p.meta[node * kMeta + 2] = __float_as_uint(G);
+    meta[node * kMeta + 1] = (unsigned)e;
+    meta[node * kMeta + 2] = __float_as_uint(G);
   }
 }
 
@@ -280,7 +286,7 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   if (!ok) return;
 
   // the tile's node (level 0; node_off[0] == 0), staged in sK (free now)
-  publish_node(cur, sK, (size_t)bh * p.nnodes + u, gamma, s_red2, p);
+  publish_node(cur, sK, (size_t)bh * p.nnodes + u, gamma, s_red2, p.img, p.meta);
 }
 
 // ---------------------------------------------------------------------------------
@@ -347,7 +353,7 @@ __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
     }
     const float G = gm[2 * jj] + gm[2 * jj + 1];
     // staged over the left child, whose row tid only this thread has read
-    publish_node(cur, smem + (2 * jj) * kImgBytes, nbase + p.node_off[m0] + 2 * i + jj, G, s_red2, p);
+    publish_node(cur, smem + (2 * jj) * kImgBytes, nbase + p.node_off[m0] + 2 * i + jj, G, s_red2, p.img, p.meta);
     if (jj == 0) {
       G0 = G;
 #pragma unroll
@@ -359,7 +365,8 @@ __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
     }
   }
   if (nj == 2)  // then i < NT >> (m0 + 1): the parent exists
-    publish_node(par, smem + kImgBytes, nbase + p.node_off[m0 + 1] + i, G0 + gm[2] + gm[3], s_red2, p);
+    publish_node(par, smem + kImgBytes, nbase + p.node_off[m0 + 1] + i, G0 + gm[2] + gm[3], s_red2, p.img,
+                 p.meta);
 }
 
 // ---------------------------------------------------------------------------------
@@ -383,6 +390,13 @@ __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
 // (asynchronously), so that no global load sits on the path of P or of a level.
 // TMEM (256 columns): S in 0..127; once role a has consumed S, P in 0..63 and O in
 // 64..127; Y0 in 192..255 and Y1 in 128..191 (free from the start).
+//
+// kMode selects what one launch computes (1 and 2 exist only as comparators):
+//  0  the level-fused forward above;
+//  1  the lambda-constant special case (Mamba-2 SSD): lambda = 1 at every level and one
+//     inter-tile term per tile, from the prefix state of all earlier tiles (pimg);
+//  2  one level lsel only, accumulated in fp32 across launches (no level fusion): an
+//     intra level masks P to that level; an inter level skips S, P and O.
 // ---------------------------------------------------------------------------------
 constexpr int kOutFixed = 104704;  // shared bytes in front of the inter-level lambda table
 constexpr int kMaxInter = 19;      // inter-tile levels per tile supported (NT <= 2^19)
@@ -418,6 +432,7 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& x, __nv_bfloat162 
                     bf16x2_to_f16x2(x.w, s2));
 }
 
+template <int kMode>
 __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                            const __grid_constant__ CUtensorMap mapK,
                                                            const __grid_constant__ CUtensorMap mapV,
@@ -455,11 +470,24 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   const size_t nbase = (size_t)bh * p.nnodes;
   const size_t row = (size_t)b * p.T + t0 + r;  // token of this thread's query row
   const float* lrow = p.lam + (row * p.H + h) * p.L;
-  const int nlev = __popc((unsigned)u);         // inter-tile levels of this tile
+  // inter-tile levels of this tile, and whether the intra-tile part runs
+  const int nlev = kMode == 0 ? __popc((unsigned)u)
+                 : kMode == 1 ? (u > 0 ? 1 : 0)
+                              : (p.lsel >= kLevIntra && ((u >> (p.lsel - kLevIntra)) & 1) ? 1 : 0);
+  const bool intra_on = kMode != 2 || p.lsel < kLevIntra;
   auto ebuf = [&](int k) { return k == 0 ? RE : RK + (k - 1) * 16384; };  // image buffer k
-  auto node_of = [&](int i) {                   // node read by level index i
-    const int m = nth_set_bit((unsigned)u, i);
-    return nbase + p.node_off[m] + ((u >> m) - 1);
+  auto lev_of = [&](int i) {  // tile level m of level index i
+    return kMode == 2 ? p.lsel - kLevIntra : nth_set_bit((unsigned)u, i);
+  };
+  auto img_of = [&](int i) -> const uint8_t* {  // image read by level index i
+    if (kMode == 1) return p.pimg + ((size_t)bh * p.NT + u) * kImgBytes;
+    const int m = lev_of(i);
+    return p.img + (nbase + p.node_off[m] + ((u >> m) - 1)) * kImgBytes;
+  };
+  auto meta_of = [&](int i) -> const unsigned* {
+    if (kMode == 1) return p.pmeta + ((size_t)bh * p.NT + u) * kMeta;
+    const int m = lev_of(i);
+    return p.meta + (nbase + p.node_off[m] + ((u >> m) - 1)) * kMeta;
   };
 
   if (tid == 0) {
@@ -473,15 +501,17 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       ptx::mbar_init(&bar_yf[i], 128);
     }
     ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 * 2 + 16384);
+    ptx::mbar_arrive_expect_tx(&bar_ld, intra_on ? 32768 * 2 + 16384 : 32768);
     ptx::tma_load_4d(RQ, &mapQ, &bar_ld, 0, g, (int)t0, b);
     ptx::tma_load_4d(RQ + 16384, &mapQ, &bar_ld, 64, g, (int)t0, b);
-    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
-    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
-    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
+    if (intra_on) {
+      ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
+      ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
+      ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
+    }
     if (nlev > 0) {
       ptx::mbar_arrive_expect_tx(&bar_e[0], kImgBytes);
-      ptx::bulk_load(RE, p.img + node_of(0) * kImgBytes, kImgBytes, &bar_e[0]);
+      ptx::bulk_load(RE, img_of(0), kImgBytes, &bar_e[0]);
     }
   }
   if (warp == 0) {
@@ -492,18 +522,20 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   // the node scalars of the tile's levels, copied asynchronously
   if (!role_b) {
 #pragma unroll
-    for (int l = 0; l < kLevIntra; ++l) ptx::cp_async4(sLam8 + r * 9 + l, lrow + l);
+    for (int l = 0; l < kLevIntra; ++l) {
+      if (kMode == 0 || (kMode == 2 && l == p.lsel)) ptx::cp_async4(sLam8 + r * 9 + l, lrow + l);
+      else sLam8[r * 9 + l] = kMode == 1 ? 1.f : 0.f;  // SSD: lambda = 1; single level: others off
+    }
   } else {
-    unsigned rest = (unsigned)u;
-    for (int i = 0; rest; ++i) {
-      const int m = __ffs(rest) - 1;
-      rest &= rest - 1;
-      ptx::cp_async4(sLamI + i * 128 + r, lrow + kLevIntra + m);
+    if (kMode == 1) {
+      if (nlev > 0) sLamI[r] = 1.f;
+    } else {
+      for (int i = 0; i < nlev; ++i) ptx::cp_async4(sLamI + i * 128 + r, lrow + kLevIntra + lev_of(i));
     }
     if (r < nlev) {
-      const size_t node = node_of(r);
-      ptx::cp_async4(sNode + 2 * r, p.meta + node * kMeta + 1);
-      ptx::cp_async4(sNode + 2 * r + 1, p.meta + node * kMeta + 2);
+      const unsigned* mt = meta_of(r);
+      ptx::cp_async4(sNode + 2 * r, mt + 1);
+      ptx::cp_async4(sNode + 2 * r + 1, mt + 2);
     }
   }
   // chunk-local log2 decay cumsum over the 128 rows (both roles compute it)
@@ -529,7 +561,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   ok = __syncthreads_and(ok);
 
   // S = Q Kᵀ (M = 128 queries, N = 128 keys, K = 128 d_k), bf16, both K-major.
-  if (ok && driver) {
+  if (ok && driver && intra_on) {
     ptx::tc_fence_after();
     const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 0);
     const uint32_t q0 = ptx::smem_u32(RQ), k0 = ptx::smem_u32(RK);
@@ -541,9 +573,11 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     }
     ptx::umma_commit(&bar_s);
   }
-  const bool s_issued = ok;
+  const bool s_issued = ok && intra_on;
 
-  if (!role_b) {
+  if (!role_b && !intra_on) {
+    __syncthreads();  // join: nothing to do without the intra-tile part
+  } else if (!role_b) {
     // ---- role a -----------------------------------------------------------------------
     // V tile scale (V is not an operand of S) and V -> fp16 in place.
     uint8_t* vrow = RV + r * 128;
@@ -713,8 +747,10 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       const __nv_bfloat162 s2 = __floats2bfloat162_rn(sq, sq);
 #pragma unroll
       for (int c = 0; c < 16; ++c) qv[c] = bf16x8_to_f16x8(qv[c], s2);
-      ok = wait_bar(&bar_s, 0);
-      if (!ok) atomicExch(p.status, kStatusTimeout);
+      if (intra_on) {
+        ok = wait_bar(&bar_s, 0);
+        if (!ok) atomicExch(p.status, kStatusTimeout);
+      }
       if (ok) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -727,7 +763,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     if (ok && driver) {
       for (int i = 1; i < 3 && i < nlev; ++i) {  // K has been read by S: RK is free
         ptx::mbar_arrive_expect_tx(&bar_e[i], kImgBytes);
-        ptx::bulk_load(ebuf(i), p.img + node_of(i) * kImgBytes, kImgBytes, &bar_e[i]);
+        ptx::bulk_load(ebuf(i), img_of(i), kImgBytes, &bar_e[i]);
         ++issued;
       }
     }
@@ -759,6 +795,13 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
 #pragma unroll
     for (int j = 0; j < kDv; ++j) acc[j] = 0.f;
     float D = 0.f;
+    if (kMode == 2 && nlev > 0) {  // one level: the nearer buckets' decay still applies
+      const int m = p.lsel - kLevIntra;
+      for (unsigned rest = (unsigned)u & ((1u << m) - 1u); rest; rest &= rest - 1) {
+        const int mm = __ffs(rest) - 1;
+        D += __uint_as_float(p.meta[(nbase + p.node_off[mm] + ((u >> mm) - 1)) * kMeta + 2]);
+      }
+    }
     bool okd = true;
     if (ok && driver && nlev > 0) okd = issue_y(0);
     for (int i = 0; ok && i < nlev; ++i) {
@@ -775,7 +818,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         ++y_seen;
         if (i + 3 < nlev) {  // the image buffer of level i is free again
           ptx::mbar_arrive_expect_tx(&bar_e[i % 3], kImgBytes);
-          ptx::bulk_load(ebuf(i % 3), p.img + node_of(i + 3) * kImgBytes, kImgBytes, &bar_e[i % 3]);
+          ptx::bulk_load(ebuf(i % 3), img_of(i + 3), kImgBytes, &bar_e[i % 3]);
           ++issued;
         }
       }
@@ -803,22 +846,52 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     }
     __syncthreads();  // join: P, its row scales and the O MMA have been issued
     const bool o_issued = s_oi != 0;
-    ok = ok && o_issued && wait_bar(&bar_o, 0);
-    if (!ok && o_issued) atomicExch(p.status, kStatusTimeout);
+    if (intra_on) {
+      ok = ok && o_issued && wait_bar(&bar_o, 0);
+      if (!ok && o_issued) atomicExch(p.status, kStatusTimeout);
+    }
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       ptx::tc_fence_after();
       const float so = pow2s(sEp[r]);
       __nv_bfloat16* orow = p.o + (row * p.H + h) * kDv;
+      float* o32row = kMode == 2 ? p.o32 + (row * p.H + h) * kDv : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float y[32];
-        ptx::tmem_ld32(tO + lane_off + half * 32, y);
-        ptx::tmem_ld_wait();
+        if (intra_on) {
+          ptx::tmem_ld32(tO + lane_off + half * 32, y);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) y[j] = y[j] * so + acc[half * 32 + j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) y[j] = acc[half * 32 + j];
+        }
+        if (kMode == 2 && !(p.lflags & 2)) {  // store or add the running fp32 sum
+          float4* d4 = reinterpret_cast<float4*>(o32row + half * 32);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float4 x = make_float4(y[4 * c], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]);
+            if (!(p.lflags & 1)) {
+              const float4 o4 = d4[c];
+              x.x += o4.x; x.y += o4.y; x.z += o4.z; x.w += o4.w;
+            }
+            d4[c] = x;
+          }
+          continue;
+        }
+        if (kMode == 2) {  // last pass: add the running sum, then write o
+          const float4* s4 = reinterpret_cast<const float4*>(o32row + half * 32);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 o4 = s4[c];
+            y[4 * c] += o4.x; y[4 * c + 1] += o4.y; y[4 * c + 2] += o4.z; y[4 * c + 3] += o4.w;
+          }
+        }
         uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2)
-          pk[j >> 1] = pack_bf16(y[j] * so + acc[half * 32 + j], y[j + 1] * so + acc[half * 32 + j + 1]);
+        for (int j = 0; j < 32; j += 2) pk[j >> 1] = pack_bf16(y[j], y[j + 1]);
         uint4* dst = reinterpret_cast<uint4*>(orow + half * 32);
 #pragma unroll
         for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
@@ -833,6 +906,76 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) ptx::tmem_dealloc(tbase, 256);
+}
+
+// ---------------------------------------------------------------------------------
+// ssd_scan: state passing over tiles for the lambda-constant special case (Mamba-2
+// SSD): prefix_0 = 0, prefix_{u+1} = 2^(gamma_u) prefix_u + H_u, from the tile states
+// (level-0 node images) that tc_state published.  One CTA per (b, h) walks the tiles in
+// order, thread tid owning row tid; four tiles' images and scalars are in flight ahead
+// of it.  prefix_u is published for u >= 1 as an fp16 image (pimg, pmeta).
+// ---------------------------------------------------------------------------------
+constexpr int kScanRing = 4;
+constexpr int kSmemScan = kScanRing * (kImgBytes + 16) + 1024;
+
+__global__ void __launch_bounds__(128) ssd_scan_kernel(TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned* smeta = reinterpret_cast<unsigned*>(smem + kScanRing * kImgBytes);  // 4 u32 per slot
+  __shared__ __align__(8) uint64_t bar[kScanRing];
+  __shared__ float2 s_red2[4];
+  const int tid = threadIdx.x, rot = tid & 7;
+  const int bh = blockIdx.x;
+  const size_t nbase = (size_t)bh * p.nnodes;  // level-0 node of tile u: nbase + u
+  const int nsteps = p.NT - 1;                 // prefixes 1 .. NT-1
+  auto issue = [&](int u) {                    // tile u's image and scalars into slot u % 4
+    const int k = u % kScanRing;
+    ptx::mbar_arrive_expect_tx(&bar[k], kImgBytes + 16);
+    ptx::bulk_load(smem + k * kImgBytes, p.img + (nbase + u) * kImgBytes, kImgBytes, &bar[k]);
+    ptx::bulk_load(smeta + 4 * k, p.meta + (nbase + u) * kMeta, 16, &bar[k]);
+  };
+  int issued = 0;
+  if (tid == 0) {
+    for (int k = 0; k < kScanRing; ++k) ptx::mbar_init(&bar[k], 1);
+    ptx::fence_mbar_init();
+    for (; issued < kScanRing && issued < nsteps; ++issued) issue(issued);
+  }
+  __syncthreads();
+  float acc[kDv];
+#pragma unroll
+  for (int j = 0; j < kDv; ++j) acc[j] = 0.f;
+  int u = 0;
+  bool ok = true;
+  for (; u < nsteps; ++u) {
+    const int k = u % kScanRing;
+    ok = wait_bar(&bar[k], (u / kScanRing) & 1);
+    if (!ok) atomicExch(p.status, kStatusTimeout);
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    const float sc = pow2i((int)smeta[4 * k + 1]);
+    const float dg = exp2f(__uint_as_float(smeta[4 * k + 2]));
+    const uint8_t* row = smem + k * kImgBytes + tid * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 x4 = *reinterpret_cast<const uint4*>(row + ((c ^ rot) << 4));
+      const __half2* hx = reinterpret_cast<const __half2*>(&x4);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(hx[e]);
+        acc[8 * c + 2 * e] = dg * acc[8 * c + 2 * e] + sc * f.x;
+        acc[8 * c + 2 * e + 1] = dg * acc[8 * c + 2 * e + 1] + sc * f.y;
+      }
+    }
+    // prefix_{u+1}, staged over slot k (row tid was read by this thread only)
+    publish_node(acc, smem + k * kImgBytes, (size_t)bh * p.NT + u + 1, 0.f, s_red2, p.pimg, p.pmeta);
+    __syncthreads();  // every thread has stored its part of the staged image
+    if (tid == 0 && issued < nsteps) {
+      ptx::fence_proxy_async_smem();
+      issue(issued++);
+    }
+  }
+  if (!ok && tid == 0)  // let this CTA's own copies land (bounded) before exit
+    for (int v = u; v < issued; ++v) wait_bar(&bar[v % kScanRing], (v / kScanRing) & 1);
 }
 
 // ---------------------------------------------------------------------------------
@@ -953,12 +1096,15 @@ bool make_tc_plan(const ll_shape& s, TcPlan* p) {
   return true;
 }
 
-cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
-  CUtensorMap mQ, mK, mV;
-  if (!make_map(&mQ, a.q, kDk, tp.G, tp.T, tp.B) || !make_map(&mK, a.k, kDk, tp.G, tp.T, tp.B) ||
-      !make_map(&mV, a.v, kDv, tp.H, tp.T, tp.B))
-    return cudaErrorInvalidValue;
-  TcParams p;
+namespace {
+
+bool tc_setup(const TcPlan& tp, const FwdArgs& a, CUtensorMap* mQ, CUtensorMap* mK, CUtensorMap* mV,
+              TcParams* pp) {
+  if (!make_map(mQ, a.q, kDk, tp.G, tp.T, tp.B) || !make_map(mK, a.k, kDk, tp.G, tp.T, tp.B) ||
+      !make_map(mV, a.v, kDv, tp.H, tp.T, tp.B))
+    return false;
+  TcParams& p = *pp;
+  p = TcParams{};
   p.B = tp.B;
   p.T = tp.T;
   p.H = tp.H;
@@ -975,14 +1121,23 @@ cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   p.img = reinterpret_cast<uint8_t*>(a.ws + tp.off_img);
   p.meta = reinterpret_cast<unsigned*>(a.ws + tp.off_meta);
   p.status = a.status;
+  return true;
+}
+
+cudaError_t launch_state(const TcPlan& tp, const FwdArgs& a, const CUtensorMap& mK, const CUtensorMap& mV,
+                         const TcParams& p, cudaStream_t st) {
   const unsigned grid = (unsigned)((size_t)tp.B * tp.NT * tp.H);
   cudaError_t e = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemState);
   if (e != cudaSuccess) return e;
   tc_state_kernel<<<grid, 128, kSmemState, st>>>(mK, mV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch(a, 0, st);
+  return cudaSuccess;
+}
+
+cudaError_t launch_tree(const TcPlan& tp, const FwdArgs& a, const TcParams& p, cudaStream_t st) {
   // tree levels 1.. two per launch; the profiling event of slot 1 follows the last one
-  e = cudaFuncSetAttribute(tc_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTree);
+  cudaError_t e = cudaFuncSetAttribute(tc_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTree);
   if (e != cudaSuccess) return e;
   for (int m0 = 1; m0 < tp.MT; m0 += 2) {
     const unsigned gt = (unsigned)((size_t)tp.B * tp.H * (((tp.NT >> m0) + 1) >> 1));
@@ -993,11 +1148,30 @@ cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   }
   if (tp.MT <= 1 && a.events && 2 < a.n_events && a.events[2])  // no tree level above tiles
     cudaEventRecord(static_cast<cudaEvent_t>(a.events[2]), st);
-  const int smem_out = out_smem_bytes(bit_length(tp.NT - 1));
-  e = cudaFuncSetAttribute(tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_out);
+  return cudaSuccess;
+}
+
+template <int kMode>
+cudaError_t launch_output(const TcPlan& tp, const CUtensorMap& mQ, const CUtensorMap& mK,
+                          const CUtensorMap& mV, const TcParams& p, int ninter, cudaStream_t st) {
+  const unsigned grid = (unsigned)((size_t)tp.B * tp.NT * tp.H);
+  const int smem_out = out_smem_bytes(ninter);
+  cudaError_t e = cudaFuncSetAttribute(tc_output_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_out);
   if (e != cudaSuccess) return e;
-  tc_output_kernel<<<grid, 256, smem_out, st>>>(mQ, mK, mV, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  tc_output_kernel<kMode><<<grid, 256, smem_out, st>>>(mQ, mK, mV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
+  CUtensorMap mQ, mK, mV;
+  TcParams p;
+  if (!tc_setup(tp, a, &mQ, &mK, &mV, &p)) return cudaErrorInvalidValue;
+  cudaError_t e = launch_state(tp, a, mK, mV, p, st);
+  if (e == cudaSuccess) e = launch_tree(tp, a, p, st);
+  if (e != cudaSuccess) return e;
+  if ((e = launch_output<0>(tp, mQ, mK, mV, p, bit_length(tp.NT - 1), st)) != cudaSuccess) return e;
   note_launch(a, 2, st);
   if (a.states_out) {
     tc_export_kernel<<<dim3(a.state_levels, tp.B * tp.H), 256, 0, st>>>(p, a.state_levels, a.states_out,
@@ -1005,6 +1179,55 @@ cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launch(a, 3, st);
   }
+  return cudaSuccess;
+}
+
+size_t tc_naive_bytes(const TcPlan& tp) {
+  return ((tp.bytes + 255) & ~size_t(255)) + (size_t)tp.B * tp.T * tp.H * kDv * sizeof(float);
+}
+
+cudaError_t launch_tc_naive(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
+  CUtensorMap mQ, mK, mV;
+  TcParams p;
+  if (!tc_setup(tp, a, &mQ, &mK, &mV, &p)) return cudaErrorInvalidValue;
+  p.o32 = reinterpret_cast<float*>(a.ws + ((tp.bytes + 255) & ~size_t(255)));
+  cudaError_t e = launch_state(tp, a, mK, mV, p, st);
+  if (e == cudaSuccess) e = launch_tree(tp, a, p, st);
+  if (e != cudaSuccess) return e;
+  const int last = kLevIntra + tp.MT - 1;  // highest level with buckets in [0, T)
+  for (int l = 0; l <= last; ++l) {  // one pass per level, no fusion
+    p.lsel = l;
+    p.lflags = (l == 0 ? 1 : 0) | (l == last ? 2 : 0);
+    if ((e = launch_output<2>(tp, mQ, mK, mV, p, 1, st)) != cudaSuccess) return e;
+    note_launch();
+  }
+  return cudaSuccess;
+}
+
+size_t tc_ssd_bytes(const TcPlan& tp) {
+  const size_t n = (size_t)tp.B * tp.H * tp.NT;
+  return ((tp.bytes + 255) & ~size_t(255)) + n * kImgBytes + n * kMeta * sizeof(unsigned);
+}
+
+cudaError_t launch_tc_ssd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
+  CUtensorMap mQ, mK, mV;
+  TcParams p;
+  if (!tc_setup(tp, a, &mQ, &mK, &mV, &p)) return cudaErrorInvalidValue;
+  const size_t base = (tp.bytes + 255) & ~size_t(255);
+  p.pimg = reinterpret_cast<uint8_t*>(a.ws + base);
+  p.pmeta = reinterpret_cast<unsigned*>(a.ws + base + (size_t)tp.B * tp.H * tp.NT * kImgBytes);
+  cudaError_t e = launch_state(tp, a, mK, mV, p, st);
+  if (e != cudaSuccess) return e;
+  if (tp.NT > 1) {
+    if ((e = cudaFuncSetAttribute(ssd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemScan)) !=
+        cudaSuccess)
+      return e;
+    ssd_scan_kernel<<<tp.B * tp.H, 128, kSmemScan, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launch();
+  }
+  if ((e = launch_output<1>(tp, mQ, mK, mV, p, 1, st)) != cudaSuccess) return e;
+  note_launch();
   return cudaSuccess;
 }
 

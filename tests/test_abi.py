@@ -23,7 +23,7 @@ def L():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(loglinear_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:loglinear|ssd)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -122,3 +122,18 @@ def test_status_strings(L):
     for code in range(9):
         assert len(sml.loglinear_status_string(code)) > 0
     assert sml.loglinear_status_string(99) == "unknown status"
+
+
+def test_comparators_validate_on_the_host(L):
+    """The naive per-level forward and the SSD special case exist for the tensor-core
+    shape only: other shapes are rejected before any launch."""
+    bad = shape(T=2000)
+    assert L.loglinear_fwd_naive_workspace_bytes(ctypes.byref(bad)) == 0
+    assert L.ssd_fwd_workspace_bytes(ctypes.byref(bad)) == 0
+    assert L.loglinear_fwd_naive(ctypes.byref(bad), *([FAKE] * 6), FAKE, 1 << 30, None) == 2
+    assert L.ssd_fwd(ctypes.byref(bad), *([FAKE] * 5), FAKE, 1 << 30, None) == 2
+    other = shape(dtype=sml.LL_F32, d_k=64, d_v=32)
+    assert L.loglinear_fwd_naive_workspace_bytes(ctypes.byref(other)) == 0
+    assert L.loglinear_fwd_naive(ctypes.byref(other), *([FAKE] * 6), FAKE, 1 << 30, None) == 8
+    assert L.ssd_fwd(ctypes.byref(other), *([FAKE] * 5), FAKE, 1 << 30, None) == 8
+    assert L.ssd_fwd(ctypes.byref(shape()), None, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) in (1, 8)
