@@ -343,3 +343,80 @@ void oracle_brute(long B, long T, long H, long hpg, long dk, long dv, long L,
   free(lo);
   free(len);
 }
+
+/* ---------------------------------------------------------------------------
+ * Backward of Form Q for the scalar loss  sum_{t,j} dO[t,j] * o[t,j].
+ * The pages give no backward; this is the chain rule applied to the forward
+ * definition above (page 1, sections 特殊结构：树划分 and
+ * 对Mamba-2和门控的对数线性推广), term by term.  With
+ *   e_ts = exp(G_t - G_s),  w_ts = lambda_t^{l(t,s)} e_ts,
+ *   A_ts = w_ts (q_t . k_s) (dO_t . v_s)          (s <= t):
+ *   dq_t += w_ts (dO_t . v_s) k_s,   dk_s += w_ts (dO_t . v_s) q_t
+ *     (q, k are per group: the heads of a group add up),
+ *   dv_s += w_ts (q_t . k_s) dO_t,
+ *   dlam_t^{l(t,s)} += e_ts (q_t . k_s) (dO_t . v_s),
+ *   d(log a_r) = sum over t >= r and s < r of A_ts (log a_r enters e_ts exactly
+ *     for s < r <= t), summed here for each t over r = 1..t with a running sum
+ *     over s < r;  da_r = d(log a_r) / a_r.
+ * Outputs are overwritten.  One group at a time (its heads share dq, dk).
+ * ------------------------------------------------------------------------- */
+void oracle_backward(long B, long T, long H, long hpg, long dk, long dv, long L,
+                     const double* q, const double* k, const double* v, const double* a,
+                     const double* lam, const double* dO, double* dq, double* dkk, double* dvv,
+                     double* da, double* dlam) {
+  long G = H / hpg;
+  memset(dq, 0, sizeof(double) * (size_t)(B * T * G * dk));
+  memset(dkk, 0, sizeof(double) * (size_t)(B * T * G * dk));
+  memset(dvv, 0, sizeof(double) * (size_t)(B * T * H * dv));
+  memset(da, 0, sizeof(double) * (size_t)(B * T * H));
+  memset(dlam, 0, sizeof(double) * (size_t)(B * T * H * L));
+#pragma omp parallel for collapse(2) schedule(dynamic)
+  for (long b = 0; b < B; b++) {
+    for (long g = 0; g < G; g++) {
+      double* Gs = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+      double* dloga = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+      for (long h = g * hpg; h < (g + 1) * hpg; h++) {
+        double acc = 0.0;
+        for (long t = 0; t < T; t++) {
+          acc += log(a[(b * T + t) * H + h]);
+          Gs[t] = acc;
+          dloga[t] = 0.0;
+        }
+        for (long t = 0; t < T; t++) {
+          const double* qt = q + ((b * T + t) * G + g) * dk;
+          const double* dot_ = dO + ((b * T + t) * H + h) * dv;
+          const double* lt = lam + ((b * T + t) * H + h) * L;
+          double* dqt = dq + ((b * T + t) * G + g) * dk;
+          double* dlt = dlam + ((b * T + t) * H + h) * L;
+          double run = 0.0;  /* sum over s < r of A_ts, for r = s + 1 */
+          for (long s = 0; s <= t; s++) {
+            const double* ks = k + ((b * T + s) * G + g) * dk;
+            const double* vs = v + ((b * T + s) * H + h) * dv;
+            double qk = 0.0, dov = 0.0;
+            for (long i = 0; i < dk; i++) qk += qt[i] * ks[i];
+            for (long j = 0; j < dv; j++) dov += dot_[j] * vs[j];
+            int l = oracle_level(t, s);
+            double e = exp(Gs[t] - Gs[s]);
+            double w = lt[l] * e;
+            double* dks = dkk + ((b * T + s) * G + g) * dk;
+            double* dvs = dvv + ((b * T + s) * H + h) * dv;
+            for (long i = 0; i < dk; i++) {
+              dqt[i] += w * dov * ks[i];
+              dks[i] += w * dov * qt[i];
+            }
+            for (long j = 0; j < dv; j++) dvs[j] += w * qk * dot_[j];
+            dlt[l] += e * qk * dov;
+            /* A_ts counts for every r with s < r <= t */
+            if (s + 1 <= t) {
+              run += w * qk * dov;
+              dloga[s + 1] += run;
+            }
+          }
+        }
+        for (long r = 0; r < T; r++) da[(b * T + r) * H + h] = dloga[r] / a[(b * T + r) * H + h];
+      }
+      free(Gs);
+      free(dloga);
+    }
+  }
+}

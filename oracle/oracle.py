@@ -17,6 +17,8 @@ file's header and above each C function.  Summary:
                             of the bucket states at position T.
 * ``form_r_head``           one head, capturing states at chosen positions.
 * ``brute``                 dense masks built by explicit loops (small T).
+* ``backward``              gradients of sum(dO * o) with respect to q, k, v, a
+                            and lambda: the chain rule on the quadratic form.
 """
 from __future__ import annotations
 
@@ -65,8 +67,9 @@ def _load():
             lib.oracle_form_r.argtypes = six + [_D] * 7 + [_l]
             lib.oracle_form_q_points.argtypes = [_l] * 4 + [_D] * 5 + [_L, _l, _D]
             lib.oracle_form_r_head.argtypes = [_l] * 4 + [_D] * 6 + [_l, _l, _L, _D]
+            lib.oracle_backward.argtypes = six + [_D] * 11
             for f in ("oracle_form_q", "oracle_brute", "oracle_form_r", "oracle_form_q_points",
-                      "oracle_form_r_head"):
+                      "oracle_form_r_head", "oracle_backward"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -178,3 +181,21 @@ def form_r_head(q, k, v, a, lam, cap_pos, levels: int):
     _load().oracle_form_r_head(T, dk, dv, L, _d(q), _d(k), _d(v), _d(a), _d(lam), _d(o),
                                levels, cap.size, cap.ctypes.data_as(_L), _d(st))
     return o, st
+
+
+def backward(q, k, v, a, lam, dO):
+    """Gradients of sum(dO * form_q(q, k, v, a, lam)): returns dq, dk (B, T, G, dk),
+    dv (B, T, H, dv), da (B, T, H) and dlam (B, T, H, L), all fp64."""
+    q, k, v, a, lam, shp = _check(q, k, v, a, lam)
+    dO = _f64(dO)
+    B, T, H, hpg, dk, dv, L = shp
+    G = H // hpg
+    assert dO.shape == (B, T, H, dv)
+    dq = np.zeros((B, T, G, dk))
+    dkk = np.zeros((B, T, G, dk))
+    dvv = np.zeros((B, T, H, dv))
+    da = np.zeros((B, T, H))
+    dl = np.zeros((B, T, H, L))
+    _load().oracle_backward(*shp, _d(q), _d(k), _d(v), _d(a), _d(lam), _d(dO), _d(dq), _d(dkk),
+                            _d(dvv), _d(da), _d(dl))
+    return dq, dkk, dvv, da, dl
