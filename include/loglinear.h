@@ -176,6 +176,38 @@ ll_status loglinear_fwd_static_workspace(const ll_shape* shape, const void* q, c
                                          void* o, float* states_out, float* state_logscale_out,
                                          int state_levels, void* stream);
 
+/* ---- backward -------------------------------------------------------------------------
+ * The pages give no backward; this is the chain rule on the forward's masked form
+ * o_t = sum_{s<=t} lambda_t^{l(t,s)} M^S(t,s) (q_t . k_s) v_s (write-up sections
+ * 特殊结构：树划分 and 对Mamba-2和门控的对数线性推广), laid out by the same chunks and
+ * Fenwick blocks as the forward (section 高效训练算法, Algorithm 1).
+ */
+
+/* Bytes of device workspace loglinear_bwd needs for this shape (0: invalid shape). */
+size_t loglinear_bwd_workspace_bytes(const ll_shape* shape);
+
+/*
+ * Gradients of the scalar sum(dO * o) where o = loglinear_fwd(q, k, v, a, lambda), for
+ * every shape loglinear_fwd accepts.  Inputs as for loglinear_fwd, plus
+ *   dO       (B, T, H, d_v)  dtype
+ * and the outputs, all written (no accumulation into them):
+ *   dq, dk   (B, T, G, d_k)  dtype; the heads of a group add up
+ *   dv       (B, T, H, d_v)  dtype
+ *   dlog_a   (B, T, H)       fp32, the gradient with respect to log a, the form in which
+ *                            a enters the forward; the gradient with respect to a is
+ *                            dlog_a / a (badly conditioned for a near 0, hence not
+ *                            returned); 0 at t = 0, whose decay multiplies nothing
+ *   dlambda  (B, T, H, L)    fp32; levels with no bucket get 0
+ *   workspace >= loglinear_bwd_workspace_bytes(shape) bytes, 16-byte aligned, contents on
+ *            entry do not matter
+ * All arithmetic is fp32 on the CUDA cores.  The dk/dv terms of the levels above a
+ * chunk are summed with fp32 atomics, so results can differ between calls by rounding.
+ */
+ll_status loglinear_bwd(const ll_shape* shape, const void* q, const void* k, const void* v,
+                        const float* a, const float* lambda, const void* dO, void* dq, void* dk,
+                        void* dv, float* dlog_a, float* dlambda, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /* ---- comparators ---------------------------------------------------------------------
  * Two other ways to compute on the tensor-core shape (bf16, d_k = 128, d_v = 64,
  * T % 128 == 0), kept to measure the level-fused forward against.  Any other shape

@@ -357,18 +357,19 @@ void oracle_brute(long B, long T, long H, long hpg, long dk, long dv, long L,
  *   dlam_t^{l(t,s)} += e_ts (q_t . k_s) (dO_t . v_s),
  *   d(log a_r) = sum over t >= r and s < r of A_ts (log a_r enters e_ts exactly
  *     for s < r <= t), summed here for each t over r = 1..t with a running sum
- *     over s < r;  da_r = d(log a_r) / a_r.
+ *     over s < r.  This gradient with respect to log a is returned (the one with
+ *     respect to a is d(log a_r) / a_r).
  * Outputs are overwritten.  One group at a time (its heads share dq, dk).
  * ------------------------------------------------------------------------- */
 void oracle_backward(long B, long T, long H, long hpg, long dk, long dv, long L,
                      const double* q, const double* k, const double* v, const double* a,
                      const double* lam, const double* dO, double* dq, double* dkk, double* dvv,
-                     double* da, double* dlam) {
+                     double* dloga_out, double* dlam) {
   long G = H / hpg;
   memset(dq, 0, sizeof(double) * (size_t)(B * T * G * dk));
   memset(dkk, 0, sizeof(double) * (size_t)(B * T * G * dk));
   memset(dvv, 0, sizeof(double) * (size_t)(B * T * H * dv));
-  memset(da, 0, sizeof(double) * (size_t)(B * T * H));
+  memset(dloga_out, 0, sizeof(double) * (size_t)(B * T * H));
   memset(dlam, 0, sizeof(double) * (size_t)(B * T * H * L));
 #pragma omp parallel for collapse(2) schedule(dynamic)
   for (long b = 0; b < B; b++) {
@@ -413,7 +414,7 @@ void oracle_backward(long B, long T, long H, long hpg, long dk, long dv, long L,
             }
           }
         }
-        for (long r = 0; r < T; r++) da[(b * T + r) * H + h] = dloga[r] / a[(b * T + r) * H + h];
+        for (long r = 0; r < T; r++) dloga_out[(b * T + r) * H + h] = dloga[r];
       }
       free(Gs);
       free(dloga);

@@ -17,8 +17,8 @@ file's header and above each C function.  Summary:
                             of the bucket states at position T.
 * ``form_r_head``           one head, capturing states at chosen positions.
 * ``brute``                 dense masks built by explicit loops (small T).
-* ``backward``              gradients of sum(dO * o) with respect to q, k, v, a
-                            and lambda: the chain rule on the quadratic form.
+* ``backward``              gradients of sum(dO * o) with respect to q, k, v,
+                            log a and lambda: the chain rule on the quadratic form.
 """
 from __future__ import annotations
 
@@ -185,7 +185,8 @@ def form_r_head(q, k, v, a, lam, cap_pos, levels: int):
 
 def backward(q, k, v, a, lam, dO):
     """Gradients of sum(dO * form_q(q, k, v, a, lam)): returns dq, dk (B, T, G, dk),
-    dv (B, T, H, dv), da (B, T, H) and dlam (B, T, H, L), all fp64."""
+    dv (B, T, H, dv), dloga (B, T, H: with respect to log a; divide by a for the
+    gradient with respect to a) and dlam (B, T, H, L), all fp64."""
     q, k, v, a, lam, shp = _check(q, k, v, a, lam)
     dO = _f64(dO)
     B, T, H, hpg, dk, dv, L = shp
@@ -194,8 +195,8 @@ def backward(q, k, v, a, lam, dO):
     dq = np.zeros((B, T, G, dk))
     dkk = np.zeros((B, T, G, dk))
     dvv = np.zeros((B, T, H, dv))
-    da = np.zeros((B, T, H))
+    dla = np.zeros((B, T, H))
     dl = np.zeros((B, T, H, L))
     _load().oracle_backward(*shp, _d(q), _d(k), _d(v), _d(a), _d(lam), _d(dO), _d(dq), _d(dkk),
-                            _d(dvv), _d(da), _d(dl))
-    return dq, dkk, dvv, da, dl
+                            _d(dvv), _d(dla), _d(dl))
+    return dq, dkk, dvv, dla, dl

@@ -93,6 +93,10 @@ def lib() -> ctypes.CDLL:
             L.loglinear_fwd_naive.argtypes = [_SP] + [_vp] * 7 + [ctypes.c_size_t, _vp]
             L.ssd_fwd_workspace_bytes.restype = ctypes.c_size_t
             L.ssd_fwd_workspace_bytes.argtypes = [_SP]
+            L.loglinear_bwd_workspace_bytes.restype = ctypes.c_size_t
+            L.loglinear_bwd_workspace_bytes.argtypes = [_SP]
+            L.loglinear_bwd.restype = ctypes.c_int
+            L.loglinear_bwd.argtypes = [_SP] + [_vp] * 12 + [ctypes.c_size_t, _vp]
             L.ssd_fwd.restype = ctypes.c_int
             L.ssd_fwd.argtypes = [_SP] + [_vp] * 6 + [ctypes.c_size_t, _vp]
             _lib = L
@@ -205,6 +209,23 @@ def loglinear_fwd_static_workspace(q, k, v, a, lam, chunk: int = 64, o=None, sta
                                               _stream_ptr(stream))
     _check(st, "loglinear_fwd_static_workspace")
     return o
+
+
+def loglinear_bwd(q, k, v, a, lam, dO, chunk: int = 64, workspace=None, stream=None):
+    """Gradients of sum(dO * loglinear_fwd(q, k, v, a, lam)): returns dq, dk (B, T, G, d_k)
+    and dv (B, T, H, d_v) in the input dtype, dlog_a (B, T, H; with respect to log a) and
+    dlam (B, T, H, L) in fp32."""
+    shape = fwd_shape(q, v, lam, chunk)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dloga, dlam = torch.empty_like(a), torch.empty_like(lam)
+    nb = int(lib().loglinear_bwd_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None:
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
+    st = lib().loglinear_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(lam),
+                             _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dloga), _ptr(dlam),
+                             _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(st, "loglinear_bwd")
+    return dq, dk, dv, dloga, dlam
 
 
 def loglinear_fwd_naive(q, k, v, a, lam, chunk: int = 64, o=None, workspace=None, stream=None):

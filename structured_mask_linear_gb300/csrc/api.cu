@@ -264,6 +264,32 @@ ll_status ssd_fwd(const ll_shape* s, const void* q, const void* k, const void* v
   return ll::launch_tc_ssd(tp, fa, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
+size_t loglinear_bwd_workspace_bytes(const ll_shape* s) {
+  if (check_fwd_shape(s) != LL_OK) return 0;
+  return ll::bwd_workspace_bytes(*s);
+}
+
+ll_status loglinear_bwd(const ll_shape* s, const void* q, const void* k, const void* v,
+                        const float* a, const float* lambda, const void* dO, void* dq, void* dk,
+                        void* dv, float* dlog_a, float* dlambda, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  ll_status st = check_fwd_shape(s);
+  if (st != LL_OK) return st;
+  if (!q || !k || !v || !a || !lambda || !dO || !dq || !dk || !dv || !dlog_a || !dlambda)
+    return LL_ERR_NULL;
+  const void* ptrs[] = {q, k, v, a, lambda, dO, dq, dk, dv, dlog_a, dlambda, workspace};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return LL_ERR_ALIGN;
+  const size_t need = ll::bwd_workspace_bytes(*s);
+  if (need == 0) return LL_ERR_SHAPE;
+  if (!workspace || workspace_bytes < need) return LL_ERR_WORKSPACE;
+  unsigned* sw = status_word();
+  if (!sw) return LL_ERR_CUDA;
+  cudaError_t e = ll::launch_bwd(*s, q, k, v, a, lambda, dO, dq, dk, dv, dlog_a, dlambda,
+                                 static_cast<char*>(workspace), sw, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
 ll_status loglinear_check_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LL_ERR_CUDA;
   unsigned v = 0, zero = 0;

@@ -45,6 +45,14 @@ void note_launch();
 
 
 cudaError_t launch_generic_fwd(const GenPlan& p, bool bf16, const FwdArgs& a, cudaStream_t st);
+// Only the chunk states and Fenwick blocks of the generic forward (for the backward).
+cudaError_t launch_generic_states(const GenPlan& p, bool bf16, const FwdArgs& a, cudaStream_t st);
+
+// Backward (csrc/backward.cu): workspace bytes (0: unsupported) and the launches.
+size_t bwd_workspace_bytes(const ll_shape& s);
+cudaError_t launch_bwd(const ll_shape& s, const void* q, const void* k, const void* v, const float* a,
+                       const float* lam, const void* dO, void* dq, void* dk, void* dv, float* dloga,
+                       float* dlam, char* ws, unsigned* status, cudaStream_t st);
 
 struct DecodeArgs {
   int B, H, hpg, G, dk, dv, L;

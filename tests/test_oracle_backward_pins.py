@@ -34,7 +34,8 @@ def test_backward_matches_finite_differences(T, H, hpg):
     dk, dv = 3, 2
     L = (T - 1).bit_length() + 2  # one level more than T needs: its gradient is zero
     x = list(_inputs(rng, 1, T, H, hpg, dk, dv, L))
-    grads = oracle.backward(*x)
+    dq, dkk, dvv, dla, dl = oracle.backward(*x)
+    grads = [dq, dkk, dvv, dla / x[3], dl]  # the finite differences below move a itself
     eps = 1e-6
     for idx in range(5):  # q, k, v, a, lam
         base = x[idx]
@@ -50,6 +51,18 @@ def test_backward_matches_finite_differences(T, H, hpg):
         np.testing.assert_allclose(grads[idx], num, rtol=1e-6, atol=1e-7,
                                    err_msg=["dq", "dk", "dv", "da", "dlam"][idx])
     assert np.all(grads[4][..., (T - 1).bit_length() + 1:] == 0.0)
+    # in log space: a -> a * exp(+-eps) moves log a by +-eps
+    num = np.zeros_like(dla)
+    a0 = x[3].copy()
+    for pos in np.ndindex(a0.shape):
+        x[3] = a0.copy()
+        x[3][pos] = a0[pos] * np.exp(eps)
+        fp = _loss(*x)
+        x[3][pos] = a0[pos] * np.exp(-eps)
+        fm = _loss(*x)
+        num[pos] = (fp - fm) / (2 * eps)
+    x[3] = a0
+    np.testing.assert_allclose(dla, num, rtol=1e-6, atol=1e-7, err_msg="dloga")
 
 
 def test_euler_identity_for_lambda():
@@ -64,13 +77,13 @@ def test_euler_identity_for_lambda():
 def test_linear_attention_special_case():
     """lambda = 1, a = 1: o = tril(Q Kᵀ) V per head, so dq = tril(dO Vᵀ) K,
     dk = tril(dO Vᵀ)ᵀ Q, dv = tril(Q Kᵀ)ᵀ dO, and d(log a_r) = sum over t >= r, s < r of
-    (q_t . k_s)(dO_t . v_s), i.e. da_r for a = 1."""
+    (q_t . k_s)(dO_t . v_s)."""
     rng = np.random.default_rng(9)
     T, dk, dv, L = 21, 5, 3, 6
     q, k, v, _, _, dO = _inputs(rng, 1, T, 1, 1, dk, dv, L)
     a = np.ones((1, T, 1))
     lam = np.ones((1, T, 1, L))
-    dq, dkk, dvv, da, _ = oracle.backward(q, k, v, a, lam, dO)
+    dq, dkk, dvv, dla, _ = oracle.backward(q, k, v, a, lam, dO)
     Q, K, V, D = q[0, :, 0], k[0, :, 0], v[0, :, 0], dO[0, :, 0]
     mask = np.tril(np.ones((T, T)))
     P = mask * (Q @ K.T)
@@ -80,4 +93,4 @@ def test_linear_attention_special_case():
     np.testing.assert_allclose(dvv[0, :, 0], P.T @ D, rtol=1e-12, atol=1e-12)
     A = P * (D @ V.T)
     want = np.array([A[r:, :r].sum() for r in range(T)])
-    np.testing.assert_allclose(da[0, :, 0], want, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dla[0, :, 0], want, rtol=1e-12, atol=1e-12)
