@@ -351,6 +351,7 @@ def main():
         line["long"] = long_measure(sml, torch, dev)
         line["decode"] = decode_measure(sml, torch, dev, hbm_peak)
         line["comparators"] = comparators_measure(sml, torch, x, w, ms)
+        line["backward"] = backward_measure(sml, torch, x, w, hbm_peak)
     else:
         line["e2e"] = e2e_measure(sml, torch, x, w, dev, min(args.steps, 10))
         if world > 1:
@@ -387,6 +388,41 @@ def e2e_measure(sml, torch, x, w, dev, steps):
     return {"value": w.batch * w.T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps,
             "api": "loglinear_fwd_host (pinned host buffers)"}
+
+
+def backward_measure(sml, torch, x, w, hbm_peak, steps=3):
+    """loglinear_bwd on the same workload (gradients of sum(dO * o) for q, k, v, log a,
+    lambda), CUDA events around whole calls, inputs in HBM.  Algorithmic bytes: q, k, v,
+    a, lambda, dO read once; dq, dk, dv, d(log a), dlambda written once."""
+    gen = torch.Generator(device=x.v.device)
+    gen.manual_seed(5)
+    dO = torch.randn(x.v.shape, generator=gen, device=x.v.device).to(x.v.dtype)
+    shape = sml.fwd_shape(x.q, x.v, x.lam, w.chunk)
+    ws = torch.empty(sml.lib().loglinear_bwd_workspace_bytes(ctypes.byref(shape)), dtype=torch.uint8,
+                     device=x.v.device)
+    call = lambda: sml.loglinear_bwd(x.q, x.k, x.v, x.a, x.lam, dO, chunk=w.chunk, workspace=ws)
+    call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    if sml.loglinear_check_status() != 0:
+        raise RuntimeError("device status error in the backward")
+    ms = e0.elapsed_time(e1) / steps
+    el = lambda t: t.numel() * t.element_size()
+    nbytes = 2 * (el(x.q) + el(x.k) + el(x.v) + el(x.a) + el(x.lam)) + el(dO)
+    res = {"workload": workload_desc(w), "ms_per_step": ms, "unit": "tokens/s",
+           "value": w.batch * w.T / (ms / 1e3), "steps": steps,
+           "path": "CUDA cores, fp32 (csrc/backward.cu)",
+           "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": hbm_peak,
+                        "unit": "GB/s", "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
+                        "algorithmic_bytes_per_step": nbytes}}
+    del ws, dO
+    torch.cuda.empty_cache()
+    return res
 
 
 def comparators_measure(sml, torch, x, w, fused_ms, steps=5):

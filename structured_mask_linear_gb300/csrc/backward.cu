@@ -66,50 +66,60 @@ struct BwdArgs {
 template <typename TIn>
 __global__ void __launch_bounds__(kT) bwd_intra(GenPlan p, BwdArgs x, size_t off_dq, size_t off_dk,
                                                size_t off_dv) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   const int C = p.C, dk = p.dk, dv = p.dv, L = p.L, nl = p.clog + 1;
-  const int j = blockIdx.x, bh = blockIdx.y;
+  const int j = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
   const int b = bh / p.H, h = bh % p.H, grp = h / p.hpg;
   const long long t0 = (long long)j * C;
-  float* qs = sm;               // C * dk
-  float* ks = qs + C * dk;      // C * dk
-  float* vs = ks + C * dk;      // C * dv
-  float* ds = vs + C * dv;      // C * dv  (dO)
+  float* qs = sm;               // C x dk
+  float* ks = qs + C * dk;      // C x dk
+  float* kTr = ks + C * dk;     // dk x C
+  float* vTr = kTr + C * dk;    // dv x C
+  float* ds = vTr + C * dv;     // C x dv  (dO)
   float* gs = ds + C * dv;      // C
-  float* ls = gs + C;           // C * nl  (lambda of the in-chunk levels)
-  float* dS = ls + C * nl;      // C * C: w (dO . v)
-  float* P = dS + C * C;        // C * C: w (q . k)
-  float* X = P + C * C;         // C * C: 2^(g_t - g_s) (q . k)(dO . v)
+  float* ls = gs + C;           // C x nl  (lambda of the in-chunk levels)
+  float* dS = ls + C * nl;      // C x C: dO.v, then w (dO . v)
+  float* P = dS + C * C;        // C x C: q.k, then w (q . k)
+  float* X = P + C * C;         // C x C: 2^(g_t - g_s) (q . k)(dO . v)
   const TIn* q = static_cast<const TIn*>(x.q);
   const TIn* k = static_cast<const TIn*>(x.k);
   const TIn* v = static_cast<const TIn*>(x.v);
   const TIn* dO = static_cast<const TIn*>(x.dO);
-  for (int e = threadIdx.x; e < C * dk; e += kT) {
+  for (int e = tid; e < C * dk; e += kT) {
     const int s = e / dk, i = e % dk;
     const size_t gi = (((size_t)b * p.T + t0 + s) * p.G + grp) * dk + i;
     qs[e] = ll_load(q, gi);
-    ks[e] = ll_load(k, gi);
+    const float kv = ll_load(k, gi);
+    ks[e] = kv;
+    kTr[i * C + s] = kv;
   }
-  for (int e = threadIdx.x; e < C * dv; e += kT) {
+  for (int e = tid; e < C * dv; e += kT) {
     const int s = e / dv, jv = e % dv;
     const size_t gi = (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv;
-    vs[e] = ll_load(v, gi);
+    vTr[jv * C + s] = ll_load(v, gi);
     ds[e] = ll_load(dO, gi);
   }
   const float* g = reinterpret_cast<const float*>(x.ws + p.off_g) + (size_t)bh * p.T + t0;
-  for (int s = threadIdx.x; s < C; s += kT) gs[s] = g[s];
-  for (int e = threadIdx.x; e < C * nl; e += kT) {
+  for (int s = tid; s < C; s += kT) gs[s] = g[s];
+  for (int e = tid; e < C * nl; e += kT) {
     const int t = e / nl, l = e % nl;
     ls[e] = x.lam[(((size_t)b * p.T + t0 + t) * p.H + h) * L + l];
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < C * C; e += kT) {
+  smem_mm(C, C, dk, qs, dk, 1, kTr, C, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+    for (int i = 0; i < 4; ++i)
+      for (int jj = 0; jj < 4; ++jj) P[(m0 + i) * C + n0 + jj] = acc[i][jj];
+  });
+  smem_mm(C, C, dv, ds, dv, 1, vTr, C, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+    for (int i = 0; i < 4; ++i)
+      for (int jj = 0; jj < 4; ++jj) dS[(m0 + i) * C + n0 + jj] = acc[i][jj];
+  });
+  __syncthreads();
+  for (int e = tid; e < C * C; e += kT) {
     const int t = e / C, s = e % C;
     float a1 = 0.f, a2 = 0.f, a3 = 0.f;
     if (s <= t) {
-      float qk = 0.f, dov = 0.f;
-      for (int i = 0; i < dk; ++i) qk += qs[t * dk + i] * ks[s * dk + i];
-      for (int jv = 0; jv < dv; ++jv) dov += ds[t * dv + jv] * vs[s * dv + jv];
+      const float qk = P[e], dov = dS[e];
       const float ed = exp2f(gs[t] - gs[s]);
       const float w = ls[t * nl + bit_length(t ^ s)] * ed;
       a1 = w * dov;
@@ -124,53 +134,55 @@ __global__ void __launch_bounds__(kT) bwd_intra(GenPlan p, BwdArgs x, size_t off
   float* dq32 = reinterpret_cast<float*>(x.ws + off_dq);
   float* dk32 = reinterpret_cast<float*>(x.ws + off_dk);
   float* dv32 = reinterpret_cast<float*>(x.ws + off_dv);
-  for (int e = threadIdx.x; e < C * dk; e += kT) {
-    const int r = e / dk, i = e % dk;
-    float aq = 0.f, ak = 0.f;
-    for (int s = 0; s <= r; ++s) aq += dS[r * C + s] * ks[s * dk + i];  // r as query
-    for (int t = r; t < C; ++t) ak += dS[t * C + r] * qs[t * dk + i];   // r as key
-    const size_t o = (((size_t)b * p.T + t0 + r) * p.H + h) * dk + i;
-    dq32[o] = aq;
-    dk32[o] = ak;
-  }
-  for (int e = threadIdx.x; e < C * dv; e += kT) {
-    const int r = e / dv, jv = e % dv;
-    float av = 0.f;
-    for (int t = r; t < C; ++t) av += P[t * C + r] * ds[t * dv + jv];
-    dv32[(((size_t)b * p.T + t0 + r) * p.H + h) * dv + jv] = av;
-  }
-  for (int e = threadIdx.x; e < C * L; e += kT) {
+  auto row = [&](int r) { return ((size_t)b * p.T + t0 + r) * p.H + h; };
+  // dq = dS K (rows: queries); dk = dSᵀ Q and dv = Pᵀ dO (rows: keys)
+  smem_mm(C, dk, C, dS, C, 1, ks, dk, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(dq32 + row(m0 + i) * dk + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  });
+  smem_mm(C, dk, C, dS, 1, C, qs, dk, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(dk32 + row(m0 + i) * dk + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  });
+  smem_mm(C, dv, C, P, 1, C, ds, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(dv32 + row(m0 + i) * dv + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  });
+  for (int e = tid; e < C * L; e += kT) {
     const int t = e / L, l = e % L;
     float acc = 0.f;
     if (l < nl)
       for (int s = 0; s <= t; ++s)
         if (bit_length(t ^ s) == l) acc += X[t * C + s];
-    x.dlam[(((size_t)b * p.T + t0 + t) * p.H + h) * L + l] = acc;  // inter levels: next kernel
+    x.dlam[row(t) * L + l] = acc;  // inter levels: next kernel
   }
 }
 
 // ---- query side of the inter-chunk levels ---------------------------------------------
 template <typename TIn>
 __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t off_dq, size_t off_dual) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   const int C = p.C, dk = p.dk, dv = p.dv, L = p.L;
-  const int j = blockIdx.x, bh = blockIdx.y;
+  const int j = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
   if (j == 0) return;  // the first chunk reads no block
   const int b = bh / p.H, h = bh % p.H, grp = h / p.hpg;
   const long long t0 = (long long)j * C;
   const int S = dk * dv;
-  float* qs = sm;            // C * dk
-  float* ds = qs + C * dk;   // C * dv
-  float* Bm = ds + C * dv;   // dk * dv: the block
-  float* ws_ = Bm + S;       // C: 2^(g_t + D) of this level
+  float* qs = sm;            // C x dk
+  float* ds = qs + C * dk;   // C x dv
+  float* Bm = ds + C * dv;   // dk x dv: the block
+  float* BT = Bm + S;        // dv x dk: its transpose
+  float* qw = BT + S;        // C x dk: w_t q_t
+  float* U = qw + C * dk;    // C x dv: q_tᵀ Bm
+  float* ws_ = U + C * dv;   // C: 2^(g_t + D) of this level
   float* wl = ws_ + C;       // C: lambda_t^l 2^(g_t + D)
   const TIn* q = static_cast<const TIn*>(x.q);
   const TIn* dO = static_cast<const TIn*>(x.dO);
-  for (int e = threadIdx.x; e < C * dk; e += kT) {
+  for (int e = tid; e < C * dk; e += kT) {
     const int s = e / dk, i = e % dk;
     qs[e] = ll_load(q, (((size_t)b * p.T + t0 + s) * p.G + grp) * dk + i);
   }
-  for (int e = threadIdx.x; e < C * dv; e += kT) {
+  for (int e = tid; e < C * dv; e += kT) {
     const int s = e / dv, jv = e % dv;
     ds[e] = ll_load(dO, (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv);
   }
@@ -179,44 +191,56 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
   const float* blkG = reinterpret_cast<const float*>(x.ws + p.off_blkG) + (size_t)bh * p.nblk;
   float* dq32 = reinterpret_cast<float*>(x.ws + off_dq);
   float* dual = reinterpret_cast<float*>(x.ws + off_dual);
+  auto row = [&](int r) { return ((size_t)b * p.T + t0 + r) * p.H + h; };
   float D = 0.f;
   for (int m = 0; (j >> m) > 0; ++m) {
     if (!((j >> m) & 1)) continue;
     const int bidx = p.blk_off[m] + (((j >> m) - 1) >> 1);
     const int lvl = p.clog + 1 + m;
-    __syncthreads();  // previous level done with Bm, ws_, wl
+    __syncthreads();  // the previous level is done with the buffers
     const float* Bsrc = blk + ((size_t)bh * p.nblk + bidx) * S;
-    for (int e = threadIdx.x; e < S; e += kT) Bm[e] = Bsrc[e];
-    for (int t = threadIdx.x; t < C; t += kT) {
+    for (int e = tid; e < S; e += kT) {
+      const float bv = Bsrc[e];
+      Bm[e] = bv;
+      BT[(e % dv) * dk + e / dv] = bv;
+    }
+    for (int t = tid; t < C; t += kT) {
       const float e2 = exp2f(g[t] + D);
       ws_[t] = e2;
-      wl[t] = x.lam[(((size_t)b * p.T + t0 + t) * p.H + h) * L + lvl] * e2;
+      wl[t] = x.lam[row(t) * L + lvl] * e2;
     }
     __syncthreads();
-    // dq_t += w_t Bm dO_t
-    for (int e = threadIdx.x; e < C * dk; e += kT) {
-      const int t = e / dk, i = e % dk;
-      float acc = 0.f;
-      for (int jv = 0; jv < dv; ++jv) acc += Bm[i * dv + jv] * ds[t * dv + jv];
-      dq32[(((size_t)b * p.T + t0 + t) * p.H + h) * dk + i] += wl[t] * acc;
-    }
-    // dlambda_t^lvl = 2^(g_t + D) q_tᵀ Bm dO_t
-    for (int t = threadIdx.x; t < C; t += kT) {
-      float acc = 0.f;
-      for (int jv = 0; jv < dv; ++jv) {
-        float u = 0.f;
-        for (int i = 0; i < dk; ++i) u += qs[t * dk + i] * Bm[i * dv + jv];
-        acc += u * ds[t * dv + jv];
+    for (int e = tid; e < C * dk; e += kT) qw[e] = wl[e / dk] * qs[e];
+    // dq_t += w_t Bm dO_t ;  U = Q Bm
+    smem_mm(C, dk, dv, ds, dv, 1, BT, dk, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+      for (int i = 0; i < 4; ++i) {
+        float4* d4 = reinterpret_cast<float4*>(dq32 + row(m0 + i) * dk + n0);
+        float4 o4 = *d4;
+        const float w = wl[m0 + i];
+        o4.x += w * acc[i][0];
+        o4.y += w * acc[i][1];
+        o4.z += w * acc[i][2];
+        o4.w += w * acc[i][3];
+        *d4 = o4;
       }
-      x.dlam[(((size_t)b * p.T + t0 + t) * p.H + h) * L + lvl] = ws_[t] * acc;
-    }
-    // dual of the block: sum_t w_t q_t dO_tᵀ
+    });
+    smem_mm(C, dv, dk, qs, dk, 1, Bm, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+      for (int i = 0; i < 4; ++i)
+        for (int jj = 0; jj < 4; ++jj) U[(m0 + i) * dv + n0 + jj] = acc[i][jj];
+    });
+    __syncthreads();  // qw and U complete
+    // dual of the block: sum_t w_t q_t dO_tᵀ, added to the sums of the other readers
     float* dst = dual + ((size_t)bh * p.nblk + bidx) * S;
-    for (int e = threadIdx.x; e < S; e += kT) {
-      const int i = e / dv, jv = e % dv;
+    smem_mm(dk, dv, C, qw, 1, dk, ds, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+      for (int i = 0; i < 4; ++i)
+        atomicAdd(reinterpret_cast<float4*>(dst + (m0 + i) * dv + n0),
+                  make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+    });
+    // dlambda_t^lvl = 2^(g_t + D) q_tᵀ Bm dO_t
+    for (int t = tid; t < C; t += kT) {
       float acc = 0.f;
-      for (int t = 0; t < C; ++t) acc += wl[t] * qs[t * dk + i] * ds[t * dv + jv];
-      atomicAdd(dst + e, acc);
+      for (int jv = 0; jv < dv; ++jv) acc += U[t * dv + jv] * ds[t * dv + jv];
+      x.dlam[row(t) * L + lvl] = ws_[t] * acc;
     }
     D += blkG[bidx];
   }
@@ -226,23 +250,24 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
 template <typename TIn>
 __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t off_dk, size_t off_dv,
                                                   size_t off_dual) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   const int C = p.C, dk = p.dk, dv = p.dv;
-  const int u = blockIdx.x, bh = blockIdx.y;
+  const int u = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
   const int b = bh / p.H, h = bh % p.H, grp = h / p.hpg;
   const long long t0 = (long long)u * C;
   const int S = dk * dv;
-  float* ks = sm;            // C * dk
-  float* vs = ks + C * dk;   // C * dv
-  float* Dm = vs + C * dv;   // dk * dv: the dual
-  float* ts = Dm + S;        // C: 2^(decay from key s to the end of the block)
+  float* ks = sm;            // C x dk
+  float* vs = ks + C * dk;   // C x dv
+  float* Dm = vs + C * dv;   // dk x dv: the dual
+  float* DT = Dm + S;        // dv x dk: its transpose
+  float* ts = DT + S;        // C: 2^(decay from key s to the end of the block)
   const TIn* k = static_cast<const TIn*>(x.k);
   const TIn* v = static_cast<const TIn*>(x.v);
-  for (int e = threadIdx.x; e < C * dk; e += kT) {
+  for (int e = tid; e < C * dk; e += kT) {
     const int s = e / dk, i = e % dk;
     ks[e] = ll_load(k, (((size_t)b * p.T + t0 + s) * p.G + grp) * dk + i);
   }
-  for (int e = threadIdx.x; e < C * dv; e += kT) {
+  for (int e = tid; e < C * dv; e += kT) {
     const int s = e / dv, jv = e % dv;
     vs[e] = ll_load(v, (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv);
   }
@@ -251,6 +276,7 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
   const float* dual = reinterpret_cast<const float*>(x.ws + off_dual);
   float* dk32 = reinterpret_cast<float*>(x.ws + off_dk);
   float* dv32 = reinterpret_cast<float*>(x.ws + off_dv);
+  auto row = [&](int r) { return ((size_t)b * p.T + t0 + r) * p.H + h; };
   const float gend = g[C - 1];
   for (int m = 0; m < p.M; ++m) {
     const int i = u >> m;
@@ -260,23 +286,40 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
     const int bidx = p.blk_off[m] + (i >> 1);
     float tail = 0.f;  // decay of the chunks after u up to the end of node (m, i)
     for (int c = u + 1; c < ((i + 1) << m); ++c) tail += gamma[c];
-    __syncthreads();  // previous level done with Dm, ts
+    __syncthreads();  // the previous level is done with the buffers
     const float* src = dual + ((size_t)bh * p.nblk + bidx) * S;
-    for (int e = threadIdx.x; e < S; e += kT) Dm[e] = src[e];
-    for (int s = threadIdx.x; s < C; s += kT) ts[s] = exp2f(gend - g[s] + tail);
+    for (int e = tid; e < S; e += kT) {
+      const float dvl = src[e];
+      Dm[e] = dvl;
+      DT[(e % dv) * dk + e / dv] = dvl;
+    }
+    for (int s = tid; s < C; s += kT) ts[s] = exp2f(gend - g[s] + tail);
     __syncthreads();
-    for (int e = threadIdx.x; e < C * dk; e += kT) {
-      const int s = e / dk, ii = e % dk;
-      float acc = 0.f;
-      for (int jv = 0; jv < dv; ++jv) acc += Dm[ii * dv + jv] * vs[s * dv + jv];
-      dk32[(((size_t)b * p.T + t0 + s) * p.H + h) * dk + ii] += ts[s] * acc;
-    }
-    for (int e = threadIdx.x; e < C * dv; e += kT) {
-      const int s = e / dv, jv = e % dv;
-      float acc = 0.f;
-      for (int ii = 0; ii < dk; ++ii) acc += Dm[ii * dv + jv] * ks[s * dk + ii];
-      dv32[(((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv] += ts[s] * acc;
-    }
+    // dk_s += t_s Dual v_s ;  dv_s += t_s Dualᵀ k_s
+    smem_mm(C, dk, dv, vs, dv, 1, DT, dk, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+      for (int r = 0; r < 4; ++r) {
+        float4* d4 = reinterpret_cast<float4*>(dk32 + row(m0 + r) * dk + n0);
+        float4 o4 = *d4;
+        const float w = ts[m0 + r];
+        o4.x += w * acc[r][0];
+        o4.y += w * acc[r][1];
+        o4.z += w * acc[r][2];
+        o4.w += w * acc[r][3];
+        *d4 = o4;
+      }
+    });
+    smem_mm(C, dv, dk, ks, dk, 1, Dm, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+      for (int r = 0; r < 4; ++r) {
+        float4* d4 = reinterpret_cast<float4*>(dv32 + row(m0 + r) * dv + n0);
+        float4 o4 = *d4;
+        const float w = ts[m0 + r];
+        o4.x += w * acc[r][0];
+        o4.y += w * acc[r][1];
+        o4.z += w * acc[r][2];
+        o4.w += w * acc[r][3];
+        *d4 = o4;
+      }
+    });
   }
 }
 
@@ -381,21 +424,21 @@ cudaError_t run_bwd(const BwdPlan& bp, const BwdArgs& x, const FwdArgs& fa, cuda
   if ((e = cudaMemsetAsync(x.ws + bp.off_dual, 0, sizeof(float) * (size_t)BH * p.nblk * dk * dv, st)) !=
       cudaSuccess)
     return e;
-  const size_t sm1 = sizeof(float) * ((size_t)2 * C * dk + 2 * C * dv + C + C * (p.clog + 1) + 3 * C * C);
+  const size_t sm1 = sizeof(float) * ((size_t)3 * C * dk + 2 * C * dv + C + C * (p.clog + 1) + 3 * C * C);
   if ((e = cudaFuncSetAttribute(bwd_intra<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) !=
       cudaSuccess)
     return e;
   bwd_intra<TIn><<<dim3(p.N, BH), kT, sm1, st>>>(p, x, bp.off_dq, bp.off_dk, bp.off_dv);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
-  const size_t sm2 = sizeof(float) * ((size_t)C * dk + C * dv + dk * dv + 2 * C);
+  const size_t sm2 = sizeof(float) * ((size_t)2 * C * dk + 2 * C * dv + 2 * dk * dv + 2 * C);
   if ((e = cudaFuncSetAttribute(bwd_inter_q<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) !=
       cudaSuccess)
     return e;
   bwd_inter_q<TIn><<<dim3(p.N, BH), kT, sm2, st>>>(p, x, bp.off_dq, bp.off_dual);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
-  const size_t sm3 = sizeof(float) * ((size_t)C * dk + C * dv + dk * dv + C);
+  const size_t sm3 = sizeof(float) * ((size_t)C * dk + C * dv + 2 * dk * dv + C);
   if ((e = cudaFuncSetAttribute(bwd_inter_kv<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) !=
       cudaSuccess)
     return e;

@@ -29,7 +29,7 @@ template <typename TIn>
 __global__ void __launch_bounds__(kThreads) gen_chunk_state(GenPlan p, const TIn* __restrict__ k,
                                                             const TIn* __restrict__ v,
                                                             const float* __restrict__ a, char* ws) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   const int C = p.C, dk = p.dk, dv = p.dv;
   float* ks = sm;
   float* vs = ks + C * dk;
@@ -60,12 +60,14 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(GenPlan p, const TIn
   if (threadIdx.x == 0) gamma[(size_t)bh * p.N + j] = gs[C - 1];
   const float gend = gs[C - 1];
   const int S = dk * dv;
-  for (int e = threadIdx.x; e < S; e += kThreads) {
-    int i = e / dv, jv = e % dv;
-    float acc = 0.f;
-    for (int s = 0; s < C; ++s) acc += exp2f(gend - gs[s]) * ks[s * dk + i] * vs[s * dv + jv];
-    Hst[((size_t)bh * p.N + j) * S + e] = acc;
-  }
+  // H_j = Kᵀ diag(2^(gend - g)) V: scale the keys once, then a tiled product
+  for (int e = threadIdx.x; e < C * dk; e += kThreads) ks[e] *= exp2f(gend - gs[e / dk]);
+  __syncthreads();
+  float* dst = Hst + ((size_t)bh * p.N + j) * S;
+  smem_mm(dk, dv, C, ks, 1, dk, vs, dv, threadIdx.x, kThreads, [&](int m0, int n0, float (&acc)[4][4]) {
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(dst + (m0 + i) * dv + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  });
 }
 
 __global__ void __launch_bounds__(kThreads) gen_blocks(GenPlan p, char* ws) {

@@ -106,6 +106,44 @@ __host__ __device__ inline int bit_length(long long x) {
 }  // namespace ll
 
 // ---- small device helpers -----------------------------------------------------
+// Shared-memory product on the CUDA cores, one 4 x 4 output tile per thread and step:
+// for every tile (m0, n0) of an M x N output (M, N multiples of 4) handed out to the
+// nthr threads in turn, acc[i][j] = sum_{k < K} A(m0+i, k) B(k, n0+j) with
+// A(m, k) = a[m*sam + k*sak] and B(k, n) = b[k*sbk + n] (b rows 16-byte aligned), then
+// epi(m0, n0, acc).  Threads of a warp share m0 where N/4 >= 32 (A is a broadcast) and
+// read consecutive float4s of B.
+template <typename Epi>
+__device__ __forceinline__ void smem_mm(int M, int N, int K, const float* a, int sam, int sak,
+                                        const float* b, int sbk, int tid, int nthr, Epi epi) {
+  const int tn_count = N >> 2;
+  const int tiles = (M >> 2) * tn_count;
+  for (int tile = tid; tile < tiles; tile += nthr) {
+    const int m0 = (tile / tn_count) << 2, n0 = (tile % tn_count) << 2;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    const float* ap = a + (size_t)m0 * sam;
+    const float* bp = b + n0;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+      const float4 bv = *reinterpret_cast<const float4*>(bp + (size_t)k * sbk);
+      float av[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = ap[i * sam + k * sak];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[i][0] += av[i] * bv.x;
+        acc[i][1] += av[i] * bv.y;
+        acc[i][2] += av[i] * bv.z;
+        acc[i][3] += av[i] * bv.w;
+      }
+    }
+    epi(m0, n0, acc);
+  }
+}
+
 __device__ __forceinline__ float ll_load(const float* p, size_t i) { return p[i]; }
 __device__ __forceinline__ float ll_load(const __nv_bfloat16* p, size_t i) {
   return __bfloat162float(p[i]);
