@@ -168,14 +168,14 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
   const int b = bh / p.H, h = bh % p.H, grp = h / p.hpg;
   const long long t0 = (long long)j * C;
   const int S = dk * dv;
-  float* qs = sm;            // C x dk
-  float* ds = qs + C * dk;   // C x dv
-  float* Bm = ds + C * dv;   // dk x dv: the block
-  float* BT = Bm + S;        // dv x dk: its transpose
-  float* qw = BT + S;        // C x dk: w_t q_t
-  float* U = qw + C * dk;    // C x dv: q_tᵀ Bm
-  float* ws_ = U + C * dv;   // C: 2^(g_t + D) of this level
-  float* wl = ws_ + C;       // C: lambda_t^l 2^(g_t + D)
+  float* qs = sm;              // C x dk
+  float* ds = qs + C * dk;     // C x dv   (dO)
+  float* dT = ds + C * dv;     // dv x C   (dOᵀ)
+  float* dw = dT + C * dv;     // C x dv   (w_t dO_t)
+  float* Bm = dw + C * dv;     // dk x dv: the block
+  float* ws_ = Bm + S;         // C: 2^(g_t + D) of this level
+  float* wl = ws_ + C;         // C: lambda_t^l 2^(g_t + D)
+  float* dl = wl + C;          // C: q_tᵀ Bm dO_t
   const TIn* q = static_cast<const TIn*>(x.q);
   const TIn* dO = static_cast<const TIn*>(x.dO);
   for (int e = tid; e < C * dk; e += kT) {
@@ -184,7 +184,9 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
   }
   for (int e = tid; e < C * dv; e += kT) {
     const int s = e / dv, jv = e % dv;
-    ds[e] = ll_load(dO, (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv);
+    const float d = ll_load(dO, (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv);
+    ds[e] = d;
+    dT[jv * C + s] = d;
   }
   const float* g = reinterpret_cast<const float*>(x.ws + p.off_g) + (size_t)bh * p.T + t0;
   const float* blk = reinterpret_cast<const float*>(x.ws + p.off_blk);
@@ -199,49 +201,45 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
     const int lvl = p.clog + 1 + m;
     __syncthreads();  // the previous level is done with the buffers
     const float* Bsrc = blk + ((size_t)bh * p.nblk + bidx) * S;
-    for (int e = tid; e < S; e += kT) {
-      const float bv = Bsrc[e];
-      Bm[e] = bv;
-      BT[(e % dv) * dk + e / dv] = bv;
-    }
+    for (int e = tid; e < S; e += kT) Bm[e] = Bsrc[e];
     for (int t = tid; t < C; t += kT) {
       const float e2 = exp2f(g[t] + D);
       ws_[t] = e2;
       wl[t] = x.lam[row(t) * L + lvl] * e2;
+      dl[t] = 0.f;
     }
     __syncthreads();
-    for (int e = tid; e < C * dk; e += kT) qw[e] = wl[e / dk] * qs[e];
-    // dq_t += w_t Bm dO_t ;  U = Q Bm
-    smem_mm(C, dk, dv, ds, dv, 1, BT, dk, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
-      for (int i = 0; i < 4; ++i) {
-        float4* d4 = reinterpret_cast<float4*>(dq32 + row(m0 + i) * dk + n0);
+    for (int e = tid; e < C * dv; e += kT) dw[e] = wl[e / dv] * ds[e];
+    // dqᵀ = Bm dOᵀ (rows i of d_k, columns t): dq_t += w_t (Bm dO_t)
+    smem_mm(dk, C, dv, Bm, dv, 1, dT, C, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+      for (int jj = 0; jj < 4; ++jj) {
+        const int t = n0 + jj;
+        float4* d4 = reinterpret_cast<float4*>(dq32 + row(t) * dk + m0);
         float4 o4 = *d4;
-        const float w = wl[m0 + i];
-        o4.x += w * acc[i][0];
-        o4.y += w * acc[i][1];
-        o4.z += w * acc[i][2];
-        o4.w += w * acc[i][3];
+        const float w = wl[t];
+        o4.x += w * acc[0][jj];
+        o4.y += w * acc[1][jj];
+        o4.z += w * acc[2][jj];
+        o4.w += w * acc[3][jj];
         *d4 = o4;
       }
     });
+    // U = Q Bm, reduced at once against dO: dl_t = q_tᵀ Bm dO_t
     smem_mm(C, dv, dk, qs, dk, 1, Bm, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
-      for (int i = 0; i < 4; ++i)
-        for (int jj = 0; jj < 4; ++jj) U[(m0 + i) * dv + n0 + jj] = acc[i][jj];
+      for (int i = 0; i < 4; ++i) {
+        const float* d = ds + (m0 + i) * dv + n0;
+        atomicAdd(dl + m0 + i, acc[i][0] * d[0] + acc[i][1] * d[1] + acc[i][2] * d[2] + acc[i][3] * d[3]);
+      }
     });
-    __syncthreads();  // qw and U complete
-    // dual of the block: sum_t w_t q_t dO_tᵀ, added to the sums of the other readers
+    __syncthreads();  // dw and dl complete
+    // dual of the block: sum_t q_t (w_t dO_t)ᵀ, added to the sums of the other readers
     float* dst = dual + ((size_t)bh * p.nblk + bidx) * S;
-    smem_mm(dk, dv, C, qw, 1, dk, ds, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+    smem_mm(dk, dv, C, qs, 1, dk, dw, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
       for (int i = 0; i < 4; ++i)
         atomicAdd(reinterpret_cast<float4*>(dst + (m0 + i) * dv + n0),
                   make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
     });
-    // dlambda_t^lvl = 2^(g_t + D) q_tᵀ Bm dO_t
-    for (int t = tid; t < C; t += kT) {
-      float acc = 0.f;
-      for (int jv = 0; jv < dv; ++jv) acc += U[t * dv + jv] * ds[t * dv + jv];
-      x.dlam[row(t) * L + lvl] = ws_[t] * acc;
-    }
+    for (int t = tid; t < C; t += kT) x.dlam[row(t) * L + lvl] = ws_[t] * dl[t];
     D += blkG[bidx];
   }
 }
@@ -257,10 +255,9 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
   const long long t0 = (long long)u * C;
   const int S = dk * dv;
   float* ks = sm;            // C x dk
-  float* vs = ks + C * dk;   // C x dv
-  float* Dm = vs + C * dv;   // dk x dv: the dual
-  float* DT = Dm + S;        // dv x dk: its transpose
-  float* ts = DT + S;        // C: 2^(decay from key s to the end of the block)
+  float* vT = ks + C * dk;   // dv x C  (Vᵀ)
+  float* Dm = vT + C * dv;   // dk x dv: the dual
+  float* ts = Dm + S;        // C: 2^(decay from key s to the end of the block)
   const TIn* k = static_cast<const TIn*>(x.k);
   const TIn* v = static_cast<const TIn*>(x.v);
   for (int e = tid; e < C * dk; e += kT) {
@@ -269,7 +266,7 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
   }
   for (int e = tid; e < C * dv; e += kT) {
     const int s = e / dv, jv = e % dv;
-    vs[e] = ll_load(v, (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv);
+    vT[jv * C + s] = ll_load(v, (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv);
   }
   const float* g = reinterpret_cast<const float*>(x.ws + p.off_g) + (size_t)bh * p.T + t0;
   const float* gamma = reinterpret_cast<const float*>(x.ws + p.off_gamma) + (size_t)bh * p.N;
@@ -288,26 +285,24 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
     for (int c = u + 1; c < ((i + 1) << m); ++c) tail += gamma[c];
     __syncthreads();  // the previous level is done with the buffers
     const float* src = dual + ((size_t)bh * p.nblk + bidx) * S;
-    for (int e = tid; e < S; e += kT) {
-      const float dvl = src[e];
-      Dm[e] = dvl;
-      DT[(e % dv) * dk + e / dv] = dvl;
-    }
+    for (int e = tid; e < S; e += kT) Dm[e] = src[e];
     for (int s = tid; s < C; s += kT) ts[s] = exp2f(gend - g[s] + tail);
     __syncthreads();
-    // dk_s += t_s Dual v_s ;  dv_s += t_s Dualᵀ k_s
-    smem_mm(C, dk, dv, vs, dv, 1, DT, dk, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
-      for (int r = 0; r < 4; ++r) {
-        float4* d4 = reinterpret_cast<float4*>(dk32 + row(m0 + r) * dk + n0);
+    // dkᵀ = Dual Vᵀ (rows i of d_k, columns s): dk_s += t_s (Dual v_s)
+    smem_mm(dk, C, dv, Dm, dv, 1, vT, C, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+      for (int jj = 0; jj < 4; ++jj) {
+        const int s = n0 + jj;
+        float4* d4 = reinterpret_cast<float4*>(dk32 + row(s) * dk + m0);
         float4 o4 = *d4;
-        const float w = ts[m0 + r];
-        o4.x += w * acc[r][0];
-        o4.y += w * acc[r][1];
-        o4.z += w * acc[r][2];
-        o4.w += w * acc[r][3];
+        const float w = ts[s];
+        o4.x += w * acc[0][jj];
+        o4.y += w * acc[1][jj];
+        o4.z += w * acc[2][jj];
+        o4.w += w * acc[3][jj];
         *d4 = o4;
       }
     });
+    // dv_s += t_s (Dualᵀ k_s)
     smem_mm(C, dv, dk, ks, dk, 1, Dm, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
       for (int r = 0; r < 4; ++r) {
         float4* d4 = reinterpret_cast<float4*>(dv32 + row(m0 + r) * dv + n0);
@@ -431,14 +426,14 @@ cudaError_t run_bwd(const BwdPlan& bp, const BwdArgs& x, const FwdArgs& fa, cuda
   bwd_intra<TIn><<<dim3(p.N, BH), kT, sm1, st>>>(p, x, bp.off_dq, bp.off_dk, bp.off_dv);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
-  const size_t sm2 = sizeof(float) * ((size_t)2 * C * dk + 2 * C * dv + 2 * dk * dv + 2 * C);
+  const size_t sm2 = sizeof(float) * ((size_t)C * dk + 3 * C * dv + dk * dv + 3 * C);
   if ((e = cudaFuncSetAttribute(bwd_inter_q<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) !=
       cudaSuccess)
     return e;
   bwd_inter_q<TIn><<<dim3(p.N, BH), kT, sm2, st>>>(p, x, bp.off_dq, bp.off_dual);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
-  const size_t sm3 = sizeof(float) * ((size_t)C * dk + C * dv + 2 * dk * dv + C);
+  const size_t sm3 = sizeof(float) * ((size_t)C * dk + C * dv + dk * dv + C);
   if ((e = cudaFuncSetAttribute(bwd_inter_kv<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) !=
       cudaSuccess)
     return e;
