@@ -421,3 +421,46 @@ void oracle_backward(long B, long T, long H, long hpg, long dk, long dv, long L,
     }
   }
 }
+
+/* ---------------------------------------------------------------------------
+ * Gated DeltaNet's transformed values.  The write-up extends Gated DeltaNet to
+ * log-linear form by keeping the model's own transition and combining its
+ * attention mask with the hierarchical one (page 1, section
+ * 对Mamba-2和门控的对数线性推广).  The transition is the gated delta rule
+ *   S_t = a_t S_{t-1} (I - beta_t k_t k_tᵀ) + beta_t v_t k_tᵀ,
+ * which is the same as S_t = a_t S_{t-1} + u_t k_tᵀ with
+ *   u_t = beta_t (v_t - a_t S_{t-1} k_t),
+ * so S_t = sum_{s<=t} M^S(t,s) u_s k_sᵀ and the output is the masked form
+ * with values u (o_t = S_t q_t for lambda = 1; the log-linear model weights the
+ * same terms by lambda_t^{l(t,s)}).  This function runs the recurrence token by
+ * token with S in fp64 (dv x dk per head) and writes u: (B, T, H, dv).
+ * k is per group as elsewhere; v, a, beta are per head.
+ * ------------------------------------------------------------------------- */
+void oracle_gdn_values(long B, long T, long H, long hpg, long dk, long dv, const double* k,
+                       const double* v, const double* a, const double* beta, double* u) {
+  long G = H / hpg;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+  for (long b = 0; b < B; b++) {
+    for (long h = 0; h < H; h++) {
+      long g = h / hpg;
+      double* S = (double*)calloc((size_t)(dv * dk), sizeof(double));
+      double* Sk = (double*)malloc(sizeof(double) * (size_t)dv);
+      for (long t = 0; t < T; t++) {
+        const double* kt = k + ((b * T + t) * G + g) * dk;
+        const double* vt = v + ((b * T + t) * H + h) * dv;
+        double at = a[(b * T + t) * H + h], bt = beta[(b * T + t) * H + h];
+        double* ut = u + ((b * T + t) * H + h) * dv;
+        for (long j = 0; j < dv; j++) {
+          double acc = 0.0;
+          for (long i = 0; i < dk; i++) acc += S[j * dk + i] * kt[i];
+          Sk[j] = acc;
+        }
+        for (long j = 0; j < dv; j++) ut[j] = bt * (vt[j] - at * Sk[j]);
+        for (long j = 0; j < dv; j++)
+          for (long i = 0; i < dk; i++) S[j * dk + i] = at * S[j * dk + i] + ut[j] * kt[i];
+      }
+      free(S);
+      free(Sk);
+    }
+  }
+}

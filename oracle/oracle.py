@@ -19,6 +19,8 @@ file's header and above each C function.  Summary:
 * ``brute``                 dense masks built by explicit loops (small T).
 * ``backward``              gradients of sum(dO * o) with respect to q, k, v,
                             log a and lambda: the chain rule on the quadratic form.
+* ``gdn_values``            Gated DeltaNet's transformed values u (gated delta rule
+                            run token by token); ``gdn_forward`` = form_q with v = u.
 """
 from __future__ import annotations
 
@@ -68,8 +70,9 @@ def _load():
             lib.oracle_form_q_points.argtypes = [_l] * 4 + [_D] * 5 + [_L, _l, _D]
             lib.oracle_form_r_head.argtypes = [_l] * 4 + [_D] * 6 + [_l, _l, _L, _D]
             lib.oracle_backward.argtypes = six + [_D] * 11
+            lib.oracle_gdn_values.argtypes = [_l] * 6 + [_D] * 5
             for f in ("oracle_form_q", "oracle_brute", "oracle_form_r", "oracle_form_q_points",
-                      "oracle_form_r_head", "oracle_backward"):
+                      "oracle_form_r_head", "oracle_backward", "oracle_gdn_values"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -200,3 +203,20 @@ def backward(q, k, v, a, lam, dO):
     _load().oracle_backward(*shp, _d(q), _d(k), _d(v), _d(a), _d(lam), _d(dO), _d(dq), _d(dkk),
                             _d(dvv), _d(dla), _d(dl))
     return dq, dkk, dvv, dla, dl
+
+
+def gdn_values(k, v, a, beta) -> np.ndarray:
+    """u_t = beta_t (v_t - a_t S_{t-1} k_t) of the gated delta rule S_t = a_t S_{t-1} +
+    u_t k_tᵀ.  k: (B, T, G, dk); v: (B, T, H, dv); a, beta: (B, T, H).  Returns (B, T, H, dv)."""
+    k, v, a, beta = (_f64(x) for x in (k, v, a, beta))
+    B, T, G, dk = k.shape
+    H, dv = v.shape[2], v.shape[3]
+    assert a.shape == (B, T, H) and beta.shape == (B, T, H) and H % G == 0
+    u = np.zeros((B, T, H, dv))
+    _load().oracle_gdn_values(B, T, H, H // G, dk, dv, _d(k), _d(v), _d(a), _d(beta), _d(u))
+    return u
+
+
+def gdn_forward(q, k, v, a, beta, lam) -> np.ndarray:
+    """Log-linear Gated DeltaNet: the masked form with the transformed values u."""
+    return form_q(q, k, gdn_values(k, v, a, beta), a, lam)
