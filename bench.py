@@ -352,6 +352,7 @@ def main():
         line["decode"] = decode_measure(sml, torch, dev, hbm_peak)
         line["comparators"] = comparators_measure(sml, torch, x, w, ms)
         line["backward"] = backward_measure(sml, torch, x, w, hbm_peak)
+        line["gated_deltanet"] = gdn_measure(sml, torch, x, w, hbm_peak)
     else:
         line["e2e"] = e2e_measure(sml, torch, x, w, dev, min(args.steps, 10))
         if world > 1:
@@ -388,6 +389,43 @@ def e2e_measure(sml, torch, x, w, dev, steps):
     return {"value": w.batch * w.T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps,
             "api": "loglinear_fwd_host (pinned host buffers)"}
+
+
+def gdn_measure(sml, torch, x, w, hbm_peak, steps=3):
+    """Log-linear Gated DeltaNet forward on the same workload (keys L2-normalised per
+    token, beta = sigmoid(z)): the delta-rule values kernel plus the level-fused forward.
+    Algorithmic bytes: q, k, v, a, beta, lambda read once, o written once."""
+    gen = torch.Generator(device=x.v.device)
+    gen.manual_seed(6)
+    kn = x.k.float()
+    kn = (kn / kn.norm(dim=-1, keepdim=True)).to(x.k.dtype)
+    beta = torch.sigmoid(torch.randn(x.a.shape, generator=gen, device=x.a.device))
+    shape = sml.fwd_shape(x.q, x.v, x.lam, w.chunk)
+    ws = torch.empty(sml.lib().loglinear_gdn_fwd_workspace_bytes(ctypes.byref(shape)), dtype=torch.uint8,
+                     device=x.v.device)
+    o = torch.empty_like(x.v)
+    call = lambda: sml.loglinear_gdn_fwd(x.q, kn, x.v, x.a, beta, x.lam, chunk=w.chunk, o=o, workspace=ws)
+    call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    if sml.loglinear_check_status() != 0:
+        raise RuntimeError("device status error in the Gated DeltaNet forward")
+    ms = e0.elapsed_time(e1) / steps
+    el = lambda t: t.numel() * t.element_size()
+    nbytes = el(x.q) + el(kn) + 2 * el(x.v) + el(x.a) + el(beta) + el(x.lam)
+    res = {"workload": workload_desc(w) + ", keys L2-normalised, beta = sigmoid(z)",
+           "ms_per_step": ms, "unit": "tokens/s", "value": w.batch * w.T / (ms / 1e3), "steps": steps,
+           "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": hbm_peak,
+                        "unit": "GB/s", "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
+                        "algorithmic_bytes_per_step": nbytes}}
+    del ws, o, kn, beta
+    torch.cuda.empty_cache()
+    return res
 
 
 def backward_measure(sml, torch, x, w, hbm_peak, steps=3):

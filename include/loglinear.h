@@ -176,6 +176,31 @@ ll_status loglinear_fwd_static_workspace(const ll_shape* shape, const void* q, c
                                          void* o, float* states_out, float* state_logscale_out,
                                          int state_levels, void* stream);
 
+/* ---- log-linear Gated DeltaNet -----------------------------------------------------------
+ * The write-up extends Gated DeltaNet the same way (section 对Mamba-2和门控的对数线性推广):
+ * the model's own transition, the gated delta rule
+ *   S_t = a_t S_{t-1} (I - beta_t k_t k_tᵀ) + beta_t v_t k_tᵀ,
+ * is kept and its attention mask is combined with the hierarchical one.  The delta rule
+ * equals S_t = a_t S_{t-1} + u_t k_tᵀ with u_t = beta_t (v_t - a_t S_{t-1} k_t), so the
+ * output is the masked form over u:
+ *   o_t = sum_{s<=t} lambda_t^{l(t,s)} M^S(t,s) (q_t . k_s) u_s.
+ */
+
+/* Bytes of device workspace loglinear_gdn_fwd needs (0: invalid shape). */
+size_t loglinear_gdn_fwd_workspace_bytes(const ll_shape* shape);
+
+/*
+ * Log-linear Gated DeltaNet forward.  Arguments as for loglinear_fwd, plus
+ *   beta  (B, T, H)  fp32, the delta-rule write strength (in [0, 1] for a stable rule)
+ * Keys are used as given; the model normalises them (the delta rule is stable for
+ * beta |k|^2 <= 2).  u is computed by one CTA per (b, h) walking the sequence in order
+ * (the delta rule is sequential across chunks), stored in the input dtype in the
+ * workspace, then the level-fused forward runs on (q, k, u, a, lambda).
+ */
+ll_status loglinear_gdn_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
+                            const float* a, const float* beta, const float* lambda, void* o,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- backward -------------------------------------------------------------------------
  * The pages give no backward; this is the chain rule on the forward's masked form
  * o_t = sum_{s<=t} lambda_t^{l(t,s)} M^S(t,s) (q_t . k_s) v_s (write-up sections

@@ -97,6 +97,10 @@ def lib() -> ctypes.CDLL:
             L.loglinear_bwd_workspace_bytes.argtypes = [_SP]
             L.loglinear_bwd.restype = ctypes.c_int
             L.loglinear_bwd.argtypes = [_SP] + [_vp] * 12 + [ctypes.c_size_t, _vp]
+            L.loglinear_gdn_fwd_workspace_bytes.restype = ctypes.c_size_t
+            L.loglinear_gdn_fwd_workspace_bytes.argtypes = [_SP]
+            L.loglinear_gdn_fwd.restype = ctypes.c_int
+            L.loglinear_gdn_fwd.argtypes = [_SP] + [_vp] * 8 + [ctypes.c_size_t, _vp]
             L.ssd_fwd.restype = ctypes.c_int
             L.ssd_fwd.argtypes = [_SP] + [_vp] * 6 + [ctypes.c_size_t, _vp]
             _lib = L
@@ -208,6 +212,21 @@ def loglinear_fwd_static_workspace(q, k, v, a, lam, chunk: int = 64, o=None, sta
                                               _ptr(state_logscale_out), int(state_levels),
                                               _stream_ptr(stream))
     _check(st, "loglinear_fwd_static_workspace")
+    return o
+
+
+def loglinear_gdn_fwd(q, k, v, a, beta, lam, chunk: int = 64, o=None, workspace=None, stream=None):
+    """Log-linear Gated DeltaNet forward: beta (B, T, H) fp32, the rest as loglinear_fwd."""
+    shape = fwd_shape(q, v, lam, chunk)
+    if o is None:
+        o = torch.empty_like(v)
+    nb = int(lib().loglinear_gdn_fwd_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None:
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
+    st = lib().loglinear_gdn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta),
+                                 _ptr(lam), _ptr(o), _ptr(workspace), workspace.numel(),
+                                 _stream_ptr(stream))
+    _check(st, "loglinear_gdn_fwd")
     return o
 
 

@@ -264,6 +264,32 @@ ll_status ssd_fwd(const ll_shape* s, const void* q, const void* k, const void* v
   return ll::launch_tc_ssd(tp, fa, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
+size_t loglinear_gdn_fwd_workspace_bytes(const ll_shape* s) {
+  const size_t f = loglinear_fwd_workspace_bytes(s);
+  return f ? a256(f) + ll::gdn_values_bytes(*s) : 0;
+}
+
+ll_status loglinear_gdn_fwd(const ll_shape* s, const void* q, const void* k, const void* v,
+                            const float* a, const float* beta, const float* lambda, void* o,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  ll_status st = check_fwd_shape(s);
+  if (st != LL_OK) return st;
+  if (!beta) return LL_ERR_NULL;
+  if (!aligned16(beta)) return LL_ERR_ALIGN;
+  const size_t need = loglinear_gdn_fwd_workspace_bytes(s);
+  if (!workspace || workspace_bytes < need) return LL_ERR_WORKSPACE;
+  if (!q || !k || !v || !a || !lambda || !o) return LL_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) || !aligned16(lambda) ||
+      !aligned16(o) || !aligned16(workspace))
+    return LL_ERR_ALIGN;
+  // u (the transformed values) after the forward's own workspace
+  const size_t fws = a256(loglinear_fwd_workspace_bytes(s));
+  char* u = static_cast<char*>(workspace) + fws;
+  if (ll::launch_gdn_values(*s, k, v, a, beta, u, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return LL_ERR_CUDA;
+  return fwd_impl(s, q, k, u, a, lambda, o, workspace, fws, nullptr, nullptr, 0, stream, nullptr, 0);
+}
+
 size_t loglinear_bwd_workspace_bytes(const ll_shape* s) {
   if (check_fwd_shape(s) != LL_OK) return 0;
   return ll::bwd_workspace_bytes(*s);

@@ -48,6 +48,11 @@ cudaError_t launch_generic_fwd(const GenPlan& p, bool bf16, const FwdArgs& a, cu
 // Only the chunk states and Fenwick blocks of the generic forward (for the backward).
 cudaError_t launch_generic_states(const GenPlan& p, bool bf16, const FwdArgs& a, cudaStream_t st);
 
+// Gated DeltaNet's transformed values (csrc/gdn.cu): buffer bytes and the launch.
+size_t gdn_values_bytes(const ll_shape& s);
+cudaError_t launch_gdn_values(const ll_shape& s, const void* k, const void* v, const float* a,
+                              const float* beta, void* u, cudaStream_t st);
+
 // Backward (csrc/backward.cu): workspace bytes (0: unsupported) and the launches.
 size_t bwd_workspace_bytes(const ll_shape& s);
 cudaError_t launch_bwd(const ll_shape& s, const void* q, const void* k, const void* v, const float* a,

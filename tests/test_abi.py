@@ -137,3 +137,19 @@ def test_comparators_validate_on_the_host(L):
     assert L.loglinear_fwd_naive(ctypes.byref(other), *([FAKE] * 6), FAKE, 1 << 30, None) == 8
     assert L.ssd_fwd(ctypes.byref(other), *([FAKE] * 5), FAKE, 1 << 30, None) == 8
     assert L.ssd_fwd(ctypes.byref(shape()), None, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) in (1, 8)
+
+
+def test_binding_signatures_match_the_header(L):
+    """Every function the binding declares to ctypes takes as many arguments as the
+    header's prototype (a miscount shifts every argument after it)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = dict(re.findall(r"\b((?:loglinear|ssd)_\w+)\s*\(([^)]*)\)\s*;", text))
+    checked = 0
+    for name, params in protos.items():
+        fn = getattr(L, name)
+        if getattr(fn, "argtypes", None) is None:
+            continue
+        n = 0 if params.strip() in ("", "void") else params.count(",") + 1
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+        checked += 1
+    assert checked >= 10
