@@ -378,9 +378,8 @@ __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
 //          as the tensor-memory A operand.
 //  role b (warps 4-7): issues S = Q Kᵀ; Q row t -> fp16 with a power-of-two scale of its
 //          own (undone in the row weight) in place once S has read Q; the inter-tile
-//          levels, nearest first, with up to three node images in flight and two Y
-//          accumulators, so that the MMA of one level overlaps the read-out of the last;
-//          then the write of o.
+//          levels, nearest first and two per MMA (N = 128 over two node images), with up
+//          to three node images in flight; then the write of o.
 // Both roles see every TMEM lane through warp % 4.
 // Shared memory (2 CTAs per SM): RQ = Q (bf16, then fp16 in place); RK = K (bf16) until
 // S completes, then node image buffers 1 and 2; RV = V (bf16, then fp16 in place);
@@ -389,7 +388,7 @@ __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
 // lambda rows and the node scalars are copied into shared memory at the start
 // (asynchronously), so that no global load sits on the path of P or of a level.
 // TMEM (256 columns): S in 0..127; once role a has consumed S, P in 0..63 and O in
-// 64..127; Y0 in 192..255 and Y1 in 128..191 (free from the start).
+// 64..127; Y of a pair of levels in 128..255 (free from the start).
 //
 // kMode selects what one launch computes (1 and 2 exist only as comparators):
 //  0  the level-fused forward above;
@@ -770,24 +769,37 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     ptx::cp_async_wait_all();
     ok = ptx::named_bar_and(2, 128, ok);  // Q fp16 in place; sLamI, sNode complete
 
-    // Levels, nearest first: Y_i = Q · Node_i (fp16, Node MN-major) into Y buffer i & 1;
-    // its rows are added with weight lambda_t^(8+m) 2^(g_t + D) and the two scales.
-    // The driver issues level i + 1 before it reads level i.
-    auto issue_y = [&](int i) -> bool {
-      if (i >= 2 && !wait_bar(&bar_yf[i & 1], ((i - 2) >> 1) & 1)) return false;  // Y buffer read
-      if (!wait_bar(&bar_e[i % 3], (i / 3) & 1)) return false;                   // image landed
+    // Levels in pairs, nearest first.  One MMA with N = 128 covers levels i and i + 1:
+    // B is the two node images as two 64-wide MN atoms, the one at the lower shared
+    // address first and the other LBO bytes above it; Y lands in TMEM columns 128..255.
+    // A last level without a partner takes N = 64 (columns 128..191).  Rows are added
+    // with weight lambda_t^(8+m) 2^(g_t + D) and the two scales.
+    auto pair_cols = [&](int i, bool two) {  // TMEM column offset of level i within the pair
+      return (two && ebuf(i % 3) > ebuf((i + 1) % 3)) ? 64 : 0;
+    };
+    auto issue_pair = [&](int i) -> bool {
+      const bool two = i + 1 < nlev;
+      if (i >= 2 && !wait_bar(&bar_yf[0], ((i >> 1) - 1) & 1)) return false;  // Y read by all
+      if (!wait_bar(&bar_e[i % 3], (i / 3) & 1)) return false;                 // images landed
       ++consumed;
+      if (two) {
+        if (!wait_bar(&bar_e[(i + 1) % 3], ((i + 1) / 3) & 1)) return false;
+        ++consumed;
+      }
       ptx::tc_fence_after();
-      const uint32_t idesc = ptx::idesc_f16_f32(128, 64, 0, 1);
-      const uint32_t q0 = ptx::smem_u32(RQ), e0 = ptx::smem_u32(ebuf(i % 3));
-      const uint32_t ty = tbase + ((i & 1) ? 128 : 192);
+      const uint32_t ea = ptx::smem_u32(ebuf(i % 3));
+      const uint32_t eb = two ? ptx::smem_u32(ebuf((i + 1) % 3)) : ea;
+      const uint32_t e0 = ea < eb ? ea : eb;
+      const uint32_t lbo = two ? (ea < eb ? eb - ea : ea - eb) : 1024;
+      const uint32_t idesc = ptx::idesc_f16_f32(128, two ? 128 : 64, 0, 1);
+      const uint32_t q0 = ptx::smem_u32(RQ);
 #pragma unroll
       for (int kk = 0; kk < kDk / 16; ++kk) {
         const uint32_t offq = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::umma_f16(ty, ptx::smem_desc_sw128(q0 + offq, 16, 1024),
-                      ptx::smem_desc_sw128(e0 + kk * 2048, 1024, 1024), idesc, kk > 0);
+        ptx::umma_f16(tbase + 128, ptx::smem_desc_sw128(q0 + offq, 16, 1024),
+                      ptx::smem_desc_sw128(e0 + kk * 2048, lbo, 1024), idesc, kk > 0);
       }
-      ptx::umma_commit(&bar_y[i & 1]);
+      ptx::umma_commit(&bar_y[0]);
       ++y_issued;
       return true;
     };
@@ -803,11 +815,13 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       }
     }
     bool okd = true;
-    if (ok && driver && nlev > 0) okd = issue_y(0);
-    for (int i = 0; ok && i < nlev; ++i) {
-      if (driver && okd && i + 1 < nlev) okd = issue_y(i + 1);  // level i + 1 ahead
-      if (driver && !okd) atomicExch(p.status, kStatusTimeout);
-      bool okw = wait_bar(&bar_y[i & 1], (i >> 1) & 1);
+    for (int i = 0; ok && i < nlev; i += 2) {
+      const bool two = i + 1 < nlev;
+      if (driver) {
+        okd = okd && issue_pair(i);
+        if (!okd) atomicExch(p.status, kStatusTimeout);
+      }
+      bool okw = wait_bar(&bar_y[0], (i >> 1) & 1);
       if (!okw) atomicExch(p.status, kStatusTimeout);
       okw = __all_sync(0xffffffffu, okw);
       if (!okw) {
@@ -816,32 +830,38 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       }
       if (driver) {
         ++y_seen;
-        if (i + 3 < nlev) {  // the image buffer of level i is free again
-          ptx::mbar_arrive_expect_tx(&bar_e[i % 3], kImgBytes);
-          ptx::bulk_load(ebuf(i % 3), img_of(i + 3), kImgBytes, &bar_e[i % 3]);
-          ++issued;
-        }
+        for (int l = i; l < i + (two ? 2 : 1); ++l)
+          if (l + 3 < nlev) {  // the image buffer of level l is free again
+            ptx::mbar_arrive_expect_tx(&bar_e[l % 3], kImgBytes);
+            ptx::bulk_load(ebuf(l % 3), img_of(l + 3), kImgBytes, &bar_e[l % 3]);
+            ++issued;
+          }
       }
       ptx::tc_fence_after();
-      const uint32_t ty = tbase + ((i & 1) ? 128 : 192) + lane_off;
-      const float wy = sLamI[i * 128 + r] * exp2f(gt + D) * pow2s(eq + __float_as_int(sNode[2 * i]));
-      float y[32];
-      ptx::tmem_ld32(ty, y);
-      ptx::tmem_ld_wait();
+      const int ci = pair_cols(i, two);
+#pragma unroll 1
+      for (int l = 0; l < (two ? 2 : 1); ++l) {
+        const int lv = i + l;
+        const uint32_t ty = tbase + 128 + (l == 0 ? ci : 64 - ci) + lane_off;
+        const float wy = sLamI[lv * 128 + r] * exp2f(gt + D) * pow2s(eq + __float_as_int(sNode[2 * lv]));
+        float y[32];
+        ptx::tmem_ld32(ty, y);
+        ptx::tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] += wy * y[j];
-      ptx::tmem_ld32(ty + 32, y);
-      ptx::tmem_ld_wait();
+        for (int j = 0; j < 32; ++j) acc[j] += wy * y[j];
+        ptx::tmem_ld32(ty + 32, y);
+        ptx::tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[32 + j] += wy * y[j];
-      D += sNode[2 * i + 1];
+        for (int j = 0; j < 32; ++j) acc[32 + j] += wy * y[j];
+        D += sNode[2 * lv + 1];
+      }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&bar_yf[i & 1]);
+      ptx::mbar_arrive(&bar_yf[0]);
     }
     if (driver) {
       // after a failed wait: let this CTA's own copies and MMAs land (bounded) before exit
       for (int j = consumed; j < issued; ++j) wait_bar(&bar_e[j % 3], (j / 3) & 1);
-      for (int j = y_seen; j < y_issued; ++j) wait_bar(&bar_y[j & 1], (j >> 1) & 1);
+      for (int j = y_seen; j < y_issued; ++j) wait_bar(&bar_y[0], j & 1);
       if (s_issued) wait_bar(&bar_s, 0);
     }
     __syncthreads();  // join: P, its row scales and the O MMA have been issued
