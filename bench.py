@@ -301,13 +301,19 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    # pass 1: the step as a user runs it (no events between kernels, so each launch may
+    # overlap the end of the one before): value and ms_per_step
     n0 = sml.loglinear_launch_count()
     t_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step()
     t_end.record(stream)
     torch.cuda.synchronize()
     n1 = sml.loglinear_launch_count()
+    # pass 2: the same steps with CUDA events between the kernels: per-kernel durations
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
@@ -341,6 +347,8 @@ def main():
                           "unit": "GB/s", "frac": path_bytes / (ms / 1e3) / 1e9 / hbm_peak,
                           "algorithmic_bytes_per_step": path_bytes},
         "kernels_ms": {n: round(t, 4) for n, t in zip(names, per_kernel)},
+        "kernels_ms_note": ("a second pass of the same steps with CUDA events between the "
+                            "kernels (which serialises them); ms_per_step is the first pass"),
         "gpu_launches": int(n1 - n0),
         "clocks": clk,
         "path": sml.loglinear_fwd_path(shape),

@@ -211,6 +211,17 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_majo
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// ---- programmatic dependent launch ---------------------------------------------------
+// Waits until the grids this one depends on (the previous launch on the stream, when
+// this one was launched with programmatic stream serialisation) have completed and their
+// memory is visible; returns at once otherwise.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next such launch on the stream start once every CTA of this grid has run
+// this (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- gpu-scope flags ---------------------------------------------------------------
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;

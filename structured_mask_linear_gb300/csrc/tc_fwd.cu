@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <utility>
 
 #include "ll_internal.cuh"
 #include "ptx.cuh"
@@ -196,6 +197,7 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   const int bh = b * p.H + h;
   const long long t0 = (long long)u * kTile;
   const float la = log2f(p.a[((size_t)b * p.T + t0 + tid) * p.H + h]);
+  ptx::griddep_launch_dependents();
 
   if (tid == 0) {
     ptx::mbar_init(&bar_ld, 1);
@@ -309,6 +311,8 @@ __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
   const int nj = (2 * i + 1 < n0) ? 2 : 1;  // level-m0 nodes built here
   const size_t nbase = (size_t)bh * p.nnodes;
   const size_t child0 = nbase + p.node_off[m0 - 1] + 4 * i;
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();  // the level below is the previous launch's output
   if (tid == 0) {
     ptx::mbar_init(&bar_ld, 1);
     ptx::fence_mbar_init();
@@ -470,6 +474,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   const size_t row = (size_t)b * p.T + t0 + r;  // token of this thread's query row
   const float* lrow = p.lam + (row * p.H + h) * p.L;
   // inter-tile levels of this tile, and whether the intra-tile part runs
+  ptx::griddep_launch_dependents();  // the next launch may start once all CTAs are resident
   const int nlev = kMode == 0 ? __popc((unsigned)u)
                  : kMode == 1 ? (u > 0 ? 1 : 0)
                               : (p.lsel >= kLevIntra && ((u >> (p.lsel - kLevIntra)) & 1) ? 1 : 0);
@@ -508,10 +513,6 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
       ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
     }
-    if (nlev > 0) {
-      ptx::mbar_arrive_expect_tx(&bar_e[0], kImgBytes);
-      ptx::bulk_load(RE, img_of(0), kImgBytes, &bar_e[0]);
-    }
   }
   if (warp == 0) {
     ptx::tmem_alloc(&tmem_base, 256);
@@ -530,11 +531,6 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       if (nlev > 0) sLamI[r] = 1.f;
     } else {
       for (int i = 0; i < nlev; ++i) ptx::cp_async4(sLamI + i * 128 + r, lrow + kLevIntra + lev_of(i));
-    }
-    if (r < nlev) {
-      const unsigned* mt = meta_of(r);
-      ptx::cp_async4(sNode + 2 * r, mt + 1);
-      ptx::cp_async4(sNode + 2 * r + 1, mt + 2);
     }
   }
   // chunk-local log2 decay cumsum over the 128 rows (both roles compute it)
@@ -729,7 +725,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     uint8_t* qrow0 = RQ + r * 128;
     uint8_t* qrow1 = RQ + 16384 + r * 128;
     int eq = 0;
-    int issued = nlev > 0 ? 1 : 0;  // image loads issued (level 0 by thread 0)
+    int issued = 0;                 // image loads issued
     int consumed = 0;               // image loads waited for by the driver
     int y_issued = 0, y_seen = 0;   // Y MMAs issued / seen complete by the driver
     if (ok) {
@@ -759,8 +755,16 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         ptx::fence_proxy_async_smem();
       }
     }
+    // From here on role b reads the tree that the previous launches built: wait for them
+    // (at once unless this grid was launched before they finished).
+    ptx::griddep_wait();
+    if (r < nlev) {
+      const unsigned* mt = meta_of(r);
+      ptx::cp_async4(sNode + 2 * r, mt + 1);
+      ptx::cp_async4(sNode + 2 * r + 1, mt + 2);
+    }
     if (ok && driver) {
-      for (int i = 1; i < 3 && i < nlev; ++i) {  // K has been read by S: RK is free
+      for (int i = 0; i < 3 && i < nlev; ++i) {  // K has been read by S: RK is free
         ptx::mbar_arrive_expect_tx(&bar_e[i], kImgBytes);
         ptx::bulk_load(ebuf(i), img_of(i), kImgBytes, &bar_e[i]);
         ++issued;
@@ -1002,6 +1006,7 @@ __global__ void __launch_bounds__(128) ssd_scan_kernel(TcParams p) {
 // tc_export: bucket states at position T (T % 128 == 0, so live levels are >= 8).
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) tc_export_kernel(TcParams p, int SL, float* st, float* lsc) {
+  ptx::griddep_wait();  // reads the tree
   const int lvl = blockIdx.x, bh = blockIdx.y;
   float* dst = st + ((size_t)bh * SL + lvl) * (kDk * kDv);
   const bool live = lvl >= 1 && ((((long long)p.T) >> (lvl - 1)) & 1);
@@ -1118,6 +1123,25 @@ bool make_tc_plan(const ll_shape& s, TcPlan* p) {
 
 namespace {
 
+// Launch that may begin while the previous launch on the stream is finishing
+// (programmatic stream serialisation); the kernel waits (griddep_wait) before it reads
+// anything that launch wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 bool tc_setup(const TcPlan& tp, const FwdArgs& a, CUtensorMap* mQ, CUtensorMap* mK, CUtensorMap* mV,
               TcParams* pp) {
   if (!make_map(mQ, a.q, kDk, tp.G, tp.T, tp.B) || !make_map(mK, a.k, kDk, tp.G, tp.T, tp.B) ||
@@ -1161,8 +1185,8 @@ cudaError_t launch_tree(const TcPlan& tp, const FwdArgs& a, const TcParams& p, c
   if (e != cudaSuccess) return e;
   for (int m0 = 1; m0 < tp.MT; m0 += 2) {
     const unsigned gt = (unsigned)((size_t)tp.B * tp.H * (((tp.NT >> m0) + 1) >> 1));
-    tc_tree_kernel<<<gt, 128, kSmemTree, st>>>(p, m0);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_overlapped(tc_tree_kernel, dim3(gt), dim3(128), kSmemTree, st, p, m0)) != cudaSuccess)
+      return e;
     if (m0 + 2 < tp.MT) note_launch();
     else note_launch(a, 1, st);
   }
@@ -1178,6 +1202,8 @@ cudaError_t launch_output(const TcPlan& tp, const CUtensorMap& mQ, const CUtenso
   const int smem_out = out_smem_bytes(ninter);
   cudaError_t e = cudaFuncSetAttribute(tc_output_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_out);
   if (e != cudaSuccess) return e;
+  if (kMode == 0)  // the comparators' passes read each other's output: plain stream order
+    return launch_overlapped(tc_output_kernel<kMode>, dim3(grid), dim3(256), smem_out, st, mQ, mK, mV, p);
   tc_output_kernel<kMode><<<grid, 256, smem_out, st>>>(mQ, mK, mV, p);
   return cudaGetLastError();
 }
@@ -1194,9 +1220,9 @@ cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   if ((e = launch_output<0>(tp, mQ, mK, mV, p, bit_length(tp.NT - 1), st)) != cudaSuccess) return e;
   note_launch(a, 2, st);
   if (a.states_out) {
-    tc_export_kernel<<<dim3(a.state_levels, tp.B * tp.H), 256, 0, st>>>(p, a.state_levels, a.states_out,
-                                                                        a.logscale_out);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_overlapped(tc_export_kernel, dim3(a.state_levels, tp.B * tp.H), dim3(256), 0, st, p,
+                               a.state_levels, a.states_out, a.logscale_out)) != cudaSuccess)
+      return e;
     note_launch(a, 3, st);
   }
   return cudaSuccess;
