@@ -174,6 +174,38 @@ def cpu_oracle_run(w, heads: int, T: int, seed: int = 0):
     return dt, oracle.num_threads()
 
 
+def cpu_oracle_other(w, what: str, T: int = 2048, seed: int = 0):
+    """The oracle beside a next-row GPU path, on a bounded sample: batch element 0, all
+    heads, the first T tokens.  what: "backward" (gradients of sum(dO * o)) or "gdn"
+    (log-linear Gated DeltaNet forward).  Returns a cpu-baseline object in all-head
+    tokens per second."""
+    import numpy as np
+    import torch
+
+    from oracle import oracle
+    from structured_mask_linear_gb300.inputs import make_inputs, to_numpy64, workload
+
+    ws = workload(w.name, batch=1, T=T, levels=max(w.levels, T.bit_length() + 1))
+    x = make_inputs(ws, "cpu", seed=seed)
+    arrs = [to_numpy64(t) for t in (x.q, x.k, x.v, x.a, x.lam)]
+    rng = np.random.default_rng(seed)
+    if what == "backward":
+        dO = rng.standard_normal(arrs[2].shape)
+        t0 = time.perf_counter()
+        oracle.backward(*arrs, dO)
+        form = "backward of the quadratic form"
+    else:
+        k = arrs[1] / np.linalg.norm(arrs[1], axis=-1, keepdims=True)
+        beta = 1.0 / (1.0 + np.exp(-rng.standard_normal(arrs[3].shape)))
+        t0 = time.perf_counter()
+        oracle.gdn_forward(arrs[0], k, arrs[2], arrs[3], beta, arrs[4])
+        form = "gated delta rule then the quadratic form"
+    dt = time.perf_counter() - t0
+    return {"value": T / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{form}, fp64, batch element 0 (all {w.heads} heads), first {T} tokens: "
+                      f"{dt:.2f} s"}
+
+
 def cpu_baseline(w):
     dt, cores = cpu_oracle_run(w, w.heads, w.T)
     return {"value": w.T / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -433,6 +465,7 @@ def gdn_measure(sml, torch, x, w, hbm_peak, steps=3):
                         "algorithmic_bytes_per_step": nbytes}}
     del ws, o, kn, beta
     torch.cuda.empty_cache()
+    res["cpu_oracle"] = cpu_oracle_other(w, "gdn")
     return res
 
 
@@ -468,6 +501,7 @@ def backward_measure(sml, torch, x, w, hbm_peak, steps=3):
                         "algorithmic_bytes_per_step": nbytes}}
     del ws, dO
     torch.cuda.empty_cache()
+    res["cpu_oracle"] = cpu_oracle_other(w, "backward")
     return res
 
 
