@@ -138,10 +138,14 @@ ll_status loglinear_decode_step(const ll_shape* shape, long long pos, const void
 /*
  * End-to-end forward from HOST buffers: copies q, k, v, a, lambda (host, same layouts
  * as loglinear_fwd; pinned memory lets the copies run asynchronously) into
- * `device_arena`, runs loglinear_fwd and copies o back to the host buffer o_host, all
- * enqueued on `stream`.  The host buffers must stay valid until the stream reaches that
- * point; the caller synchronises.  `device_arena` must hold at least
- * loglinear_fwd_host_arena_bytes(shape) bytes (16-byte aligned).
+ * `device_arena`, runs loglinear_fwd and copies o back to the host buffer o_host.  The
+ * batch is cut into up to 8 pieces of consecutive batch elements whose copies and
+ * forwards overlap: inputs go in on a library stream, each piece's forward runs on
+ * `stream`, outputs come back on a second library stream, and `stream` waits for the
+ * last copy, so the call is complete once `stream` reaches that point.  The first call
+ * on a device creates the two streams and their events (kept until exit).  The host
+ * buffers must stay valid until then; the caller synchronises.  `device_arena` must hold
+ * at least loglinear_fwd_host_arena_bytes(shape) bytes (16-byte aligned).
  */
 size_t loglinear_fwd_host_arena_bytes(const ll_shape* shape);
 ll_status loglinear_fwd_host(const ll_shape* shape, const void* q_host, const void* k_host,

@@ -172,6 +172,46 @@ size_t loglinear_fwd_host_arena_bytes(const ll_shape* s) {
   return n;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Streams and events of the pipelined host forward, created once per device.
+constexpr int kHostPieces = 8;
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t ein[kHostPieces] = {}, eout[kHostPieces] = {};
+  bool ready = false;
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[128];
+
+HostPipe* host_pipe() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    const unsigned ef = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.start, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.done, ef) != cudaSuccess)
+      return nullptr;
+    for (int i = 0; i < kHostPieces; ++i)
+      if (cudaEventCreateWithFlags(&hp.ein[i], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&hp.eout[i], ef) != cudaSuccess)
+        return nullptr;
+    hp.ready = true;
+  }
+  return &hp;
+}
+
+}  // namespace
+
+extern "C" {
+
 ll_status loglinear_fwd_host(const ll_shape* s, const void* q_host, const void* k_host,
                              const void* v_host, const float* a_host, const float* lambda_host,
                              void* o_host, void* device_arena, size_t arena_bytes, void* stream) {
@@ -195,16 +235,43 @@ ll_status loglinear_fwd_host(const ll_shape* s, const void* q_host, const void* 
   char* dws = p;
   const size_t wsb = loglinear_fwd_workspace_bytes(s);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(dq, q_host, bq, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-      cudaMemcpyAsync(dk, k_host, bq, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-      cudaMemcpyAsync(dv, v_host, bv, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-      cudaMemcpyAsync(da, a_host, ba, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-      cudaMemcpyAsync(dl, lambda_host, bl, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+  HostPipe* hp = host_pipe();
+  if (!hp) return LL_ERR_CUDA;
+  // Pipeline over pieces of the batch (consecutive batch elements; every tensor is
+  // batch-major, so a piece is one contiguous slice of each): the input copies of piece
+  // i + 1 run on hp->in while piece i computes on `stream` and piece i - 1's output
+  // copies back on hp->out.  `stream` waits for the last output copy at the end.
+  const int np = (int)(B < (size_t)kHostPieces ? B : (size_t)kHostPieces);
+  const size_t pq = bq / B, pv = bv / B, pa = ba / B, pl = bl / B;  // bytes per batch element
+  if (cudaEventRecord(hp->start, cs) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
     return LL_ERR_CUDA;
-  st = loglinear_fwd(s, dq, dk, dv, reinterpret_cast<float*>(da), reinterpret_cast<float*>(dl),
-                     dout, dws, wsb, nullptr, nullptr, 0, stream);
-  if (st != LL_OK) return st;
-  if (cudaMemcpyAsync(o_host, dout, bv, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+  for (int i = 0; i < np; ++i) {
+    const size_t b0 = B * i / np, nb = B * (i + 1) / np - b0;
+    const char* qh = static_cast<const char*>(q_host);
+    const char* kh = static_cast<const char*>(k_host);
+    const char* vh = static_cast<const char*>(v_host);
+    const char* ah = reinterpret_cast<const char*>(a_host);
+    const char* lh = reinterpret_cast<const char*>(lambda_host);
+    if (cudaMemcpyAsync(dq + b0 * pq, qh + b0 * pq, nb * pq, cudaMemcpyHostToDevice, hp->in) != cudaSuccess ||
+        cudaMemcpyAsync(dk + b0 * pq, kh + b0 * pq, nb * pq, cudaMemcpyHostToDevice, hp->in) != cudaSuccess ||
+        cudaMemcpyAsync(dv + b0 * pv, vh + b0 * pv, nb * pv, cudaMemcpyHostToDevice, hp->in) != cudaSuccess ||
+        cudaMemcpyAsync(da + b0 * pa, ah + b0 * pa, nb * pa, cudaMemcpyHostToDevice, hp->in) != cudaSuccess ||
+        cudaMemcpyAsync(dl + b0 * pl, lh + b0 * pl, nb * pl, cudaMemcpyHostToDevice, hp->in) != cudaSuccess ||
+        cudaEventRecord(hp->ein[i], hp->in) != cudaSuccess || cudaStreamWaitEvent(cs, hp->ein[i], 0) != cudaSuccess)
+      return LL_ERR_CUDA;
+    ll_shape sp = *s;
+    sp.batch = (int)nb;
+    st = loglinear_fwd(&sp, dq + b0 * pq, dk + b0 * pq, dv + b0 * pv, reinterpret_cast<float*>(da + b0 * pa),
+                       reinterpret_cast<float*>(dl + b0 * pl), dout + b0 * pv, dws, wsb, nullptr, nullptr, 0,
+                       stream);
+    if (st != LL_OK) return st;
+    if (cudaEventRecord(hp->eout[i], cs) != cudaSuccess || cudaStreamWaitEvent(hp->out, hp->eout[i], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<char*>(o_host) + b0 * pv, dout + b0 * pv, nb * pv, cudaMemcpyDeviceToHost,
+                        hp->out) != cudaSuccess)
+      return LL_ERR_CUDA;
+  }
+  if (cudaEventRecord(hp->done, hp->out) != cudaSuccess || cudaStreamWaitEvent(cs, hp->done, 0) != cudaSuccess)
     return LL_ERR_CUDA;
   return LL_OK;
 }
