@@ -73,9 +73,10 @@ __global__ void __launch_bounds__(kT) bwd_intra(GenPlan p, BwdArgs x, size_t off
   const long long t0 = (long long)j * C;
   float* qs = sm;               // C x dk
   float* ks = qs + C * dk;      // C x dk
-  float* kTr = ks + C * dk;     // dk x C
-  float* vTr = kTr + C * dk;    // dv x C
-  float* ds = vTr + C * dv;     // C x dv  (dO)
+  const int CP = C + 4;         // padded row of a transposed tile (16-byte rows, 4-way banks)
+  float* kTr = ks + C * dk;     // dk x C (row stride CP)
+  float* vTr = kTr + CP * dk;   // dv x C (row stride CP)
+  float* ds = vTr + CP * dv;    // C x dv  (dO)
   float* gs = ds + C * dv;      // C
   float* ls = gs + C;           // C x nl  (lambda of the in-chunk levels)
   float* dS = ls + C * nl;      // C x C: dO.v, then w (dO . v)
@@ -91,12 +92,12 @@ __global__ void __launch_bounds__(kT) bwd_intra(GenPlan p, BwdArgs x, size_t off
     qs[e] = ll_load(q, gi);
     const float kv = ll_load(k, gi);
     ks[e] = kv;
-    kTr[i * C + s] = kv;
+    kTr[i * CP + s] = kv;
   }
   for (int e = tid; e < C * dv; e += kT) {
     const int s = e / dv, jv = e % dv;
     const size_t gi = (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv;
-    vTr[jv * C + s] = ll_load(v, gi);
+    vTr[jv * CP + s] = ll_load(v, gi);
     ds[e] = ll_load(dO, gi);
   }
   const float* g = reinterpret_cast<const float*>(x.ws + p.off_g) + (size_t)bh * p.T + t0;
@@ -106,11 +107,11 @@ __global__ void __launch_bounds__(kT) bwd_intra(GenPlan p, BwdArgs x, size_t off
     ls[e] = x.lam[(((size_t)b * p.T + t0 + t) * p.H + h) * L + l];
   }
   __syncthreads();
-  smem_mm(C, C, dk, qs, dk, 1, kTr, C, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+  smem_mm(C, C, dk, qs, dk, 1, kTr, CP, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
     for (int i = 0; i < 4; ++i)
       for (int jj = 0; jj < 4; ++jj) P[(m0 + i) * C + n0 + jj] = acc[i][jj];
   });
-  smem_mm(C, C, dv, ds, dv, 1, vTr, C, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+  smem_mm(C, C, dv, ds, dv, 1, vTr, CP, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
     for (int i = 0; i < 4; ++i)
       for (int jj = 0; jj < 4; ++jj) dS[(m0 + i) * C + n0 + jj] = acc[i][jj];
   });
@@ -168,10 +169,11 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
   const int b = bh / p.H, h = bh % p.H, grp = h / p.hpg;
   const long long t0 = (long long)j * C;
   const int S = dk * dv;
+  const int CP = C;            // row stride of the transposed tile (unpadded: two CTAs per SM)
   float* qs = sm;              // C x dk
   float* ds = qs + C * dk;     // C x dv   (dO)
   float* dT = ds + C * dv;     // dv x C   (dOᵀ)
-  float* dw = dT + C * dv;     // C x dv   (w_t dO_t)
+  float* dw = dT + CP * dv;    // C x dv   (w_t dO_t)
   float* Bm = dw + C * dv;     // dk x dv: the block
   float* ws_ = Bm + S;         // C: 2^(g_t + D) of this level
   float* wl = ws_ + C;         // C: lambda_t^l 2^(g_t + D)
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
     const int s = e / dv, jv = e % dv;
     const float d = ll_load(dO, (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv);
     ds[e] = d;
-    dT[jv * C + s] = d;
+    dT[jv * CP + s] = d;
   }
   const float* g = reinterpret_cast<const float*>(x.ws + p.off_g) + (size_t)bh * p.T + t0;
   const float* blk = reinterpret_cast<const float*>(x.ws + p.off_blk);
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
     __syncthreads();
     for (int e = tid; e < C * dv; e += kT) dw[e] = wl[e / dv] * ds[e];
     // dqᵀ = Bm dOᵀ (rows i of d_k, columns t): dq_t += w_t (Bm dO_t)
-    smem_mm(dk, C, dv, Bm, dv, 1, dT, C, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+    smem_mm(dk, C, dv, Bm, dv, 1, dT, CP, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
       for (int jj = 0; jj < 4; ++jj) {
         const int t = n0 + jj;
         float4* d4 = reinterpret_cast<float4*>(dq32 + row(t) * dk + m0);
@@ -254,9 +256,10 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
   const int b = bh / p.H, h = bh % p.H, grp = h / p.hpg;
   const long long t0 = (long long)u * C;
   const int S = dk * dv;
+  const int CP = C + 4;      // padded row of a transposed tile
   float* ks = sm;            // C x dk
-  float* vT = ks + C * dk;   // dv x C  (Vᵀ)
-  float* Dm = vT + C * dv;   // dk x dv: the dual
+  float* vT = ks + C * dk;   // dv x C  (Vᵀ, row stride CP)
+  float* Dm = vT + CP * dv;  // dk x dv: the dual
   float* ts = Dm + S;        // C: 2^(decay from key s to the end of the block)
   const TIn* k = static_cast<const TIn*>(x.k);
   const TIn* v = static_cast<const TIn*>(x.v);
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
   }
   for (int e = tid; e < C * dv; e += kT) {
     const int s = e / dv, jv = e % dv;
-    vT[jv * C + s] = ll_load(v, (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv);
+    vT[jv * CP + s] = ll_load(v, (((size_t)b * p.T + t0 + s) * p.H + h) * dv + jv);
   }
   const float* g = reinterpret_cast<const float*>(x.ws + p.off_g) + (size_t)bh * p.T + t0;
   const float* gamma = reinterpret_cast<const float*>(x.ws + p.off_gamma) + (size_t)bh * p.N;
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
     for (int s = tid; s < C; s += kT) ts[s] = exp2f(gend - g[s] + tail);
     __syncthreads();
     // dkᵀ = Dual Vᵀ (rows i of d_k, columns s): dk_s += t_s (Dual v_s)
-    smem_mm(dk, C, dv, Dm, dv, 1, vT, C, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+    smem_mm(dk, C, dv, Dm, dv, 1, vT, CP, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
       for (int jj = 0; jj < 4; ++jj) {
         const int s = n0 + jj;
         float4* d4 = reinterpret_cast<float4*>(dk32 + row(s) * dk + m0);
@@ -419,7 +422,8 @@ cudaError_t run_bwd(const BwdPlan& bp, const BwdArgs& x, const FwdArgs& fa, cuda
   if ((e = cudaMemsetAsync(x.ws + bp.off_dual, 0, sizeof(float) * (size_t)BH * p.nblk * dk * dv, st)) !=
       cudaSuccess)
     return e;
-  const size_t sm1 = sizeof(float) * ((size_t)3 * C * dk + 2 * C * dv + C + C * (p.clog + 1) + 3 * C * C);
+  const size_t sm1 = sizeof(float) * ((size_t)2 * C * dk + (size_t)(C + 4) * (dk + dv) + C * dv + C +
+                                      C * (p.clog + 1) + 3 * C * C);
   if ((e = cudaFuncSetAttribute(bwd_intra<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) !=
       cudaSuccess)
     return e;
@@ -433,7 +437,7 @@ cudaError_t run_bwd(const BwdPlan& bp, const BwdArgs& x, const FwdArgs& fa, cuda
   bwd_inter_q<TIn><<<dim3(p.N, BH), kT, sm2, st>>>(p, x, bp.off_dq, bp.off_dual);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
-  const size_t sm3 = sizeof(float) * ((size_t)C * dk + C * dv + dk * dv + C);
+  const size_t sm3 = sizeof(float) * ((size_t)C * dk + (size_t)(C + 4) * dv + dk * dv + C);
   if ((e = cudaFuncSetAttribute(bwd_inter_kv<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) !=
       cudaSuccess)
     return e;
