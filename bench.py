@@ -56,6 +56,22 @@ def dist_env():
     return ws, rank, local
 
 
+def job_time(ms: float, world: int, dist=None, device=None) -> float:
+    """Per-step time of the whole job: the slowest rank's (max over ranks; a no-op at N=1)."""
+    if world <= 1:
+        return ms
+    import torch
+
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_value(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the job's per-step time."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -351,12 +367,8 @@ def main():
         dist.barrier()
     if sml.loglinear_check_status() != 0:
         raise RuntimeError("device status error in the timed region")
-    ms = t_start.elapsed_time(t_end) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * B * T / (ms / 1e3)
+    ms = job_time(t_start.elapsed_time(t_end) / args.steps, world, dist, dev)
+    value = job_value(B * T, world, ms)
     per_kernel = [statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
                   for j in range(nk)]
     dom = max(range(nk), key=lambda j: per_kernel[j])
@@ -396,9 +408,8 @@ def main():
     else:
         line["e2e"] = e2e_measure(sml, torch, x, w, dev, min(args.steps, 10))
         if world > 1:
-            tt = torch.tensor([line["e2e"]["ms_per_step"]], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            line["e2e"]["value"] = world * B * T / (float(tt.item()) / 1e3)
+            e_ms = job_time(line["e2e"]["ms_per_step"], world, dist, dev)
+            line["e2e"]["value"] = job_value(B * T, world, e_ms)
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
