@@ -377,13 +377,14 @@ __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
 // tc_output: intra-tile masked attention + level-fused inter-tile buckets.
 //
 // 256 threads in two roles after a common prologue (loads, decay cumsum):
-//  role a (warps 0-3): V tile scale and V -> fp16 in place; P row t = thread, written as
-//          fp16 into tensor memory over the columns of S it has consumed; O = P V with P
-//          as the tensor-memory A operand.
-//  role b (warps 4-7): issues S = Q Kᵀ; Q row t -> fp16 with a power-of-two scale of its
-//          own (undone in the row weight) in place once S has read Q; the inter-tile
-//          levels, nearest first and two per MMA (N = 128 over two node images), with up
-//          to three node images in flight; then the write of o.
+//  role a (warps 0-3): once S has landed, P row t = thread, written as fp16 into tensor
+//          memory over the columns of S it has consumed; then the V tile scale and V ->
+//          fp16 in place; O = P V with P as the tensor-memory A operand.
+//  role b (warps 4-7): issues S = Q Kᵀ; waits for the tree's launches and fetches the
+//          node scalars and the first node image; Q row t -> fp16 with a power-of-two
+//          scale of its own (undone in the row weight) in place once S has read Q; the
+//          inter-tile levels, nearest first and two per MMA (N = 128 over two node
+//          images), with up to three node images in flight; then the write of o.
 // Both roles see every TMEM lane through warp % 4.
 // Shared memory (2 CTAs per SM): RQ = Q (bf16, then fp16 in place); RK = K (bf16) until
 // S completes, then node image buffers 1 and 2; RV = V (bf16, then fp16 in place);
@@ -574,35 +575,14 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     __syncthreads();  // join: nothing to do without the intra-tile part
   } else if (!role_b) {
     // ---- role a -----------------------------------------------------------------------
-    // V tile scale (V is not an operand of S) and V -> fp16 in place.
-    uint8_t* vrow = RV + r * 128;
-    uint4 vv[8];
-    int ev = 0;
+    // P as soon as S has landed; then the V tile scale and V -> fp16 in place (V is an
+    // operand of O only, and P does not depend on V's scale).
     if (ok) {
-      uint32_t mx = 0u;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        vv[c] = *reinterpret_cast<const uint4*>(vrow + ((c ^ rot) << 4));
-        mx = absmax_u4(mx, vv[c]);
-      }
-      float mv = bf16x2_maxhalf(mx);
-#pragma unroll
-      for (int off = 16; off; off >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
-      if (lane == 0) s_red[warp] = mv;
-    }
-    ptx::named_bar_sync(1, 128);
-    if (ok) {
-      ev = f16_exp(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
-      const float sv_ = pow2i(-ev);
-      const __nv_bfloat162 s2 = __floats2bfloat162_rn(sv_, sv_);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(vrow + ((c ^ rot) << 4)) = bf16x8_to_f16x8(vv[c], s2);
-      ptx::fence_proxy_async_smem();
       ok = wait_bar(&bar_s, 0);
       if (!ok) atomicExch(p.status, kStatusTimeout);
     }
     ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld / st below are warp-collective
+    int ep = 0;
     // P row t = r in fp16 with row scale 2^-ep, into TMEM columns 0..63 over S.
     if (ok) {
       ptx::tc_fence_after();
@@ -629,8 +609,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         for (int j = 0; j < 32; ++j)
           if (j <= tl) smax = fmaxf(smax, fabsf(sv[j]));
       }
-      const int ep = f16_exp(smax * lmax);  // |P| <= max|S| * max lambda (decays are <= 1)
-      sEp[t] = ep + ev;
+      ep = f16_exp(smax * lmax);  // |P| <= max|S| * max lambda (decays are <= 1)
       const float coef = pow2i(-ep);
       // Decay 2^(g_t - g_s) = A_kb B8[s], with A_kb = 2^(g_t - g_end8(kb)) per row and
       // 8-key block kb and B8[s] = 2^(g_end8(s) - g_s) per key; both are <= 1 for keys of
@@ -702,6 +681,31 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       }
       ptx::tmem_st_wait();
     }
+    uint8_t* vrow = RV + r * 128;
+    uint4 vv[8];
+    if (ok) {
+      uint32_t mx = 0u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        vv[c] = *reinterpret_cast<const uint4*>(vrow + ((c ^ rot) << 4));
+        mx = absmax_u4(mx, vv[c]);
+      }
+      float mv = bf16x2_maxhalf(mx);
+#pragma unroll
+      for (int off = 16; off; off >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+      if (lane == 0) s_red[warp] = mv;
+    }
+    ptx::named_bar_sync(1, 128);
+    if (ok) {
+      const int ev = f16_exp(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
+      const float sv_ = pow2i(-ev);
+      const __nv_bfloat162 s2 = __floats2bfloat162_rn(sv_, sv_);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(vrow + ((c ^ rot) << 4)) = bf16x8_to_f16x8(vv[c], s2);
+      ptx::fence_proxy_async_smem();
+      sEp[r] = ep + ev;
+    }
     ptx::tc_fence_before();
     const bool ok_a = ptx::named_bar_and(1, 128, ok);
     // O = P V (M = 128, N = 64, K = 128 keys): P from TMEM, V fp16 MN-major, into the
@@ -720,6 +724,9 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     __syncthreads();  // join (role b waits here after its levels)
   } else {
     // ---- role b -----------------------------------------------------------------------
+    // The tree that the previous launches built is read from here on: wait for them (at
+    // once unless this grid was launched before they finished), then fetch the node
+    // scalars and the first image (into RE, free from the start) behind the Q work.
     // Q row r -> fp16 with scale 2^-eq of its own: read and converted while S runs,
     // stored back once S has completed.  Then images 1 and 2 go into RK.
     uint8_t* qrow0 = RQ + r * 128;
@@ -728,6 +735,17 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     int issued = 0;                 // image loads issued
     int consumed = 0;               // image loads waited for by the driver
     int y_issued = 0, y_seen = 0;   // Y MMAs issued / seen complete by the driver
+    ptx::griddep_wait();
+    if (r < nlev) {
+      const unsigned* mt = meta_of(r);
+      ptx::cp_async4(sNode + 2 * r, mt + 1);
+      ptx::cp_async4(sNode + 2 * r + 1, mt + 2);
+    }
+    if (ok && driver && nlev > 0) {
+      ptx::mbar_arrive_expect_tx(&bar_e[0], kImgBytes);
+      ptx::bulk_load(ebuf(0), img_of(0), kImgBytes, &bar_e[0]);
+      ++issued;
+    }
     if (ok) {
       uint4 qv[16];
       uint32_t mx = 0u;
@@ -755,16 +773,8 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         ptx::fence_proxy_async_smem();
       }
     }
-    // From here on role b reads the tree that the previous launches built: wait for them
-    // (at once unless this grid was launched before they finished).
-    ptx::griddep_wait();
-    if (r < nlev) {
-      const unsigned* mt = meta_of(r);
-      ptx::cp_async4(sNode + 2 * r, mt + 1);
-      ptx::cp_async4(sNode + 2 * r + 1, mt + 2);
-    }
     if (ok && driver) {
-      for (int i = 0; i < 3 && i < nlev; ++i) {  // K has been read by S: RK is free
+      for (int i = 1; i < 3 && i < nlev; ++i) {  // K has been read by S: RK is free
         ptx::mbar_arrive_expect_tx(&bar_e[i], kImgBytes);
         ptx::bulk_load(ebuf(i), img_of(i), kImgBytes, &bar_e[i]);
         ++issued;
