@@ -51,7 +51,7 @@ cudaError_t launch_generic_states(const GenPlan& p, bool bf16, const FwdArgs& a,
 // Gated DeltaNet's transformed values (csrc/gdn.cu): buffer bytes and the launch.
 size_t gdn_values_bytes(const ll_shape& s);
 cudaError_t launch_gdn_values(const ll_shape& s, const void* k, const void* v, const float* a,
-                              const float* beta, void* u, unsigned* status, cudaStream_t st);
+                              const float* beta, void* u, cudaStream_t st);
 
 // Backward (csrc/backward.cu): workspace bytes (0: unsupported) and the launches.
 size_t bwd_workspace_bytes(const ll_shape& s);
