@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(kG) gdn_local(int T, int H, int hpg, int dk, i
 // Value columns j0 .. j0 + JW - 1 of one (b, h).  Each thread owns fixed output tiles: a
 // 2 x 4 tile (tokens x columns) of u = U_loc - W S and a 4 x 4 tile (key rows x columns) of
 // the state, kept in registers across chunks; shared memory holds S only as the operand
-// of u.  Copies run in two groups per chunk: W and g (needed first) are fetched behind
-// the state update of the chunk before, U_loc and the keys behind the product W S.
+// of u.  Copies run in two groups per chunk: W and g (needed first; two buffers) are
+// fetched a chunk and a half ahead, U_loc and the keys behind the product W S.
 template <typename TIn>
 __global__ void __launch_bounds__(kG, 3) gdn_pass(int T, int H, int hpg, int dk, int dv, int C, int JW,
                                                   const TIn* __restrict__ k, const float* __restrict__ xg,
@@ -254,18 +254,20 @@ __global__ void __launch_bounds__(kG, 3) gdn_pass(int T, int H, int hpg, int dk,
   const int b = bh / H, h = bh % H, G = H / hpg, grp = h / hpg;
   const int tid = threadIdx.x, n = T / C, WP = dk + 4;
   const size_t cst = (size_t)C * (dk + dv + 1);   // workspace floats per chunk: W, U_loc, g
-  float* Wm = sm;                                   // C x WP: W (rows padded)
-  float* Um = Wm + C * WP;                          // C x JW: U_loc, then 2^(g_end - g) u
-  float* gm = Um + C * JW;                          // C
-  float* Sm = gm + C;                               // dk x JW: S
+  float* Wm = sm;                                   // 2 x C x WP: W (rows padded), by chunk parity
+  float* gm = Wm + 2 * C * WP;                      // 2 x C: g, by chunk parity
+  float* Um = gm + 2 * C;                           // C x JW: U_loc, then 2^(g_end - g) u
+  float* Sm = Um + C * JW;                          // dk x JW: S
   TIn* Km = reinterpret_cast<TIn*>(Sm + dk * JW);   // C x dk: keys
   const float* xb = xg + (size_t)bh * n * cst;
   auto load_wg = [&](int c) {
     if (c < n) {
       const float* src = xb + c * cst;
+      float* wd = Wm + (c & 1) * C * WP;
+      float* gd = gm + (c & 1) * C;
       const int q4 = dk >> 2;
-      for (int e = tid; e < C * q4; e += kG) ptx::cp_async16(Wm + (e / q4) * WP + 4 * (e % q4), src + 4 * e);
-      for (int e = tid; e < (C >> 2); e += kG) ptx::cp_async16(gm + 4 * e, src + (size_t)C * (dk + dv) + 4 * e);
+      for (int e = tid; e < C * q4; e += kG) ptx::cp_async16(wd + (e / q4) * WP + 4 * (e % q4), src + 4 * e);
+      for (int e = tid; e < (C >> 2); e += kG) ptx::cp_async16(gd + 4 * e, src + (size_t)C * (dk + dv) + 4 * e);
     }
     ptx::cp_async_commit();
   };
@@ -294,16 +296,19 @@ __global__ void __launch_bounds__(kG, 3) gdn_pass(int T, int H, int hpg, int dk,
   for (int e = tid; e < dk * JW; e += kG) Sm[e] = 0.f;
   load_wg(0);
   load_uk(0);
+  load_wg(1);
   for (int c = 0; c < n; ++c) {
-    ptx::cp_async_wait_group<1>();
-    __syncthreads();  // W and g of chunk c; S of the previous chunk
+    const float* Wc = Wm + (c & 1) * C * WP;
+    const float* gc = gm + (c & 1) * C;
+    ptx::cp_async_wait_group<2>();  // W and g of chunk c (only chunk 0 can still be waiting)
+    __syncthreads();                // ... and S of the previous chunk
     float acc[2][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     if (own1) {
-      const float* w0 = Wm + m1 * WP;
+      const float* w0 = Wc + m1 * WP;
       const float* w1 = w0 + WP;
 #pragma unroll 2
       for (int i = 0; i < dk; i += 4) {
@@ -322,14 +327,14 @@ __global__ void __launch_bounds__(kG, 3) gdn_pass(int T, int H, int hpg, int dk,
         }
       }
     }
-    const float gend = gm[C - 1];
+    const float gend = gc[C - 1];
     ptx::cp_async_wait_group<0>();
-    __syncthreads();  // U_loc and keys of chunk c
+    __syncthreads();  // U_loc and keys of chunk c (and W and g of chunk c + 1)
     if (own1) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int s = m1 + r;
-        const float f = exp2f(gend - gm[s]);
+        const float f = exp2f(gend - gc[s]);
         float* ur = Um + s * JW + n0;
         TIn* out = u + (((size_t)b * T + (size_t)c * C + s) * H + h) * dv + j0 + n0;
 #pragma unroll
@@ -340,8 +345,8 @@ __global__ void __launch_bounds__(kG, 3) gdn_pass(int T, int H, int hpg, int dk,
         }
       }
     }
-    __syncthreads();  // decayed u complete; W and g no longer read
-    load_wg(c + 1);
+    __syncthreads();  // decayed u complete; W and g of chunk c no longer read
+    load_wg(c + 2);
     if (own2) {
       float a2[4][4];
 #pragma unroll
@@ -399,7 +404,7 @@ cudaError_t run_gdn(const ll_shape& s, const void* k, const void* v, const float
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   const int JW = dv > 32 ? 32 : dv;
-  const size_t sm2 = sizeof(float) * ((size_t)C * (dk + 4) + (size_t)C * JW + C + (size_t)dk * JW) +
+  const size_t sm2 = sizeof(float) * (2 * (size_t)C * (dk + 4) + 2 * (size_t)C + (size_t)C * JW + (size_t)dk * JW) +
                      sizeof(TIn) * (size_t)C * dk;
   if ((e = cudaFuncSetAttribute(gdn_pass<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) !=
       cudaSuccess)
