@@ -116,12 +116,16 @@ __host__ __device__ inline int bit_length(long long x) {
 // nthr threads in turn, acc[i][j] = sum_{k < K} A(m0+i, k) B(k, n0+j) with
 // A(m, k) = a[m*sam + k*sak] and B(k, n) = b[k*sbk + n] (b rows 16-byte aligned), then
 // epi(m0, n0, acc).  Threads of a warp share m0 where N/4 >= 32 (A is a broadcast) and
-// read consecutive float4s of B.
+// read consecutive float4s of B.  Where A's k (sak == 1) or m (sam == 1) index is
+// contiguous and 16-byte aligned, A is read four values per load.
 template <typename Epi>
 __device__ __forceinline__ void smem_mm(int M, int N, int K, const float* a, int sam, int sak,
                                         const float* b, int sbk, int tid, int nthr, Epi epi) {
   const int tn_count = N >> 2;
   const int tiles = (M >> 2) * tn_count;
+  const bool a16 = (reinterpret_cast<uintptr_t>(a) & 15u) == 0;
+  const bool krow = a16 && sak == 1 && (sam & 3) == 0 && (K & 3) == 0;  // A rows along k
+  const bool mcol = a16 && !krow && sam == 1 && (sak & 3) == 0;         // A columns along m
   for (int tile = tid; tile < tiles; tile += nthr) {
     const int m0 = (tile / tn_count) << 2, n0 = (tile % tn_count) << 2;
     float acc[4][4];
@@ -131,18 +135,58 @@ __device__ __forceinline__ void smem_mm(int M, int N, int K, const float* a, int
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     const float* ap = a + (size_t)m0 * sam;
     const float* bp = b + n0;
+    if (krow) {
+#pragma unroll 2
+      for (int k = 0; k < K; k += 4) {
+        float ar[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 x = *reinterpret_cast<const float4*>(ap + i * sam + k);
+          ar[i][0] = x.x;
+          ar[i][1] = x.y;
+          ar[i][2] = x.z;
+          ar[i][3] = x.w;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float4 bv = *reinterpret_cast<const float4*>(bp + (size_t)(k + kk) * sbk);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[i][0] += ar[i][kk] * bv.x;
+            acc[i][1] += ar[i][kk] * bv.y;
+            acc[i][2] += ar[i][kk] * bv.z;
+            acc[i][3] += ar[i][kk] * bv.w;
+          }
+        }
+      }
+    } else if (mcol) {
 #pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-      const float4 bv = *reinterpret_cast<const float4*>(bp + (size_t)k * sbk);
-      float av[4];
+      for (int k = 0; k < K; ++k) {
+        const float4 x = *reinterpret_cast<const float4*>(ap + (size_t)k * sak);
+        const float4 bv = *reinterpret_cast<const float4*>(bp + (size_t)k * sbk);
+        const float av[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = ap[i * sam + k * sak];
+        for (int i = 0; i < 4; ++i) {
+          acc[i][0] += av[i] * bv.x;
+          acc[i][1] += av[i] * bv.y;
+          acc[i][2] += av[i] * bv.z;
+          acc[i][3] += av[i] * bv.w;
+        }
+      }
+    } else {
+#pragma unroll 4
+      for (int k = 0; k < K; ++k) {
+        const float4 bv = *reinterpret_cast<const float4*>(bp + (size_t)k * sbk);
+        float av[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[i][0] += av[i] * bv.x;
-        acc[i][1] += av[i] * bv.y;
-        acc[i][2] += av[i] * bv.z;
-        acc[i][3] += av[i] * bv.w;
+        for (int i = 0; i < 4; ++i) av[i] = ap[i * sam + k * sak];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[i][0] += av[i] * bv.x;
+          acc[i][1] += av[i] * bv.y;
+          acc[i][2] += av[i] * bv.z;
+          acc[i][3] += av[i] * bv.w;
+        }
       }
     }
     epi(m0, n0, acc);
