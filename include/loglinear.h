@@ -100,7 +100,9 @@ size_t loglinear_fwd_workspace_bytes(const ll_shape* shape);
  *   states_out        NULL, or (B, H, state_levels, d_k, d_v) fp32: the Fenwick bucket
  *                     states at position T, i.e. the memory a decode step at position T
  *                     starts from.  Level l holds sum over the level-l bucket of T of
- *                     M^S(T-1, s) k_s v_sᵀ; levels that are not live at T are zero.
+ *                     M^S(T-1, s) k_s v_sᵀ.  Only the levels live at T (level l >= 1
+ *                     with bit l-1 of T set) are written; the other slots hold
+ *                     unspecified values, as the decode step allows.
  *   state_logscale_out NULL, or (B, H, state_levels) fp32, written as zeros (the decay
  *                     is folded into states_out).
  *   state_levels      slots in states_out; must be >= bit_length(T) + 1 when states_out

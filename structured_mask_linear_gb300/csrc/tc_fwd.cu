@@ -1015,34 +1015,40 @@ __global__ void __launch_bounds__(128) ssd_scan_kernel(TcParams p) {
 // ---------------------------------------------------------------------------------
 // tc_export: bucket states at position T (T % 128 == 0, so live levels are >= 8).
 // ---------------------------------------------------------------------------------
+// One CTA per live level of T (level l >= 1 with bit l-1 of T set) and (b, h); CTA 0 of
+// each (b, h) also writes the zero log-scales of all SL slots.  Slots of levels that are
+// not live at T are left as they are.
 __global__ void __launch_bounds__(256) tc_export_kernel(TcParams p, int SL, float* st, float* lsc) {
   ptx::griddep_wait();  // reads the tree
-  const int lvl = blockIdx.x, bh = blockIdx.y;
+  const int bh = blockIdx.y;
+  if (lsc && blockIdx.x == 0)
+    for (int l = threadIdx.x; l < SL; l += 256) lsc[(size_t)bh * SL + l] = 0.f;
+  const int lvl = nth_set_bit((unsigned)p.T, blockIdx.x) + 1;
   float* dst = st + ((size_t)bh * SL + lvl) * (kDk * kDv);
-  const bool live = lvl >= 1 && ((((long long)p.T) >> (lvl - 1)) & 1);
-  float scale = 0.f;
-  const uint8_t* img = nullptr;
-  if (live) {
-    const int m = lvl - kLevIntra;
-    const size_t nbase = (size_t)bh * p.nnodes;
-    float D = 0.f;
-    for (int mm = 0; mm < m; ++mm)
-      if ((p.NT >> mm) & 1)
-        D += __uint_as_float(p.meta[(nbase + p.node_off[mm] + ((p.NT >> mm) - 1)) * kMeta + 2]);
-    const size_t node = nbase + p.node_off[m] + ((p.NT >> m) - 1);
-    scale = exp2f(D) * pow2i((int)p.meta[node * kMeta + 1]);
-    img = p.img + node * kImgBytes;
-  }
-  for (int e = threadIdx.x; e < kDk * kDv; e += 256) {
-    float v = 0.f;
-    if (live) {
-      const int i = e / kDv, j = e % kDv, c = j >> 3;
-      const __half x = *reinterpret_cast<const __half*>(img + i * 128 + ((c ^ (i & 7)) << 4) + (j & 7) * 2);
-      v = scale * __half2float(x);
+  const int m = lvl - kLevIntra;
+  const size_t nbase = (size_t)bh * p.nnodes;
+  float D = 0.f;
+  for (int mm = 0; mm < m; ++mm)
+    if ((p.NT >> mm) & 1)
+      D += __uint_as_float(p.meta[(nbase + p.node_off[mm] + ((p.NT >> mm) - 1)) * kMeta + 2]);
+  const size_t node = nbase + p.node_off[m] + ((p.NT >> m) - 1);
+  const float scale = exp2f(D) * pow2i((int)p.meta[node * kMeta + 1]);
+  const uint8_t* img = p.img + node * kImgBytes;
+  for (int e = threadIdx.x; e < kDk * 8; e += 256) {  // 16-byte chunk c of image row i
+    const int i = e >> 3, c = e & 7;
+    const uint4 x = *reinterpret_cast<const uint4*>(img + i * 128 + ((c ^ (i & 7)) << 4));
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    float f[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+      f[2 * q] = scale * h2.x;
+      f[2 * q + 1] = scale * h2.y;
     }
-    dst[e] = v;
+    float4* d4 = reinterpret_cast<float4*>(dst + i * kDv + c * 8);
+    d4[0] = make_float4(f[0], f[1], f[2], f[3]);
+    d4[1] = make_float4(f[4], f[5], f[6], f[7]);
   }
-  if (lsc && threadIdx.x == 0) lsc[(size_t)bh * SL + lvl] = 0.f;
 }
 
 __global__ void wait_selftest_kernel(unsigned* status, long long spins) {
@@ -1230,7 +1236,7 @@ cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   if ((e = launch_output<0>(tp, mQ, mK, mV, p, bit_length(tp.NT - 1), st)) != cudaSuccess) return e;
   note_launch(a, 2, st);
   if (a.states_out) {
-    if ((e = launch_overlapped(tc_export_kernel, dim3(a.state_levels, tp.B * tp.H), dim3(256), 0, st, p,
+    if ((e = launch_overlapped(tc_export_kernel, dim3(__builtin_popcount((unsigned)tp.T), tp.B * tp.H), dim3(256), 0, st, p,
                                a.state_levels, a.states_out, a.logscale_out)) != cudaSuccess)
       return e;
     note_launch(a, 3, st);

@@ -164,7 +164,8 @@ def test_bitexact_sum_fp32(sml):
 def test_state_export(sml, T, decay):
     """Exported bucket states at position T.  With the iid decay the far levels decay
     below the fp32 range, so the live levels are compared jointly (relative to the
-    whole export); with slow decay every live level is compared on its own."""
+    whole export); with slow decay every live level is compared on its own.  Slots of
+    levels that are not live hold unspecified values and are not compared."""
     w = workload("small", batch=1, heads=4, T=T, levels=levels_for(T), decay=decay)
     x = make_inputs(w, "cpu", seed=9)
     SL = T.bit_length() + 1
@@ -176,10 +177,8 @@ def test_state_export(sml, T, decay):
     assert torch.all(lsc == 0)
     got = st.double().cpu().numpy()
     live = [lvl for lvl in range(SL) if lvl >= 1 and (T >> (lvl - 1)) & 1]
-    for lvl in range(SL):
-        if lvl not in live:
-            assert np.all(got[:, :, lvl] == 0)
-        elif decay == "slow":
+    for lvl in live:
+        if decay == "slow":
             assert_parity(got[:, :, lvl], ref_st[:, :, lvl], f"state level {lvl}", "f32")
     assert_parity(got[:, :, live], ref_st[:, :, live], "live levels", "f32")
 
