@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
 // images of level m0 - 1.  Node_{m+1}[i] = 2^(Gamma(Node_m[2i+1])) Node_m[2i] +
 // Node_m[2i+1].  One CTA per pair of level-m0 nodes (2i, 2i+1): it loads their four
 // children with bulk copies, merges each pair in fp32 (thread tid owns row tid),
-// publishes both, and the parent Node_{m0+1}[i] from the fp32 sums when it exists.  No
+// publishes the even one, and the parent Node_{m0+1}[i] from the fp32 sums when it exists.  No
 // CTA waits for another: the launches before it on the stream produced its inputs.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
@@ -356,8 +356,12 @@ __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
       }
     }
     const float G = gm[2 * jj] + gm[2 * jj + 1];
-    // staged over the left child, whose row tid only this thread has read
-    publish_node(cur, smem + (2 * jj) * kImgBytes, nbase + p.node_off[m0] + 2 * i + jj, G, s_red2, p.img, p.meta);
+    // staged over the left child, whose row tid only this thread has read.  An odd node
+    // is read by nothing but its parent (tile u reads Node_m[(u >> m) - 1] with u >> m
+    // odd; the export reads Node_m[(NT >> m) - 1] with NT >> m odd; the next launch reads
+    // the parents), so it stays in registers.
+    if (jj == 0)
+      publish_node(cur, smem, nbase + p.node_off[m0] + 2 * i, G, s_red2, p.img, p.meta);
     if (jj == 0) {
       G0 = G;
 #pragma unroll
