@@ -17,8 +17,9 @@
 // Kernels (chunk C <= 64 tokens; the forward's chunk states and Fenwick blocks first):
 //   bwd_intra     per chunk: the in-chunk pairs (levels 0 .. log2 C) of every output;
 //   bwd_inter_q   per query chunk, per set bit m of its index: dq and dlambda from the
-//                 block it reads, and that block's "dual" Σ w_t q_t dO_tᵀ (added up over
-//                 the query chunks that read the block, with atomics);
+//                 block it reads (both from the one product Bm dO_t), and that block's
+//                 "dual" Σ w_t q_t dO_tᵀ (added up over the query chunks that read the
+//                 block, with atomics);
 //   bwd_inter_kv  per key chunk, per level whose block holds it and has readers: dk and
 //                 dv from the dual, decayed from each key to the end of the block;
 //   bwd_final     group sums of dq and dk, casts;
@@ -212,7 +213,8 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
     }
     __syncthreads();
     for (int e = tid; e < C * dv; e += kT) dw[e] = wl[e / dv] * ds[e];
-    // dqᵀ = Bm dOᵀ (rows i of d_k, columns t): dq_t += w_t (Bm dO_t)
+    // (Bm dO_t) for every t, as dqᵀ = Bm dOᵀ (rows i of d_k, columns t): dq_t += w_t (Bm dO_t),
+    // and dl_t = q_tᵀ (Bm dO_t) from the same tiles
     smem_mm(dk, C, dv, Bm, dv, 1, dT, CP, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
       for (int jj = 0; jj < 4; ++jj) {
         const int t = n0 + jj;
@@ -224,13 +226,8 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
         o4.z += w * acc[2][jj];
         o4.w += w * acc[3][jj];
         *d4 = o4;
-      }
-    });
-    // U = Q Bm, reduced at once against dO: dl_t = q_tᵀ Bm dO_t
-    smem_mm(C, dv, dk, qs, dk, 1, Bm, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
-      for (int i = 0; i < 4; ++i) {
-        const float* d = ds + (m0 + i) * dv + n0;
-        atomicAdd(dl + m0 + i, acc[i][0] * d[0] + acc[i][1] * d[1] + acc[i][2] * d[2] + acc[i][3] * d[3]);
+        const float4 q4 = *reinterpret_cast<const float4*>(qs + t * dk + m0);
+        atomicAdd(dl + t, q4.x * acc[0][jj] + q4.y * acc[1][jj] + q4.z * acc[2][jj] + q4.w * acc[3][jj]);
       }
     });
     __syncthreads();  // dw and dl complete
