@@ -108,11 +108,18 @@ __global__ void __launch_bounds__(kT) bwd_intra(GenPlan p, BwdArgs x, size_t off
     ls[e] = x.lam[(((size_t)b * p.T + t0 + t) * p.H + h) * L + l];
   }
   __syncthreads();
-  smem_mm(C, C, dk, qs, dk, 1, kTr, CP, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+  // causal ranges: tiles of (t, s) above the diagonal are zero; in dS K (rows t) only keys
+  // s < m0 + 4 contribute, in dSᵀ Q and Pᵀ dO (rows s) only queries t >= m0
+  auto lower = [](int m0, int n0, int& kb, int& ke) {
+    if (n0 > m0) kb = ke = 0;
+  };
+  auto upto = [](int m0, int, int& kb, int& ke) { ke = m0 + 4; };
+  auto from = [](int m0, int, int& kb, int& ke) { kb = m0; };
+  smem_mm_r(C, C, dk, qs, dk, 1, kTr, CP, tid, kT, lower, [&](int m0, int n0, float (&acc)[4][4]) {
     for (int i = 0; i < 4; ++i)
       for (int jj = 0; jj < 4; ++jj) P[(m0 + i) * C + n0 + jj] = acc[i][jj];
   });
-  smem_mm(C, C, dv, ds, dv, 1, vTr, CP, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+  smem_mm_r(C, C, dv, ds, dv, 1, vTr, CP, tid, kT, lower, [&](int m0, int n0, float (&acc)[4][4]) {
     for (int i = 0; i < 4; ++i)
       for (int jj = 0; jj < 4; ++jj) dS[(m0 + i) * C + n0 + jj] = acc[i][jj];
   });
@@ -138,15 +145,15 @@ __global__ void __launch_bounds__(kT) bwd_intra(GenPlan p, BwdArgs x, size_t off
   float* dv32 = reinterpret_cast<float*>(x.ws + off_dv);
   auto row = [&](int r) { return ((size_t)b * p.T + t0 + r) * p.H + h; };
   // dq = dS K (rows: queries); dk = dSᵀ Q and dv = Pᵀ dO (rows: keys)
-  smem_mm(C, dk, C, dS, C, 1, ks, dk, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+  smem_mm_r(C, dk, C, dS, C, 1, ks, dk, tid, kT, upto, [&](int m0, int n0, float (&acc)[4][4]) {
     for (int i = 0; i < 4; ++i)
       *reinterpret_cast<float4*>(dq32 + row(m0 + i) * dk + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
   });
-  smem_mm(C, dk, C, dS, 1, C, qs, dk, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+  smem_mm_r(C, dk, C, dS, 1, C, qs, dk, tid, kT, from, [&](int m0, int n0, float (&acc)[4][4]) {
     for (int i = 0; i < 4; ++i)
       *reinterpret_cast<float4*>(dk32 + row(m0 + i) * dk + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
   });
-  smem_mm(C, dv, C, P, 1, C, ds, dv, tid, kT, [&](int m0, int n0, float (&acc)[4][4]) {
+  smem_mm_r(C, dv, C, P, 1, C, ds, dv, tid, kT, from, [&](int m0, int n0, float (&acc)[4][4]) {
     for (int i = 0; i < 4; ++i)
       *reinterpret_cast<float4*>(dv32 + row(m0 + i) * dv + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
   });

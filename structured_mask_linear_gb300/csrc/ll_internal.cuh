@@ -117,10 +117,12 @@ __host__ __device__ inline int bit_length(long long x) {
 // A(m, k) = a[m*sam + k*sak] and B(k, n) = b[k*sbk + n] (b rows 16-byte aligned), then
 // epi(m0, n0, acc).  Threads of a warp share m0 where N/4 >= 32 (A is a broadcast) and
 // read consecutive float4s of B.  Where A's k (sak == 1) or m (sam == 1) index is
-// contiguous and 16-byte aligned, A is read four values per load.
-template <typename Epi>
-__device__ __forceinline__ void smem_mm(int M, int N, int K, const float* a, int sam, int sak,
-                                        const float* b, int sbk, int tid, int nthr, Epi epi) {
+// contiguous and 16-byte aligned, A is read four values per load.  smem_mm_r takes the
+// k range of each tile from range(m0, n0, kb, ke) (multiples of 4; outside it the
+// products are known to be zero, e.g. above a causal diagonal).
+template <typename Range, typename Epi>
+__device__ __forceinline__ void smem_mm_r(int M, int N, int K, const float* a, int sam, int sak,
+                                          const float* b, int sbk, int tid, int nthr, Range range, Epi epi) {
   const int tn_count = N >> 2;
   const int tiles = (M >> 2) * tn_count;
   const bool a16 = (reinterpret_cast<uintptr_t>(a) & 15u) == 0;
@@ -135,9 +137,11 @@ __device__ __forceinline__ void smem_mm(int M, int N, int K, const float* a, int
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     const float* ap = a + (size_t)m0 * sam;
     const float* bp = b + n0;
+    int kb = 0, ke = K;
+    range(m0, n0, kb, ke);
     if (krow) {
 #pragma unroll 2
-      for (int k = 0; k < K; k += 4) {
+      for (int k = kb; k < ke; k += 4) {
         float ar[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -161,7 +165,7 @@ __device__ __forceinline__ void smem_mm(int M, int N, int K, const float* a, int
       }
     } else if (mcol) {
 #pragma unroll 4
-      for (int k = 0; k < K; ++k) {
+      for (int k = kb; k < ke; ++k) {
         const float4 x = *reinterpret_cast<const float4*>(ap + (size_t)k * sak);
         const float4 bv = *reinterpret_cast<const float4*>(bp + (size_t)k * sbk);
         const float av[4] = {x.x, x.y, x.z, x.w};
@@ -175,7 +179,7 @@ __device__ __forceinline__ void smem_mm(int M, int N, int K, const float* a, int
       }
     } else {
 #pragma unroll 4
-      for (int k = 0; k < K; ++k) {
+      for (int k = kb; k < ke; ++k) {
         const float4 bv = *reinterpret_cast<const float4*>(bp + (size_t)k * sbk);
         float av[4];
 #pragma unroll
@@ -191,6 +195,11 @@ __device__ __forceinline__ void smem_mm(int M, int N, int K, const float* a, int
     }
     epi(m0, n0, acc);
   }
+}
+template <typename Epi>
+__device__ __forceinline__ void smem_mm(int M, int N, int K, const float* a, int sam, int sak,
+                                        const float* b, int sbk, int tid, int nthr, Epi epi) {
+  smem_mm_r(M, N, K, a, sam, sak, b, sbk, tid, nthr, [](int, int, int&, int&) {}, epi);
 }
 
 __device__ __forceinline__ float ll_load(const float* p, size_t i) { return p[i]; }
