@@ -15,7 +15,10 @@
 //     sum_l lambda_u^l dlambda_u^l (o is linear in lambda_u) and C_u = v_u . dv_u;
 //     this is the sum of the terms A_ts over t >= r > s, in which log a_r appears.
 // Kernels (chunk C <= 64 tokens; the forward's chunk states and Fenwick blocks first):
-//   bwd_intra     per chunk: the in-chunk pairs (levels 0 .. log2 C) of every output;
+//   bwd_intra     per chunk: the in-chunk pairs (levels 0 .. log2 C) of every output; for
+//                 bf16, d_k = 128, d_v = 64 and T % 128 == 0 the tensor-core kernel
+//                 tc_bwd_intra does the pairs inside 128-token tiles instead (chunk level
+//                 0 included), and the two inter kernels start at chunk level 1;
 //   bwd_inter_q   per query chunk, per set bit m of its index: dq and dlambda from the
 //                 block it reads (both from the one product Bm dO_t), and that block's
 //                 "dual" Σ w_t q_t dO_tᵀ (added up over the query chunks that read the
@@ -169,7 +172,8 @@ __global__ void __launch_bounds__(kT) bwd_intra(GenPlan p, BwdArgs x, size_t off
 
 // ---- query side of the inter-chunk levels ---------------------------------------------
 template <typename TIn>
-__global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t off_dq, size_t off_dual) {
+__global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t off_dq, size_t off_dual,
+                                                 int m_start) {
   extern __shared__ __align__(16) float sm[];
   const int C = p.C, dk = p.dk, dv = p.dv, L = p.L;
   const int j = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
@@ -208,6 +212,10 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
   for (int m = 0; (j >> m) > 0; ++m) {
     if (!((j >> m) & 1)) continue;
     const int bidx = p.blk_off[m] + (((j >> m) - 1) >> 1);
+    if (m < m_start) {  // done by the in-tile kernel; its decay still separates the levels above
+      D += blkG[bidx];
+      continue;
+    }
     const int lvl = p.clog + 1 + m;
     __syncthreads();  // the previous level is done with the buffers
     const float* Bsrc = blk + ((size_t)bh * p.nblk + bidx) * S;
@@ -253,7 +261,7 @@ __global__ void __launch_bounds__(kT) bwd_inter_q(GenPlan p, BwdArgs x, size_t o
 // ---- key side of the inter-chunk levels -----------------------------------------------
 template <typename TIn>
 __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t off_dk, size_t off_dv,
-                                                  size_t off_dual) {
+                                                  size_t off_dual, int m_start) {
   extern __shared__ __align__(16) float sm[];
   const int C = p.C, dk = p.dk, dv = p.dv;
   const int u = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
@@ -282,7 +290,7 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
   float* dv32 = reinterpret_cast<float*>(x.ws + off_dv);
   auto row = [&](int r) { return ((size_t)b * p.T + t0 + r) * p.H + h; };
   const float gend = g[C - 1];
-  for (int m = 0; m < p.M; ++m) {
+  for (int m = m_start; m < p.M; ++m) {
     const int i = u >> m;
     // node (m, i) is read at level log2 C + 1 + m by the chunks of node (m, i + 1) when
     // i is even and that node starts inside the sequence
@@ -416,7 +424,7 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
 }
 
 template <typename TIn>
-cudaError_t run_bwd(const BwdPlan& bp, const BwdArgs& x, const FwdArgs& fa, cudaStream_t st) {
+cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, const FwdArgs& fa, cudaStream_t st) {
   const GenPlan& p = bp.g;
   const int BH = p.B * p.H;
   const int C = p.C, dk = p.dk, dv = p.dv;
@@ -426,26 +434,37 @@ cudaError_t run_bwd(const BwdPlan& bp, const BwdArgs& x, const FwdArgs& fa, cuda
   if ((e = cudaMemsetAsync(x.ws + bp.off_dual, 0, sizeof(float) * (size_t)BH * p.nblk * dk * dv, st)) !=
       cudaSuccess)
     return e;
-  const size_t sm1 = sizeof(float) * ((size_t)2 * C * dk + (size_t)(C + 4) * (dk + dv) + C * dv + C +
-                                      C * (p.clog + 1) + 3 * C * C);
-  if ((e = cudaFuncSetAttribute(bwd_intra<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) !=
-      cudaSuccess)
-    return e;
-  bwd_intra<TIn><<<dim3(p.N, BH), kT, sm1, st>>>(p, x, bp.off_dq, bp.off_dk, bp.off_dv);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
+  // the pairs inside 128-token tiles (two 64-token chunks) on the tensor cores where the
+  // shape allows; the inter-chunk kernels then start at chunk level 1
+  const bool tc = sizeof(TIn) == 2 && C == 64 && tc_supported(s);
+  const int m_start = tc ? 1 : 0;
+  if (tc) {
+    if ((e = launch_tc_bwd_intra(s, x.q, x.k, x.v, x.dO, x.a, x.lam, reinterpret_cast<float*>(x.ws + bp.off_dq),
+                                 reinterpret_cast<float*>(x.ws + bp.off_dk),
+                                 reinterpret_cast<float*>(x.ws + bp.off_dv), x.dlam, fa.status, st)) != cudaSuccess)
+      return e;
+  } else {
+    const size_t sm1 = sizeof(float) * ((size_t)2 * C * dk + (size_t)(C + 4) * (dk + dv) + C * dv + C +
+                                        C * (p.clog + 1) + 3 * C * C);
+    if ((e = cudaFuncSetAttribute(bwd_intra<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) !=
+        cudaSuccess)
+      return e;
+    bwd_intra<TIn><<<dim3(p.N, BH), kT, sm1, st>>>(p, x, bp.off_dq, bp.off_dk, bp.off_dv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launch();
+  }
   const size_t sm2 = sizeof(float) * ((size_t)C * dk + 3 * C * dv + dk * dv + 3 * C);
   if ((e = cudaFuncSetAttribute(bwd_inter_q<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) !=
       cudaSuccess)
     return e;
-  bwd_inter_q<TIn><<<dim3(p.N, BH), kT, sm2, st>>>(p, x, bp.off_dq, bp.off_dual);
+  bwd_inter_q<TIn><<<dim3(p.N, BH), kT, sm2, st>>>(p, x, bp.off_dq, bp.off_dual, m_start);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   const size_t sm3 = sizeof(float) * ((size_t)C * dk + (size_t)(C + 4) * dv + dk * dv + C);
   if ((e = cudaFuncSetAttribute(bwd_inter_kv<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) !=
       cudaSuccess)
     return e;
-  bwd_inter_kv<TIn><<<dim3(p.N, BH), kT, sm3, st>>>(p, x, bp.off_dk, bp.off_dv, bp.off_dual);
+  bwd_inter_kv<TIn><<<dim3(p.N, BH), kT, sm3, st>>>(p, x, bp.off_dk, bp.off_dv, bp.off_dual, m_start);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   const size_t n = (size_t)p.B * p.T * (p.G * dk + p.H * dv);
@@ -473,7 +492,7 @@ cudaError_t launch_bwd(const ll_shape& s, const void* q, const void* k, const vo
   if (!make_bwd_plan(s, &bp)) return cudaErrorInvalidValue;
   BwdArgs x{q, k, v, a, lam, dO, dq, dk, dv, dloga, dlam, ws};
   FwdArgs fa{q, k, v, a, lam, nullptr, ws, nullptr, nullptr, 0, status, nullptr, 0};
-  return s.dtype == LL_BF16 ? run_bwd<__nv_bfloat16>(bp, x, fa, st) : run_bwd<float>(bp, x, fa, st);
+  return s.dtype == LL_BF16 ? run_bwd<__nv_bfloat16>(s, bp, x, fa, st) : run_bwd<float>(s, bp, x, fa, st);
 }
 
 }  // namespace ll

@@ -98,6 +98,11 @@ cudaError_t launch_tc_naive(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
 size_t tc_ssd_bytes(const TcPlan& p);
 cudaError_t launch_tc_ssd(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
 const char* tc_kernel_names(bool with_export);
+// Backward: the in-tile pairs (levels 0..7) on the tensor cores, for tc_supported shapes;
+// assigns the fp32 per-head dq, dk, dv buffers and dlambda (levels >= 8 zeroed).
+cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k, const void* v, const void* dO,
+                                const float* a, const float* lam, float* dq32, float* dk32, float* dv32,
+                                float* dlam, unsigned* status, cudaStream_t st);
 
 __host__ __device__ inline int bit_length(long long x) {
   int l = 0;

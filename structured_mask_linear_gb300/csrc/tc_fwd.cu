@@ -1068,6 +1068,422 @@ __global__ void wait_selftest_kernel(unsigned* status, long long spins) {
 }
 
 // ---------------------------------------------------------------------------------
+// tc_bwd_intra: the in-tile pairs (levels 0..7) of the backward on the tensor cores.
+//
+// Chain rule on o_t = sum_{s<=t} lambda_t^{l(t,s)} 2^(g_t - g_s) (q_t . k_s) v_s for the
+// loss sum(dO . o), restricted to pairs inside one 128-token tile (u): with S = Q Kᵀ,
+// E = dO Vᵀ and w_ts = lambda_t^{l(t,s)} 2^(g_t - g_s) [s <= t],
+//   dq = (w ⊙ E) K,  dk = (w ⊙ E)ᵀ Q,  dv = (w ⊙ S)ᵀ dO,
+//   dlambda_t^l = sum over s at level l of 2^(g_t - g_s) S_ts E_ts   (l = 0..7).
+// One CTA (256 threads, one per SM: 512 TMEM columns, 175 KB shared memory) per
+// (b, h, tile):
+//   S and E on the tensor cores from the bf16 inputs (TMEM columns 0..127, 128..255);
+//   role a (warps 0-3, thread = query row): dS = w ⊙ E and P = w ⊙ S as fp16 with
+//     power-of-two tile scales into shared memory (in the layout a TMA box of 64 columns
+//     has), dlambda from S ⊙ E in fp32;
+//   role b (warps 4-7): Q, K and dO to fp16 in place with power-of-two tile scales;
+//   dq = dS K (columns 256..383), dk = dSᵀ Q (384..511) and dv = Pᵀ dO (0..63) on the
+//   tensor cores; dq rows are read by role a, dk and dv rows (keys) by role b, and all
+//   three are written to the fp32 per-head gradient buffers (assigned, not added).
+// The pairs across tiles are the inter-tile part of the backward.
+// ---------------------------------------------------------------------------------
+struct TcBwdParams {
+  int B, T, H, hpg, G, L, NT;
+  const float* a;
+  const float* lam;
+  float* dq32;   // (B, T, H, d_k) fp32, per head
+  float* dk32;   // (B, T, H, d_k)
+  float* dv32;   // (B, T, H, d_v)
+  float* dlam;   // (B, T, H, L): levels 0..7 written, the rest zeroed
+  unsigned* status;
+};
+
+constexpr int kBwdFixed = 163840;  // Q, K, V, dO, dS, P in front of the small tables
+constexpr int kSmemBwd = kBwdFixed + 2 * 128 * 4 + 2 * 128 * 9 * 4 + 1024;
+
+// Shared-memory address of the 16-byte chunk holding keys 8c..8c+7 (c = 0..15) of row r of
+// a 128 x 128 fp16 tile stored as two 64-column boxes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t tile_chunk(int r, int c) {
+  return (uint32_t)((c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap mapQ,
+                                                              const __grid_constant__ CUtensorMap mapK,
+                                                              const __grid_constant__ CUtensorMap mapV,
+                                                              const __grid_constant__ CUtensorMap mapD,
+                                                              TcBwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* RQ = smem;            // 32 KB: Q (bf16, then fp16)
+  uint8_t* RK = smem + 32768;    // 32 KB: K (bf16, then fp16)
+  uint8_t* RV = smem + 65536;    // 16 KB: V (bf16)
+  uint8_t* RD = smem + 81920;    // 16 KB: dO (bf16, then fp16)
+  uint8_t* RS = smem + 98304;    // 32 KB: dS (fp16)
+  uint8_t* RP = smem + 131072;   // 32 KB: P (fp16)
+  float* sG = reinterpret_cast<float*>(smem + kBwdFixed);  // 128: g
+  float* sB8 = sG + 128;                                    // 128: 2^(g_end8(s) - g_s)
+  float* sLam8 = sB8 + 128;                                 // 128 x 9: lambda levels 0..7 of row r
+  float* sAcc = sLam8 + 128 * 9;                            // 128 x 9: dlambda of the diagonal group
+  __shared__ __align__(8) uint64_t bar_ld, bar_se, bar_mm;
+  __shared__ uint32_t tmem_base;
+  __shared__ float s_red[8];
+  __shared__ float s_mx[8][3];
+  __shared__ int s_sc[6];  // tile scale exponents: dS, P (role a); Q, K, dO (role b)
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & 127, quad = warp & 3, rot = r & 7;
+  const bool role_b = warp >= 4;
+  const int lin = blockIdx.x;
+  const int h = lin % p.H;
+  const int u = (lin / p.H) % p.NT;
+  const int b = lin / (p.H * p.NT);
+  const int g = h / p.hpg;
+  const long long t0 = (long long)u * kTile;
+  const size_t row = (size_t)b * p.T + t0 + r;  // token of this thread's row
+  const float* lrow = p.lam + (row * p.H + h) * p.L;
+
+  if (tid == 0) {
+    ptx::mbar_init(&bar_ld, 1);
+    ptx::mbar_init(&bar_se, 1);
+    ptx::mbar_init(&bar_mm, 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 * 2 + 16384 * 2);
+    ptx::tma_load_4d(RQ, &mapQ, &bar_ld, 0, g, (int)t0, b);
+    ptx::tma_load_4d(RQ + 16384, &mapQ, &bar_ld, 64, g, (int)t0, b);
+    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
+    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
+    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
+    ptx::tma_load_4d(RD, &mapD, &bar_ld, 0, h, (int)t0, b);
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_base, 512);
+    ptx::tmem_relinquish();
+  }
+  if (!role_b) {
+#pragma unroll
+    for (int l = 0; l < kLevIntra; ++l) ptx::cp_async4(sLam8 + r * 9 + l, lrow + l);
+#pragma unroll
+    for (int l = 0; l < 9; ++l) sAcc[r * 9 + l] = 0.f;
+  }
+  // chunk-local log2 decay cumsum over the 128 rows (both roles compute it)
+  float gt = log2f(p.a[row * p.H + h]);
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, gt, off);
+    if (lane >= off) gt += y;
+  }
+  if (lane == 31) s_red[warp] = gt;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  for (int w = 0; w < quad; ++w) gt += s_red[w];
+  const uint32_t tbase = tmem_base;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const uint32_t tS = tbase, tE = tbase + 128, tDQ = tbase + 256, tDK = tbase + 384, tDV = tbase;
+  if (!role_b) sG[r] = gt;
+  __syncthreads();
+  if (!role_b) sB8[r] = exp2f(sG[r | 7] - gt);
+  bool ok = wait_bar(&bar_ld, 0);
+  if (!ok) atomicExch(p.status, kStatusTimeout);
+  ok = __syncthreads_and(ok);
+
+  // S = Q Kᵀ (K = 128 d_k) and E = dO Vᵀ (K = 64 d_v), bf16, all K-major
+  if (ok && tid == 128) {
+    ptx::tc_fence_after();
+    const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 0);
+    const uint32_t q0 = ptx::smem_u32(RQ), k0 = ptx::smem_u32(RK);
+    const uint32_t d0 = ptx::smem_u32(RD), v0 = ptx::smem_u32(RV);
+#pragma unroll
+    for (int kk = 0; kk < kDk / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+      ptx::umma_f16(tS, ptx::smem_desc_sw128(q0 + off, 16, 1024), ptx::smem_desc_sw128(k0 + off, 16, 1024),
+                    idesc, kk > 0);
+    }
+#pragma unroll
+    for (int kk = 0; kk < kDv / 16; ++kk)
+      ptx::umma_f16(tE, ptx::smem_desc_sw128(d0 + kk * 32, 16, 1024), ptx::smem_desc_sw128(v0 + kk * 32, 16, 1024),
+                    idesc, kk > 0);
+    ptx::umma_commit(&bar_se);
+  }
+  const bool se_issued = ok;
+  if (ok) {
+    ok = wait_bar(&bar_se, 0);
+    if (!ok) atomicExch(p.status, kStatusTimeout);
+  }
+  ok = __syncthreads_and(ok);  // also: S and E no longer read Q, K, V, dO
+
+  if (!role_b) {
+    // ---- role a: dS and P into shared memory, dlambda ------------------------------
+    const int t = r, tl = t & 31;
+    const float* lamr = sLam8 + r * 9;
+    float lmax = 0.f, smax = 0.f, emax = 0.f;
+    ptx::cp_async_wait_all();  // lambda of this row (issued by this thread)
+    if (ok) {
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int l = 0; l < kLevIntra; ++l) lmax = fmaxf(lmax, fabsf(lamr[l]));
+#pragma unroll 1
+      for (int cg = 0; cg <= quad; ++cg) {
+        float sv[32], ev[32];
+        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+        ptx::tmem_ld32(tE + lane_off + cg * 32, ev);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (cg < quad || j <= tl) {
+            smax = fmaxf(smax, fabsf(sv[j]));
+            emax = fmaxf(emax, fabsf(ev[j]));
+          }
+      }
+    }
+    // tile maxima of |P| <= max|S| max lambda and |dS| <= max|E| max lambda (decays <= 1)
+    float mp = smax * lmax, ms = emax * lmax;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, off));
+      ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, off));
+    }
+    if (lane == 0) {
+      s_mx[warp][0] = ms;
+      s_mx[warp][1] = mp;
+    }
+    ptx::named_bar_sync(1, 128);
+    const int es = f16_exp(fmaxf(fmaxf(s_mx[0][0], s_mx[1][0]), fmaxf(s_mx[2][0], s_mx[3][0])));
+    const int ep = f16_exp(fmaxf(fmaxf(s_mx[0][1], s_mx[1][1]), fmaxf(s_mx[2][1], s_mx[3][1])));
+    if (tid == 0) {
+      s_sc[0] = es;
+      s_sc[1] = ep;
+    }
+    const float cs = pow2i(-es), cp = pow2i(-ep);
+    float acc6 = 0.f, acc7 = 0.f;
+    const float* gq = sG + quad * 32;
+    const float span8 = fmaxf(fmaxf(gq[0] - gq[7], gq[8] - gq[15]), fmaxf(gq[16] - gq[23], gq[24] - gq[31]));
+    const bool fastd = span8 <= 60.f;
+#pragma unroll 1
+    for (int cg = 0; cg < 4; ++cg) {
+      uint32_t pd[16], pp[16];
+      if (ok && cg < quad) {
+        // keys of an earlier 32-group: one level (6 or 7) and the factored decay
+        float sv[32], ev[32];
+        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+        ptx::tmem_ld32(tE + lane_off + cg * 32, ev);
+        ptx::tmem_ld_wait();
+        const bool l7 = (quad ^ cg) >= 2;
+        const float lv = lamr[l7 ? 7 : 6];
+        float ak[4];
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) ak[kb] = exp2f(gt - sG[cg * 32 + kb * 8 + 7]);
+        const float4* b4 = reinterpret_cast<const float4*>(sB8 + cg * 32);
+        float xs = 0.f;
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 bb = b4[j4];
+          const float bj[4] = {bb.x, bb.y, bb.z, bb.w};
+          float vs[4], vp[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * j4 + e;
+            const float dd = ak[j4 >> 1] * bj[e];
+            xs += dd * (sv[j] * ev[j]);
+            const float w = lv * dd;
+            vs[e] = (w * cs) * ev[j];
+            vp[e] = (w * cp) * sv[j];
+          }
+          pd[2 * j4] = pack_h2(vs[0], vs[1]);
+          pd[2 * j4 + 1] = pack_h2(vs[2], vs[3]);
+          pp[2 * j4] = pack_h2(vp[0], vp[1]);
+          pp[2 * j4 + 1] = pack_h2(vp[2], vp[3]);
+        }
+        if (l7) acc7 += xs;
+        else acc6 += xs;
+      } else if (ok && cg == quad) {
+        // the diagonal 32-group: levels 0..5 (level of key j: bit length of tl ^ j)
+        float sv[32], ev[32];
+        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
+        ptx::tmem_ld32(tE + lane_off + cg * 32, ev);
+        ptx::tmem_ld_wait();
+        float ak[4];
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) ak[kb] = exp2f(gt - gq[kb * 8 + 7]);
+        const float4* b4 = reinterpret_cast<const float4*>(sB8 + cg * 32);
+        float* accr = sAcc + r * 9;
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 bb = b4[j4];
+          const float bj[4] = {bb.x, bb.y, bb.z, bb.w};
+          float vs[4], vp[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * j4 + e;
+            // blocks after t's may give ak = inf; their keys are masked by the select
+            const float dd = fastd ? ak[j >> 3] * bj[e] : exp2f(gt - gq[j]);
+            const int lvj = 32 - __clz(tl ^ j);
+            const bool on = j <= tl;
+            const float w = on ? lamr[lvj] * dd : 0.f;
+            vs[e] = (w * cs) * ev[j];
+            vp[e] = (w * cp) * sv[j];
+            if (on) accr[lvj] += dd * (sv[j] * ev[j]);
+          }
+          pd[2 * j4] = pack_h2(vs[0], vs[1]);
+          pd[2 * j4 + 1] = pack_h2(vs[2], vs[3]);
+          pp[2 * j4] = pack_h2(vp[0], vp[1]);
+          pp[2 * j4 + 1] = pack_h2(vp[2], vp[3]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pd[j] = pp[j] = 0u;
+      }
+      // keys cg*32 .. cg*32+31 are chunks 4cg .. 4cg+3 of row r
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t off = tile_chunk(r, 4 * cg + q4);
+        *reinterpret_cast<uint4*>(RS + off) = make_uint4(pd[4 * q4], pd[4 * q4 + 1], pd[4 * q4 + 2], pd[4 * q4 + 3]);
+        *reinterpret_cast<uint4*>(RP + off) = make_uint4(pp[4 * q4], pp[4 * q4 + 1], pp[4 * q4 + 2], pp[4 * q4 + 3]);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    if (ok) {
+      float* dl = p.dlam + (row * p.H + h) * p.L;
+      const float* accr = sAcc + r * 9;
+#pragma unroll
+      for (int l = 0; l < 6; ++l) dl[l] = accr[l];
+      dl[6] = acc6 + accr[6];
+      dl[7] = acc7 + accr[7];
+      for (int l = kLevIntra; l < p.L; ++l) dl[l] = 0.f;  // inter-tile levels: added later
+    }
+  } else {
+    // ---- role b: Q, K, dO -> fp16 in place with tile scales ---------------------------
+    uint32_t mq = 0u, mk = 0u, md = 0u;
+    uint8_t* qr0 = RQ + r * 128;
+    uint8_t* kr0 = RK + r * 128;
+    uint8_t* dr0 = RD + r * 128;
+    if (ok) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int cc = (c ^ rot) << 4;
+        mq = absmax_u4(absmax_u4(mq, *reinterpret_cast<const uint4*>(qr0 + cc)),
+                       *reinterpret_cast<const uint4*>(qr0 + 16384 + cc));
+        mk = absmax_u4(absmax_u4(mk, *reinterpret_cast<const uint4*>(kr0 + cc)),
+                       *reinterpret_cast<const uint4*>(kr0 + 16384 + cc));
+        md = absmax_u4(md, *reinterpret_cast<const uint4*>(dr0 + cc));
+      }
+    }
+    float fq = bf16x2_maxhalf(mq), fk = bf16x2_maxhalf(mk), fd = bf16x2_maxhalf(md);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      fq = fmaxf(fq, __shfl_xor_sync(0xffffffffu, fq, off));
+      fk = fmaxf(fk, __shfl_xor_sync(0xffffffffu, fk, off));
+      fd = fmaxf(fd, __shfl_xor_sync(0xffffffffu, fd, off));
+    }
+    if (lane == 0) {
+      s_mx[warp][0] = fq;
+      s_mx[warp][1] = fk;
+      s_mx[warp][2] = fd;
+    }
+    ptx::named_bar_sync(2, 128);
+    int ex[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+      ex[i] = f16_exp(fmaxf(fmaxf(s_mx[4][i], s_mx[5][i]), fmaxf(s_mx[6][i], s_mx[7][i])));
+    if (tid == 128) {
+      s_sc[2] = ex[0];
+      s_sc[3] = ex[1];
+      s_sc[4] = ex[2];
+    }
+    if (ok) {
+      const float sq = pow2i(-ex[0]), sk = pow2i(-ex[1]), sd = pow2i(-ex[2]);
+      const __nv_bfloat162 q2 = __floats2bfloat162_rn(sq, sq), k2 = __floats2bfloat162_rn(sk, sk),
+                           d2 = __floats2bfloat162_rn(sd, sd);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int cc = (c ^ rot) << 4;
+        uint4* a0 = reinterpret_cast<uint4*>(qr0 + cc);
+        uint4* a1 = reinterpret_cast<uint4*>(qr0 + 16384 + cc);
+        uint4* b0 = reinterpret_cast<uint4*>(kr0 + cc);
+        uint4* b1 = reinterpret_cast<uint4*>(kr0 + 16384 + cc);
+        uint4* d0 = reinterpret_cast<uint4*>(dr0 + cc);
+        *a0 = bf16x8_to_f16x8(*a0, q2);
+        *a1 = bf16x8_to_f16x8(*a1, q2);
+        *b0 = bf16x8_to_f16x8(*b0, k2);
+        *b1 = bf16x8_to_f16x8(*b1, k2);
+        *d0 = bf16x8_to_f16x8(*d0, d2);
+      }
+      ptx::fence_proxy_async_smem();
+    }
+  }
+  ptx::tc_fence_before();
+  ok = __syncthreads_and(ok);  // dS, P, fp16 Q, K, dO and the scales complete; S, E read
+
+  // dq = dS K (keys), dk = dSᵀ Q and dv = Pᵀ dO (queries); fp16
+  if (ok && tid == 128) {
+    ptx::tc_fence_after();
+    const uint32_t s0 = ptx::smem_u32(RS), p0 = ptx::smem_u32(RP), q0 = ptx::smem_u32(RQ),
+                   k0 = ptx::smem_u32(RK), d0 = ptx::smem_u32(RD);
+    const uint32_t id_q = ptx::idesc_f16_f32(128, 128, 0, 1);
+    const uint32_t id_k = ptx::idesc_f16_f32(128, 128, 1, 1);
+    const uint32_t id_v = ptx::idesc_f16_f32(128, 64, 1, 1);
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk) {
+      const uint32_t offk = (kk >> 2) * 16384 + (kk & 3) * 32;  // K-major step over keys
+      ptx::umma_f16(tDQ, ptx::smem_desc_sw128(s0 + offk, 16, 1024), ptx::smem_desc_sw128(k0 + kk * 2048, 16384, 1024),
+                    id_q, kk > 0);
+      ptx::umma_f16(tDK, ptx::smem_desc_sw128(s0 + kk * 2048, 16384, 1024),
+                    ptx::smem_desc_sw128(q0 + kk * 2048, 16384, 1024), id_k, kk > 0);
+      ptx::umma_f16(tDV, ptx::smem_desc_sw128(p0 + kk * 2048, 16384, 1024),
+                    ptx::smem_desc_sw128(d0 + kk * 2048, 1024, 1024), id_v, kk > 0);
+    }
+    ptx::umma_commit(&bar_mm);
+  }
+  const bool mm_issued = ok;
+  if (ok) {
+    ok = wait_bar(&bar_mm, 0);
+    if (!ok) atomicExch(p.status, kStatusTimeout);
+  }
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok) {
+    ptx::tc_fence_after();
+    if (!role_b) {
+      const float sc = pow2s(s_sc[0] + s_sc[3]);  // dS and K
+      float* dst = p.dq32 + (row * p.H + h) * kDk;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kDk; c0 += 32) {
+        float y[32];
+        ptx::tmem_ld32(tDQ + lane_off + c0, y);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(sc * y[j], sc * y[j + 1], sc * y[j + 2], sc * y[j + 3]);
+      }
+    } else {
+      const float sk = pow2s(s_sc[0] + s_sc[2]);  // dS and Q
+      const float sv = pow2s(s_sc[1] + s_sc[4]);  // P and dO
+      float* dk = p.dk32 + (row * p.H + h) * kDk;
+      float* dv = p.dv32 + (row * p.H + h) * kDv;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kDk + kDv; c0 += 32) {
+        const bool isk = c0 < kDk;
+        float y[32];
+        ptx::tmem_ld32((isk ? tDK + c0 : tDV + (c0 - kDk)) + lane_off, y);
+        ptx::tmem_ld_wait();
+        const float s = isk ? sk : sv;
+        float* d = isk ? dk + c0 : dv + (c0 - kDk);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(d + j) = make_float4(s * y[j], s * y[j + 1], s * y[j + 2], s * y[j + 3]);
+      }
+    }
+  }
+  if (tid == 128) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
+    wait_bar(&bar_ld, 0);
+    if (se_issued) wait_bar(&bar_se, 0);
+    if (mm_issued) wait_bar(&bar_mm, 0);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tbase, 512);
+}
+
+// ---------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1293,6 +1709,25 @@ cudaError_t launch_tc_ssd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
     note_launch();
   }
   if ((e = launch_output<1>(tp, mQ, mK, mV, p, 1, st)) != cudaSuccess) return e;
+  note_launch();
+  return cudaSuccess;
+}
+
+cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k, const void* v, const void* dO,
+                                const float* a, const float* lam, float* dq32, float* dk32, float* dv32,
+                                float* dlam, unsigned* status, cudaStream_t st) {
+  if (!tc_supported(s)) return cudaErrorInvalidValue;
+  const int G = s.heads / s.heads_per_group, NT = s.T / kTile;
+  CUtensorMap mQ, mK, mV, mD;
+  if (!make_map(&mQ, q, kDk, G, s.T, s.batch) || !make_map(&mK, k, kDk, G, s.T, s.batch) ||
+      !make_map(&mV, v, kDv, s.heads, s.T, s.batch) || !make_map(&mD, dO, kDv, s.heads, s.T, s.batch))
+    return cudaErrorInvalidValue;
+  const TcBwdParams p{s.batch, s.T, s.heads, s.heads_per_group, G, s.levels, NT, a, lam,
+                      dq32, dk32, dv32, dlam, status};
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwd);
+  if (e != cudaSuccess) return e;
+  tc_bwd_intra_kernel<<<(unsigned)((size_t)s.batch * NT * s.heads), 256, kSmemBwd, st>>>(mQ, mK, mV, mD, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
 }

@@ -5,7 +5,9 @@ CPU tests.  Called through the C ABI.
 The bar is the forward's: relative L2 <= 1e-2 and max |err| <= 5e-2 RMS per gradient,
 the cast of dq, dk, dv to the input dtype charged at half an ulp.  Cases: fp32 and
 bf16, grouped and ungrouped heads, chunk counts that are not powers of two, every chunk
-length, slow decay (all levels live) and a one-chunk sequence.
+length, slow decay (all levels live) and a one-chunk sequence.  bf16 with d_k = 128,
+d_v = 64, T % 128 == 0 and chunk >= 64 takes the tensor-core kernel for the pairs inside
+128-token tiles (T = 1024 and 640 here, the decay cases too); the others the CUDA-core one.
 """
 import pytest
 import torch
@@ -47,7 +49,7 @@ def test_tiny_fp32(sml):
 
 
 @pytest.mark.parametrize("T,chunk", [(1024, 64), (64 * 37, 64), (64, 64), (512, 16), (768, 32),
-                                     (1024, 128)])
+                                     (1024, 128), (640, 64)])
 def test_bf16_grouped(sml, T, chunk):
     w = workload("small", batch=1, heads=4, T=T, levels=levels_for(T))
     _check(sml, w, make_inputs(w, "cpu", seed=32), chunk, f"T={T} C={chunk}")
