@@ -42,10 +42,13 @@ constexpr int kT = 256;  // threads per CTA
 
 struct BwdPlan {
   GenPlan g;       // the forward's chunk states and blocks, at chunk C <= 64
+  bool tc;         // 128-token tiles on the tensor cores (in-tile pairs, query side)
+  TcPlan tp;       // the forward's tree over tiles, at off_tc, when tc
   size_t off_dual; // BH * nblk * dk * dv fp32, zeroed per call
   size_t off_dq;   // (B, T, H, dk) fp32 per-head dq
   size_t off_dk;   // (B, T, H, dk) fp32 per-head dk
   size_t off_dv;   // (B, T, H, dv) fp32
+  size_t off_tc;
   size_t bytes;
 };
 
@@ -419,6 +422,9 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
   o = al(o + sizeof(float) * (size_t)s.batch * s.T * s.heads * s.d_k);
   bp->off_dv = o;
   o = al(o + sizeof(float) * (size_t)s.batch * s.T * s.heads * s.d_v);
+  bp->tc = s.dtype == LL_BF16 && bp->g.C == 64 && make_tc_plan(s, &bp->tp);
+  bp->off_tc = o;
+  if (bp->tc) o = al(o + bp->tp.bytes);
   bp->bytes = o;
   return true;
 }
@@ -435,10 +441,14 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
       cudaSuccess)
     return e;
   // the pairs inside 128-token tiles (two 64-token chunks) on the tensor cores where the
-  // shape allows; the inter-chunk kernels then start at chunk level 1
-  const bool tc = sizeof(TIn) == 2 && C == 64 && tc_supported(s);
+  // shape allows; the inter-chunk kernels then start at chunk level 1, and the query side
+  // of those levels runs on the tensor cores over the forward's tree of tile nodes
+  const bool tc = bp.tc;
   const int m_start = tc ? 1 : 0;
   if (tc) {
+    FwdArgs ta = fa;
+    ta.ws = x.ws + bp.off_tc;
+    if ((e = launch_tc_nodes(bp.tp, ta, st)) != cudaSuccess) return e;
     if ((e = launch_tc_bwd_intra(s, x.q, x.k, x.v, x.dO, x.a, x.lam, reinterpret_cast<float*>(x.ws + bp.off_dq),
                                  reinterpret_cast<float*>(x.ws + bp.off_dk),
                                  reinterpret_cast<float*>(x.ws + bp.off_dv), x.dlam, fa.status, st)) != cudaSuccess)
@@ -457,9 +467,18 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
   if ((e = cudaFuncSetAttribute(bwd_inter_q<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) !=
       cudaSuccess)
     return e;
-  bwd_inter_q<TIn><<<dim3(p.N, BH), kT, sm2, st>>>(p, x, bp.off_dq, bp.off_dual, m_start);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
+  if (tc) {
+    int dual_off[32];
+    for (int m = 0; m < 32; ++m) dual_off[m] = m + 1 < p.M ? p.blk_off[m + 1] : 0;  // chunk level m + 1
+    if ((e = launch_tc_bwd_q(bp.tp, x.q, x.dO, x.a, x.lam, x.ws + bp.off_tc, reinterpret_cast<float*>(x.ws + bp.off_dq),
+                             x.dlam, reinterpret_cast<float*>(x.ws + bp.off_dual), dual_off, p.nblk, fa.status,
+                             st)) != cudaSuccess)
+      return e;
+  } else {
+    bwd_inter_q<TIn><<<dim3(p.N, BH), kT, sm2, st>>>(p, x, bp.off_dq, bp.off_dual, m_start);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launch();
+  }
   const size_t sm3 = sizeof(float) * ((size_t)C * dk + (size_t)(C + 4) * dv + dk * dv + C);
   if ((e = cudaFuncSetAttribute(bwd_inter_kv<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) !=
       cudaSuccess)

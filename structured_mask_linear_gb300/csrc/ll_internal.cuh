@@ -98,6 +98,14 @@ cudaError_t launch_tc_naive(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
 size_t tc_ssd_bytes(const TcPlan& p);
 cudaError_t launch_tc_ssd(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
 const char* tc_kernel_names(bool with_export);
+// The forward's tree only (tile states, levels above), into a.ws laid out per p.
+cudaError_t launch_tc_nodes(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
+// Backward, query side of the inter-tile levels on the tensor cores: adds into dq32,
+// assigns dlambda levels >= 8 of the set bits, adds the nodes' duals (dual slot of the
+// even node (m, i): dual_off[m] + i / 2, nslots per (b, h); dual zero before the first call).
+cudaError_t launch_tc_bwd_q(const TcPlan& p, const void* q, const void* dO, const float* a, const float* lam,
+                            const char* tree_ws, float* dq32, float* dlam, float* dual, const int* dual_off,
+                            int nslots, unsigned* status, cudaStream_t st);
 // Backward: the in-tile pairs (levels 0..7) on the tensor cores, for tc_supported shapes;
 // assigns the fp32 per-head dq, dk, dv buffers and dlambda (levels >= 8 zeroed).
 cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k, const void* v, const void* dO,

@@ -1484,6 +1484,326 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------------
+// tc_bwd_q: the query side of the inter-tile levels of the backward on the tensor cores.
+//
+// With the forward's tree over tiles (node images and scalars), tile u reads for every set
+// bit m of u the node N = Node_m[(u >> m) - 1] with weight w_t = lambda_t^(8+m) 2^(g_t + D_m)
+// (o_t += w_t q_tᵀ N).  Its backward, per level:
+//   dq_t += w_t N dO_t                   Z = dO Nᵀ, added into registers with w_t;
+//   dlambda_t^(8+m) = 2^(g_t + D_m) q_tᵀ N dO_t    Y = Q N, dotted with dO_t;
+//   dual(N) += sum_t w_t q_t dO_tᵀ       Qᵀ diag(w) dO, added into the node's fp32 dual
+//                                        with vector atomics (the readers of a node are
+//                                        the 2^m tiles of the node after it).
+// One CTA (256 threads, two per SM) per (b, h, tile) with u > 0; levels nearest first,
+// node images two deep.  Q, dO fp16 with power-of-two tile scales, diag(w) dO fp16 with
+// a power-of-two scale per level.  Thread (row t, half hf) keeps d_k columns 64 hf ..
+// 64 hf + 63 of dq_t; half 0 does the dlambda dot; the dual rows (d_k index = TMEM lane)
+// are split by d_v halves.  dq is added to the per-head fp32 buffer (the in-tile part
+// wrote it); dlambda levels >= 8 are assigned (the in-tile kernel zeroed them).
+// ---------------------------------------------------------------------------------
+struct TcBwdQParams {
+  int B, T, H, hpg, G, L, NT, nnodes;
+  int node_off[32];
+  int dual_off[32];   // first dual slot of the even nodes of tile level m
+  int nslots;         // dual slots per (b, h)
+  const float* a;
+  const float* lam;
+  const uint8_t* img;
+  const unsigned* meta;
+  float* dq32;
+  float* dlam;
+  float* dual;        // (B*H, nslots, d_k, d_v) fp32, zero on entry
+  unsigned* status;
+};
+
+constexpr int kBwdQFixed = 98304;  // Q, dO, two node images, diag(w) dO
+__host__ __device__ constexpr int bwdq_smem_bytes(int ninter) {
+  return kBwdQFixed + 512 * (ninter > 0 ? ninter : 1) + 1024;
+}
+
+__global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant__ CUtensorMap mapQ,
+                                                          const __grid_constant__ CUtensorMap mapD,
+                                                          TcBwdQParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* RQ = smem;             // 32 KB: Q (bf16, then fp16)
+  uint8_t* RD = smem + 32768;     // 16 KB: dO (bf16, then fp16)
+  uint8_t* RI = smem + 49152;     // 2 x 16 KB: node images
+  uint8_t* RB = smem + 81920;     // 16 KB: diag(w) dO of the current level (fp16)
+  float* sLamI = reinterpret_cast<float*>(smem + kBwdQFixed);  // [level index][row]
+  __shared__ __align__(8) uint64_t bar_ld, bar_y, bar_e[2], bar_yf;
+  __shared__ uint32_t tmem_base;
+  __shared__ float s_red[8];
+  __shared__ float s_mx[8][2];
+  __shared__ unsigned s_lmax[32];
+  __shared__ float sNode[32][2];  // per level index: scale exponent (bits), log2 decay
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & 127, hf = tid >> 7, quad = warp & 3, rot = r & 7;
+  const int lin = blockIdx.x;
+  const int h = lin % p.H;
+  const int u = (lin / p.H) % p.NT;
+  const int b = lin / (p.H * p.NT);
+  const int nlev = __popc((unsigned)u);
+  if (nlev == 0) return;  // the first tile reads no node
+  const int g = h / p.hpg;
+  const int bh = b * p.H + h;
+  const long long t0 = (long long)u * kTile;
+  const size_t nbase = (size_t)bh * p.nnodes;
+  const size_t row = (size_t)b * p.T + t0 + r;
+  const float* lrow = p.lam + (row * p.H + h) * p.L;
+  auto node_of = [&](int i) {
+    const int m = nth_set_bit((unsigned)u, i);
+    return nbase + p.node_off[m] + ((u >> m) - 1);
+  };
+
+  if (tid == 0) {
+    ptx::mbar_init(&bar_ld, 1);
+    ptx::mbar_init(&bar_y, 1);
+    ptx::mbar_init(&bar_e[0], 1);
+    ptx::mbar_init(&bar_e[1], 1);
+    ptx::mbar_init(&bar_yf, 256);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
+    ptx::tma_load_4d(RQ, &mapQ, &bar_ld, 0, g, (int)t0, b);
+    ptx::tma_load_4d(RQ + 16384, &mapQ, &bar_ld, 64, g, (int)t0, b);
+    ptx::tma_load_4d(RD, &mapD, &bar_ld, 0, h, (int)t0, b);
+    for (int i = 0; i < 2 && i < nlev; ++i) {
+      ptx::mbar_arrive_expect_tx(&bar_e[i], kImgBytes);
+      ptx::bulk_load(RI + i * kImgBytes, p.img + node_of(i) * kImgBytes, kImgBytes, &bar_e[i]);
+    }
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_base, 256);
+    ptx::tmem_relinquish();
+  }
+  if (tid < 32) s_lmax[tid] = 0u;
+  if (hf == 0)
+    for (int i = 0; i < nlev; ++i) ptx::cp_async4(sLamI + i * 128 + r, lrow + kLevIntra + nth_set_bit((unsigned)u, i));
+  if (tid < nlev) {
+    const unsigned* mt = p.meta + node_of(tid) * kMeta;
+    sNode[tid][0] = __uint_as_float(mt[1]);
+    sNode[tid][1] = __uint_as_float(mt[2]);
+  }
+  // chunk-local log2 decay cumsum over the 128 rows (both halves compute it)
+  float gt = log2f(p.a[row * p.H + h]);
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, gt, off);
+    if (lane >= off) gt += y;
+  }
+  if (lane == 31) s_red[warp] = gt;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  for (int w = 0; w < quad; ++w) gt += s_red[w];
+  const uint32_t tbase = tmem_base;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const uint32_t tZ = tbase, tY = tbase + 128, tU = tbase + 192;
+  bool ok = wait_bar(&bar_ld, 0);
+  if (!ok) atomicExch(p.status, kStatusTimeout);
+  ok = __syncthreads_and(ok);
+
+  // Q (half hf converts box hf of row r) and dO (half 0) -> fp16 with tile scales
+  uint8_t* qrow = RQ + hf * 16384 + r * 128;
+  uint8_t* drow = RD + r * 128;
+  {
+    uint32_t mq = 0u, md = 0u;
+    if (ok) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        mq = absmax_u4(mq, *reinterpret_cast<const uint4*>(qrow + ((c ^ rot) << 4)));
+        if (hf == 0) md = absmax_u4(md, *reinterpret_cast<const uint4*>(drow + ((c ^ rot) << 4)));
+      }
+    }
+    float fq = bf16x2_maxhalf(mq), fd = bf16x2_maxhalf(md);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      fq = fmaxf(fq, __shfl_xor_sync(0xffffffffu, fq, off));
+      fd = fmaxf(fd, __shfl_xor_sync(0xffffffffu, fd, off));
+    }
+    if (lane == 0) {
+      s_mx[warp][0] = fq;
+      s_mx[warp][1] = fd;
+    }
+  }
+  ptx::cp_async_wait_all();
+  __syncthreads();  // maxima; lambda rows
+  float maxq = 0.f, maxd = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    maxq = fmaxf(maxq, s_mx[w][0]);
+    maxd = fmaxf(maxd, s_mx[w][1]);
+  }
+  const int eq = f16_exp(maxq), ed = f16_exp(maxd);
+  if (ok) {
+    const float sq = pow2i(-eq), sd = pow2i(-ed);
+    const __nv_bfloat162 q2 = __floats2bfloat162_rn(sq, sq), d2 = __floats2bfloat162_rn(sd, sd);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4* x = reinterpret_cast<uint4*>(qrow + ((c ^ rot) << 4));
+      *x = bf16x8_to_f16x8(*x, q2);
+      if (hf == 0) {
+        uint4* y = reinterpret_cast<uint4*>(drow + ((c ^ rot) << 4));
+        *y = bf16x8_to_f16x8(*y, d2);
+      }
+    }
+    if (hf == 0)
+      for (int i = 0; i < nlev; ++i) atomicMax(&s_lmax[i], __float_as_uint(fabsf(sLamI[i * 128 + r])));
+  }
+  __syncthreads();  // fp16 Q, dO; lambda maxima
+  // level weights: w_t = lambda_t^(8+m) 2^(g_t + D) (D: the nearer levels' decay)
+  auto weight = [&](int i, float D) { return sLamI[i * 128 + r] * exp2f(gt + D); };
+  // diag(w) dO 2^-tau for level i: row r, d_v columns 32 hf .. 32 hf + 31 (chunks 4 hf ..)
+  auto write_b = [&](int i, float D, int tau) {
+    const float f = weight(i, D) * pow2s(ed - tau);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int cc = ((4 * hf + c) ^ rot) << 4;
+      const uint4 x = *reinterpret_cast<const uint4*>(drow + cc);
+      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+      uint32_t o4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+        o4[e] = pack_h2(f * v.x, f * v.y);
+      }
+      *reinterpret_cast<uint4*>(RB + r * 128 + cc) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    }
+  };
+  auto tau_of = [&](int i) { return f16_exp(__uint_as_float(s_lmax[i]) * maxd); };
+  float D = 0.f;
+  if (ok) write_b(0, 0.f, tau_of(0));
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  ok = __syncthreads_and(ok);
+
+  float acc[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+  int issued = nlev < 2 ? nlev : 2, consumed = 0, y_issued = 0;
+  const uint32_t id_z = ptx::idesc_f16_f32(128, 128, 0, 0);
+  const uint32_t id_y = ptx::idesc_f16_f32(128, 64, 0, 1);
+  const uint32_t id_u = ptx::idesc_f16_f32(128, 64, 1, 1);
+  for (int i = 0; ok && i < nlev; ++i) {
+    const int m = nth_set_bit((unsigned)u, i);
+    if (tid == 0) {
+      bool okd = i == 0 || wait_bar(&bar_yf, (i - 1) & 1);   // TMEM read, next diag(w) dO written
+      okd = okd && wait_bar(&bar_e[i & 1], (i >> 1) & 1);    // image landed
+      if (okd) {
+        ++consumed;
+        ptx::tc_fence_after();
+        const uint32_t im = ptx::smem_u32(RI + (i & 1) * kImgBytes);
+        const uint32_t q0 = ptx::smem_u32(RQ), d0 = ptx::smem_u32(RD), b0 = ptx::smem_u32(RB);
+#pragma unroll
+        for (int kk = 0; kk < kDv / 16; ++kk)  // Z = dO Nᵀ: K = d_v, B = image rows (d_k) K-major
+          ptx::umma_f16(tZ, ptx::smem_desc_sw128(d0 + kk * 32, 16, 1024), ptx::smem_desc_sw128(im + kk * 32, 16, 1024),
+                        id_z, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kDk / 16; ++kk) {
+          const uint32_t offq = (kk >> 2) * 16384 + (kk & 3) * 32;
+          ptx::umma_f16(tY, ptx::smem_desc_sw128(q0 + offq, 16, 1024), ptx::smem_desc_sw128(im + kk * 2048, 1024, 1024),
+                        id_y, kk > 0);  // Y = Q N
+        }
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)  // Qᵀ diag(w) dO: M = d_k, K = tokens
+          ptx::umma_f16(tU, ptx::smem_desc_sw128(q0 + kk * 2048, 16384, 1024),
+                        ptx::smem_desc_sw128(b0 + kk * 2048, 1024, 1024), id_u, kk > 0);
+        ptx::umma_commit(&bar_y);
+        ++y_issued;
+      } else {
+        atomicExch(p.status, kStatusTimeout);
+      }
+    }
+    bool okw = wait_bar(&bar_y, i & 1);
+    if (!okw) atomicExch(p.status, kStatusTimeout);
+    okw = __syncthreads_and(okw);
+    if (!okw) {
+      ok = false;
+      break;
+    }
+    if (tid == 0 && i + 2 < nlev) {  // the image buffer of level i is free again
+      ptx::mbar_arrive_expect_tx(&bar_e[i & 1], kImgBytes);
+      ptx::bulk_load(RI + (i & 1) * kImgBytes, p.img + node_of(i + 2) * kImgBytes, kImgBytes, &bar_e[i & 1]);
+      ++issued;
+    }
+    ptx::tc_fence_after();
+    const int en = __float_as_int(sNode[i][0]);
+    const float wt = weight(i, D);
+    {  // dq: columns 64 hf .. 64 hf + 63 of Z, weighted
+      const float wz = wt * pow2s(ed + en);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float y[32];
+        ptx::tmem_ld32(tZ + lane_off + hf * 64 + half * 32, y);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[half * 32 + j] += wz * y[j];
+      }
+    }
+    if (hf == 0) {  // dlambda_t^(8+m) = 2^(g_t + D + eq + en + ed) sum_j Y_tj dO^_tj
+      float dot = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float y[32];
+        ptx::tmem_ld32(tY + lane_off + half * 32, y);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 x = *reinterpret_cast<const uint4*>(drow + (((4 * half + c) ^ rot) << 4));
+          const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+            dot += y[c * 8 + 2 * e] * v.x + y[c * 8 + 2 * e + 1] * v.y;
+          }
+        }
+      }
+      p.dlam[(row * p.H + h) * p.L + kLevIntra + m] = exp2f(gt + D) * pow2s(eq + en + ed) * dot;
+    }
+    {  // dual rows (TMEM lane = d_k index r), d_v columns 32 hf .. 32 hf + 31
+      const int tau = tau_of(i);
+      const float su = pow2s(eq + tau);
+      float y[32];
+      ptx::tmem_ld32(tU + lane_off + hf * 32, y);
+      ptx::tmem_ld_wait();
+      const int nd = (u >> m) - 1;  // even
+      float* dst = p.dual + (((size_t)bh * p.nslots + p.dual_off[m] + (nd >> 1)) * kDk + r) * kDv + hf * 32;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        atomicAdd(reinterpret_cast<float4*>(dst + j), make_float4(su * y[j], su * y[j + 1], su * y[j + 2], su * y[j + 3]));
+    }
+    D += sNode[i][1];
+    if (i + 1 < nlev) {  // diag(w) dO of the next level (its MMA has read this one)
+      write_b(i + 1, D, tau_of(i + 1));
+      ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&bar_yf);
+  }
+  if (ok) {
+    float* dst = p.dq32 + (row * p.H + h) * kDk + hf * 64;
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) {
+      float4 o = *reinterpret_cast<float4*>(dst + j);
+      o.x += acc[j];
+      o.y += acc[j + 1];
+      o.z += acc[j + 2];
+      o.w += acc[j + 3];
+      *reinterpret_cast<float4*>(dst + j) = o;
+    }
+  }
+  if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
+    wait_bar(&bar_ld, 0);
+    for (int j = consumed; j < issued; ++j) wait_bar(&bar_e[j & 1], (j >> 1) & 1);
+    if (y_issued > 0) wait_bar(&bar_y, (y_issued - 1) & 1);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tbase, 256);
+}
+
+// ---------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1709,6 +2029,53 @@ cudaError_t launch_tc_ssd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
     note_launch();
   }
   if ((e = launch_output<1>(tp, mQ, mK, mV, p, 1, st)) != cudaSuccess) return e;
+  note_launch();
+  return cudaSuccess;
+}
+
+// The forward's tree only (tile states and the levels above), into a.ws per tp's layout.
+cudaError_t launch_tc_nodes(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
+  CUtensorMap mQ, mK, mV;
+  TcParams p;
+  if (!tc_setup(tp, a, &mQ, &mK, &mV, &p)) return cudaErrorInvalidValue;
+  cudaError_t e = launch_state(tp, a, mK, mV, p, st);
+  if (e == cudaSuccess) e = launch_tree(tp, a, p, st);
+  return e;
+}
+
+cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, const float* a, const float* lam,
+                            const char* tree_ws, float* dq32, float* dlam, float* dual, const int* dual_off,
+                            int nslots, unsigned* status, cudaStream_t st) {
+  CUtensorMap mQ, mD;
+  if (!make_map(&mQ, q, kDk, tp.G, tp.T, tp.B) || !make_map(&mD, dO, kDv, tp.H, tp.T, tp.B))
+    return cudaErrorInvalidValue;
+  TcBwdQParams p{};
+  p.B = tp.B;
+  p.T = tp.T;
+  p.H = tp.H;
+  p.hpg = tp.hpg;
+  p.G = tp.G;
+  p.L = tp.L;
+  p.NT = tp.NT;
+  p.nnodes = tp.nnodes;
+  for (int m = 0; m < 32; ++m) {
+    p.node_off[m] = m < tp.MT ? tp.node_off[m] : 0;
+    p.dual_off[m] = m < tp.MT ? dual_off[m] : 0;
+  }
+  p.nslots = nslots;
+  p.a = a;
+  p.lam = lam;
+  p.img = reinterpret_cast<const uint8_t*>(tree_ws + tp.off_img);
+  p.meta = reinterpret_cast<const unsigned*>(tree_ws + tp.off_meta);
+  p.dq32 = dq32;
+  p.dlam = dlam;
+  p.dual = dual;
+  p.status = status;
+  const int smem = bwdq_smem_bytes(bit_length(tp.NT - 1));
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  tc_bwd_q_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 256, smem, st>>>(mQ, mD, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
 }
