@@ -48,7 +48,10 @@ struct BwdPlan {
   size_t off_dq;   // (B, T, H, dk) fp32 per-head dq
   size_t off_dk;   // (B, T, H, dk) fp32 per-head dk
   size_t off_dv;   // (B, T, H, dv) fp32
-  size_t off_tc;
+  size_t off_tc;   // tc: the tree over tiles (TcPlan layout)
+  size_t off_dimg; // tc: the duals as fp16 images, 16 KB per slot
+  size_t off_dmeta;// tc: their scalars, 4 u32 per slot
+  size_t off_P;    // tc: running sums of the tile decays, (B*H, NT + 1) fp64
   size_t bytes;
 };
 
@@ -413,7 +416,10 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
   c.chunk = s.chunk < 64 ? s.chunk : 64;  // the result does not depend on the chunk
   if (!make_gen_plan(c, &bp->g)) return false;
   const size_t BH = (size_t)s.batch * s.heads, S = (size_t)s.d_k * s.d_v;
-  size_t o = al(bp->g.bytes);
+  bp->tc = s.dtype == LL_BF16 && bp->g.C == 64 && make_tc_plan(s, &bp->tp);
+  // the generic chunk states and blocks only off the tensor-core path (which uses the
+  // plan for the dual slots alone)
+  size_t o = bp->tc ? 0 : al(bp->g.bytes);
   bp->off_dual = o;
   o = al(o + sizeof(float) * BH * bp->g.nblk * S);
   bp->off_dq = o;
@@ -422,9 +428,16 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
   o = al(o + sizeof(float) * (size_t)s.batch * s.T * s.heads * s.d_k);
   bp->off_dv = o;
   o = al(o + sizeof(float) * (size_t)s.batch * s.T * s.heads * s.d_v);
-  bp->tc = s.dtype == LL_BF16 && bp->g.C == 64 && make_tc_plan(s, &bp->tp);
-  bp->off_tc = o;
-  if (bp->tc) o = al(o + bp->tp.bytes);
+  bp->off_tc = bp->off_dimg = bp->off_dmeta = bp->off_P = o;
+  if (bp->tc) {
+    o = al(o + bp->tp.bytes);
+    bp->off_dimg = o;
+    o = al(o + BH * bp->g.nblk * S * 2);
+    bp->off_dmeta = o;
+    o = al(o + BH * bp->g.nblk * 4 * sizeof(unsigned));
+    bp->off_P = o;
+    o = al(o + BH * (bp->tp.NT + 1) * sizeof(double));
+  }
   bp->bytes = o;
   return true;
 }
@@ -434,9 +447,10 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
   const GenPlan& p = bp.g;
   const int BH = p.B * p.H;
   const int C = p.C, dk = p.dk, dv = p.dv;
-  // the forward's chunk states and Fenwick blocks (same kernels as the generic forward)
-  cudaError_t e = launch_generic_states(p, sizeof(TIn) == 2, fa, st);
-  if (e != cudaSuccess) return e;
+  // the forward's chunk states and Fenwick blocks (same kernels as the generic forward),
+  // off the tensor-core path
+  cudaError_t e = cudaSuccess;
+  if (!bp.tc && (e = launch_generic_states(p, sizeof(TIn) == 2, fa, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(x.ws + bp.off_dual, 0, sizeof(float) * (size_t)BH * p.nblk * dk * dv, st)) !=
       cudaSuccess)
     return e;
@@ -479,13 +493,25 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launch();
   }
-  const size_t sm3 = sizeof(float) * ((size_t)C * dk + (size_t)(C + 4) * dv + dk * dv + C);
-  if ((e = cudaFuncSetAttribute(bwd_inter_kv<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) !=
-      cudaSuccess)
-    return e;
-  bwd_inter_kv<TIn><<<dim3(p.N, BH), kT, sm3, st>>>(p, x, bp.off_dk, bp.off_dv, bp.off_dual, m_start);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
+  if (tc) {
+    int dual_off[32];
+    for (int m = 0; m < 32; ++m) dual_off[m] = m + 1 < p.M ? p.blk_off[m + 1] : 0;
+    if ((e = launch_tc_bwd_kv(bp.tp, x.k, x.v, x.a, x.ws + bp.off_tc, reinterpret_cast<const float*>(x.ws + bp.off_dual),
+                              reinterpret_cast<uint8_t*>(x.ws + bp.off_dimg),
+                              reinterpret_cast<unsigned*>(x.ws + bp.off_dmeta),
+                              reinterpret_cast<double*>(x.ws + bp.off_P), dual_off, p.nblk,
+                              reinterpret_cast<float*>(x.ws + bp.off_dk), reinterpret_cast<float*>(x.ws + bp.off_dv),
+                              fa.status, st)) != cudaSuccess)
+      return e;
+  } else {
+    const size_t sm3 = sizeof(float) * ((size_t)C * dk + (size_t)(C + 4) * dv + dk * dv + C);
+    if ((e = cudaFuncSetAttribute(bwd_inter_kv<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) !=
+        cudaSuccess)
+      return e;
+    bwd_inter_kv<TIn><<<dim3(p.N, BH), kT, sm3, st>>>(p, x, bp.off_dk, bp.off_dv, bp.off_dual, m_start);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launch();
+  }
   const size_t n = (size_t)p.B * p.T * (p.G * dk + p.H * dv);
   const unsigned gf = (unsigned)((n + kT - 1) / kT < 4096 ? (n + kT - 1) / kT : 4096);
   bwd_final<TIn><<<gf, kT, 0, st>>>(p, x, bp.off_dq, bp.off_dk, bp.off_dv);

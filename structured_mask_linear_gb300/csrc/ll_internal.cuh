@@ -106,6 +106,12 @@ cudaError_t launch_tc_nodes(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_tc_bwd_q(const TcPlan& p, const void* q, const void* dO, const float* a, const float* lam,
                             const char* tree_ws, float* dq32, float* dlam, float* dual, const int* dual_off,
                             int nslots, unsigned* status, cudaStream_t st);
+// Backward, key side of the inter-tile levels on the tensor cores: the tile-decay running
+// sums (fp64, (B*H, NT+1) in P), the duals as fp16 images (dimg: 16 KB per slot, dmeta: 4
+// u32 per slot), then adds into dk32 and dv32.
+cudaError_t launch_tc_bwd_kv(const TcPlan& p, const void* k, const void* v, const float* a, const char* tree_ws,
+                             const float* dual, uint8_t* dimg, unsigned* dmeta, double* P, const int* dual_off,
+                             int nslots, float* dk32, float* dv32, unsigned* status, cudaStream_t st);
 // Backward: the in-tile pairs (levels 0..7) on the tensor cores, for tc_supported shapes;
 // assigns the fp32 per-head dq, dk, dv buffers and dlambda (levels >= 8 zeroed).
 cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k, const void* v, const void* dO,

@@ -1804,6 +1804,297 @@ __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant_
 }
 
 // ---------------------------------------------------------------------------------
+// Key side of the inter-tile levels of the backward.
+//
+// tc_tile_prefix: per (b, h) the running sum P[c] of the tile decays gamma_0 .. gamma_{c-1}
+//   (the log2 decays of the level-0 nodes), in fp64, c = 0 .. NT.
+// tc_dual_publish: every dual slot as an fp16 image with a power-of-two scale (the node
+//   publication of the tree), for use as an MMA operand.
+// tc_bwd_kv: per key tile u and every tile level m whose node (m, i = u >> m) is read
+//   (i even, node (m, i + 1) inside the sequence), with c_m = 2^(P[(i+1) 2^m] - P[u+1])
+//   the decay of the tiles after u inside the node and r_s = 2^(gamma_u - g_s):
+//     dk_s += r_s sum_m c_m Dual_m v_s,   dv_s += r_s sum_m c_m Dual_mᵀ k_s,
+//   as Zk = V Dualᵀ and Zv = K Dual on the tensor cores (V, K fp16 with tile scales),
+//   added into registers per level (512 threads: four per key row, 32 d_k and 16 d_v
+//   columns each), then added to the per-head fp32 buffers.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tc_tile_prefix_kernel(const unsigned* meta, int nnodes, int NT,
+                                                             double* P) {
+  __shared__ double s_part[8];
+  __shared__ double s_carry;
+  const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_carry = 0.0;
+  double* out = P + (size_t)bh * (NT + 1);
+  if (tid == 0) out[0] = 0.0;
+  __syncthreads();
+  for (int c0 = 0; c0 < NT; c0 += 256) {
+    const int c = c0 + tid;
+    double x = c < NT ? (double)__uint_as_float(meta[((size_t)bh * nnodes + c) * kMeta + 2]) : 0.0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_part[warp] = x;
+    __syncthreads();
+    double add = s_carry;
+    for (int w = 0; w < warp; ++w) add += s_part[w];
+    x += add;
+    if (c < NT) out[c + 1] = x;
+    __syncthreads();
+    if (tid == 255) s_carry = x;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(128) tc_dual_publish_kernel(const float* dual, uint8_t* img, unsigned* meta) {
+  __shared__ __align__(1024) uint8_t stage[kImgBytes];
+  __shared__ float2 s_red2[4];
+  const size_t slot = blockIdx.x;
+  const float* src = dual + (slot * kDk + threadIdx.x) * kDv;
+  float cur[kDv];
+#pragma unroll
+  for (int j = 0; j < kDv; j += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(src + j);
+    cur[j] = v.x;
+    cur[j + 1] = v.y;
+    cur[j + 2] = v.z;
+    cur[j + 3] = v.w;
+  }
+  publish_node(cur, stage, slot, 0.f, s_red2, img, meta);
+}
+
+struct TcBwdKVParams {
+  int B, T, H, hpg, G, NT, MT;
+  int dual_off[32];
+  int nslots;
+  const float* a;
+  const uint8_t* dimg;    // dual images (B*H, nslots, 16 KB)
+  const unsigned* dmeta;  // (B*H, nslots, 4): scale exponent in [1]
+  const double* P;        // (B*H, NT + 1)
+  float* dk32;
+  float* dv32;
+  unsigned* status;
+};
+
+constexpr int kSmemBwdKV = 32768 + 16384 + 2 * kImgBytes + 1024;
+
+__global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap mapK,
+                                                           const __grid_constant__ CUtensorMap mapV,
+                                                           TcBwdKVParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* RK = smem;           // 32 KB: K (bf16, then fp16)
+  uint8_t* RV = smem + 32768;   // 16 KB: V (bf16, then fp16)
+  uint8_t* RI = smem + 49152;   // 2 x 16 KB: dual images
+  __shared__ __align__(8) uint64_t bar_ld, bar_z, bar_e[2], bar_zf;
+  __shared__ uint32_t tmem_base;
+  __shared__ float s_red[16];
+  __shared__ float s_mx[16][2];
+  __shared__ int s_lv[32];
+  __shared__ int s_nl;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & 127, qq = tid >> 7, quad = warp & 3, rot = r & 7;
+  const int lin = blockIdx.x;
+  const int h = lin % p.H;
+  const int u = (lin / p.H) % p.NT;
+  const int b = lin / (p.H * p.NT);
+  const int g = h / p.hpg;
+  const int bh = b * p.H + h;
+  const long long t0 = (long long)u * kTile;
+  const size_t row = (size_t)b * p.T + t0 + r;
+  if (tid == 0) {  // tile levels whose node holding u is read by a later node
+    int n = 0;
+    for (int m = 0; m < p.MT; ++m) {
+      const int i = u >> m;
+      if (!(i & 1) && ((long long)(i + 1) << m) < p.NT) s_lv[n++] = m;
+    }
+    s_nl = n;
+  }
+  __syncthreads();
+  const int nl = s_nl;
+  if (nl == 0) return;  // no level reads this tile's nodes
+  auto slot_of = [&](int j) {
+    const int m = s_lv[j];
+    return (size_t)bh * p.nslots + p.dual_off[m] + ((u >> m) >> 1);
+  };
+  if (tid == 0) {
+    ptx::mbar_init(&bar_ld, 1);
+    ptx::mbar_init(&bar_z, 1);
+    ptx::mbar_init(&bar_e[0], 1);
+    ptx::mbar_init(&bar_e[1], 1);
+    ptx::mbar_init(&bar_zf, 512);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
+    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
+    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
+    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
+    for (int j = 0; j < 2 && j < nl; ++j) {
+      ptx::mbar_arrive_expect_tx(&bar_e[j], kImgBytes);
+      ptx::bulk_load(RI + j * kImgBytes, p.dimg + slot_of(j) * kImgBytes, kImgBytes, &bar_e[j]);
+    }
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_base, 256);
+    ptx::tmem_relinquish();
+  }
+  // tile-local log2 decay cumsum (every quarter computes it for its rows)
+  float gt = log2f(p.a[row * p.H + h]);
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, gt, off);
+    if (lane >= off) gt += y;
+  }
+  if (lane == 31) s_red[warp] = gt;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  for (int w = 0; w < quad; ++w) gt += s_red[w];
+  const float gam = s_red[0] + s_red[1] + s_red[2] + s_red[3];  // gamma_u
+  const uint32_t tbase = tmem_base;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const uint32_t tZk = tbase, tZv = tbase + 128;
+  bool ok = wait_bar(&bar_ld, 0);
+  if (!ok) atomicExch(p.status, kStatusTimeout);
+  ok = __syncthreads_and(ok);
+  // K (quarters 0, 1: boxes 0, 1 of row r) and V (quarter 2) -> fp16 with tile scales
+  uint8_t* crow = qq < 2 ? RK + qq * 16384 + r * 128 : RV + r * 128;
+  {
+    uint32_t mx = 0u;
+    if (ok && qq < 3) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mx = absmax_u4(mx, *reinterpret_cast<const uint4*>(crow + ((c ^ rot) << 4)));
+    }
+    float f = bf16x2_maxhalf(mx);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, off));
+    if (lane == 0) s_mx[warp][0] = f;
+  }
+  __syncthreads();
+  float mk = 0.f, mv = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) mk = fmaxf(mk, s_mx[w][0]);
+#pragma unroll
+  for (int w = 8; w < 12; ++w) mv = fmaxf(mv, s_mx[w][0]);
+  const int ek = f16_exp(mk), ev = f16_exp(mv);
+  if (ok && qq < 3) {
+    const float sc = pow2i(qq < 2 ? -ek : -ev);
+    const __nv_bfloat162 s2 = __floats2bfloat162_rn(sc, sc);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4* x = reinterpret_cast<uint4*>(crow + ((c ^ rot) << 4));
+      *x = bf16x8_to_f16x8(*x, s2);
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  ok = __syncthreads_and(ok);
+
+  float ak[32], av[16];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) ak[j] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) av[j] = 0.f;
+  const double* P = p.P + (size_t)bh * (p.NT + 1);
+  const uint32_t id_k = ptx::idesc_f16_f32(128, 128, 0, 0);
+  const uint32_t id_v = ptx::idesc_f16_f32(128, 64, 0, 1);
+  int issued = nl < 2 ? nl : 2, consumed = 0, z_issued = 0;
+  for (int j = 0; ok && j < nl; ++j) {
+    if (tid == 0) {
+      bool okd = j == 0 || wait_bar(&bar_zf, (j - 1) & 1);  // Z of the level before read
+      okd = okd && wait_bar(&bar_e[j & 1], (j >> 1) & 1);
+      if (okd) {
+        ++consumed;
+        ptx::tc_fence_after();
+        const uint32_t im = ptx::smem_u32(RI + (j & 1) * kImgBytes);
+        const uint32_t k0 = ptx::smem_u32(RK), v0 = ptx::smem_u32(RV);
+#pragma unroll
+        for (int kk = 0; kk < kDv / 16; ++kk)  // Zk = V Dualᵀ: K = d_v; the image rows (d_k) K-major
+          ptx::umma_f16(tZk, ptx::smem_desc_sw128(v0 + kk * 32, 16, 1024), ptx::smem_desc_sw128(im + kk * 32, 16, 1024),
+                        id_k, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kDk / 16; ++kk) {  // Zv = K Dual: K = d_k; the image MN-major
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          ptx::umma_f16(tZv, ptx::smem_desc_sw128(k0 + off, 16, 1024), ptx::smem_desc_sw128(im + kk * 2048, 1024, 1024),
+                        id_v, kk > 0);
+        }
+        ptx::umma_commit(&bar_z);
+        ++z_issued;
+      } else {
+        atomicExch(p.status, kStatusTimeout);
+      }
+    }
+    bool okw = wait_bar(&bar_z, j & 1);
+    if (!okw) atomicExch(p.status, kStatusTimeout);
+    okw = __syncthreads_and(okw);
+    if (!okw) {
+      ok = false;
+      break;
+    }
+    if (tid == 0 && j + 2 < nl) {
+      ptx::mbar_arrive_expect_tx(&bar_e[j & 1], kImgBytes);
+      ptx::bulk_load(RI + (j & 1) * kImgBytes, p.dimg + slot_of(j + 2) * kImgBytes, kImgBytes, &bar_e[j & 1]);
+      ++issued;
+    }
+    ptx::tc_fence_after();
+    const int m = s_lv[j];
+    const int end = ((u >> m) + 1) << m;
+    const float cm = exp2f((float)(P[end] - P[u + 1]));
+    const int ed = (int)p.dmeta[slot_of(j) * kMeta + 1];
+    {
+      float y[32];
+      ptx::tmem_ld32(tZk + lane_off + qq * 32, y);
+      ptx::tmem_ld_wait();
+      const float w = cm * pow2s(ed + ev);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) ak[c] += w * y[c];
+    }
+    {
+      float y[16];
+      ptx::tmem_ld16(tZv + lane_off + qq * 16, y);
+      ptx::tmem_ld_wait();
+      const float w = cm * pow2s(ed + ek);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) av[c] += w * y[c];
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&bar_zf);
+  }
+  if (ok) {
+    const float rs = exp2f(gam - gt);
+    float* dk = p.dk32 + (row * p.H + h) * kDk + qq * 32;
+    float* dv = p.dv32 + (row * p.H + h) * kDv + qq * 16;
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+      float4 o = *reinterpret_cast<float4*>(dk + c);
+      o.x += rs * ak[c];
+      o.y += rs * ak[c + 1];
+      o.z += rs * ak[c + 2];
+      o.w += rs * ak[c + 3];
+      *reinterpret_cast<float4*>(dk + c) = o;
+    }
+#pragma unroll
+    for (int c = 0; c < 16; c += 4) {
+      float4 o = *reinterpret_cast<float4*>(dv + c);
+      o.x += rs * av[c];
+      o.y += rs * av[c + 1];
+      o.z += rs * av[c + 2];
+      o.w += rs * av[c + 3];
+      *reinterpret_cast<float4*>(dv + c) = o;
+    }
+  }
+  if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
+    wait_bar(&bar_ld, 0);
+    for (int j = consumed; j < issued; ++j) wait_bar(&bar_e[j & 1], (j >> 1) & 1);
+    if (z_issued > 0) wait_bar(&bar_z, (z_issued - 1) & 1);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tbase, 256);
+}
+
+// ---------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -2075,6 +2366,47 @@ cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, con
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   tc_bwd_q_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 256, smem, st>>>(mQ, mD, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
+  return cudaSuccess;
+}
+
+cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, const float* a, const char* tree_ws,
+                             const float* dual, uint8_t* dimg, unsigned* dmeta, double* P, const int* dual_off,
+                             int nslots, float* dk32, float* dv32, unsigned* status, cudaStream_t st) {
+  const unsigned BH = (unsigned)(tp.B * tp.H);
+  tc_tile_prefix_kernel<<<BH, 256, 0, st>>>(reinterpret_cast<const unsigned*>(tree_ws + tp.off_meta), tp.nnodes,
+                                            tp.NT, P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  note_launch();
+  tc_dual_publish_kernel<<<(unsigned)((size_t)BH * nslots), 128, 0, st>>>(dual, dimg, dmeta);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
+  CUtensorMap mK, mV;
+  if (!make_map(&mK, k, kDk, tp.G, tp.T, tp.B) || !make_map(&mV, v, kDv, tp.H, tp.T, tp.B))
+    return cudaErrorInvalidValue;
+  TcBwdKVParams p{};
+  p.B = tp.B;
+  p.T = tp.T;
+  p.H = tp.H;
+  p.hpg = tp.hpg;
+  p.G = tp.G;
+  p.NT = tp.NT;
+  p.MT = tp.MT;
+  for (int m = 0; m < 32; ++m) p.dual_off[m] = m < tp.MT ? dual_off[m] : 0;
+  p.nslots = nslots;
+  p.a = a;
+  p.dimg = dimg;
+  p.dmeta = dmeta;
+  p.P = P;
+  p.dk32 = dk32;
+  p.dv32 = dv32;
+  p.status = status;
+  if ((e = cudaFuncSetAttribute(tc_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwdKV)) !=
+      cudaSuccess)
+    return e;
+  tc_bwd_kv_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 512, kSmemBwdKV, st>>>(mK, mV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
