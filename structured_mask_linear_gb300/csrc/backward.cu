@@ -26,7 +26,8 @@
 //   bwd_inter_kv  per key chunk, per level whose block holds it and has readers: dk and
 //                 dv from the dual, decayed from each key to the end of the block;
 //   bwd_final     group sums of dq and dk, casts;
-//   bwd_dloga     d(log a) as a reverse running sum per (b, h), kept in fp64.
+//   bwd_dloga_*   d(log a) as a reverse running sum per (b, h), kept in fp64 (per 128-token
+//                 chunk, across chunks, then both added).
 // The gradient is returned with respect to log a, the form a enters the forward in: for
 // a close to 0 the one with respect to a, d(log a)/a, would turn the fp32 rounding of
 // the running sum into arbitrarily large errors.
@@ -52,6 +53,9 @@ struct BwdPlan {
   size_t off_dimg; // tc: the duals as fp16 images, 16 KB per slot
   size_t off_dmeta;// tc: their scalars, 4 u32 per slot
   size_t off_P;    // tc: running sums of the tile decays, (B*H, NT + 1) fp64
+  size_t off_loc;  // d(log a): per-token reverse running sums inside 128-token chunks, fp64
+  size_t off_tot;  // chunk totals, then (off_carry) their reverse running sums, fp64
+  size_t off_carry;
   size_t bytes;
 };
 
@@ -340,6 +344,14 @@ __global__ void __launch_bounds__(kT) bwd_inter_kv(GenPlan p, BwdArgs x, size_t 
 }
 
 // ---- group sums and casts -----------------------------------------------------------------
+__device__ __forceinline__ void store4(float* p, size_t i, float4 v) { *reinterpret_cast<float4*>(p + i) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, size_t i, float4 v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  *reinterpret_cast<uint2*>(p + i) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+// Four consecutive elements per thread (d_k and d_v are multiples of 4).
 template <typename TIn>
 __global__ void __launch_bounds__(kT) bwd_final(GenPlan p, BwdArgs x, size_t off_dq, size_t off_dk,
                                                size_t off_dv) {
@@ -348,47 +360,93 @@ __global__ void __launch_bounds__(kT) bwd_final(GenPlan p, BwdArgs x, size_t off
   const float* dv32 = reinterpret_cast<const float*>(x.ws + off_dv);
   const size_t nqk = (size_t)p.B * p.T * p.G * p.dk;
   const size_t nv = (size_t)p.B * p.T * p.H * p.dv;
-  for (size_t e = blockIdx.x * (size_t)kT + threadIdx.x; e < nqk + nv; e += (size_t)gridDim.x * kT) {
+  for (size_t e4 = blockIdx.x * (size_t)kT + threadIdx.x; 4 * e4 < nqk + nv; e4 += (size_t)gridDim.x * kT) {
+    const size_t e = 4 * e4;
     if (e < nqk) {
       const size_t i = e % p.dk, bt_g = e / p.dk, grp = bt_g % p.G, bt = bt_g / p.G;
-      float sq = 0.f, sk = 0.f;
+      float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
       for (int hh = 0; hh < p.hpg; ++hh) {
         const size_t o = (bt * p.H + grp * p.hpg + hh) * p.dk + i;
-        sq += dq32[o];
-        sk += dk32[o];
+        const float4 a = *reinterpret_cast<const float4*>(dq32 + o), c = *reinterpret_cast<const float4*>(dk32 + o);
+        sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
+        sk.x += c.x; sk.y += c.y; sk.z += c.z; sk.w += c.w;
       }
-      ll_store(static_cast<TIn*>(x.dq), e, sq);
-      ll_store(static_cast<TIn*>(x.dk), e, sk);
+      store4(static_cast<TIn*>(x.dq), e, sq);
+      store4(static_cast<TIn*>(x.dk), e, sk);
     } else {
-      ll_store(static_cast<TIn*>(x.dv), e - nqk, dv32[e - nqk]);
+      store4(static_cast<TIn*>(x.dv), e - nqk, *reinterpret_cast<const float4*>(dv32 + (e - nqk)));
     }
   }
 }
 
 // ---- d(log a) as a reverse running sum of R_u - C_u ----------------------------------------
+// Three passes over chunks of 128 tokens, every sum in fp64: per chunk the values and their
+// reverse running sums (thread i holds token 128 c + 127 - i) and the chunk's total; per
+// (b, h) the reverse running sums of the chunk totals after each chunk; then both added.
+constexpr int kDlChunk = 128;
+
+__device__ __forceinline__ void load4v(const float* p, float (&x)[4]) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  x[0] = v.x;
+  x[1] = v.y;
+  x[2] = v.z;
+  x[3] = v.w;
+}
+__device__ __forceinline__ void load4v(const __nv_bfloat16* p, float (&x)[4]) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  x[0] = __uint_as_float(v.x << 16);
+  x[1] = __uint_as_float(v.x & 0xffff0000u);
+  x[2] = __uint_as_float(v.y << 16);
+  x[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+
 template <typename TIn>
-__global__ void __launch_bounds__(kT) bwd_dloga(GenPlan p, BwdArgs x, size_t off_dv) {
-  __shared__ double s_part[kT / 32];
-  __shared__ double s_carry;
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
-  const int L = p.L, dv = p.dv;
+__global__ void __launch_bounds__(kDlChunk) bwd_dloga_local(GenPlan p, BwdArgs x, size_t off_dv, double* loc,
+                                                           double* tot) {
+  __shared__ double s_part[kDlChunk / 32];
+  const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H, nch = gridDim.x;
+  const int L = p.L, dv = p.dv, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float* dv32 = reinterpret_cast<const float*>(x.ws + off_dv);
   const TIn* v = static_cast<const TIn*>(x.v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long t = (long long)c * kDlChunk + (kDlChunk - 1 - threadIdx.x);
+  double val = 0.0;
+  if (t < p.T) {
+    const size_t row = ((size_t)b * p.T + t) * p.H + h;
+    float R = 0.f, Cv = 0.f;
+    for (int l = 0; l < L; ++l) R += x.lam[row * L + l] * x.dlam[row * L + l];
+    const float* dr = dv32 + row * dv;
+    const TIn* vr = v + row * dv;
+    for (int jv = 0; jv < dv; jv += 4) {  // rows 16-byte aligned (d_v a multiple of 16)
+      const float4 d4 = *reinterpret_cast<const float4*>(dr + jv);
+      float v4[4];
+      load4v(vr + jv, v4);
+      Cv += v4[0] * d4.x + v4[1] * d4.y + v4[2] * d4.z + v4[3] * d4.w;
+    }
+    val = (double)R - (double)Cv;
+  }
+  double inc = val;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += y;
+  }
+  if (lane == 31) s_part[warp] = inc;
+  __syncthreads();
+  for (int w = 0; w < warp; ++w) inc += s_part[w];
+  if (t < p.T) loc[(size_t)bh * p.T + t] = inc;
+  if (threadIdx.x == kDlChunk - 1) tot[(size_t)bh * nch + c] = inc;
+}
+
+// carry[c] = sum of the totals of the chunks after c, per (b, h)
+__global__ void __launch_bounds__(kT) bwd_dloga_carry(int nch, const double* tot, double* carry) {
+  __shared__ double s_part[kT / 32];
+  __shared__ double s_carry;
+  const int bh = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) s_carry = 0.0;
   __syncthreads();
-  // segments of kT tokens from the end; inside a segment thread i holds token end - i
-  for (long long end = (long long)p.T - 1; end >= 0; end -= kT) {
-    const long long t = end - threadIdx.x;
-    double val = 0.0;
-    if (t >= 0) {
-      const size_t row = ((size_t)b * p.T + t) * p.H + h;
-      float R = 0.f, Cv = 0.f;
-      for (int l = 0; l < L; ++l) R += x.lam[row * L + l] * x.dlam[row * L + l];
-      for (int jv = 0; jv < dv; ++jv) Cv += ll_load(v, row * dv + jv) * dv32[row * dv + jv];
-      val = (double)R - (double)Cv;
-    }
-    // inclusive scan over the segment in thread order (= decreasing token index)
+  for (int end = nch - 1; end >= 0; end -= kT) {  // thread i holds chunk end - i
+    const int c = end - (int)threadIdx.x;
+    const double val = c >= 0 ? tot[(size_t)bh * nch + c] : 0.0;
     double inc = val;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -400,15 +458,21 @@ __global__ void __launch_bounds__(kT) bwd_dloga(GenPlan p, BwdArgs x, size_t off
     double add = s_carry;
     for (int w = 0; w < warp; ++w) add += s_part[w];
     inc += add;
-    if (t >= 0) {
-      const size_t row = ((size_t)b * p.T + t) * p.H + h;
-      // position 0 of the sequence: no key precedes it, so its log-decay has no effect
-      x.dloga[row] = t == 0 ? 0.f : (float)inc;
-    }
+    if (c >= 0) carry[(size_t)bh * nch + c] = inc - val;  // exclusive: the chunks after c
     __syncthreads();
     if (threadIdx.x == kT - 1) s_carry = inc;
     __syncthreads();
   }
+}
+
+__global__ void __launch_bounds__(kDlChunk) bwd_dloga_apply(GenPlan p, BwdArgs x, const double* loc,
+                                                           const double* carry) {
+  const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H, nch = gridDim.x;
+  const long long t = (long long)c * kDlChunk + threadIdx.x;
+  if (t >= p.T) return;
+  // position 0 of the sequence: no key precedes it, so its log-decay has no effect
+  x.dloga[((size_t)b * p.T + t) * p.H + h] =
+      t == 0 ? 0.f : (float)(loc[(size_t)bh * p.T + t] + carry[(size_t)bh * nch + c]);
 }
 
 bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
@@ -438,6 +502,13 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
     bp->off_P = o;
     o = al(o + BH * (bp->tp.NT + 1) * sizeof(double));
   }
+  const size_t nch = ((size_t)s.T + kDlChunk - 1) / kDlChunk;
+  bp->off_loc = o;
+  o = al(o + BH * (size_t)s.T * sizeof(double));
+  bp->off_tot = o;
+  o = al(o + BH * nch * sizeof(double));
+  bp->off_carry = o;
+  o = al(o + BH * nch * sizeof(double));
   bp->bytes = o;
   return true;
 }
@@ -512,12 +583,22 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launch();
   }
-  const size_t n = (size_t)p.B * p.T * (p.G * dk + p.H * dv);
-  const unsigned gf = (unsigned)((n + kT - 1) / kT < 4096 ? (n + kT - 1) / kT : 4096);
+  const size_t n4 = (size_t)p.B * p.T * (p.G * dk + p.H * dv) / 4;
+  const unsigned gf = (unsigned)((n4 + kT - 1) / kT < 8192 ? (n4 + kT - 1) / kT : 8192);
   bwd_final<TIn><<<gf, kT, 0, st>>>(p, x, bp.off_dq, bp.off_dk, bp.off_dv);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
-  bwd_dloga<TIn><<<BH, kT, 0, st>>>(p, x, bp.off_dv);
+  const int nch = (p.T + kDlChunk - 1) / kDlChunk;
+  double* loc = reinterpret_cast<double*>(x.ws + bp.off_loc);
+  double* tot = reinterpret_cast<double*>(x.ws + bp.off_tot);
+  double* carry = reinterpret_cast<double*>(x.ws + bp.off_carry);
+  bwd_dloga_local<TIn><<<dim3(nch, BH), kDlChunk, 0, st>>>(p, x, bp.off_dv, loc, tot);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
+  bwd_dloga_carry<<<BH, kT, 0, st>>>(nch, tot, carry);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
+  bwd_dloga_apply<<<dim3(nch, BH), kDlChunk, 0, st>>>(p, x, loc, carry);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
