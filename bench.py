@@ -506,7 +506,7 @@ def backward_measure(sml, torch, x, w, hbm_peak, steps=3):
     nbytes = 2 * (el(x.q) + el(x.k) + el(x.v) + el(x.a) + el(x.lam)) + el(dO)
     res = {"workload": workload_desc(w), "ms_per_step": ms, "unit": "tokens/s",
            "value": w.batch * w.T / (ms / 1e3), "steps": steps,
-           "path": "CUDA cores, fp32 (csrc/backward.cu)",
+           "path": "tensor cores: tc_bwd_intra, tc_bwd_q, tc_bwd_kv (csrc/tc_fwd.cu), sums in csrc/backward.cu",
            "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": hbm_peak,
                         "unit": "GB/s", "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
                         "algorithmic_bytes_per_step": nbytes}}

@@ -231,8 +231,11 @@ size_t loglinear_bwd_workspace_bytes(const ll_shape* shape);
  *   dlambda  (B, T, H, L)    fp32; levels with no bucket get 0
  *   workspace >= loglinear_bwd_workspace_bytes(shape) bytes, 16-byte aligned, contents on
  *            entry do not matter
- * All arithmetic is fp32 on the CUDA cores.  The dk/dv terms of the levels above a
- * chunk are summed with fp32 atomics, so results can differ between calls by rounding.
+ * For bf16 with d_k = 128, d_v = 64, T % 128 == 0 and chunk >= 64 the products run on the
+ * tensor cores (fp16 operands with power-of-two scales, fp32 accumulation); other shapes
+ * run fp32 on the CUDA cores.  The terms of the levels above a tile (or chunk) are summed
+ * through each node's dual with fp32 atomics, so results can differ between calls by
+ * rounding.
  */
 ll_status loglinear_bwd(const ll_shape* shape, const void* q, const void* k, const void* v,
                         const float* a, const float* lambda, const void* dO, void* dq, void* dk,
