@@ -27,7 +27,10 @@
 //                 dv from the dual, decayed from each key to the end of the block;
 //   bwd_final     group sums of dq and dk, casts;
 //   bwd_dloga_*   d(log a) as a reverse running sum per (b, h), kept in fp64 (per 128-token
-//                 chunk, across chunks, then both added).
+//                 chunk, across chunks, then both added).  R_u and C_u nearly cancel (their
+//                 totals are equal), so on the tensor-core path C_u is the fp32 sum of the
+//                 pair terms from the exact products S and E (in-tile) plus v_u . (the
+//                 inter-tile part of dv_u), not v_u . dv_u with dv from fp16 operands.
 // The gradient is returned with respect to log a, the form a enters the forward in: for
 // a close to 0 the one with respect to a, d(log a)/a, would turn the fp32 rounding of
 // the running sum into arbitrarily large errors.
@@ -53,6 +56,7 @@ struct BwdPlan {
   size_t off_dimg; // tc: the duals as fp16 images, 16 KB per slot
   size_t off_dmeta;// tc: their scalars, 4 u32 per slot
   size_t off_P;    // tc: running sums of the tile decays, (B*H, NT + 1) fp64
+  size_t off_cu;   // tc: C_u = v_u . dv_u summed from the pair terms, (B, T, H) fp32
   size_t off_loc;  // d(log a): per-token reverse running sums inside 128-token chunks, fp64
   size_t off_tot;  // chunk totals, then (off_carry) their reverse running sums, fp64
   size_t off_carry;
@@ -400,9 +404,10 @@ __device__ __forceinline__ void load4v(const __nv_bfloat16* p, float (&x)[4]) {
   x[3] = __uint_as_float(v.y & 0xffff0000u);
 }
 
+// cu: C_u from the pair terms where the tensor-core kernels summed it (else v_u . dv_u).
 template <typename TIn>
-__global__ void __launch_bounds__(kDlChunk) bwd_dloga_local(GenPlan p, BwdArgs x, size_t off_dv, double* loc,
-                                                           double* tot) {
+__global__ void __launch_bounds__(kDlChunk) bwd_dloga_local(GenPlan p, BwdArgs x, size_t off_dv, const float* cu,
+                                                           double* loc, double* tot) {
   __shared__ double s_part[kDlChunk / 32];
   const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H, nch = gridDim.x;
   const int L = p.L, dv = p.dv, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -414,13 +419,17 @@ __global__ void __launch_bounds__(kDlChunk) bwd_dloga_local(GenPlan p, BwdArgs x
     const size_t row = ((size_t)b * p.T + t) * p.H + h;
     float R = 0.f, Cv = 0.f;
     for (int l = 0; l < L; ++l) R += x.lam[row * L + l] * x.dlam[row * L + l];
-    const float* dr = dv32 + row * dv;
-    const TIn* vr = v + row * dv;
-    for (int jv = 0; jv < dv; jv += 4) {  // rows 16-byte aligned (d_v a multiple of 16)
-      const float4 d4 = *reinterpret_cast<const float4*>(dr + jv);
-      float v4[4];
-      load4v(vr + jv, v4);
-      Cv += v4[0] * d4.x + v4[1] * d4.y + v4[2] * d4.z + v4[3] * d4.w;
+    if (cu) {
+      Cv = cu[row];
+    } else {
+      const float* dr = dv32 + row * dv;
+      const TIn* vr = v + row * dv;
+      for (int jv = 0; jv < dv; jv += 4) {  // rows 16-byte aligned (d_v a multiple of 16)
+        const float4 d4 = *reinterpret_cast<const float4*>(dr + jv);
+        float v4[4];
+        load4v(vr + jv, v4);
+        Cv += v4[0] * d4.x + v4[1] * d4.y + v4[2] * d4.z + v4[3] * d4.w;
+      }
     }
     val = (double)R - (double)Cv;
   }
@@ -492,7 +501,7 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
   o = al(o + sizeof(float) * (size_t)s.batch * s.T * s.heads * s.d_k);
   bp->off_dv = o;
   o = al(o + sizeof(float) * (size_t)s.batch * s.T * s.heads * s.d_v);
-  bp->off_tc = bp->off_dimg = bp->off_dmeta = bp->off_P = o;
+  bp->off_tc = bp->off_dimg = bp->off_dmeta = bp->off_P = bp->off_cu = o;
   if (bp->tc) {
     o = al(o + bp->tp.bytes);
     bp->off_dimg = o;
@@ -501,6 +510,8 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
     o = al(o + BH * bp->g.nblk * 4 * sizeof(unsigned));
     bp->off_P = o;
     o = al(o + BH * (bp->tp.NT + 1) * sizeof(double));
+    bp->off_cu = o;
+    o = al(o + (size_t)s.batch * s.T * s.heads * sizeof(float));
   }
   const size_t nch = ((size_t)s.T + kDlChunk - 1) / kDlChunk;
   bp->off_loc = o;
@@ -536,7 +547,8 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
     if ((e = launch_tc_nodes(bp.tp, ta, st)) != cudaSuccess) return e;
     if ((e = launch_tc_bwd_intra(s, x.q, x.k, x.v, x.dO, x.a, x.lam, reinterpret_cast<float*>(x.ws + bp.off_dq),
                                  reinterpret_cast<float*>(x.ws + bp.off_dk),
-                                 reinterpret_cast<float*>(x.ws + bp.off_dv), x.dlam, fa.status, st)) != cudaSuccess)
+                                 reinterpret_cast<float*>(x.ws + bp.off_dv), x.dlam,
+                                 reinterpret_cast<float*>(x.ws + bp.off_cu), fa.status, st)) != cudaSuccess)
       return e;
   } else {
     const size_t sm1 = sizeof(float) * ((size_t)2 * C * dk + (size_t)(C + 4) * (dk + dv) + C * dv + C +
@@ -572,7 +584,7 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
                               reinterpret_cast<unsigned*>(x.ws + bp.off_dmeta),
                               reinterpret_cast<double*>(x.ws + bp.off_P), dual_off, p.nblk,
                               reinterpret_cast<float*>(x.ws + bp.off_dk), reinterpret_cast<float*>(x.ws + bp.off_dv),
-                              fa.status, st)) != cudaSuccess)
+                              reinterpret_cast<float*>(x.ws + bp.off_cu), fa.status, st)) != cudaSuccess)
       return e;
   } else {
     const size_t sm3 = sizeof(float) * ((size_t)C * dk + (size_t)(C + 4) * dv + dk * dv + C);
@@ -592,7 +604,8 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
   double* loc = reinterpret_cast<double*>(x.ws + bp.off_loc);
   double* tot = reinterpret_cast<double*>(x.ws + bp.off_tot);
   double* carry = reinterpret_cast<double*>(x.ws + bp.off_carry);
-  bwd_dloga_local<TIn><<<dim3(nch, BH), kDlChunk, 0, st>>>(p, x, bp.off_dv, loc, tot);
+  const float* cu = tc ? reinterpret_cast<const float*>(x.ws + bp.off_cu) : nullptr;
+  bwd_dloga_local<TIn><<<dim3(nch, BH), kDlChunk, 0, st>>>(p, x, bp.off_dv, cu, loc, tot);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   bwd_dloga_carry<<<BH, kT, 0, st>>>(nch, tot, carry);

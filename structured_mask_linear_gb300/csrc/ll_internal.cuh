@@ -108,15 +108,16 @@ cudaError_t launch_tc_bwd_q(const TcPlan& p, const void* q, const void* dO, cons
                             int nslots, unsigned* status, cudaStream_t st);
 // Backward, key side of the inter-tile levels on the tensor cores: the tile-decay running
 // sums (fp64, (B*H, NT+1) in P), the duals as fp16 images (dimg: 16 KB per slot, dmeta: 4
-// u32 per slot), then adds into dk32 and dv32.
+// u32 per slot), then adds into dk32 and dv32, and v_s . (that part of dv_s) into cu.
 cudaError_t launch_tc_bwd_kv(const TcPlan& p, const void* k, const void* v, const float* a, const char* tree_ws,
                              const float* dual, uint8_t* dimg, unsigned* dmeta, double* P, const int* dual_off,
-                             int nslots, float* dk32, float* dv32, unsigned* status, cudaStream_t st);
+                             int nslots, float* dk32, float* dv32, float* cu, unsigned* status, cudaStream_t st);
 // Backward: the in-tile pairs (levels 0..7) on the tensor cores, for tc_supported shapes;
-// assigns the fp32 per-head dq, dk, dv buffers and dlambda (levels >= 8 zeroed).
+// assigns the fp32 per-head dq, dk, dv buffers, dlambda (levels >= 8 zeroed) and cu, the
+// column sums C_s of the in-tile pair terms.
 cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k, const void* v, const void* dO,
                                 const float* a, const float* lam, float* dq32, float* dk32, float* dv32,
-                                float* dlam, unsigned* status, cudaStream_t st);
+                                float* dlam, float* cu, unsigned* status, cudaStream_t st);
 
 __host__ __device__ inline int bit_length(long long x) {
   int l = 0;

@@ -1074,7 +1074,9 @@ __global__ void wait_selftest_kernel(unsigned* status, long long spins) {
 // loss sum(dO . o), restricted to pairs inside one 128-token tile (u): with S = Q Kᵀ,
 // E = dO Vᵀ and w_ts = lambda_t^{l(t,s)} 2^(g_t - g_s) [s <= t],
 //   dq = (w ⊙ E) K,  dk = (w ⊙ E)ᵀ Q,  dv = (w ⊙ S)ᵀ dO,
-//   dlambda_t^l = sum over s at level l of 2^(g_t - g_s) S_ts E_ts   (l = 0..7).
+//   dlambda_t^l = sum over s at level l of 2^(g_t - g_s) S_ts E_ts   (l = 0..7),
+//   C_s = sum_t w_ts S_ts E_ts (the column sums of the pair terms; with the row sums
+//   R_t = sum_l lambda_t^l dlambda_t^l they give d(log a) without the rounding of dv).
 // One CTA (256 threads, one per SM: 512 TMEM columns, 175 KB shared memory) per
 // (b, h, tile):
 //   S and E on the tensor cores from the bf16 inputs (TMEM columns 0..127, 128..255);
@@ -1095,11 +1097,28 @@ struct TcBwdParams {
   float* dk32;   // (B, T, H, d_k)
   float* dv32;   // (B, T, H, d_v)
   float* dlam;   // (B, T, H, L): levels 0..7 written, the rest zeroed
+  float* cu;     // (B, T, H): C_s = sum_t A_ts over the in-tile pairs (fp32, from S and E)
   unsigned* status;
 };
 
+// Warp reduce-scatter of 32 columns: on return lane j holds the sum over the warp's lanes
+// of v[j] (31 shuffles).
+__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) {
+    const bool up = (lane & k) != 0;
+#pragma unroll
+    for (int i = 0; i < k; ++i) {
+      const float send = up ? v[i] : v[i + k];
+      const float keep = up ? v[i + k] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+    }
+  }
+  return v[0];
+}
+
 constexpr int kBwdFixed = 163840;  // Q, K, V, dO, dS, P in front of the small tables
-constexpr int kSmemBwd = kBwdFixed + 2 * 128 * 4 + 2 * 128 * 9 * 4 + 1024;
+constexpr int kSmemBwd = kBwdFixed + 3 * 128 * 4 + 2 * 128 * 9 * 4 + 1024;
 
 // Shared-memory address of the 16-byte chunk holding keys 8c..8c+7 (c = 0..15) of row r of
 // a 128 x 128 fp16 tile stored as two 64-column boxes with the 128-byte swizzle.
@@ -1124,6 +1143,7 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
   float* sB8 = sG + 128;                                    // 128: 2^(g_end8(s) - g_s)
   float* sLam8 = sB8 + 128;                                 // 128 x 9: lambda levels 0..7 of row r
   float* sAcc = sLam8 + 128 * 9;                            // 128 x 9: dlambda of the diagonal group
+  float* sCol = sAcc + 128 * 9;                             // 128: column sums C_s
   __shared__ __align__(8) uint64_t bar_ld, bar_se, bar_mm;
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[8];
@@ -1164,6 +1184,7 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
     for (int l = 0; l < kLevIntra; ++l) ptx::cp_async4(sLam8 + r * 9 + l, lrow + l);
 #pragma unroll
     for (int l = 0; l < 9; ++l) sAcc[r * 9 + l] = 0.f;
+    sCol[r] = 0.f;
   }
   // chunk-local log2 decay cumsum over the 128 rows (both roles compute it)
   float gt = log2f(p.a[row * p.H + h]);
@@ -1275,6 +1296,7 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
         for (int kb = 0; kb < 4; ++kb) ak[kb] = exp2f(gt - sG[cg * 32 + kb * 8 + 7]);
         const float4* b4 = reinterpret_cast<const float4*>(sB8 + cg * 32);
         float xs = 0.f;
+        float colv[32];
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
           const float4 bb = b4[j4];
@@ -1284,7 +1306,9 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
           for (int e = 0; e < 4; ++e) {
             const int j = 4 * j4 + e;
             const float dd = ak[j4 >> 1] * bj[e];
-            xs += dd * (sv[j] * ev[j]);
+            const float xj = dd * (sv[j] * ev[j]);
+            xs += xj;
+            colv[j] = lv * xj;
             const float w = lv * dd;
             vs[e] = (w * cs) * ev[j];
             vp[e] = (w * cp) * sv[j];
@@ -1296,6 +1320,7 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
         }
         if (l7) acc7 += xs;
         else acc6 += xs;
+        atomicAdd(sCol + cg * 32 + lane, warp_colsum32(colv, lane));
       } else if (ok && cg == quad) {
         // the diagonal 32-group: levels 0..5 (level of key j: bit length of tl ^ j)
         float sv[32], ev[32];
@@ -1307,6 +1332,7 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
         for (int kb = 0; kb < 4; ++kb) ak[kb] = exp2f(gt - gq[kb * 8 + 7]);
         const float4* b4 = reinterpret_cast<const float4*>(sB8 + cg * 32);
         float* accr = sAcc + r * 9;
+        float colv[32];
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
           const float4 bb = b4[j4];
@@ -1322,13 +1348,16 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
             const float w = on ? lamr[lvj] * dd : 0.f;
             vs[e] = (w * cs) * ev[j];
             vp[e] = (w * cp) * sv[j];
-            if (on) accr[lvj] += dd * (sv[j] * ev[j]);
+            const float xj = on ? dd * (sv[j] * ev[j]) : 0.f;
+            if (on) accr[lvj] += xj;
+            colv[j] = on ? lamr[lvj] * xj : 0.f;
           }
           pd[2 * j4] = pack_h2(vs[0], vs[1]);
           pd[2 * j4 + 1] = pack_h2(vs[2], vs[3]);
           pp[2 * j4] = pack_h2(vp[0], vp[1]);
           pp[2 * j4 + 1] = pack_h2(vp[2], vp[3]);
         }
+        atomicAdd(sCol + cg * 32 + lane, warp_colsum32(colv, lane));
       } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j) pd[j] = pp[j] = 0u;
@@ -1342,7 +1371,9 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
       }
     }
     ptx::fence_proxy_async_smem();
+    ptx::named_bar_sync(1, 128);  // column sums complete
     if (ok) {
+      p.cu[row * p.H + h] = sCol[r];
       float* dl = p.dlam + (row * p.H + h) * p.L;
       const float* accr = sAcc + r * 9;
 #pragma unroll
@@ -1874,6 +1905,7 @@ struct TcBwdKVParams {
   const double* P;        // (B*H, NT + 1)
   float* dk32;
   float* dv32;
+  float* cu;    // (B, T, H): adds v_s . (the inter-tile part of dv_s)
   unsigned* status;
 };
 
@@ -2083,6 +2115,19 @@ __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant
       o.w += rs * av[c + 3];
       *reinterpret_cast<float4*>(dv + c) = o;
     }
+    // v_s . (these d_v columns): V is fp16 in shared memory, 2^ev times the input
+    float cdot = 0.f;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint4 x = *reinterpret_cast<const uint4*>(RV + r * 128 + (((2 * qq + c) ^ rot) << 4));
+      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 vv = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+        cdot += vv.x * av[8 * c + 2 * e] + vv.y * av[8 * c + 2 * e + 1];
+      }
+    }
+    atomicAdd(p.cu + row * p.H + h, rs * pow2i(ev) * cdot);
   }
   if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
     wait_bar(&bar_ld, 0);
@@ -2373,7 +2418,7 @@ cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, con
 
 cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, const float* a, const char* tree_ws,
                              const float* dual, uint8_t* dimg, unsigned* dmeta, double* P, const int* dual_off,
-                             int nslots, float* dk32, float* dv32, unsigned* status, cudaStream_t st) {
+                             int nslots, float* dk32, float* dv32, float* cu, unsigned* status, cudaStream_t st) {
   const unsigned BH = (unsigned)(tp.B * tp.H);
   tc_tile_prefix_kernel<<<BH, 256, 0, st>>>(reinterpret_cast<const unsigned*>(tree_ws + tp.off_meta), tp.nnodes,
                                             tp.NT, P);
@@ -2402,6 +2447,7 @@ cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, con
   p.P = P;
   p.dk32 = dk32;
   p.dv32 = dv32;
+  p.cu = cu;
   p.status = status;
   if ((e = cudaFuncSetAttribute(tc_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwdKV)) !=
       cudaSuccess)
@@ -2414,7 +2460,7 @@ cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, con
 
 cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k, const void* v, const void* dO,
                                 const float* a, const float* lam, float* dq32, float* dk32, float* dv32,
-                                float* dlam, unsigned* status, cudaStream_t st) {
+                                float* dlam, float* cu, unsigned* status, cudaStream_t st) {
   if (!tc_supported(s)) return cudaErrorInvalidValue;
   const int G = s.heads / s.heads_per_group, NT = s.T / kTile;
   CUtensorMap mQ, mK, mV, mD;
@@ -2422,7 +2468,7 @@ cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k,
       !make_map(&mV, v, kDv, s.heads, s.T, s.batch) || !make_map(&mD, dO, kDv, s.heads, s.T, s.batch))
     return cudaErrorInvalidValue;
   const TcBwdParams p{s.batch, s.T, s.heads, s.heads_per_group, G, s.levels, NT, a, lam,
-                      dq32, dk32, dv32, dlam, status};
+                      dq32, dk32, dv32, dlam, cu, status};
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwd);
   if (e != cudaSuccess) return e;
   tc_bwd_intra_kernel<<<(unsigned)((size_t)s.batch * NT * s.heads), 256, kSmemBwd, st>>>(mQ, mK, mV, mD, p);

@@ -65,3 +65,31 @@ def test_ungrouped_small_dims(sml):
     w = workload("small", batch=1, heads=3, heads_per_group=1, T=640, levels=levels_for(640) + 1,
                  d_k=32, d_v=16, decay="slow")
     _check(sml, w, make_inputs(w, "cpu", seed=34), 32, "ungrouped")
+
+
+def test_pages_workload_group_slice(sml):
+    """The backward at the benchmark's size and launch configuration (pages workload:
+    B=4, H=48 in 24 Q/K groups, T=8192, chunk 64): the oracle computes one Q/K group (its
+    two heads) of one batch element over the whole sequence, and every gradient of that
+    slice is compared (dq and dk are sums over the group's heads)."""
+    import numpy as np
+
+    w = workload("pages")
+    x = make_inputs(w, DEV, seed=0)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(99)
+    dO = torch.randn(x.v.shape, generator=gen, device=DEV).to(x.v.dtype)
+    got = sml.loglinear_bwd(x.q, x.k, x.v, x.a, x.lam, dO, chunk=w.chunk)
+    torch.cuda.synchronize()
+    assert sml.loglinear_check_status() == 0
+    r = np.random.default_rng(7)
+    b, g = int(r.integers(w.batch)), int(r.integers(w.heads // w.heads_per_group))
+    hs = slice(g * w.heads_per_group, (g + 1) * w.heads_per_group)
+    gs = slice(g, g + 1)
+    bs = slice(b, b + 1)
+    ref = oracle.backward(to_numpy64(x.q[bs, :, gs]), to_numpy64(x.k[bs, :, gs]), to_numpy64(x.v[bs, :, hs]),
+                          to_numpy64(x.a[bs, :, hs]), to_numpy64(x.lam[bs, :, hs]), to_numpy64(dO[bs, :, hs]))
+    sel = (gs, gs, hs, hs, hs)
+    for name, t, rr, s in zip(NAMES, got, ref, sel):
+        dtype = t.dtype if name in ("dq", "dk", "dv") else torch.float32
+        assert_parity(t[bs, :, s].double().cpu().numpy(), rr, f"pages b={b} g={g} {name}", dtype)

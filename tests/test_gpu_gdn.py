@@ -66,3 +66,38 @@ def test_gdn_zero_beta_is_zero(sml):
     x, beta = _inputs(w, seed=52)
     o = _run(sml, w, x, torch.zeros_like(beta), 64)
     assert float(o.abs().max()) == 0.0
+
+
+def test_pages_workload_sampled(sml):
+    """The Gated DeltaNet forward at the benchmark's size (pages workload: B=4, H=48,
+    T=8192, chunk 64): the oracle's delta-rule values of two heads over the whole
+    sequence, then sampled outputs (edges of tiles, chunks and the sequence, plus random
+    positions) through the oracle's point form of the masked sum."""
+    import numpy as np
+
+    w = workload("pages")
+    x = make_inputs(w, DEV, seed=0)
+    k = x.k.float()
+    kn = (k / k.norm(dim=-1, keepdim=True)).to(x.k.dtype)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(6)
+    beta = torch.sigmoid(torch.randn(x.a.shape, generator=gen, device=DEV))
+    o = sml.loglinear_gdn_fwd(x.q, kn, x.v, x.a, beta, x.lam, chunk=w.chunk)
+    torch.cuda.synchronize()
+    assert sml.loglinear_check_status() == 0
+    assert torch.isfinite(o).all()
+    r = np.random.default_rng(8)
+    T = w.T
+    for _ in range(2):
+        b, h = int(r.integers(w.batch)), int(r.integers(w.heads))
+        g = h // w.heads_per_group
+        u = oracle.gdn_values(to_numpy64(kn[b:b + 1, :, g:g + 1]), to_numpy64(x.v[b:b + 1, :, h:h + 1]),
+                              to_numpy64(x.a[b:b + 1, :, h:h + 1]), to_numpy64(beta[b:b + 1, :, h:h + 1]))
+        ts = {0, 1, 31, 32, 63, 64, 127, 128, T // 2 - 1, T // 2, T - 65, T - 64, T - 1}
+        ts = np.array(sorted(ts | set(int(t) for t in r.integers(0, T, size=60))))
+        tm = int(ts.max()) + 1
+        ref = oracle.form_q_points(to_numpy64(x.q[b, :tm, g]), to_numpy64(kn[b, :tm, g]), u[0, :tm, 0],
+                                   to_numpy64(x.a[b, :tm, h]), to_numpy64(x.lam[b, torch.as_tensor(ts, device=DEV), h]),
+                                   ts)
+        got = o[b, torch.as_tensor(ts, device=DEV), h].double().cpu().numpy()
+        assert_parity(got, ref, f"gdn pages b={b} h={h}", o.dtype)
