@@ -43,9 +43,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the long/decode/e2e extras")
-    ap.add_argument("--ncu-case", action="store_true",
-                    help="profiling case: 3 forwards of the pages workload at batch 1 "
-                         "(inputs 225 MB > L2), no timing, no JSON")
+    ap.add_argument("--ncu-case", nargs="?", const="fwd", choices=["fwd", "bwd", "gdn"],
+                    help="profiling case on the pages workload at batch 1 (inputs 225 MB > L2), "
+                         "no timing, no JSON: three forwards (fwd, the default), two backwards "
+                         "(bwd) or two Gated DeltaNet forwards (gdn)")
     return ap.parse_args()
 
 
@@ -271,7 +272,7 @@ def run_reference(args):
 
 
 # ---- GPU arm --------------------------------------------------------------------------
-def ncu_case():
+def ncu_case(what: str = "fwd"):
     import torch
 
     import structured_mask_linear_gb300 as sml
@@ -280,10 +281,23 @@ def ncu_case():
     sml.lib()
     w = workload("pages", batch=1)
     x = make_inputs(w, "cuda", seed=0)
-    st = torch.empty((1, w.heads, w.T.bit_length() + 1, w.d_k, w.d_v), device="cuda")
-    for _ in range(3):
-        sml.loglinear_fwd(x.q, x.k, x.v, x.a, x.lam, chunk=w.chunk, states_out=st,
-                          state_levels=w.T.bit_length() + 1)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(99)
+    if what == "fwd":
+        st = torch.empty((1, w.heads, w.T.bit_length() + 1, w.d_k, w.d_v), device="cuda")
+        for _ in range(3):
+            sml.loglinear_fwd(x.q, x.k, x.v, x.a, x.lam, chunk=w.chunk, states_out=st,
+                              state_levels=w.T.bit_length() + 1)
+    elif what == "bwd":
+        dO = torch.randn(x.v.shape, generator=gen, device="cuda").to(x.v.dtype)
+        for _ in range(2):
+            sml.loglinear_bwd(x.q, x.k, x.v, x.a, x.lam, dO, chunk=w.chunk)
+    else:
+        kn = x.k.float()
+        kn = (kn / kn.norm(dim=-1, keepdim=True)).to(x.k.dtype)
+        beta = torch.sigmoid(torch.randn(x.a.shape, generator=gen, device="cuda"))
+        for _ in range(2):
+            sml.loglinear_gdn_fwd(x.q, kn, x.v, x.a, beta, x.lam, chunk=w.chunk)
     torch.cuda.synchronize()
     assert sml.loglinear_check_status() == 0
 
@@ -291,7 +305,7 @@ def ncu_case():
 def main():
     args = parse()
     if args.ncu_case:
-        ncu_case()
+        ncu_case(args.ncu_case)
         return
     if args.impl == "reference":
         run_reference(args)
