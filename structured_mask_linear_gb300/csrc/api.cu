@@ -352,7 +352,9 @@ ll_status loglinear_gdn_fwd(const ll_shape* s, const void* q, const void* k, con
   // u (the transformed values) after the forward's own workspace
   const size_t fws = a256(loglinear_fwd_workspace_bytes(s));
   char* u = static_cast<char*>(workspace) + fws;
-  if (ll::launch_gdn_values(*s, k, v, a, beta, u, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  unsigned* sw = status_word();
+  if (!sw) return LL_ERR_CUDA;
+  if (ll::launch_gdn_values(*s, k, v, a, beta, u, sw, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return LL_ERR_CUDA;
   return fwd_impl(s, q, k, u, a, lambda, o, workspace, fws, nullptr, nullptr, 0, stream, nullptr, 0);
 }

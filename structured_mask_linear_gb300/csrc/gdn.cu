@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(kG, 3) gdn_pass(int T, int H, int hpg, int dk,
 size_t gdn_values_bytes(const ll_shape& s) {
   const size_t e = s.dtype == LL_BF16 ? 2 : 4;
   const size_t ub = (((size_t)s.batch * s.T * s.heads * s.d_v * e) + 255) & ~size_t(255);
+  if (tc_supported(s)) return ub + tc_gdn_bytes(s);  // the tensor-core chunks (128 tokens)
   const size_t xb = (size_t)s.batch * s.T * s.heads * (s.d_v + s.d_k + 1) * sizeof(float);
   return ub + ((xb + 255) & ~size_t(255));
 }
@@ -418,7 +419,11 @@ cudaError_t run_gdn(const ll_shape& s, const void* k, const void* v, const float
 }  // namespace
 
 cudaError_t launch_gdn_values(const ll_shape& s, const void* k, const void* v, const float* a,
-                              const float* beta, void* u, cudaStream_t st) {
+                              const float* beta, void* u, unsigned* status, cudaStream_t st) {
+  if (tc_supported(s)) {
+    const size_t ub = (((size_t)s.batch * s.T * s.heads * s.d_v * 2) + 255) & ~size_t(255);
+    return launch_tc_gdn(s, k, v, a, beta, u, static_cast<char*>(u) + ub, status, st);
+  }
   return s.dtype == LL_BF16 ? run_gdn<__nv_bfloat16>(s, k, v, a, beta, u, st)
                             : run_gdn<float>(s, k, v, a, beta, u, st);
 }

@@ -48,10 +48,15 @@ cudaError_t launch_generic_fwd(const GenPlan& p, bool bf16, const FwdArgs& a, cu
 // Only the chunk states and Fenwick blocks of the generic forward (for the backward).
 cudaError_t launch_generic_states(const GenPlan& p, bool bf16, const FwdArgs& a, cudaStream_t st);
 
+// Gated DeltaNet's transformed values on the tensor cores (128-token chunks) for
+// tc_supported shapes: workspace bytes and the launch (u: (B, T, H, d_v) bf16).
+size_t tc_gdn_bytes(const ll_shape& s);
+cudaError_t launch_tc_gdn(const ll_shape& s, const void* k, const void* v, const float* a, const float* beta,
+                          void* u, char* ws, unsigned* status, cudaStream_t st);
 // Gated DeltaNet's transformed values (csrc/gdn.cu): buffer bytes and the launch.
 size_t gdn_values_bytes(const ll_shape& s);
 cudaError_t launch_gdn_values(const ll_shape& s, const void* k, const void* v, const float* a,
-                              const float* beta, void* u, cudaStream_t st);
+                              const float* beta, void* u, unsigned* status, cudaStream_t st);
 
 // Backward (csrc/backward.cu): workspace bytes (0: unsupported) and the launches.
 size_t bwd_workspace_bytes(const ll_shape& s);
