@@ -2147,7 +2147,7 @@ __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant
 // tc_gdn_local, one CTA per (b, h, chunk), 256 threads, one CTA per SM:
 //   K Kᵀ on tcgen05 from the bf16 keys (exact products, fp32 sums); A in fp32 in shared
 //   memory; T by 16-row blocks on the CUDA cores (diagonal blocks by substitution in
-//   registers, then T_ij = -T_ii sum_{j <= k < i} A_ik T_kj, column block j by warp j);
+//   registers, then T_ij = -T_ii sum_{j <= k < i} A_ik T_kj column block by column block);
 //   then [W | U_loc] = T [diag(beta 2^g) K | diag(beta) V] on tcgen05 with every operand
 //   split into an fp16 high part and the fp16 rounding remainder (hi hi + lo hi + hi lo,
 //   about 22 significant bits), each with a power-of-two tile scale.  Per chunk the
@@ -2306,45 +2306,76 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     for (int t = 0; t < 16; ++t) Tm[(r0 + t) * kGP + r0 + j] = x[t];
   }
   __syncthreads();
-  // blocks below the diagonal: column block jb by warp jb, with warp syncs only (its
-  // blocks need the diagonal blocks and its own earlier ones):
+  // blocks below the diagonal, column block by column block (each needs only the diagonal
+  // blocks and its own earlier ones):
   //   Y = sum_{jb <= k < ib} A_{ib,k} T_{k,jb},  T_{ib,jb} = -T_{ib,ib} Y,  ib = jb+1 .. 7.
-  // Lane (rr, half) holds row rr, columns 8 half .. 8 half + 7 of the block.
+  // The work of column block jb falls with jb: blocks 0, 1, 2 go to warp pairs (rows
+  // split, a 64-thread barrier per step), blocks 3 + 6 and 4 + 5 to single warps.
   if (ok) {
-    const int jb = warp, rr = lane >> 1, c0 = (lane & 1) * 8;
-    float* Yw = Ym + warp * 256;
-    for (int ib = jb + 1; ib < 8; ++ib) {
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = 0.f;
-      const float* arow = Am + (16 * ib + rr) * kGP;
+    const bool pair = warp < 6;
+    const int njb = pair ? 1 : 2;
+    const int jb0 = pair ? (warp >> 1) : (warp == 6 ? 3 : 4);
+    float* Yw = Ym + (pair ? (warp >> 1) : warp - 3) * 256;
+    for (int q = 0; q < njb; ++q) {
+      const int jb = q == 0 ? jb0 : 9 - jb0;  // 3 then 6, 4 then 5
+      for (int ib = jb + 1; ib < 8; ++ib) {
+        if (pair) {  // rows 8 (warp & 1) + lane / 4, columns 4 (lane % 4) .. + 3
+          const int rr = (warp & 1) * 8 + (lane >> 2), c0 = (lane & 3) * 4;
+          float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+          const float* arow = Am + (16 * ib + rr) * kGP;
 #pragma unroll 4
-      for (int s2 = 16 * jb; s2 < 16 * ib; ++s2) {
-        const float av = arow[s2];
-        const float4 t0v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0);
-        const float4 t1v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0 + 4);
-        y[0] += av * t0v.x; y[1] += av * t0v.y; y[2] += av * t0v.z; y[3] += av * t0v.w;
-        y[4] += av * t1v.x; y[5] += av * t1v.y; y[6] += av * t1v.z; y[7] += av * t1v.w;
-      }
-      *reinterpret_cast<float4*>(Yw + rr * 16 + c0) = make_float4(y[0], y[1], y[2], y[3]);
-      *reinterpret_cast<float4*>(Yw + rr * 16 + c0 + 4) = make_float4(y[4], y[5], y[6], y[7]);
-      __syncwarp();
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.f;
-      const float* trow = Tm + (16 * ib + rr) * kGP + 16 * ib;
+          for (int s2 = 16 * jb; s2 < 16 * ib; ++s2) {
+            const float av = arow[s2];
+            const float4 tv = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0);
+            y0 += av * tv.x; y1 += av * tv.y; y2 += av * tv.z; y3 += av * tv.w;
+          }
+          *reinterpret_cast<float4*>(Yw + rr * 16 + c0) = make_float4(y0, y1, y2, y3);
+          ptx::named_bar_sync(1 + (warp >> 1), 64);
+          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+          const float* trow = Tm + (16 * ib + rr) * kGP + 16 * ib;
 #pragma unroll 4
-      for (int s2 = 0; s2 < 16; ++s2) {
-        const float tv = trow[s2];
-        const float4 y0 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0);
-        const float4 y1 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0 + 4);
-        x[0] += tv * y0.x; x[1] += tv * y0.y; x[2] += tv * y0.z; x[3] += tv * y0.w;
-        x[4] += tv * y1.x; x[5] += tv * y1.y; x[6] += tv * y1.z; x[7] += tv * y1.w;
+          for (int s2 = 0; s2 < 16; ++s2) {
+            const float tv = trow[s2];
+            const float4 yv = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0);
+            x0 += tv * yv.x; x1 += tv * yv.y; x2 += tv * yv.z; x3 += tv * yv.w;
+          }
+          *reinterpret_cast<float4*>(Tm + (16 * ib + rr) * kGP + 16 * jb + c0) = make_float4(-x0, -x1, -x2, -x3);
+          ptx::named_bar_sync(1 + (warp >> 1), 64);
+        } else {  // row lane / 2, columns 8 (lane % 2) .. + 7
+          const int rr = lane >> 1, c0 = (lane & 1) * 8;
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = 0.f;
+          const float* arow = Am + (16 * ib + rr) * kGP;
+#pragma unroll 4
+          for (int s2 = 16 * jb; s2 < 16 * ib; ++s2) {
+            const float av = arow[s2];
+            const float4 t0v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0);
+            const float4 t1v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0 + 4);
+            y[0] += av * t0v.x; y[1] += av * t0v.y; y[2] += av * t0v.z; y[3] += av * t0v.w;
+            y[4] += av * t1v.x; y[5] += av * t1v.y; y[6] += av * t1v.z; y[7] += av * t1v.w;
+          }
+          *reinterpret_cast<float4*>(Yw + rr * 16 + c0) = make_float4(y[0], y[1], y[2], y[3]);
+          *reinterpret_cast<float4*>(Yw + rr * 16 + c0 + 4) = make_float4(y[4], y[5], y[6], y[7]);
+          __syncwarp();
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+          const float* trow = Tm + (16 * ib + rr) * kGP + 16 * ib;
+#pragma unroll 4
+          for (int s2 = 0; s2 < 16; ++s2) {
+            const float tv = trow[s2];
+            const float4 y0 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0);
+            const float4 y1 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0 + 4);
+            x[0] += tv * y0.x; x[1] += tv * y0.y; x[2] += tv * y0.z; x[3] += tv * y0.w;
+            x[4] += tv * y1.x; x[5] += tv * y1.y; x[6] += tv * y1.z; x[7] += tv * y1.w;
+          }
+          float* dst = Tm + (16 * ib + rr) * kGP + 16 * jb + c0;
+          *reinterpret_cast<float4*>(dst) = make_float4(-x[0], -x[1], -x[2], -x[3]);
+          *reinterpret_cast<float4*>(dst + 4) = make_float4(-x[4], -x[5], -x[6], -x[7]);
+          __syncwarp();
+        }
       }
-      float* dst = Tm + (16 * ib + rr) * kGP + 16 * jb + c0;
-      *reinterpret_cast<float4*>(dst) = make_float4(-x[0], -x[1], -x[2], -x[3]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(-x[4], -x[5], -x[6], -x[7]);
-      __syncwarp();
     }
   }
   __syncthreads();
