@@ -199,9 +199,13 @@ size_t loglinear_gdn_fwd_workspace_bytes(const ll_shape* shape);
  * Log-linear Gated DeltaNet forward.  Arguments as for loglinear_fwd, plus
  *   beta  (B, T, H)  fp32, the delta-rule write strength (in [0, 1] for a stable rule)
  * Keys are used as given; the model normalises them (the delta rule is stable for
- * beta |k|^2 <= 2).  u is computed by one CTA per (b, h) walking the sequence in order
- * (the delta rule is sequential across chunks), stored in the input dtype in the
- * workspace, then the level-fused forward runs on (q, k, u, a, lambda).
+ * beta |k|^2 <= 2).  u is computed chunk by chunk in the delta rule's WY form: the
+ * chunks' local solves run in parallel, then one CTA per (b, h) carries the state across
+ * the chunks in order.  For bf16 with d_k = 128, d_v = 64 and T % 128 == 0 the chunks
+ * are 128 tokens and the products run on the tensor cores (fp16 high and low parts,
+ * fp32 accumulation); otherwise 32-token chunks run in fp32 on the CUDA cores.  u is
+ * stored in the input dtype in the workspace, then the level-fused forward runs on
+ * (q, k, u, a, lambda).
  */
 ll_status loglinear_gdn_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
                             const float* a, const float* beta, const float* lambda, void* o,
