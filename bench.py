@@ -164,11 +164,14 @@ def traffic_for(kernel: str, w):
     d = json.load(open(p)).get(kernel)
     if not d:
         return None
-    src = os.path.join(ROOT, "structured_mask_linear_gb300", "csrc", d["source"])
-    if not os.path.exists(src):
-        return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if sha != d["source_sha256"]:
+    srcs = d["source"] if isinstance(d["source"], list) else [d["source"]]
+    h = hashlib.sha256()
+    for name in srcs:  # every file the kernel is compiled from, in order
+        src = os.path.join(ROOT, "structured_mask_linear_gb300", "csrc", name)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    if h.hexdigest() != d["source_sha256"]:
         return None
     return d["bytes_per_token"] * w.batch * w.T
 
@@ -520,7 +523,7 @@ def backward_measure(sml, torch, x, w, hbm_peak, steps=3):
     nbytes = 2 * (el(x.q) + el(x.k) + el(x.v) + el(x.a) + el(x.lam)) + el(dO)
     res = {"workload": workload_desc(w), "ms_per_step": ms, "unit": "tokens/s",
            "value": w.batch * w.T / (ms / 1e3), "steps": steps,
-           "path": "tensor cores: tc_bwd_intra, tc_bwd_q, tc_bwd_kv (csrc/tc_fwd.cu), sums in csrc/backward.cu",
+           "path": "tensor cores: tc_bwd_intra, tc_bwd_q, tc_bwd_kv (csrc/tc_bwd.cu), sums in csrc/backward.cu",
            "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": hbm_peak,
                         "unit": "GB/s", "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
                         "algorithmic_bytes_per_step": nbytes}}

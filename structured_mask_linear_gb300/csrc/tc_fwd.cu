@@ -28,150 +28,13 @@
 //
 // Every mbarrier wait is bounded by 2 s of %globaltimer; a wait that runs out records
 // LL_ERR_TIMEOUT in the status word and the CTA skips the rest of its work.
-#include <cuda.h>
-#include <cuda_fp16.h>
-#include <cudaTypedefs.h>
-#include <cuda_runtime.h>
-
-#include <mutex>
 #include <utility>
 
-#include "ll_internal.cuh"
-#include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace ll {
 
 namespace {
-
-constexpr int kTile = 128;                   // tokens per tile
-constexpr int kDk = 128, kDv = 64;            // supported head dims
-constexpr int kLevIntra = 8;                  // levels 0..7 live inside a 128-token tile
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
-constexpr int kImgBytes = kDk * kDv * 2;      // fp16 node image, 128 rows x 128 bytes
-constexpr int kMeta = 4;  // u32 per node: spare, scale exponent, log2 decay (f32 bits), spare
-
-struct TcParams {
-  int B, T, H, hpg, G, L, NT, nnodes, MT;
-  int node_off[32];
-  const float* a;
-  const float* lam;
-  __nv_bfloat16* o;
-  uint8_t* img;    // (B*H, nnodes, 16 KB) fp16 node images
-  unsigned* meta;  // (B*H, nnodes, 4)
-  unsigned* status;
-  // comparators only (single-level and SSD output modes)
-  float* o32;      // (B, T, H, d_v) fp32 running sum of the single-level passes
-  int lsel;        // the one level of a single-level pass
-  int lflags;      // bit 0: first pass (store), bit 1: last pass (write o)
-  uint8_t* pimg;   // (B*H, NT, 16 KB) SSD prefix-state images
-  unsigned* pmeta; // (B*H, NT, 4)
-};
-
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (ptx::globaltimer_ns() - t0 > kWaitNs) return false;
-  }
-}
-
-// 2^e as an exact float, e in [-126, 127].
-__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
-// 2^e for a sum of two exponents (|e| <= 252): product of two exact powers of two.
-__device__ __forceinline__ float pow2s(int e) {
-  const int h = e / 2;
-  return pow2i(h) * pow2i(e - h);
-}
-
-// Exponent e with m * 2^-e in [2^14, 2^15): scaling by 2^-e keeps fp16 away from
-// overflow (max 65504) and keeps 29 binades below the maximum in fp16's normal range.
-__device__ __forceinline__ int f16_exp(float m) {
-  if (!(m > 0.f)) return 0;
-  int eb = ((__float_as_int(m) >> 23) & 0xff) - 127;
-  if (eb < -126) eb = -126;
-  int e = eb - 14;
-  return e < -100 ? -100 : (e > 100 ? 100 : e);
-}
-
-// Block-wide inclusive prefix sum over 128 threads (one value each).
-__device__ __forceinline__ float block_scan128(float x, float* s_red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    float y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) s_red[warp] = x;
-  __syncthreads();
-  float add = 0.f;
-  for (int w = 0; w < warp; ++w) add += s_red[w];
-  __syncthreads();
-  return x + add;
-}
-
-// Block-wide max of two values (128 threads).
-__device__ __forceinline__ float2 block_max2(float2 v, float2* s_red2) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off; off >>= 1) {
-    v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, off));
-    v.y = fmaxf(v.y, __shfl_xor_sync(0xffffffffu, v.y, off));
-  }
-  if (lane == 0) s_red2[warp] = v;
-  __syncthreads();
-  float2 r = s_red2[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
-    r.x = fmaxf(r.x, s_red2[w].x);
-    r.y = fmaxf(r.y, s_red2[w].y);
-  }
-  __syncthreads();
-  return r;
-}
-
-__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-  __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Publishes one tree node from 128 threads, thread tid holding row tid (d_k index) of the
-// d_k x d_v fp32 state in cur: an fp16 image with a power-of-two scale 2^e (maximum in
-// [2^14, 2^15)), row tid at chunk slots c ^ (tid & 7), staged through `stage` (16 KB of
-// shared memory whose row tid only this thread uses before the call) so that the global
-// stores coalesce; then the scale exponent and the node's log2 decay G into meta.
-__device__ __forceinline__ void publish_node(const float (&cur)[kDv], uint8_t* stage, size_t node,
-                                             float G, float2* s_red2, uint8_t* img, unsigned* meta) {
-  const int tid = threadIdx.x, rot = tid & 7;
-  float m = 0.f;
-#pragma unroll
-  for (int j = 0; j < kDv; ++j) m = fmaxf(m, fabsf(cur[j]));
-  const int e = f16_exp(block_max2(make_float2(m, 0.f), s_red2).x);
-  const float s = pow2i(-e);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const int cc = c ^ rot;
-    *reinterpret_cast<uint4*>(stage + tid * 128 + (cc << 4)) =
-        make_uint4(pack_h2(cur[8 * c] * s, cur[8 * c + 1] * s), pack_h2(cur[8 * c + 2] * s, cur[8 * c + 3] * s),
-                   pack_h2(cur[8 * c + 4] * s, cur[8 * c + 5] * s), pack_h2(cur[8 * c + 6] * s, cur[8 * c + 7] * s));
-  }
-  __syncthreads();
-  uint4* dst = reinterpret_cast<uint4*>(img + node * kImgBytes);
-#pragma unroll
-  for (int r = 0; r < kImgBytes / 16 / 128; ++r)
-    dst[r * 128 + tid] = reinterpret_cast<const uint4*>(stage)[r * 128 + tid];
-  if (tid == 0) {
-    meta[node * kMeta + 1] = (unsigned)e;
-    meta[node * kMeta + 2] = __float_as_uint(G);
-  }
-}
-
 // ---------------------------------------------------------------------------------
 // tc_state: tile states (level 0 of the Fenwick tree over tiles).
 // ---------------------------------------------------------------------------------
@@ -410,34 +273,6 @@ constexpr int kOutFixed = 104704;  // shared bytes in front of the inter-level l
 constexpr int kMaxInter = 19;      // inter-tile levels per tile supported (NT <= 2^19)
 __host__ __device__ constexpr int out_smem_bytes(int ninter) {
   return kOutFixed + 512 * (ninter > 0 ? ninter : 1) + 1024;
-}
-
-__device__ __forceinline__ int nth_set_bit(unsigned x, int i) {
-  for (int j = 0; j < i; ++j) x &= x - 1;
-  return __ffs(x) - 1;
-}
-// |.|-max of two bf16 pairs, halfwise (the sign of the result is meaningless)
-__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t w) {
-  uint32_t d;
-  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(acc), "r"(w));
-  return d;
-}
-__device__ __forceinline__ float bf16x2_maxhalf(uint32_t w) {
-  return fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xffff0000u)));
-}
-__device__ __forceinline__ uint32_t absmax_u4(uint32_t acc, const uint4& x) {
-  return bf16x2_absmax(bf16x2_absmax(acc, x.x), bf16x2_absmax(x.y, bf16x2_absmax(x.z, x.w)));
-}
-// bf16 pair -> fp16 pair, both times s2 (an exact power of two, so the bf16 product is exact)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, __nv_bfloat162 s2) {
-  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&w);
-  x = __hmul2(x, s2);
-  const uint32_t y = *reinterpret_cast<uint32_t*>(&x);
-  return pack_h2(__uint_as_float(y << 16), __uint_as_float(y & 0xffff0000u));
-}
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& x, __nv_bfloat162 s2) {
-  return make_uint4(bf16x2_to_f16x2(x.x, s2), bf16x2_to_f16x2(x.y, s2), bf16x2_to_f16x2(x.z, s2),
-                    bf16x2_to_f16x2(x.w, s2));
 }
 
 template <int kMode>
@@ -1068,1811 +903,8 @@ __global__ void wait_selftest_kernel(unsigned* status, long long spins) {
 }
 
 // ---------------------------------------------------------------------------------
-// tc_bwd_intra: the in-tile pairs (levels 0..7) of the backward on the tensor cores.
-//
-// Chain rule on o_t = sum_{s<=t} lambda_t^{l(t,s)} 2^(g_t - g_s) (q_t . k_s) v_s for the
-// loss sum(dO . o), restricted to pairs inside one 128-token tile (u): with S = Q Kᵀ,
-// E = dO Vᵀ and w_ts = lambda_t^{l(t,s)} 2^(g_t - g_s) [s <= t],
-//   dq = (w ⊙ E) K,  dk = (w ⊙ E)ᵀ Q,  dv = (w ⊙ S)ᵀ dO,
-//   dlambda_t^l = sum over s at level l of 2^(g_t - g_s) S_ts E_ts   (l = 0..7),
-//   C_s = sum_t w_ts S_ts E_ts (the column sums of the pair terms; with the row sums
-//   R_t = sum_l lambda_t^l dlambda_t^l they give d(log a) without the rounding of dv).
-// One CTA (256 threads, one per SM: 512 TMEM columns, 175 KB shared memory) per
-// (b, h, tile):
-//   S and E on the tensor cores from the bf16 inputs (TMEM columns 0..127, 128..255);
-//   role a (warps 0-3, thread = query row): dS = w ⊙ E and P = w ⊙ S as fp16 with
-//     power-of-two tile scales into shared memory (in the layout a TMA box of 64 columns
-//     has), dlambda from S ⊙ E in fp32;
-//   role b (warps 4-7): Q, K and dO to fp16 in place with power-of-two tile scales;
-//   dq = dS K (columns 256..383), dk = dSᵀ Q (384..511) and dv = Pᵀ dO (0..63) on the
-//   tensor cores; dq rows are read by role a, dk and dv rows (keys) by role b, and all
-//   three are written to the fp32 per-head gradient buffers (assigned, not added).
-// The pairs across tiles are the inter-tile part of the backward.
-// ---------------------------------------------------------------------------------
-struct TcBwdParams {
-  int B, T, H, hpg, G, L, NT;
-  const float* a;
-  const float* lam;
-  float* dq32;   // (B, T, H, d_k) fp32, per head
-  float* dk32;   // (B, T, H, d_k)
-  float* dv32;   // (B, T, H, d_v)
-  float* dlam;   // (B, T, H, L): levels 0..7 written, the rest zeroed
-  float* cu;     // (B, T, H): C_s = sum_t A_ts over the in-tile pairs (fp32, from S and E)
-  unsigned* status;
-};
-
-// Warp reduce-scatter of 32 columns: on return lane j holds the sum over the warp's lanes
-// of v[j] (31 shuffles).
-__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int k = 16; k >= 1; k >>= 1) {
-    const bool up = (lane & k) != 0;
-#pragma unroll
-    for (int i = 0; i < k; ++i) {
-      const float send = up ? v[i] : v[i + k];
-      const float keep = up ? v[i + k] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
-    }
-  }
-  return v[0];
-}
-
-constexpr int kBwdFixed = 163840;  // Q, K, V, dO, dS, P in front of the small tables
-constexpr int kSmemBwd = kBwdFixed + 3 * 128 * 4 + 2 * 128 * 9 * 4 + 1024;
-
-// Shared-memory address of the 16-byte chunk holding keys 8c..8c+7 (c = 0..15) of row r of
-// a 128 x 128 fp16 tile stored as two 64-column boxes with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t tile_chunk(int r, int c) {
-  return (uint32_t)((c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
-
-__global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap mapQ,
-                                                              const __grid_constant__ CUtensorMap mapK,
-                                                              const __grid_constant__ CUtensorMap mapV,
-                                                              const __grid_constant__ CUtensorMap mapD,
-                                                              TcBwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* RQ = smem;            // 32 KB: Q (bf16, then fp16)
-  uint8_t* RK = smem + 32768;    // 32 KB: K (bf16, then fp16)
-  uint8_t* RV = smem + 65536;    // 16 KB: V (bf16)
-  uint8_t* RD = smem + 81920;    // 16 KB: dO (bf16, then fp16)
-  uint8_t* RS = smem + 98304;    // 32 KB: dS (fp16)
-  uint8_t* RP = smem + 131072;   // 32 KB: P (fp16)
-  float* sG = reinterpret_cast<float*>(smem + kBwdFixed);  // 128: g
-  float* sB8 = sG + 128;                                    // 128: 2^(g_end8(s) - g_s)
-  float* sLam8 = sB8 + 128;                                 // 128 x 9: lambda levels 0..7 of row r
-  float* sAcc = sLam8 + 128 * 9;                            // 128 x 9: dlambda of the diagonal group
-  float* sCol = sAcc + 128 * 9;                             // 128: column sums C_s
-  __shared__ __align__(8) uint64_t bar_ld, bar_se, bar_mm;
-  __shared__ uint32_t tmem_base;
-  __shared__ float s_red[8];
-  __shared__ float s_mx[8][3];
-  __shared__ int s_sc[6];  // tile scale exponents: dS, P (role a); Q, K, dO (role b)
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r = tid & 127, quad = warp & 3, rot = r & 7;
-  const bool role_b = warp >= 4;
-  const int lin = blockIdx.x;
-  const int h = lin % p.H;
-  const int u = (lin / p.H) % p.NT;
-  const int b = lin / (p.H * p.NT);
-  const int g = h / p.hpg;
-  const long long t0 = (long long)u * kTile;
-  const size_t row = (size_t)b * p.T + t0 + r;  // token of this thread's row
-  const float* lrow = p.lam + (row * p.H + h) * p.L;
-
-  if (tid == 0) {
-    ptx::mbar_init(&bar_ld, 1);
-    ptx::mbar_init(&bar_se, 1);
-    ptx::mbar_init(&bar_mm, 1);
-    ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 * 2 + 16384 * 2);
-    ptx::tma_load_4d(RQ, &mapQ, &bar_ld, 0, g, (int)t0, b);
-    ptx::tma_load_4d(RQ + 16384, &mapQ, &bar_ld, 64, g, (int)t0, b);
-    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
-    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
-    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
-    ptx::tma_load_4d(RD, &mapD, &bar_ld, 0, h, (int)t0, b);
-  }
-  if (warp == 0) {
-    ptx::tmem_alloc(&tmem_base, 512);
-    ptx::tmem_relinquish();
-  }
-  if (!role_b) {
-#pragma unroll
-    for (int l = 0; l < kLevIntra; ++l) ptx::cp_async4(sLam8 + r * 9 + l, lrow + l);
-#pragma unroll
-    for (int l = 0; l < 9; ++l) sAcc[r * 9 + l] = 0.f;
-    sCol[r] = 0.f;
-  }
-  // chunk-local log2 decay cumsum over the 128 rows (both roles compute it)
-  float gt = log2f(p.a[row * p.H + h]);
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, gt, off);
-    if (lane >= off) gt += y;
-  }
-  if (lane == 31) s_red[warp] = gt;
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  for (int w = 0; w < quad; ++w) gt += s_red[w];
-  const uint32_t tbase = tmem_base;
-  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const uint32_t tS = tbase, tE = tbase + 128, tDQ = tbase + 256, tDK = tbase + 384, tDV = tbase;
-  if (!role_b) sG[r] = gt;
-  __syncthreads();
-  if (!role_b) sB8[r] = exp2f(sG[r | 7] - gt);
-  bool ok = wait_bar(&bar_ld, 0);
-  if (!ok) atomicExch(p.status, kStatusTimeout);
-  ok = __syncthreads_and(ok);
-
-  // S = Q Kᵀ (K = 128 d_k) and E = dO Vᵀ (K = 64 d_v), bf16, all K-major
-  if (ok && tid == 128) {
-    ptx::tc_fence_after();
-    const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 0);
-    const uint32_t q0 = ptx::smem_u32(RQ), k0 = ptx::smem_u32(RK);
-    const uint32_t d0 = ptx::smem_u32(RD), v0 = ptx::smem_u32(RV);
-#pragma unroll
-    for (int kk = 0; kk < kDk / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      ptx::umma_f16(tS, ptx::smem_desc_sw128(q0 + off, 16, 1024), ptx::smem_desc_sw128(k0 + off, 16, 1024),
-                    idesc, kk > 0);
-    }
-#pragma unroll
-    for (int kk = 0; kk < kDv / 16; ++kk)
-      ptx::umma_f16(tE, ptx::smem_desc_sw128(d0 + kk * 32, 16, 1024), ptx::smem_desc_sw128(v0 + kk * 32, 16, 1024),
-                    idesc, kk > 0);
-    ptx::umma_commit(&bar_se);
-  }
-  const bool se_issued = ok;
-  if (ok) {
-    ok = wait_bar(&bar_se, 0);
-    if (!ok) atomicExch(p.status, kStatusTimeout);
-  }
-  ok = __syncthreads_and(ok);  // also: S and E no longer read Q, K, V, dO
-
-  if (!role_b) {
-    // ---- role a: dS and P into shared memory, dlambda ------------------------------
-    const int t = r, tl = t & 31;
-    const float* lamr = sLam8 + r * 9;
-    float lmax = 0.f, smax = 0.f, emax = 0.f;
-    ptx::cp_async_wait_all();  // lambda of this row (issued by this thread)
-    if (ok) {
-      ptx::tc_fence_after();
-#pragma unroll
-      for (int l = 0; l < kLevIntra; ++l) lmax = fmaxf(lmax, fabsf(lamr[l]));
-#pragma unroll 1
-      for (int cg = 0; cg <= quad; ++cg) {
-        float sv[32], ev[32];
-        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
-        ptx::tmem_ld32(tE + lane_off + cg * 32, ev);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (cg < quad || j <= tl) {
-            smax = fmaxf(smax, fabsf(sv[j]));
-            emax = fmaxf(emax, fabsf(ev[j]));
-          }
-      }
-    }
-    // tile maxima of |P| <= max|S| max lambda and |dS| <= max|E| max lambda (decays <= 1)
-    float mp = smax * lmax, ms = emax * lmax;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, off));
-      ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, off));
-    }
-    if (lane == 0) {
-      s_mx[warp][0] = ms;
-      s_mx[warp][1] = mp;
-    }
-    ptx::named_bar_sync(1, 128);
-    const int es = f16_exp(fmaxf(fmaxf(s_mx[0][0], s_mx[1][0]), fmaxf(s_mx[2][0], s_mx[3][0])));
-    const int ep = f16_exp(fmaxf(fmaxf(s_mx[0][1], s_mx[1][1]), fmaxf(s_mx[2][1], s_mx[3][1])));
-    if (tid == 0) {
-      s_sc[0] = es;
-      s_sc[1] = ep;
-    }
-    const float cs = pow2i(-es), cp = pow2i(-ep);
-    float acc6 = 0.f, acc7 = 0.f;
-    const float* gq = sG + quad * 32;
-    const float span8 = fmaxf(fmaxf(gq[0] - gq[7], gq[8] - gq[15]), fmaxf(gq[16] - gq[23], gq[24] - gq[31]));
-    const bool fastd = span8 <= 60.f;
-#pragma unroll 1
-    for (int cg = 0; cg < 4; ++cg) {
-      uint32_t pd[16], pp[16];
-      if (ok && cg < quad) {
-        // keys of an earlier 32-group: one level (6 or 7) and the factored decay
-        float sv[32], ev[32];
-        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
-        ptx::tmem_ld32(tE + lane_off + cg * 32, ev);
-        ptx::tmem_ld_wait();
-        const bool l7 = (quad ^ cg) >= 2;
-        const float lv = lamr[l7 ? 7 : 6];
-        float ak[4];
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb) ak[kb] = exp2f(gt - sG[cg * 32 + kb * 8 + 7]);
-        const float4* b4 = reinterpret_cast<const float4*>(sB8 + cg * 32);
-        float xs = 0.f;
-        float colv[32];
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 bb = b4[j4];
-          const float bj[4] = {bb.x, bb.y, bb.z, bb.w};
-          float vs[4], vp[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 4 * j4 + e;
-            const float dd = ak[j4 >> 1] * bj[e];
-            const float xj = dd * (sv[j] * ev[j]);
-            xs += xj;
-            colv[j] = lv * xj;
-            const float w = lv * dd;
-            vs[e] = (w * cs) * ev[j];
-            vp[e] = (w * cp) * sv[j];
-          }
-          pd[2 * j4] = pack_h2(vs[0], vs[1]);
-          pd[2 * j4 + 1] = pack_h2(vs[2], vs[3]);
-          pp[2 * j4] = pack_h2(vp[0], vp[1]);
-          pp[2 * j4 + 1] = pack_h2(vp[2], vp[3]);
-        }
-        if (l7) acc7 += xs;
-        else acc6 += xs;
-        atomicAdd(sCol + cg * 32 + lane, warp_colsum32(colv, lane));
-      } else if (ok && cg == quad) {
-        // the diagonal 32-group: levels 0..5 (level of key j: bit length of tl ^ j)
-        float sv[32], ev[32];
-        ptx::tmem_ld32(tS + lane_off + cg * 32, sv);
-        ptx::tmem_ld32(tE + lane_off + cg * 32, ev);
-        ptx::tmem_ld_wait();
-        float ak[4];
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb) ak[kb] = exp2f(gt - gq[kb * 8 + 7]);
-        const float4* b4 = reinterpret_cast<const float4*>(sB8 + cg * 32);
-        float* accr = sAcc + r * 9;
-        float colv[32];
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 bb = b4[j4];
-          const float bj[4] = {bb.x, bb.y, bb.z, bb.w};
-          float vs[4], vp[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 4 * j4 + e;
-            // blocks after t's may give ak = inf; their keys are masked by the select
-            const float dd = fastd ? ak[j >> 3] * bj[e] : exp2f(gt - gq[j]);
-            const int lvj = 32 - __clz(tl ^ j);
-            const bool on = j <= tl;
-            const float w = on ? lamr[lvj] * dd : 0.f;
-            vs[e] = (w * cs) * ev[j];
-            vp[e] = (w * cp) * sv[j];
-            const float xj = on ? dd * (sv[j] * ev[j]) : 0.f;
-            if (on) accr[lvj] += xj;
-            colv[j] = on ? lamr[lvj] * xj : 0.f;
-          }
-          pd[2 * j4] = pack_h2(vs[0], vs[1]);
-          pd[2 * j4 + 1] = pack_h2(vs[2], vs[3]);
-          pp[2 * j4] = pack_h2(vp[0], vp[1]);
-          pp[2 * j4 + 1] = pack_h2(vp[2], vp[3]);
-        }
-        atomicAdd(sCol + cg * 32 + lane, warp_colsum32(colv, lane));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) pd[j] = pp[j] = 0u;
-      }
-      // keys cg*32 .. cg*32+31 are chunks 4cg .. 4cg+3 of row r
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint32_t off = tile_chunk(r, 4 * cg + q4);
-        *reinterpret_cast<uint4*>(RS + off) = make_uint4(pd[4 * q4], pd[4 * q4 + 1], pd[4 * q4 + 2], pd[4 * q4 + 3]);
-        *reinterpret_cast<uint4*>(RP + off) = make_uint4(pp[4 * q4], pp[4 * q4 + 1], pp[4 * q4 + 2], pp[4 * q4 + 3]);
-      }
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::named_bar_sync(1, 128);  // column sums complete
-    if (ok) {
-      p.cu[row * p.H + h] = sCol[r];
-      float* dl = p.dlam + (row * p.H + h) * p.L;
-      const float* accr = sAcc + r * 9;
-#pragma unroll
-      for (int l = 0; l < 6; ++l) dl[l] = accr[l];
-      dl[6] = acc6 + accr[6];
-      dl[7] = acc7 + accr[7];
-      for (int l = kLevIntra; l < p.L; ++l) dl[l] = 0.f;  // inter-tile levels: added later
-    }
-  } else {
-    // ---- role b: Q, K, dO -> fp16 in place with tile scales ---------------------------
-    uint32_t mq = 0u, mk = 0u, md = 0u;
-    uint8_t* qr0 = RQ + r * 128;
-    uint8_t* kr0 = RK + r * 128;
-    uint8_t* dr0 = RD + r * 128;
-    if (ok) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int cc = (c ^ rot) << 4;
-        mq = absmax_u4(absmax_u4(mq, *reinterpret_cast<const uint4*>(qr0 + cc)),
-                       *reinterpret_cast<const uint4*>(qr0 + 16384 + cc));
-        mk = absmax_u4(absmax_u4(mk, *reinterpret_cast<const uint4*>(kr0 + cc)),
-                       *reinterpret_cast<const uint4*>(kr0 + 16384 + cc));
-        md = absmax_u4(md, *reinterpret_cast<const uint4*>(dr0 + cc));
-      }
-    }
-    float fq = bf16x2_maxhalf(mq), fk = bf16x2_maxhalf(mk), fd = bf16x2_maxhalf(md);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      fq = fmaxf(fq, __shfl_xor_sync(0xffffffffu, fq, off));
-      fk = fmaxf(fk, __shfl_xor_sync(0xffffffffu, fk, off));
-      fd = fmaxf(fd, __shfl_xor_sync(0xffffffffu, fd, off));
-    }
-    if (lane == 0) {
-      s_mx[warp][0] = fq;
-      s_mx[warp][1] = fk;
-      s_mx[warp][2] = fd;
-    }
-    ptx::named_bar_sync(2, 128);
-    int ex[3];
-#pragma unroll
-    for (int i = 0; i < 3; ++i)
-      ex[i] = f16_exp(fmaxf(fmaxf(s_mx[4][i], s_mx[5][i]), fmaxf(s_mx[6][i], s_mx[7][i])));
-    if (tid == 128) {
-      s_sc[2] = ex[0];
-      s_sc[3] = ex[1];
-      s_sc[4] = ex[2];
-    }
-    if (ok) {
-      const float sq = pow2i(-ex[0]), sk = pow2i(-ex[1]), sd = pow2i(-ex[2]);
-      const __nv_bfloat162 q2 = __floats2bfloat162_rn(sq, sq), k2 = __floats2bfloat162_rn(sk, sk),
-                           d2 = __floats2bfloat162_rn(sd, sd);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int cc = (c ^ rot) << 4;
-        uint4* a0 = reinterpret_cast<uint4*>(qr0 + cc);
-        uint4* a1 = reinterpret_cast<uint4*>(qr0 + 16384 + cc);
-        uint4* b0 = reinterpret_cast<uint4*>(kr0 + cc);
-        uint4* b1 = reinterpret_cast<uint4*>(kr0 + 16384 + cc);
-        uint4* d0 = reinterpret_cast<uint4*>(dr0 + cc);
-        *a0 = bf16x8_to_f16x8(*a0, q2);
-        *a1 = bf16x8_to_f16x8(*a1, q2);
-        *b0 = bf16x8_to_f16x8(*b0, k2);
-        *b1 = bf16x8_to_f16x8(*b1, k2);
-        *d0 = bf16x8_to_f16x8(*d0, d2);
-      }
-      ptx::fence_proxy_async_smem();
-    }
-  }
-  ptx::tc_fence_before();
-  ok = __syncthreads_and(ok);  // dS, P, fp16 Q, K, dO and the scales complete; S, E read
-
-  // dq = dS K (keys), dk = dSᵀ Q and dv = Pᵀ dO (queries); fp16
-  if (ok && tid == 128) {
-    ptx::tc_fence_after();
-    const uint32_t s0 = ptx::smem_u32(RS), p0 = ptx::smem_u32(RP), q0 = ptx::smem_u32(RQ),
-                   k0 = ptx::smem_u32(RK), d0 = ptx::smem_u32(RD);
-    const uint32_t id_q = ptx::idesc_f16_f32(128, 128, 0, 1);
-    const uint32_t id_k = ptx::idesc_f16_f32(128, 128, 1, 1);
-    const uint32_t id_v = ptx::idesc_f16_f32(128, 64, 1, 1);
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk) {
-      const uint32_t offk = (kk >> 2) * 16384 + (kk & 3) * 32;  // K-major step over keys
-      ptx::umma_f16(tDQ, ptx::smem_desc_sw128(s0 + offk, 16, 1024), ptx::smem_desc_sw128(k0 + kk * 2048, 16384, 1024),
-                    id_q, kk > 0);
-      ptx::umma_f16(tDK, ptx::smem_desc_sw128(s0 + kk * 2048, 16384, 1024),
-                    ptx::smem_desc_sw128(q0 + kk * 2048, 16384, 1024), id_k, kk > 0);
-      ptx::umma_f16(tDV, ptx::smem_desc_sw128(p0 + kk * 2048, 16384, 1024),
-                    ptx::smem_desc_sw128(d0 + kk * 2048, 1024, 1024), id_v, kk > 0);
-    }
-    ptx::umma_commit(&bar_mm);
-  }
-  const bool mm_issued = ok;
-  if (ok) {
-    ok = wait_bar(&bar_mm, 0);
-    if (!ok) atomicExch(p.status, kStatusTimeout);
-  }
-  ok = __all_sync(0xffffffffu, ok);
-  if (ok) {
-    ptx::tc_fence_after();
-    if (!role_b) {
-      const float sc = pow2s(s_sc[0] + s_sc[3]);  // dS and K
-      float* dst = p.dq32 + (row * p.H + h) * kDk;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kDk; c0 += 32) {
-        float y[32];
-        ptx::tmem_ld32(tDQ + lane_off + c0, y);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(sc * y[j], sc * y[j + 1], sc * y[j + 2], sc * y[j + 3]);
-      }
-    } else {
-      const float sk = pow2s(s_sc[0] + s_sc[2]);  // dS and Q
-      const float sv = pow2s(s_sc[1] + s_sc[4]);  // P and dO
-      float* dk = p.dk32 + (row * p.H + h) * kDk;
-      float* dv = p.dv32 + (row * p.H + h) * kDv;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kDk + kDv; c0 += 32) {
-        const bool isk = c0 < kDk;
-        float y[32];
-        ptx::tmem_ld32((isk ? tDK + c0 : tDV + (c0 - kDk)) + lane_off, y);
-        ptx::tmem_ld_wait();
-        const float s = isk ? sk : sv;
-        float* d = isk ? dk + c0 : dv + (c0 - kDk);
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(d + j) = make_float4(s * y[j], s * y[j + 1], s * y[j + 2], s * y[j + 3]);
-      }
-    }
-  }
-  if (tid == 128) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
-    wait_bar(&bar_ld, 0);
-    if (se_issued) wait_bar(&bar_se, 0);
-    if (mm_issued) wait_bar(&bar_mm, 0);
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tbase, 512);
-}
-
-// ---------------------------------------------------------------------------------
-// tc_bwd_q: the query side of the inter-tile levels of the backward on the tensor cores.
-//
-// With the forward's tree over tiles (node images and scalars), tile u reads for every set
-// bit m of u the node N = Node_m[(u >> m) - 1] with weight w_t = lambda_t^(8+m) 2^(g_t + D_m)
-// (o_t += w_t q_tᵀ N).  Its backward, per level:
-//   dq_t += w_t N dO_t                   Z = dO Nᵀ, added into registers with w_t;
-//   dlambda_t^(8+m) = 2^(g_t + D_m) q_tᵀ N dO_t    Y = Q N, dotted with dO_t;
-//   dual(N) += sum_t w_t q_t dO_tᵀ       Qᵀ diag(w) dO, added into the node's fp32 dual
-//                                        with vector atomics (the readers of a node are
-//                                        the 2^m tiles of the node after it).
-// One CTA (256 threads, two per SM) per (b, h, tile) with u > 0; levels nearest first,
-// node images two deep.  Q, dO fp16 with power-of-two tile scales, diag(w) dO fp16 with
-// a power-of-two scale per level.  Thread (row t, half hf) keeps d_k columns 64 hf ..
-// 64 hf + 63 of dq_t; half 0 does the dlambda dot; the dual rows (d_k index = TMEM lane)
-// are split by d_v halves.  dq is added to the per-head fp32 buffer (the in-tile part
-// wrote it); dlambda levels >= 8 are assigned (the in-tile kernel zeroed them).
-// ---------------------------------------------------------------------------------
-struct TcBwdQParams {
-  int B, T, H, hpg, G, L, NT, nnodes;
-  int node_off[32];
-  int dual_off[32];   // first dual slot of the even nodes of tile level m
-  int nslots;         // dual slots per (b, h)
-  const float* a;
-  const float* lam;
-  const uint8_t* img;
-  const unsigned* meta;
-  float* dq32;
-  float* dlam;
-  float* dual;        // (B*H, nslots, d_k, d_v) fp32, zero on entry
-  unsigned* status;
-};
-
-constexpr int kBwdQFixed = 98304;  // Q, dO, two node images, diag(w) dO
-__host__ __device__ constexpr int bwdq_smem_bytes(int ninter) {
-  return kBwdQFixed + 512 * (ninter > 0 ? ninter : 1) + 1024;
-}
-
-__global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant__ CUtensorMap mapQ,
-                                                          const __grid_constant__ CUtensorMap mapD,
-                                                          TcBwdQParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* RQ = smem;             // 32 KB: Q (bf16, then fp16)
-  uint8_t* RD = smem + 32768;     // 16 KB: dO (bf16, then fp16)
-  uint8_t* RI = smem + 49152;     // 2 x 16 KB: node images
-  uint8_t* RB = smem + 81920;     // 16 KB: diag(w) dO of the current level (fp16)
-  float* sLamI = reinterpret_cast<float*>(smem + kBwdQFixed);  // [level index][row]
-  __shared__ __align__(8) uint64_t bar_ld, bar_y, bar_e[2], bar_yf;
-  __shared__ uint32_t tmem_base;
-  __shared__ float s_red[8];
-  __shared__ float s_mx[8][2];
-  __shared__ unsigned s_lmax[32];
-  __shared__ float sNode[32][2];  // per level index: scale exponent (bits), log2 decay
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r = tid & 127, hf = tid >> 7, quad = warp & 3, rot = r & 7;
-  const int lin = blockIdx.x;
-  const int h = lin % p.H;
-  const int u = (lin / p.H) % p.NT;
-  const int b = lin / (p.H * p.NT);
-  const int nlev = __popc((unsigned)u);
-  if (nlev == 0) return;  // the first tile reads no node
-  const int g = h / p.hpg;
-  const int bh = b * p.H + h;
-  const long long t0 = (long long)u * kTile;
-  const size_t nbase = (size_t)bh * p.nnodes;
-  const size_t row = (size_t)b * p.T + t0 + r;
-  const float* lrow = p.lam + (row * p.H + h) * p.L;
-  auto node_of = [&](int i) {
-    const int m = nth_set_bit((unsigned)u, i);
-    return nbase + p.node_off[m] + ((u >> m) - 1);
-  };
-
-  if (tid == 0) {
-    ptx::mbar_init(&bar_ld, 1);
-    ptx::mbar_init(&bar_y, 1);
-    ptx::mbar_init(&bar_e[0], 1);
-    ptx::mbar_init(&bar_e[1], 1);
-    ptx::mbar_init(&bar_yf, 256);
-    ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
-    ptx::tma_load_4d(RQ, &mapQ, &bar_ld, 0, g, (int)t0, b);
-    ptx::tma_load_4d(RQ + 16384, &mapQ, &bar_ld, 64, g, (int)t0, b);
-    ptx::tma_load_4d(RD, &mapD, &bar_ld, 0, h, (int)t0, b);
-    for (int i = 0; i < 2 && i < nlev; ++i) {
-      ptx::mbar_arrive_expect_tx(&bar_e[i], kImgBytes);
-      ptx::bulk_load(RI + i * kImgBytes, p.img + node_of(i) * kImgBytes, kImgBytes, &bar_e[i]);
-    }
-  }
-  if (warp == 0) {
-    ptx::tmem_alloc(&tmem_base, 256);
-    ptx::tmem_relinquish();
-  }
-  if (tid < 32) s_lmax[tid] = 0u;
-  if (hf == 0)
-    for (int i = 0; i < nlev; ++i) ptx::cp_async4(sLamI + i * 128 + r, lrow + kLevIntra + nth_set_bit((unsigned)u, i));
-  if (tid < nlev) {
-    const unsigned* mt = p.meta + node_of(tid) * kMeta;
-    sNode[tid][0] = __uint_as_float(mt[1]);
-    sNode[tid][1] = __uint_as_float(mt[2]);
-  }
-  // chunk-local log2 decay cumsum over the 128 rows (both halves compute it)
-  float gt = log2f(p.a[row * p.H + h]);
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, gt, off);
-    if (lane >= off) gt += y;
-  }
-  if (lane == 31) s_red[warp] = gt;
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  for (int w = 0; w < quad; ++w) gt += s_red[w];
-  const uint32_t tbase = tmem_base;
-  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const uint32_t tZ = tbase, tY = tbase + 128, tU = tbase + 192;
-  bool ok = wait_bar(&bar_ld, 0);
-  if (!ok) atomicExch(p.status, kStatusTimeout);
-  ok = __syncthreads_and(ok);
-
-  // Q (half hf converts box hf of row r) and dO (half 0) -> fp16 with tile scales
-  uint8_t* qrow = RQ + hf * 16384 + r * 128;
-  uint8_t* drow = RD + r * 128;
-  {
-    uint32_t mq = 0u, md = 0u;
-    if (ok) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        mq = absmax_u4(mq, *reinterpret_cast<const uint4*>(qrow + ((c ^ rot) << 4)));
-        if (hf == 0) md = absmax_u4(md, *reinterpret_cast<const uint4*>(drow + ((c ^ rot) << 4)));
-      }
-    }
-    float fq = bf16x2_maxhalf(mq), fd = bf16x2_maxhalf(md);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      fq = fmaxf(fq, __shfl_xor_sync(0xffffffffu, fq, off));
-      fd = fmaxf(fd, __shfl_xor_sync(0xffffffffu, fd, off));
-    }
-    if (lane == 0) {
-      s_mx[warp][0] = fq;
-      s_mx[warp][1] = fd;
-    }
-  }
-  ptx::cp_async_wait_all();
-  __syncthreads();  // maxima; lambda rows
-  float maxq = 0.f, maxd = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    maxq = fmaxf(maxq, s_mx[w][0]);
-    maxd = fmaxf(maxd, s_mx[w][1]);
-  }
-  const int eq = f16_exp(maxq), ed = f16_exp(maxd);
-  if (ok) {
-    const float sq = pow2i(-eq), sd = pow2i(-ed);
-    const __nv_bfloat162 q2 = __floats2bfloat162_rn(sq, sq), d2 = __floats2bfloat162_rn(sd, sd);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint4* x = reinterpret_cast<uint4*>(qrow + ((c ^ rot) << 4));
-      *x = bf16x8_to_f16x8(*x, q2);
-      if (hf == 0) {
-        uint4* y = reinterpret_cast<uint4*>(drow + ((c ^ rot) << 4));
-        *y = bf16x8_to_f16x8(*y, d2);
-      }
-    }
-    if (hf == 0)
-      for (int i = 0; i < nlev; ++i) atomicMax(&s_lmax[i], __float_as_uint(fabsf(sLamI[i * 128 + r])));
-  }
-  __syncthreads();  // fp16 Q, dO; lambda maxima
-  // level weights: w_t = lambda_t^(8+m) 2^(g_t + D) (D: the nearer levels' decay)
-  auto weight = [&](int i, float D) { return sLamI[i * 128 + r] * exp2f(gt + D); };
-  // diag(w) dO 2^-tau for level i: row r, d_v columns 32 hf .. 32 hf + 31 (chunks 4 hf ..)
-  auto write_b = [&](int i, float D, int tau) {
-    const float f = weight(i, D) * pow2s(ed - tau);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int cc = ((4 * hf + c) ^ rot) << 4;
-      const uint4 x = *reinterpret_cast<const uint4*>(drow + cc);
-      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-      uint32_t o4[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-        o4[e] = pack_h2(f * v.x, f * v.y);
-      }
-      *reinterpret_cast<uint4*>(RB + r * 128 + cc) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-    }
-  };
-  auto tau_of = [&](int i) { return f16_exp(__uint_as_float(s_lmax[i]) * maxd); };
-  float D = 0.f;
-  if (ok) write_b(0, 0.f, tau_of(0));
-  ptx::fence_proxy_async_smem();
-  ptx::tc_fence_before();
-  ok = __syncthreads_and(ok);
-
-  float acc[64];
-#pragma unroll
-  for (int j = 0; j < 64; ++j) acc[j] = 0.f;
-  int issued = nlev < 2 ? nlev : 2, consumed = 0, y_issued = 0;
-  const uint32_t id_z = ptx::idesc_f16_f32(128, 128, 0, 0);
-  const uint32_t id_y = ptx::idesc_f16_f32(128, 64, 0, 1);
-  const uint32_t id_u = ptx::idesc_f16_f32(128, 64, 1, 1);
-  for (int i = 0; ok && i < nlev; ++i) {
-    const int m = nth_set_bit((unsigned)u, i);
-    if (tid == 0) {
-      bool okd = i == 0 || wait_bar(&bar_yf, (i - 1) & 1);   // TMEM read, next diag(w) dO written
-      okd = okd && wait_bar(&bar_e[i & 1], (i >> 1) & 1);    // image landed
-      if (okd) {
-        ++consumed;
-        ptx::tc_fence_after();
-        const uint32_t im = ptx::smem_u32(RI + (i & 1) * kImgBytes);
-        const uint32_t q0 = ptx::smem_u32(RQ), d0 = ptx::smem_u32(RD), b0 = ptx::smem_u32(RB);
-#pragma unroll
-        for (int kk = 0; kk < kDv / 16; ++kk)  // Z = dO Nᵀ: K = d_v, B = image rows (d_k) K-major
-          ptx::umma_f16(tZ, ptx::smem_desc_sw128(d0 + kk * 32, 16, 1024), ptx::smem_desc_sw128(im + kk * 32, 16, 1024),
-                        id_z, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < kDk / 16; ++kk) {
-          const uint32_t offq = (kk >> 2) * 16384 + (kk & 3) * 32;
-          ptx::umma_f16(tY, ptx::smem_desc_sw128(q0 + offq, 16, 1024), ptx::smem_desc_sw128(im + kk * 2048, 1024, 1024),
-                        id_y, kk > 0);  // Y = Q N
-        }
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)  // Qᵀ diag(w) dO: M = d_k, K = tokens
-          ptx::umma_f16(tU, ptx::smem_desc_sw128(q0 + kk * 2048, 16384, 1024),
-                        ptx::smem_desc_sw128(b0 + kk * 2048, 1024, 1024), id_u, kk > 0);
-        ptx::umma_commit(&bar_y);
-        ++y_issued;
-      } else {
-        atomicExch(p.status, kStatusTimeout);
-      }
-    }
-    bool okw = wait_bar(&bar_y, i & 1);
-    if (!okw) atomicExch(p.status, kStatusTimeout);
-    okw = __syncthreads_and(okw);
-    if (!okw) {
-      ok = false;
-      break;
-    }
-    if (tid == 0 && i + 2 < nlev) {  // the image buffer of level i is free again
-      ptx::mbar_arrive_expect_tx(&bar_e[i & 1], kImgBytes);
-      ptx::bulk_load(RI + (i & 1) * kImgBytes, p.img + node_of(i + 2) * kImgBytes, kImgBytes, &bar_e[i & 1]);
-      ++issued;
-    }
-    ptx::tc_fence_after();
-    const int en = __float_as_int(sNode[i][0]);
-    const float wt = weight(i, D);
-    {  // dq: columns 64 hf .. 64 hf + 63 of Z, weighted
-      const float wz = wt * pow2s(ed + en);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float y[32];
-        ptx::tmem_ld32(tZ + lane_off + hf * 64 + half * 32, y);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[half * 32 + j] += wz * y[j];
-      }
-    }
-    if (hf == 0) {  // dlambda_t^(8+m) = 2^(g_t + D + eq + en + ed) sum_j Y_tj dO^_tj
-      float dot = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float y[32];
-        ptx::tmem_ld32(tY + lane_off + half * 32, y);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 x = *reinterpret_cast<const uint4*>(drow + (((4 * half + c) ^ rot) << 4));
-          const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-            dot += y[c * 8 + 2 * e] * v.x + y[c * 8 + 2 * e + 1] * v.y;
-          }
-        }
-      }
-      p.dlam[(row * p.H + h) * p.L + kLevIntra + m] = exp2f(gt + D) * pow2s(eq + en + ed) * dot;
-    }
-    {  // dual rows (TMEM lane = d_k index r), d_v columns 32 hf .. 32 hf + 31
-      const int tau = tau_of(i);
-      const float su = pow2s(eq + tau);
-      float y[32];
-      ptx::tmem_ld32(tU + lane_off + hf * 32, y);
-      ptx::tmem_ld_wait();
-      const int nd = (u >> m) - 1;  // even
-      float* dst = p.dual + (((size_t)bh * p.nslots + p.dual_off[m] + (nd >> 1)) * kDk + r) * kDv + hf * 32;
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        atomicAdd(reinterpret_cast<float4*>(dst + j), make_float4(su * y[j], su * y[j + 1], su * y[j + 2], su * y[j + 3]));
-    }
-    D += sNode[i][1];
-    if (i + 1 < nlev) {  // diag(w) dO of the next level (its MMA has read this one)
-      write_b(i + 1, D, tau_of(i + 1));
-      ptx::fence_proxy_async_smem();
-    }
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(&bar_yf);
-  }
-  if (ok) {
-    float* dst = p.dq32 + (row * p.H + h) * kDk + hf * 64;
-#pragma unroll
-    for (int j = 0; j < 64; j += 4) {
-      float4 o = *reinterpret_cast<float4*>(dst + j);
-      o.x += acc[j];
-      o.y += acc[j + 1];
-      o.z += acc[j + 2];
-      o.w += acc[j + 3];
-      *reinterpret_cast<float4*>(dst + j) = o;
-    }
-  }
-  if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
-    wait_bar(&bar_ld, 0);
-    for (int j = consumed; j < issued; ++j) wait_bar(&bar_e[j & 1], (j >> 1) & 1);
-    if (y_issued > 0) wait_bar(&bar_y, (y_issued - 1) & 1);
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tbase, 256);
-}
-
-// ---------------------------------------------------------------------------------
-// Key side of the inter-tile levels of the backward.
-//
-// tc_tile_prefix: per (b, h) the running sum P[c] of the tile decays gamma_0 .. gamma_{c-1}
-//   (the log2 decays of the level-0 nodes), in fp64, c = 0 .. NT.
-// tc_dual_publish: every dual slot as an fp16 image with a power-of-two scale (the node
-//   publication of the tree), for use as an MMA operand.
-// tc_bwd_kv: per key tile u and every tile level m whose node (m, i = u >> m) is read
-//   (i even, node (m, i + 1) inside the sequence), with c_m = 2^(P[(i+1) 2^m] - P[u+1])
-//   the decay of the tiles after u inside the node and r_s = 2^(gamma_u - g_s):
-//     dk_s += r_s sum_m c_m Dual_m v_s,   dv_s += r_s sum_m c_m Dual_mᵀ k_s,
-//   as Zk = V Dualᵀ and Zv = K Dual on the tensor cores (V, K fp16 with tile scales),
-//   added into registers per level (512 threads: four per key row, 32 d_k and 16 d_v
-//   columns each), then added to the per-head fp32 buffers.
-// ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) tc_tile_prefix_kernel(const unsigned* meta, int nnodes, int NT,
-                                                             double* P) {
-  __shared__ double s_part[8];
-  __shared__ double s_carry;
-  const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) s_carry = 0.0;
-  double* out = P + (size_t)bh * (NT + 1);
-  if (tid == 0) out[0] = 0.0;
-  __syncthreads();
-  for (int c0 = 0; c0 < NT; c0 += 256) {
-    const int c = c0 + tid;
-    double x = c < NT ? (double)__uint_as_float(meta[((size_t)bh * nnodes + c) * kMeta + 2]) : 0.0;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
-    }
-    if (lane == 31) s_part[warp] = x;
-    __syncthreads();
-    double add = s_carry;
-    for (int w = 0; w < warp; ++w) add += s_part[w];
-    x += add;
-    if (c < NT) out[c + 1] = x;
-    __syncthreads();
-    if (tid == 255) s_carry = x;
-    __syncthreads();
-  }
-}
-
-__global__ void __launch_bounds__(128) tc_dual_publish_kernel(const float* dual, uint8_t* img, unsigned* meta) {
-  __shared__ __align__(1024) uint8_t stage[kImgBytes];
-  __shared__ float2 s_red2[4];
-  const size_t slot = blockIdx.x;
-  const float* src = dual + (slot * kDk + threadIdx.x) * kDv;
-  float cur[kDv];
-#pragma unroll
-  for (int j = 0; j < kDv; j += 4) {
-    const float4 v = *reinterpret_cast<const float4*>(src + j);
-    cur[j] = v.x;
-    cur[j + 1] = v.y;
-    cur[j + 2] = v.z;
-    cur[j + 3] = v.w;
-  }
-  publish_node(cur, stage, slot, 0.f, s_red2, img, meta);
-}
-
-struct TcBwdKVParams {
-  int B, T, H, hpg, G, NT, MT;
-  int dual_off[32];
-  int nslots;
-  const float* a;
-  const uint8_t* dimg;    // dual images (B*H, nslots, 16 KB)
-  const unsigned* dmeta;  // (B*H, nslots, 4): scale exponent in [1]
-  const double* P;        // (B*H, NT + 1)
-  float* dk32;
-  float* dv32;
-  float* cu;    // (B, T, H): adds v_s . (the inter-tile part of dv_s)
-  unsigned* status;
-};
-
-constexpr int kSmemBwdKV = 32768 + 16384 + 2 * kImgBytes + 1024;
-
-__global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap mapK,
-                                                           const __grid_constant__ CUtensorMap mapV,
-                                                           TcBwdKVParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* RK = smem;           // 32 KB: K (bf16, then fp16)
-  uint8_t* RV = smem + 32768;   // 16 KB: V (bf16, then fp16)
-  uint8_t* RI = smem + 49152;   // 2 x 16 KB: dual images
-  __shared__ __align__(8) uint64_t bar_ld, bar_z, bar_e[2], bar_zf;
-  __shared__ uint32_t tmem_base;
-  __shared__ float s_red[16];
-  __shared__ float s_mx[16][2];
-  __shared__ int s_lv[32];
-  __shared__ int s_nl;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r = tid & 127, qq = tid >> 7, quad = warp & 3, rot = r & 7;
-  const int lin = blockIdx.x;
-  const int h = lin % p.H;
-  const int u = (lin / p.H) % p.NT;
-  const int b = lin / (p.H * p.NT);
-  const int g = h / p.hpg;
-  const int bh = b * p.H + h;
-  const long long t0 = (long long)u * kTile;
-  const size_t row = (size_t)b * p.T + t0 + r;
-  if (tid == 0) {  // tile levels whose node holding u is read by a later node
-    int n = 0;
-    for (int m = 0; m < p.MT; ++m) {
-      const int i = u >> m;
-      if (!(i & 1) && ((long long)(i + 1) << m) < p.NT) s_lv[n++] = m;
-    }
-    s_nl = n;
-  }
-  __syncthreads();
-  const int nl = s_nl;
-  if (nl == 0) return;  // no level reads this tile's nodes
-  auto slot_of = [&](int j) {
-    const int m = s_lv[j];
-    return (size_t)bh * p.nslots + p.dual_off[m] + ((u >> m) >> 1);
-  };
-  if (tid == 0) {
-    ptx::mbar_init(&bar_ld, 1);
-    ptx::mbar_init(&bar_z, 1);
-    ptx::mbar_init(&bar_e[0], 1);
-    ptx::mbar_init(&bar_e[1], 1);
-    ptx::mbar_init(&bar_zf, 512);
-    ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
-    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
-    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
-    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
-    for (int j = 0; j < 2 && j < nl; ++j) {
-      ptx::mbar_arrive_expect_tx(&bar_e[j], kImgBytes);
-      ptx::bulk_load(RI + j * kImgBytes, p.dimg + slot_of(j) * kImgBytes, kImgBytes, &bar_e[j]);
-    }
-  }
-  if (warp == 0) {
-    ptx::tmem_alloc(&tmem_base, 256);
-    ptx::tmem_relinquish();
-  }
-  // tile-local log2 decay cumsum (every quarter computes it for its rows)
-  float gt = log2f(p.a[row * p.H + h]);
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, gt, off);
-    if (lane >= off) gt += y;
-  }
-  if (lane == 31) s_red[warp] = gt;
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  for (int w = 0; w < quad; ++w) gt += s_red[w];
-  const float gam = s_red[0] + s_red[1] + s_red[2] + s_red[3];  // gamma_u
-  const uint32_t tbase = tmem_base;
-  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const uint32_t tZk = tbase, tZv = tbase + 128;
-  bool ok = wait_bar(&bar_ld, 0);
-  if (!ok) atomicExch(p.status, kStatusTimeout);
-  ok = __syncthreads_and(ok);
-  // K (quarters 0, 1: boxes 0, 1 of row r) and V (quarter 2) -> fp16 with tile scales
-  uint8_t* crow = qq < 2 ? RK + qq * 16384 + r * 128 : RV + r * 128;
-  {
-    uint32_t mx = 0u;
-    if (ok && qq < 3) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) mx = absmax_u4(mx, *reinterpret_cast<const uint4*>(crow + ((c ^ rot) << 4)));
-    }
-    float f = bf16x2_maxhalf(mx);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, off));
-    if (lane == 0) s_mx[warp][0] = f;
-  }
-  __syncthreads();
-  float mk = 0.f, mv = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) mk = fmaxf(mk, s_mx[w][0]);
-#pragma unroll
-  for (int w = 8; w < 12; ++w) mv = fmaxf(mv, s_mx[w][0]);
-  const int ek = f16_exp(mk), ev = f16_exp(mv);
-  if (ok && qq < 3) {
-    const float sc = pow2i(qq < 2 ? -ek : -ev);
-    const __nv_bfloat162 s2 = __floats2bfloat162_rn(sc, sc);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint4* x = reinterpret_cast<uint4*>(crow + ((c ^ rot) << 4));
-      *x = bf16x8_to_f16x8(*x, s2);
-    }
-    ptx::fence_proxy_async_smem();
-  }
-  ptx::tc_fence_before();
-  ok = __syncthreads_and(ok);
-
-  float ak[32], av[16];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) ak[j] = 0.f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) av[j] = 0.f;
-  const double* P = p.P + (size_t)bh * (p.NT + 1);
-  const uint32_t id_k = ptx::idesc_f16_f32(128, 128, 0, 0);
-  const uint32_t id_v = ptx::idesc_f16_f32(128, 64, 0, 1);
-  int issued = nl < 2 ? nl : 2, consumed = 0, z_issued = 0;
-  for (int j = 0; ok && j < nl; ++j) {
-    if (tid == 0) {
-      bool okd = j == 0 || wait_bar(&bar_zf, (j - 1) & 1);  // Z of the level before read
-      okd = okd && wait_bar(&bar_e[j & 1], (j >> 1) & 1);
-      if (okd) {
-        ++consumed;
-        ptx::tc_fence_after();
-        const uint32_t im = ptx::smem_u32(RI + (j & 1) * kImgBytes);
-        const uint32_t k0 = ptx::smem_u32(RK), v0 = ptx::smem_u32(RV);
-#pragma unroll
-        for (int kk = 0; kk < kDv / 16; ++kk)  // Zk = V Dualᵀ: K = d_v; the image rows (d_k) K-major
-          ptx::umma_f16(tZk, ptx::smem_desc_sw128(v0 + kk * 32, 16, 1024), ptx::smem_desc_sw128(im + kk * 32, 16, 1024),
-                        id_k, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < kDk / 16; ++kk) {  // Zv = K Dual: K = d_k; the image MN-major
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          ptx::umma_f16(tZv, ptx::smem_desc_sw128(k0 + off, 16, 1024), ptx::smem_desc_sw128(im + kk * 2048, 1024, 1024),
-                        id_v, kk > 0);
-        }
-        ptx::umma_commit(&bar_z);
-        ++z_issued;
-      } else {
-        atomicExch(p.status, kStatusTimeout);
-      }
-    }
-    bool okw = wait_bar(&bar_z, j & 1);
-    if (!okw) atomicExch(p.status, kStatusTimeout);
-    okw = __syncthreads_and(okw);
-    if (!okw) {
-      ok = false;
-      break;
-    }
-    if (tid == 0 && j + 2 < nl) {
-      ptx::mbar_arrive_expect_tx(&bar_e[j & 1], kImgBytes);
-      ptx::bulk_load(RI + (j & 1) * kImgBytes, p.dimg + slot_of(j + 2) * kImgBytes, kImgBytes, &bar_e[j & 1]);
-      ++issued;
-    }
-    ptx::tc_fence_after();
-    const int m = s_lv[j];
-    const int end = ((u >> m) + 1) << m;
-    const float cm = exp2f((float)(P[end] - P[u + 1]));
-    const int ed = (int)p.dmeta[slot_of(j) * kMeta + 1];
-    {
-      float y[32];
-      ptx::tmem_ld32(tZk + lane_off + qq * 32, y);
-      ptx::tmem_ld_wait();
-      const float w = cm * pow2s(ed + ev);
-#pragma unroll
-      for (int c = 0; c < 32; ++c) ak[c] += w * y[c];
-    }
-    {
-      float y[16];
-      ptx::tmem_ld16(tZv + lane_off + qq * 16, y);
-      ptx::tmem_ld_wait();
-      const float w = cm * pow2s(ed + ek);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) av[c] += w * y[c];
-    }
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(&bar_zf);
-  }
-  if (ok) {
-    const float rs = exp2f(gam - gt);
-    float* dk = p.dk32 + (row * p.H + h) * kDk + qq * 32;
-    float* dv = p.dv32 + (row * p.H + h) * kDv + qq * 16;
-#pragma unroll
-    for (int c = 0; c < 32; c += 4) {
-      float4 o = *reinterpret_cast<float4*>(dk + c);
-      o.x += rs * ak[c];
-      o.y += rs * ak[c + 1];
-      o.z += rs * ak[c + 2];
-      o.w += rs * ak[c + 3];
-      *reinterpret_cast<float4*>(dk + c) = o;
-    }
-#pragma unroll
-    for (int c = 0; c < 16; c += 4) {
-      float4 o = *reinterpret_cast<float4*>(dv + c);
-      o.x += rs * av[c];
-      o.y += rs * av[c + 1];
-      o.z += rs * av[c + 2];
-      o.w += rs * av[c + 3];
-      *reinterpret_cast<float4*>(dv + c) = o;
-    }
-    // v_s . (these d_v columns): V is fp16 in shared memory, 2^ev times the input
-    float cdot = 0.f;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint4 x = *reinterpret_cast<const uint4*>(RV + r * 128 + (((2 * qq + c) ^ rot) << 4));
-      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 vv = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-        cdot += vv.x * av[8 * c + 2 * e] + vv.y * av[8 * c + 2 * e + 1];
-      }
-    }
-    atomicAdd(p.cu + row * p.H + h, rs * pow2i(ev) * cdot);
-  }
-  if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
-    wait_bar(&bar_ld, 0);
-    for (int j = consumed; j < issued; ++j) wait_bar(&bar_e[j & 1], (j >> 1) & 1);
-    if (z_issued > 0) wait_bar(&bar_z, (z_issued - 1) & 1);
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tbase, 256);
-}
-
-// ---------------------------------------------------------------------------------
-// Gated DeltaNet values on the tensor cores, 128-token chunks (the delta rule's WY form,
-// as in gdn.cu: u = U_loc - W S per chunk, T = (I + diag(beta) A)^-1, A = (K Kᵀ) ⊙
-// 2^(g_t - g_s) strictly lower, U_loc = T diag(beta) V, W = T diag(beta 2^g) K).
-//
-// tc_gdn_local, one CTA per (b, h, chunk), 256 threads, one CTA per SM:
-//   K Kᵀ on tcgen05 from the bf16 keys (exact products, fp32 sums); A in fp32 in shared
-//   memory; T by 16-row blocks on the CUDA cores (diagonal blocks by substitution in
-//   registers, then T_ij = -T_ii sum_{j <= k < i} A_ik T_kj column block by column block);
-//   then [W | U_loc] = T [diag(beta 2^g) K | diag(beta) V] on tcgen05 with every operand
-//   split into an fp16 high part and the fp16 rounding remainder (hi hi + lo hi + hi lo,
-//   about 22 significant bits), each with a power-of-two tile scale.  Per chunk the
-//   workspace gets W split the same way (hi and lo fp16 in the MMA operand layout, with
-//   its scale exponent), U_loc (fp32) and g, for tc_gdn_pass.
-// ---------------------------------------------------------------------------------
-// Workspace per (b, h, chunk): W hi, W lo (fp16, 16 KB boxes of 64 d_k columns with the
-// 128-byte swizzle), U_loc (128 x d_v fp32), g (128 fp32), W's scale exponent.
-constexpr int kGdnOffU = 65536, kGdnOffG = 65536 + 32768, kGdnOffE = kGdnOffG + 512;
-constexpr size_t kGdnChunkBytes = 99328;
-
-struct TcGdnParams {
-  int B, T, H, hpg, G;
-  const float* a;
-  const float* beta;
-  uint8_t* xw;  // (B*H, T/128, kGdnChunkBytes)
-  void* u;      // (B, T, H, d_v) bf16: the transformed values (tc_gdn_pass)
-  unsigned* status;
-};
-
-constexpr int kGP = 132;  // padded fp32 row of the 128 x 128 matrices
-constexpr int kSmemGdnL = 32768 + 16384 + 2 * 128 * kGP * 4 + 8 * 256 * 4 + 4 * 128 * 4 + 1024;
-
-// fp32 value -> fp16 high part and fp16 remainder, both of x * 2^-e
-__device__ __forceinline__ void split_h(float x, float sc, __half& hi, __half& lo) {
-  const float y = x * sc;
-  hi = __float2half_rn(y);
-  lo = __float2half_rn(y - __half2float(hi));
-}
-
-__global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_constant__ CUtensorMap mapK,
-                                                              const __grid_constant__ CUtensorMap mapV,
-                                                              TcGdnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* RK = smem;                                          // 32 KB: K (bf16); later V hi, lo (fp16)
-  uint8_t* RV = smem + 32768;                                  // 16 KB: V (bf16)
-  float* Am = reinterpret_cast<float*>(smem + 49152);          // 128 x kGP: A; later T hi, lo (fp16)
-  float* Tm = Am + 128 * kGP;                                  // 128 x kGP: T; later Kd hi, lo (fp16)
-  float* Ym = Tm + 128 * kGP;                                  // 8 x (16 x 16): one per warp
-  float* gs = Ym + 8 * 256;                                    // 128: g
-  float* bs = gs + 128;                                        // 128: beta
-  float* fk = bs + 128;                                        // 128: beta 2^g
-  __shared__ __align__(8) uint64_t bar_ld, bar_a, bar_w;
-  __shared__ uint32_t tmem_base;
-  __shared__ float s_red[8];
-  __shared__ float s_mx[8][3];
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
-  const int r = tid & 127, rot = r & 7;
-  const int nch = p.T >> 7;
-  const int lin = blockIdx.x;
-  const int h = lin % p.H;
-  const int c = (lin / p.H) % nch;
-  const int b = lin / (p.H * nch);
-  const int g = h / p.hpg;
-  const long long t0 = (long long)c * kTile;
-  const size_t row = (size_t)b * p.T + t0 + r;
-  if (tid == 0) {
-    ptx::mbar_init(&bar_ld, 1);
-    ptx::mbar_init(&bar_a, 1);
-    ptx::mbar_init(&bar_w, 1);
-    ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
-    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
-    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
-    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
-  }
-  if (warp == 0) {
-    ptx::tmem_alloc(&tmem_base, 256);
-    ptx::tmem_relinquish();
-  }
-  // chunk-local log2 decay cumsum (both halves of the block compute it)
-  float gt = log2f(p.a[row * p.H + h]);
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, gt, off);
-    if (lane >= off) gt += y;
-  }
-  if (lane == 31) s_red[warp] = gt;
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  for (int w = 0; w < quad; ++w) gt += s_red[w];
-  const uint32_t tbase = tmem_base;
-  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const uint32_t tA = tbase, tW = tbase + 128, tU = tbase;
-  if (tid < 128) {
-    const float bt = p.beta[row * p.H + h];
-    gs[r] = gt;
-    bs[r] = bt;
-    fk[r] = bt * exp2f(gt);
-  }
-  bool ok = wait_bar(&bar_ld, 0);
-  if (!ok) atomicExch(p.status, kStatusTimeout);
-  ok = __syncthreads_and(ok);
-  if (ok && tid == 0) {  // K Kᵀ: M = N = 128 tokens, K = 128 d_k, bf16, both K-major
-    ptx::tc_fence_after();
-    const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 0);
-    const uint32_t k0 = ptx::smem_u32(RK);
-#pragma unroll
-    for (int kk = 0; kk < kDk / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      ptx::umma_f16(tA, ptx::smem_desc_sw128(k0 + off, 16, 1024), ptx::smem_desc_sw128(k0 + off, 16, 1024), idesc,
-                    kk > 0);
-    }
-    ptx::umma_commit(&bar_a);
-  }
-  const bool a_issued = ok;
-  if (ok) {
-    ok = wait_bar(&bar_a, 0);
-    if (!ok) atomicExch(p.status, kStatusTimeout);
-  }
-  ok = __syncthreads_and(ok);
-  // A_ts = beta_t 2^(g_t - g_s) (k_t . k_s), s < t (threads 0..127: row t); T zeroed above
-  if (ok) {
-    ptx::tc_fence_after();
-    if (tid < 128) {
-      const int t = r;
-      const float bt = bs[t];
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        float y[32];
-        ptx::tmem_ld32(tA + lane_off + c0, y);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float4 v;
-          float* vv = reinterpret_cast<float*>(&v);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int s2 = c0 + j + e;
-            vv[e] = s2 < t ? bt * exp2f(gt - gs[s2]) * y[j + e] : 0.f;
-          }
-          *reinterpret_cast<float4*>(Am + t * kGP + c0 + j) = v;
-        }
-      }
-    } else {
-      for (int e = r; e < 128 * kGP; e += 128) Tm[e] = 0.f;
-    }
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  // diagonal 16 x 16 blocks of T: thread (block, column j), substitution in registers
-  if (ok && tid < 128) {
-    const int r0 = tid & ~15, j = tid & 15;
-    float x[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      float acc = 0.f;
-#pragma unroll
-      for (int s2 = 0; s2 < t; ++s2) acc += Am[(r0 + t) * kGP + r0 + s2] * x[s2];
-      x[t] = t < j ? 0.f : (t == j ? 1.f : -acc);
-    }
-#pragma unroll
-    for (int t = 0; t < 16; ++t) Tm[(r0 + t) * kGP + r0 + j] = x[t];
-  }
-  __syncthreads();
-  // blocks below the diagonal, column block by column block (each needs only the diagonal
-  // blocks and its own earlier ones):
-  //   Y = sum_{jb <= k < ib} A_{ib,k} T_{k,jb},  T_{ib,jb} = -T_{ib,ib} Y,  ib = jb+1 .. 7.
-  // The work of column block jb falls with jb: blocks 0, 1, 2 go to warp pairs (rows
-  // split, a 64-thread barrier per step), blocks 3 + 6 and 4 + 5 to single warps.
-  if (ok) {
-    const bool pair = warp < 6;
-    const int njb = pair ? 1 : 2;
-    const int jb0 = pair ? (warp >> 1) : (warp == 6 ? 3 : 4);
-    float* Yw = Ym + (pair ? (warp >> 1) : warp - 3) * 256;
-    for (int q = 0; q < njb; ++q) {
-      const int jb = q == 0 ? jb0 : 9 - jb0;  // 3 then 6, 4 then 5
-      for (int ib = jb + 1; ib < 8; ++ib) {
-        if (pair) {  // rows 8 (warp & 1) + lane / 4, columns 4 (lane % 4) .. + 3
-          const int rr = (warp & 1) * 8 + (lane >> 2), c0 = (lane & 3) * 4;
-          float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
-          const float* arow = Am + (16 * ib + rr) * kGP;
-#pragma unroll 4
-          for (int s2 = 16 * jb; s2 < 16 * ib; ++s2) {
-            const float av = arow[s2];
-            const float4 tv = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0);
-            y0 += av * tv.x; y1 += av * tv.y; y2 += av * tv.z; y3 += av * tv.w;
-          }
-          *reinterpret_cast<float4*>(Yw + rr * 16 + c0) = make_float4(y0, y1, y2, y3);
-          ptx::named_bar_sync(1 + (warp >> 1), 64);
-          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-          const float* trow = Tm + (16 * ib + rr) * kGP + 16 * ib;
-#pragma unroll 4
-          for (int s2 = 0; s2 < 16; ++s2) {
-            const float tv = trow[s2];
-            const float4 yv = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0);
-            x0 += tv * yv.x; x1 += tv * yv.y; x2 += tv * yv.z; x3 += tv * yv.w;
-          }
-          *reinterpret_cast<float4*>(Tm + (16 * ib + rr) * kGP + 16 * jb + c0) = make_float4(-x0, -x1, -x2, -x3);
-          ptx::named_bar_sync(1 + (warp >> 1), 64);
-        } else {  // row lane / 2, columns 8 (lane % 2) .. + 7
-          const int rr = lane >> 1, c0 = (lane & 1) * 8;
-          float y[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = 0.f;
-          const float* arow = Am + (16 * ib + rr) * kGP;
-#pragma unroll 4
-          for (int s2 = 16 * jb; s2 < 16 * ib; ++s2) {
-            const float av = arow[s2];
-            const float4 t0v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0);
-            const float4 t1v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0 + 4);
-            y[0] += av * t0v.x; y[1] += av * t0v.y; y[2] += av * t0v.z; y[3] += av * t0v.w;
-            y[4] += av * t1v.x; y[5] += av * t1v.y; y[6] += av * t1v.z; y[7] += av * t1v.w;
-          }
-          *reinterpret_cast<float4*>(Yw + rr * 16 + c0) = make_float4(y[0], y[1], y[2], y[3]);
-          *reinterpret_cast<float4*>(Yw + rr * 16 + c0 + 4) = make_float4(y[4], y[5], y[6], y[7]);
-          __syncwarp();
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
-          const float* trow = Tm + (16 * ib + rr) * kGP + 16 * ib;
-#pragma unroll 4
-          for (int s2 = 0; s2 < 16; ++s2) {
-            const float tv = trow[s2];
-            const float4 y0 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0);
-            const float4 y1 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0 + 4);
-            x[0] += tv * y0.x; x[1] += tv * y0.y; x[2] += tv * y0.z; x[3] += tv * y0.w;
-            x[4] += tv * y1.x; x[5] += tv * y1.y; x[6] += tv * y1.z; x[7] += tv * y1.w;
-          }
-          float* dst = Tm + (16 * ib + rr) * kGP + 16 * jb + c0;
-          *reinterpret_cast<float4*>(dst) = make_float4(-x[0], -x[1], -x[2], -x[3]);
-          *reinterpret_cast<float4*>(dst + 4) = make_float4(-x[4], -x[5], -x[6], -x[7]);
-          __syncwarp();
-        }
-      }
-    }
-  }
-  __syncthreads();
-  // tile scales of T, diag(beta 2^g) K, diag(beta) V (maxima over their elements)
-  {
-    float mt = 0.f, mk = 0.f, mv = 0.f;
-    if (ok) {
-      // thread: T row r, half (tid >> 7) of its columns; K and V rows r (tid < 128)
-      const float* trow = Tm + r * kGP + (tid >> 7) * 64;
-      for (int j = 0; j < 64; ++j) mt = fmaxf(mt, fabsf(trow[j]));
-      if (tid < 128) {
-        uint32_t m0 = 0u, m1 = 0u;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const int off = r * 128 + ((cc ^ rot) << 4);
-          m0 = absmax_u4(absmax_u4(m0, *reinterpret_cast<const uint4*>(RK + off)),
-                         *reinterpret_cast<const uint4*>(RK + 16384 + off));
-          m1 = absmax_u4(m1, *reinterpret_cast<const uint4*>(RV + off));
-        }
-        mk = bf16x2_maxhalf(m0) * fabsf(fk[r]);
-        mv = bf16x2_maxhalf(m1) * fabsf(bs[r]);
-      }
-    }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-      mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
-      mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
-    }
-    if (lane == 0) {
-      s_mx[warp][0] = mt;
-      s_mx[warp][1] = mk;
-      s_mx[warp][2] = mv;
-    }
-  }
-  __syncthreads();
-  float mxs[3] = {0.f, 0.f, 0.f};
-#pragma unroll
-  for (int w = 0; w < 8; ++w)
-#pragma unroll
-    for (int i = 0; i < 3; ++i) mxs[i] = fmaxf(mxs[i], s_mx[w][i]);
-  const int et = f16_exp(mxs[0]), ek = f16_exp(mxs[1]), ev = f16_exp(mxs[2]);
-  // T -> fp16 hi, lo (A operands, K-major: row t, columns s in two 64-wide boxes) over A
-  uint8_t* THI = reinterpret_cast<uint8_t*>(Am);
-  uint8_t* TLO = THI + 32768;
-  if (ok) {
-    const float sc = pow2i(-et);
-    const int hf = tid >> 7;  // this thread's box (columns 64 hf .. 64 hf + 63) of row r
-#pragma unroll 1
-    for (int cc = 0; cc < 8; ++cc) {
-      const float* src = Tm + r * kGP + hf * 64 + cc * 8;
-      __half hi[8], lo[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) split_h(src[e], sc, hi[e], lo[e]);
-      const uint32_t off = hf * 16384 + r * 128 + ((cc ^ rot) << 4);
-      *reinterpret_cast<uint4*>(THI + off) = *reinterpret_cast<const uint4*>(hi);
-      *reinterpret_cast<uint4*>(TLO + off) = *reinterpret_cast<const uint4*>(lo);
-    }
-  }
-  __syncthreads();  // T read: its space takes diag(beta 2^g) K
-  // diag(beta 2^g) K -> fp16 hi, lo (B operands, MN-major: row s, d_k in two 64-wide boxes)
-  uint8_t* KHI = reinterpret_cast<uint8_t*>(Tm);
-  uint8_t* KLO = KHI + 32768;
-  if (ok) {
-    const float sc = fk[r] * pow2i(-ek);
-    const int hf = tid >> 7;
-#pragma unroll 1
-    for (int cc = 0; cc < 8; ++cc) {
-      const uint32_t off = hf * 16384 + r * 128 + ((cc ^ rot) << 4);
-      const uint4 x = *reinterpret_cast<const uint4*>(RK + off);
-      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-      __half hi[8], lo[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        split_h(__uint_as_float(w4[e] << 16), sc, hi[2 * e], lo[2 * e]);
-        split_h(__uint_as_float(w4[e] & 0xffff0000u), sc, hi[2 * e + 1], lo[2 * e + 1]);
-      }
-      *reinterpret_cast<uint4*>(KHI + off) = *reinterpret_cast<const uint4*>(hi);
-      *reinterpret_cast<uint4*>(KLO + off) = *reinterpret_cast<const uint4*>(lo);
-    }
-  }
-  __syncthreads();  // K read: its space takes diag(beta) V
-  uint8_t* VHI = RK;
-  uint8_t* VLO = RK + 16384;
-  if (ok && tid < 128) {
-    const float sc = bs[r] * pow2i(-ev);
-#pragma unroll 1
-    for (int cc = 0; cc < 8; ++cc) {
-      const uint32_t off = r * 128 + ((cc ^ rot) << 4);
-      const uint4 x = *reinterpret_cast<const uint4*>(RV + off);
-      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-      __half hi[8], lo[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        split_h(__uint_as_float(w4[e] << 16), sc, hi[2 * e], lo[2 * e]);
-        split_h(__uint_as_float(w4[e] & 0xffff0000u), sc, hi[2 * e + 1], lo[2 * e + 1]);
-      }
-      *reinterpret_cast<uint4*>(VHI + off) = *reinterpret_cast<const uint4*>(hi);
-      *reinterpret_cast<uint4*>(VLO + off) = *reinterpret_cast<const uint4*>(lo);
-    }
-  }
-  ptx::fence_proxy_async_smem();
-  ptx::tc_fence_before();
-  ok = __syncthreads_and(ok);
-  // W = T Kd and U = T Vd, each as hi hi + lo hi + hi lo (fp16, fp32 accumulation)
-  if (ok && tid == 0) {
-    ptx::tc_fence_after();
-    const uint32_t id_w = ptx::idesc_f16_f32(128, 128, 0, 1);
-    const uint32_t id_u = ptx::idesc_f16_f32(128, 64, 0, 1);
-    const uint32_t ta[3] = {ptx::smem_u32(THI), ptx::smem_u32(TLO), ptx::smem_u32(THI)};
-    const uint32_t kb[3] = {ptx::smem_u32(KHI), ptx::smem_u32(KHI), ptx::smem_u32(KLO)};
-    const uint32_t vb[3] = {ptx::smem_u32(VHI), ptx::smem_u32(VHI), ptx::smem_u32(VLO)};
-#pragma unroll
-    for (int pass = 0; pass < 3; ++pass)
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint64_t da = ptx::smem_desc_sw128(ta[pass] + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-        ptx::umma_f16(tW, da, ptx::smem_desc_sw128(kb[pass] + kk * 2048, 16384, 1024), id_w, pass > 0 || kk > 0);
-        ptx::umma_f16(tU, da, ptx::smem_desc_sw128(vb[pass] + kk * 2048, 1024, 1024), id_u, pass > 0 || kk > 0);
-      }
-    ptx::umma_commit(&bar_w);
-  }
-  const bool w_issued = ok;
-  if (ok) {
-    ok = wait_bar(&bar_w, 0);
-    if (!ok) atomicExch(p.status, kStatusTimeout);
-  }
-  ok = __all_sync(0xffffffffu, ok);
-  // W: its tile maximum, then hi and lo fp16 of W 2^-ew in the operand layout; U_loc, g
-  uint8_t* dst = p.xw + ((size_t)(b * p.H + h) * nch + c) * kGdnChunkBytes;
-  const float sw = pow2s(et + ek), su = pow2s(et + ev);
-  float mw = 0.f;
-  if (ok && tid < 128) {
-    ptx::tc_fence_after();
-#pragma unroll 1
-    for (int c0 = 0; c0 < kDk; c0 += 32) {
-      float y[32];
-      ptx::tmem_ld32(tW + lane_off + c0, y);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) mw = fmaxf(mw, fabsf(y[j]));
-    }
-  }
-#pragma unroll
-  for (int off = 16; off; off >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
-  if (lane == 0) s_red[warp] = mw;
-  __syncthreads();
-  const int ew = f16_exp(sw * fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
-  if (ok && tid < 128) {
-    const float sc = sw * pow2i(-ew);
-#pragma unroll 1
-    for (int c0 = 0; c0 < kDk; c0 += 32) {
-      float y[32];
-      ptx::tmem_ld32(tW + lane_off + c0, y);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {  // d_k columns c0 + 8 q4 .. + 7: one 16-byte chunk
-        const int col = c0 + 8 * q4, bx = col >> 6, cc = (col & 63) >> 3;
-        __half hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) split_h(y[8 * q4 + e], sc, hi[e], lo[e]);
-        const size_t off = (size_t)bx * 16384 + r * 128 + ((cc ^ rot) << 4);
-        *reinterpret_cast<uint4*>(dst + off) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(dst + 32768 + off) = *reinterpret_cast<const uint4*>(lo);
-      }
-    }
-    float* du = reinterpret_cast<float*>(dst + kGdnOffU);
-#pragma unroll 1
-    for (int c0 = 0; c0 < kDv; c0 += 32) {
-      float y[32];
-      ptx::tmem_ld32(tU + lane_off + c0, y);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(du + r * kDv + c0 + j) = make_float4(su * y[j], su * y[j + 1], su * y[j + 2], su * y[j + 3]);
-    }
-    reinterpret_cast<float*>(dst + kGdnOffG)[r] = gt;
-    if (r == 0) *reinterpret_cast<int*>(dst + kGdnOffE) = ew;
-  }
-  if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
-    wait_bar(&bar_ld, 0);
-    if (a_issued) wait_bar(&bar_a, 0);
-    if (w_issued) wait_bar(&bar_w, 0);
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tbase, 256);
-}
-
-// tc_gdn_pass, one CTA per (b, h), chunks in order, 256 threads, one CTA per SM.  The
-// state is kept in TMEM as Ŝ = S 2^-sigma (d_k rows as lanes, d_v columns).  Per chunk:
-//   Ŝ -> fp16 hi, lo with a tile scale (the B operand); Z = W S as hi hi + lo hi + hi lo;
-//   u = U_loc - Z, written in bf16; ũ = 2^(g_end - g) u -> fp16 hi, lo; K -> fp16;
-//   Ŝ <- Ŝ 2^(g_end + sigma - sigma') in TMEM, then Ŝ += Kᵀ (ũ hi + ũ lo) with
-//   sigma' = the scales of K and ũ.  W (hi and lo) is copied one chunk ahead, K by TMA
-//   behind the product W S.
-constexpr int kSmemGdnP = 2 * 65536 + 3 * 32768 + 1024;
-
-__global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_constant__ CUtensorMap mapK,
-                                                             TcGdnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* RWb = smem;           // 2 x 64 KB: W hi | W lo of a chunk
-  uint8_t* RS = smem + 131072;   // 32 KB: Ŝ hi | lo (B of W S: rows d_k, 64 d_v)
-  uint8_t* RU = smem + 163840;   // 32 KB: ũ hi | lo (B of Kᵀ ũ: rows tokens, 64 d_v)
-  uint8_t* RK = smem + 196608;   // 32 KB: K (bf16, then fp16; MN-major A of Kᵀ ũ)
-  __shared__ __align__(8) uint64_t bar_w[2], bar_k, bar_z, bar_su;
-  __shared__ uint32_t tmem_base;
-  __shared__ float s_mx[8][2];
-  __shared__ float sg[128];
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
-  const int r = tid & 127, hf = tid >> 7, rot = r & 7;
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H, g = h / p.hpg;
-  const int nch = p.T >> 7;
-  const uint8_t* xw = p.xw + (size_t)bh * nch * kGdnChunkBytes;
-  __nv_bfloat16* uo = static_cast<__nv_bfloat16*>(p.u);
-  if (tid == 0) {
-    ptx::mbar_init(&bar_w[0], 1);
-    ptx::mbar_init(&bar_w[1], 1);
-    ptx::mbar_init(&bar_k, 1);
-    ptx::mbar_init(&bar_z, 1);
-    ptx::mbar_init(&bar_su, 1);
-    ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(&bar_w[0], 65536);
-    ptx::bulk_load(RWb, xw, 65536, &bar_w[0]);
-    ptx::mbar_arrive_expect_tx(&bar_k, 32768);
-    ptx::tma_load_4d(RK, &mapK, &bar_k, 0, g, 0, b);
-    ptx::tma_load_4d(RK + 16384, &mapK, &bar_k, 64, g, 0, b);
-  }
-  if (warp == 0) {
-    ptx::tmem_alloc(&tmem_base, 128);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tbase = tmem_base;
-  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const uint32_t tS = tbase + hf * 32, tZ = tbase + 64 + hf * 32;  // this thread's 32 columns
-  {
-    uint32_t z[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) z[j] = 0u;
-    ptx::tmem_st16(tS + lane_off, z);
-    ptx::tmem_st16(tS + lane_off + 16, z);
-    ptx::tmem_st_wait();
-  }
-  int sigma = 0;
-  bool ok = true;
-  int w_issued = 1, w_done = 0, k_issued = 1, k_done = 0, mma_z = 0, z_done = 0, mma_s = 0, s_done = 0;
-  const uint32_t id_z = ptx::idesc_f16_f32(128, 64, 0, 1);
-  const uint32_t id_s = ptx::idesc_f16_f32(128, 64, 1, 1);
-  for (int c = 0; ok && c < nch; ++c) {
-    const uint8_t* xc = xw + (size_t)c * kGdnChunkBytes;
-    if (tid == 0 && c + 1 < nch) {  // W of the next chunk (its buffer's W S has completed)
-      ptx::mbar_arrive_expect_tx(&bar_w[(c + 1) & 1], 65536);
-      ptx::bulk_load(RWb + ((c + 1) & 1) * 65536, xc + kGdnChunkBytes, 65536, &bar_w[(c + 1) & 1]);
-      ++w_issued;
-    }
-    const int tokr = c * kTile + r;  // this thread's token (rows of u, Z)
-    // this thread's half of U_loc row r, and g
-    float uu[32];
-    {
-      const float4* us = reinterpret_cast<const float4*>(xc + kGdnOffU) + (r * kDv + hf * 32) / 4;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 v = us[j];
-        uu[4 * j] = v.x;
-        uu[4 * j + 1] = v.y;
-        uu[4 * j + 2] = v.z;
-        uu[4 * j + 3] = v.w;
-      }
-      if (tid < 128) sg[r] = reinterpret_cast<const float*>(xc + kGdnOffG)[r];
-    }
-    const int ew = *reinterpret_cast<const int*>(xc + kGdnOffE);
-    // Ŝ (lane r = d_k row) -> tile maximum
-    float sv[32];
-    ptx::tc_fence_after();
-    ptx::tmem_ld32(tS + lane_off, sv);
-    ptx::tmem_ld_wait();
-    float ms = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) ms = fmaxf(ms, fabsf(sv[j]));
-#pragma unroll
-    for (int off = 16; off; off >>= 1) ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, off));
-    if (lane == 0) s_mx[warp][0] = ms;
-    __syncthreads();
-    float mxs = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) mxs = fmaxf(mxs, s_mx[w][0]);
-    const int es = f16_exp(mxs);
-    {  // Ŝ 2^-es -> hi, lo: row r, d_v columns 32 hf .. (chunks 4 hf ..)
-      const float sc = pow2i(-es);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        __half hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) split_h(sv[8 * q4 + e], sc, hi[e], lo[e]);
-        const int off = r * 128 + (((4 * hf + q4) ^ rot) << 4);
-        *reinterpret_cast<uint4*>(RS + off) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(RS + 16384 + off) = *reinterpret_cast<const uint4*>(lo);
-      }
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {  // Z = W S (M = 128 tokens, N = 64, K = 128 d_k)
-      bool okw = wait_bar(&bar_w[c & 1], (c >> 1) & 1);
-      if (okw) {
-        ++w_done;
-        ptx::tc_fence_after();
-        const uint32_t w0 = ptx::smem_u32(RWb + (c & 1) * 65536), s0 = ptx::smem_u32(RS);
-        const uint32_t wa[3] = {w0, w0 + 32768, w0};
-        const uint32_t sb[3] = {s0, s0, s0 + 16384};
-#pragma unroll
-        for (int pass = 0; pass < 3; ++pass)
-#pragma unroll
-          for (int kk = 0; kk < kDk / 16; ++kk)
-            ptx::umma_f16(tbase + 64, ptx::smem_desc_sw128(wa[pass] + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                          ptx::smem_desc_sw128(sb[pass] + kk * 2048, 1024, 1024), id_z, pass > 0 || kk > 0);
-        ptx::umma_commit(&bar_z);
-        ++mma_z;
-      } else {
-        atomicExch(p.status, kStatusTimeout);
-      }
-    }
-    bool okz = wait_bar(&bar_z, c & 1);
-    if (!okz) atomicExch(p.status, kStatusTimeout);
-    okz = __syncthreads_and(okz);
-    if (okz) ++z_done;
-    if (!okz) {
-      ok = false;
-      break;
-    }
-    ptx::tc_fence_after();
-    // u = U_loc - Z (row r = token), written in bf16; ũ = 2^(g_end - g_r) u
-    const float gend = sg[127];
-    const float zs = pow2s(ew + sigma + es);
-    float z[32];
-    ptx::tmem_ld32(tZ + lane_off, z);
-    ptx::tmem_ld_wait();
-    const float fu = exp2f(gend - sg[r]);
-    float mu = 0.f;
-    {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        z[j] = uu[j] - zs * z[j];  // u
-        uu[j] = fu * z[j];         // ũ
-        mu = fmaxf(mu, fabsf(uu[j]));
-      }
-      uint32_t pk[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(z[2 * j], z[2 * j + 1]);
-      uint4* dst = reinterpret_cast<uint4*>(uo + (((size_t)b * p.T + tokr) * p.H + h) * kDv + hf * 32);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-    }
-    // K of this chunk (by TMA, behind W S): tile maximum
-    bool okk = true;
-    if (tid == 0) {
-      okk = wait_bar(&bar_k, c & 1);
-      if (okk) ++k_done;
-      else atomicExch(p.status, kStatusTimeout);
-    }
-    okk = __syncthreads_and(okk);
-    if (!okk) {
-      ok = false;
-      break;
-    }
-    uint8_t* krow = RK + hf * 16384 + r * 128;  // this thread's box of key row r
-    uint32_t mk = 0u;
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) mk = absmax_u4(mk, *reinterpret_cast<const uint4*>(krow + ((cc ^ rot) << 4)));
-    float fk = bf16x2_maxhalf(mk);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
-      fk = fmaxf(fk, __shfl_xor_sync(0xffffffffu, fk, off));
-    }
-    if (lane == 0) {
-      s_mx[warp][0] = mu;
-      s_mx[warp][1] = fk;
-    }
-    __syncthreads();
-    float mxu = 0.f, mxk = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      mxu = fmaxf(mxu, s_mx[w][0]);
-      mxk = fmaxf(mxk, s_mx[w][1]);
-    }
-    const int eu = f16_exp(mxu), ek = f16_exp(mxk);
-    {  // ũ 2^-eu -> hi, lo (row r = token, d_v columns 32 hf ..); K -> fp16 2^-ek in place
-      const float sc = pow2i(-eu);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        __half hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) split_h(uu[8 * q4 + e], sc, hi[e], lo[e]);
-        const int off = r * 128 + (((4 * hf + q4) ^ rot) << 4);
-        *reinterpret_cast<uint4*>(RU + off) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(RU + 16384 + off) = *reinterpret_cast<const uint4*>(lo);
-      }
-      const float sk = pow2i(-ek);
-      const __nv_bfloat162 k2 = __floats2bfloat162_rn(sk, sk);
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint4* x = reinterpret_cast<uint4*>(krow + ((cc ^ rot) << 4));
-        *x = bf16x8_to_f16x8(*x, k2);
-      }
-    }
-    // Ŝ <- Ŝ 2^(g_end + sigma - (ek + eu)) (the new scale of the state)
-    {
-      const float f = exp2f(gend + (float)(sigma - (ek + eu)));
-      uint32_t o[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(f * sv[j]);
-      ptx::tmem_st16(tS + lane_off, o);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(f * sv[16 + j]);
-      ptx::tmem_st16(tS + lane_off + 16, o);
-      ptx::tmem_st_wait();
-    }
-    sigma = ek + eu;
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {  // Ŝ += Kᵀ (ũ hi + ũ lo): M = 128 d_k, N = 64, K = 128 tokens
-      ptx::tc_fence_after();
-      const uint32_t k0 = ptx::smem_u32(RK), u0 = ptx::smem_u32(RU);
-#pragma unroll
-      for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          ptx::umma_f16(tbase, ptx::smem_desc_sw128(k0 + kk * 2048, 16384, 1024),
-                        ptx::smem_desc_sw128(u0 + pass * 16384 + kk * 2048, 1024, 1024), id_s, 1);
-      ptx::umma_commit(&bar_su);
-      ++mma_s;
-    }
-    bool oks = wait_bar(&bar_su, c & 1);
-    if (!oks) atomicExch(p.status, kStatusTimeout);
-    oks = __syncthreads_and(oks);
-    if (oks) ++s_done;
-    if (!oks) {
-      ok = false;
-      break;
-    }
-    if (tid == 0 && c + 1 < nch) {  // K of the next chunk (Kᵀ ũ has read this one)
-      ptx::mbar_arrive_expect_tx(&bar_k, 32768);
-      ptx::tma_load_4d(RK, &mapK, &bar_k, 0, g, (c + 1) * kTile, b);
-      ptx::tma_load_4d(RK + 16384, &mapK, &bar_k, 64, g, (c + 1) * kTile, b);
-      ++k_issued;
-    }
-  }
-  if (tid == 0) {  // bounded: let this CTA's outstanding copies and MMAs land before TMEM goes
-    for (int j = w_done; j < w_issued; ++j) wait_bar(&bar_w[j & 1], (j >> 1) & 1);
-    for (int j = k_done; j < k_issued; ++j) wait_bar(&bar_k, j & 1);
-    if (z_done < mma_z) wait_bar(&bar_z, (mma_z - 1) & 1);
-    if (s_done < mma_s) wait_bar(&bar_su, (mma_s - 1) & 1);
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tbase, 128);
-}
-
-// ---------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-// 4-D bf16 map over (inner, count, T, B) with a (64, 1, 128, 1) box, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int inner, int count, int T, int B) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)count, (cuuint64_t)T, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * count,
-                           (cuuint64_t)inner * 2 * count * T};
-  cuuint32_t box[4] = {64, 1, kTile, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int kSmemState = 32768 + 32768 + 1024;
 constexpr int kSmemTree = 4 * kImgBytes + 1024;
@@ -3081,129 +1113,10 @@ cudaError_t launch_tc_nodes(const TcPlan& tp, const FwdArgs& a, cudaStream_t st)
   return e;
 }
 
-cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, const float* a, const float* lam,
-                            const char* tree_ws, float* dq32, float* dlam, float* dual, const int* dual_off,
-                            int nslots, unsigned* status, cudaStream_t st) {
-  CUtensorMap mQ, mD;
-  if (!make_map(&mQ, q, kDk, tp.G, tp.T, tp.B) || !make_map(&mD, dO, kDv, tp.H, tp.T, tp.B))
-    return cudaErrorInvalidValue;
-  TcBwdQParams p{};
-  p.B = tp.B;
-  p.T = tp.T;
-  p.H = tp.H;
-  p.hpg = tp.hpg;
-  p.G = tp.G;
-  p.L = tp.L;
-  p.NT = tp.NT;
-  p.nnodes = tp.nnodes;
-  for (int m = 0; m < 32; ++m) {
-    p.node_off[m] = m < tp.MT ? tp.node_off[m] : 0;
-    p.dual_off[m] = m < tp.MT ? dual_off[m] : 0;
-  }
-  p.nslots = nslots;
-  p.a = a;
-  p.lam = lam;
-  p.img = reinterpret_cast<const uint8_t*>(tree_ws + tp.off_img);
-  p.meta = reinterpret_cast<const unsigned*>(tree_ws + tp.off_meta);
-  p.dq32 = dq32;
-  p.dlam = dlam;
-  p.dual = dual;
-  p.status = status;
-  const int smem = bwdq_smem_bytes(bit_length(tp.NT - 1));
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  tc_bwd_q_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 256, smem, st>>>(mQ, mD, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
-  return cudaSuccess;
-}
 
-cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, const float* a, const char* tree_ws,
-                             const float* dual, uint8_t* dimg, unsigned* dmeta, double* P, const int* dual_off,
-                             int nslots, float* dk32, float* dv32, float* cu, unsigned* status, cudaStream_t st) {
-  const unsigned BH = (unsigned)(tp.B * tp.H);
-  tc_tile_prefix_kernel<<<BH, 256, 0, st>>>(reinterpret_cast<const unsigned*>(tree_ws + tp.off_meta), tp.nnodes,
-                                            tp.NT, P);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  note_launch();
-  tc_dual_publish_kernel<<<(unsigned)((size_t)BH * nslots), 128, 0, st>>>(dual, dimg, dmeta);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
-  CUtensorMap mK, mV;
-  if (!make_map(&mK, k, kDk, tp.G, tp.T, tp.B) || !make_map(&mV, v, kDv, tp.H, tp.T, tp.B))
-    return cudaErrorInvalidValue;
-  TcBwdKVParams p{};
-  p.B = tp.B;
-  p.T = tp.T;
-  p.H = tp.H;
-  p.hpg = tp.hpg;
-  p.G = tp.G;
-  p.NT = tp.NT;
-  p.MT = tp.MT;
-  for (int m = 0; m < 32; ++m) p.dual_off[m] = m < tp.MT ? dual_off[m] : 0;
-  p.nslots = nslots;
-  p.a = a;
-  p.dimg = dimg;
-  p.dmeta = dmeta;
-  p.P = P;
-  p.dk32 = dk32;
-  p.dv32 = dv32;
-  p.cu = cu;
-  p.status = status;
-  if ((e = cudaFuncSetAttribute(tc_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwdKV)) !=
-      cudaSuccess)
-    return e;
-  tc_bwd_kv_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 512, kSmemBwdKV, st>>>(mK, mV, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
-  return cudaSuccess;
-}
 
-size_t tc_gdn_bytes(const ll_shape& s) {
-  return (size_t)s.batch * s.heads * (s.T / kTile) * kGdnChunkBytes;
-}
 
-cudaError_t launch_tc_gdn(const ll_shape& s, const void* k, const void* v, const float* a, const float* beta,
-                          void* u, char* ws, unsigned* status, cudaStream_t st) {
-  if (!tc_supported(s)) return cudaErrorInvalidValue;
-  const int G = s.heads / s.heads_per_group, nch = s.T / kTile;
-  CUtensorMap mK, mV;
-  if (!make_map(&mK, k, kDk, G, s.T, s.batch) || !make_map(&mV, v, kDv, s.heads, s.T, s.batch))
-    return cudaErrorInvalidValue;
-  TcGdnParams p{s.batch, s.T, s.heads, s.heads_per_group, G, a, beta, reinterpret_cast<uint8_t*>(ws), u, status};
-  cudaError_t e = cudaFuncSetAttribute(tc_gdn_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGdnL);
-  if (e != cudaSuccess) return e;
-  tc_gdn_local_kernel<<<(unsigned)((size_t)s.batch * s.heads * nch), 256, kSmemGdnL, st>>>(mK, mV, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
-  if ((e = cudaFuncSetAttribute(tc_gdn_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGdnP)) !=
-      cudaSuccess)
-    return e;
-  tc_gdn_pass_kernel<<<(unsigned)(s.batch * s.heads), 256, kSmemGdnP, st>>>(mK, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
-  return cudaSuccess;
-}
 
-cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k, const void* v, const void* dO,
-                                const float* a, const float* lam, float* dq32, float* dk32, float* dv32,
-                                float* dlam, float* cu, unsigned* status, cudaStream_t st) {
-  if (!tc_supported(s)) return cudaErrorInvalidValue;
-  const int G = s.heads / s.heads_per_group, NT = s.T / kTile;
-  CUtensorMap mQ, mK, mV, mD;
-  if (!make_map(&mQ, q, kDk, G, s.T, s.batch) || !make_map(&mK, k, kDk, G, s.T, s.batch) ||
-      !make_map(&mV, v, kDv, s.heads, s.T, s.batch) || !make_map(&mD, dO, kDv, s.heads, s.T, s.batch))
-    return cudaErrorInvalidValue;
-  const TcBwdParams p{s.batch, s.T, s.heads, s.heads_per_group, G, s.levels, NT, a, lam,
-                      dq32, dk32, dv32, dlam, cu, status};
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwd);
-  if (e != cudaSuccess) return e;
-  tc_bwd_intra_kernel<<<(unsigned)((size_t)s.batch * NT * s.heads), 256, kSmemBwd, st>>>(mQ, mK, mV, mD, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
-  return cudaSuccess;
-}
 
 cudaError_t launch_wait_selftest(unsigned* status, long long spins, cudaStream_t st) {
   wait_selftest_kernel<<<1, 32, 0, st>>>(status, spins);

@@ -1,0 +1,740 @@
+// Tensor-core kernels of the log-linear Gated DeltaNet values (for bf16, d_k = 128,
+// d_v = 64, T % 128 == 0), in 128-token chunks: tc_gdn_local and tc_gdn_pass.  The
+// delta rule's WY form they follow is set out in gdn.cu.
+#include "tc_common.cuh"
+
+namespace ll {
+
+namespace {
+
+// ---------------------------------------------------------------------------------
+// Gated DeltaNet values on the tensor cores, 128-token chunks (the delta rule's WY form,
+// as in gdn.cu: u = U_loc - W S per chunk, T = (I + diag(beta) A)^-1, A = (K Kᵀ) ⊙
+// 2^(g_t - g_s) strictly lower, U_loc = T diag(beta) V, W = T diag(beta 2^g) K).
+//
+// tc_gdn_local, one CTA per (b, h, chunk), 256 threads, one CTA per SM:
+//   K Kᵀ on tcgen05 from the bf16 keys (exact products, fp32 sums); A in fp32 in shared
+//   memory; T by 16-row blocks on the CUDA cores (diagonal blocks by substitution in
+//   registers, then T_ij = -T_ii sum_{j <= k < i} A_ik T_kj column block by column block);
+//   then [W | U_loc] = T [diag(beta 2^g) K | diag(beta) V] on tcgen05 with every operand
+//   split into an fp16 high part and the fp16 rounding remainder (hi hi + lo hi + hi lo,
+//   about 22 significant bits), each with a power-of-two tile scale.  Per chunk the
+//   workspace gets W split the same way (hi and lo fp16 in the MMA operand layout, with
+//   its scale exponent), U_loc (fp32) and g, for tc_gdn_pass.
+// ---------------------------------------------------------------------------------
+// Workspace per (b, h, chunk): W hi, W lo (fp16, 16 KB boxes of 64 d_k columns with the
+// 128-byte swizzle), U_loc (128 x d_v fp32), g (128 fp32), W's scale exponent.
+constexpr int kGdnOffU = 65536, kGdnOffG = 65536 + 32768, kGdnOffE = kGdnOffG + 512;
+constexpr size_t kGdnChunkBytes = 99328;
+
+struct TcGdnParams {
+  int B, T, H, hpg, G;
+  const float* a;
+  const float* beta;
+  uint8_t* xw;  // (B*H, T/128, kGdnChunkBytes)
+  void* u;      // (B, T, H, d_v) bf16: the transformed values (tc_gdn_pass)
+  unsigned* status;
+};
+
+constexpr int kGP = 132;  // padded fp32 row of the 128 x 128 matrices
+constexpr int kSmemGdnL = 32768 + 16384 + 2 * 128 * kGP * 4 + 8 * 256 * 4 + 4 * 128 * 4 + 1024;
+
+// fp32 value -> fp16 high part and fp16 remainder, both of x * 2^-e
+__device__ __forceinline__ void split_h(float x, float sc, __half& hi, __half& lo) {
+  const float y = x * sc;
+  hi = __float2half_rn(y);
+  lo = __float2half_rn(y - __half2float(hi));
+}
+
+__global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_constant__ CUtensorMap mapK,
+                                                              const __grid_constant__ CUtensorMap mapV,
+                                                              TcGdnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* RK = smem;                                          // 32 KB: K (bf16); later V hi, lo (fp16)
+  uint8_t* RV = smem + 32768;                                  // 16 KB: V (bf16)
+  float* Am = reinterpret_cast<float*>(smem + 49152);          // 128 x kGP: A; later T hi, lo (fp16)
+  float* Tm = Am + 128 * kGP;                                  // 128 x kGP: T; later Kd hi, lo (fp16)
+  float* Ym = Tm + 128 * kGP;                                  // 8 x (16 x 16): one per warp
+  float* gs = Ym + 8 * 256;                                    // 128: g
+  float* bs = gs + 128;                                        // 128: beta
+  float* fk = bs + 128;                                        // 128: beta 2^g
+  __shared__ __align__(8) uint64_t bar_ld, bar_a, bar_w;
+  __shared__ uint32_t tmem_base;
+  __shared__ float s_red[8];
+  __shared__ float s_mx[8][3];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
+  const int r = tid & 127, rot = r & 7;
+  const int nch = p.T >> 7;
+  const int lin = blockIdx.x;
+  const int h = lin % p.H;
+  const int c = (lin / p.H) % nch;
+  const int b = lin / (p.H * nch);
+  const int g = h / p.hpg;
+  const long long t0 = (long long)c * kTile;
+  const size_t row = (size_t)b * p.T + t0 + r;
+  if (tid == 0) {
+    ptx::mbar_init(&bar_ld, 1);
+    ptx::mbar_init(&bar_a, 1);
+    ptx::mbar_init(&bar_w, 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
+    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
+    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
+    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_base, 256);
+    ptx::tmem_relinquish();
+  }
+  // chunk-local log2 decay cumsum (both halves of the block compute it)
+  float gt = log2f(p.a[row * p.H + h]);
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, gt, off);
+    if (lane >= off) gt += y;
+  }
+  if (lane == 31) s_red[warp] = gt;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  for (int w = 0; w < quad; ++w) gt += s_red[w];
+  const uint32_t tbase = tmem_base;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const uint32_t tA = tbase, tW = tbase + 128, tU = tbase;
+  if (tid < 128) {
+    const float bt = p.beta[row * p.H + h];
+    gs[r] = gt;
+    bs[r] = bt;
+    fk[r] = bt * exp2f(gt);
+  }
+  bool ok = wait_bar(&bar_ld, 0);
+  if (!ok) atomicExch(p.status, kStatusTimeout);
+  ok = __syncthreads_and(ok);
+  if (ok && tid == 0) {  // K Kᵀ: M = N = 128 tokens, K = 128 d_k, bf16, both K-major
+    ptx::tc_fence_after();
+    const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 0);
+    const uint32_t k0 = ptx::smem_u32(RK);
+#pragma unroll
+    for (int kk = 0; kk < kDk / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+      ptx::umma_f16(tA, ptx::smem_desc_sw128(k0 + off, 16, 1024), ptx::smem_desc_sw128(k0 + off, 16, 1024), idesc,
+                    kk > 0);
+    }
+    ptx::umma_commit(&bar_a);
+  }
+  const bool a_issued = ok;
+  if (ok) {
+    ok = wait_bar(&bar_a, 0);
+    if (!ok) atomicExch(p.status, kStatusTimeout);
+  }
+  ok = __syncthreads_and(ok);
+  // A_ts = beta_t 2^(g_t - g_s) (k_t . k_s), s < t (threads 0..127: row t); T zeroed above
+  if (ok) {
+    ptx::tc_fence_after();
+    if (tid < 128) {
+      const int t = r;
+      const float bt = bs[t];
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float y[32];
+        ptx::tmem_ld32(tA + lane_off + c0, y);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          float4 v;
+          float* vv = reinterpret_cast<float*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s2 = c0 + j + e;
+            vv[e] = s2 < t ? bt * exp2f(gt - gs[s2]) * y[j + e] : 0.f;
+          }
+          *reinterpret_cast<float4*>(Am + t * kGP + c0 + j) = v;
+        }
+      }
+    } else {
+      for (int e = r; e < 128 * kGP; e += 128) Tm[e] = 0.f;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  // diagonal 16 x 16 blocks of T: thread (block, column j), substitution in registers
+  if (ok && tid < 128) {
+    const int r0 = tid & ~15, j = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      float acc = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < t; ++s2) acc += Am[(r0 + t) * kGP + r0 + s2] * x[s2];
+      x[t] = t < j ? 0.f : (t == j ? 1.f : -acc);
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) Tm[(r0 + t) * kGP + r0 + j] = x[t];
+  }
+  __syncthreads();
+  // blocks below the diagonal, column block by column block (each needs only the diagonal
+  // blocks and its own earlier ones):
+  //   Y = sum_{jb <= k < ib} A_{ib,k} T_{k,jb},  T_{ib,jb} = -T_{ib,ib} Y,  ib = jb+1 .. 7.
+  // The work of column block jb falls with jb: blocks 0, 1, 2 go to warp pairs (rows
+  // split, a 64-thread barrier per step), blocks 3 + 6 and 4 + 5 to single warps.
+  if (ok) {
+    const bool pair = warp < 6;
+    const int njb = pair ? 1 : 2;
+    const int jb0 = pair ? (warp >> 1) : (warp == 6 ? 3 : 4);
+    float* Yw = Ym + (pair ? (warp >> 1) : warp - 3) * 256;
+    for (int q = 0; q < njb; ++q) {
+      const int jb = q == 0 ? jb0 : 9 - jb0;  // 3 then 6, 4 then 5
+      for (int ib = jb + 1; ib < 8; ++ib) {
+        if (pair) {  // rows 8 (warp & 1) + lane / 4, columns 4 (lane % 4) .. + 3
+          const int rr = (warp & 1) * 8 + (lane >> 2), c0 = (lane & 3) * 4;
+          float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+          const float* arow = Am + (16 * ib + rr) * kGP;
+#pragma unroll 4
+          for (int s2 = 16 * jb; s2 < 16 * ib; ++s2) {
+            const float av = arow[s2];
+            const float4 tv = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0);
+            y0 += av * tv.x; y1 += av * tv.y; y2 += av * tv.z; y3 += av * tv.w;
+          }
+          *reinterpret_cast<float4*>(Yw + rr * 16 + c0) = make_float4(y0, y1, y2, y3);
+          ptx::named_bar_sync(1 + (warp >> 1), 64);
+          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+          const float* trow = Tm + (16 * ib + rr) * kGP + 16 * ib;
+#pragma unroll 4
+          for (int s2 = 0; s2 < 16; ++s2) {
+            const float tv = trow[s2];
+            const float4 yv = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0);
+            x0 += tv * yv.x; x1 += tv * yv.y; x2 += tv * yv.z; x3 += tv * yv.w;
+          }
+          *reinterpret_cast<float4*>(Tm + (16 * ib + rr) * kGP + 16 * jb + c0) = make_float4(-x0, -x1, -x2, -x3);
+          ptx::named_bar_sync(1 + (warp >> 1), 64);
+        } else {  // row lane / 2, columns 8 (lane % 2) .. + 7
+          const int rr = lane >> 1, c0 = (lane & 1) * 8;
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = 0.f;
+          const float* arow = Am + (16 * ib + rr) * kGP;
+#pragma unroll 4
+          for (int s2 = 16 * jb; s2 < 16 * ib; ++s2) {
+            const float av = arow[s2];
+            const float4 t0v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0);
+            const float4 t1v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0 + 4);
+            y[0] += av * t0v.x; y[1] += av * t0v.y; y[2] += av * t0v.z; y[3] += av * t0v.w;
+            y[4] += av * t1v.x; y[5] += av * t1v.y; y[6] += av * t1v.z; y[7] += av * t1v.w;
+          }
+          *reinterpret_cast<float4*>(Yw + rr * 16 + c0) = make_float4(y[0], y[1], y[2], y[3]);
+          *reinterpret_cast<float4*>(Yw + rr * 16 + c0 + 4) = make_float4(y[4], y[5], y[6], y[7]);
+          __syncwarp();
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+          const float* trow = Tm + (16 * ib + rr) * kGP + 16 * ib;
+#pragma unroll 4
+          for (int s2 = 0; s2 < 16; ++s2) {
+            const float tv = trow[s2];
+            const float4 y0 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0);
+            const float4 y1 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0 + 4);
+            x[0] += tv * y0.x; x[1] += tv * y0.y; x[2] += tv * y0.z; x[3] += tv * y0.w;
+            x[4] += tv * y1.x; x[5] += tv * y1.y; x[6] += tv * y1.z; x[7] += tv * y1.w;
+          }
+          float* dst = Tm + (16 * ib + rr) * kGP + 16 * jb + c0;
+          *reinterpret_cast<float4*>(dst) = make_float4(-x[0], -x[1], -x[2], -x[3]);
+          *reinterpret_cast<float4*>(dst + 4) = make_float4(-x[4], -x[5], -x[6], -x[7]);
+          __syncwarp();
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // tile scales of T, diag(beta 2^g) K, diag(beta) V (maxima over their elements)
+  {
+    float mt = 0.f, mk = 0.f, mv = 0.f;
+    if (ok) {
+      // thread: T row r, half (tid >> 7) of its columns; K and V rows r (tid < 128)
+      const float* trow = Tm + r * kGP + (tid >> 7) * 64;
+      for (int j = 0; j < 64; ++j) mt = fmaxf(mt, fabsf(trow[j]));
+      if (tid < 128) {
+        uint32_t m0 = 0u, m1 = 0u;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const int off = r * 128 + ((cc ^ rot) << 4);
+          m0 = absmax_u4(absmax_u4(m0, *reinterpret_cast<const uint4*>(RK + off)),
+                         *reinterpret_cast<const uint4*>(RK + 16384 + off));
+          m1 = absmax_u4(m1, *reinterpret_cast<const uint4*>(RV + off));
+        }
+        mk = bf16x2_maxhalf(m0) * fabsf(fk[r]);
+        mv = bf16x2_maxhalf(m1) * fabsf(bs[r]);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+      mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
+      mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+    }
+    if (lane == 0) {
+      s_mx[warp][0] = mt;
+      s_mx[warp][1] = mk;
+      s_mx[warp][2] = mv;
+    }
+  }
+  __syncthreads();
+  float mxs[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+  for (int w = 0; w < 8; ++w)
+#pragma unroll
+    for (int i = 0; i < 3; ++i) mxs[i] = fmaxf(mxs[i], s_mx[w][i]);
+  const int et = f16_exp(mxs[0]), ek = f16_exp(mxs[1]), ev = f16_exp(mxs[2]);
+  // T -> fp16 hi, lo (A operands, K-major: row t, columns s in two 64-wide boxes) over A
+  uint8_t* THI = reinterpret_cast<uint8_t*>(Am);
+  uint8_t* TLO = THI + 32768;
+  if (ok) {
+    const float sc = pow2i(-et);
+    const int hf = tid >> 7;  // this thread's box (columns 64 hf .. 64 hf + 63) of row r
+#pragma unroll 1
+    for (int cc = 0; cc < 8; ++cc) {
+      const float* src = Tm + r * kGP + hf * 64 + cc * 8;
+      __half hi[8], lo[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) split_h(src[e], sc, hi[e], lo[e]);
+      const uint32_t off = hf * 16384 + r * 128 + ((cc ^ rot) << 4);
+      *reinterpret_cast<uint4*>(THI + off) = *reinterpret_cast<const uint4*>(hi);
+      *reinterpret_cast<uint4*>(TLO + off) = *reinterpret_cast<const uint4*>(lo);
+    }
+  }
+  __syncthreads();  // T read: its space takes diag(beta 2^g) K
+  // diag(beta 2^g) K -> fp16 hi, lo (B operands, MN-major: row s, d_k in two 64-wide boxes)
+  uint8_t* KHI = reinterpret_cast<uint8_t*>(Tm);
+  uint8_t* KLO = KHI + 32768;
+  if (ok) {
+    const float sc = fk[r] * pow2i(-ek);
+    const int hf = tid >> 7;
+#pragma unroll 1
+    for (int cc = 0; cc < 8; ++cc) {
+      const uint32_t off = hf * 16384 + r * 128 + ((cc ^ rot) << 4);
+      const uint4 x = *reinterpret_cast<const uint4*>(RK + off);
+      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+      __half hi[8], lo[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        split_h(__uint_as_float(w4[e] << 16), sc, hi[2 * e], lo[2 * e]);
+        split_h(__uint_as_float(w4[e] & 0xffff0000u), sc, hi[2 * e + 1], lo[2 * e + 1]);
+      }
+      *reinterpret_cast<uint4*>(KHI + off) = *reinterpret_cast<const uint4*>(hi);
+      *reinterpret_cast<uint4*>(KLO + off) = *reinterpret_cast<const uint4*>(lo);
+    }
+  }
+  __syncthreads();  // K read: its space takes diag(beta) V
+  uint8_t* VHI = RK;
+  uint8_t* VLO = RK + 16384;
+  if (ok && tid < 128) {
+    const float sc = bs[r] * pow2i(-ev);
+#pragma unroll 1
+    for (int cc = 0; cc < 8; ++cc) {
+      const uint32_t off = r * 128 + ((cc ^ rot) << 4);
+      const uint4 x = *reinterpret_cast<const uint4*>(RV + off);
+      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+      __half hi[8], lo[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        split_h(__uint_as_float(w4[e] << 16), sc, hi[2 * e], lo[2 * e]);
+        split_h(__uint_as_float(w4[e] & 0xffff0000u), sc, hi[2 * e + 1], lo[2 * e + 1]);
+      }
+      *reinterpret_cast<uint4*>(VHI + off) = *reinterpret_cast<const uint4*>(hi);
+      *reinterpret_cast<uint4*>(VLO + off) = *reinterpret_cast<const uint4*>(lo);
+    }
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  ok = __syncthreads_and(ok);
+  // W = T Kd and U = T Vd, each as hi hi + lo hi + hi lo (fp16, fp32 accumulation)
+  if (ok && tid == 0) {
+    ptx::tc_fence_after();
+    const uint32_t id_w = ptx::idesc_f16_f32(128, 128, 0, 1);
+    const uint32_t id_u = ptx::idesc_f16_f32(128, 64, 0, 1);
+    const uint32_t ta[3] = {ptx::smem_u32(THI), ptx::smem_u32(TLO), ptx::smem_u32(THI)};
+    const uint32_t kb[3] = {ptx::smem_u32(KHI), ptx::smem_u32(KHI), ptx::smem_u32(KLO)};
+    const uint32_t vb[3] = {ptx::smem_u32(VHI), ptx::smem_u32(VHI), ptx::smem_u32(VLO)};
+#pragma unroll
+    for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const uint64_t da = ptx::smem_desc_sw128(ta[pass] + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+        ptx::umma_f16(tW, da, ptx::smem_desc_sw128(kb[pass] + kk * 2048, 16384, 1024), id_w, pass > 0 || kk > 0);
+        ptx::umma_f16(tU, da, ptx::smem_desc_sw128(vb[pass] + kk * 2048, 1024, 1024), id_u, pass > 0 || kk > 0);
+      }
+    ptx::umma_commit(&bar_w);
+  }
+  const bool w_issued = ok;
+  if (ok) {
+    ok = wait_bar(&bar_w, 0);
+    if (!ok) atomicExch(p.status, kStatusTimeout);
+  }
+  ok = __all_sync(0xffffffffu, ok);
+  // W: its tile maximum, then hi and lo fp16 of W 2^-ew in the operand layout; U_loc, g
+  uint8_t* dst = p.xw + ((size_t)(b * p.H + h) * nch + c) * kGdnChunkBytes;
+  const float sw = pow2s(et + ek), su = pow2s(et + ev);
+  float mw = 0.f;
+  if (ok && tid < 128) {
+    ptx::tc_fence_after();
+#pragma unroll 1
+    for (int c0 = 0; c0 < kDk; c0 += 32) {
+      float y[32];
+      ptx::tmem_ld32(tW + lane_off + c0, y);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mw = fmaxf(mw, fabsf(y[j]));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
+  if (lane == 0) s_red[warp] = mw;
+  __syncthreads();
+  const int ew = f16_exp(sw * fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
+  if (ok && tid < 128) {
+    const float sc = sw * pow2i(-ew);
+#pragma unroll 1
+    for (int c0 = 0; c0 < kDk; c0 += 32) {
+      float y[32];
+      ptx::tmem_ld32(tW + lane_off + c0, y);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {  // d_k columns c0 + 8 q4 .. + 7: one 16-byte chunk
+        const int col = c0 + 8 * q4, bx = col >> 6, cc = (col & 63) >> 3;
+        __half hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split_h(y[8 * q4 + e], sc, hi[e], lo[e]);
+        const size_t off = (size_t)bx * 16384 + r * 128 + ((cc ^ rot) << 4);
+        *reinterpret_cast<uint4*>(dst + off) = *reinterpret_cast<const uint4*>(hi);
+        *reinterpret_cast<uint4*>(dst + 32768 + off) = *reinterpret_cast<const uint4*>(lo);
+      }
+    }
+    float* du = reinterpret_cast<float*>(dst + kGdnOffU);
+#pragma unroll 1
+    for (int c0 = 0; c0 < kDv; c0 += 32) {
+      float y[32];
+      ptx::tmem_ld32(tU + lane_off + c0, y);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(du + r * kDv + c0 + j) = make_float4(su * y[j], su * y[j + 1], su * y[j + 2], su * y[j + 3]);
+    }
+    reinterpret_cast<float*>(dst + kGdnOffG)[r] = gt;
+    if (r == 0) *reinterpret_cast<int*>(dst + kGdnOffE) = ew;
+  }
+  if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
+    wait_bar(&bar_ld, 0);
+    if (a_issued) wait_bar(&bar_a, 0);
+    if (w_issued) wait_bar(&bar_w, 0);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tbase, 256);
+}
+
+// tc_gdn_pass, one CTA per (b, h), chunks in order, 256 threads, one CTA per SM.  The
+// state is kept in TMEM as Ŝ = S 2^-sigma (d_k rows as lanes, d_v columns).  Per chunk:
+//   Ŝ -> fp16 hi, lo with a tile scale (the B operand); Z = W S as hi hi + lo hi + hi lo;
+//   u = U_loc - Z, written in bf16; ũ = 2^(g_end - g) u -> fp16 hi, lo; K -> fp16;
+//   Ŝ <- Ŝ 2^(g_end + sigma - sigma') in TMEM, then Ŝ += Kᵀ (ũ hi + ũ lo) with
+//   sigma' = the scales of K and ũ.  W (hi and lo) is copied one chunk ahead, K by TMA
+//   behind the product W S.
+constexpr int kSmemGdnP = 2 * 65536 + 3 * 32768 + 1024;
+
+__global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_constant__ CUtensorMap mapK,
+                                                             TcGdnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* RWb = smem;           // 2 x 64 KB: W hi | W lo of a chunk
+  uint8_t* RS = smem + 131072;   // 32 KB: Ŝ hi | lo (B of W S: rows d_k, 64 d_v)
+  uint8_t* RU = smem + 163840;   // 32 KB: ũ hi | lo (B of Kᵀ ũ: rows tokens, 64 d_v)
+  uint8_t* RK = smem + 196608;   // 32 KB: K (bf16, then fp16; MN-major A of Kᵀ ũ)
+  __shared__ __align__(8) uint64_t bar_w[2], bar_k, bar_z, bar_su;
+  __shared__ uint32_t tmem_base;
+  __shared__ float s_mx[8][2];
+  __shared__ float sg[128];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
+  const int r = tid & 127, hf = tid >> 7, rot = r & 7;
+  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H, g = h / p.hpg;
+  const int nch = p.T >> 7;
+  const uint8_t* xw = p.xw + (size_t)bh * nch * kGdnChunkBytes;
+  __nv_bfloat16* uo = static_cast<__nv_bfloat16*>(p.u);
+  if (tid == 0) {
+    ptx::mbar_init(&bar_w[0], 1);
+    ptx::mbar_init(&bar_w[1], 1);
+    ptx::mbar_init(&bar_k, 1);
+    ptx::mbar_init(&bar_z, 1);
+    ptx::mbar_init(&bar_su, 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(&bar_w[0], 65536);
+    ptx::bulk_load(RWb, xw, 65536, &bar_w[0]);
+    ptx::mbar_arrive_expect_tx(&bar_k, 32768);
+    ptx::tma_load_4d(RK, &mapK, &bar_k, 0, g, 0, b);
+    ptx::tma_load_4d(RK + 16384, &mapK, &bar_k, 64, g, 0, b);
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_base, 128);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const uint32_t tS = tbase + hf * 32, tZ = tbase + 64 + hf * 32;  // this thread's 32 columns
+  {
+    uint32_t z[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) z[j] = 0u;
+    ptx::tmem_st16(tS + lane_off, z);
+    ptx::tmem_st16(tS + lane_off + 16, z);
+    ptx::tmem_st_wait();
+  }
+  int sigma = 0;
+  bool ok = true;
+  int w_issued = 1, w_done = 0, k_issued = 1, k_done = 0, mma_z = 0, z_done = 0, mma_s = 0, s_done = 0;
+  const uint32_t id_z = ptx::idesc_f16_f32(128, 64, 0, 1);
+  const uint32_t id_s = ptx::idesc_f16_f32(128, 64, 1, 1);
+  for (int c = 0; ok && c < nch; ++c) {
+    const uint8_t* xc = xw + (size_t)c * kGdnChunkBytes;
+    if (tid == 0 && c + 1 < nch) {  // W of the next chunk (its buffer's W S has completed)
+      ptx::mbar_arrive_expect_tx(&bar_w[(c + 1) & 1], 65536);
+      ptx::bulk_load(RWb + ((c + 1) & 1) * 65536, xc + kGdnChunkBytes, 65536, &bar_w[(c + 1) & 1]);
+      ++w_issued;
+    }
+    const int tokr = c * kTile + r;  // this thread's token (rows of u, Z)
+    // this thread's half of U_loc row r, and g
+    float uu[32];
+    {
+      const float4* us = reinterpret_cast<const float4*>(xc + kGdnOffU) + (r * kDv + hf * 32) / 4;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 v = us[j];
+        uu[4 * j] = v.x;
+        uu[4 * j + 1] = v.y;
+        uu[4 * j + 2] = v.z;
+        uu[4 * j + 3] = v.w;
+      }
+      if (tid < 128) sg[r] = reinterpret_cast<const float*>(xc + kGdnOffG)[r];
+    }
+    const int ew = *reinterpret_cast<const int*>(xc + kGdnOffE);
+    // Ŝ (lane r = d_k row) -> tile maximum
+    float sv[32];
+    ptx::tc_fence_after();
+    ptx::tmem_ld32(tS + lane_off, sv);
+    ptx::tmem_ld_wait();
+    float ms = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) ms = fmaxf(ms, fabsf(sv[j]));
+#pragma unroll
+    for (int off = 16; off; off >>= 1) ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, off));
+    if (lane == 0) s_mx[warp][0] = ms;
+    __syncthreads();
+    float mxs = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) mxs = fmaxf(mxs, s_mx[w][0]);
+    const int es = f16_exp(mxs);
+    {  // Ŝ 2^-es -> hi, lo: row r, d_v columns 32 hf .. (chunks 4 hf ..)
+      const float sc = pow2i(-es);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        __half hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split_h(sv[8 * q4 + e], sc, hi[e], lo[e]);
+        const int off = r * 128 + (((4 * hf + q4) ^ rot) << 4);
+        *reinterpret_cast<uint4*>(RS + off) = *reinterpret_cast<const uint4*>(hi);
+        *reinterpret_cast<uint4*>(RS + 16384 + off) = *reinterpret_cast<const uint4*>(lo);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // Z = W S (M = 128 tokens, N = 64, K = 128 d_k)
+      bool okw = wait_bar(&bar_w[c & 1], (c >> 1) & 1);
+      if (okw) {
+        ++w_done;
+        ptx::tc_fence_after();
+        const uint32_t w0 = ptx::smem_u32(RWb + (c & 1) * 65536), s0 = ptx::smem_u32(RS);
+        const uint32_t wa[3] = {w0, w0 + 32768, w0};
+        const uint32_t sb[3] = {s0, s0, s0 + 16384};
+#pragma unroll
+        for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+          for (int kk = 0; kk < kDk / 16; ++kk)
+            ptx::umma_f16(tbase + 64, ptx::smem_desc_sw128(wa[pass] + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                          ptx::smem_desc_sw128(sb[pass] + kk * 2048, 1024, 1024), id_z, pass > 0 || kk > 0);
+        ptx::umma_commit(&bar_z);
+        ++mma_z;
+      } else {
+        atomicExch(p.status, kStatusTimeout);
+      }
+    }
+    bool okz = wait_bar(&bar_z, c & 1);
+    if (!okz) atomicExch(p.status, kStatusTimeout);
+    okz = __syncthreads_and(okz);
+    if (okz) ++z_done;
+    if (!okz) {
+      ok = false;
+      break;
+    }
+    ptx::tc_fence_after();
+    // u = U_loc - Z (row r = token), written in bf16; ũ = 2^(g_end - g_r) u
+    const float gend = sg[127];
+    const float zs = pow2s(ew + sigma + es);
+    float z[32];
+    ptx::tmem_ld32(tZ + lane_off, z);
+    ptx::tmem_ld_wait();
+    const float fu = exp2f(gend - sg[r]);
+    float mu = 0.f;
+    {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        z[j] = uu[j] - zs * z[j];  // u
+        uu[j] = fu * z[j];         // ũ
+        mu = fmaxf(mu, fabsf(uu[j]));
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(z[2 * j], z[2 * j + 1]);
+      uint4* dst = reinterpret_cast<uint4*>(uo + (((size_t)b * p.T + tokr) * p.H + h) * kDv + hf * 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+    // K of this chunk (by TMA, behind W S): tile maximum
+    bool okk = true;
+    if (tid == 0) {
+      okk = wait_bar(&bar_k, c & 1);
+      if (okk) ++k_done;
+      else atomicExch(p.status, kStatusTimeout);
+    }
+    okk = __syncthreads_and(okk);
+    if (!okk) {
+      ok = false;
+      break;
+    }
+    uint8_t* krow = RK + hf * 16384 + r * 128;  // this thread's box of key row r
+    uint32_t mk = 0u;
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) mk = absmax_u4(mk, *reinterpret_cast<const uint4*>(krow + ((cc ^ rot) << 4)));
+    float fk = bf16x2_maxhalf(mk);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
+      fk = fmaxf(fk, __shfl_xor_sync(0xffffffffu, fk, off));
+    }
+    if (lane == 0) {
+      s_mx[warp][0] = mu;
+      s_mx[warp][1] = fk;
+    }
+    __syncthreads();
+    float mxu = 0.f, mxk = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      mxu = fmaxf(mxu, s_mx[w][0]);
+      mxk = fmaxf(mxk, s_mx[w][1]);
+    }
+    const int eu = f16_exp(mxu), ek = f16_exp(mxk);
+    {  // ũ 2^-eu -> hi, lo (row r = token, d_v columns 32 hf ..); K -> fp16 2^-ek in place
+      const float sc = pow2i(-eu);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        __half hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split_h(uu[8 * q4 + e], sc, hi[e], lo[e]);
+        const int off = r * 128 + (((4 * hf + q4) ^ rot) << 4);
+        *reinterpret_cast<uint4*>(RU + off) = *reinterpret_cast<const uint4*>(hi);
+        *reinterpret_cast<uint4*>(RU + 16384 + off) = *reinterpret_cast<const uint4*>(lo);
+      }
+      const float sk = pow2i(-ek);
+      const __nv_bfloat162 k2 = __floats2bfloat162_rn(sk, sk);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint4* x = reinterpret_cast<uint4*>(krow + ((cc ^ rot) << 4));
+        *x = bf16x8_to_f16x8(*x, k2);
+      }
+    }
+    // Ŝ <- Ŝ 2^(g_end + sigma - (ek + eu)) (the new scale of the state)
+    {
+      const float f = exp2f(gend + (float)(sigma - (ek + eu)));
+      uint32_t o[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(f * sv[j]);
+      ptx::tmem_st16(tS + lane_off, o);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(f * sv[16 + j]);
+      ptx::tmem_st16(tS + lane_off + 16, o);
+      ptx::tmem_st_wait();
+    }
+    sigma = ek + eu;
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // Ŝ += Kᵀ (ũ hi + ũ lo): M = 128 d_k, N = 64, K = 128 tokens
+      ptx::tc_fence_after();
+      const uint32_t k0 = ptx::smem_u32(RK), u0 = ptx::smem_u32(RU);
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          ptx::umma_f16(tbase, ptx::smem_desc_sw128(k0 + kk * 2048, 16384, 1024),
+                        ptx::smem_desc_sw128(u0 + pass * 16384 + kk * 2048, 1024, 1024), id_s, 1);
+      ptx::umma_commit(&bar_su);
+      ++mma_s;
+    }
+    bool oks = wait_bar(&bar_su, c & 1);
+    if (!oks) atomicExch(p.status, kStatusTimeout);
+    oks = __syncthreads_and(oks);
+    if (oks) ++s_done;
+    if (!oks) {
+      ok = false;
+      break;
+    }
+    if (tid == 0 && c + 1 < nch) {  // K of the next chunk (Kᵀ ũ has read this one)
+      ptx::mbar_arrive_expect_tx(&bar_k, 32768);
+      ptx::tma_load_4d(RK, &mapK, &bar_k, 0, g, (c + 1) * kTile, b);
+      ptx::tma_load_4d(RK + 16384, &mapK, &bar_k, 64, g, (c + 1) * kTile, b);
+      ++k_issued;
+    }
+  }
+  if (tid == 0) {  // bounded: let this CTA's outstanding copies and MMAs land before TMEM goes
+    for (int j = w_done; j < w_issued; ++j) wait_bar(&bar_w[j & 1], (j >> 1) & 1);
+    for (int j = k_done; j < k_issued; ++j) wait_bar(&bar_k, j & 1);
+    if (z_done < mma_z) wait_bar(&bar_z, (mma_z - 1) & 1);
+    if (s_done < mma_s) wait_bar(&bar_su, (mma_s - 1) & 1);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tbase, 128);
+}
+
+}  // namespace
+
+size_t tc_gdn_bytes(const ll_shape& s) {
+  return (size_t)s.batch * s.heads * (s.T / kTile) * kGdnChunkBytes;
+}
+
+cudaError_t launch_tc_gdn(const ll_shape& s, const void* k, const void* v, const float* a, const float* beta,
+                          void* u, char* ws, unsigned* status, cudaStream_t st) {
+  if (!tc_supported(s)) return cudaErrorInvalidValue;
+  const int G = s.heads / s.heads_per_group, nch = s.T / kTile;
+  CUtensorMap mK, mV;
+  if (!make_map(&mK, k, kDk, G, s.T, s.batch) || !make_map(&mV, v, kDv, s.heads, s.T, s.batch))
+    return cudaErrorInvalidValue;
+  TcGdnParams p{s.batch, s.T, s.heads, s.heads_per_group, G, a, beta, reinterpret_cast<uint8_t*>(ws), u, status};
+  cudaError_t e = cudaFuncSetAttribute(tc_gdn_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGdnL);
+  if (e != cudaSuccess) return e;
+  tc_gdn_local_kernel<<<(unsigned)((size_t)s.batch * s.heads * nch), 256, kSmemGdnL, st>>>(mK, mV, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
+  if ((e = cudaFuncSetAttribute(tc_gdn_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGdnP)) !=
+      cudaSuccess)
+    return e;
+  tc_gdn_pass_kernel<<<(unsigned)(s.batch * s.heads), 256, kSmemGdnP, st>>>(mK, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
+  return cudaSuccess;
+}
+
+}  // namespace ll
