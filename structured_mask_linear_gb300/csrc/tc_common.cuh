@@ -31,7 +31,6 @@ struct TcParams {
   int node_off[32];
   const float* a;
   const float* lam;
-  __nv_bfloat16* o;
   uint8_t* img;    // (B*H, nnodes, 16 KB) fp16 node images
   unsigned* meta;  // (B*H, nnodes, 4)
   unsigned* status;

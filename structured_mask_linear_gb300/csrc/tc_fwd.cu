@@ -279,6 +279,7 @@ template <int kMode>
 __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                            const __grid_constant__ CUtensorMap mapK,
                                                            const __grid_constant__ CUtensorMap mapV,
+                                                           const __grid_constant__ CUtensorMap mapO,
                                                            TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -372,6 +373,15 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     } else {
       for (int i = 0; i < nlev; ++i) ptx::cp_async4(sLamI + i * 128 + r, lrow + kLevIntra + lev_of(i));
     }
+    // The tree that the previous launches built is read from here on.  The wait (at once
+    // unless this grid was launched before they finished) and the node scalars' fetch
+    // overlap the tile's loads.
+    ptx::griddep_wait();
+    if (r < nlev) {
+      const unsigned* mt = meta_of(r);
+      ptx::cp_async4(sNode + 2 * r, mt + 1);
+      ptx::cp_async4(sNode + 2 * r + 1, mt + 2);
+    }
   }
   // chunk-local log2 decay cumsum over the 128 rows (both roles compute it)
   float gt = log2f(p.a[row * p.H + h]);
@@ -391,12 +401,19 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   if (!role_b) sG[r] = gt;
   __syncthreads();  // sG complete; s_red free again
   if (!role_b) sB8[r] = exp2f(sG[r | 7] - gt);  // decay from key r to the end of its 8-block
+  // role b's driver: the first node image into RE (free from the start), also while the
+  // tile loads; the barriers were initialised before the first __syncthreads
+  if (driver && nlev > 0) {
+    ptx::mbar_arrive_expect_tx(&bar_e[0], kImgBytes);
+    ptx::bulk_load(ebuf(0), img_of(0), kImgBytes, &bar_e[0]);
+  }
   bool ok = wait_bar(&bar_ld, 0);
   if (!ok) atomicExch(p.status, kStatusTimeout);
   ok = __syncthreads_and(ok);
 
-  // S = Q Kᵀ (M = 128 queries, N = 128 keys, K = 128 d_k), bf16, both K-major.
-  if (ok && driver && intra_on) {
+  // S = Q Kᵀ (M = 128 queries, N = 128 keys, K = 128 d_k), bf16, both K-major; issued by
+  // role a, which waits for it first, so that role b goes straight to its Q work.
+  if (ok && tid == 0 && intra_on) {
     ptx::tc_fence_after();
     const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 0);
     const uint32_t q0 = ptx::smem_u32(RQ), k0 = ptx::smem_u32(RK);
@@ -563,28 +580,15 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     __syncthreads();  // join (role b waits here after its levels)
   } else {
     // ---- role b -----------------------------------------------------------------------
-    // The tree that the previous launches built is read from here on: wait for them (at
-    // once unless this grid was launched before they finished), then fetch the node
-    // scalars and the first image (into RE, free from the start) behind the Q work.
+    // The tree wait, the node scalars and the first image were issued in the prologue.
     // Q row r -> fp16 with scale 2^-eq of its own: read and converted while S runs,
     // stored back once S has completed.  Then images 1 and 2 go into RK.
     uint8_t* qrow0 = RQ + r * 128;
     uint8_t* qrow1 = RQ + 16384 + r * 128;
     int eq = 0;
-    int issued = 0;                 // image loads issued
+    int issued = nlev > 0 ? 1 : 0;  // image loads issued by the driver (image 0 in the prologue)
     int consumed = 0;               // image loads waited for by the driver
     int y_issued = 0, y_seen = 0;   // Y MMAs issued / seen complete by the driver
-    ptx::griddep_wait();
-    if (r < nlev) {
-      const unsigned* mt = meta_of(r);
-      ptx::cp_async4(sNode + 2 * r, mt + 1);
-      ptx::cp_async4(sNode + 2 * r + 1, mt + 2);
-    }
-    if (ok && driver && nlev > 0) {
-      ptx::mbar_arrive_expect_tx(&bar_e[0], kImgBytes);
-      ptx::bulk_load(ebuf(0), img_of(0), kImgBytes, &bar_e[0]);
-      ++issued;
-    }
     if (ok) {
       uint4 qv[16];
       uint32_t mx = 0u;
@@ -724,10 +728,14 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       if (!ok && o_issued) atomicExch(p.status, kStatusTimeout);
     }
     ok = __all_sync(0xffffffffu, ok);
+    // o row r is staged in RV (V's buffer: free once O has completed, and never loaded
+    // when the intra-tile part is off) in the 128-byte-swizzled layout of o's tensor map,
+    // then the tile goes out in one TMA store.
+    const bool write_o = kMode != 2 || (p.lflags & 2);
+    uint8_t* orow_s = RV + r * 128;
     if (ok) {
       ptx::tc_fence_after();
       const float so = pow2s(sEp[r]);
-      __nv_bfloat16* orow = p.o + (row * p.H + h) * kDv;
       float* o32row = kMode == 2 ? p.o32 + (row * p.H + h) * kDv : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -765,9 +773,19 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) pk[j >> 1] = pack_bf16(y[j], y[j + 1]);
-        uint4* dst = reinterpret_cast<uint4*>(orow + half * 32);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        for (int c = 0; c < 4; ++c)  // 16-byte chunk half * 4 + c of the row
+          *reinterpret_cast<uint4*>(orow_s + (((half * 4 + c) ^ rot) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+    }
+    if (write_o) {
+      ptx::fence_proxy_async_smem();
+      const bool ok_o = ptx::named_bar_and(2, 128, ok);  // every row staged
+      if (driver && ok_o) {
+        ptx::tma_store_4d(&mapO, RV, 0, h, (int)t0, b);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_read_all();  // RV is read before the CTA ends
       }
     }
   }
@@ -968,11 +986,14 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Tensor maps of q, k, v (loads) and, when mO is given, of o (the output tile's store,
+// with v's geometry; a.o must then be set).
 bool tc_setup(const TcPlan& tp, const FwdArgs& a, CUtensorMap* mQ, CUtensorMap* mK, CUtensorMap* mV,
-              TcParams* pp) {
+              CUtensorMap* mO, TcParams* pp) {
   if (!make_map(mQ, a.q, kDk, tp.G, tp.T, tp.B) || !make_map(mK, a.k, kDk, tp.G, tp.T, tp.B) ||
       !make_map(mV, a.v, kDv, tp.H, tp.T, tp.B))
     return false;
+  if (mO && (!a.o || !make_map(mO, a.o, kDv, tp.H, tp.T, tp.B))) return false;
   TcParams& p = *pp;
   p = TcParams{};
   p.B = tp.B;
@@ -987,7 +1008,6 @@ bool tc_setup(const TcPlan& tp, const FwdArgs& a, CUtensorMap* mQ, CUtensorMap* 
   for (int m = 0; m < 32; ++m) p.node_off[m] = m < tp.MT ? tp.node_off[m] : 0;
   p.a = a.a;
   p.lam = a.lam;
-  p.o = static_cast<__nv_bfloat16*>(a.o);
   p.img = reinterpret_cast<uint8_t*>(a.ws + tp.off_img);
   p.meta = reinterpret_cast<unsigned*>(a.ws + tp.off_meta);
   p.status = a.status;
@@ -1023,27 +1043,28 @@ cudaError_t launch_tree(const TcPlan& tp, const FwdArgs& a, const TcParams& p, c
 
 template <int kMode>
 cudaError_t launch_output(const TcPlan& tp, const CUtensorMap& mQ, const CUtensorMap& mK,
-                          const CUtensorMap& mV, const TcParams& p, int ninter, cudaStream_t st) {
+                          const CUtensorMap& mV, const CUtensorMap& mO, const TcParams& p, int ninter,
+                          cudaStream_t st) {
   const unsigned grid = (unsigned)((size_t)tp.B * tp.NT * tp.H);
   const int smem_out = out_smem_bytes(ninter);
   cudaError_t e = cudaFuncSetAttribute(tc_output_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_out);
   if (e != cudaSuccess) return e;
   if (kMode == 0)  // the comparators' passes read each other's output: plain stream order
-    return launch_overlapped(tc_output_kernel<kMode>, dim3(grid), dim3(256), smem_out, st, mQ, mK, mV, p);
-  tc_output_kernel<kMode><<<grid, 256, smem_out, st>>>(mQ, mK, mV, p);
+    return launch_overlapped(tc_output_kernel<kMode>, dim3(grid), dim3(256), smem_out, st, mQ, mK, mV, mO, p);
+  tc_output_kernel<kMode><<<grid, 256, smem_out, st>>>(mQ, mK, mV, mO, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
-  CUtensorMap mQ, mK, mV;
+  CUtensorMap mQ, mK, mV, mO;
   TcParams p;
-  if (!tc_setup(tp, a, &mQ, &mK, &mV, &p)) return cudaErrorInvalidValue;
+  if (!tc_setup(tp, a, &mQ, &mK, &mV, &mO, &p)) return cudaErrorInvalidValue;
   cudaError_t e = launch_state(tp, a, mK, mV, p, st);
   if (e == cudaSuccess) e = launch_tree(tp, a, p, st);
   if (e != cudaSuccess) return e;
-  if ((e = launch_output<0>(tp, mQ, mK, mV, p, bit_length(tp.NT - 1), st)) != cudaSuccess) return e;
+  if ((e = launch_output<0>(tp, mQ, mK, mV, mO, p, bit_length(tp.NT - 1), st)) != cudaSuccess) return e;
   note_launch(a, 2, st);
   if (a.states_out) {
     if ((e = launch_overlapped(tc_export_kernel, dim3(__builtin_popcount((unsigned)tp.T), tp.B * tp.H), dim3(256), 0, st, p,
@@ -1059,9 +1080,9 @@ size_t tc_naive_bytes(const TcPlan& tp) {
 }
 
 cudaError_t launch_tc_naive(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
-  CUtensorMap mQ, mK, mV;
+  CUtensorMap mQ, mK, mV, mO;
   TcParams p;
-  if (!tc_setup(tp, a, &mQ, &mK, &mV, &p)) return cudaErrorInvalidValue;
+  if (!tc_setup(tp, a, &mQ, &mK, &mV, &mO, &p)) return cudaErrorInvalidValue;
   p.o32 = reinterpret_cast<float*>(a.ws + ((tp.bytes + 255) & ~size_t(255)));
   cudaError_t e = launch_state(tp, a, mK, mV, p, st);
   if (e == cudaSuccess) e = launch_tree(tp, a, p, st);
@@ -1070,7 +1091,7 @@ cudaError_t launch_tc_naive(const TcPlan& tp, const FwdArgs& a, cudaStream_t st)
   for (int l = 0; l <= last; ++l) {  // one pass per level, no fusion
     p.lsel = l;
     p.lflags = (l == 0 ? 1 : 0) | (l == last ? 2 : 0);
-    if ((e = launch_output<2>(tp, mQ, mK, mV, p, 1, st)) != cudaSuccess) return e;
+    if ((e = launch_output<2>(tp, mQ, mK, mV, mO, p, 1, st)) != cudaSuccess) return e;
     note_launch();
   }
   return cudaSuccess;
@@ -1082,9 +1103,9 @@ size_t tc_ssd_bytes(const TcPlan& tp) {
 }
 
 cudaError_t launch_tc_ssd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
-  CUtensorMap mQ, mK, mV;
+  CUtensorMap mQ, mK, mV, mO;
   TcParams p;
-  if (!tc_setup(tp, a, &mQ, &mK, &mV, &p)) return cudaErrorInvalidValue;
+  if (!tc_setup(tp, a, &mQ, &mK, &mV, &mO, &p)) return cudaErrorInvalidValue;
   const size_t base = (tp.bytes + 255) & ~size_t(255);
   p.pimg = reinterpret_cast<uint8_t*>(a.ws + base);
   p.pmeta = reinterpret_cast<unsigned*>(a.ws + base + (size_t)tp.B * tp.H * tp.NT * kImgBytes);
@@ -1098,7 +1119,7 @@ cudaError_t launch_tc_ssd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launch();
   }
-  if ((e = launch_output<1>(tp, mQ, mK, mV, p, 1, st)) != cudaSuccess) return e;
+  if ((e = launch_output<1>(tp, mQ, mK, mV, mO, p, 1, st)) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
 }
@@ -1107,16 +1128,11 @@ cudaError_t launch_tc_ssd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
 cudaError_t launch_tc_nodes(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   CUtensorMap mQ, mK, mV;
   TcParams p;
-  if (!tc_setup(tp, a, &mQ, &mK, &mV, &p)) return cudaErrorInvalidValue;
+  if (!tc_setup(tp, a, &mQ, &mK, &mV, nullptr, &p)) return cudaErrorInvalidValue;
   cudaError_t e = launch_state(tp, a, mK, mV, p, st);
   if (e == cudaSuccess) e = launch_tree(tp, a, p, st);
   return e;
 }
-
-
-
-
-
 
 cudaError_t launch_wait_selftest(unsigned* status, long long spins, cudaStream_t st) {
   wait_selftest_kernel<<<1, 32, 0, st>>>(status, spins);
