@@ -504,10 +504,21 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
           ptx::tmem_ld_wait();
           float v[32];
           if (fastd) {
-            // blocks after t's may give A = inf; their keys are masked by the select
+            // 8-key blocks before t's: one level each, bit length of (tb ^ kb) plus 3, and
+            // the factored decay.  t's own block: level of key e is the bit length of
+            // te ^ e (0..3), zero above t.  Blocks after t's are zero (a select: A may be
+            // inf there).
+            const int tb = tl >> 3, te = tl & 7;
             float ak[4];
 #pragma unroll
-            for (int kb = 0; kb < 4; ++kb) ak[kb] = exp2f(gt - gq[kb * 8 + 7]);
+            for (int kb = 0; kb < 4; ++kb) {
+              const float lv = kb == tb ? 1.f : lamr[35 - __clz(tb ^ kb)];
+              const float x = coef * lv * exp2f(gt - gq[kb * 8 + 7]);
+              ak[kb] = kb > tb ? 0.f : x;
+            }
+            float fo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) fo[e] = e <= te ? lamr[32 - __clz(te ^ e)] : 0.f;
             const float4* b4 = reinterpret_cast<const float4*>(sB8 + cg * 32);
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {
@@ -515,9 +526,9 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
               const float bj[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const int j = 4 * j4 + e;
-                const float x = (sv[j] * coef) * lamr[32 - __clz(tl ^ j)] * (ak[j >> 3] * bj[e]);
-                v[j] = j <= tl ? x : 0.f;
+                const int j = 4 * j4 + e, kb = j >> 3;
+                const float f = kb == tb ? fo[j & 7] : 1.f;
+                v[j] = sv[j] * (ak[kb] * bj[e]) * f;
               }
             }
           } else {
