@@ -335,7 +335,11 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     return p.meta + (nbase + p.node_off[m] + ((u >> m) - 1)) * kMeta;
   };
 
-  if (tid == 0) {
+  // Warp 0's prologue path held the tile's loads back: tcgen05.alloc takes about 1 us, and
+  // the load of a behind it another 1 us.  So a is loaded first, warp 1 initialises the
+  // barriers and issues the tile loads, and warp 0 allocates after the lambda copies.
+  const float a_row = p.a[row * p.H + h];
+  if (tid == 32) {
     s_oi = 0;
     ptx::mbar_init(&bar_ld, 1);
     ptx::mbar_init(&bar_s, 1);
@@ -354,10 +358,6 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
       ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
     }
-  }
-  if (warp == 0) {
-    ptx::tmem_alloc(&tmem_base, 256);
-    ptx::tmem_relinquish();
   }
   // lambda of this row (levels 0..7 for role a, the tile's inter levels for role b) and
   // the node scalars of the tile's levels, copied asynchronously
@@ -383,8 +383,12 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       ptx::cp_async4(sNode + 2 * r + 1, mt + 2);
     }
   }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_base, 256);
+    ptx::tmem_relinquish();
+  }
   // chunk-local log2 decay cumsum over the 128 rows (both roles compute it)
-  float gt = log2f(p.a[row * p.H + h]);
+  float gt = log2f(a_row);
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const float y = __shfl_up_sync(0xffffffffu, gt, off);
