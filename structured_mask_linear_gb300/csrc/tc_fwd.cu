@@ -243,19 +243,21 @@ __global__ void __launch_bounds__(128, 3) tc_tree_kernel(TcParams p, int m0) {
 // ---------------------------------------------------------------------------------
 // tc_output: intra-tile masked attention + level-fused inter-tile buckets.
 //
-// 256 threads in two roles after a common prologue (loads, decay cumsum):
-//  role a (warps 0-3): once S has landed, P row t = thread, written as fp16 into tensor
-//          memory over the columns of S it has consumed; then the V tile scale and V ->
-//          fp16 in place; O = P V with P as the tensor-memory A operand.
-//  role b (warps 4-7): issues S = Q Kᵀ; waits for the tree's launches and fetches the
-//          node scalars and the first node image; Q row t -> fp16 with a power-of-two
+// 256 threads in two roles after a common prologue (warp 1 issues the tile loads; both
+// roles copy their lambda rows and compute the decay cumsum; warp 0 allocates TMEM):
+//  role a (warps 0-3): issues S = Q Kᵀ; once S has landed, P row t = thread, written as
+//          fp16 into tensor memory over the columns of S it has consumed; then the V tile
+//          scale and V -> fp16 in place; O = P V with P as the tensor-memory A operand.
+//  role b (warps 4-7): waits for the tree's launches and fetches the node scalars and
+//          the first node image, all in the prologue; Q row t -> fp16 with a power-of-two
 //          scale of its own (undone in the row weight) in place once S has read Q; the
 //          inter-tile levels, nearest first and two per MMA (N = 128 over two node
-//          images), with up to three node images in flight; then the write of o.
+//          images), with up to three node images in flight; then the write of o, staged
+//          in RV and stored with one TMA store.
 // Both roles see every TMEM lane through warp % 4.
 // Shared memory (2 CTAs per SM): RQ = Q (bf16, then fp16 in place); RK = K (bf16) until
-// S completes, then node image buffers 1 and 2; RV = V (bf16, then fp16 in place);
-// RE = node image buffer 0.  The image of level index i (i-th set bit of u from the
+// S completes, then node image buffers 1 and 2; RV = V (bf16, then fp16 in place), then
+// the staging of o; RE = node image buffer 0.  The image of level index i (i-th set bit of u from the
 // bottom) goes to buffer i % 3, completing phase (i / 3) & 1 of bar_e[i % 3].
 // lambda rows and the node scalars are copied into shared memory at the start
 // (asynchronously), so that no global load sits on the path of P or of a level.
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   const int r = tid & 127;             // query row (tile-local token)
   const int quad = warp & 3;           // TMEM lane quadrant of this warp
   const bool role_b = warp >= 4;       // S, inter-tile levels and the final write
-  const bool driver = tid == 128;      // role b's MMA and image-load issuer
+  const bool driver = tid == 128;      // role b's MMA, image-load and o-store issuer
   const int rot = r & 7;
   const int lin = blockIdx.x;
   const int h = lin % p.H;
