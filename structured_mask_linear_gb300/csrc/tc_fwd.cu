@@ -59,7 +59,9 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   const int g = h / p.hpg;
   const int bh = b * p.H + h;
   const long long t0 = (long long)u * kTile;
-  const float la = log2f(p.a[((size_t)b * p.T + t0 + tid) * p.H + h]);
+  // a of token t0 + tid: loaded first, its log2 taken only where the scan needs it, so
+  // that thread 0 issues the tile loads without waiting for this load
+  const float a_t = p.a[((size_t)b * p.T + t0 + tid) * p.H + h];
   ptx::griddep_launch_dependents();
 
   if (tid == 0) {
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   }
   // decay of token t0 + tid: chunk-local log2 cumsum (the scan also publishes tmem_base)
   ptx::tc_fence_before();
-  const float gi = block_scan128(la, s_red);
+  const float gi = block_scan128(log2f(a_t), s_red);
   ptx::tc_fence_after();
   const uint32_t tbase = tmem_base;
   if (tid == kTile - 1) s_gamma = gi;
