@@ -51,7 +51,7 @@ typedef enum {
   LL_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than the query says */
   LL_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed */
   LL_ERR_TIMEOUT = 7,       /* a bounded device-side wait ran out (see check_status) */
-  LL_ERR_UNIMPLEMENTED = 8  /* valid request that this build does not cover */
+  LL_ERR_UNIMPLEMENTED = 8  /* valid request that this library does not implement */
 } ll_status;
 
 typedef enum { LL_F32 = 0, LL_BF16 = 1 } ll_dtype;
