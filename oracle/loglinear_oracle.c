@@ -283,6 +283,117 @@ void oracle_form_r_head(long T, long dk, long dv, long L, const double* q, const
 }
 
 /* ---------------------------------------------------------------------------
+ * Sequence segments.  Page 1 (section 特殊结构：树划分) keeps one memory per
+ * bucket of the Fenwick partition of the prefix; section 高效训练算法 forms the
+ * memories of chunks and combines them level by level.  The same holds for
+ * any split of the sequence into segments: the memory of a bucket is the
+ * decayed sum of the memories of the pieces it is made of.
+ * ------------------------------------------------------------------------- */
+
+/* Form R for the tokens at positions T0 .. T0+T-1 of one head, starting from
+ * the bucket memories at position T0 (the live levels of T0, each already
+ * decayed to position T0-1, i.e. what form_r_head captures at T0).  The same
+ * three steps per token as form_r_head, with the level tests on the absolute
+ * position.  q, k (T, dk), v, o (T, dv), a (T), lam (T, L) hold the segment's
+ * tokens only; init (Ls, dk, dv); final_states (Ls, dk, dv), if non-null,
+ * receives the live memories at T0+T (zero elsewhere).  Ls must be at least
+ * bit_length(T0 + T) + 1. */
+void oracle_form_r_from(long T0, long T, long dk, long dv, long L, const double* q,
+                        const double* k, const double* v, const double* a, const double* lam,
+                        long Ls, const double* init, double* o, double* final_states) {
+  long sz = dk * dv;
+  double* S = (double*)malloc(sizeof(double) * (size_t)(Ls * sz));
+  for (long l = 0; l < Ls; l++) {
+    int live = l >= 1 && ((T0 >> (l - 1)) & 1L);
+    for (long e = 0; e < sz; e++) S[l * sz + e] = live ? init[l * sz + e] : 0.0;
+  }
+  for (long i = 0; i < T; i++) {
+    long t = T0 + i; /* absolute position */
+    const double* qt = q + i * dk;
+    const double* kt = k + i * dk;
+    const double* vt = v + i * dv;
+    double* ot = o + i * dv;
+    for (long l = 1; l < Ls; l++) /* 1. decay the live buckets */
+      if ((t >> (l - 1)) & 1L)
+        for (long e = 0; e < sz; e++) S[l * sz + e] *= a[i];
+    double dot = 0.0; /* 2. output */
+    for (long c = 0; c < dk; c++) dot += qt[c] * kt[c];
+    for (long j = 0; j < dv; j++) ot[j] = lam[i * L] * dot * vt[j];
+    for (long l = 1; l < Ls; l++) {
+      if (!((t >> (l - 1)) & 1L)) continue;
+      for (long c = 0; c < dk; c++) {
+        double qc = lam[i * L + l] * qt[c];
+        for (long j = 0; j < dv; j++) ot[j] += qc * S[l * sz + c * dv + j];
+      }
+    }
+    long m = 0; /* 3. carry into level m+1 of t+1 */
+    while ((t >> m) & 1L) m++;
+    double* Sn = S + (m + 1) * sz;
+    for (long c = 0; c < dk; c++)
+      for (long j = 0; j < dv; j++) Sn[c * dv + j] = kt[c] * vt[j];
+    for (long l = 1; l <= m; l++)
+      for (long e = 0; e < sz; e++) {
+        Sn[e] += S[l * sz + e];
+        S[l * sz + e] = 0.0;
+      }
+  }
+  if (final_states) {
+    long E = T0 + T;
+    for (long l = 0; l < Ls; l++) {
+      int live = l >= 1 && ((E >> (l - 1)) & 1L);
+      for (long e = 0; e < sz; e++) final_states[l * sz + e] = live ? S[l * sz + e] : 0.0;
+    }
+  }
+  free(S);
+}
+
+/* The memory of a whole segment of T tokens of one head, by the definition:
+ * total = sum over s < T of (a_{s+1} * ... * a_{T-1}) k_s v_sᵀ, the product
+ * formed by an explicit loop, and logdecay = sum over r < T of log a_r (the
+ * decay the segment applies to everything before it).  k (T, dk), v (T, dv),
+ * a (T); total (dk, dv). */
+void oracle_segment_total(long T, long dk, long dv, const double* k, const double* v,
+                          const double* a, double* total, double* logdecay) {
+  memset(total, 0, sizeof(double) * (size_t)(dk * dv));
+  for (long s = 0; s < T; s++) {
+    double w = 1.0;
+    for (long r = s + 1; r < T; r++) w *= a[r];
+    for (long c = 0; c < dk; c++)
+      for (long j = 0; j < dv; j++) total[c * dv + j] += w * k[s * dk + c] * v[s * dv + j];
+  }
+  double g = 0.0;
+  for (long r = 0; r < T; r++) g += log(a[r]);
+  *logdecay = g;
+}
+
+/* Bucket memories at position T0 = r * seg_len from the memories of the r
+ * segments before it (seg_len a power of two, so every bucket of the prefix
+ * [0, T0) is made of whole segments).  The buckets come from the
+ * binary-indexed-tree decomposition of the prefix (oracle_prefix_buckets); a
+ * bucket of n positions has level log2(n) + 1, and its memory is
+ *   sum over its segments sigma of exp(sum of logdecay over the segments
+ *   after sigma and before T0) * seg_states[sigma].
+ * seg_states (r, dk, dv), seg_logdecay (r); states (Ls, dk, dv), zero for the
+ * levels that are not live at T0. */
+void oracle_prefix_from_segments(long r, long seg_len, long dk, long dv, const double* seg_states,
+                                 const double* seg_logdecay, long Ls, double* states) {
+  long sz = dk * dv;
+  memset(states, 0, sizeof(double) * (size_t)(Ls * sz));
+  long lo[64], len[64];
+  int nb = oracle_prefix_buckets(r * seg_len, lo, len, 64);
+  for (int b = 0; b < nb; b++) {
+    long lvl = ilog2_exact(len[b]) + 1;
+    double* dst = states + lvl * sz;
+    for (long sg = lo[b] / seg_len; sg < (lo[b] + len[b]) / seg_len; sg++) {
+      double g = 0.0;
+      for (long later = sg + 1; later < r; later++) g += seg_logdecay[later];
+      double w = exp(g);
+      for (long e = 0; e < sz; e++) dst[e] += w * seg_states[sg * sz + e];
+    }
+  }
+}
+
+/* ---------------------------------------------------------------------------
  * Brute force for small T: the dense T x T masks built without the level
  * formula, then O = (Q Kᵀ ⊙ M^S ⊙ M^H) V (page 1, section 结构矩阵).
  *   M^S(t,s) = a_{s+1} * ... * a_t by an explicit product loop;

@@ -21,6 +21,11 @@ file's header and above each C function.  Summary:
                             log a and lambda: the chain rule on the quadratic form.
 * ``gdn_values``            Gated DeltaNet's transformed values u (gated delta rule
                             run token by token); ``gdn_forward`` = form_q with v = u.
+* ``form_r_from``           the recurrent form over the tokens T0 .. T0+T-1 of one
+                            head, starting from the bucket memories at T0.
+* ``segment_total``         the memory of a whole segment and its summed log-decay.
+* ``prefix_from_segments``  the bucket memories at T0 = r * seg_len built from the
+                            memories of the r segments before it.
 """
 from __future__ import annotations
 
@@ -71,8 +76,12 @@ def _load():
             lib.oracle_form_r_head.argtypes = [_l] * 4 + [_D] * 6 + [_l, _l, _L, _D]
             lib.oracle_backward.argtypes = six + [_D] * 11
             lib.oracle_gdn_values.argtypes = [_l] * 6 + [_D] * 5
+            lib.oracle_form_r_from.argtypes = [_l] * 5 + [_D] * 5 + [_l] + [_D] * 3
+            lib.oracle_segment_total.argtypes = [_l] * 3 + [_D] * 5
+            lib.oracle_prefix_from_segments.argtypes = [_l] * 4 + [_D] * 2 + [_l, _D]
             for f in ("oracle_form_q", "oracle_brute", "oracle_form_r", "oracle_form_q_points",
-                      "oracle_form_r_head", "oracle_backward", "oracle_gdn_values"):
+                      "oracle_form_r_head", "oracle_backward", "oracle_gdn_values",
+                      "oracle_form_r_from", "oracle_segment_total", "oracle_prefix_from_segments"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -220,3 +229,50 @@ def gdn_values(k, v, a, beta) -> np.ndarray:
 def gdn_forward(q, k, v, a, beta, lam) -> np.ndarray:
     """Log-linear Gated DeltaNet: the masked form with the transformed values u."""
     return form_q(q, k, gdn_values(k, v, a, beta), a, lam)
+
+
+def form_r_from(q, k, v, a, lam, T0: int, init_states, levels: int):
+    """One head, the tokens at positions T0 .. T0+T-1: q, k (T, dk), v (T, dv), a (T),
+    lam (T, L), and the bucket memories at T0 init_states (>= bit_length(T0)+1 levels,
+    dk, dv; levels not live at T0 are ignored).  Returns o (T, dv) and the live memories
+    at T0+T (levels, dk, dv)."""
+    q, k, v, a, lam = (_f64(x) for x in (q, k, v, a, lam))
+    T, dk = q.shape
+    dv = v.shape[1]
+    L = lam.shape[1]
+    assert levels >= _bitlen(T0 + T) + 1 and L >= _bitlen(max(T0 + T - 1, 0)) + 1
+    init = np.zeros((levels, dk, dv))
+    if init_states is not None:
+        src = _f64(init_states)
+        n = min(levels, src.shape[0])
+        init[:n] = src[:n]
+    o = np.zeros((T, dv))
+    fin = np.zeros((levels, dk, dv))
+    _load().oracle_form_r_from(int(T0), T, dk, dv, L, _d(q), _d(k), _d(v), _d(a), _d(lam), levels,
+                               _d(init), _d(o), _d(fin))
+    return o, fin
+
+
+def segment_total(k, v, a):
+    """One head's segment: k (T, dk), v (T, dv), a (T).  Returns the segment's memory
+    sum_s (a_{s+1} ... a_{T-1}) k_s v_sᵀ (dk, dv) and its summed log-decay."""
+    k, v, a = (_f64(x) for x in (k, v, a))
+    T, dk = k.shape
+    dv = v.shape[1]
+    tot = np.zeros((dk, dv))
+    g = np.zeros(1)
+    _load().oracle_segment_total(T, dk, dv, _d(k), _d(v), _d(a), _d(tot), _d(g))
+    return tot, float(g[0])
+
+
+def prefix_from_segments(seg_states, seg_logdecay, seg_len: int, levels: int):
+    """Bucket memories at T0 = r * seg_len (r = len(seg_states), seg_len a power of two)
+    from the r segments' memories (r, dk, dv) and summed log-decays (r)."""
+    st = _f64(seg_states)
+    g = _f64(seg_logdecay)
+    r, dk, dv = st.shape
+    assert seg_len > 0 and seg_len & (seg_len - 1) == 0
+    assert levels >= _bitlen(r * seg_len) + 1
+    out = np.zeros((levels, dk, dv))
+    _load().oracle_prefix_from_segments(r, seg_len, dk, dv, _d(st), _d(g), levels, _d(out))
+    return out
