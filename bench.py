@@ -43,10 +43,13 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the long/decode/e2e extras")
-    ap.add_argument("--ncu-case", nargs="?", const="fwd", choices=["fwd", "bwd", "gdn"],
-                    help="profiling case on the pages workload at batch 1 (inputs 225 MB > L2), "
-                         "no timing, no JSON: three forwards (fwd, the default), two backwards "
-                         "(bwd) or two Gated DeltaNet forwards (gdn)")
+    ap.add_argument("--ncu-case", nargs="?", const="fwd",
+                    choices=["fwd", "bwd", "gdn", "decode", "long"],
+                    help="profiling case, no timing, no JSON: on the pages workload at batch 1 "
+                         "(inputs 225 MB > L2) three forwards (fwd, the default), two backwards "
+                         "(bwd) or two Gated DeltaNet forwards (gdn); decode: three decode steps "
+                         "of the decode workload at batch 8 (states 214 MB > L2); long: two "
+                         "forwards of the long workload's shape with 4 of its 48 heads")
     return ap.parse_args()
 
 
@@ -155,13 +158,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def traffic_for(kernel: str, w):
+def traffic_for(kernel: str, w, key: str | None = None):
     """ncu DRAM bytes per launch from profiles/traffic.json, if the kernel's source is
-    unchanged since the capture (scaled to this workload's units)."""
+    unchanged since the capture (scaled to this workload's units: the record holds bytes
+    per token of all heads).  key names the record (default: the kernel's name)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel)
+    d = json.load(open(p)).get(key or kernel)
     if not d:
         return None
     srcs = d["source"] if isinstance(d["source"], list) else [d["source"]]
@@ -184,7 +188,7 @@ def cpu_oracle_run(w, heads: int, T: int, seed: int = 0):
     from oracle import oracle
     from structured_mask_linear_gb300.inputs import make_inputs, to_numpy64, workload
 
-    ws = workload(w.name, batch=1, heads=heads, T=T,
+    ws = workload(w.name, batch=1, heads=heads, T=T, decode_steps=0,
                   heads_per_group=min(w.heads_per_group, heads))
     x = make_inputs(ws, "cpu", seed=seed)
     arrs = [to_numpy64(t) for t in (x.q, x.k, x.v, x.a, x.lam)]
@@ -282,6 +286,22 @@ def ncu_case(what: str = "fwd"):
     from structured_mask_linear_gb300.inputs import make_inputs, workload
 
     sml.lib()
+    if what == "decode":
+        wd = workload("decode", batch=8)
+        st, lsc, q, k, v, a, lam = decode_inputs(torch, wd, "cuda", steps=3)
+        for i in range(3):
+            sml.loglinear_decode_step(wd.T + i, q[i], k[i], v[i], a[i], lam[i], st, lsc)
+        torch.cuda.synchronize()
+        assert sml.loglinear_check_status() == 0
+        return
+    if what == "long":
+        wl = workload("long", heads=4)
+        x = make_inputs(wl, "cuda", seed=1)
+        for _ in range(2):
+            sml.loglinear_fwd(x.q, x.k, x.v, x.a, x.lam, chunk=wl.chunk)
+        torch.cuda.synchronize()
+        assert sml.loglinear_check_status() == 0
+        return
     w = workload("pages", batch=1)
     x = make_inputs(w, "cuda", seed=0)
     gen = torch.Generator(device="cuda")
@@ -572,6 +592,9 @@ def comparators_measure(sml, torch, x, w, fused_ms, steps=5):
 
 
 def long_measure(sml, torch, dev, steps=5):
+    """The long workload (B=1, H=48, T=131072): whole-step time, then the same steps with
+    CUDA events between the kernels for the dominant kernel's roofline, and the oracle's
+    recurrent form on a bounded sample of the same workload."""
     from structured_mask_linear_gb300.inputs import make_inputs, workload
 
     w = workload("long")
@@ -579,6 +602,7 @@ def long_measure(sml, torch, dev, steps=5):
     o = torch.empty_like(x.v)
     shape = sml.fwd_shape(x.q, x.v, x.lam, w.chunk)
     wsb = torch.empty(sml.loglinear_fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    names = sml.loglinear_fwd_kernel_names(shape, with_export=False)
     for _ in range(3):
         sml.loglinear_fwd(x.q, x.k, x.v, x.a, x.lam, chunk=w.chunk, o=o, workspace=wsb)
     torch.cuda.synchronize()
@@ -589,22 +613,54 @@ def long_measure(sml, torch, dev, steps=5):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    hbm_peak, _, _ = peaks()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(steps)]
+    for row in evs:  # torch creates the CUDA event on its first record
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    for row in evs:
+        sml.loglinear_fwd_profiled(x.q, x.k, x.v, x.a, x.lam, row, chunk=w.chunk, o=o, workspace=wsb)
+    torch.cuda.synchronize()
+    if sml.loglinear_check_status() != 0:
+        raise RuntimeError("device status error in the long workload")
+    per_kernel = [statistics.mean(r[j].elapsed_time(r[j + 1]) for r in evs) for j in range(len(names))]
+    dom = max(range(len(names)), key=lambda j: per_kernel[j])
+    hbm_peak, _, peak_src = peaks()
     pb = algorithmic_bytes(w, "path")
+    db = algorithmic_bytes(w, names[dom])
+    ach = db / (per_kernel[dom] / 1e3) / 1e9
     res = {"workload": workload_desc(w), "value": w.batch * w.T / (ms / 1e3), "unit": "tokens/s",
            "ms_per_step": ms, "steps": steps,
-           "path_frac": pb / (ms / 1e3) / 1e9 / hbm_peak}
-    del x, o, wsb
+           "path_frac": pb / (ms / 1e3) / 1e9 / hbm_peak,
+           "kernels_ms": {n: round(t, 4) for n, t in zip(names, per_kernel)},
+           "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": ach, "peak": hbm_peak,
+                        "unit": "GB/s", "frac": ach / hbm_peak, "peak_source": peak_src,
+                        "traffic": traffic_for(names[dom], w, key=names[dom] + ":long"),
+                        "algorithmic_bytes_per_launch": db}}
+    del x, o, wsb, evs
     torch.cuda.empty_cache()
+    res["cpu_baseline"] = cpu_baseline_sampled(w)
     return res
 
 
-def decode_measure(sml, torch, dev, hbm_peak, steps=1024):
-    """Decode workload timing: B=64, H=48, positions 32768..33791 (the live levels of each
-    position decide the work; state values do not)."""
-    from structured_mask_linear_gb300.inputs import workload
+def cpu_baseline_sampled(w, T: int | None = None):
+    """The oracle's recurrent form on batch element 0, as many heads as host cores (even,
+    at most H), the first T tokens (default all): all-head token equivalents per second."""
+    import multiprocessing
 
-    w = workload("decode")
+    from oracle import oracle
+
+    heads = max(2, min(w.heads, (multiprocessing.cpu_count() // 2) * 2))
+    T = w.T if T is None else T
+    dt, cores = cpu_oracle_run(w, heads, T)
+    return {"value": T * heads / w.heads / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"recurrent Fenwick form, fp64, batch element 0, {heads} of {w.heads} heads, "
+                      f"first {T} tokens: {dt:.2f} s, scaled to all {w.heads} heads"}
+
+
+def decode_inputs(torch, w, dev, steps):
+    """Random fp32 states at every level (the live levels of each position decide the
+    work; state values do not) and per-step token inputs for `steps` decode steps."""
     B, H, G, L = w.batch, w.heads, w.groups, w.levels
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
@@ -615,6 +671,25 @@ def decode_measure(sml, torch, dev, hbm_peak, steps=1024):
     v = torch.randn((steps, B, H, w.d_v), generator=gen, device=dev).to(torch.bfloat16)
     a = torch.rand((steps, B, H), generator=gen, device=dev) * 0.5 + 0.5
     lam = torch.rand((steps, B, H, L), generator=gen, device=dev)
+    return st, lsc, q, k, v, a, lam
+
+
+def decode_bytes(w, pos: int) -> int:
+    """Algorithmic bytes of one decode step at position pos: every live state read once,
+    the merged state written once, the token's inputs read and its output written."""
+    B, H, G, L = w.batch, w.heads, w.groups, w.levels
+    state = w.d_k * w.d_v * 4
+    tok_io = B * (2 * G * w.d_k * 2 + H * w.d_v * 2 * 2 + H * 4 + H * L * 4)
+    return B * H * (bin(pos).count("1") * state + state) + tok_io
+
+
+def decode_measure(sml, torch, dev, hbm_peak, steps=1024):
+    """Decode workload timing: B=64, H=48, positions 32768..33791."""
+    from structured_mask_linear_gb300.inputs import workload
+
+    w = workload("decode")
+    B, H, L = w.batch, w.heads, w.levels
+    st, lsc, q, k, v, a, lam = decode_inputs(torch, w, dev, steps)
     o = torch.empty((B, H, w.d_v), dtype=torch.bfloat16, device=dev)
     for i in range(5):
         sml.loglinear_decode_step(w.T + i, q[i], k[i], v[i], a[i], lam[i], st, lsc, o_t=o)
@@ -627,15 +702,26 @@ def decode_measure(sml, torch, dev, hbm_peak, steps=1024):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    state = w.d_k * w.d_v * 4
-    tok_io = B * (2 * G * w.d_k * 2 + H * w.d_v * 2 * 2 + H * 4 + H * L * 4)
-    nbytes = sum(B * H * (bin(w.T + i).count("1") * state + state) for i in range(steps)) / steps
-    nbytes += tok_io
-    return {"workload": f"decode: B={B} H={H} d_k={w.d_k} d_v={w.d_v}, positions "
-                        f"{w.T}..{w.T + steps - 1}, {L} fp32 state levels",
-            "value": B / (ms / 1e3), "unit": "tokens/s", "us_per_step": 1e3 * ms,
-            "achieved_gbs": nbytes / (ms / 1e3) / 1e9, "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
-            "algorithmic_bytes_per_step": int(nbytes)}
+    nbytes = sum(decode_bytes(w, w.T + i) for i in range(steps)) / steps
+    res = {"workload": f"decode: B={B} H={H} d_k={w.d_k} d_v={w.d_v}, positions "
+                       f"{w.T}..{w.T + steps - 1}, {L} fp32 state levels",
+           "value": B / (ms / 1e3), "unit": "tokens/s", "us_per_step": 1e3 * ms,
+           "achieved_gbs": nbytes / (ms / 1e3) / 1e9, "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
+           "algorithmic_bytes_per_step": int(nbytes),
+           "roofline": {"bound": "hbm", "kernel": "decode_step_kernel",
+                        "achieved": nbytes / (ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
+                        "traffic": traffic_for("decode_step_kernel", w, key="decode_step_kernel:decode"),
+                        "algorithmic_bytes_per_launch": int(nbytes)}}
+    del st, lsc, q, k, v, a, lam, o
+    torch.cuda.empty_cache()
+    # the oracle's recurrent form over the prefix and the decode positions (0..33791), one
+    # token at a time as a decode loop runs it; a token = one step of one stream, all heads
+    cb = cpu_baseline_sampled(w, T=w.T + steps)
+    cb["sample"] += (" (positions 0..%d: the prefix and the decode positions, token by token)"
+                     % (w.T + steps - 1))
+    res["cpu_baseline"] = cb
+    return res
 
 
 if __name__ == "__main__":

@@ -107,6 +107,10 @@ size_t loglinear_fwd_workspace_bytes(const ll_shape* shape);
  *                     is folded into states_out).
  *   state_levels      slots in states_out; must be >= bit_length(T) + 1 when states_out
  *                     is given, ignored otherwise.
+ * Which kernels run (loglinear_fwd_path reports it): bf16 with d_k = 128, d_v = 64 and
+ * T % 128 == 0 takes the tensor-core path (tcgen05 products over 128-token tiles).  Every
+ * other accepted shape, including that bf16 shape with T % 128 == 64 (e.g. T = 2368), runs
+ * the fp32 CUDA-core path, which computes the same result several times more slowly.
  */
 ll_status loglinear_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
                         const float* a, const float* lambda, void* o, void* workspace,
@@ -148,6 +152,9 @@ ll_status loglinear_decode_step(const ll_shape* shape, long long pos, const void
  * on a device creates the two streams and their events (kept until exit).  The host
  * buffers must stay valid until then; the caller synchronises.  `device_arena` must hold
  * at least loglinear_fwd_host_arena_bytes(shape) bytes (16-byte aligned).
+ * Calls from several host threads are safe: the library holds a per-device lock while a
+ * call enqueues its work.  Their copies share the two library streams, so concurrent
+ * calls' copies run one after another; each call needs its own arena and host buffers.
  */
 size_t loglinear_fwd_host_arena_bytes(const ll_shape* shape);
 ll_status loglinear_fwd_host(const ll_shape* shape, const void* q_host, const void* k_host,

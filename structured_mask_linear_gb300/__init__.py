@@ -138,6 +138,20 @@ def _check(status: int, where: str):
         raise LogLinearError(status, where)
 
 
+def _on_device(*tensors):
+    """Context that makes the tensors' CUDA device current for the call.  The library
+    works on the current device (its status word, its stream lookups, the static
+    workspace) and the default stream is the current device's, so every tensor of a call
+    must live on one device and that device must be current while the call enqueues."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors of a call must be on one CUDA device, got {sorted(map(str, devs))}")
+    dev = devs.pop()
+    if dev.type != "cuda":
+        raise ValueError(f"tensors must be on a CUDA device, got {dev}")
+    return torch.cuda.device(dev)
+
+
 def loglinear_fwd_workspace_bytes(shape: LLShape) -> int:
     return int(lib().loglinear_fwd_workspace_bytes(ctypes.byref(shape)))
 
@@ -167,10 +181,11 @@ def loglinear_fwd(q, k, v, a, lam, chunk: int = 64, o=None, workspace=None, stat
     for x in (q, k, v, a, lam, o):
         if not x.is_contiguous():
             raise ValueError("all tensors must be contiguous")
-    st = lib().loglinear_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(lam),
-                             _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                             _ptr(states_out), _ptr(state_logscale_out), int(state_levels),
-                             _stream_ptr(stream))
+    with _on_device(q, k, v, a, lam, o, workspace, states_out, state_logscale_out):
+        st = lib().loglinear_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(lam),
+                                 _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _ptr(states_out), _ptr(state_logscale_out), int(state_levels),
+                                 _stream_ptr(stream))
     _check(st, "loglinear_fwd")
     return o
 
@@ -187,11 +202,12 @@ def loglinear_fwd_profiled(q, k, v, a, lam, events, chunk: int = 64, o=None, wor
         workspace = torch.empty(loglinear_fwd_workspace_bytes(shape), dtype=torch.uint8,
                                 device=q.device)
     arr = (_vp * len(events))(*[e.cuda_event for e in events])
-    st = lib().loglinear_fwd_profiled(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
-                                      _ptr(lam), _ptr(o), _ptr(workspace),
-                                      workspace.numel() * workspace.element_size(),
-                                      _ptr(states_out), _ptr(state_logscale_out),
-                                      int(state_levels), _stream_ptr(stream), arr, len(events))
+    with _on_device(q, k, v, a, lam, o, workspace, states_out, state_logscale_out):
+        st = lib().loglinear_fwd_profiled(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                          _ptr(lam), _ptr(o), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          _ptr(states_out), _ptr(state_logscale_out),
+                                          int(state_levels), _stream_ptr(stream), arr, len(events))
     _check(st, "loglinear_fwd_profiled")
     return o
 
@@ -207,10 +223,11 @@ def loglinear_fwd_static_workspace(q, k, v, a, lam, chunk: int = 64, o=None, sta
     shape = fwd_shape(q, v, lam, chunk)
     if o is None:
         o = torch.empty_like(v)
-    st = lib().loglinear_fwd_static_workspace(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
-                                              _ptr(a), _ptr(lam), _ptr(o), _ptr(states_out),
-                                              _ptr(state_logscale_out), int(state_levels),
-                                              _stream_ptr(stream))
+    with _on_device(q, k, v, a, lam, o, states_out, state_logscale_out):
+        st = lib().loglinear_fwd_static_workspace(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                                  _ptr(a), _ptr(lam), _ptr(o), _ptr(states_out),
+                                                  _ptr(state_logscale_out), int(state_levels),
+                                                  _stream_ptr(stream))
     _check(st, "loglinear_fwd_static_workspace")
     return o
 
@@ -223,9 +240,10 @@ def loglinear_gdn_fwd(q, k, v, a, beta, lam, chunk: int = 64, o=None, workspace=
     nb = int(lib().loglinear_gdn_fwd_workspace_bytes(ctypes.byref(shape)))
     if workspace is None:
         workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
-    st = lib().loglinear_gdn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta),
-                                 _ptr(lam), _ptr(o), _ptr(workspace), workspace.numel(),
-                                 _stream_ptr(stream))
+    with _on_device(q, k, v, a, beta, lam, o, workspace):
+        st = lib().loglinear_gdn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta),
+                                     _ptr(lam), _ptr(o), _ptr(workspace), workspace.numel(),
+                                     _stream_ptr(stream))
     _check(st, "loglinear_gdn_fwd")
     return o
 
@@ -240,9 +258,10 @@ def loglinear_bwd(q, k, v, a, lam, dO, chunk: int = 64, workspace=None, stream=N
     nb = int(lib().loglinear_bwd_workspace_bytes(ctypes.byref(shape)))
     if workspace is None:
         workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
-    st = lib().loglinear_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(lam),
-                             _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dloga), _ptr(dlam),
-                             _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    with _on_device(q, k, v, a, lam, dO, dq, dk, dv, dloga, dlam, workspace):
+        st = lib().loglinear_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(lam),
+                                 _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dloga), _ptr(dlam),
+                                 _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check(st, "loglinear_bwd")
     return dq, dk, dv, dloga, dlam
 
@@ -256,9 +275,10 @@ def loglinear_fwd_naive(q, k, v, a, lam, chunk: int = 64, o=None, workspace=None
     nb = int(lib().loglinear_fwd_naive_workspace_bytes(ctypes.byref(shape)))
     if workspace is None:
         workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
-    st = lib().loglinear_fwd_naive(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
-                                   _ptr(lam), _ptr(o), _ptr(workspace), workspace.numel(),
-                                   _stream_ptr(stream))
+    with _on_device(q, k, v, a, lam, o, workspace):
+        st = lib().loglinear_fwd_naive(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                       _ptr(lam), _ptr(o), _ptr(workspace), workspace.numel(),
+                                       _stream_ptr(stream))
     _check(st, "loglinear_fwd_naive")
     return o
 
@@ -274,8 +294,9 @@ def ssd_fwd(q, k, v, a, chunk: int = 64, o=None, workspace=None, stream=None):
     nb = int(lib().ssd_fwd_workspace_bytes(ctypes.byref(shape)))
     if workspace is None:
         workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
-    st = lib().ssd_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o),
-                       _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    with _on_device(q, k, v, a, o, workspace):
+        st = lib().ssd_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o),
+                           _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check(st, "ssd_fwd")
     return o
 
@@ -300,9 +321,10 @@ def loglinear_decode_step(pos: int, q_t, k_t, v_t, a_t, lam_t, states, state_log
     shape = make_shape(B, 1, H, H // G, dk, dv, 16, L, q_t.dtype)
     if o_t is None:
         o_t = torch.empty_like(v_t)
-    st = lib().loglinear_decode_step(ctypes.byref(shape), int(pos), _ptr(q_t), _ptr(k_t),
-                                     _ptr(v_t), _ptr(a_t), _ptr(lam_t), _ptr(o_t), _ptr(states),
-                                     _ptr(state_logscale), _stream_ptr(stream))
+    with _on_device(q_t, k_t, v_t, a_t, lam_t, o_t, states, state_logscale):
+        st = lib().loglinear_decode_step(ctypes.byref(shape), int(pos), _ptr(q_t), _ptr(k_t),
+                                         _ptr(v_t), _ptr(a_t), _ptr(lam_t), _ptr(o_t), _ptr(states),
+                                         _ptr(state_logscale), _stream_ptr(stream))
     _check(st, "loglinear_decode_step")
     return o_t
 
@@ -315,9 +337,10 @@ def loglinear_fwd_host(q, k, v, a, lam, o, arena, chunk: int = 64, stream=None):
     """End-to-end forward from host tensors (pinned for async copies) into host o,
     using the device buffer `arena`; enqueued on `stream`, the caller synchronises."""
     shape = fwd_shape(q, v, lam, chunk)
-    st = lib().loglinear_fwd_host(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
-                                  _ptr(lam), _ptr(o), _ptr(arena),
-                                  arena.numel() * arena.element_size(), _stream_ptr(stream))
+    with _on_device(arena):
+        st = lib().loglinear_fwd_host(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                      _ptr(lam), _ptr(o), _ptr(arena),
+                                      arena.numel() * arena.element_size(), _stream_ptr(stream))
     _check(st, "loglinear_fwd_host")
     return o
 

@@ -183,6 +183,9 @@ struct HostPipe {
   cudaEvent_t start = nullptr, done = nullptr;
   cudaEvent_t ein[kHostPieces] = {}, eout[kHostPieces] = {};
   bool ready = false;
+  // Held for the whole enqueue of one call: the events are re-recorded by every call, so
+  // a second thread must not record them between this call's record and its wait.
+  std::mutex call_mu;
 };
 std::mutex g_pipe_mu;
 HostPipe g_pipe[128];
@@ -237,6 +240,7 @@ ll_status loglinear_fwd_host(const ll_shape* s, const void* q_host, const void* 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   HostPipe* hp = host_pipe();
   if (!hp) return LL_ERR_CUDA;
+  std::lock_guard<std::mutex> call_lock(hp->call_mu);
   // Pipeline over pieces of the batch (consecutive batch elements; every tensor is
   // batch-major, so a piece is one contiguous slice of each): the input copies of piece
   // i + 1 run on hp->in while piece i computes on `stream` and piece i - 1's output

@@ -34,10 +34,20 @@ def errors(got, ref, dtype="bf16"):
     return float(rel), mx, rms
 
 
+def raw_max_err(got, ref) -> float:
+    """max |got - ref| with nothing charged for the output cast."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.abs(got - ref).max()) if ref.size else 0.0
+
+
 def assert_parity(got, ref, what="", dtype="bf16"):
     assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), f"{what}: non-finite output"
     rel, mx, rms = errors(got, ref, dtype)
-    assert rel <= REL_L2 and mx <= MAX_REL_RMS * rms, (
-        f"{what}: rel_l2={rel:.3e} (<= {REL_L2}), max_err-cast={mx:.3e} "
-        f"(<= {MAX_REL_RMS}*rms={MAX_REL_RMS * rms:.3e})")
+    if not (rel <= REL_L2 and mx <= MAX_REL_RMS * rms):
+        raw = raw_max_err(got, ref)
+        raise AssertionError(
+            f"{what}: rel_l2={rel:.3e} (<= {REL_L2}), max_err-cast={mx:.3e} "
+            f"(<= {MAX_REL_RMS}*rms={MAX_REL_RMS * rms:.3e}); raw max|err|={raw:.3e} = "
+            f"{raw / rms if rms > 0 else float('inf'):.3e}*rms")
     return rel, mx, rms
