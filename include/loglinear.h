@@ -189,6 +189,84 @@ ll_status loglinear_fwd_static_workspace(const ll_shape* shape, const void* q, c
                                          void* o, float* states_out, float* state_logscale_out,
                                          int state_levels, void* stream);
 
+/* ---- sequence segments -------------------------------------------------------------------
+ * A forward can start at a position T0 > 0 from the bucket memories there, and those
+ * memories can be built from the memories of whole earlier segments.  This is what a
+ * sequence split over several devices needs (each holds one segment of 2^p tokens; one
+ * all-gather of the segments' memories and summed log-decays lets every segment form the
+ * buckets of its start), and what a prefill in pieces needs.  Sources: the per-bucket
+ * memories of the write-up (section 特殊结构：树划分, Fig. 2) and the combination of the
+ * memories of pieces level by level (section 高效训练算法, Algorithm 1).
+ *
+ * Bucket memories use the decode step's format: (B, H, levels, d_k, d_v) fp32 blocks with
+ * (B, H, levels) fp32 log-scales; the memory of level l is exp(logscale[l]) * block[l];
+ * level l >= 1 is live at a position p when bit l-1 of p is set, and the block holds
+ * sum over the bucket of M^S(p-1, s) k_s v_sᵀ.  Slots of levels that are not live hold
+ * unspecified values and are neither read nor written.
+ */
+
+/* Bytes of workspace loglinear_fwd_continue needs (0: invalid shape or start). */
+size_t loglinear_fwd_continue_workspace_bytes(const ll_shape* shape, long long T0);
+
+/*
+ * Forward over the tokens at positions T0 .. T0+T-1 (T = shape->T), given the bucket
+ * memories at T0.  q, k, v, a, lambda and o hold the segment's T tokens, laid out as for
+ * loglinear_fwd; lambda's levels are absolute (level l of every bucket, near or far), so
+ * shape->levels must be >= bit_length(T0 + T - 1) + 1.
+ *   T0               >= 0 and a multiple of the smallest power of two >= T (then every
+ *                    bucket of a position in the segment lies either inside the segment
+ *                    or before T0, where it is a bucket of T0); else LL_ERR_SHAPE
+ *   prefix_states    (B, H, prefix_levels, d_k, d_v) fp32, the memories at T0 (read);
+ *   prefix_logscale  (B, H, prefix_levels) fp32; both may be NULL when T0 == 0
+ *   prefix_levels    >= bit_length(T0) + 1, <= 64
+ *   states_out       NULL, or (B, H, state_levels, d_k, d_v): the memories at T0 + T
+ *                    (written with zero log-scales into state_logscale_out if given), the
+ *                    live levels only; may be the same buffer as prefix_states (then with
+ *                    state_levels == prefix_levels, and state_logscale_out may be
+ *                    prefix_logscale): a decode or a further continuation goes on from it
+ *   state_levels     >= bit_length(T0 + T) + 1 when states_out is given
+ *   workspace        >= loglinear_fwd_continue_workspace_bytes(shape, T0) bytes
+ * With T0 == 0 this is loglinear_fwd.  The shapes of loglinear_fwd run on the same paths
+ * (tensor cores for bf16, d_k = 128, d_v = 64, T % 128 == 0; the CUDA cores otherwise).
+ */
+ll_status loglinear_fwd_continue(const ll_shape* shape, long long T0, const void* q, const void* k,
+                                 const void* v, const float* a, const float* lambda,
+                                 const float* prefix_states, const float* prefix_logscale,
+                                 int prefix_levels, void* o, void* workspace, size_t workspace_bytes,
+                                 float* states_out, float* state_logscale_out, int state_levels,
+                                 void* stream);
+
+/* Bytes of workspace loglinear_segment_total needs (0: invalid shape; shape->levels is
+ * ignored). */
+size_t loglinear_segment_total_workspace_bytes(const ll_shape* shape);
+
+/*
+ * The memory of a whole segment of T tokens and the decay it applies to everything
+ * before it:
+ *   total_state     (B, H, d_k, d_v) fp32: sum over s < T of M^S(T-1, s) k_s v_sᵀ
+ *   total_logdecay  (B, H) fp32: sum over t < T of ln a_t
+ * k, v, a as for loglinear_fwd (no q or lambda).  shape->levels is ignored.
+ */
+ll_status loglinear_segment_total(const ll_shape* shape, const void* k, const void* v, const float* a,
+                                  void* workspace, size_t workspace_bytes, float* total_state,
+                                  float* total_logdecay, void* stream);
+
+/*
+ * The bucket memories at T0 = n_segments * T (T = shape->T, a power of two: every bucket
+ * of T0 is then made of whole segments) from the memories of the n_segments segments
+ * before it, as loglinear_segment_total returns them:
+ *   seg_states     (n_segments, B, H, d_k, d_v) fp32, segment 0 first
+ *   seg_logdecay   (n_segments, B, H) fp32
+ *   states_out     (B, H, state_levels, d_k, d_v): the levels live at T0 are written;
+ *   state_logscale_out NULL or (B, H, state_levels): zeros at those levels
+ *   state_levels   >= bit_length(T0) + 1, <= 64
+ * n_segments <= 64.  Uses shape->batch, heads, d_k, d_v and T.  Nothing is enqueued for
+ * n_segments == 0 (position 0 has no buckets).
+ */
+ll_status loglinear_prefix_states(const ll_shape* shape, int n_segments, const float* seg_states,
+                                  const float* seg_logdecay, float* states_out,
+                                  float* state_logscale_out, int state_levels, void* stream);
+
 /* ---- log-linear Gated DeltaNet -----------------------------------------------------------
  * The write-up extends Gated DeltaNet the same way (section 对Mamba-2和门控的对数线性推广):
  * the model's own transition, the gated delta rule

@@ -10,6 +10,10 @@ Functions mirror the C names:
   bucket states at position T)
 * ``loglinear_decode_step(pos, q_t, k_t, v_t, a_t, lam_t, states, state_logscale)`` -> o_t
 * ``loglinear_fwd_host(...)`` end-to-end from host (pinned) tensors
+* ``loglinear_fwd_continue``, ``loglinear_segment_total``, ``loglinear_prefix_states``:
+  a forward that starts from the bucket memories at a position T0, and the pieces that
+  build those memories from whole earlier segments (see ``sharded`` for a sequence split
+  over ranks)
 * ``loglinear_fwd_workspace_bytes``, ``loglinear_fwd_path``, ``loglinear_check_status``,
   ``loglinear_selftest_wait_timeout``, ``loglinear_status_string``
 """
@@ -103,6 +107,17 @@ def lib() -> ctypes.CDLL:
             L.loglinear_gdn_fwd.argtypes = [_SP] + [_vp] * 8 + [ctypes.c_size_t, _vp]
             L.ssd_fwd.restype = ctypes.c_int
             L.ssd_fwd.argtypes = [_SP] + [_vp] * 6 + [ctypes.c_size_t, _vp]
+            L.loglinear_fwd_continue_workspace_bytes.restype = ctypes.c_size_t
+            L.loglinear_fwd_continue_workspace_bytes.argtypes = [_SP, ctypes.c_longlong]
+            L.loglinear_fwd_continue.restype = ctypes.c_int
+            L.loglinear_fwd_continue.argtypes = ([_SP, ctypes.c_longlong] + [_vp] * 7 + [ctypes.c_int] +
+                                                 [_vp, _vp, ctypes.c_size_t, _vp, _vp, ctypes.c_int, _vp])
+            L.loglinear_segment_total_workspace_bytes.restype = ctypes.c_size_t
+            L.loglinear_segment_total_workspace_bytes.argtypes = [_SP]
+            L.loglinear_segment_total.restype = ctypes.c_int
+            L.loglinear_segment_total.argtypes = [_SP] + [_vp] * 4 + [ctypes.c_size_t, _vp, _vp, _vp]
+            L.loglinear_prefix_states.restype = ctypes.c_int
+            L.loglinear_prefix_states.argtypes = [_SP, ctypes.c_int] + [_vp] * 4 + [ctypes.c_int, _vp]
             _lib = L
     return _lib
 
@@ -299,6 +314,74 @@ def ssd_fwd(q, k, v, a, chunk: int = 64, o=None, workspace=None, stream=None):
                            _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check(st, "ssd_fwd")
     return o
+
+
+def loglinear_fwd_continue(q, k, v, a, lam, T0: int, prefix_states=None, prefix_logscale=None,
+                           chunk: int = 64, o=None, workspace=None, states_out=None,
+                           state_logscale_out=None, state_levels: int = 0, stream=None):
+    """Forward over the positions T0 .. T0+T-1 (the segment's tensors, laid out as for
+    loglinear_fwd, lambda with absolute levels) from the bucket memories at T0:
+    prefix_states (B, H, Lp, d_k, d_v) fp32 and prefix_logscale (B, H, Lp) fp32.  T0 must
+    be a multiple of the smallest power of two >= T.  states_out (may be prefix_states)
+    receives the memories at T0 + T."""
+    shape = fwd_shape(q, v, lam, chunk)
+    if o is None:
+        o = torch.empty_like(v)
+    nb = int(lib().loglinear_fwd_continue_workspace_bytes(ctypes.byref(shape), int(T0)))
+    if nb == 0:
+        raise LogLinearError(2, "loglinear_fwd_continue_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(nb, dtype=torch.uint8, device=q.device)
+    Lp = 0 if prefix_states is None else prefix_states.shape[2]
+    with _on_device(q, k, v, a, lam, o, workspace, prefix_states, prefix_logscale, states_out,
+                    state_logscale_out):
+        st = lib().loglinear_fwd_continue(ctypes.byref(shape), int(T0), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                          _ptr(lam), _ptr(prefix_states), _ptr(prefix_logscale), int(Lp),
+                                          _ptr(o), _ptr(workspace), workspace.numel(), _ptr(states_out),
+                                          _ptr(state_logscale_out), int(state_levels), _stream_ptr(stream))
+    _check(st, "loglinear_fwd_continue")
+    return o
+
+
+def loglinear_segment_total(k, v, a, chunk: int = 64, workspace=None, stream=None):
+    """The memory of the whole segment held by k, v, a ((B, T, G, d_k), (B, T, H, d_v),
+    (B, T, H)): returns total_state (B, H, d_k, d_v) fp32 and total_logdecay (B, H) fp32."""
+    B, T, G, dk = k.shape
+    H, dv = v.shape[2], v.shape[3]
+    shape = make_shape(B, T, H, H // G, dk, dv, chunk, max(1, (T - 1).bit_length() + 1), k.dtype)
+    nb = int(lib().loglinear_segment_total_workspace_bytes(ctypes.byref(shape)))
+    if nb == 0:
+        raise LogLinearError(2, "loglinear_segment_total_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(nb, dtype=torch.uint8, device=k.device)
+    total = torch.empty((B, H, dk, dv), dtype=torch.float32, device=k.device)
+    logdecay = torch.empty((B, H), dtype=torch.float32, device=k.device)
+    with _on_device(k, v, a, workspace, total, logdecay):
+        st = lib().loglinear_segment_total(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(a), _ptr(workspace),
+                                           workspace.numel(), _ptr(total), _ptr(logdecay), _stream_ptr(stream))
+    _check(st, "loglinear_segment_total")
+    return total, logdecay
+
+
+def loglinear_prefix_states(seg_states, seg_logdecay, seg_len: int, state_levels: int, states_out=None,
+                            state_logscale_out=None, stream=None):
+    """Bucket memories at T0 = n * seg_len from the memories of the n segments before it:
+    seg_states (n, B, H, d_k, d_v) and seg_logdecay (n, B, H), fp32.  Returns states
+    (B, H, state_levels, d_k, d_v) and log-scales (B, H, state_levels); only the levels
+    live at T0 are written (zero log-scales there)."""
+    n, B, H, dk, dv = seg_states.shape
+    dev = seg_states.device
+    if states_out is None:
+        states_out = torch.zeros((B, H, state_levels, dk, dv), dtype=torch.float32, device=dev)
+    if state_logscale_out is None:
+        state_logscale_out = torch.zeros((B, H, state_levels), dtype=torch.float32, device=dev)
+    shape = make_shape(B, seg_len, H, 1, dk, dv, 16, 1, LL_F32)
+    with _on_device(seg_states, seg_logdecay, states_out, state_logscale_out):
+        st = lib().loglinear_prefix_states(ctypes.byref(shape), int(n), _ptr(seg_states), _ptr(seg_logdecay),
+                                           _ptr(states_out), _ptr(state_logscale_out), int(state_levels),
+                                           _stream_ptr(stream))
+    _check(st, "loglinear_prefix_states")
+    return states_out, state_logscale_out
 
 
 def loglinear_fwd_kernel_names(shape: LLShape, with_export: bool = False):

@@ -389,6 +389,202 @@ ll_status loglinear_bwd(const ll_shape* s, const void* q, const void* k, const v
   return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
+}  // extern "C"
+
+// ---- sequence segments -----------------------------------------------------------------
+
+namespace {
+
+// Layout of a continuation's workspace after the forward's own: the tensor-core path's
+// images of the prefix memories, the segment's export at its end, its summed ln-decay.
+struct ContLayout {
+  size_t fwd, pre, loc, segg, bytes;
+  int npre, SLloc;
+};
+
+bool cont_layout(const ll_shape* s, long long T0, ContLayout* c) {
+  const size_t f = loglinear_fwd_workspace_bytes(s);
+  if (!f) return false;
+  const size_t BH = (size_t)s->batch * s->heads, S = (size_t)s->d_k * s->d_v;
+  c->npre = __builtin_popcountll((unsigned long long)(T0 > 0 ? T0 : 0));
+  c->SLloc = ll::bit_length(s->T) + 1;
+  size_t o = a256(f);
+  c->fwd = 0;
+  c->pre = o;
+  if (ll::tc_supported(*s)) {
+    ll::TcPlan tp;
+    if (!ll::make_tc_plan(*s, &tp)) return false;
+    o += a256(ll::tc_prefix_bytes(tp, c->npre));
+  }
+  c->loc = o;
+  o += a256(BH * c->SLloc * S * sizeof(float));
+  c->segg = o;
+  o += a256(BH * sizeof(float));
+  c->bytes = o;
+  return true;
+}
+
+// T0 is a multiple of the smallest power of two >= T: then every bucket of a position
+// in [T0, T0 + T) lies either before T0 (a bucket of T0) or inside the segment.
+bool aligned_start(long long T0, int T) {
+  const long long p2 = 1LL << ll::bit_length((long long)T - 1);
+  return T0 >= 0 && T0 % p2 == 0;
+}
+
+ll_status check_continue(const ll_shape* s, long long T0) {
+  ll_status st = check_fwd_shape(s);
+  if (st != LL_OK) return st;
+  if (T0 < 0 || T0 > (1LL << 40) || !aligned_start(T0, s->T)) return LL_ERR_SHAPE;
+  if (s->levels < ll::bit_length(T0 + s->T - 1) + 1) return LL_ERR_SHAPE;
+  return LL_OK;
+}
+
+// A shape for the kernels that read no lambda: the smallest valid level count.
+ll_shape no_lambda(const ll_shape* s) {
+  ll_shape t = *s;
+  if (t.T >= 1) t.levels = ll::bit_length(t.T - 1) + 1;
+  return t;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t loglinear_fwd_continue_workspace_bytes(const ll_shape* s, long long T0) {
+  ContLayout c;
+  if (check_continue(s, T0) != LL_OK || !cont_layout(s, T0, &c)) return 0;
+  return c.bytes;
+}
+
+ll_status loglinear_fwd_continue(const ll_shape* s, long long T0, const void* q, const void* k,
+                                 const void* v, const float* a, const float* lambda,
+                                 const float* prefix_states, const float* prefix_logscale,
+                                 int prefix_levels, void* o, void* workspace, size_t workspace_bytes,
+                                 float* states_out, float* state_logscale_out, int state_levels,
+                                 void* stream) {
+  ll_status st = check_continue(s, T0);
+  if (st != LL_OK) return st;
+  if (!q || !k || !v || !a || !lambda || !o) return LL_ERR_NULL;
+  if (T0 > 0) {
+    if (!prefix_states || !prefix_logscale) return LL_ERR_NULL;
+    if (prefix_levels < ll::bit_length(T0) + 1 || prefix_levels > 64) return LL_ERR_SHAPE;
+    if (!aligned16(prefix_states)) return LL_ERR_ALIGN;
+  }
+  if (states_out) {
+    if (state_levels < ll::bit_length(T0 + s->T) + 1 || state_levels > 64) return LL_ERR_SHAPE;
+    if (!aligned16(states_out)) return LL_ERR_ALIGN;
+    if (T0 > 0 && (const void*)states_out == (const void*)prefix_states && state_levels != prefix_levels)
+      return LL_ERR_SHAPE;  // in place only with one layout
+  }
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) || !aligned16(lambda) ||
+      !aligned16(o))
+    return LL_ERR_ALIGN;
+  ContLayout c;
+  if (!cont_layout(s, T0, &c)) return LL_ERR_SHAPE;
+  if (!workspace || workspace_bytes < c.bytes) return LL_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return LL_ERR_ALIGN;
+  if (T0 == 0)
+    return fwd_impl(s, q, k, v, a, lambda, o, workspace, workspace_bytes, states_out, state_logscale_out,
+                    state_levels, stream, nullptr, 0);
+  unsigned* sw = status_word();
+  if (!sw) return LL_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  float* loc = reinterpret_cast<float*>(ws + c.loc);
+  float* segg = reinterpret_cast<float*>(ws + c.segg);
+  ll::FwdArgs fa{q, k, v, a, lambda, o, ws, states_out ? loc : nullptr, nullptr, c.SLloc, sw, nullptr, 0};
+  fa.T0 = T0;
+  fa.pre_st = prefix_states;
+  fa.pre_lsc = prefix_logscale;
+  fa.pre_levels = prefix_levels;
+  fa.pre_ws = ws + c.pre;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (ll::tc_supported(*s)) {
+    ll::TcPlan tp;
+    if (!ll::make_tc_plan(*s, &tp)) return LL_ERR_SHAPE;
+    e = ll::launch_tc_fwd(tp, fa, cs);
+  } else {
+    ll::GenPlan p;
+    if (!ll::make_gen_plan(*s, &p)) return LL_ERR_SHAPE;
+    e = ll::launch_generic_fwd(p, s->dtype == LL_BF16, fa, cs);
+  }
+  if (e != cudaSuccess) return LL_ERR_CUDA;
+  if (states_out) {
+    const int BH = s->batch * s->heads, S = s->d_k * s->d_v;
+    if (ll::launch_seg_logdecay(a, s->batch, s->T, s->heads, segg, cs) != cudaSuccess ||
+        ll::launch_continue_export(T0, s->T, BH, prefix_states, prefix_logscale, prefix_levels, loc, c.SLloc,
+                                   segg, S, states_out, state_logscale_out, state_levels, cs) != cudaSuccess)
+      return LL_ERR_CUDA;
+  }
+  return LL_OK;
+}
+
+size_t loglinear_segment_total_workspace_bytes(const ll_shape* s) {
+  if (!s) return 0;
+  const ll_shape t = no_lambda(s);
+  ContLayout c;
+  if (check_fwd_shape(&t) != LL_OK || !cont_layout(&t, 0, &c)) return 0;
+  return c.bytes;
+}
+
+ll_status loglinear_segment_total(const ll_shape* s, const void* k, const void* v, const float* a,
+                                  void* workspace, size_t workspace_bytes, float* total_state,
+                                  float* total_logdecay, void* stream) {
+  if (!s) return LL_ERR_NULL;
+  const ll_shape t = no_lambda(s);
+  ll_status st = check_fwd_shape(&t);
+  if (st != LL_OK) return st;
+  if (!k || !v || !a || !total_state || !total_logdecay) return LL_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(a) || !aligned16(total_state)) return LL_ERR_ALIGN;
+  ContLayout c;
+  if (!cont_layout(&t, 0, &c)) return LL_ERR_SHAPE;
+  if (!workspace || workspace_bytes < c.bytes) return LL_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return LL_ERR_ALIGN;
+  unsigned* sw = status_word();
+  if (!sw) return LL_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  float* loc = reinterpret_cast<float*>(ws + c.loc);
+  // the export needs no q, lambda or o; k stands in for q where a tensor map is built
+  ll::FwdArgs fa{k, k, v, a, nullptr, nullptr, ws, loc, nullptr, c.SLloc, sw, nullptr, 0};
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (ll::tc_supported(t)) {
+    ll::TcPlan tp;
+    if (!ll::make_tc_plan(t, &tp)) return LL_ERR_SHAPE;
+    e = ll::launch_tc_export_only(tp, fa, cs);
+  } else {
+    ll::GenPlan p;
+    if (!ll::make_gen_plan(t, &p)) return LL_ERR_SHAPE;
+    e = ll::launch_generic_export_only(p, t.dtype == LL_BF16, fa, cs);
+  }
+  const int BH = t.batch * t.heads, S = t.d_k * t.d_v;
+  if (e != cudaSuccess || ll::launch_sum_live_levels(loc, BH, c.SLloc, t.T, S, total_state, cs) != cudaSuccess ||
+      ll::launch_seg_logdecay(a, t.batch, t.T, t.heads, total_logdecay, cs) != cudaSuccess)
+    return LL_ERR_CUDA;
+  return LL_OK;
+}
+
+ll_status loglinear_prefix_states(const ll_shape* s, int n_segments, const float* seg_states,
+                                  const float* seg_logdecay, float* states_out,
+                                  float* state_logscale_out, int state_levels, void* stream) {
+  if (!s) return LL_ERR_NULL;
+  ll_status st = check_common(s);
+  if (st != LL_OK) return st;
+  if (s->T < 1 || (s->T & (s->T - 1)) || n_segments < 0 || n_segments > 64) return LL_ERR_SHAPE;
+  const long long T0 = (long long)n_segments * s->T;
+  if (state_levels < ll::bit_length(T0) + 1 || state_levels > 64) return LL_ERR_SHAPE;
+  if (n_segments == 0) return LL_OK;
+  if (!seg_states || !seg_logdecay || !states_out) return LL_ERR_NULL;
+  if (!aligned16(seg_states) || !aligned16(states_out)) return LL_ERR_ALIGN;
+  const int BH = s->batch * s->heads, S = s->d_k * s->d_v;
+  const int seg_log = ll::bit_length(s->T) - 1;
+  return ll::launch_prefix_from_segments(n_segments, seg_log, BH, seg_states, seg_logdecay, S, states_out,
+                                         state_logscale_out, state_levels,
+                                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LL_OK
+             : LL_ERR_CUDA;
+}
+
 ll_status loglinear_check_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LL_ERR_CUDA;
   unsigned v = 0, zero = 0;

@@ -168,6 +168,16 @@ __global__ void __launch_bounds__(kThreads) gen_output(GenPlan p, int QT, const 
       acc += w * dot;
       D += blkG[bidx];
     }
+    // continuation: the live levels of the start position, whose memories lie before every
+    // chunk of the segment (D now spans the chunks 0 .. j-1) and carry their own log-scale
+    for (int ip = 0; ip < p.npre; ++ip) {
+      const int lv = p.prelev[ip];
+      const float* Sp = p.pre_st + ((size_t)bh * p.Lp + lv) * S;
+      const float w = ls[r * L + lv] * exp2f(gs[t] + D + p.pre_lsc[(size_t)bh * p.Lp + lv] * 1.4426950408889634f);
+      float dot = 0.f;
+      for (int i = 0; i < dk; ++i) dot += qs[r * dk + i] * Sp[i * dv + jv];
+      acc += w * dot;
+    }
     ll_store(o, (((size_t)b * p.T + t0 + t) * p.H + h) * dv + jv, acc);
   }
 }
@@ -197,7 +207,17 @@ __global__ void __launch_bounds__(kThreads) gen_export(GenPlan p, int SL, const 
 }
 
 template <typename TIn>
-cudaError_t run(const GenPlan& p, const FwdArgs& a, cudaStream_t st, bool states_only = false) {
+cudaError_t run(const GenPlan& p0, const FwdArgs& a, cudaStream_t st, bool states_only = false,
+                bool export_only = false) {
+  GenPlan p = p0;
+  p.npre = 0;
+  if (a.T0 > 0) {  // continuation: the live levels of the start position
+    for (int l = 1; l <= 62 && p.npre < 32; ++l)
+      if ((a.T0 >> (l - 1)) & 1) p.prelev[p.npre++] = l;
+    p.Lp = a.pre_levels;
+    p.pre_st = a.pre_st;
+    p.pre_lsc = a.pre_lsc;
+  }
   const int BH = p.B * p.H;
   size_t sm1 = sizeof(float) * ((size_t)p.C * p.dk + (size_t)p.C * p.dv + p.C);
   cudaError_t e = cudaFuncSetAttribute(gen_chunk_state<TIn>,
@@ -211,6 +231,14 @@ cudaError_t run(const GenPlan& p, const FwdArgs& a, cudaStream_t st, bool states
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch(a, 1, st);
   if (states_only) return cudaSuccess;
+  if (export_only) {
+    if (!a.states_out) return cudaErrorInvalidValue;
+    gen_export<<<dim3(a.state_levels, BH), kThreads, 0, st>>>(p, a.state_levels, a.ws, a.states_out,
+                                                             a.logscale_out);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launch();
+    return cudaSuccess;
+  }
   const int QT = p.C < 32 ? p.C : 32;
   size_t sm3 = sizeof(float) * ((size_t)QT * p.dk + (size_t)p.C * p.dk + (size_t)p.C * p.dv + p.C +
                                 (size_t)QT * p.C + (size_t)QT * p.L);
@@ -266,6 +294,10 @@ bool make_gen_plan(const ll_shape& s, GenPlan* p) {
   p->off_blkG = o;
   o = align256(o + sizeof(float) * BH * p->nblk);
   p->bytes = o;
+  p->npre = 0;
+  p->Lp = 0;
+  p->pre_st = nullptr;
+  p->pre_lsc = nullptr;
   return true;
 }
 
@@ -275,6 +307,10 @@ cudaError_t launch_generic_fwd(const GenPlan& p, bool bf16, const FwdArgs& a, cu
 
 cudaError_t launch_generic_states(const GenPlan& p, bool bf16, const FwdArgs& a, cudaStream_t st) {
   return bf16 ? run<__nv_bfloat16>(p, a, st, true) : run<float>(p, a, st, true);
+}
+
+cudaError_t launch_generic_export_only(const GenPlan& p, bool bf16, const FwdArgs& a, cudaStream_t st) {
+  return bf16 ? run<__nv_bfloat16>(p, a, st, false, true) : run<float>(p, a, st, false, true);
 }
 
 }  // namespace ll

@@ -19,6 +19,13 @@ struct GenPlan {
   int nblk;                                    // Fenwick block states per (b, h)
   int blk_off[32];                             // first block of chunk level m
   size_t off_g, off_gamma, off_H, off_blk, off_blkG, bytes;
+  // continuation from the bucket memories at a start position (0 prefix levels otherwise):
+  // level prelev[i] of pre_st (B*H, Lp, dk, dv) with log-scale pre_lsc (B*H, Lp)
+  int npre;
+  int prelev[32];
+  int Lp;
+  const float* pre_st;
+  const float* pre_lsc;
 };
 
 bool make_gen_plan(const ll_shape& s, GenPlan* p);
@@ -37,6 +44,15 @@ struct FwdArgs {
   unsigned* status;
   void** events;  // optional: events[0] before the first kernel, events[i+1] after kernel i
   int n_events;
+  // continuation (loglinear_fwd_continue): the tokens are the positions T0 .. T0+T-1 and
+  // the terms of the bucket memories at T0 are added: pre_st (B*H, pre_levels, dk, dv)
+  // fp32 with log-scales pre_lsc (B*H, pre_levels); pre_ws holds the tensor-core path's
+  // fp16 images of them (tc_prefix_bytes).
+  long long T0;
+  const float* pre_st;
+  const float* pre_lsc;
+  int pre_levels;
+  char* pre_ws;
 };
 
 // Counts a kernel launch and records the profiling event that follows kernel `i`.
@@ -81,6 +97,18 @@ cudaError_t launch_decode(const DecodeArgs& d, bool bf16, cudaStream_t st);
 
 cudaError_t launch_wait_selftest(unsigned* status, long long spins, cudaStream_t st);
 
+// Sequence segments (csrc/segments.cu).
+cudaError_t launch_seg_logdecay(const float* a, int B, int T, int H, float* out, cudaStream_t st);
+cudaError_t launch_sum_live_levels(const float* stl, int BH, int SL, long long T, int S, float* total,
+                                   cudaStream_t st);
+cudaError_t launch_prefix_from_segments(int r, int seg_log, int BH, const float* seg_st, const float* seg_g,
+                                        int S, float* stl, float* lsc, int SL, cudaStream_t st);
+cudaError_t launch_continue_export(long long T0, long long T, int BH, const float* pst, const float* plsc, int Lp,
+                                   const float* loc, int SLloc, const float* segg, int S, float* stl, float* lsc,
+                                   int SL, cudaStream_t st);
+// Generic path: chunk states, Fenwick blocks and the export at position T only.
+cudaError_t launch_generic_export_only(const GenPlan& p, bool bf16, const FwdArgs& a, cudaStream_t st);
+
 // ---- tensor-core path (tcgen05) --------------------------------------------
 struct TcPlan {
   int B, T, H, hpg, G, L;
@@ -105,6 +133,10 @@ cudaError_t launch_tc_ssd(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
 const char* tc_kernel_names(bool with_export);
 // The forward's tree only (tile states, levels above), into a.ws laid out per p.
 cudaError_t launch_tc_nodes(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
+// The tree and the export of the memories at position T into a.states_out (no output).
+cudaError_t launch_tc_export_only(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
+// Bytes of the fp16 images of npre prefix memories per (b, h) (continuation).
+size_t tc_prefix_bytes(const TcPlan& p, int npre);
 // Backward, query side of the inter-tile levels on the tensor cores: adds into dq32,
 // assigns dlambda levels >= 8 of the set bits, adds the nodes' duals (dual slot of the
 // even node (m, i): dual_off[m] + i / 2, nslots per (b, h); dual zero before the first call).

@@ -40,6 +40,13 @@ struct TcParams {
   int lflags;      // bit 0: first pass (store), bit 1: last pass (write o)
   uint8_t* pimg;   // (B*H, NT, 16 KB) SSD prefix-state images
   unsigned* pmeta; // (B*H, NT, 4)
+  // continuation from the bucket memories at a start position T0 (level-fused mode only):
+  // npre live levels of T0, their levels (lambda columns) and their fp16 images, whose
+  // log2 decay is 0 (the memories are already decayed to T0 - 1)
+  int npre;
+  int prelev[32];
+  uint8_t* preimg;   // (B*H, npre, 16 KB)
+  unsigned* premeta; // (B*H, npre, 4)
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {

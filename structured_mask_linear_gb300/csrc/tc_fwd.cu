@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   float* sLam8 = reinterpret_cast<float*>(smem + 99840);   // 128 x 9: lambda levels 0..7 of row r
   float* sNode = reinterpret_cast<float*>(smem + 104448);  // 32 x 2: node scale exp. (bits), log2 decay
   float* sLamI = reinterpret_cast<float*>(smem + kOutFixed);  // [level index][row]: lambda_t^(8+m)
-  __shared__ __align__(8) uint64_t bar_ld, bar_s, bar_o, bar_e[3], bar_y[2], bar_yf[2];
+  __shared__ __align__(8) uint64_t bar_ld, bar_s, bar_o, bar_e[3], bar_y, bar_yf;
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[8];
   __shared__ int s_oi;  // role a -> all: the O MMA was issued
@@ -320,21 +320,30 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   const float* lrow = p.lam + (row * p.H + h) * p.L;
   // inter-tile levels of this tile, and whether the intra-tile part runs
   ptx::griddep_launch_dependents();  // the next launch may start once all CTAs are resident
-  const int nlev = kMode == 0 ? __popc((unsigned)u)
+  // Level indices 0 .. nloc-1 are the set bits of u (nearest first); in the level-fused
+  // mode the live levels of a start position T0 > 0 follow them (a forward that continues
+  // from the bucket memories at T0: those buckets lie before every bucket of the segment).
+  const int nloc = kMode == 0 ? __popc((unsigned)u)
                  : kMode == 1 ? (u > 0 ? 1 : 0)
                               : (p.lsel >= kLevIntra && ((u >> (p.lsel - kLevIntra)) & 1) ? 1 : 0);
+  const int nlev = nloc + (kMode == 0 ? p.npre : 0);
   const bool intra_on = kMode != 2 || p.lsel < kLevIntra;
   auto ebuf = [&](int k) { return k == 0 ? RE : RK + (k - 1) * 16384; };  // image buffer k
-  auto lev_of = [&](int i) {  // tile level m of level index i
+  auto lev_of = [&](int i) {  // tile level m of level index i < nloc
     return kMode == 2 ? p.lsel - kLevIntra : nth_set_bit((unsigned)u, i);
+  };
+  auto lam_col = [&](int i) {  // lambda column (token level) of level index i
+    return (kMode == 0 && i >= nloc) ? p.prelev[i - nloc] : kLevIntra + lev_of(i);
   };
   auto img_of = [&](int i) -> const uint8_t* {  // image read by level index i
     if (kMode == 1) return p.pimg + ((size_t)bh * p.NT + u) * kImgBytes;
+    if (kMode == 0 && i >= nloc) return p.preimg + ((size_t)bh * p.npre + (i - nloc)) * kImgBytes;
     const int m = lev_of(i);
     return p.img + (nbase + p.node_off[m] + ((u >> m) - 1)) * kImgBytes;
   };
   auto meta_of = [&](int i) -> const unsigned* {
     if (kMode == 1) return p.pmeta + ((size_t)bh * p.NT + u) * kMeta;
+    if (kMode == 0 && i >= nloc) return p.premeta + ((size_t)bh * p.npre + (i - nloc)) * kMeta;
     const int m = lev_of(i);
     return p.meta + (nbase + p.node_off[m] + ((u >> m) - 1)) * kMeta;
   };
@@ -349,10 +358,8 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     ptx::mbar_init(&bar_s, 1);
     ptx::mbar_init(&bar_o, 1);
     for (int i = 0; i < 3; ++i) ptx::mbar_init(&bar_e[i], 1);
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&bar_y[i], 1);
-      ptx::mbar_init(&bar_yf[i], 128);
-    }
+    ptx::mbar_init(&bar_y, 1);
+    ptx::mbar_init(&bar_yf, 128);
     ptx::fence_mbar_init();
     ptx::mbar_arrive_expect_tx(&bar_ld, intra_on ? 32768 * 2 + 16384 : 32768);
     ptx::tma_load_4d(RQ, &mapQ, &bar_ld, 0, g, (int)t0, b);
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     if (kMode == 1) {
       if (nlev > 0) sLamI[r] = 1.f;
     } else {
-      for (int i = 0; i < nlev; ++i) ptx::cp_async4(sLamI + i * 128 + r, lrow + kLevIntra + lev_of(i));
+      for (int i = 0; i < nlev; ++i) ptx::cp_async4(sLamI + i * 128 + r, lrow + lam_col(i));
     }
     // The tree that the previous launches built is read from here on.  The wait (at once
     // unless this grid was launched before they finished) and the node scalars' fetch
@@ -655,7 +662,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     };
     auto issue_pair = [&](int i) -> bool {
       const bool two = i + 1 < nlev;
-      if (i >= 2 && !wait_bar(&bar_yf[0], ((i >> 1) - 1) & 1)) return false;  // Y read by all
+      if (i >= 2 && !wait_bar(&bar_yf, ((i >> 1) - 1) & 1)) return false;  // Y read by all
       if (!wait_bar(&bar_e[i % 3], (i / 3) & 1)) return false;                 // images landed
       ++consumed;
       if (two) {
@@ -675,7 +682,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         ptx::umma_f16(tbase + 128, ptx::smem_desc_sw128(q0 + offq, 16, 1024),
                       ptx::smem_desc_sw128(e0 + kk * 2048, lbo, 1024), idesc, kk > 0);
       }
-      ptx::umma_commit(&bar_y[0]);
+      ptx::umma_commit(&bar_y);
       ++y_issued;
       return true;
     };
@@ -697,7 +704,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         okd = okd && issue_pair(i);
         if (!okd) atomicExch(p.status, kStatusTimeout);
       }
-      bool okw = wait_bar(&bar_y[0], (i >> 1) & 1);
+      bool okw = wait_bar(&bar_y, (i >> 1) & 1);
       if (!okw) atomicExch(p.status, kStatusTimeout);
       okw = __all_sync(0xffffffffu, okw);
       if (!okw) {
@@ -732,12 +739,12 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         D += sNode[2 * lv + 1];
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&bar_yf[0]);
+      ptx::mbar_arrive(&bar_yf);
     }
     if (driver) {
       // after a failed wait: let this CTA's own copies and MMAs land (bounded) before exit
       for (int j = consumed; j < issued; ++j) wait_bar(&bar_e[j % 3], (j / 3) & 1);
-      for (int j = y_seen; j < y_issued; ++j) wait_bar(&bar_y[0], j & 1);
+      for (int j = y_seen; j < y_issued; ++j) wait_bar(&bar_y, j & 1);
       if (s_issued) wait_bar(&bar_s, 0);
     }
     __syncthreads();  // join: P, its row scales and the O MMA have been issued
@@ -927,6 +934,33 @@ __global__ void __launch_bounds__(256) tc_export_kernel(TcParams p, int SL, floa
   }
 }
 
+// ---------------------------------------------------------------------------------
+// tc_prefix_publish: the bucket memories at a start position T0 (continuation) as node
+// images for tc_output: exp(log-scale) * memory, published like a tree node with log2
+// decay 0.  One CTA per (b, h, live level of T0); thread tid owns row tid.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) tc_prefix_publish_kernel(TcParams p, const float* pst, const float* plsc,
+                                                                int Lp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ float2 s_red2[4];
+  const int tid = threadIdx.x;
+  const int bh = blockIdx.x / p.npre, j = blockIdx.x % p.npre;
+  const int lvl = p.prelev[j];
+  const float sc = expf(plsc[(size_t)bh * Lp + lvl]);
+  const float4* src = reinterpret_cast<const float4*>(pst + ((size_t)bh * Lp + lvl) * (kDk * kDv) + tid * kDv);
+  float cur[kDv];
+#pragma unroll
+  for (int c = 0; c < kDv / 4; ++c) {
+    const float4 x = src[c];
+    cur[4 * c] = sc * x.x;
+    cur[4 * c + 1] = sc * x.y;
+    cur[4 * c + 2] = sc * x.z;
+    cur[4 * c + 3] = sc * x.w;
+  }
+  publish_node(cur, stage, (size_t)bh * p.npre + j, 0.f, s_red2, p.preimg, p.premeta);
+}
+
 __global__ void wait_selftest_kernel(unsigned* status, long long spins) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
@@ -945,6 +979,7 @@ __global__ void wait_selftest_kernel(unsigned* status, long long spins) {
 
 constexpr int kSmemState = 32768 + 32768 + 1024;
 constexpr int kSmemTree = 4 * kImgBytes + 1024;
+constexpr int kSmemPublish = kImgBytes + 1024;
 
 }  // namespace
 
@@ -1076,14 +1111,36 @@ cudaError_t launch_output(const TcPlan& tp, const CUtensorMap& mQ, const CUtenso
 
 }  // namespace
 
+size_t tc_prefix_bytes(const TcPlan& tp, int npre) {
+  const size_t n = (size_t)tp.B * tp.H * (npre > 0 ? npre : 0);
+  return a256(n * kImgBytes) + a256(n * kMeta * sizeof(unsigned));
+}
+
 cudaError_t launch_tc_fwd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   CUtensorMap mQ, mK, mV, mO;
   TcParams p;
   if (!tc_setup(tp, a, &mQ, &mK, &mV, &mO, &p)) return cudaErrorInvalidValue;
-  cudaError_t e = launch_state(tp, a, mK, mV, p, st);
+  cudaError_t e;
+  if (a.T0 > 0) {
+    // continuation: the live levels of T0, nearest first, as images for tc_output.  Plain
+    // stream order: the dependent launches after it wait for it transitively.
+    p.npre = 0;
+    for (int l = 1; l <= 62 && p.npre < 32; ++l)
+      if ((a.T0 >> (l - 1)) & 1) p.prelev[p.npre++] = l;
+    const size_t n = (size_t)tp.B * tp.H * p.npre;
+    p.preimg = reinterpret_cast<uint8_t*>(a.pre_ws);
+    p.premeta = reinterpret_cast<unsigned*>(a.pre_ws + a256(n * kImgBytes));
+    if ((e = cudaFuncSetAttribute(tc_prefix_publish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSmemPublish)) != cudaSuccess)
+      return e;
+    tc_prefix_publish_kernel<<<(unsigned)n, 128, kSmemPublish, st>>>(p, a.pre_st, a.pre_lsc, a.pre_levels);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launch();
+  }
+  e = launch_state(tp, a, mK, mV, p, st);
   if (e == cudaSuccess) e = launch_tree(tp, a, p, st);
   if (e != cudaSuccess) return e;
-  if ((e = launch_output<0>(tp, mQ, mK, mV, mO, p, bit_length(tp.NT - 1), st)) != cudaSuccess) return e;
+  if ((e = launch_output<0>(tp, mQ, mK, mV, mO, p, bit_length(tp.NT - 1) + p.npre, st)) != cudaSuccess) return e;
   note_launch(a, 2, st);
   if (a.states_out) {
     if ((e = launch_overlapped(tc_export_kernel, dim3(__builtin_popcount((unsigned)tp.T), tp.B * tp.H), dim3(256), 0, st, p,
@@ -1151,6 +1208,21 @@ cudaError_t launch_tc_nodes(const TcPlan& tp, const FwdArgs& a, cudaStream_t st)
   cudaError_t e = launch_state(tp, a, mK, mV, p, st);
   if (e == cudaSuccess) e = launch_tree(tp, a, p, st);
   return e;
+}
+
+// The tree and the export of the memories at position T into a.states_out.
+cudaError_t launch_tc_export_only(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
+  CUtensorMap mQ, mK, mV;
+  TcParams p;
+  if (!a.states_out || !tc_setup(tp, a, &mQ, &mK, &mV, nullptr, &p)) return cudaErrorInvalidValue;
+  cudaError_t e = launch_state(tp, a, mK, mV, p, st);
+  if (e == cudaSuccess) e = launch_tree(tp, a, p, st);
+  if (e != cudaSuccess) return e;
+  if ((e = launch_overlapped(tc_export_kernel, dim3(__builtin_popcount((unsigned)tp.T), tp.B * tp.H), dim3(256), 0,
+                             st, p, a.state_levels, a.states_out, a.logscale_out)) != cudaSuccess)
+    return e;
+  note_launch();
+  return cudaSuccess;
 }
 
 cudaError_t launch_wait_selftest(unsigned* status, long long spins, cudaStream_t st) {
