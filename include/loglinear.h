@@ -108,9 +108,9 @@ size_t loglinear_fwd_workspace_bytes(const ll_shape* shape);
  *   state_levels      slots in states_out; must be >= bit_length(T) + 1 when states_out
  *                     is given, ignored otherwise.
  * Which kernels run (loglinear_fwd_path reports it): bf16 with d_k = 128, d_v = 64 and
- * T % 128 == 0 takes the tensor-core path (tcgen05 products over 128-token tiles).  Every
- * other accepted shape, including that bf16 shape with T % 128 == 64 (e.g. T = 2368), runs
- * the fp32 CUDA-core path, which computes the same result several times more slowly.
+ * T % 64 == 0 takes the tensor-core path (tcgen05 products over 128-token tiles; when
+ * T % 128 == 64 the last tile holds 64 tokens).  Every other accepted shape runs the fp32
+ * CUDA-core path, which computes the same result several times more slowly.
  */
 ll_status loglinear_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
                         const float* a, const float* lambda, void* o, void* workspace,
@@ -227,7 +227,7 @@ size_t loglinear_fwd_continue_workspace_bytes(const ll_shape* shape, long long T
  *   state_levels     >= bit_length(T0 + T) + 1 when states_out is given
  *   workspace        >= loglinear_fwd_continue_workspace_bytes(shape, T0) bytes
  * With T0 == 0 this is loglinear_fwd.  The shapes of loglinear_fwd run on the same paths
- * (tensor cores for bf16, d_k = 128, d_v = 64, T % 128 == 0; the CUDA cores otherwise).
+ * (tensor cores for bf16, d_k = 128, d_v = 64, T % 64 == 0; the CUDA cores otherwise).
  */
 ll_status loglinear_fwd_continue(const ll_shape* shape, long long T0, const void* q, const void* k,
                                  const void* v, const float* a, const float* lambda,

@@ -98,14 +98,14 @@ const char* loglinear_status_string(ll_status s) {
 
 int loglinear_fwd_path(const ll_shape* s) {
   if (check_fwd_shape(s) != LL_OK) return 0;
-  return ll::tc_supported(*s) ? 2 : 1;
+  return ll::tc_fwd_supported(*s) ? 2 : 1;
 }
 
 size_t loglinear_fwd_workspace_bytes(const ll_shape* s) {
   if (check_fwd_shape(s) != LL_OK) return 0;
-  if (ll::tc_supported(*s)) {
+  if (ll::tc_fwd_supported(*s)) {
     ll::TcPlan tp;
-    return ll::make_tc_plan(*s, &tp) ? tp.bytes : 0;
+    return ll::make_tc_fwd_plan(*s, &tp) ? tp.bytes : 0;
   }
   ll::GenPlan p;
   if (!ll::make_gen_plan(*s, &p)) return 0;
@@ -131,7 +131,7 @@ ll_status loglinear_fwd_profiled(const ll_shape* s, const void* q, const void* k
 
 const char* loglinear_fwd_kernel_names(const ll_shape* s, int with_export) {
   if (check_fwd_shape(s) != LL_OK) return "";
-  if (ll::tc_supported(*s)) return ll::tc_kernel_names(with_export != 0);
+  if (ll::tc_fwd_supported(*s)) return ll::tc_kernel_names(with_export != 0);
   return with_export ? "gen_chunk_state,gen_blocks,gen_output,gen_export"
                      : "gen_chunk_state,gen_blocks,gen_output";
 }
@@ -411,9 +411,9 @@ bool cont_layout(const ll_shape* s, long long T0, ContLayout* c) {
   size_t o = a256(f);
   c->fwd = 0;
   c->pre = o;
-  if (ll::tc_supported(*s)) {
+  if (ll::tc_fwd_supported(*s)) {
     ll::TcPlan tp;
-    if (!ll::make_tc_plan(*s, &tp)) return false;
+    if (!ll::make_tc_fwd_plan(*s, &tp)) return false;
     o += a256(ll::tc_prefix_bytes(tp, c->npre));
   }
   c->loc = o;
@@ -499,9 +499,9 @@ ll_status loglinear_fwd_continue(const ll_shape* s, long long T0, const void* q,
   fa.pre_ws = ws + c.pre;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (ll::tc_supported(*s)) {
+  if (ll::tc_fwd_supported(*s)) {
     ll::TcPlan tp;
-    if (!ll::make_tc_plan(*s, &tp)) return LL_ERR_SHAPE;
+    if (!ll::make_tc_fwd_plan(*s, &tp)) return LL_ERR_SHAPE;
     e = ll::launch_tc_fwd(tp, fa, cs);
   } else {
     ll::GenPlan p;
@@ -548,9 +548,9 @@ ll_status loglinear_segment_total(const ll_shape* s, const void* k, const void* 
   ll::FwdArgs fa{k, k, v, a, nullptr, nullptr, ws, loc, nullptr, c.SLloc, sw, nullptr, 0};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (ll::tc_supported(t)) {
+  if (ll::tc_fwd_supported(t)) {
     ll::TcPlan tp;
-    if (!ll::make_tc_plan(t, &tp)) return LL_ERR_SHAPE;
+    if (!ll::make_tc_fwd_plan(t, &tp)) return LL_ERR_SHAPE;
     e = ll::launch_tc_export_only(tp, fa, cs);
   } else {
     ll::GenPlan p;
@@ -632,9 +632,9 @@ ll_status fwd_impl(const ll_shape* s, const void* q, const void* k, const void* 
   if (events && n_events > 0 && events[0])
     cudaEventRecord(static_cast<cudaEvent_t>(events[0]), cs);
   cudaError_t e;
-  if (ll::tc_supported(*s)) {
+  if (ll::tc_fwd_supported(*s)) {
     ll::TcPlan tp;
-    if (!ll::make_tc_plan(*s, &tp)) return LL_ERR_SHAPE;
+    if (!ll::make_tc_fwd_plan(*s, &tp)) return LL_ERR_SHAPE;
     e = ll::launch_tc_fwd(tp, fa, cs);
   } else {
     ll::GenPlan p;

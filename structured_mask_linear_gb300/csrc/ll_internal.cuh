@@ -121,8 +121,12 @@ struct TcPlan {
   size_t meta_bytes, bytes;
 };
 
+// bf16, d_k = 128, d_v = 64, T % 128 == 0: every tensor-core kernel (backward, Gated
+// DeltaNet, comparators); the forward also takes T % 128 == 64 (a last tile of 64 tokens).
 bool tc_supported(const ll_shape& s);
+bool tc_fwd_supported(const ll_shape& s);
 bool make_tc_plan(const ll_shape& s, TcPlan* p);
+bool make_tc_fwd_plan(const ll_shape& s, TcPlan* p);
 cudaError_t launch_tc_fwd(const TcPlan& p, const FwdArgs& a, cudaStream_t st);
 // Comparators on the tensor-core shape (not the product path): the forward with one
 // output pass per level (no level fusion), and the lambda-constant special case (SSD).

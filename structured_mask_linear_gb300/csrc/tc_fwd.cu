@@ -1,5 +1,7 @@
 // Tensor-core (tcgen05 / TMEM / TMA) path of the log-linear Mamba-2 forward for
-// bf16 q/k/v/o, d_k = 128, d_v = 64, T % 128 == 0.
+// bf16 q/k/v/o, d_k = 128, d_v = 64, T % 64 == 0.  When T % 128 == 64 the last tile holds
+// 64 tokens: TMA fills the rows past T with zeros (k = v = q = 0), their a is 1 and their
+// lambda 0, and the store of o leaves them out.
 //
 // Chunkwise algorithm of the log-linear attention write-up
 // (https://www.yoousoft.com/industry/3746.html, section 高效训练算法, Algorithm 1 / Fig. 3),
@@ -61,7 +63,8 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   const long long t0 = (long long)u * kTile;
   // a of token t0 + tid: loaded first, its log2 taken only where the scan needs it, so
   // that thread 0 issues the tile loads without waiting for this load
-  const float a_t = p.a[((size_t)b * p.T + t0 + tid) * p.H + h];
+  // (rows past T in a last, partial tile: a = 1, and TMA fills their k and v with zeros)
+  const float a_t = t0 + tid < p.T ? p.a[((size_t)b * p.T + t0 + tid) * p.H + h] : 1.f;
   ptx::griddep_launch_dependents();
 
   if (tid == 0) {
@@ -317,6 +320,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   const long long t0 = (long long)u * kTile;
   const size_t nbase = (size_t)bh * p.nnodes;
   const size_t row = (size_t)b * p.T + t0 + r;  // token of this thread's query row
+  const bool in_t = t0 + r < p.T;  // false for the rows past T of a last, partial tile
   const float* lrow = p.lam + (row * p.H + h) * p.L;
   // inter-tile levels of this tile, and whether the intra-tile part runs
   ptx::griddep_launch_dependents();  // the next launch may start once all CTAs are resident
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   // Warp 0's prologue path held the tile's loads back: tcgen05.alloc takes about 1 us, and
   // the load of a behind it another 1 us.  So a is loaded first, warp 1 initialises the
   // barriers and issues the tile loads, and warp 0 allocates after the lambda copies.
-  const float a_row = p.a[row * p.H + h];
+  const float a_row = in_t ? p.a[row * p.H + h] : 1.f;
   if (tid == 32) {
     s_oi = 0;
     ptx::mbar_init(&bar_ld, 1);
@@ -375,14 +379,17 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   if (!role_b) {
 #pragma unroll
     for (int l = 0; l < kLevIntra; ++l) {
-      if (kMode == 0 || (kMode == 2 && l == p.lsel)) ptx::cp_async4(sLam8 + r * 9 + l, lrow + l);
-      else sLam8[r * 9 + l] = kMode == 1 ? 1.f : 0.f;  // SSD: lambda = 1; single level: others off
+      if (in_t && (kMode == 0 || (kMode == 2 && l == p.lsel))) ptx::cp_async4(sLam8 + r * 9 + l, lrow + l);
+      else sLam8[r * 9 + l] = (kMode == 1 && in_t) ? 1.f : 0.f;  // SSD: lambda = 1; single level: others off
     }
   } else {
     if (kMode == 1) {
       if (nlev > 0) sLamI[r] = 1.f;
     } else {
-      for (int i = 0; i < nlev; ++i) ptx::cp_async4(sLamI + i * 128 + r, lrow + lam_col(i));
+      for (int i = 0; i < nlev; ++i) {
+        if (in_t) ptx::cp_async4(sLamI + i * 128 + r, lrow + lam_col(i));
+        else sLamI[i * 128 + r] = 0.f;
+      }
     }
     // The tree that the previous launches built is read from here on.  The wait (at once
     // unless this grid was launched before they finished) and the node scalars' fetch
@@ -762,7 +769,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     if (ok) {
       ptx::tc_fence_after();
       const float so = pow2s(sEp[r]);
-      float* o32row = kMode == 2 ? p.o32 + (row * p.H + h) * kDv : nullptr;
+      float* o32row = (kMode == 2 && in_t) ? p.o32 + (row * p.H + h) * kDv : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float y[32];
@@ -775,6 +782,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
 #pragma unroll
           for (int j = 0; j < 32; ++j) y[j] = acc[half * 32 + j];
         }
+        if (kMode == 2 && !in_t) continue;  // rows past T: nothing to keep (the store clips them)
         if (kMode == 2 && !(p.lflags & 2)) {  // store or add the running fp32 sum
           float4* d4 = reinterpret_cast<float4*>(o32row + half * 32);
 #pragma unroll
@@ -896,11 +904,13 @@ __global__ void __launch_bounds__(128) ssd_scan_kernel(TcParams p) {
 }
 
 // ---------------------------------------------------------------------------------
-// tc_export: bucket states at position T (T % 128 == 0, so live levels are >= 8).
+// tc_export: bucket states at position T (T % 64 == 0, so live levels are >= 7).
 // ---------------------------------------------------------------------------------
 // One CTA per live level of T (level l >= 1 with bit l-1 of T set) and (b, h); CTA 0 of
 // each (b, h) also writes the zero log-scales of all SL slots.  Slots of levels that are
-// not live at T are left as they are.
+// not live at T are left as they are.  With nf = T / 128 full tiles, level 8 + m is the
+// node (m, (nf >> m) - 1) for each set bit m of nf; when T % 128 == 64, level 7 is the
+// last, partial tile's node (0, nf), the nearest bucket of all.
 __global__ void __launch_bounds__(256) tc_export_kernel(TcParams p, int SL, float* st, float* lsc) {
   ptx::griddep_wait();  // reads the tree
   const int bh = blockIdx.y;
@@ -908,13 +918,20 @@ __global__ void __launch_bounds__(256) tc_export_kernel(TcParams p, int SL, floa
     for (int l = threadIdx.x; l < SL; l += 256) lsc[(size_t)bh * SL + l] = 0.f;
   const int lvl = nth_set_bit((unsigned)p.T, blockIdx.x) + 1;
   float* dst = st + ((size_t)bh * SL + lvl) * (kDk * kDv);
-  const int m = lvl - kLevIntra;
+  const int nf = p.T / kTile;
+  const bool part = (p.T % kTile) != 0;
   const size_t nbase = (size_t)bh * p.nnodes;
+  size_t node;
   float D = 0.f;
-  for (int mm = 0; mm < m; ++mm)
-    if ((p.NT >> mm) & 1)
-      D += __uint_as_float(p.meta[(nbase + p.node_off[mm] + ((p.NT >> mm) - 1)) * kMeta + 2]);
-  const size_t node = nbase + p.node_off[m] + ((p.NT >> m) - 1);
+  if (lvl < kLevIntra) {
+    node = nbase + nf;  // node (0, nf): the partial tile
+  } else {
+    const int m = lvl - kLevIntra;
+    if (part) D += __uint_as_float(p.meta[(nbase + nf) * kMeta + 2]);
+    for (int mm = 0; mm < m; ++mm)
+      if ((nf >> mm) & 1) D += __uint_as_float(p.meta[(nbase + p.node_off[mm] + ((nf >> mm) - 1)) * kMeta + 2]);
+    node = nbase + p.node_off[m] + ((nf >> m) - 1);
+  }
   const float scale = exp2f(D) * pow2i((int)p.meta[node * kMeta + 1]);
   const uint8_t* img = p.img + node * kImgBytes;
   for (int e = threadIdx.x; e < kDk * 8; e += 256) {  // 16-byte chunk c of image row i
@@ -988,19 +1005,27 @@ bool tc_supported(const ll_shape& s) {
          s.levels <= 32 && bit_length(s.T / kTile - 1) <= kMaxInter && encode_fn() != nullptr;
 }
 
+bool tc_fwd_supported(const ll_shape& s) {
+  const int nt = (s.T + kTile - 1) / kTile;
+  return s.dtype == LL_BF16 && s.d_k == kDk && s.d_v == kDv && s.T % (kTile / 2) == 0 && s.T > 0 &&
+         s.levels <= 32 && bit_length(nt - 1) <= kMaxInter && encode_fn() != nullptr;
+}
+
 const char* tc_kernel_names(bool with_export) {
   return with_export ? "tc_state,tc_tree,tc_output,tc_export" : "tc_state,tc_tree,tc_output";
 }
 
-bool make_tc_plan(const ll_shape& s, TcPlan* p) {
-  if (!tc_supported(s)) return false;
+bool make_tc_plan(const ll_shape& s, TcPlan* p) { return tc_supported(s) && make_tc_fwd_plan(s, p); }
+
+bool make_tc_fwd_plan(const ll_shape& s, TcPlan* p) {
+  if (!tc_fwd_supported(s)) return false;
   p->B = s.batch;
   p->T = s.T;
   p->H = s.heads;
   p->hpg = s.heads_per_group;
   p->G = s.heads / s.heads_per_group;
   p->L = s.levels;
-  p->NT = s.T / kTile;
+  p->NT = (s.T + kTile - 1) / kTile;  // a last tile of 64 tokens when T % 128 == 64
   p->MT = bit_length(p->NT);
   int off = 0;
   for (int m = 0; m < p->MT; ++m) {

@@ -43,6 +43,7 @@ def _prefix_and_steps(sml, x, T0, steps, chunk, L):
     dict(dtype=torch.float32, d_k=32, d_v=16, chunk=16, T0=64, steps=200),
     dict(dtype=torch.bfloat16, d_k=128, d_v=64, chunk=64, T0=256, steps=300),
     dict(dtype=torch.bfloat16, d_k=64, d_v=32, chunk=64, T0=64 * 5, steps=130),
+    dict(dtype=torch.bfloat16, d_k=128, d_v=64, chunk=64, T0=64 * 5, steps=100),  # export with a 64-token last tile
 ])
 def test_decode_matches_recurrent_form(sml, cfg):
     T0, steps = cfg["T0"], cfg["steps"]

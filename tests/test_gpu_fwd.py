@@ -33,9 +33,10 @@ def _np(x):
 
 
 @pytest.mark.parametrize("name,T,path", [("small", 2048, 2), ("pages", 8192, 2), ("long", 131072, 2),
-                                         ("small", 64 * 37, 1), ("tiny", 256, 1)])
+                                         ("small", 64 * 37, 2), ("small", 64, 2), ("tiny", 256, 1)])
 def test_path_selection(sml, name, T, path):
-    """bf16 with d_k = 128, d_v = 64 and T % 128 == 0 runs the tensor-core kernels."""
+    """bf16 with d_k = 128, d_v = 64 and T % 64 == 0 runs the tensor-core kernels (a last
+    tile of 64 tokens when T % 128 == 64); fp32 runs the CUDA-core ones."""
     w = workload(name, T=T, levels=levels_for(T))
     shape = sml.make_shape(w.batch, T, w.heads, w.heads_per_group, w.d_k, w.d_v, w.chunk,
                            w.levels, w.dtype)
@@ -130,11 +131,13 @@ def test_bitexact_level_map_intra(sml, dtype, chunk):
     assert np.array_equal(o.double().cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("T", [4096, 4032])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_bitexact_level_map_inter(sml, dtype):
-    """T = 4096, C = 64: v is e_j only at the first token of chunk j, so o_t[j] = 2^l(t, jC)
-    exactly for every earlier chunk, which checks every chunk-level bucket."""
-    T, C, dv = 4096, 64, 64
+def test_bitexact_level_map_inter(sml, dtype, T):
+    """C = 64: v is e_j only at the first token of chunk j, so o_t[j] = 2^l(t, jC) exactly
+    for every earlier chunk, which checks every chunk-level bucket (T = 4032: the last
+    128-token tile of the bf16 tensor-core path holds 64 tokens)."""
+    C, dv = 64, 64
     L = levels_for(T)
     v = torch.zeros(1, T, 2, dv)
     for j in range(T // C):

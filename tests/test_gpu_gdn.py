@@ -46,7 +46,7 @@ def _run(sml, w, x, beta, chunk):
 @pytest.mark.parametrize("name,kw,chunk", [
     ("tiny", {}, 16),
     ("small", dict(batch=1, heads=4, T=1024), 64),            # tensor-core forward
-    ("small", dict(batch=1, heads=4, T=64 * 37), 64),         # generic forward
+    ("small", dict(batch=1, heads=4, T=64 * 37), 64),         # CUDA-core values, 64-token last tile
     ("small", dict(batch=1, heads=2, T=512), 16),
     ("small", dict(batch=1, heads=4, T=1024, decay="slow"), 64),
     ("small", dict(batch=1, heads=4, T=1024, decay="mamba2"), 64),

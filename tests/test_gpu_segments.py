@@ -46,6 +46,7 @@ CASES = [  # name, overrides, chunk, segment length T, start T0
     ("tc", dict(d_k=128, d_v=64, dtype=torch.bfloat16), 64, 1024, 3072),
     ("tc_far", dict(d_k=128, d_v=64, dtype=torch.bfloat16), 64, 512, 7680),
     ("tc_carry", dict(d_k=128, d_v=64, dtype=torch.bfloat16), 64, 1024, 1024),
+    ("tc_partial", dict(d_k=128, d_v=64, dtype=torch.bfloat16), 64, 192, 768),
     ("generic", dict(d_k=32, d_v=16, dtype=torch.float32), 32, 256, 768),
     ("generic_bf16", dict(d_k=64, d_v=32, dtype=torch.bfloat16), 64, 192 * 2, 512 * 3),
 ]
@@ -112,6 +113,7 @@ def test_fwd_continue_rejects_unaligned_starts(sml):
 @pytest.mark.parametrize("name,kw,chunk,T", [
     ("tc", dict(d_k=128, d_v=64, dtype=torch.bfloat16), 64, 2048),
     ("tc_ragged", dict(d_k=128, d_v=64, dtype=torch.bfloat16), 64, 1408),
+    ("tc_partial", dict(d_k=128, d_v=64, dtype=torch.bfloat16), 64, 1472),
     ("generic", dict(d_k=32, d_v=16, dtype=torch.float32), 16, 320),
 ])
 def test_segment_total(sml, name, kw, chunk, T):
@@ -147,13 +149,6 @@ def test_prefix_states(sml, n):
                 if (T0 >> (lvl - 1)) & 1:
                     assert_parity(got[b, h, lvl], ref[lvl], f"n={n} level {lvl}", "f32")
                     assert float(lsc[b, h, lvl]) == 0.0
-
-
-class _OneProcess:
-    """Stands in for a process group: every segment in this process, in rank order."""
-
-    def __init__(self, world):
-        self.world = world
 
 
 def test_sharded_forward_in_one_process(sml):
