@@ -38,6 +38,7 @@ struct TcParams {
   float* o32;      // (B, T, H, d_v) fp32 running sum of the single-level passes
   int lsel;        // the one level of a single-level pass
   int lflags;      // bit 0: first pass (store), bit 1: last pass (write o)
+  int all_tiles;   // tc_state stores every tile state's image (the SSD scan reads them all)
   uint8_t* pimg;   // (B*H, NT, 16 KB) SSD prefix-state images
   unsigned* pmeta; // (B*H, NT, 4)
   // continuation from the bucket memories at a start position T0 (level-fused mode only):

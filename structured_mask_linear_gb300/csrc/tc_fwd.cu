@@ -8,13 +8,15 @@
 // with 128-token tiles (two 64-token chunks; the result does not depend on the chunk
 // length, so the tile only decides which levels are dense inside a tile: 0..7):
 //
-//  tc_state   one CTA per (b, h, tile u): chunk-local log2 decay cumsum g, tile decay
-//             gamma_u, tile state H_u = K_uᵀ diag(2^(gamma_u - g)) V_u on the tensor
-//             cores (M = d_k, N = d_v, K = tokens), published as node (0, u) of the
-//             Fenwick tree over tiles.  Nodes are fp16 images in the UMMA operand layout
-//             with a power-of-two scale and their total log2 decay.
-//  tc_tree    two tree levels per launch, Node_{m+1}[i] = 2^(Gamma(right)) Node_m[2i] +
-//             Node_m[2i+1], from the images of the level below (no CTA waits for another).
+//  tc_state   one CTA per (b, h, four tiles): per tile u the chunk-local log2 decay
+//             cumsum g, the tile decay gamma_u and the tile state H_u = K_uᵀ
+//             diag(2^(gamma_u - g)) V_u on the tensor cores (M = d_k, N = d_v, K = tokens),
+//             node (0, u) of the Fenwick tree over tiles; nodes (1, 2i) and (2, i) are summed
+//             in fp32 registers on the way.  Nodes are fp16 images in the UMMA operand
+//             layout with a power-of-two scale and their total log2 decay.
+//  tc_tree    two tree levels per launch from level 3 up, Node_{m+1}[i] =
+//             2^(Gamma(right)) Node_m[2i] + Node_m[2i+1], from the images of the level below
+//             (no CTA waits for another).
 //  tc_output  one CTA per (b, h, tile u): S = Q Kᵀ on the tensor cores; P = S ⊙ lambda^l
 //             ⊙ 2^(g_t - g_s) ⊙ [s <= t] (levels 0..7) written to tensor memory as fp16
 //             with a power-of-two row scale; O = P V with P as the tensor-memory operand;
@@ -38,15 +40,24 @@ namespace ll {
 
 namespace {
 // ---------------------------------------------------------------------------------
-// tc_state: tile states (level 0 of the Fenwick tree over tiles).
+// tc_state: tile states and the first two tree levels above them.  One CTA per (b, h,
+// group of four tiles 4i .. 4i+3); tile by tile (thread tid owns row tid of a state):
+// g and the tile decay gamma, H_u = K_uᵀ diag(2^(gamma_u - g)) V_u on the tensor cores,
+// published as node (0, u); a running fp32 sum L = 2^(gamma_u) L + H_u gives node (1, 2i)
+// after the second tile and node (2, i) after the fourth.  The odd node (1, 2i + 1) is read
+// by nothing but its parent, so it is never published; nor is the image of an odd tile
+// (its decay is), except a last, partial tile or when all_tiles asks for every image.
+// The next tile's K and V are requested as soon as the MMA has read the current ones, so
+// that the copy overlaps the read-out and the stores.  No CTA waits for another.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ CUtensorMap mapK,
                                                        const __grid_constant__ CUtensorMap mapV,
                                                        TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = smem;          // 32 KB: K (bf16, two 64-wide d_k boxes); later node staging
-  uint8_t* sV = smem + 32768;  // 32 KB: Ṽ hi part (the TMA box) then Ṽ lo part
+  uint8_t* sK = smem;             // 32 KB: K (bf16, two 64-wide d_k boxes)
+  uint8_t* sV = smem + 32768;     // 32 KB: Ṽ hi part (the TMA box) then Ṽ lo part
+  uint8_t* stage = smem + 65536;  // 16 KB: a node's fp16 image on its way out
   __shared__ __align__(8) uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[4];
@@ -54,91 +65,107 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
   __shared__ float s_gamma;
 
   const int tid = threadIdx.x, warp = tid >> 5, rot = tid & 7;
+  const int ng4 = (p.NT + 3) >> 2;  // groups of four tiles per (b, h)
   const int lin = blockIdx.x;
   const int h = lin % p.H;
-  const int u = (lin / p.H) % p.NT;
-  const int b = lin / (p.H * p.NT);
+  const int i4 = (lin / p.H) % ng4;
+  const int b = lin / (p.H * ng4);
   const int g = h / p.hpg;
-  const int bh = b * p.H + h;
-  const long long t0 = (long long)u * kTile;
-  // a of token t0 + tid: loaded first, its log2 taken only where the scan needs it, so
-  // that thread 0 issues the tile loads without waiting for this load
-  // (rows past T in a last, partial tile: a = 1, and TMA fills their k and v with zeros)
-  const float a_t = t0 + tid < p.T ? p.a[((size_t)b * p.T + t0 + tid) * p.H + h] : 1.f;
+  const size_t nbase = (size_t)(b * p.H + h) * p.nnodes;
+  const int nt4 = min(4, p.NT - 4 * i4);  // tiles of this group (fewer at the end)
+  // a of token tid of each tile (rows past T in a last, partial tile: a = 1, and TMA
+  // fills their k and v with zeros)
+  float a4[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const long long t = (long long)(4 * i4 + k) * kTile + tid;
+    a4[k] = (k < nt4 && t < p.T) ? p.a[((size_t)b * p.T + t) * p.H + h] : 1.f;
+  }
   ptx::griddep_launch_dependents();
 
+  auto load_tile = [&](int u) {
+    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
+    ptx::tma_load_4d(sK, &mapK, &bar_ld, 0, g, u * kTile, b);
+    ptx::tma_load_4d(sK + 16384, &mapK, &bar_ld, 64, g, u * kTile, b);
+    ptx::tma_load_4d(sV, &mapV, &bar_ld, 0, h, u * kTile, b);
+  };
   if (tid == 0) {
     ptx::mbar_init(&bar_ld, 1);
     ptx::mbar_init(&bar_mma, 1);
     ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
-    ptx::tma_load_4d(sK, &mapK, &bar_ld, 0, g, (int)t0, b);
-    ptx::tma_load_4d(sK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
-    ptx::tma_load_4d(sV, &mapV, &bar_ld, 0, h, (int)t0, b);
+    load_tile(4 * i4);
   }
   if (warp == 0) {
     ptx::tmem_alloc(&tmem_base, 128);
     ptx::tmem_relinquish();
   }
-  // decay of token t0 + tid: chunk-local log2 cumsum (the scan also publishes tmem_base)
   ptx::tc_fence_before();
-  const float gi = block_scan128(log2f(a_t), s_red);
+  __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tbase = tmem_base;
-  if (tid == kTile - 1) s_gamma = gi;
-  bool ok = wait_bar(&bar_ld, 0);
-  if (!ok) atomicExch(p.status, kStatusTimeout);
-  ok = __syncthreads_and(ok);
-  const float gamma = s_gamma;
-  if (ok) {
-    // Ṽ row tid = 2^(gamma - g_tid) v_tid as a bf16 hi part (in place) plus a bf16 lo
-    // part (the rounding remainder), so that Kᵀ(Ṽhi + Ṽlo) keeps ~16 bits.  The 128-byte
-    // swizzle permutes 16-byte chunks inside a row only, so rows map in place.
-    const float w = exp2f(gamma - gi);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int off = tid * 128 + ((c ^ rot) << 4);
-      uint4 x = *reinterpret_cast<uint4*>(sV + off), y;
-      __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
-      __nv_bfloat162* hy = reinterpret_cast<__nv_bfloat162*>(&y);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float2 f = __bfloat1622float2(hx[e]);
-        f.x *= w;
-        f.y *= w;
-        hx[e] = __floats2bfloat162_rn(f.x, f.y);
-        float2 r = __bfloat1622float2(hx[e]);
-        hy[e] = __floats2bfloat162_rn(f.x - r.x, f.y - r.y);
-      }
-      *reinterpret_cast<uint4*>(sV + off) = x;
-      *reinterpret_cast<uint4*>(sV + 16384 + off) = y;
-    }
-    ptx::fence_proxy_async_smem();
-  }
-  __syncthreads();
-  if (ok && tid == 0) {
-    ptx::tc_fence_after();
-    // [Hhi | Hlo] (M = d_k 128, N = 2 x d_v, K = 128 tokens): A = Kᵀ and B = [Ṽhi | Ṽlo],
-    // both MN-major; the two 64-wide N atoms of B sit 16 KB apart.
-    const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 1, 1);
-    const uint32_t a0 = ptx::smem_u32(sK), b0 = ptx::smem_u32(sV);
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk) {
-      uint64_t da = ptx::smem_desc_sw128(a0 + kk * 2048, 16384, 1024);
-      uint64_t db = ptx::smem_desc_sw128(b0 + kk * 2048, 16384, 1024);
-      ptx::umma_f16(tbase, da, db, idesc, kk > 0);
-    }
-    ptx::umma_commit(&bar_mma);
-  }
-  if (ok) {
-    ok = wait_bar(&bar_mma, 0);
+  float L[kDv];  // running sum of the group's tile states, decayed to the latest tile's end
+  float GL = 0.f;
+  int k = 0, fail = 0;  // fail: 1 = tile k's copy timed out, 2 = its MMA did
+  for (; k < nt4; ++k) {
+    const int u = 4 * i4 + k;
+    // decay of token u * 128 + tid: chunk-local log2 cumsum
+    const float gi = block_scan128(log2f(a4[k]), s_red);
+    if (tid == kTile - 1) s_gamma = gi;
+    bool ok = wait_bar(&bar_ld, k & 1);
     if (!ok) atomicExch(p.status, kStatusTimeout);
-  }
-  ok = __syncthreads_and(ok);
-  float cur[kDv];
+    if (!__syncthreads_and(ok)) {
+      fail = 1;
+      break;
+    }
+    const float gamma = s_gamma;
+    {
+      // Ṽ row tid = 2^(gamma - g_tid) v_tid as a bf16 hi part (in place) plus a bf16 lo
+      // part (the rounding remainder), so that Kᵀ(Ṽhi + Ṽlo) keeps ~16 bits.  The 128-byte
+      // swizzle permutes 16-byte chunks inside a row only, so rows map in place.
+      const float w = exp2f(gamma - gi);
 #pragma unroll
-  for (int j = 0; j < kDv; ++j) cur[j] = 0.f;
-  if (ok) {
+      for (int c = 0; c < 8; ++c) {
+        const int off = tid * 128 + ((c ^ rot) << 4);
+        uint4 x = *reinterpret_cast<uint4*>(sV + off), y;
+        __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
+        __nv_bfloat162* hy = reinterpret_cast<__nv_bfloat162*>(&y);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f = __bfloat1622float2(hx[e]);
+          f.x *= w;
+          f.y *= w;
+          hx[e] = __floats2bfloat162_rn(f.x, f.y);
+          float2 rr = __bfloat1622float2(hx[e]);
+          hy[e] = __floats2bfloat162_rn(f.x - rr.x, f.y - rr.y);
+        }
+        *reinterpret_cast<uint4*>(sV + off) = x;
+        *reinterpret_cast<uint4*>(sV + 16384 + off) = y;
+      }
+      ptx::fence_proxy_async_smem();
+    }
+    __syncthreads();  // also: every read-out of the previous tile's accumulator is done
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      // [Hhi | Hlo] (M = d_k 128, N = 2 x d_v, K = 128 tokens): A = Kᵀ and B = [Ṽhi | Ṽlo],
+      // both MN-major; the two 64-wide N atoms of B sit 16 KB apart.
+      const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 1, 1);
+      const uint32_t a0 = ptx::smem_u32(sK), b0 = ptx::smem_u32(sV);
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        uint64_t da = ptx::smem_desc_sw128(a0 + kk * 2048, 16384, 1024);
+        uint64_t db = ptx::smem_desc_sw128(b0 + kk * 2048, 16384, 1024);
+        ptx::umma_f16(tbase, da, db, idesc, kk > 0);
+      }
+      ptx::umma_commit(&bar_mma);
+    }
+    ok = wait_bar(&bar_mma, k & 1);
+    if (!ok) atomicExch(p.status, kStatusTimeout);
+    if (!__syncthreads_and(ok)) {
+      fail = 2;
+      break;
+    }
+    if (tid == 0 && k + 1 < nt4) load_tile(u + 1);  // the MMA has read sK and sV
+    float cur[kDv];
     ptx::tc_fence_after();
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -149,14 +176,36 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
 #pragma unroll
       for (int j = 0; j < 32; ++j) cur[half * 32 + j] = hi[j] + lo[j];
     }
+    ptx::tc_fence_before();
+    // the tile's node (level 0; node_off[0] == 0).  Readers of the tree take even nodes
+    // only, and a last, partial tile's node (the state export's nearest bucket); another
+    // odd tile's state goes into node (1, 2i) here, so only its decay is stored.
+    if ((k & 1) == 0 || p.all_tiles || (u == p.NT - 1 && p.T % kTile != 0))
+      publish_node(cur, stage, nbase + u, gamma, s_red2, p.img, p.meta);
+    else if (tid == 0) p.meta[(nbase + u) * kMeta + 2] = __float_as_uint(gamma);
+    if (k == 0) {
+#pragma unroll
+      for (int j = 0; j < kDv; ++j) L[j] = cur[j];
+    } else {
+      const float d = exp2f(gamma);
+#pragma unroll
+      for (int j = 0; j < kDv; ++j) L[j] = d * L[j] + cur[j];
+    }
+    GL += gamma;
+    if (k == 1 || k == 3) {
+      __syncthreads();  // every row of the staged tile node is stored
+      publish_node(L, stage, nbase + p.node_off[k == 1 ? 1 : 2] + (k == 1 ? 2 * i4 : i4), GL, s_red2, p.img,
+                   p.meta);
+    }
+    __syncthreads();  // the staging area is free again
+  }
+  if (fail && tid == 0) {  // tile k gave up: let what it started end (bounded waits)
+    wait_bar(&bar_ld, k & 1);
+    if (fail == 2) wait_bar(&bar_mma, k & 1);
   }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) ptx::tmem_dealloc(tbase, 128);
-  if (!ok) return;
-
-  // the tile's node (level 0; node_off[0] == 0), staged in sK (free now)
-  publish_node(cur, sK, (size_t)bh * p.nnodes + u, gamma, s_red2, p.img, p.meta);
 }
 
 // ---------------------------------------------------------------------------------
@@ -994,7 +1043,7 @@ __global__ void wait_selftest_kernel(unsigned* status, long long spins) {
 // host side
 // ---------------------------------------------------------------------------------
 
-constexpr int kSmemState = 32768 + 32768 + 1024;
+constexpr int kSmemState = 32768 + 32768 + 16384 + 1024;
 constexpr int kSmemTree = 4 * kImgBytes + 1024;
 constexpr int kSmemPublish = kImgBytes + 1024;
 
@@ -1095,7 +1144,7 @@ bool tc_setup(const TcPlan& tp, const FwdArgs& a, CUtensorMap* mQ, CUtensorMap* 
 
 cudaError_t launch_state(const TcPlan& tp, const FwdArgs& a, const CUtensorMap& mK, const CUtensorMap& mV,
                          const TcParams& p, cudaStream_t st) {
-  const unsigned grid = (unsigned)((size_t)tp.B * tp.NT * tp.H);
+  const unsigned grid = (unsigned)((size_t)tp.B * ((tp.NT + 3) / 4) * tp.H);
   cudaError_t e = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemState);
   if (e != cudaSuccess) return e;
   tc_state_kernel<<<grid, 128, kSmemState, st>>>(mK, mV, p);
@@ -1105,17 +1154,18 @@ cudaError_t launch_state(const TcPlan& tp, const FwdArgs& a, const CUtensorMap& 
 }
 
 cudaError_t launch_tree(const TcPlan& tp, const FwdArgs& a, const TcParams& p, cudaStream_t st) {
-  // tree levels 1.. two per launch; the profiling event of slot 1 follows the last one
+  // tree levels 3.. two per launch (tc_state built levels 0..2); the profiling event of
+  // slot 1 follows the last one
   cudaError_t e = cudaFuncSetAttribute(tc_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTree);
   if (e != cudaSuccess) return e;
-  for (int m0 = 1; m0 < tp.MT; m0 += 2) {
+  for (int m0 = 3; m0 < tp.MT; m0 += 2) {
     const unsigned gt = (unsigned)((size_t)tp.B * tp.H * (((tp.NT >> m0) + 1) >> 1));
     if ((e = launch_overlapped(tc_tree_kernel, dim3(gt), dim3(128), kSmemTree, st, p, m0)) != cudaSuccess)
       return e;
     if (m0 + 2 < tp.MT) note_launch();
     else note_launch(a, 1, st);
   }
-  if (tp.MT <= 1 && a.events && 2 < a.n_events && a.events[2])  // no tree level above tiles
+  if (tp.MT <= 3 && a.events && 2 < a.n_events && a.events[2])  // no tree level above level 2
     cudaEventRecord(static_cast<cudaEvent_t>(a.events[2]), st);
   return cudaSuccess;
 }
@@ -1210,6 +1260,7 @@ cudaError_t launch_tc_ssd(const TcPlan& tp, const FwdArgs& a, cudaStream_t st) {
   const size_t base = (tp.bytes + 255) & ~size_t(255);
   p.pimg = reinterpret_cast<uint8_t*>(a.ws + base);
   p.pmeta = reinterpret_cast<unsigned*>(a.ws + base + (size_t)tp.B * tp.H * tp.NT * kImgBytes);
+  p.all_tiles = 1;
   cudaError_t e = launch_state(tp, a, mK, mV, p, st);
   if (e != cudaSuccess) return e;
   if (tp.NT > 1) {
