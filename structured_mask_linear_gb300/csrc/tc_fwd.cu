@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[8];
   __shared__ int s_oi;  // role a -> all: the O MMA was issued
+  __shared__ int s_e12; // node images 1 and 2 issued by thread 0 once S has read K
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = tid & 127;             // query row (tile-local token)
@@ -407,6 +408,7 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
   const float a_row = in_t ? p.a[row * p.H + h] : 1.f;
   if (tid == 32) {
     s_oi = 0;
+    s_e12 = 0;
     ptx::mbar_init(&bar_ld, 1);
     ptx::mbar_init(&bar_s, 1);
     ptx::mbar_init(&bar_o, 1);
@@ -507,6 +509,15 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     if (ok) {
       ok = wait_bar(&bar_s, 0);
       if (!ok) atomicExch(p.status, kStatusTimeout);
+    }
+    if (ok && tid == 0 && nlev > 1) {  // K has been read by S: node images 1 and 2 into RK
+      ptx::mbar_arrive_expect_tx(&bar_e[1], kImgBytes);
+      ptx::bulk_load(RK, img_of(1), kImgBytes, &bar_e[1]);
+      if (nlev > 2) {
+        ptx::mbar_arrive_expect_tx(&bar_e[2], kImgBytes);
+        ptx::bulk_load(RK + 16384, img_of(2), kImgBytes, &bar_e[2]);
+      }
+      s_e12 = nlev > 2 ? 2 : 1;
     }
     ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld / st below are warp-collective
     int ep = 0;
@@ -668,7 +679,9 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
     uint8_t* qrow0 = RQ + r * 128;
     uint8_t* qrow1 = RQ + 16384 + r * 128;
     int eq = 0;
-    int issued = nlev > 0 ? 1 : 0;  // image loads issued by the driver (image 0 in the prologue)
+    // image loads issued by the driver: image 0 in the prologue, images from 3 on in the
+    // level loop (thread 0 issues images 1 and 2, or the driver does without the S part)
+    int issued = nlev > 0 ? 1 : 0;
     int consumed = 0;               // image loads waited for by the driver
     int y_issued = 0, y_seen = 0;   // Y MMAs issued / seen complete by the driver
     if (ok) {
@@ -698,8 +711,8 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
         ptx::fence_proxy_async_smem();
       }
     }
-    if (ok && driver) {
-      for (int i = 1; i < 3 && i < nlev; ++i) {  // K has been read by S: RK is free
+    if (ok && driver && !intra_on) {
+      for (int i = 1; i < 3 && i < nlev; ++i) {  // K was never loaded: RK is free
         ptx::mbar_arrive_expect_tx(&bar_e[i], kImgBytes);
         ptx::bulk_load(ebuf(i), img_of(i), kImgBytes, &bar_e[i]);
         ++issued;
@@ -797,13 +810,15 @@ __global__ void __launch_bounds__(256, 2) tc_output_kernel(const __grid_constant
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bar_yf);
     }
+    __syncthreads();  // join: P, its row scales and the O MMA have been issued
     if (driver) {
       // after a failed wait: let this CTA's own copies and MMAs land (bounded) before exit
+      // (image loads are issued in level order, so the unconsumed ones are the last)
+      if (intra_on) issued += s_e12;
       for (int j = consumed; j < issued; ++j) wait_bar(&bar_e[j % 3], (j / 3) & 1);
       for (int j = y_seen; j < y_issued; ++j) wait_bar(&bar_y, j & 1);
       if (s_issued) wait_bar(&bar_s, 0);
     }
-    __syncthreads();  // join: P, its row scales and the O MMA have been issued
     const bool o_issued = s_oi != 0;
     if (intra_on) {
       ok = ok && o_issued && wait_bar(&bar_o, 0);
