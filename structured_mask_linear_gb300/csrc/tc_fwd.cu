@@ -50,14 +50,16 @@ namespace {
 // The next tile's K and V are requested as soon as the MMA has read the current ones, so
 // that the copy overlaps the read-out and the stores.  No CTA waits for another.
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ CUtensorMap mapK,
+__global__ void __launch_bounds__(128, 3) tc_state_kernel(const __grid_constant__ CUtensorMap mapK,
                                                        const __grid_constant__ CUtensorMap mapV,
                                                        TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = smem;             // 32 KB: K (bf16, two 64-wide d_k boxes)
-  uint8_t* sV = smem + 32768;     // 32 KB: Ṽ hi part (the TMA box) then Ṽ lo part
-  uint8_t* stage = smem + 65536;  // 16 KB: a node's fp16 image on its way out
+  uint8_t* sK = smem;          // 32 KB: K (bf16, two 64-wide d_k boxes)
+  uint8_t* sV = smem + 32768;  // 32 KB: Ṽ hi part (the TMA box) then Ṽ lo part
+  // a node's fp16 image on its way out: Ṽ's lo part, free once the MMA has read it (the
+  // next tile's copy fills K and Ṽ's hi part only)
+  uint8_t* stage = sV + 16384;
   __shared__ __align__(8) uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[4];
@@ -165,32 +167,56 @@ __global__ void __launch_bounds__(128) tc_state_kernel(const __grid_constant__ C
       break;
     }
     if (tid == 0 && k + 1 < nt4) load_tile(u + 1);  // the MMA has read sK and sV
-    float cur[kDv];
     ptx::tc_fence_after();
+    // H_u row tid = Hhi + Hlo, 16 columns at a time: folded into L and its maximum taken;
+    // the tile's node (level 0; node_off[0] == 0) is staged from a second read of the
+    // accumulator.  Readers of the tree take even nodes only, and a last, partial tile's
+    // node (the state export's nearest bucket); another odd tile's state goes into node
+    // (1, 2i) here, so only its decay is stored.
+    const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
+    const float d = exp2f(gamma);
+    float m = 0.f;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float hi[32], lo[32];
-      ptx::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16) + half * 32, hi);
-      ptx::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16) + 64 + half * 32, lo);
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float hi[16], lo[16];
+      ptx::tmem_ld16(trow + q4 * 16, hi);
+      ptx::tmem_ld16(trow + 64 + q4 * 16, lo);
       ptx::tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) cur[half * 32 + j] = hi[j] + lo[j];
+      for (int j = 0; j < 16; ++j) {
+        const float c = hi[j] + lo[j];
+        m = fmaxf(m, fabsf(c));
+        L[q4 * 16 + j] = k == 0 ? c : d * L[q4 * 16 + j] + c;
+      }
     }
+    const size_t node0 = nbase + u;
+    if ((k & 1) == 0 || p.all_tiles || (u == p.NT - 1 && p.T % kTile != 0)) {
+      const int e = f16_exp(block_max2(make_float2(m, 0.f), s_red2).x);
+      const float sc = pow2i(-e);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float hi[16], lo[16];
+        ptx::tmem_ld16(trow + q4 * 16, hi);
+        ptx::tmem_ld16(trow + 64 + q4 * 16, lo);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {  // 16-byte chunk 2 q4 + c2 of the row
+          const float* x = hi + 8 * c2;
+          const float* y = lo + 8 * c2;
+          *reinterpret_cast<uint4*>(stage + tid * 128 + (((2 * q4 + c2) ^ rot) << 4)) =
+              make_uint4(pack_h2((x[0] + y[0]) * sc, (x[1] + y[1]) * sc), pack_h2((x[2] + y[2]) * sc, (x[3] + y[3]) * sc),
+                         pack_h2((x[4] + y[4]) * sc, (x[5] + y[5]) * sc), pack_h2((x[6] + y[6]) * sc, (x[7] + y[7]) * sc));
+        }
+      }
+      __syncthreads();
+      uint4* dst = reinterpret_cast<uint4*>(p.img + node0 * kImgBytes);
+#pragma unroll
+      for (int rr = 0; rr < kImgBytes / 16 / 128; ++rr)
+        dst[rr * 128 + tid] = reinterpret_cast<const uint4*>(stage)[rr * 128 + tid];
+      if (tid == 0) p.meta[node0 * kMeta + 1] = (unsigned)e;
+    }
+    if (tid == 0) p.meta[node0 * kMeta + 2] = __float_as_uint(gamma);
     ptx::tc_fence_before();
-    // the tile's node (level 0; node_off[0] == 0).  Readers of the tree take even nodes
-    // only, and a last, partial tile's node (the state export's nearest bucket); another
-    // odd tile's state goes into node (1, 2i) here, so only its decay is stored.
-    if ((k & 1) == 0 || p.all_tiles || (u == p.NT - 1 && p.T % kTile != 0))
-      publish_node(cur, stage, nbase + u, gamma, s_red2, p.img, p.meta);
-    else if (tid == 0) p.meta[(nbase + u) * kMeta + 2] = __float_as_uint(gamma);
-    if (k == 0) {
-#pragma unroll
-      for (int j = 0; j < kDv; ++j) L[j] = cur[j];
-    } else {
-      const float d = exp2f(gamma);
-#pragma unroll
-      for (int j = 0; j < kDv; ++j) L[j] = d * L[j] + cur[j];
-    }
     GL += gamma;
     if (k == 1 || k == 3) {
       __syncthreads();  // every row of the staged tile node is stored
@@ -1058,7 +1084,7 @@ __global__ void wait_selftest_kernel(unsigned* status, long long spins) {
 // host side
 // ---------------------------------------------------------------------------------
 
-constexpr int kSmemState = 32768 + 32768 + 16384 + 1024;
+constexpr int kSmemState = 32768 + 32768 + 1024;
 constexpr int kSmemTree = 4 * kImgBytes + 1024;
 constexpr int kSmemPublish = kImgBytes + 1024;
 
