@@ -71,6 +71,9 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
                                                               const __grid_constant__ CUtensorMap mapK,
                                                               const __grid_constant__ CUtensorMap mapV,
                                                               const __grid_constant__ CUtensorMap mapD,
+                                                              const __grid_constant__ CUtensorMap mapDQ,
+                                                              const __grid_constant__ CUtensorMap mapDK,
+                                                              const __grid_constant__ CUtensorMap mapDV,
                                                               TcBwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -412,38 +415,48 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
     if (!ok) atomicExch(p.status, kStatusTimeout);
   }
   ok = __all_sync(0xffffffffu, ok);
+  // The fp32 rows of dq (role a), dk and dv (role b) are staged in the tile buffers, free
+  // now (every MMA has read them), as 128-byte-swizzled boxes of 32 columns (dq: 4 boxes
+  // from 0, dk: 4 from 64 KB, dv: 2 from 128 KB), then written with one TMA store each.
+  // Thread r writes row r of a box as eight 16-byte chunks, chunk c at c ^ (r & 7).
+  auto stage_row = [&](uint8_t* box, const float (&y)[32], float sc) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<float4*>(box + r * 128 + ((c ^ rot) << 4)) =
+          make_float4(sc * y[4 * c], sc * y[4 * c + 1], sc * y[4 * c + 2], sc * y[4 * c + 3]);
+  };
   if (ok) {
     ptx::tc_fence_after();
     if (!role_b) {
       const float sc = pow2s(s_sc[0] + s_sc[3]);  // dS and K
-      float* dst = p.dq32 + (row * p.H + h) * kDk;
 #pragma unroll 1
       for (int c0 = 0; c0 < kDk; c0 += 32) {
         float y[32];
         ptx::tmem_ld32(tDQ + lane_off + c0, y);
         ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(sc * y[j], sc * y[j + 1], sc * y[j + 2], sc * y[j + 3]);
+        stage_row(smem + (c0 >> 5) * 16384, y, sc);
       }
     } else {
       const float sk = pow2s(s_sc[0] + s_sc[2]);  // dS and Q
       const float sv = pow2s(s_sc[1] + s_sc[4]);  // P and dO
-      float* dk = p.dk32 + (row * p.H + h) * kDk;
-      float* dv = p.dv32 + (row * p.H + h) * kDv;
 #pragma unroll 1
       for (int c0 = 0; c0 < kDk + kDv; c0 += 32) {
         const bool isk = c0 < kDk;
         float y[32];
         ptx::tmem_ld32((isk ? tDK + c0 : tDV + (c0 - kDk)) + lane_off, y);
         ptx::tmem_ld_wait();
-        const float s = isk ? sk : sv;
-        float* d = isk ? dk + c0 : dv + (c0 - kDk);
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(d + j) = make_float4(s * y[j], s * y[j + 1], s * y[j + 2], s * y[j + 3]);
+        stage_row(smem + 65536 + (c0 >> 5) * 16384, y, isk ? sk : sv);
       }
     }
+    ptx::fence_proxy_async_smem();
+  }
+  ok = __syncthreads_and(ok);  // every row staged
+  if (ok && tid == 0) {
+    for (int j = 0; j < 4; ++j) ptx::tma_store_4d(&mapDQ, smem + j * 16384, 32 * j, h, (int)t0, b);
+    for (int j = 0; j < 4; ++j) ptx::tma_store_4d(&mapDK, smem + 65536 + j * 16384, 32 * j, h, (int)t0, b);
+    for (int j = 0; j < 2; ++j) ptx::tma_store_4d(&mapDV, smem + 131072 + j * 16384, 32 * j, h, (int)t0, b);
+    ptx::bulk_commit_group();
+    ptx::bulk_wait_read_all();  // the staging is read before the CTA ends
   }
   if (tid == 128) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
     wait_bar(&bar_ld, 0);
@@ -1087,15 +1100,18 @@ cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k,
                                 float* dlam, float* cu, unsigned* status, cudaStream_t st) {
   if (!tc_supported(s)) return cudaErrorInvalidValue;
   const int G = s.heads / s.heads_per_group, NT = s.T / kTile;
-  CUtensorMap mQ, mK, mV, mD;
+  CUtensorMap mQ, mK, mV, mD, mDQ, mDK, mDV;
   if (!make_map(&mQ, q, kDk, G, s.T, s.batch) || !make_map(&mK, k, kDk, G, s.T, s.batch) ||
-      !make_map(&mV, v, kDv, s.heads, s.T, s.batch) || !make_map(&mD, dO, kDv, s.heads, s.T, s.batch))
+      !make_map(&mV, v, kDv, s.heads, s.T, s.batch) || !make_map(&mD, dO, kDv, s.heads, s.T, s.batch) ||
+      !make_map_f32(&mDQ, dq32, kDk, s.heads, s.T, s.batch) || !make_map_f32(&mDK, dk32, kDk, s.heads, s.T, s.batch) ||
+      !make_map_f32(&mDV, dv32, kDv, s.heads, s.T, s.batch))
     return cudaErrorInvalidValue;
   const TcBwdParams p{s.batch, s.T, s.heads, s.heads_per_group, G, s.levels, NT, a, lam,
                       dq32, dk32, dv32, dlam, cu, status};
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwd);
   if (e != cudaSuccess) return e;
-  tc_bwd_intra_kernel<<<(unsigned)((size_t)s.batch * NT * s.heads), 256, kSmemBwd, st>>>(mQ, mK, mV, mD, p);
+  tc_bwd_intra_kernel<<<(unsigned)((size_t)s.batch * NT * s.heads), 256, kSmemBwd, st>>>(mQ, mK, mV, mD, mDQ, mDK,
+                                                                                   mDV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;

@@ -212,6 +212,21 @@ bool make_map(CUtensorMap* m, const void* base, int inner, int count, int T, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D fp32 map over (inner, count, T, B) with a (32, 1, 128, 1) box (128-byte rows),
+// 128-byte swizzle: the per-head fp32 gradient rows of a 128-token tile, 32 columns a box.
+bool make_map_f32(CUtensorMap* m, void* base, int inner, int count, int T, int B) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)count, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)inner * 4, (cuuint64_t)inner * 4 * count,
+                           (cuuint64_t)inner * 4 * count * T};
+  cuuint32_t box[4] = {32, 1, kTile, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
