@@ -86,6 +86,15 @@ __device__ __forceinline__ void tma_store_4d(const void* tmap, const void* src, 
                "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
                : "memory");
 }
+// Tiled TMA reduction shared -> global: adds the box element-wise (in the map's element
+// type) into the global tensor, in the bulk async-group of the issuing thread.
+__device__ __forceinline__ void tma_reduce_add_4d(const void* tmap, const void* src, int c0, int c1, int c2,
+                                                  int c3) {
+  asm volatile("cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::
+                   "l"(tmap),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk store of this thread has read its shared-memory source.
 __device__ __forceinline__ void bulk_wait_read_all() {

@@ -508,6 +508,7 @@ __host__ __device__ constexpr int bwdq_smem_bytes(int ninter) {
 
 __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                           const __grid_constant__ CUtensorMap mapD,
+                                                          const __grid_constant__ CUtensorMap mapDQ,
                                                           TcBwdQParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -766,17 +767,27 @@ __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant_
     ptx::tc_fence_before();
     ptx::mbar_arrive(&bar_yf);
   }
+  // dq rows (columns 64 hf .. 64 hf + 63: boxes 2 hf, 2 hf + 1) are staged over Q, dO and
+  // the images, free once every level is read, and added into the per-head buffer (which
+  // the in-tile kernel wrote) with TMA reductions.
+  __syncthreads();
   if (ok) {
-    float* dst = p.dq32 + (row * p.H + h) * kDk + hf * 64;
 #pragma unroll
-    for (int j = 0; j < 64; j += 4) {
-      float4 o = *reinterpret_cast<float4*>(dst + j);
-      o.x += acc[j];
-      o.y += acc[j + 1];
-      o.z += acc[j + 2];
-      o.w += acc[j + 3];
-      *reinterpret_cast<float4*>(dst + j) = o;
+    for (int j2 = 0; j2 < 2; ++j2) {
+      uint8_t* box = smem + (2 * hf + j2) * 16384 + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(box + ((c ^ rot) << 4)) =
+            make_float4(acc[32 * j2 + 4 * c], acc[32 * j2 + 4 * c + 1], acc[32 * j2 + 4 * c + 2],
+                        acc[32 * j2 + 4 * c + 3]);
     }
+    ptx::fence_proxy_async_smem();
+  }
+  ok = __syncthreads_and(ok);
+  if (ok && tid == 0) {
+    for (int j = 0; j < 4; ++j) ptx::tma_reduce_add_4d(&mapDQ, smem + j * 16384, 32 * j, h, (int)t0, b);
+    ptx::bulk_commit_group();
+    ptx::bulk_wait_read_all();  // the staging is read before the CTA ends
   }
   if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
     wait_bar(&bar_ld, 0);
@@ -863,10 +874,12 @@ struct TcBwdKVParams {
   unsigned* status;
 };
 
-constexpr int kSmemBwdKV = 32768 + 16384 + 2 * kImgBytes + 1024;
+constexpr int kSmemBwdKV = 98304 + 1024;  // K, V, two dual images; then the dk and dv staging
 
 __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap mapK,
                                                            const __grid_constant__ CUtensorMap mapV,
+                                                           const __grid_constant__ CUtensorMap mapDK,
+                                                           const __grid_constant__ CUtensorMap mapDV,
                                                            TcBwdKVParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1047,28 +1060,8 @@ __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant
     ptx::tc_fence_before();
     ptx::mbar_arrive(&bar_zf);
   }
+  const float rs = exp2f(gam - gt);
   if (ok) {
-    const float rs = exp2f(gam - gt);
-    float* dk = p.dk32 + (row * p.H + h) * kDk + qq * 32;
-    float* dv = p.dv32 + (row * p.H + h) * kDv + qq * 16;
-#pragma unroll
-    for (int c = 0; c < 32; c += 4) {
-      float4 o = *reinterpret_cast<float4*>(dk + c);
-      o.x += rs * ak[c];
-      o.y += rs * ak[c + 1];
-      o.z += rs * ak[c + 2];
-      o.w += rs * ak[c + 3];
-      *reinterpret_cast<float4*>(dk + c) = o;
-    }
-#pragma unroll
-    for (int c = 0; c < 16; c += 4) {
-      float4 o = *reinterpret_cast<float4*>(dv + c);
-      o.x += rs * av[c];
-      o.y += rs * av[c + 1];
-      o.z += rs * av[c + 2];
-      o.w += rs * av[c + 3];
-      *reinterpret_cast<float4*>(dv + c) = o;
-    }
     // v_s . (these d_v columns): V is fp16 in shared memory, 2^ev times the input
     float cdot = 0.f;
 #pragma unroll
@@ -1082,6 +1075,31 @@ __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant
       }
     }
     atomicAdd(p.cu + row * p.H + h, rs * pow2i(ev) * cdot);
+  }
+  // dk (columns 32 qq .. 32 qq + 31: box qq, from 0) and dv (columns 16 qq .. 16 qq + 15:
+  // half of box qq >> 1, from 64 KB) are staged over K, V and the images, free once every
+  // level is read and V's dot is taken, and added into the per-head buffers with TMA
+  // reductions.
+  __syncthreads();
+  if (ok) {
+    uint8_t* kb = smem + qq * 16384 + r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<float4*>(kb + ((c ^ rot) << 4)) =
+          make_float4(rs * ak[4 * c], rs * ak[4 * c + 1], rs * ak[4 * c + 2], rs * ak[4 * c + 3]);
+    uint8_t* vb = smem + 65536 + (qq >> 1) * 16384 + r * 128;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<float4*>(vb + (((4 * (qq & 1) + c) ^ rot) << 4)) =
+          make_float4(rs * av[4 * c], rs * av[4 * c + 1], rs * av[4 * c + 2], rs * av[4 * c + 3]);
+    ptx::fence_proxy_async_smem();
+  }
+  ok = __syncthreads_and(ok);
+  if (ok && tid == 0) {
+    for (int j = 0; j < 4; ++j) ptx::tma_reduce_add_4d(&mapDK, smem + j * 16384, 32 * j, h, (int)t0, b);
+    for (int j = 0; j < 2; ++j) ptx::tma_reduce_add_4d(&mapDV, smem + 65536 + j * 16384, 32 * j, h, (int)t0, b);
+    ptx::bulk_commit_group();
+    ptx::bulk_wait_read_all();  // the staging is read before the CTA ends
   }
   if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
     wait_bar(&bar_ld, 0);
@@ -1120,8 +1138,9 @@ cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k,
 cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, const float* a, const float* lam,
                             const char* tree_ws, float* dq32, float* dlam, float* dual, const int* dual_off,
                             int nslots, unsigned* status, cudaStream_t st) {
-  CUtensorMap mQ, mD;
-  if (!make_map(&mQ, q, kDk, tp.G, tp.T, tp.B) || !make_map(&mD, dO, kDv, tp.H, tp.T, tp.B))
+  CUtensorMap mQ, mD, mDQ;
+  if (!make_map(&mQ, q, kDk, tp.G, tp.T, tp.B) || !make_map(&mD, dO, kDv, tp.H, tp.T, tp.B) ||
+      !make_map_f32(&mDQ, dq32, kDk, tp.H, tp.T, tp.B))
     return cudaErrorInvalidValue;
   TcBwdQParams p{};
   p.B = tp.B;
@@ -1148,7 +1167,7 @@ cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, con
   const int smem = bwdq_smem_bytes(bit_length(tp.NT - 1));
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tc_bwd_q_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 256, smem, st>>>(mQ, mD, p);
+  tc_bwd_q_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 256, smem, st>>>(mQ, mD, mDQ, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
@@ -1166,8 +1185,9 @@ cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, con
   tc_dual_publish_kernel<<<(unsigned)((size_t)BH * nslots), 128, 0, st>>>(dual, dimg, dmeta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
-  CUtensorMap mK, mV;
-  if (!make_map(&mK, k, kDk, tp.G, tp.T, tp.B) || !make_map(&mV, v, kDv, tp.H, tp.T, tp.B))
+  CUtensorMap mK, mV, mDK, mDV;
+  if (!make_map(&mK, k, kDk, tp.G, tp.T, tp.B) || !make_map(&mV, v, kDv, tp.H, tp.T, tp.B) ||
+      !make_map_f32(&mDK, dk32, kDk, tp.H, tp.T, tp.B) || !make_map_f32(&mDV, dv32, kDv, tp.H, tp.T, tp.B))
     return cudaErrorInvalidValue;
   TcBwdKVParams p{};
   p.B = tp.B;
@@ -1190,7 +1210,7 @@ cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, con
   if ((e = cudaFuncSetAttribute(tc_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwdKV)) !=
       cudaSuccess)
     return e;
-  tc_bwd_kv_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 512, kSmemBwdKV, st>>>(mK, mV, p);
+  tc_bwd_kv_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 512, kSmemBwdKV, st>>>(mK, mV, mDK, mDV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
