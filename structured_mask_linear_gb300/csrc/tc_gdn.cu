@@ -174,79 +174,57 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     for (int t = 0; t < 16; ++t) Tm[(r0 + t) * kGP + r0 + j] = x[t];
   }
   __syncthreads();
-  // blocks below the diagonal, column block by column block (each needs only the diagonal
-  // blocks and its own earlier ones):
-  //   Y = sum_{jb <= k < ib} A_{ib,k} T_{k,jb},  T_{ib,jb} = -T_{ib,ib} Y,  ib = jb+1 .. 7.
-  // The work of column block jb falls with jb: blocks 0, 1, 2 go to warp pairs (rows
-  // split, a 64-thread barrier per step), blocks 3 + 6 and 4 + 5 to single warps.
-  if (ok) {
-    const bool pair = warp < 6;
-    const int njb = pair ? 1 : 2;
-    const int jb0 = pair ? (warp >> 1) : (warp == 6 ? 3 : 4);
-    float* Yw = Ym + (pair ? (warp >> 1) : warp - 3) * 256;
-    for (int q = 0; q < njb; ++q) {
-      const int jb = q == 0 ? jb0 : 9 - jb0;  // 3 then 6, 4 then 5
-      for (int ib = jb + 1; ib < 8; ++ib) {
-        if (pair) {  // rows 8 (warp & 1) + lane / 4, columns 4 (lane % 4) .. + 3
-          const int rr = (warp & 1) * 8 + (lane >> 2), c0 = (lane & 3) * 4;
-          float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
-          const float* arow = Am + (16 * ib + rr) * kGP;
-#pragma unroll 4
-          for (int s2 = 16 * jb; s2 < 16 * ib; ++s2) {
-            const float av = arow[s2];
-            const float4 tv = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0);
-            y0 += av * tv.x; y1 += av * tv.y; y2 += av * tv.z; y3 += av * tv.w;
-          }
-          *reinterpret_cast<float4*>(Yw + rr * 16 + c0) = make_float4(y0, y1, y2, y3);
-          ptx::named_bar_sync(1 + (warp >> 1), 64);
-          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-          const float* trow = Tm + (16 * ib + rr) * kGP + 16 * ib;
-#pragma unroll 4
-          for (int s2 = 0; s2 < 16; ++s2) {
-            const float tv = trow[s2];
-            const float4 yv = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0);
-            x0 += tv * yv.x; x1 += tv * yv.y; x2 += tv * yv.z; x3 += tv * yv.w;
-          }
-          *reinterpret_cast<float4*>(Tm + (16 * ib + rr) * kGP + 16 * jb + c0) = make_float4(-x0, -x1, -x2, -x3);
-          ptx::named_bar_sync(1 + (warp >> 1), 64);
-        } else {  // row lane / 2, columns 8 (lane % 2) .. + 7
-          const int rr = lane >> 1, c0 = (lane & 1) * 8;
-          float y[8];
+  // Blocks below the diagonal by doubling: once the inverses T11 and T22 of two adjacent
+  // diagonal blocks of size n are known, the block below them is T21 = -T22 A21 T11, A21
+  // the block of A between them (the inverse of a 2 x 2 block lower triangle).  For n =
+  // 16, 32, 64 every pair is done at once: X = A21 T11 into A's upper triangle (zero and
+  // not read again) at rows i0.., columns i0 + n.., then T21 = -T22 X.  Each thread takes
+  // 4 x 4 outputs, the column tiles fastest across a warp: the rows it reads of A21 and T22
+  // are the same for many threads (broadcasts), the rows of T11 and X are read along
+  // (conflict-free).  T22 is lower triangular, so its sum stops at the tile's last row.
+  for (int n = 16; n < 128; n *= 2) {
+    const int nt = n / 4, per = nt * nt, items = (128 / (2 * n)) * per;
+    if (ok)
+      for (int w = tid; w < items; w += 256) {  // X = A21 T11
+        const int i0 = (w / per) * 2 * n, tj = (w % nt) * 4, ti = ((w % per) / nt) * 4;
+        float acc[4][4] = {};
+        const float* arow = Am + (i0 + n + ti) * kGP + i0;
+#pragma unroll 2
+        for (int k = 0; k < n; ++k) {
+          const float4 tv = *reinterpret_cast<const float4*>(Tm + (i0 + k) * kGP + i0 + tj);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = 0.f;
-          const float* arow = Am + (16 * ib + rr) * kGP;
-#pragma unroll 4
-          for (int s2 = 16 * jb; s2 < 16 * ib; ++s2) {
-            const float av = arow[s2];
-            const float4 t0v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0);
-            const float4 t1v = *reinterpret_cast<const float4*>(Tm + s2 * kGP + 16 * jb + c0 + 4);
-            y[0] += av * t0v.x; y[1] += av * t0v.y; y[2] += av * t0v.z; y[3] += av * t0v.w;
-            y[4] += av * t1v.x; y[5] += av * t1v.y; y[6] += av * t1v.z; y[7] += av * t1v.w;
+          for (int ii = 0; ii < 4; ++ii) {
+            const float av = arow[ii * kGP + k];
+            acc[ii][0] += av * tv.x; acc[ii][1] += av * tv.y; acc[ii][2] += av * tv.z; acc[ii][3] += av * tv.w;
           }
-          *reinterpret_cast<float4*>(Yw + rr * 16 + c0) = make_float4(y[0], y[1], y[2], y[3]);
-          *reinterpret_cast<float4*>(Yw + rr * 16 + c0 + 4) = make_float4(y[4], y[5], y[6], y[7]);
-          __syncwarp();
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
-          const float* trow = Tm + (16 * ib + rr) * kGP + 16 * ib;
-#pragma unroll 4
-          for (int s2 = 0; s2 < 16; ++s2) {
-            const float tv = trow[s2];
-            const float4 y0 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0);
-            const float4 y1 = *reinterpret_cast<const float4*>(Yw + s2 * 16 + c0 + 4);
-            x[0] += tv * y0.x; x[1] += tv * y0.y; x[2] += tv * y0.z; x[3] += tv * y0.w;
-            x[4] += tv * y1.x; x[5] += tv * y1.y; x[6] += tv * y1.z; x[7] += tv * y1.w;
-          }
-          float* dst = Tm + (16 * ib + rr) * kGP + 16 * jb + c0;
-          *reinterpret_cast<float4*>(dst) = make_float4(-x[0], -x[1], -x[2], -x[3]);
-          *reinterpret_cast<float4*>(dst + 4) = make_float4(-x[4], -x[5], -x[6], -x[7]);
-          __syncwarp();
         }
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii)
+          *reinterpret_cast<float4*>(Am + (i0 + ti + ii) * kGP + i0 + n + tj) =
+              make_float4(acc[ii][0], acc[ii][1], acc[ii][2], acc[ii][3]);
       }
-    }
+    __syncthreads();
+    if (ok)
+      for (int w = tid; w < items; w += 256) {  // T21 = -T22 X
+        const int i0 = (w / per) * 2 * n, tj = (w % nt) * 4, ti = ((w % per) / nt) * 4;
+        float acc[4][4] = {};
+        const float* trow = Tm + (i0 + n + ti) * kGP + i0 + n;
+#pragma unroll 2
+        for (int k = 0; k < ti + 4; ++k) {
+          const float4 xv = *reinterpret_cast<const float4*>(Am + (i0 + k) * kGP + i0 + n + tj);
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii) {
+            const float tv = trow[ii * kGP + k];
+            acc[ii][0] += tv * xv.x; acc[ii][1] += tv * xv.y; acc[ii][2] += tv * xv.z; acc[ii][3] += tv * xv.w;
+          }
+        }
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii)
+          *reinterpret_cast<float4*>(Tm + (i0 + n + ti + ii) * kGP + i0 + tj) =
+              make_float4(-acc[ii][0], -acc[ii][1], -acc[ii][2], -acc[ii][3]);
+      }
+    __syncthreads();
   }
-  __syncthreads();
   // tile scales of T, diag(beta 2^g) K, diag(beta) V (maxima over their elements)
   {
     float mt = 0.f, mk = 0.f, mv = 0.f;
