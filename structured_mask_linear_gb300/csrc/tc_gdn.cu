@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   float* gs = Ym + 8 * 256;                                    // 128: g
   float* bs = gs + 128;                                        // 128: beta
   float* fk = bs + 128;                                        // 128: beta 2^g
+  float* b8 = fk + 128;                                        // 128: 2^(g_end8(s) - g_s)
   __shared__ __align__(8) uint64_t bar_ld, bar_a, bar_w;
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[8];
@@ -125,36 +126,55 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     ptx::umma_commit(&bar_a);
   }
   const bool a_issued = ok;
+  if (tid < 128) b8[r] = exp2f(gs[r | 7] - gt);  // decay from key r to the end of its 8-block
   if (ok) {
     ok = wait_bar(&bar_a, 0);
     if (!ok) atomicExch(p.status, kStatusTimeout);
   }
   ok = __syncthreads_and(ok);
-  // A_ts = beta_t 2^(g_t - g_s) (k_t . k_s), s < t (threads 0..127: row t); T zeroed above
+  // A_ts = beta_t 2^(g_t - g_s) (k_t . k_s), s < t (threads 0..127: row t); T zeroed by
+  // the others.  Only the lower triangle of A is read later, so a warp stops at the 32-key
+  // group of its own rows.  In an earlier group, 2^(g_t - g_s) is 2^(g_t - g_end8) b8[s]
+  // (both factors <= 1) with one exp2 per 8-key block; the rows' own group takes one exp2
+  // per key.
   if (ok) {
     ptx::tc_fence_after();
     if (tid < 128) {
       const int t = r;
       const float bt = bs[t];
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 <= quad * 32; c0 += 32) {  // warp-uniform
         float y[32];
         ptx::tmem_ld32(tA + lane_off + c0, y);
         ptx::tmem_ld_wait();
+        if (c0 < quad * 32) {  // an earlier group: every block before t's (warp-uniform)
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float4 v;
-          float* vv = reinterpret_cast<float*>(&v);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int s2 = c0 + j + e;
-            vv[e] = s2 < t ? bt * exp2f(gt - gs[s2]) * y[j + e] : 0.f;
+          for (int kb = 0; kb < 4; ++kb) {
+            const int blk = (c0 >> 3) + kb;
+            const float fb = bt * exp2f(gt - gs[8 * blk + 7]);
+            const float4 b0 = *reinterpret_cast<const float4*>(b8 + 8 * blk);
+            const float4 b1 = *reinterpret_cast<const float4*>(b8 + 8 * blk + 4);
+            const float* yy = y + 8 * kb;
+            *reinterpret_cast<float4*>(Am + t * kGP + 8 * blk) =
+                make_float4(fb * b0.x * yy[0], fb * b0.y * yy[1], fb * b0.z * yy[2], fb * b0.w * yy[3]);
+            *reinterpret_cast<float4*>(Am + t * kGP + 8 * blk + 4) =
+                make_float4(fb * b1.x * yy[4], fb * b1.y * yy[5], fb * b1.z * yy[6], fb * b1.w * yy[7]);
           }
-          *reinterpret_cast<float4*>(Am + t * kGP + c0 + j) = v;
+        } else {  // the rows' own group: one exp2 per key
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int s2 = c0 + j + e;
+              v[e] = s2 < t ? bt * exp2f(gt - gs[s2]) * y[j + e] : 0.f;
+            }
+            *reinterpret_cast<float4*>(Am + t * kGP + c0 + j) = make_float4(v[0], v[1], v[2], v[3]);
+          }
         }
       }
     } else {
-      for (int e = r; e < 128 * kGP; e += 128) Tm[e] = 0.f;
+      for (int e = 4 * r; e < 128 * kGP; e += 512) *reinterpret_cast<float4*>(Tm + e) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
   ptx::tc_fence_before();
