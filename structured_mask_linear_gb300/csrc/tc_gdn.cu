@@ -370,8 +370,11 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     if (!ok) atomicExch(p.status, kStatusTimeout);
   }
   ok = __all_sync(0xffffffffu, ok);
-  // W: its tile maximum, then hi and lo fp16 of W 2^-ew in the operand layout; U_loc, g
-  uint8_t* dst = p.xw + ((size_t)(b * p.H + h) * nch + c) * kGdnChunkBytes;
+  // W: its tile maximum, then hi and lo fp16 of W 2^-ew in the operand layout; U_loc, g.
+  // The chunk's workspace record is put together in shared memory (free: the products
+  // have read their operands), in its global layout, then copied out by all threads with
+  // consecutive 16-byte stores.
+  uint8_t* dst = smem;
   const float sw = pow2s(et + ek), su = pow2s(et + ev);
   float mw = 0.f;
   if (ok && tid < 128) {
@@ -420,6 +423,12 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     }
     reinterpret_cast<float*>(dst + kGdnOffG)[r] = gt;
     if (r == 0) *reinterpret_cast<int*>(dst + kGdnOffE) = ew;
+  }
+  ok = __syncthreads_and(ok);  // the record is complete
+  if (ok) {
+    uint4* gdst = reinterpret_cast<uint4*>(p.xw + ((size_t)(b * p.H + h) * nch + c) * kGdnChunkBytes);
+    const uint4* ssrc = reinterpret_cast<const uint4*>(smem);
+    for (int i = tid; i < (int)(kGdnChunkBytes / 16); i += 256) gdst[i] = ssrc[i];
   }
   if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
     wait_bar(&bar_ld, 0);
