@@ -418,7 +418,18 @@ __global__ void __launch_bounds__(kDlChunk) bwd_dloga_local(GenPlan p, BwdArgs x
   if (t < p.T) {
     const size_t row = ((size_t)b * p.T + t) * p.H + h;
     float R = 0.f, Cv = 0.f;
-    for (int l = 0; l < L; ++l) R += x.lam[row * L + l] * x.dlam[row * L + l];
+    if ((L & 1) == 0) {  // rows of an even level count are 8-byte aligned: pairs
+      const float2* l2 = reinterpret_cast<const float2*>(x.lam + row * L);
+      const float2* d2 = reinterpret_cast<const float2*>(x.dlam + row * L);
+#pragma unroll 4
+      for (int l = 0; l < L / 2; ++l) {
+        const float2 a2 = l2[l], b2 = d2[l];
+        R += a2.x * b2.x + a2.y * b2.y;
+      }
+    } else {
+#pragma unroll 4
+      for (int l = 0; l < L; ++l) R += x.lam[row * L + l] * x.dlam[row * L + l];
+    }
     if (cu) {
       Cv = cu[row];
     } else {
