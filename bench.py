@@ -44,12 +44,13 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the long/decode/e2e extras")
     ap.add_argument("--ncu-case", nargs="?", const="fwd",
-                    choices=["fwd", "bwd", "gdn", "decode", "long"],
+                    choices=["fwd", "bwd", "gdn", "decode", "decode64", "long"],
                     help="profiling case, no timing, no JSON: on the pages workload at batch 1 "
                          "(inputs 225 MB > L2) three forwards (fwd, the default), two backwards "
                          "(bwd) or two Gated DeltaNet forwards (gdn); decode: three decode steps "
-                         "of the decode workload at batch 8 (states 214 MB > L2); long: two "
-                         "forwards of the long workload's shape with 4 of its 48 heads")
+                         "of the decode workload at batch 8 (states 214 MB > L2); decode64: 64 "
+                         "steps of the decode workload itself (batch 64, positions 32768..32831); "
+                         "long: two forwards of the long workload's shape with 4 of its 48 heads")
     return ap.parse_args()
 
 
@@ -158,10 +159,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def traffic_for(kernel: str, w, key: str | None = None):
+def traffic_for(kernel: str, w, key: str | None = None, algorithmic: float | None = None):
     """ncu DRAM bytes per launch from profiles/traffic.json, if the kernel's source is
     unchanged since the capture (scaled to this workload's units: the record holds bytes
-    per token of all heads).  key names the record (default: the kernel's name)."""
+    per token of all heads, or, with `algorithmic` given, DRAM bytes per algorithmic byte
+    over a run of launches).  key names the record (default: the kernel's name)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -177,6 +179,8 @@ def traffic_for(kernel: str, w, key: str | None = None):
         h.update(open(src, "rb").read())
     if h.hexdigest() != d["source_sha256"]:
         return None
+    if algorithmic is not None:
+        return d["bytes_per_algorithmic_byte"] * algorithmic if "bytes_per_algorithmic_byte" in d else None
     return d["bytes_per_token"] * w.batch * w.T
 
 
@@ -286,10 +290,11 @@ def ncu_case(what: str = "fwd"):
     from structured_mask_linear_gb300.inputs import make_inputs, workload
 
     sml.lib()
-    if what == "decode":
-        wd = workload("decode", batch=8)
-        st, lsc, q, k, v, a, lam = decode_inputs(torch, wd, "cuda", steps=3)
-        for i in range(3):
+    if what in ("decode", "decode64"):
+        wd = workload("decode", batch=8) if what == "decode" else workload("decode")
+        n = 3 if what == "decode" else 64
+        st, lsc, q, k, v, a, lam = decode_inputs(torch, wd, "cuda", steps=n)
+        for i in range(n):
             sml.loglinear_decode_step(wd.T + i, q[i], k[i], v[i], a[i], lam[i], st, lsc)
         torch.cuda.synchronize()
         assert sml.loglinear_check_status() == 0
@@ -701,17 +706,41 @@ def decode_measure(sml, torch, dev, hbm_peak, steps=1024):
         sml.loglinear_decode_step(w.T + i, q[i], k[i], v[i], a[i], lam[i], st, lsc, o_t=o)
     e1.record()
     torch.cuda.synchronize()
+    ms_eager = e0.elapsed_time(e1) / steps
+    # The same steps captured once in a CUDA graph and replayed: one launch per step without
+    # the host's per-call work between them (the positions, hence the live levels and the
+    # work, are those of the eager loop; the state values do not change the work).
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(steps):
+                sml.loglinear_decode_step(w.T + i, q[i], k[i], v[i], a[i], lam[i], st, lsc, o_t=o)
+    torch.cuda.current_stream().wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if sml.loglinear_check_status() != 0:
+        raise RuntimeError("decode: device status set")
     ms = e0.elapsed_time(e1) / steps
+    del graph
     nbytes = sum(decode_bytes(w, w.T + i) for i in range(steps)) / steps
     res = {"workload": f"decode: B={B} H={H} d_k={w.d_k} d_v={w.d_v}, positions "
                        f"{w.T}..{w.T + steps - 1}, {L} fp32 state levels",
            "value": B / (ms / 1e3), "unit": "tokens/s", "us_per_step": 1e3 * ms,
+           "launch": "the steps replayed from one CUDA graph",
+           "us_per_step_eager_loop": 1e3 * ms_eager,
            "achieved_gbs": nbytes / (ms / 1e3) / 1e9, "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
            "algorithmic_bytes_per_step": int(nbytes),
            "roofline": {"bound": "hbm", "kernel": "decode_step_kernel",
                         "achieved": nbytes / (ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                         "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
-                        "traffic": traffic_for("decode_step_kernel", w, key="decode_step_kernel:decode"),
+                        "traffic": traffic_for("decode_step_kernel", w, key="decode_step_kernel:decode",
+                                               algorithmic=nbytes),
                         "algorithmic_bytes_per_launch": int(nbytes)}}
     del st, lsc, q, k, v, a, lam, o
     torch.cuda.empty_cache()
