@@ -14,9 +14,10 @@ namespace {
 //
 // tc_gdn_local, one CTA per (b, h, chunk), 256 threads, one CTA per SM:
 //   K Kᵀ on tcgen05 from the bf16 keys (exact products, fp32 sums); A in fp32 in shared
-//   memory; T by 16-row blocks on the CUDA cores (diagonal blocks by substitution in
-//   registers, then T_ij = -T_ii sum_{j <= k < i} A_ik T_kj column block by column block);
-//   then [W | U_loc] = T [diag(beta 2^g) K | diag(beta) V] on tcgen05 with every operand
+//   memory (meanwhile the other four warps take the K and V tile maxima and split
+//   diag(beta) V); T on the CUDA cores (its 16 x 16 diagonal blocks by substitution in
+//   registers, then the blocks below them by doubling, T21 = -T22 A21 T11 for blocks of
+//   16, 32 and 64); then [W | U_loc] = T [diag(beta 2^g) K | diag(beta) V] on tcgen05 with every operand
 //   split into an fp16 high part and the fp16 rounding remainder (hi hi + lo hi + hi lo,
 //   about 22 significant bits), each with a power-of-two tile scale.  Per chunk the
 //   workspace gets W split the same way (hi and lo fp16 in the MMA operand layout, with
@@ -37,7 +38,12 @@ struct TcGdnParams {
 };
 
 constexpr int kGP = 132;  // padded fp32 row of the 128 x 128 matrices
-constexpr int kSmemGdnL = 32768 + 16384 + 2 * 128 * kGP * 4 + 8 * 256 * 4 + 4 * 128 * 4 + 1024;
+constexpr int kSmemGdnL = 32768 + 16384 + 2 * 128 * kGP * 4 + 8 * 256 * 4 + 4 * 128 * 4 + 32768 + 1024;
+
+// component i (0..3, known at compile time after unrolling) of a float4
+__device__ __forceinline__ float f4_at(const float4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
 
 // fp32 value -> fp16 high part and fp16 remainder, both of x * 2^-e
 __device__ __forceinline__ void split_h(float x, float sc, __half& hi, __half& lo) {
@@ -60,10 +66,13 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   float* bs = gs + 128;                                        // 128: beta
   float* fk = bs + 128;                                        // 128: beta 2^g
   float* b8 = fk + 128;                                        // 128: 2^(g_end8(s) - g_s)
+  uint8_t* VHI = reinterpret_cast<uint8_t*>(b8 + 128);         // 16 KB: diag(beta) V hi (fp16)
+  uint8_t* VLO = VHI + 16384;                                  // 16 KB: ... lo
   __shared__ __align__(8) uint64_t bar_ld, bar_a, bar_w;
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[8];
-  __shared__ float s_mx[8][3];
+  __shared__ float s_mx[8];
+  __shared__ float s_kv[4][2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
   const int r = tid & 127, rot = r & 7;
@@ -175,6 +184,43 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
       }
     } else {
       for (int e = 4 * r; e < 128 * kGP; e += 512) *reinterpret_cast<float4*>(Tm + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      // the tile maxima of diag(beta 2^g) K and diag(beta) V (row r each), then V's fp16 hi
+      // and lo parts (B operand, MN-major: row s, 64 d_v), by these otherwise idle warps
+      uint32_t m0 = 0u, m1 = 0u;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const int off = r * 128 + ((cc ^ rot) << 4);
+        m0 = absmax_u4(absmax_u4(m0, *reinterpret_cast<const uint4*>(RK + off)),
+                       *reinterpret_cast<const uint4*>(RK + 16384 + off));
+        m1 = absmax_u4(m1, *reinterpret_cast<const uint4*>(RV + off));
+      }
+      float mk = bf16x2_maxhalf(m0) * fabsf(fk[r]), mv = bf16x2_maxhalf(m1) * fabsf(bs[r]);
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
+        mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+      }
+      if (lane == 0) {
+        s_kv[warp - 4][0] = mk;
+        s_kv[warp - 4][1] = mv;
+      }
+      ptx::named_bar_sync(1, 128);
+      const int ev = f16_exp(fmaxf(fmaxf(s_kv[0][1], s_kv[1][1]), fmaxf(s_kv[2][1], s_kv[3][1])));
+      const float sc = bs[r] * pow2i(-ev);
+#pragma unroll 1
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint32_t off = r * 128 + ((cc ^ rot) << 4);
+        const uint4 x = *reinterpret_cast<const uint4*>(RV + off);
+        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+        __half hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          split_h(__uint_as_float(w4[e] << 16), sc, hi[2 * e], lo[2 * e]);
+          split_h(__uint_as_float(w4[e] & 0xffff0000u), sc, hi[2 * e + 1], lo[2 * e + 1]);
+        }
+        *reinterpret_cast<uint4*>(VHI + off) = *reinterpret_cast<const uint4*>(hi);
+        *reinterpret_cast<uint4*>(VLO + off) = *reinterpret_cast<const uint4*>(lo);
+      }
     }
   }
   ptx::tc_fence_before();
@@ -209,13 +255,19 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
         const int i0 = (w / per) * 2 * n, tj = (w % nt) * 4, ti = ((w % per) / nt) * 4;
         float acc[4][4] = {};
         const float* arow = Am + (i0 + n + ti) * kGP + i0;
-#pragma unroll 2
-        for (int k = 0; k < n; ++k) {
-          const float4 tv = *reinterpret_cast<const float4*>(Tm + (i0 + k) * kGP + i0 + tj);
+#pragma unroll 1
+        for (int k = 0; k < n; k += 4) {  // four k at a time: A21's rows read 16 bytes at once
+          float4 av[4];
 #pragma unroll
-          for (int ii = 0; ii < 4; ++ii) {
-            const float av = arow[ii * kGP + k];
-            acc[ii][0] += av * tv.x; acc[ii][1] += av * tv.y; acc[ii][2] += av * tv.z; acc[ii][3] += av * tv.w;
+          for (int ii = 0; ii < 4; ++ii) av[ii] = *reinterpret_cast<const float4*>(arow + ii * kGP + k);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const float4 tv = *reinterpret_cast<const float4*>(Tm + (i0 + k + kk) * kGP + i0 + tj);
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+              const float a = f4_at(av[ii], kk);
+              acc[ii][0] += a * tv.x; acc[ii][1] += a * tv.y; acc[ii][2] += a * tv.z; acc[ii][3] += a * tv.w;
+            }
           }
         }
 #pragma unroll
@@ -229,13 +281,19 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
         const int i0 = (w / per) * 2 * n, tj = (w % nt) * 4, ti = ((w % per) / nt) * 4;
         float acc[4][4] = {};
         const float* trow = Tm + (i0 + n + ti) * kGP + i0 + n;
-#pragma unroll 2
-        for (int k = 0; k < ti + 4; ++k) {
-          const float4 xv = *reinterpret_cast<const float4*>(Am + (i0 + k) * kGP + i0 + n + tj);
+#pragma unroll 1
+        for (int k = 0; k < ti + 4; k += 4) {  // four k at a time: T22's rows read 16 bytes at once
+          float4 tv[4];
 #pragma unroll
-          for (int ii = 0; ii < 4; ++ii) {
-            const float tv = trow[ii * kGP + k];
-            acc[ii][0] += tv * xv.x; acc[ii][1] += tv * xv.y; acc[ii][2] += tv * xv.z; acc[ii][3] += tv * xv.w;
+          for (int ii = 0; ii < 4; ++ii) tv[ii] = *reinterpret_cast<const float4*>(trow + ii * kGP + k);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const float4 xv = *reinterpret_cast<const float4*>(Am + (i0 + k + kk) * kGP + i0 + n + tj);
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+              const float t = f4_at(tv[ii], kk);
+              acc[ii][0] += t * xv.x; acc[ii][1] += t * xv.y; acc[ii][2] += t * xv.z; acc[ii][3] += t * xv.w;
+            }
           }
         }
 #pragma unroll
@@ -245,45 +303,29 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
       }
     __syncthreads();
   }
-  // tile scales of T, diag(beta 2^g) K, diag(beta) V (maxima over their elements)
+  // tile scale of T (the maximum over its elements); those of K and V came with the A phase
   {
-    float mt = 0.f, mk = 0.f, mv = 0.f;
+    float mt = 0.f;
     if (ok) {
-      // thread: T row r, half (tid >> 7) of its columns; K and V rows r (tid < 128)
-      const float* trow = Tm + r * kGP + (tid >> 7) * 64;
-      for (int j = 0; j < 64; ++j) mt = fmaxf(mt, fabsf(trow[j]));
-      if (tid < 128) {
-        uint32_t m0 = 0u, m1 = 0u;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const int off = r * 128 + ((cc ^ rot) << 4);
-          m0 = absmax_u4(absmax_u4(m0, *reinterpret_cast<const uint4*>(RK + off)),
-                         *reinterpret_cast<const uint4*>(RK + 16384 + off));
-          m1 = absmax_u4(m1, *reinterpret_cast<const uint4*>(RV + off));
-        }
-        mk = bf16x2_maxhalf(m0) * fabsf(fk[r]);
-        mv = bf16x2_maxhalf(m1) * fabsf(bs[r]);
+      // thread: T row r, half (tid >> 7) of its columns
+      const float4* trow = reinterpret_cast<const float4*>(Tm + r * kGP + (tid >> 7) * 64);
+#pragma unroll 4
+      for (int j = 0; j < 16; ++j) {
+        const float4 x = trow[j];
+        mt = fmaxf(mt, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
       }
     }
 #pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-      mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
-      mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
-    }
-    if (lane == 0) {
-      s_mx[warp][0] = mt;
-      s_mx[warp][1] = mk;
-      s_mx[warp][2] = mv;
-    }
+    for (int off = 16; off; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+    if (lane == 0) s_mx[warp] = mt;
   }
   __syncthreads();
-  float mxs[3] = {0.f, 0.f, 0.f};
+  float mxt = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w)
-#pragma unroll
-    for (int i = 0; i < 3; ++i) mxs[i] = fmaxf(mxs[i], s_mx[w][i]);
-  const int et = f16_exp(mxs[0]), ek = f16_exp(mxs[1]), ev = f16_exp(mxs[2]);
+  for (int w = 0; w < 8; ++w) mxt = fmaxf(mxt, s_mx[w]);
+  const int et = f16_exp(mxt);
+  const int ek = f16_exp(fmaxf(fmaxf(s_kv[0][0], s_kv[1][0]), fmaxf(s_kv[2][0], s_kv[3][0])));
+  const int ev = f16_exp(fmaxf(fmaxf(s_kv[0][1], s_kv[1][1]), fmaxf(s_kv[2][1], s_kv[3][1])));
   // T -> fp16 hi, lo (A operands, K-major: row t, columns s in two 64-wide boxes) over A
   uint8_t* THI = reinterpret_cast<uint8_t*>(Am);
   uint8_t* TLO = THI + 32768;
@@ -321,26 +363,6 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
       }
       *reinterpret_cast<uint4*>(KHI + off) = *reinterpret_cast<const uint4*>(hi);
       *reinterpret_cast<uint4*>(KLO + off) = *reinterpret_cast<const uint4*>(lo);
-    }
-  }
-  __syncthreads();  // K read: its space takes diag(beta) V
-  uint8_t* VHI = RK;
-  uint8_t* VLO = RK + 16384;
-  if (ok && tid < 128) {
-    const float sc = bs[r] * pow2i(-ev);
-#pragma unroll 1
-    for (int cc = 0; cc < 8; ++cc) {
-      const uint32_t off = r * 128 + ((cc ^ rot) << 4);
-      const uint4 x = *reinterpret_cast<const uint4*>(RV + off);
-      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-      __half hi[8], lo[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        split_h(__uint_as_float(w4[e] << 16), sc, hi[2 * e], lo[2 * e]);
-        split_h(__uint_as_float(w4[e] & 0xffff0000u), sc, hi[2 * e + 1], lo[2 * e + 1]);
-      }
-      *reinterpret_cast<uint4*>(VHI + off) = *reinterpret_cast<const uint4*>(hi);
-      *reinterpret_cast<uint4*>(VLO + off) = *reinterpret_cast<const uint4*>(lo);
     }
   }
   ptx::fence_proxy_async_smem();
