@@ -24,7 +24,8 @@ namespace {
 //   its scale exponent), U_loc (fp32) and g, for tc_gdn_pass.
 // ---------------------------------------------------------------------------------
 // Workspace per (b, h, chunk): W hi, W lo (fp16, 16 KB boxes of 64 d_k columns with the
-// 128-byte swizzle), U_loc (128 x d_v fp32), g (128 fp32), W's scale exponent.
+// 128-byte swizzle), U_loc (128 x d_v fp32; in each half row of 32 values, 16-byte chunk j
+// stored at j ^ (row & 7)), g (128 fp32), W's scale exponent.
 constexpr int kGdnOffU = 65536, kGdnOffG = 65536 + 32768, kGdnOffE = kGdnOffG + 512;
 constexpr size_t kGdnChunkBytes = 99328;
 
@@ -50,6 +51,66 @@ __device__ __forceinline__ void split_h(float x, float sc, __half& hi, __half& l
   const float y = x * sc;
   hi = __float2half_rn(y);
   lo = __float2half_rn(y - __half2float(hi));
+}
+
+// One level of T's doubling for diagonal blocks of size n (every pair at once; see the
+// comment at the call): X = A21 T11 into A's upper triangle, then T21 = -T22 X.  Each of
+// the 256 threads takes one output tile of RT rows x 4 columns (RT = n / 16), the column
+// tiles fastest across a warp, and reads the rows of A21 and T22 four k at a time.  T22
+// is lower triangular, so its sum stops at the tile's last row (rounded up to 4).
+template <int RT>
+__device__ __forceinline__ void gdn_double_level(float* Am, float* Tm, int n, int tid, bool ok) {
+  const int nt = n / 4, per = (n / RT) * nt;  // column tiles; tiles per pair (128 / (2 n) pairs)
+  const int i0 = (tid / per) * 2 * n, tj = (tid % nt) * 4, ti = ((tid % per) / nt) * RT;
+  if (ok) {  // X = A21 T11
+    float acc[RT][4] = {};
+    const float* arow = Am + (i0 + n + ti) * kGP + i0;
+#pragma unroll 1
+    for (int k = 0; k < n; k += 4) {
+      float4 av[RT];
+#pragma unroll
+      for (int ii = 0; ii < RT; ++ii) av[ii] = *reinterpret_cast<const float4*>(arow + ii * kGP + k);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 tv = *reinterpret_cast<const float4*>(Tm + (i0 + k + kk) * kGP + i0 + tj);
+#pragma unroll
+        for (int ii = 0; ii < RT; ++ii) {
+          const float a = f4_at(av[ii], kk);
+          acc[ii][0] += a * tv.x; acc[ii][1] += a * tv.y; acc[ii][2] += a * tv.z; acc[ii][3] += a * tv.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int ii = 0; ii < RT; ++ii)
+      *reinterpret_cast<float4*>(Am + (i0 + ti + ii) * kGP + i0 + n + tj) =
+          make_float4(acc[ii][0], acc[ii][1], acc[ii][2], acc[ii][3]);
+  }
+  __syncthreads();
+  if (ok) {  // T21 = -T22 X
+    float acc[RT][4] = {};
+    const float* trow = Tm + (i0 + n + ti) * kGP + i0 + n;
+    const int kend = (ti + RT + 3) & ~3;
+#pragma unroll 1
+    for (int k = 0; k < kend; k += 4) {
+      float4 tv[RT];
+#pragma unroll
+      for (int ii = 0; ii < RT; ++ii) tv[ii] = *reinterpret_cast<const float4*>(trow + ii * kGP + k);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 xv = *reinterpret_cast<const float4*>(Am + (i0 + k + kk) * kGP + i0 + n + tj);
+#pragma unroll
+        for (int ii = 0; ii < RT; ++ii) {
+          const float t = f4_at(tv[ii], kk);
+          acc[ii][0] += t * xv.x; acc[ii][1] += t * xv.y; acc[ii][2] += t * xv.z; acc[ii][3] += t * xv.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int ii = 0; ii < RT; ++ii)
+      *reinterpret_cast<float4*>(Tm + (i0 + n + ti + ii) * kGP + i0 + tj) =
+          make_float4(-acc[ii][0], -acc[ii][1], -acc[ii][2], -acc[ii][3]);
+  }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_constant__ CUtensorMap mapK,
@@ -245,64 +306,12 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   // the block of A between them (the inverse of a 2 x 2 block lower triangle).  For n =
   // 16, 32, 64 every pair is done at once: X = A21 T11 into A's upper triangle (zero and
   // not read again) at rows i0.., columns i0 + n.., then T21 = -T22 X.  Each thread takes
-  // 4 x 4 outputs, the column tiles fastest across a warp: the rows it reads of A21 and T22
-  // are the same for many threads (broadcasts), the rows of T11 and X are read along
-  // (conflict-free).  T22 is lower triangular, so its sum stops at the tile's last row.
-  for (int n = 16; n < 128; n *= 2) {
-    const int nt = n / 4, per = nt * nt, items = (128 / (2 * n)) * per;
-    if (ok)
-      for (int w = tid; w < items; w += 256) {  // X = A21 T11
-        const int i0 = (w / per) * 2 * n, tj = (w % nt) * 4, ti = ((w % per) / nt) * 4;
-        float acc[4][4] = {};
-        const float* arow = Am + (i0 + n + ti) * kGP + i0;
-#pragma unroll 1
-        for (int k = 0; k < n; k += 4) {  // four k at a time: A21's rows read 16 bytes at once
-          float4 av[4];
-#pragma unroll
-          for (int ii = 0; ii < 4; ++ii) av[ii] = *reinterpret_cast<const float4*>(arow + ii * kGP + k);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const float4 tv = *reinterpret_cast<const float4*>(Tm + (i0 + k + kk) * kGP + i0 + tj);
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-              const float a = f4_at(av[ii], kk);
-              acc[ii][0] += a * tv.x; acc[ii][1] += a * tv.y; acc[ii][2] += a * tv.z; acc[ii][3] += a * tv.w;
-            }
-          }
-        }
-#pragma unroll
-        for (int ii = 0; ii < 4; ++ii)
-          *reinterpret_cast<float4*>(Am + (i0 + ti + ii) * kGP + i0 + n + tj) =
-              make_float4(acc[ii][0], acc[ii][1], acc[ii][2], acc[ii][3]);
-      }
-    __syncthreads();
-    if (ok)
-      for (int w = tid; w < items; w += 256) {  // T21 = -T22 X
-        const int i0 = (w / per) * 2 * n, tj = (w % nt) * 4, ti = ((w % per) / nt) * 4;
-        float acc[4][4] = {};
-        const float* trow = Tm + (i0 + n + ti) * kGP + i0 + n;
-#pragma unroll 1
-        for (int k = 0; k < ti + 4; k += 4) {  // four k at a time: T22's rows read 16 bytes at once
-          float4 tv[4];
-#pragma unroll
-          for (int ii = 0; ii < 4; ++ii) tv[ii] = *reinterpret_cast<const float4*>(trow + ii * kGP + k);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const float4 xv = *reinterpret_cast<const float4*>(Am + (i0 + k + kk) * kGP + i0 + n + tj);
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-              const float t = f4_at(tv[ii], kk);
-              acc[ii][0] += t * xv.x; acc[ii][1] += t * xv.y; acc[ii][2] += t * xv.z; acc[ii][3] += t * xv.w;
-            }
-          }
-        }
-#pragma unroll
-        for (int ii = 0; ii < 4; ++ii)
-          *reinterpret_cast<float4*>(Tm + (i0 + n + ti + ii) * kGP + i0 + tj) =
-              make_float4(-acc[ii][0], -acc[ii][1], -acc[ii][2], -acc[ii][3]);
-      }
-    __syncthreads();
-  }
+  // n / 16 x 4 outputs (so all threads work at every level), the column tiles fastest
+  // across a warp: the rows it reads of A21 and T22 are the same for many threads
+  // (broadcasts), the rows of T11 and X are read along (conflict-free).
+  gdn_double_level<1>(Am, Tm, 16, tid, ok);
+  gdn_double_level<2>(Am, Tm, 32, tid, ok);
+  gdn_double_level<4>(Am, Tm, 64, tid, ok);
   // tile scale of T (the maximum over its elements); those of K and V came with the A phase
   {
     float mt = 0.f;
@@ -398,13 +407,16 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   // consecutive 16-byte stores.
   uint8_t* dst = smem;
   const float sw = pow2s(et + ek), su = pow2s(et + ev);
+  // Every thread takes half of its row r: W's d_k columns 64 hf .. 64 hf + 63 (the box hf of
+  // the operand layout) and U_loc's d_v columns 32 hf .. 32 hf + 31.
+  const int hf = tid >> 7;
   float mw = 0.f;
-  if (ok && tid < 128) {
+  if (ok) {
     ptx::tc_fence_after();
 #pragma unroll 1
-    for (int c0 = 0; c0 < kDk; c0 += 32) {
+    for (int c0 = 0; c0 < 64; c0 += 32) {
       float y[32];
-      ptx::tmem_ld32(tW + lane_off + c0, y);
+      ptx::tmem_ld32(tW + lane_off + hf * 64 + c0, y);
       ptx::tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 32; ++j) mw = fmaxf(mw, fabsf(y[j]));
@@ -414,37 +426,41 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   for (int off = 16; off; off >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
   if (lane == 0) s_red[warp] = mw;
   __syncthreads();
-  const int ew = f16_exp(sw * fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])));
-  if (ok && tid < 128) {
+  float mwa = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) mwa = fmaxf(mwa, s_red[w]);
+  const int ew = f16_exp(sw * mwa);
+  if (ok) {
     const float sc = sw * pow2i(-ew);
 #pragma unroll 1
-    for (int c0 = 0; c0 < kDk; c0 += 32) {
+    for (int c0 = 0; c0 < 64; c0 += 32) {
       float y[32];
-      ptx::tmem_ld32(tW + lane_off + c0, y);
+      ptx::tmem_ld32(tW + lane_off + hf * 64 + c0, y);
       ptx::tmem_ld_wait();
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {  // d_k columns c0 + 8 q4 .. + 7: one 16-byte chunk
-        const int col = c0 + 8 * q4, bx = col >> 6, cc = (col & 63) >> 3;
+      for (int q4 = 0; q4 < 4; ++q4) {  // d_k columns 64 hf + c0 + 8 q4 .. + 7: one 16-byte chunk
+        const int cc = (c0 >> 3) + q4;
         __half hi[8], lo[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) split_h(y[8 * q4 + e], sc, hi[e], lo[e]);
-        const size_t off = (size_t)bx * 16384 + r * 128 + ((cc ^ rot) << 4);
+        const size_t off = (size_t)hf * 16384 + r * 128 + ((cc ^ rot) << 4);
         *reinterpret_cast<uint4*>(dst + off) = *reinterpret_cast<const uint4*>(hi);
         *reinterpret_cast<uint4*>(dst + 32768 + off) = *reinterpret_cast<const uint4*>(lo);
       }
     }
-    float* du = reinterpret_cast<float*>(dst + kGdnOffU);
-#pragma unroll 1
-    for (int c0 = 0; c0 < kDv; c0 += 32) {
+    // U_loc row r: 16-byte chunk j of its half goes to chunk j ^ (r & 7) of that half
+    float* du = reinterpret_cast<float*>(dst + kGdnOffU) + r * kDv + hf * 32;
+    {
       float y[32];
-      ptx::tmem_ld32(tU + lane_off + c0, y);
+      ptx::tmem_ld32(tU + lane_off + hf * 32, y);
       ptx::tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(du + r * kDv + c0 + j) = make_float4(su * y[j], su * y[j + 1], su * y[j + 2], su * y[j + 3]);
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(du + 4 * (j ^ rot)) =
+            make_float4(su * y[4 * j], su * y[4 * j + 1], su * y[4 * j + 2], su * y[4 * j + 3]);
     }
-    reinterpret_cast<float*>(dst + kGdnOffG)[r] = gt;
-    if (r == 0) *reinterpret_cast<int*>(dst + kGdnOffE) = ew;
+    if (hf == 0) reinterpret_cast<float*>(dst + kGdnOffG)[r] = gt;
+    if (tid == 0) *reinterpret_cast<int*>(dst + kGdnOffE) = ew;
   }
   ok = __syncthreads_and(ok);  // the record is complete
   if (ok) {
@@ -539,8 +555,8 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_consta
     {
       const float4* us = reinterpret_cast<const float4*>(xc + kGdnOffU) + (r * kDv + hf * 32) / 4;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 v = us[j];
+      for (int j = 0; j < 8; ++j) {  // chunk j of the half row sits at j ^ (r & 7)
+        const float4 v = us[j ^ rot];
         uu[4 * j] = v.x;
         uu[4 * j + 1] = v.y;
         uu[4 * j + 2] = v.z;
