@@ -34,12 +34,20 @@ struct TcGdnParams {
   const float* a;
   const float* beta;
   uint8_t* xw;  // (B*H, T/128, kGdnChunkBytes)
-  void* u;      // (B, T, H, d_v) bf16: the transformed values (tc_gdn_pass)
+  int pf_stride;  // tc_gdn_local: the CTA this far ahead (the SM count) gets its tiles prefetched
+  void* u;        // (B, T, H, d_v) bf16: the transformed values (tc_gdn_pass)
   unsigned* status;
 };
 
 constexpr int kGP = 132;  // padded fp32 row of the 128 x 128 matrices
 constexpr int kSmemGdnL = 32768 + 16384 + 2 * 128 * kGP * 4 + 8 * 256 * 4 + 4 * 128 * 4 + 32768 + 1024;
+
+// L2 prefetch of one tile through a 4-D tensor map (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap), "r"(c0),
+               "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
 
 // component i (0..3, known at compile time after unrolling) of a float4
 __device__ __forceinline__ float f4_at(const float4& v, int i) {
@@ -154,6 +162,15 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
     ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
     ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
+    // One CTA per SM: the CTA that will most likely run next on this SM (one SM count
+    // ahead) finds its K and V tiles in L2.
+    const int l2 = lin + p.pf_stride;
+    if (p.pf_stride > 0 && l2 < (int)gridDim.x) {
+      const int h2 = l2 % p.H, c2 = (l2 / p.H) % nch, b2 = l2 / (p.H * nch), g2 = h2 / p.hpg;
+      tma_prefetch_4d(&mapK, 0, g2, c2 * kTile, b2);
+      tma_prefetch_4d(&mapK, 64, g2, c2 * kTile, b2);
+      tma_prefetch_4d(&mapV, 0, h2, c2 * kTile, b2);
+    }
   }
   if (warp == 0) {
     ptx::tmem_alloc(&tmem_base, 256);
@@ -312,53 +329,25 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   gdn_double_level<1>(Am, Tm, 16, tid, ok);
   gdn_double_level<2>(Am, Tm, 32, tid, ok);
   gdn_double_level<4>(Am, Tm, 64, tid, ok);
-  // tile scale of T (the maximum over its elements); those of K and V came with the A phase
-  {
-    float mt = 0.f;
-    if (ok) {
-      // thread: T row r, half (tid >> 7) of its columns
-      const float4* trow = reinterpret_cast<const float4*>(Tm + r * kGP + (tid >> 7) * 64);
-#pragma unroll 4
-      for (int j = 0; j < 16; ++j) {
-        const float4 x = trow[j];
-        mt = fmaxf(mt, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-      }
-    }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-    if (lane == 0) s_mx[warp] = mt;
-  }
-  __syncthreads();
-  float mxt = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) mxt = fmaxf(mxt, s_mx[w]);
-  const int et = f16_exp(mxt);
-  const int ek = f16_exp(fmaxf(fmaxf(s_kv[0][0], s_kv[1][0]), fmaxf(s_kv[2][0], s_kv[3][0])));
-  const int ev = f16_exp(fmaxf(fmaxf(s_kv[0][1], s_kv[1][1]), fmaxf(s_kv[2][1], s_kv[3][1])));
-  // T -> fp16 hi, lo (A operands, K-major: row t, columns s in two 64-wide boxes) over A
-  uint8_t* THI = reinterpret_cast<uint8_t*>(Am);
-  uint8_t* TLO = THI + 32768;
-  if (ok) {
-    const float sc = pow2i(-et);
-    const int hf = tid >> 7;  // this thread's box (columns 64 hf .. 64 hf + 63) of row r
-#pragma unroll 1
-    for (int cc = 0; cc < 8; ++cc) {
-      const float* src = Tm + r * kGP + hf * 64 + cc * 8;
-      __half hi[8], lo[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) split_h(src[e], sc, hi[e], lo[e]);
-      const uint32_t off = hf * 16384 + r * 128 + ((cc ^ rot) << 4);
-      *reinterpret_cast<uint4*>(THI + off) = *reinterpret_cast<const uint4*>(hi);
-      *reinterpret_cast<uint4*>(TLO + off) = *reinterpret_cast<const uint4*>(lo);
-    }
-  }
-  __syncthreads();  // T read: its space takes diag(beta 2^g) K
-  // diag(beta 2^g) K -> fp16 hi, lo (B operands, MN-major: row s, d_k in two 64-wide boxes)
-  uint8_t* KHI = reinterpret_cast<uint8_t*>(Tm);
+  // T's tile scale (the maximum over its elements; those of K and V came with the A
+  // phase): every thread keeps half of its row r (columns 64 hf ..) in registers, so that
+  // T's hi and lo parts can go over T itself.  Meanwhile diag(beta 2^g) K -> fp16 hi, lo
+  // (B operands, MN-major: row s, d_k in two 64-wide boxes) into A's space, free since
+  // the doubling.
+  const int hf = tid >> 7;
+  float4 tr[16];
+  float mt = 0.f;
+  uint8_t* KHI = reinterpret_cast<uint8_t*>(Am);
   uint8_t* KLO = KHI + 32768;
   if (ok) {
+    const float4* trow = reinterpret_cast<const float4*>(Tm + r * kGP + hf * 64);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      tr[j] = trow[j];
+      mt = fmaxf(mt, fmaxf(fmaxf(fabsf(tr[j].x), fabsf(tr[j].y)), fmaxf(fabsf(tr[j].z), fabsf(tr[j].w))));
+    }
+    const int ek = f16_exp(fmaxf(fmaxf(s_kv[0][0], s_kv[1][0]), fmaxf(s_kv[2][0], s_kv[3][0])));
     const float sc = fk[r] * pow2i(-ek);
-    const int hf = tid >> 7;
 #pragma unroll 1
     for (int cc = 0; cc < 8; ++cc) {
       const uint32_t off = hf * 16384 + r * 128 + ((cc ^ rot) << 4);
@@ -372,6 +361,33 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
       }
       *reinterpret_cast<uint4*>(KHI + off) = *reinterpret_cast<const uint4*>(hi);
       *reinterpret_cast<uint4*>(KLO + off) = *reinterpret_cast<const uint4*>(lo);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+  if (lane == 0) s_mx[warp] = mt;
+  __syncthreads();  // also: every thread has read its part of T
+  float mxt = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) mxt = fmaxf(mxt, s_mx[w]);
+  const int et = f16_exp(mxt);
+  const int ek = f16_exp(fmaxf(fmaxf(s_kv[0][0], s_kv[1][0]), fmaxf(s_kv[2][0], s_kv[3][0])));
+  const int ev = f16_exp(fmaxf(fmaxf(s_kv[0][1], s_kv[1][1]), fmaxf(s_kv[2][1], s_kv[3][1])));
+  // T -> fp16 hi, lo (A operands, K-major: row t, columns s in two 64-wide boxes) over T
+  uint8_t* THI = reinterpret_cast<uint8_t*>(Tm);
+  uint8_t* TLO = THI + 32768;
+  if (ok) {
+    const float sc = pow2i(-et);
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      const float4 x0 = tr[2 * cc], x1 = tr[2 * cc + 1];
+      const float src[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      __half hi[8], lo[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) split_h(src[e], sc, hi[e], lo[e]);
+      const uint32_t off = hf * 16384 + r * 128 + ((cc ^ rot) << 4);
+      *reinterpret_cast<uint4*>(THI + off) = *reinterpret_cast<const uint4*>(hi);
+      *reinterpret_cast<uint4*>(TLO + off) = *reinterpret_cast<const uint4*>(lo);
     }
   }
   ptx::fence_proxy_async_smem();
@@ -409,7 +425,6 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   const float sw = pow2s(et + ek), su = pow2s(et + ev);
   // Every thread takes half of its row r: W's d_k columns 64 hf .. 64 hf + 63 (the box hf of
   // the operand layout) and U_loc's d_v columns 32 hf .. 32 hf + 31.
-  const int hf = tid >> 7;
   float mw = 0.f;
   if (ok) {
     ptx::tc_fence_after();
@@ -767,7 +782,10 @@ cudaError_t launch_tc_gdn(const ll_shape& s, const void* k, const void* v, const
   CUtensorMap mK, mV;
   if (!make_map(&mK, k, kDk, G, s.T, s.batch) || !make_map(&mV, v, kDv, s.heads, s.T, s.batch))
     return cudaErrorInvalidValue;
-  TcGdnParams p{s.batch, s.T, s.heads, s.heads_per_group, G, a, beta, reinterpret_cast<uint8_t*>(ws), u, status};
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    nsm = 0;  // no prefetch
+  TcGdnParams p{s.batch, s.T, s.heads, s.heads_per_group, G, a, beta, reinterpret_cast<uint8_t*>(ws), nsm, u, status};
   cudaError_t e = cudaFuncSetAttribute(tc_gdn_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGdnL);
   if (e != cudaSuccess) return e;
   tc_gdn_local_kernel<<<(unsigned)((size_t)s.batch * s.heads * nch), 256, kSmemGdnL, st>>>(mK, mV, p);
