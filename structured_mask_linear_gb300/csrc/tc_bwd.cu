@@ -40,7 +40,15 @@ struct TcBwdParams {
   float* dlam;   // (B, T, H, L): levels 0..7 written, the rest zeroed
   float* cu;     // (B, T, H): C_s = sum_t A_ts over the in-tile pairs (fp32, from S and E)
   unsigned* status;
+  int pf_stride;  // the CTA this far ahead (the SM count) gets its tiles prefetched into L2
 };
+
+// L2 prefetch of one tile through a 4-D tensor map (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap), "r"(c0),
+               "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
 
 // Warp reduce-scatter of 32 columns: on return lane j holds the sum over the warp's lanes
 // of v[j] (31 shuffles).
@@ -118,6 +126,18 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
     ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
     ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
     ptx::tma_load_4d(RD, &mapD, &bar_ld, 0, h, (int)t0, b);
+    // One CTA per SM: the CTA that will most likely run next on this SM (one SM count
+    // ahead) finds its tiles in L2.
+    const int l2 = lin + p.pf_stride;
+    if (p.pf_stride > 0 && l2 < (int)gridDim.x) {
+      const int h2 = l2 % p.H, u2 = (l2 / p.H) % p.NT, b2 = l2 / (p.H * p.NT), g2 = h2 / p.hpg;
+      tma_prefetch_4d(&mapQ, 0, g2, u2 * kTile, b2);
+      tma_prefetch_4d(&mapQ, 64, g2, u2 * kTile, b2);
+      tma_prefetch_4d(&mapK, 0, g2, u2 * kTile, b2);
+      tma_prefetch_4d(&mapK, 64, g2, u2 * kTile, b2);
+      tma_prefetch_4d(&mapV, 0, h2, u2 * kTile, b2);
+      tma_prefetch_4d(&mapD, 0, h2, u2 * kTile, b2);
+    }
   }
   if (warp == 0) {
     ptx::tmem_alloc(&tmem_base, 512);
@@ -1124,8 +1144,11 @@ cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k,
       !make_map_f32(&mDQ, dq32, kDk, s.heads, s.T, s.batch) || !make_map_f32(&mDK, dk32, kDk, s.heads, s.T, s.batch) ||
       !make_map_f32(&mDV, dv32, kDv, s.heads, s.T, s.batch))
     return cudaErrorInvalidValue;
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    nsm = 0;  // no prefetch
   const TcBwdParams p{s.batch, s.T, s.heads, s.heads_per_group, G, s.levels, NT, a, lam,
-                      dq32, dk32, dv32, dlam, cu, status};
+                      dq32, dk32, dv32, dlam, cu, status, nsm};
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwd);
   if (e != cudaSuccess) return e;
   tc_bwd_intra_kernel<<<(unsigned)((size_t)s.batch * NT * s.heads), 256, kSmemBwd, st>>>(mQ, mK, mV, mD, mDQ, mDK,
