@@ -435,46 +435,48 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
     if (!ok) atomicExch(p.status, kStatusTimeout);
   }
   ok = __all_sync(0xffffffffu, ok);
-  // The fp32 rows of dq (role a), dk and dv (role b) are staged in the tile buffers, free
-  // now (every MMA has read them), as 128-byte-swizzled boxes of 32 columns (dq: 4 boxes
-  // from 0, dk: 4 from 64 KB, dv: 2 from 128 KB), then written with one TMA store each.
-  // Thread r writes row r of a box as eight 16-byte chunks, chunk c at c ^ (r & 7).
+  // The fp32 rows of dq and dv's columns 0..31 (role a), dk and dv's columns 32..63 (role
+  // b) are staged in the tile buffers, free now (every MMA has read them), as
+  // 128-byte-swizzled boxes of 32 columns (dq: 4 boxes from 0, dk: 4 from 64 KB, dv: 2
+  // from 128 KB), and each role writes its boxes with TMA stores as soon as they are
+  // staged, while the other role may still be staging.  Thread r writes row r of a box as
+  // eight 16-byte chunks, chunk c at c ^ (r & 7).
   auto stage_row = [&](uint8_t* box, const float (&y)[32], float sc) {
 #pragma unroll
     for (int c = 0; c < 8; ++c)
       *reinterpret_cast<float4*>(box + r * 128 + ((c ^ rot) << 4)) =
           make_float4(sc * y[4 * c], sc * y[4 * c + 1], sc * y[4 * c + 2], sc * y[4 * c + 3]);
   };
+  const float sv = pow2s(s_sc[1] + s_sc[4]);  // P and dO
   if (ok) {
     ptx::tc_fence_after();
-    if (!role_b) {
-      const float sc = pow2s(s_sc[0] + s_sc[3]);  // dS and K
+    const float sx = role_b ? pow2s(s_sc[0] + s_sc[2]) : pow2s(s_sc[0] + s_sc[3]);  // dS and Q / dS and K
+    const uint32_t tX = role_b ? tDK : tDQ;
+    uint8_t* bx = smem + (role_b ? 65536 : 0);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kDk; c0 += 32) {
-        float y[32];
-        ptx::tmem_ld32(tDQ + lane_off + c0, y);
-        ptx::tmem_ld_wait();
-        stage_row(smem + (c0 >> 5) * 16384, y, sc);
-      }
-    } else {
-      const float sk = pow2s(s_sc[0] + s_sc[2]);  // dS and Q
-      const float sv = pow2s(s_sc[1] + s_sc[4]);  // P and dO
-#pragma unroll 1
-      for (int c0 = 0; c0 < kDk + kDv; c0 += 32) {
-        const bool isk = c0 < kDk;
-        float y[32];
-        ptx::tmem_ld32((isk ? tDK + c0 : tDV + (c0 - kDk)) + lane_off, y);
-        ptx::tmem_ld_wait();
-        stage_row(smem + 65536 + (c0 >> 5) * 16384, y, isk ? sk : sv);
-      }
+    for (int c0 = 0; c0 < kDk; c0 += 32) {
+      float y[32];
+      ptx::tmem_ld32(tX + lane_off + c0, y);
+      ptx::tmem_ld_wait();
+      stage_row(bx + (c0 >> 5) * 16384, y, sx);
+    }
+    {
+      const int hv = role_b ? 1 : 0;
+      float y[32];
+      ptx::tmem_ld32(tDV + lane_off + 32 * hv, y);
+      ptx::tmem_ld_wait();
+      stage_row(smem + 131072 + hv * 16384, y, sv);
     }
     ptx::fence_proxy_async_smem();
   }
-  ok = __syncthreads_and(ok);  // every row staged
-  if (ok && tid == 0) {
-    for (int j = 0; j < 4; ++j) ptx::tma_store_4d(&mapDQ, smem + j * 16384, 32 * j, h, (int)t0, b);
-    for (int j = 0; j < 4; ++j) ptx::tma_store_4d(&mapDK, smem + 65536 + j * 16384, 32 * j, h, (int)t0, b);
-    for (int j = 0; j < 2; ++j) ptx::tma_store_4d(&mapDV, smem + 131072 + j * 16384, 32 * j, h, (int)t0, b);
+  if (role_b) ok = ptx::named_bar_and(4, 128, ok);  // this role's rows staged
+  else ok = ptx::named_bar_and(3, 128, ok);
+  if (ok && (tid & 127) == 0) {
+    const CUtensorMap* mX = role_b ? &mapDK : &mapDQ;
+    uint8_t* bx = smem + (role_b ? 65536 : 0);
+    const int hv = role_b ? 1 : 0;
+    for (int j = 0; j < 4; ++j) ptx::tma_store_4d(mX, bx + j * 16384, 32 * j, h, (int)t0, b);
+    ptx::tma_store_4d(&mapDV, smem + 131072 + hv * 16384, 32 * hv, h, (int)t0, b);
     ptx::bulk_commit_group();
     ptx::bulk_wait_read_all();  // the staging is read before the CTA ends
   }
@@ -892,6 +894,7 @@ struct TcBwdKVParams {
   float* dv32;
   float* cu;    // (B, T, H): adds v_s . (the inter-tile part of dv_s)
   unsigned* status;
+  int pf_stride;  // the CTA this far ahead (the SM count) gets its K and V tiles prefetched into L2
 };
 
 constexpr int kSmemBwdKV = 98304 + 1024;  // K, V, two dual images; then the dk and dv staging
@@ -949,6 +952,13 @@ __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant
     ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
     ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
     ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
+    const int l2 = lin + p.pf_stride;  // one CTA per SM: the one most likely next on this SM
+    if (p.pf_stride > 0 && l2 < (int)gridDim.x) {
+      const int h2 = l2 % p.H, u2 = (l2 / p.H) % p.NT, b2 = l2 / (p.H * p.NT), g2 = h2 / p.hpg;
+      tma_prefetch_4d(&mapK, 0, g2, u2 * kTile, b2);
+      tma_prefetch_4d(&mapK, 64, g2, u2 * kTile, b2);
+      tma_prefetch_4d(&mapV, 0, h2, u2 * kTile, b2);
+    }
     for (int j = 0; j < 2 && j < nl; ++j) {
       ptx::mbar_arrive_expect_tx(&bar_e[j], kImgBytes);
       ptx::bulk_load(RI + j * kImgBytes, p.dimg + slot_of(j) * kImgBytes, kImgBytes, &bar_e[j]);
@@ -1230,6 +1240,12 @@ cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, con
   p.dv32 = dv32;
   p.cu = cu;
   p.status = status;
+  {
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      p.pf_stride = nsm;  // otherwise 0: no prefetch
+  }
   if ((e = cudaFuncSetAttribute(tc_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwdKV)) !=
       cudaSuccess)
     return e;
