@@ -54,11 +54,32 @@ __device__ __forceinline__ float f4_at(const float4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// fp32 value -> fp16 high part and fp16 remainder, both of x * 2^-e
-__device__ __forceinline__ void split_h(float x, float sc, __half& hi, __half& lo) {
-  const float y = x * sc;
-  hi = __float2half_rn(y);
-  lo = __float2half_rn(y - __half2float(hi));
+// Eight fp32 values x * sc -> their fp16 high parts and the fp16 rounding remainders,
+// packed two per 32-bit word (element 2j in the low half), with paired conversions.
+__device__ __forceinline__ void split8(const float (&x)[8], float sc, uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float a = x[2 * j] * sc, b = x[2 * j + 1] * sc;
+    const __half2 hh = __floats2half2_rn(a, b);
+    const float2 hf = __half22float2(hh);
+    const __half2 ll = __floats2half2_rn(a - hf.x, b - hf.y);
+    h[j] = *reinterpret_cast<const uint32_t*>(&hh);
+    l[j] = *reinterpret_cast<const uint32_t*>(&ll);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+// ... of eight bf16 values (a 16-byte chunk)
+__device__ __forceinline__ void split8_bf16(const uint4& v, float sc, uint4& hi, uint4& lo) {
+  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  float x[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w4[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+  }
+  split8(x, sc, hi, lo);
 }
 
 // One level of T's doubling for diagonal blocks of size n (every pair at once; see the
@@ -288,16 +309,10 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
 #pragma unroll 1
       for (int cc = 0; cc < 8; ++cc) {
         const uint32_t off = r * 128 + ((cc ^ rot) << 4);
-        const uint4 x = *reinterpret_cast<const uint4*>(RV + off);
-        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-        __half hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          split_h(__uint_as_float(w4[e] << 16), sc, hi[2 * e], lo[2 * e]);
-          split_h(__uint_as_float(w4[e] & 0xffff0000u), sc, hi[2 * e + 1], lo[2 * e + 1]);
-        }
-        *reinterpret_cast<uint4*>(VHI + off) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(VLO + off) = *reinterpret_cast<const uint4*>(lo);
+        uint4 hi, lo;
+        split8_bf16(*reinterpret_cast<const uint4*>(RV + off), sc, hi, lo);
+        *reinterpret_cast<uint4*>(VHI + off) = hi;
+        *reinterpret_cast<uint4*>(VLO + off) = lo;
       }
     }
   }
@@ -348,19 +363,13 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     }
     const int ek = f16_exp(fmaxf(fmaxf(s_kv[0][0], s_kv[1][0]), fmaxf(s_kv[2][0], s_kv[3][0])));
     const float sc = fk[r] * pow2i(-ek);
-#pragma unroll 1
+#pragma unroll
     for (int cc = 0; cc < 8; ++cc) {
       const uint32_t off = hf * 16384 + r * 128 + ((cc ^ rot) << 4);
-      const uint4 x = *reinterpret_cast<const uint4*>(RK + off);
-      const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-      __half hi[8], lo[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        split_h(__uint_as_float(w4[e] << 16), sc, hi[2 * e], lo[2 * e]);
-        split_h(__uint_as_float(w4[e] & 0xffff0000u), sc, hi[2 * e + 1], lo[2 * e + 1]);
-      }
-      *reinterpret_cast<uint4*>(KHI + off) = *reinterpret_cast<const uint4*>(hi);
-      *reinterpret_cast<uint4*>(KLO + off) = *reinterpret_cast<const uint4*>(lo);
+      uint4 hi, lo;
+      split8_bf16(*reinterpret_cast<const uint4*>(RK + off), sc, hi, lo);
+      *reinterpret_cast<uint4*>(KHI + off) = hi;
+      *reinterpret_cast<uint4*>(KLO + off) = lo;
     }
   }
 #pragma unroll
@@ -382,12 +391,11 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     for (int cc = 0; cc < 8; ++cc) {
       const float4 x0 = tr[2 * cc], x1 = tr[2 * cc + 1];
       const float src[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      __half hi[8], lo[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) split_h(src[e], sc, hi[e], lo[e]);
+      uint4 hi, lo;
+      split8(src, sc, hi, lo);
       const uint32_t off = hf * 16384 + r * 128 + ((cc ^ rot) << 4);
-      *reinterpret_cast<uint4*>(THI + off) = *reinterpret_cast<const uint4*>(hi);
-      *reinterpret_cast<uint4*>(TLO + off) = *reinterpret_cast<const uint4*>(lo);
+      *reinterpret_cast<uint4*>(THI + off) = hi;
+      *reinterpret_cast<uint4*>(TLO + off) = lo;
     }
   }
   ptx::fence_proxy_async_smem();
@@ -455,12 +463,13 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {  // d_k columns 64 hf + c0 + 8 q4 .. + 7: one 16-byte chunk
         const int cc = (c0 >> 3) + q4;
-        __half hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) split_h(y[8 * q4 + e], sc, hi[e], lo[e]);
+        const float src[8] = {y[8 * q4], y[8 * q4 + 1], y[8 * q4 + 2], y[8 * q4 + 3],
+                              y[8 * q4 + 4], y[8 * q4 + 5], y[8 * q4 + 6], y[8 * q4 + 7]};
+        uint4 hi, lo;
+        split8(src, sc, hi, lo);
         const size_t off = (size_t)hf * 16384 + r * 128 + ((cc ^ rot) << 4);
-        *reinterpret_cast<uint4*>(dst + off) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(dst + 32768 + off) = *reinterpret_cast<const uint4*>(lo);
+        *reinterpret_cast<uint4*>(dst + off) = hi;
+        *reinterpret_cast<uint4*>(dst + 32768 + off) = lo;
       }
     }
     // U_loc row r: 16-byte chunk j of its half goes to chunk j ^ (r & 7) of that half
@@ -600,12 +609,13 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_consta
       const float sc = pow2i(-es);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        __half hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) split_h(sv[8 * q4 + e], sc, hi[e], lo[e]);
+        const float src[8] = {sv[8 * q4], sv[8 * q4 + 1], sv[8 * q4 + 2], sv[8 * q4 + 3],
+                              sv[8 * q4 + 4], sv[8 * q4 + 5], sv[8 * q4 + 6], sv[8 * q4 + 7]};
+        uint4 hi, lo;
+        split8(src, sc, hi, lo);
         const int off = r * 128 + (((4 * hf + q4) ^ rot) << 4);
-        *reinterpret_cast<uint4*>(RS + off) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(RS + 16384 + off) = *reinterpret_cast<const uint4*>(lo);
+        *reinterpret_cast<uint4*>(RS + off) = hi;
+        *reinterpret_cast<uint4*>(RS + 16384 + off) = lo;
       }
     }
     ptx::fence_proxy_async_smem();
@@ -700,12 +710,13 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_consta
       const float sc = pow2i(-eu);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        __half hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) split_h(uu[8 * q4 + e], sc, hi[e], lo[e]);
+        const float src[8] = {uu[8 * q4], uu[8 * q4 + 1], uu[8 * q4 + 2], uu[8 * q4 + 3],
+                              uu[8 * q4 + 4], uu[8 * q4 + 5], uu[8 * q4 + 6], uu[8 * q4 + 7]};
+        uint4 hi, lo;
+        split8(src, sc, hi, lo);
         const int off = r * 128 + (((4 * hf + q4) ^ rot) << 4);
-        *reinterpret_cast<uint4*>(RU + off) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(RU + 16384 + off) = *reinterpret_cast<const uint4*>(lo);
+        *reinterpret_cast<uint4*>(RU + off) = hi;
+        *reinterpret_cast<uint4*>(RU + 16384 + off) = lo;
       }
       const float sk = pow2i(-ek);
       const __nv_bfloat162 k2 = __floats2bfloat162_rn(sk, sk);
