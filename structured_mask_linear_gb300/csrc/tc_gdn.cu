@@ -40,7 +40,7 @@ struct TcGdnParams {
 };
 
 constexpr int kGP = 132;  // padded fp32 row of the 128 x 128 matrices
-constexpr int kSmemGdnL = 32768 + 16384 + 2 * 128 * kGP * 4 + 8 * 256 * 4 + 4 * 128 * 4 + 32768 + 1024;
+constexpr int kSmemGdnL = 32768 + 16384 + 2 * 128 * kGP * 4 + 4 * 128 * 4 + 32768 + 1024;
 
 // L2 prefetch of one tile through a 4-D tensor map (no shared memory, no completion)
 __device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1, int c2, int c3) {
@@ -147,12 +147,12 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
                                                               TcGdnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* RK = smem;                                          // 32 KB: K (bf16); later V hi, lo (fp16)
+  uint8_t* RK = smem;                                          // 32 KB: K (bf16)
   uint8_t* RV = smem + 32768;                                  // 16 KB: V (bf16)
-  float* Am = reinterpret_cast<float*>(smem + 49152);          // 128 x kGP: A; later T hi, lo (fp16)
-  float* Tm = Am + 128 * kGP;                                  // 128 x kGP: T; later Kd hi, lo (fp16)
-  float* Ym = Tm + 128 * kGP;                                  // 8 x (16 x 16): one per warp
-  float* gs = Ym + 8 * 256;                                    // 128: g
+  float* Am = reinterpret_cast<float*>(smem + 49152);          // 128 x kGP: A; later Kd hi, lo (fp16)
+  float* Tm = Am + 128 * kGP;                                  // 128 x kGP: T; later T hi, lo (fp16)
+  // (once the products have read them, the first 97 KB take the chunk's workspace record)
+  float* gs = Tm + 128 * kGP;                                  // 128: g
   float* bs = gs + 128;                                        // 128: beta
   float* fk = bs + 128;                                        // 128: beta 2^g
   float* b8 = fk + 128;                                        // 128: 2^(g_end8(s) - g_s)
