@@ -62,9 +62,9 @@ __global__ void __launch_bounds__(128, 3) tc_state_kernel(const __grid_constant_
   uint8_t* stage = sV + 16384;
   __shared__ __align__(8) uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_red[4];
+  __shared__ float s_scan[4][4];
   __shared__ float2 s_red2[4];
-  __shared__ float s_gamma;
+  __shared__ float s_gamma4[4];
 
   const int tid = threadIdx.x, warp = tid >> 5, rot = tid & 7;
   const int ng4 = (p.NT + 3) >> 2;  // groups of four tiles per (b, h)
@@ -105,21 +105,47 @@ __global__ void __launch_bounds__(128, 3) tc_state_kernel(const __grid_constant_
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tbase = tmem_base;
+  // decay of token u * 128 + tid for the group's four tiles u at once (while the first
+  // tile loads): chunk-local log2 cumsums, and each tile's total gamma_u
+  float gi4[4];
+  {
+    const int lane = tid & 31;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) gi4[j] = log2f(a4[j]);
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float y = __shfl_up_sync(0xffffffffu, gi4[j], off);
+        if (lane >= off) gi4[j] += y;
+      }
+    if (lane == 31)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s_scan[warp][j] = gi4[j];
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float add = 0.f;
+      for (int w = 0; w < warp; ++w) add += s_scan[w][j];
+      gi4[j] += add;
+    }
+    if (tid == kTile - 1)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s_gamma4[j] = gi4[j];  // read after the barrier below
+  }
   float L[kDv];  // running sum of the group's tile states, decayed to the latest tile's end
   float GL = 0.f;
   int k = 0, fail = 0;  // fail: 1 = tile k's copy timed out, 2 = its MMA did
   for (; k < nt4; ++k) {
     const int u = 4 * i4 + k;
-    // decay of token u * 128 + tid: chunk-local log2 cumsum
-    const float gi = block_scan128(log2f(a4[k]), s_red);
-    if (tid == kTile - 1) s_gamma = gi;
+    const float gi = k == 0 ? gi4[0] : k == 1 ? gi4[1] : k == 2 ? gi4[2] : gi4[3];
     bool ok = wait_bar(&bar_ld, k & 1);
     if (!ok) atomicExch(p.status, kStatusTimeout);
     if (!__syncthreads_and(ok)) {
       fail = 1;
       break;
     }
-    const float gamma = s_gamma;
+    const float gamma = s_gamma4[k];
     {
       // Ṽ row tid = 2^(gamma - g_tid) v_tid as a bf16 hi part (in place) plus a bf16 lo
       // part (the rounding remainder), so that Kᵀ(Ṽhi + Ṽlo) keeps ~16 bits.  The 128-byte
