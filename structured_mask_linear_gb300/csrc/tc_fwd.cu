@@ -203,16 +203,18 @@ __global__ void __launch_bounds__(128, 3) tc_state_kernel(const __grid_constant_
     const float d = exp2f(gamma);
     float m = 0.f;
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float hi[16], lo[16];
-      ptx::tmem_ld16(trow + q4 * 16, hi);
-      ptx::tmem_ld16(trow + 64 + q4 * 16, lo);
+    for (int q2 = 0; q2 < 2; ++q2) {  // 32 columns per wait
+      float hi[32], lo[32];
+      ptx::tmem_ld16(trow + q2 * 32, hi);
+      ptx::tmem_ld16(trow + q2 * 32 + 16, hi + 16);
+      ptx::tmem_ld16(trow + 64 + q2 * 32, lo);
+      ptx::tmem_ld16(trow + 64 + q2 * 32 + 16, lo + 16);
       ptx::tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < 32; ++j) {
         const float c = hi[j] + lo[j];
         m = fmaxf(m, fabsf(c));
-        L[q4 * 16 + j] = k == 0 ? c : d * L[q4 * 16 + j] + c;
+        L[q2 * 32 + j] = k == 0 ? c : d * L[q2 * 32 + j] + c;
       }
     }
     const size_t node0 = nbase + u;
