@@ -752,13 +752,13 @@ __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant_
     if (hf == 0) {  // dlambda_t^(8+m) = 2^(g_t + D + eq + en + ed) sum_j Y_tj dO^_tj
       float dot = 0.f;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float y[32];
-        ptx::tmem_ld32(tY + lane_off + half * 32, y);
+      for (int q = 0; q < 4; ++q) {  // 16 columns at a time (fewer live registers)
+        float y[16];
+        ptx::tmem_ld16(tY + lane_off + q * 16, y);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 x = *reinterpret_cast<const uint4*>(drow + (((4 * half + c) ^ rot) << 4));
+        for (int c = 0; c < 2; ++c) {
+          const uint4 x = *reinterpret_cast<const uint4*>(drow + (((2 * q + c) ^ rot) << 4));
           const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
