@@ -290,7 +290,12 @@ size_t loglinear_gdn_fwd_workspace_bytes(const ll_shape* shape);
  * are 128 tokens and the products run on the tensor cores (fp16 high and low parts,
  * fp32 accumulation); otherwise 32-token chunks run in fp32 on the CUDA cores.  u is
  * stored in the input dtype in the workspace, then the level-fused forward runs on
- * (q, k, u, a, lambda).
+ * (q, k, u, a, lambda).  On the tensor-core path with batch >= 2 the last batch element's
+ * state pass and forward run on a second, high-priority stream that the library creates
+ * on a device's first such call, forked from and joined back into `stream` with events,
+ * so that the other elements' forward starts as soon as their passes end; every launch
+ * is still ordered after the work already on `stream`, and later work on `stream` waits
+ * for all of it.  Concurrent calls on one device are serialised inside the library.
  */
 ll_status loglinear_gdn_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
                             const float* a, const float* beta, const float* lambda, void* o,

@@ -71,6 +71,12 @@ ll_status fwd_impl(const ll_shape* s, const void* q, const void* k, const void* 
 }  // namespace
 
 namespace ll {
+// tc_gdn.cu: the Gated DeltaNet values' chunk solves and the state pass over batch
+// elements b0 .. b0 + nb - 1
+cudaError_t launch_tc_gdn_local(const ll_shape& s, const void* k, const void* v, const float* a, const float* beta,
+                                void* u, char* ws, unsigned* status, cudaStream_t st);
+cudaError_t launch_tc_gdn_pass(const ll_shape& s, int b0, int nb, const void* k, const void* v, const float* a,
+                               const float* beta, void* u, char* ws, unsigned* status, cudaStream_t st);
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 void note_launch(const FwdArgs& a, int i, cudaStream_t st) {
   note_launch();
@@ -211,6 +217,37 @@ HostPipe* host_pipe() {
   return &hp;
 }
 
+// Streams and events of the Gated DeltaNet forward's split (created once per device): two
+// streams of the highest priority, so that the passes and the last element's forward take
+// SMs ahead of the other elements' forward on the caller's stream.
+struct GdnPipe {
+  cudaStream_t first = nullptr, last = nullptr;
+  cudaEvent_t local = nullptr, first_done = nullptr, last_done = nullptr;
+  bool ready = false;
+  std::mutex call_mu;  // the events are re-recorded by every call
+};
+GdnPipe g_gdn_pipe[128];
+
+GdnPipe* gdn_pipe() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  GdnPipe& gp = g_gdn_pipe[dev];
+  if (!gp.ready) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+    const unsigned ef = cudaEventDisableTiming;
+    if (cudaStreamCreateWithPriority(&gp.first, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&gp.last, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+        cudaEventCreateWithFlags(&gp.local, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&gp.first_done, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&gp.last_done, ef) != cudaSuccess)
+      return nullptr;
+    gp.ready = true;
+  }
+  return &gp;
+}
+
 }  // namespace
 
 extern "C" {
@@ -335,9 +372,22 @@ ll_status ssd_fwd(const ll_shape* s, const void* q, const void* k, const void* v
   return ll::launch_tc_ssd(tp, fa, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
+// Gated DeltaNet on the tensor-core shape with more than one batch element: the state pass
+// of the last element and its forward run on a second stream, so that the forward of the
+// others starts as soon as their passes end (the pass takes one CTA per (b, h) for all
+// its chunks; at B * H above the SM count the last element's CTAs would otherwise run as a
+// second wave alone).  Its forward has a workspace of its own.
+bool gdn_split(const ll_shape* s) { return s->batch >= 2 && ll::tc_supported(*s); }
+size_t gdn_fwd_ws_last(const ll_shape* s) {
+  ll_shape s1 = *s;
+  s1.batch = 1;
+  return a256(loglinear_fwd_workspace_bytes(&s1));
+}
+
 size_t loglinear_gdn_fwd_workspace_bytes(const ll_shape* s) {
   const size_t f = loglinear_fwd_workspace_bytes(s);
-  return f ? a256(f) + ll::gdn_values_bytes(*s) : 0;
+  if (!f) return 0;
+  return a256(f) + (gdn_split(s) ? gdn_fwd_ws_last(s) : 0) + ll::gdn_values_bytes(*s);
 }
 
 ll_status loglinear_gdn_fwd(const ll_shape* s, const void* q, const void* k, const void* v,
@@ -353,14 +403,53 @@ ll_status loglinear_gdn_fwd(const ll_shape* s, const void* q, const void* k, con
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) || !aligned16(lambda) ||
       !aligned16(o) || !aligned16(workspace))
     return LL_ERR_ALIGN;
-  // u (the transformed values) after the forward's own workspace
+  // u (the transformed values) after the forward's own workspace(s)
   const size_t fws = a256(loglinear_fwd_workspace_bytes(s));
-  char* u = static_cast<char*>(workspace) + fws;
+  const bool split = gdn_split(s);
+  const size_t fws1 = split ? gdn_fwd_ws_last(s) : 0;
+  char* u = static_cast<char*>(workspace) + fws + fws1;
   unsigned* sw = status_word();
   if (!sw) return LL_ERR_CUDA;
-  if (ll::launch_gdn_values(*s, k, v, a, beta, u, sw, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (!split) {
+    if (ll::launch_gdn_values(*s, k, v, a, beta, u, sw, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return LL_ERR_CUDA;
+    return fwd_impl(s, q, k, u, a, lambda, o, workspace, fws, nullptr, nullptr, 0, stream, nullptr, 0);
+  }
+  const int B = s->batch;
+  const size_t ub = ((size_t)s->batch * s->T * s->heads * s->d_v * 2 + 255) & ~size_t(255);  // bf16 u
+  char* rec = u + ub;  // the chunk records (tc_gdn.cu)
+  GdnPipe* gp = gdn_pipe();
+  if (!gp) return LL_ERR_CUDA;
+  std::lock_guard<std::mutex> call_lock(gp->call_mu);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (ll::launch_tc_gdn_local(*s, k, v, a, beta, u, rec, sw, cs) != cudaSuccess) return LL_ERR_CUDA;
+  if (cudaEventRecord(gp->local, cs) != cudaSuccess || cudaStreamWaitEvent(gp->first, gp->local, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(gp->last, gp->local, 0) != cudaSuccess)
     return LL_ERR_CUDA;
-  return fwd_impl(s, q, k, u, a, lambda, o, workspace, fws, nullptr, nullptr, 0, stream, nullptr, 0);
+  // the passes of elements 0 .. B-2 are issued first, so that their CTAs start first
+  if (ll::launch_tc_gdn_pass(*s, 0, B - 1, k, v, a, beta, u, rec, sw, gp->first) != cudaSuccess ||
+      cudaEventRecord(gp->first_done, gp->first) != cudaSuccess ||
+      ll::launch_tc_gdn_pass(*s, B - 1, 1, k, v, a, beta, u, rec, sw, gp->last) != cudaSuccess)
+    return LL_ERR_CUDA;
+  // the forward of the last element on its stream (pointers of element B - 1)
+  const size_t G = (size_t)(s->heads / s->heads_per_group), es = 2;
+  const size_t pq = (size_t)s->T * G * s->d_k * es, pv = (size_t)s->T * s->heads * s->d_v * es,
+               pa = (size_t)s->T * s->heads, pl = (size_t)s->T * s->heads * s->levels;
+  ll_shape s1 = *s;
+  s1.batch = 1;
+  const size_t bl = (size_t)(B - 1);
+  ll_status st1 = fwd_impl(&s1, static_cast<const char*>(q) + bl * pq, static_cast<const char*>(k) + bl * pq,
+                           u + bl * pv, a + bl * pa, lambda + bl * pl, static_cast<char*>(o) + bl * pv,
+                           static_cast<char*>(workspace) + fws, fws1, nullptr, nullptr, 0, gp->last, nullptr, 0);
+  if (st1 != LL_OK) return st1;
+  if (cudaEventRecord(gp->last_done, gp->last) != cudaSuccess) return LL_ERR_CUDA;
+  // the forward of elements 0 .. B-2 on the caller's stream, once their passes are done
+  if (cudaStreamWaitEvent(cs, gp->first_done, 0) != cudaSuccess) return LL_ERR_CUDA;
+  ll_shape s0 = *s;
+  s0.batch = B - 1;
+  ll_status st0 = fwd_impl(&s0, q, k, u, a, lambda, o, workspace, fws, nullptr, nullptr, 0, stream, nullptr, 0);
+  if (st0 != LL_OK) return st0;
+  return cudaStreamWaitEvent(cs, gp->last_done, 0) == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
 size_t loglinear_bwd_workspace_bytes(const ll_shape* s) {

@@ -35,6 +35,7 @@ struct TcGdnParams {
   const float* beta;
   uint8_t* xw;  // (B*H, T/128, kGdnChunkBytes)
   int pf_stride;  // tc_gdn_local: the CTA this far ahead (the SM count) gets its tiles prefetched
+  int b0;         // tc_gdn_pass: first batch element of this launch (CTA x: (b0 + x / H, x % H))
   void* u;        // (B, T, H, d_v) bf16: the transformed values (tc_gdn_pass)
   unsigned* status;
 };
@@ -526,7 +527,7 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_consta
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
   const int r = tid & 127, hf = tid >> 7, rot = r & 7;
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H, g = h / p.hpg;
+  const int bh = p.b0 * p.H + blockIdx.x, b = bh / p.H, h = bh % p.H, g = h / p.hpg;
   const int nch = p.T >> 7;
   const uint8_t* xw = p.xw + (size_t)bh * nch * kGdnChunkBytes;
   __nv_bfloat16* uo = static_cast<__nv_bfloat16*>(p.u);
@@ -786,29 +787,54 @@ size_t tc_gdn_bytes(const ll_shape& s) {
   return (size_t)s.batch * s.heads * (s.T / kTile) * kGdnChunkBytes;
 }
 
-cudaError_t launch_tc_gdn(const ll_shape& s, const void* k, const void* v, const float* a, const float* beta,
-                          void* u, char* ws, unsigned* status, cudaStream_t st) {
-  if (!tc_supported(s)) return cudaErrorInvalidValue;
-  const int G = s.heads / s.heads_per_group, nch = s.T / kTile;
-  CUtensorMap mK, mV;
-  if (!make_map(&mK, k, kDk, G, s.T, s.batch) || !make_map(&mV, v, kDv, s.heads, s.T, s.batch))
-    return cudaErrorInvalidValue;
+namespace {
+bool tc_gdn_params(const ll_shape& s, const void* k, const void* v, const float* a, const float* beta, void* u,
+                   char* ws, unsigned* status, CUtensorMap* mK, CUtensorMap* mV, TcGdnParams* p) {
+  if (!tc_supported(s)) return false;
+  const int G = s.heads / s.heads_per_group;
+  if (!make_map(mK, k, kDk, G, s.T, s.batch) || !make_map(mV, v, kDv, s.heads, s.T, s.batch)) return false;
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     nsm = 0;  // no prefetch
-  TcGdnParams p{s.batch, s.T, s.heads, s.heads_per_group, G, a, beta, reinterpret_cast<uint8_t*>(ws), nsm, u, status};
+  *p = TcGdnParams{s.batch, s.T, s.heads, s.heads_per_group, G, a, beta, reinterpret_cast<uint8_t*>(ws), nsm, 0, u,
+                   status};
+  return true;
+}
+}  // namespace
+
+cudaError_t launch_tc_gdn_local(const ll_shape& s, const void* k, const void* v, const float* a, const float* beta,
+                                void* u, char* ws, unsigned* status, cudaStream_t st) {
+  CUtensorMap mK, mV;
+  TcGdnParams p;
+  if (!tc_gdn_params(s, k, v, a, beta, u, ws, status, &mK, &mV, &p)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_gdn_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGdnL);
   if (e != cudaSuccess) return e;
-  tc_gdn_local_kernel<<<(unsigned)((size_t)s.batch * s.heads * nch), 256, kSmemGdnL, st>>>(mK, mV, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  note_launch();
-  if ((e = cudaFuncSetAttribute(tc_gdn_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGdnP)) !=
-      cudaSuccess)
-    return e;
-  tc_gdn_pass_kernel<<<(unsigned)(s.batch * s.heads), 256, kSmemGdnP, st>>>(mK, p);
+  tc_gdn_local_kernel<<<(unsigned)((size_t)s.batch * s.heads * (s.T / kTile)), 256, kSmemGdnL, st>>>(mK, mV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
+}
+
+cudaError_t launch_tc_gdn_pass(const ll_shape& s, int b0, int nb, const void* k, const void* v, const float* a,
+                               const float* beta, void* u, char* ws, unsigned* status, cudaStream_t st) {
+  CUtensorMap mK, mV;
+  TcGdnParams p;
+  if (b0 < 0 || nb < 1 || b0 + nb > s.batch) return cudaErrorInvalidValue;
+  if (!tc_gdn_params(s, k, v, a, beta, u, ws, status, &mK, &mV, &p)) return cudaErrorInvalidValue;
+  p.b0 = b0;
+  cudaError_t e = cudaFuncSetAttribute(tc_gdn_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGdnP);
+  if (e != cudaSuccess) return e;
+  tc_gdn_pass_kernel<<<(unsigned)(nb * s.heads), 256, kSmemGdnP, st>>>(mK, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
+  return cudaSuccess;
+}
+
+cudaError_t launch_tc_gdn(const ll_shape& s, const void* k, const void* v, const float* a, const float* beta,
+                          void* u, char* ws, unsigned* status, cudaStream_t st) {
+  cudaError_t e = launch_tc_gdn_local(s, k, v, a, beta, u, ws, status, st);
+  if (e != cudaSuccess) return e;
+  return launch_tc_gdn_pass(s, 0, s.batch, k, v, a, beta, u, ws, status, st);
 }
 
 }  // namespace ll
