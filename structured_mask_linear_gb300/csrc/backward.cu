@@ -504,8 +504,10 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
   // the generic chunk states and blocks only off the tensor-core path (which uses the
   // plan for the dual slots alone)
   size_t o = bp->tc ? 0 : al(bp->g.bytes);
+  // dual slots per (b, h): every block, or on the tensor-core path those from chunk level 1
+  const size_t nsl = bp->tc ? (size_t)(bp->g.nblk - (bp->g.M > 1 ? bp->g.blk_off[1] : 0)) : (size_t)bp->g.nblk;
   bp->off_dual = o;
-  o = al(o + sizeof(float) * BH * bp->g.nblk * S);
+  o = al(o + sizeof(float) * BH * nsl * S);
   bp->off_dq = o;
   o = al(o + sizeof(float) * (size_t)s.batch * s.T * s.heads * s.d_k);
   bp->off_dk = o;
@@ -516,9 +518,9 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
   if (bp->tc) {
     o = al(o + bp->tp.bytes);
     bp->off_dimg = o;
-    o = al(o + BH * bp->g.nblk * S * 2);
+    o = al(o + BH * nsl * S * 2);
     bp->off_dmeta = o;
-    o = al(o + BH * bp->g.nblk * 4 * sizeof(unsigned));
+    o = al(o + BH * nsl * 4 * sizeof(unsigned));
     bp->off_P = o;
     o = al(o + BH * (bp->tp.NT + 1) * sizeof(double));
     bp->off_cu = o;
@@ -544,8 +546,14 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
   // off the tensor-core path
   cudaError_t e = cudaSuccess;
   if (!bp.tc && (e = launch_generic_states(p, sizeof(TIn) == 2, fa, st)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(x.ws + bp.off_dual, 0, sizeof(float) * (size_t)BH * p.nblk * dk * dv, st)) !=
-      cudaSuccess)
+  // The tensor-core kernels use the blocks from chunk level 1 up only, so their duals take
+  // a compact slot range per (b, h): slot = blk_off[m + 1] - blk_off[1] + index, of
+  // tc_slots per (b, h); the CUDA-core kernels use every block.
+  const int tc_base = p.M > 1 ? p.blk_off[1] : 0, tc_slots = p.nblk - tc_base;
+  int tc_dual_off[32];
+  for (int m = 0; m < 32; ++m) tc_dual_off[m] = m + 1 < p.M ? p.blk_off[m + 1] - tc_base : 0;  // chunk level m + 1
+  const size_t nslot_zero = (size_t)BH * (bp.tc ? tc_slots : p.nblk);
+  if ((e = cudaMemsetAsync(x.ws + bp.off_dual, 0, sizeof(float) * nslot_zero * dk * dv, st)) != cudaSuccess)
     return e;
   // the pairs inside 128-token tiles (two 64-token chunks) on the tensor cores where the
   // shape allows; the inter-chunk kernels then start at chunk level 1, and the query side
@@ -576,10 +584,8 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
       cudaSuccess)
     return e;
   if (tc) {
-    int dual_off[32];
-    for (int m = 0; m < 32; ++m) dual_off[m] = m + 1 < p.M ? p.blk_off[m + 1] : 0;  // chunk level m + 1
     if ((e = launch_tc_bwd_q(bp.tp, x.q, x.dO, x.a, x.lam, x.ws + bp.off_tc, reinterpret_cast<float*>(x.ws + bp.off_dq),
-                             x.dlam, reinterpret_cast<float*>(x.ws + bp.off_dual), dual_off, p.nblk, fa.status,
+                             x.dlam, reinterpret_cast<float*>(x.ws + bp.off_dual), tc_dual_off, tc_slots, fa.status,
                              st)) != cudaSuccess)
       return e;
   } else {
@@ -588,12 +594,10 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
     note_launch();
   }
   if (tc) {
-    int dual_off[32];
-    for (int m = 0; m < 32; ++m) dual_off[m] = m + 1 < p.M ? p.blk_off[m + 1] : 0;
     if ((e = launch_tc_bwd_kv(bp.tp, x.k, x.v, x.a, x.ws + bp.off_tc, reinterpret_cast<const float*>(x.ws + bp.off_dual),
                               reinterpret_cast<uint8_t*>(x.ws + bp.off_dimg),
                               reinterpret_cast<unsigned*>(x.ws + bp.off_dmeta),
-                              reinterpret_cast<double*>(x.ws + bp.off_P), dual_off, p.nblk,
+                              reinterpret_cast<double*>(x.ws + bp.off_P), tc_dual_off, tc_slots,
                               reinterpret_cast<float*>(x.ws + bp.off_dk), reinterpret_cast<float*>(x.ws + bp.off_dv),
                               reinterpret_cast<float*>(x.ws + bp.off_cu), fa.status, st)) != cudaSuccess)
       return e;
