@@ -404,7 +404,8 @@ __device__ __forceinline__ void load4v(const __nv_bfloat16* p, float (&x)[4]) {
   x[3] = __uint_as_float(v.y & 0xffff0000u);
 }
 
-// cu: C_u from the pair terms where the tensor-core kernels summed it (else v_u . dv_u).
+// cu: C_u from the pair terms and R_u where the tensor-core kernels summed them (else
+// v_u . dv_u and sum_l lambda_u^l dlambda_u^l here).
 template <typename TIn>
 __global__ void __launch_bounds__(kDlChunk) bwd_dloga_local(GenPlan p, BwdArgs x, size_t off_dv, const float* cu,
                                                            double* loc, double* tot) {
@@ -418,21 +419,22 @@ __global__ void __launch_bounds__(kDlChunk) bwd_dloga_local(GenPlan p, BwdArgs x
   if (t < p.T) {
     const size_t row = ((size_t)b * p.T + t) * p.H + h;
     float R = 0.f, Cv = 0.f;
-    if ((L & 1) == 0) {  // rows of an even level count are 8-byte aligned: pairs
-      const float2* l2 = reinterpret_cast<const float2*>(x.lam + row * L);
-      const float2* d2 = reinterpret_cast<const float2*>(x.dlam + row * L);
-#pragma unroll 4
-      for (int l = 0; l < L / 2; ++l) {
-        const float2 a2 = l2[l], b2 = d2[l];
-        R += a2.x * b2.x + a2.y * b2.y;
-      }
-    } else {
-#pragma unroll 4
-      for (int l = 0; l < L; ++l) R += x.lam[row * L + l] * x.dlam[row * L + l];
-    }
-    if (cu) {
+    if (cu) {  // both summed by the tensor-core kernels: C_u, then R_u after B T H values
       Cv = cu[row];
+      R = cu[(size_t)p.B * p.T * p.H + row];
     } else {
+      if ((L & 1) == 0) {  // rows of an even level count are 8-byte aligned: pairs
+        const float2* l2 = reinterpret_cast<const float2*>(x.lam + row * L);
+        const float2* d2 = reinterpret_cast<const float2*>(x.dlam + row * L);
+#pragma unroll 4
+        for (int l = 0; l < L / 2; ++l) {
+          const float2 a2 = l2[l], b2 = d2[l];
+          R += a2.x * b2.x + a2.y * b2.y;
+        }
+      } else {
+#pragma unroll 4
+        for (int l = 0; l < L; ++l) R += x.lam[row * L + l] * x.dlam[row * L + l];
+      }
       const float* dr = dv32 + row * dv;
       const TIn* vr = v + row * dv;
       for (int jv = 0; jv < dv; jv += 4) {  // rows 16-byte aligned (d_v a multiple of 16)
@@ -523,8 +525,8 @@ bool make_bwd_plan(const ll_shape& s, BwdPlan* bp) {
     o = al(o + BH * nsl * 4 * sizeof(unsigned));
     bp->off_P = o;
     o = al(o + BH * (bp->tp.NT + 1) * sizeof(double));
-    bp->off_cu = o;
-    o = al(o + (size_t)s.batch * s.T * s.heads * sizeof(float));
+    bp->off_cu = o;  // C_u, then R_u
+    o = al(o + 2 * (size_t)s.batch * s.T * s.heads * sizeof(float));
   }
   const size_t nch = ((size_t)s.T + kDlChunk - 1) / kDlChunk;
   bp->off_loc = o;
@@ -585,7 +587,8 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
     return e;
   if (tc) {
     if ((e = launch_tc_bwd_q(bp.tp, x.q, x.dO, x.a, x.lam, x.ws + bp.off_tc, reinterpret_cast<float*>(x.ws + bp.off_dq),
-                             x.dlam, reinterpret_cast<float*>(x.ws + bp.off_dual), tc_dual_off, tc_slots, fa.status,
+                             x.dlam, reinterpret_cast<float*>(x.ws + bp.off_dual), tc_dual_off, tc_slots,
+                             reinterpret_cast<float*>(x.ws + bp.off_cu) + (size_t)p.B * p.T * p.H, fa.status,
                              st)) != cudaSuccess)
       return e;
   } else {

@@ -143,10 +143,11 @@ cudaError_t launch_tc_export_only(const TcPlan& p, const FwdArgs& a, cudaStream_
 size_t tc_prefix_bytes(const TcPlan& p, int npre);
 // Backward, query side of the inter-tile levels on the tensor cores: adds into dq32,
 // assigns dlambda levels >= 8 of the set bits, adds the nodes' duals (dual slot of the
-// even node (m, i): dual_off[m] + i / 2, nslots per (b, h); dual zero before the first call).
+// even node (m, i): dual_off[m] + i / 2, nslots per (b, h); dual zero before the first call),
+// and adds sum_m lambda_t^(8+m) dlambda_t^(8+m) into ru (B, T, H) of the tiles it runs.
 cudaError_t launch_tc_bwd_q(const TcPlan& p, const void* q, const void* dO, const float* a, const float* lam,
                             const char* tree_ws, float* dq32, float* dlam, float* dual, const int* dual_off,
-                            int nslots, unsigned* status, cudaStream_t st);
+                            int nslots, float* ru, unsigned* status, cudaStream_t st);
 // Backward, key side of the inter-tile levels on the tensor cores: the tile-decay running
 // sums (fp64, (B*H, NT+1) in P), the duals as fp16 images (dimg: 16 KB per slot, dmeta: 4
 // u32 per slot), then adds into dk32 and dv32, and v_s . (that part of dv_s) into cu.
@@ -155,7 +156,8 @@ cudaError_t launch_tc_bwd_kv(const TcPlan& p, const void* k, const void* v, cons
                              int nslots, float* dk32, float* dv32, float* cu, unsigned* status, cudaStream_t st);
 // Backward: the in-tile pairs (levels 0..7) on the tensor cores, for tc_supported shapes;
 // assigns the fp32 per-head dq, dk, dv buffers, dlambda (levels >= 8 zeroed) and cu, the
-// column sums C_s of the in-tile pair terms.
+// column sums C_s of the in-tile pair terms, followed in the same buffer by R_t = sum over
+// levels 0..7 of lambda_t^l dlambda_t^l (both (B, T, H) fp32).
 cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k, const void* v, const void* dO,
                                 const float* a, const float* lam, float* dq32, float* dk32, float* dv32,
                                 float* dlam, float* cu, unsigned* status, cudaStream_t st);

@@ -38,7 +38,8 @@ struct TcBwdParams {
   float* dk32;   // (B, T, H, d_k)
   float* dv32;   // (B, T, H, d_v)
   float* dlam;   // (B, T, H, L): levels 0..7 written, the rest zeroed
-  float* cu;     // (B, T, H): C_s = sum_t A_ts over the in-tile pairs (fp32, from S and E)
+  float* cu;     // (B, T, H): C_s = sum_t A_ts over the in-tile pairs (fp32, from S and E);
+                 // followed by R_t = sum_l lambda_t^l dlambda_t^l over levels 0..7 (B, T, H)
   unsigned* status;
   int pf_stride;  // the CTA this far ahead (the SM count) gets its tiles prefetched into L2
 };
@@ -340,10 +341,19 @@ __global__ void __launch_bounds__(256, 1) tc_bwd_intra_kernel(const __grid_const
       p.cu[row * p.H + h] = sCol[r];
       float* dl = p.dlam + (row * p.H + h) * p.L;
       const float* accr = sAcc + r * 9;
+      const float* lamr = sLam8 + r * 9;
+      float dv8[kLevIntra];
 #pragma unroll
-      for (int l = 0; l < 6; ++l) dl[l] = accr[l];
-      dl[6] = acc6 + accr[6];
-      dl[7] = acc7 + accr[7];
+      for (int l = 0; l < 6; ++l) dv8[l] = accr[l];
+      dv8[6] = acc6 + accr[6];
+      dv8[7] = acc7 + accr[7];
+      float R = 0.f;  // this row's part of R_t (d(log a) reads it instead of lambda and dlambda)
+#pragma unroll
+      for (int l = 0; l < kLevIntra; ++l) {
+        dl[l] = dv8[l];
+        R += lamr[l] * dv8[l];
+      }
+      p.cu[(size_t)p.B * p.T * p.H + row * p.H + h] = R;
       for (int l = kLevIntra; l < p.L; ++l) dl[l] = 0.f;  // inter-tile levels: added later
     }
   } else {
@@ -520,6 +530,7 @@ struct TcBwdQParams {
   float* dq32;
   float* dlam;
   float* dual;        // (B*H, nslots, d_k, d_v) fp32, zero on entry
+  float* ru;          // (B, T, H): R_t, to which the inter-tile levels' lambda dlambda is added
   unsigned* status;
 };
 
@@ -689,6 +700,7 @@ __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant_
   float acc[64];
 #pragma unroll
   for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+  float Rq = 0.f;  // sum over this tile's inter levels of lambda_t^(8+m) dlambda_t^(8+m)
   int issued = nlev < 2 ? nlev : 2, consumed = 0, y_issued = 0;
   const uint32_t id_z = ptx::idesc_f16_f32(128, 128, 0, 0);
   const uint32_t id_y = ptx::idesc_f16_f32(128, 64, 0, 1);
@@ -767,7 +779,9 @@ __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant_
           }
         }
       }
-      p.dlam[(row * p.H + h) * p.L + kLevIntra + m] = exp2f(gt + D) * pow2s(eq + en + ed) * dot;
+      const float dlm = exp2f(gt + D) * pow2s(eq + en + ed) * dot;
+      p.dlam[(row * p.H + h) * p.L + kLevIntra + m] = dlm;
+      Rq += sLamI[i * 128 + r] * dlm;
     }
     {  // dual rows (TMEM lane = d_k index r), d_v columns 32 hf .. 32 hf + 31
       const int tau = tau_of(i);
@@ -789,6 +803,9 @@ __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant_
     ptx::tc_fence_before();
     ptx::mbar_arrive(&bar_yf);
   }
+  // the in-tile kernel wrote its part; a reduction (not a load and a store) keeps the
+  // read off this CTA's path, and this is the only addition to the value
+  if (ok && hf == 0) atomicAdd(p.ru + row * p.H + h, Rq);
   // dq rows (columns 64 hf .. 64 hf + 63: boxes 2 hf, 2 hf + 1) are staged over Q, dO and
   // the images, free once every level is read, and added into the per-head buffer (which
   // the in-tile kernel wrote) with TMA reductions.
@@ -1170,7 +1187,7 @@ cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k,
 
 cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, const float* a, const float* lam,
                             const char* tree_ws, float* dq32, float* dlam, float* dual, const int* dual_off,
-                            int nslots, unsigned* status, cudaStream_t st) {
+                            int nslots, float* ru, unsigned* status, cudaStream_t st) {
   CUtensorMap mQ, mD, mDQ;
   if (!make_map(&mQ, q, kDk, tp.G, tp.T, tp.B) || !make_map(&mD, dO, kDv, tp.H, tp.T, tp.B) ||
       !make_map_f32(&mDQ, dq32, kDk, tp.H, tp.T, tp.B))
@@ -1196,6 +1213,7 @@ cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, con
   p.dq32 = dq32;
   p.dlam = dlam;
   p.dual = dual;
+  p.ru = ru;
   p.status = status;
   const int smem = bwdq_smem_bytes(bit_length(tp.NT - 1));
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
