@@ -358,12 +358,12 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, size_t i, float4 v) {
 // Four consecutive elements per thread (d_k and d_v are multiples of 4).
 template <typename TIn>
 __global__ void __launch_bounds__(kT) bwd_final(GenPlan p, BwdArgs x, size_t off_dq, size_t off_dk,
-                                               size_t off_dv) {
+                                               size_t off_dv, bool with_dv) {
   const float* dq32 = reinterpret_cast<const float*>(x.ws + off_dq);
   const float* dk32 = reinterpret_cast<const float*>(x.ws + off_dk);
   const float* dv32 = reinterpret_cast<const float*>(x.ws + off_dv);
   const size_t nqk = (size_t)p.B * p.T * p.G * p.dk;
-  const size_t nv = (size_t)p.B * p.T * p.H * p.dv;
+  const size_t nv = with_dv ? (size_t)p.B * p.T * p.H * p.dv : 0;  // (tensor cores: written by tc_bwd_kv)
   for (size_t e4 = blockIdx.x * (size_t)kT + threadIdx.x; 4 * e4 < nqk + nv; e4 += (size_t)gridDim.x * kT) {
     const size_t e = 4 * e4;
     if (e < nqk) {
@@ -601,7 +601,7 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
                               reinterpret_cast<uint8_t*>(x.ws + bp.off_dimg),
                               reinterpret_cast<unsigned*>(x.ws + bp.off_dmeta),
                               reinterpret_cast<double*>(x.ws + bp.off_P), tc_dual_off, tc_slots,
-                              reinterpret_cast<float*>(x.ws + bp.off_dk), reinterpret_cast<float*>(x.ws + bp.off_dv),
+                              reinterpret_cast<float*>(x.ws + bp.off_dk), reinterpret_cast<float*>(x.ws + bp.off_dv), x.dv,
                               reinterpret_cast<float*>(x.ws + bp.off_cu), fa.status, st)) != cudaSuccess)
       return e;
   } else {
@@ -615,7 +615,7 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
   }
   const size_t n4 = (size_t)p.B * p.T * (p.G * dk + p.H * dv) / 4;
   const unsigned gf = (unsigned)((n4 + kT - 1) / kT < 8192 ? (n4 + kT - 1) / kT : 8192);
-  bwd_final<TIn><<<gf, kT, 0, st>>>(p, x, bp.off_dq, bp.off_dk, bp.off_dv);
+  bwd_final<TIn><<<gf, kT, 0, st>>>(p, x, bp.off_dq, bp.off_dk, bp.off_dv, !bp.tc);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   const int nch = (p.T + kDlChunk - 1) / kDlChunk;

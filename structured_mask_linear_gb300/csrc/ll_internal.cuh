@@ -150,10 +150,12 @@ cudaError_t launch_tc_bwd_q(const TcPlan& p, const void* q, const void* dO, cons
                             int nslots, float* ru, unsigned* status, cudaStream_t st);
 // Backward, key side of the inter-tile levels on the tensor cores: the tile-decay running
 // sums (fp64, (B*H, NT+1) in P), the duals as fp16 images (dimg: 16 KB per slot, dmeta: 4
-// u32 per slot), then adds into dk32 and dv32, and v_s . (that part of dv_s) into cu.
+// u32 per slot), then adds into dk32, writes dv_out (bf16, (B, T, H, d_v)) as dv32 (the
+// in-tile part) plus its own part, and adds v_s . (its part of dv_s) into cu.
 cudaError_t launch_tc_bwd_kv(const TcPlan& p, const void* k, const void* v, const float* a, const char* tree_ws,
                              const float* dual, uint8_t* dimg, unsigned* dmeta, double* P, const int* dual_off,
-                             int nslots, float* dk32, float* dv32, float* cu, unsigned* status, cudaStream_t st);
+                             int nslots, float* dk32, float* dv32, void* dv_out, float* cu, unsigned* status,
+                             cudaStream_t st);
 // Backward: the in-tile pairs (levels 0..7) on the tensor cores, for tc_supported shapes;
 // assigns the fp32 per-head dq, dk, dv buffers, dlambda (levels >= 8 zeroed) and cu, the
 // column sums C_s of the in-tile pair terms, followed in the same buffer by R_t = sum over

@@ -914,19 +914,45 @@ struct TcBwdKVParams {
   int pf_stride;  // the CTA this far ahead (the SM count) gets its K and V tiles prefetched into L2
 };
 
-constexpr int kSmemBwdKV = 98304 + 1024;  // K, V, two dual images; then the dk and dv staging
+// K, V, two dual images (then the dk staging and dv's bf16 staging), the in-tile part of dv
+constexpr int kSmemBwdKV = 98304 + 32768 + 1024;
+
+// dv of row r, columns 16 qq .. 16 qq + 15: the in-tile part (fp32 boxes of 32 columns with
+// the 128-byte swizzle, as loaded) plus add[] (already weighted), as bf16 into the 64-wide
+// output box (the same swizzle) of the staging area.
+__device__ __forceinline__ void kv_stage_dv(const uint8_t* rdv, uint8_t* ob, int r, int qq, const float (&add)[16]) {
+  const int rot = r & 7;
+  const uint8_t* src = rdv + (qq >> 1) * 16384 + r * 128;
+  float d[16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float4 x = *reinterpret_cast<const float4*>(src + (((4 * (qq & 1) + c) ^ rot) << 4));
+    d[4 * c] = x.x + add[4 * c];
+    d[4 * c + 1] = x.y + add[4 * c + 1];
+    d[4 * c + 2] = x.z + add[4 * c + 2];
+    d[4 * c + 3] = x.w + add[4 * c + 3];
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    *reinterpret_cast<uint4*>(ob + r * 128 + (((2 * qq + j) ^ rot) << 4)) =
+        make_uint4(pack_bf16(d[8 * j], d[8 * j + 1]), pack_bf16(d[8 * j + 2], d[8 * j + 3]),
+                   pack_bf16(d[8 * j + 4], d[8 * j + 5]), pack_bf16(d[8 * j + 6], d[8 * j + 7]));
+}
 
 __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap mapK,
                                                            const __grid_constant__ CUtensorMap mapV,
                                                            const __grid_constant__ CUtensorMap mapDK,
                                                            const __grid_constant__ CUtensorMap mapDV,
+                                                           const __grid_constant__ CUtensorMap mapDVO,
                                                            TcBwdKVParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* RK = smem;           // 32 KB: K (bf16, then fp16)
-  uint8_t* RV = smem + 32768;   // 16 KB: V (bf16, then fp16)
-  uint8_t* RI = smem + 49152;   // 2 x 16 KB: dual images
-  __shared__ __align__(8) uint64_t bar_ld, bar_z, bar_e[2], bar_zf;
+  uint8_t* RK = smem;            // 32 KB: K (bf16, then fp16)
+  uint8_t* RV = smem + 32768;    // 16 KB: V (bf16, then fp16)
+  uint8_t* RI = smem + 49152;    // 2 x 16 KB: dual images
+  uint8_t* RDV = smem + 98304;   // 32 KB: the in-tile part of dv (fp32, two 32-column boxes)
+  uint8_t* ROV = smem + 65536;   // 16 KB at the end: dv in bf16 (over the second image)
+  __shared__ __align__(8) uint64_t bar_ld, bar_z, bar_e[2], bar_zf, bar_dv;
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[16];
   __shared__ float s_mx[16][2];
@@ -953,7 +979,34 @@ __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant
   }
   __syncthreads();
   const int nl = s_nl;
-  if (nl == 0) return;  // no level reads this tile's nodes
+  if (nl == 0) {  // no level reads this tile's nodes: dv is the in-tile part, cast to bf16
+    if (tid == 0) {
+      ptx::mbar_init(&bar_dv, 1);
+      ptx::fence_mbar_init();
+      ptx::mbar_arrive_expect_tx(&bar_dv, 32768);
+      ptx::tma_load_4d(RDV, &mapDV, &bar_dv, 0, h, (int)t0, b);
+      ptx::tma_load_4d(RDV + 16384, &mapDV, &bar_dv, 32, h, (int)t0, b);
+    }
+    __syncthreads();
+    bool ok = wait_bar(&bar_dv, 0);
+    if (!ok) atomicExch(p.status, kStatusTimeout);
+    if (ok) {
+      float zero[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) zero[c] = 0.f;
+      kv_stage_dv(RDV, ROV, r, qq, zero);
+      ptx::fence_proxy_async_smem();
+    }
+    ok = __syncthreads_and(ok);
+    if (ok && tid == 0) {
+      ptx::tma_store_4d(&mapDVO, ROV, 0, h, (int)t0, b);
+      ptx::bulk_commit_group();
+      ptx::bulk_wait_read_all();  // the staging is read before the CTA ends
+    }
+    if (!ok && tid == 0) wait_bar(&bar_dv, 0);  // bounded: let the copy land before the CTA ends
+    __syncthreads();
+    return;
+  }
   auto slot_of = [&](int j) {
     const int m = s_lv[j];
     return (size_t)bh * p.nslots + p.dual_off[m] + ((u >> m) >> 1);
@@ -964,7 +1017,12 @@ __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant
     ptx::mbar_init(&bar_e[0], 1);
     ptx::mbar_init(&bar_e[1], 1);
     ptx::mbar_init(&bar_zf, 512);
+    ptx::mbar_init(&bar_dv, 1);
     ptx::fence_mbar_init();
+    // the in-tile part of dv (the in-tile kernel's store), read at the end
+    ptx::mbar_arrive_expect_tx(&bar_dv, 32768);
+    ptx::tma_load_4d(RDV, &mapDV, &bar_dv, 0, h, (int)t0, b);
+    ptx::tma_load_4d(RDV + 16384, &mapDV, &bar_dv, 32, h, (int)t0, b);
     ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
     ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
     ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
@@ -1123,33 +1181,37 @@ __global__ void __launch_bounds__(512, 1) tc_bwd_kv_kernel(const __grid_constant
     }
     atomicAdd(p.cu + row * p.H + h, rs * pow2i(ev) * cdot);
   }
-  // dk (columns 32 qq .. 32 qq + 31: box qq, from 0) and dv (columns 16 qq .. 16 qq + 15:
-  // half of box qq >> 1, from 64 KB) are staged over K, V and the images, free once every
-  // level is read and V's dot is taken, and added into the per-head buffers with TMA
-  // reductions.
+  // dk (columns 32 qq .. 32 qq + 31: box qq, from 0) is staged over K, V and the first
+  // image, free once every level is read and V's dot is taken, and added into the per-head
+  // buffer with TMA reductions.  dv (columns 16 qq .. 16 qq + 15) is final here: the
+  // in-tile part plus this kernel's, in bf16, staged over the second image and stored
+  // into the output.
   __syncthreads();
+  bool okv = ok && wait_bar(&bar_dv, 0);
+  if (ok && !okv) atomicExch(p.status, kStatusTimeout);
+  ok = ok && okv;
   if (ok) {
     uint8_t* kb = smem + qq * 16384 + r * 128;
 #pragma unroll
     for (int c = 0; c < 8; ++c)
       *reinterpret_cast<float4*>(kb + ((c ^ rot) << 4)) =
           make_float4(rs * ak[4 * c], rs * ak[4 * c + 1], rs * ak[4 * c + 2], rs * ak[4 * c + 3]);
-    uint8_t* vb = smem + 65536 + (qq >> 1) * 16384 + r * 128;
+    float add[16];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      *reinterpret_cast<float4*>(vb + (((4 * (qq & 1) + c) ^ rot) << 4)) =
-          make_float4(rs * av[4 * c], rs * av[4 * c + 1], rs * av[4 * c + 2], rs * av[4 * c + 3]);
+    for (int c = 0; c < 16; ++c) add[c] = rs * av[c];
+    kv_stage_dv(RDV, ROV, r, qq, add);
     ptx::fence_proxy_async_smem();
   }
   ok = __syncthreads_and(ok);
   if (ok && tid == 0) {
     for (int j = 0; j < 4; ++j) ptx::tma_reduce_add_4d(&mapDK, smem + j * 16384, 32 * j, h, (int)t0, b);
-    for (int j = 0; j < 2; ++j) ptx::tma_reduce_add_4d(&mapDV, smem + 65536 + j * 16384, 32 * j, h, (int)t0, b);
+    ptx::tma_store_4d(&mapDVO, ROV, 0, h, (int)t0, b);
     ptx::bulk_commit_group();
     ptx::bulk_wait_read_all();  // the staging is read before the CTA ends
   }
   if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
     wait_bar(&bar_ld, 0);
+    wait_bar(&bar_dv, 0);
     for (int j = consumed; j < issued; ++j) wait_bar(&bar_e[j & 1], (j >> 1) & 1);
     if (z_issued > 0) wait_bar(&bar_z, (z_issued - 1) & 1);
   }
@@ -1226,7 +1288,8 @@ cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, con
 
 cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, const float* a, const char* tree_ws,
                              const float* dual, uint8_t* dimg, unsigned* dmeta, double* P, const int* dual_off,
-                             int nslots, float* dk32, float* dv32, float* cu, unsigned* status, cudaStream_t st) {
+                             int nslots, float* dk32, float* dv32, void* dv_out, float* cu, unsigned* status,
+                             cudaStream_t st) {
   const unsigned BH = (unsigned)(tp.B * tp.H);
   tc_tile_prefix_kernel<<<BH, 256, 0, st>>>(reinterpret_cast<const unsigned*>(tree_ws + tp.off_meta), tp.nnodes,
                                             tp.NT, P);
@@ -1236,9 +1299,10 @@ cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, con
   tc_dual_publish_kernel<<<(unsigned)((size_t)BH * nslots), 128, 0, st>>>(dual, dimg, dmeta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
-  CUtensorMap mK, mV, mDK, mDV;
+  CUtensorMap mK, mV, mDK, mDV, mDVO;
   if (!make_map(&mK, k, kDk, tp.G, tp.T, tp.B) || !make_map(&mV, v, kDv, tp.H, tp.T, tp.B) ||
-      !make_map_f32(&mDK, dk32, kDk, tp.H, tp.T, tp.B) || !make_map_f32(&mDV, dv32, kDv, tp.H, tp.T, tp.B))
+      !make_map_f32(&mDK, dk32, kDk, tp.H, tp.T, tp.B) || !make_map_f32(&mDV, dv32, kDv, tp.H, tp.T, tp.B) ||
+      !make_map(&mDVO, dv_out, kDv, tp.H, tp.T, tp.B))
     return cudaErrorInvalidValue;
   TcBwdKVParams p{};
   p.B = tp.B;
@@ -1267,7 +1331,7 @@ cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, con
   if ((e = cudaFuncSetAttribute(tc_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBwdKV)) !=
       cudaSuccess)
     return e;
-  tc_bwd_kv_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 512, kSmemBwdKV, st>>>(mK, mV, mDK, mDV, p);
+  tc_bwd_kv_kernel<<<(unsigned)((size_t)tp.B * tp.NT * tp.H), 512, kSmemBwdKV, st>>>(mK, mV, mDK, mDV, mDVO, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
