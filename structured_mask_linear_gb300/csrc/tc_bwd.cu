@@ -882,21 +882,41 @@ __global__ void __launch_bounds__(256) tc_tile_prefix_kernel(const unsigned* met
   }
 }
 
+// One CTA per dual slot: the fp32 dual (d_k x d_v) -> its fp16 image with a power-of-two
+// scale, as a node is published.  The threads read the slot in consecutive 16-byte pieces
+// (thread i: pieces i, i + 128, ...), not a row each, so that every warp load is four whole
+// 128-byte lines; each piece is half of a 16-byte chunk of the image.
 __global__ void __launch_bounds__(128) tc_dual_publish_kernel(const float* dual, uint8_t* img, unsigned* meta) {
   __shared__ __align__(1024) uint8_t stage[kImgBytes];
   __shared__ float2 s_red2[4];
+  const int tid = threadIdx.x;
   const size_t slot = blockIdx.x;
-  const float* src = dual + (slot * kDk + threadIdx.x) * kDv;
-  float cur[kDv];
+  const float4* src = reinterpret_cast<const float4*>(dual + slot * kDk * kDv);
+  constexpr int kPieces = kDk * kDv / 4 / 128;  // 16 per thread
+  float4 v[kPieces];
+  float m = 0.f;
 #pragma unroll
-  for (int j = 0; j < kDv; j += 4) {
-    const float4 v = *reinterpret_cast<const float4*>(src + j);
-    cur[j] = v.x;
-    cur[j + 1] = v.y;
-    cur[j + 2] = v.z;
-    cur[j + 3] = v.w;
+  for (int i = 0; i < kPieces; ++i) {
+    v[i] = src[tid + 128 * i];
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
   }
-  publish_node(cur, stage, slot, 0.f, s_red2, img, meta);
+  const int e = f16_exp(block_max2(make_float2(m, 0.f), s_red2).x);
+  const float sc = pow2i(-e);
+#pragma unroll
+  for (int i = 0; i < kPieces; ++i) {
+    const int idx = tid + 128 * i;           // piece: elements 4 idx .. 4 idx + 3
+    const int row = idx >> 4, c = (idx & 15) >> 1, half = idx & 1;  // d_k row, 8-column chunk
+    *reinterpret_cast<uint2*>(stage + row * 128 + ((c ^ (row & 7)) << 4) + half * 8) =
+        make_uint2(pack_h2(v[i].x * sc, v[i].y * sc), pack_h2(v[i].z * sc, v[i].w * sc));
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(img + slot * kImgBytes);
+#pragma unroll
+  for (int r = 0; r < kImgBytes / 16 / 128; ++r) dst[r * 128 + tid] = reinterpret_cast<const uint4*>(stage)[r * 128 + tid];
+  if (tid == 0) {
+    meta[slot * kMeta + 1] = (unsigned)e;
+    meta[slot * kMeta + 2] = __float_as_uint(0.f);
+  }
 }
 
 struct TcBwdKVParams {
