@@ -117,6 +117,14 @@ __device__ __forceinline__ void gdn_double_level(float* Am, float* Tm, int n, in
   }
   __syncthreads();
   if (ok) {  // T21 = -T22 X
+    // T22 is lower triangular, so a tile's sum runs over (ti + RT + 3) / 4 steps.  Warps w
+    // and w + 4 share a sub-partition: warps 4..7 take their row tiles in reverse order
+    // (within their pair, or within the upper half when one pair spans all warps), so that
+    // each sub-partition gets a short and a long share while every warp keeps adjacent
+    // rows (a uniform trip count).
+    const int q = (tid % per) / nt;  // 16 row tiles per pair
+    const int qr = tid < 128 ? q : (n == 64 ? 23 - q : 15 - q);
+    const int ti = qr * RT;
     float acc[RT][4] = {};
     const float* trow = Tm + (i0 + n + ti) * kGP + i0 + n;
     const int kend = (ti + RT + 3) & ~3;
