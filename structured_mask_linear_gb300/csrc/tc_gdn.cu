@@ -15,9 +15,9 @@ namespace {
 // tc_gdn_local, one CTA per (b, h, chunk), 256 threads, one CTA per SM:
 //   K Kᵀ on tcgen05 from the bf16 keys (exact products, fp32 sums); A in fp32 in shared
 //   memory (meanwhile the other four warps take the K and V tile maxima and split
-//   diag(beta) V); T on the CUDA cores (its 16 x 16 diagonal blocks by substitution in
-//   registers, then the blocks below them by doubling, T21 = -T22 A21 T11 for blocks of
-//   16, 32 and 64); then [W | U_loc] = T [diag(beta 2^g) K | diag(beta) V] on tcgen05 with every operand
+//   diag(beta) V); T's 16 x 16 diagonal blocks by substitution in registers, then the
+//   blocks below them by doubling, T21 = -T22 A21 T11, for blocks of 16 and 32 on the
+//   CUDA cores and of 64 on tcgen05; then [W | U_loc] = T [diag(beta 2^g) K | diag(beta) V] on tcgen05 with every operand
 //   split into an fp16 high part and the fp16 rounding remainder (hi hi + lo hi + hi lo,
 //   about 22 significant bits), each with a power-of-two tile scale.  Per chunk the
 //   workspace gets W split the same way (hi and lo fp16 in the MMA operand layout, with
@@ -167,11 +167,12 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   float* b8 = fk + 128;                                        // 128: 2^(g_end8(s) - g_s)
   uint8_t* VHI = reinterpret_cast<uint8_t*>(b8 + 128);         // 16 KB: diag(beta) V hi (fp16)
   uint8_t* VLO = VHI + 16384;                                  // 16 KB: ... lo
-  __shared__ __align__(8) uint64_t bar_ld, bar_a, bar_w;
+  __shared__ __align__(8) uint64_t bar_ld, bar_a, bar_w, bar_d;
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[8];
   __shared__ float s_mx[8];
   __shared__ float s_kv[4][2];
+  __shared__ float s_m3[8][3];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
   const int r = tid & 127, rot = r & 7;
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     ptx::mbar_init(&bar_ld, 1);
     ptx::mbar_init(&bar_a, 1);
     ptx::mbar_init(&bar_w, 1);
+    ptx::mbar_init(&bar_d, 1);
     ptx::fence_mbar_init();
     ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
     ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
@@ -345,14 +347,189 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   // Blocks below the diagonal by doubling: once the inverses T11 and T22 of two adjacent
   // diagonal blocks of size n are known, the block below them is T21 = -T22 A21 T11, A21
   // the block of A between them (the inverse of a 2 x 2 block lower triangle).  For n =
-  // 16, 32, 64 every pair is done at once: X = A21 T11 into A's upper triangle (zero and
+  // 16 and 32 every pair is done at once: X = A21 T11 into A's upper triangle (zero and
   // not read again) at rows i0.., columns i0 + n.., then T21 = -T22 X.  Each thread takes
   // n / 16 x 4 outputs (so all threads work at every level), the column tiles fastest
   // across a warp: the rows it reads of A21 and T22 are the same for many threads
   // (broadcasts), the rows of T11 and X are read along (conflict-free).
   gdn_double_level<1>(Am, Tm, 16, tid, ok);
   gdn_double_level<2>(Am, Tm, 32, tid, ok);
-  gdn_double_level<4>(Am, Tm, 64, tid, ok);
+  // The n = 64 level on the tensor cores: T21 = -T22 X with X = A21 T11 (64 x 64 blocks),
+  // as two M = 128 products with the A operand in tensor memory (free since the A phase)
+  // and B in RV (free since V's split): X' = A[:, 0:64] T11, whose rows 64..127 are X,
+  // then T21' = T[:, 64:128] X, whose rows 64..127 are T22 X (T's rows 0..63 are zero
+  // there).  Every operand is split into fp16 high and low parts with a power-of-two tile
+  // scale (hi hi + lo hi + hi lo, about 22 significant bits).  Thread (r, hf) holds row r,
+  // K columns 32 hf .. 32 hf + 31 of the A operands; B rows are 64 d_k-wide, 128-byte
+  // swizzled.
+  int d_issued = 0;
+  {
+    const int hf = tid >> 7;
+    uint8_t* BHI = RV;           // B operand, hi (64 rows x 128 B)
+    uint8_t* BLO = RV + 8192;    // ... lo
+    const int kb = tid >> 2, qb = tid & 3;  // T11 row and 16-column quarter of this thread
+    float mA = 0.f, m1 = 0.f, m2 = 0.f;
+    if (ok) {
+      const float* ar = Am + r * kGP + 32 * hf;
+      const float* t2 = Tm + r * kGP + 64 + 32 * hf;
+      const float* t1 = Tm + kb * kGP + 16 * qb;
+      if (r >= 64)  // rows 0..63 of A's first 64 columns hold the smaller levels' X blocks
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(ar + j), y = *reinterpret_cast<const float4*>(t2 + j);
+          mA = fmaxf(mA, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+          m2 = fmaxf(m2, fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w))));
+        }
+#pragma unroll
+      for (int j = 0; j < 16; j += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(t1 + j);
+        m1 = fmaxf(m1, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, off));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+      m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, off));
+    }
+    if (lane == 0) {
+      s_m3[warp][0] = mA;
+      s_m3[warp][1] = m1;
+      s_m3[warp][2] = m2;
+    }
+    __syncthreads();
+    float xA = 0.f, x1 = 0.f, x2 = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      xA = fmaxf(xA, s_m3[w][0]);
+      x1 = fmaxf(x1, s_m3[w][1]);
+      x2 = fmaxf(x2, s_m3[w][2]);
+    }
+    const int eA = f16_exp(xA), e1 = f16_exp(x1), e2 = f16_exp(x2);
+    if (ok) {
+      // A[r, 32 hf ..] -> TMEM columns 16 hf .. (hi: tA + 0..31, lo: tA + 32..63); the
+      // same for T[r, 64 + 32 hf ..] at tW
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const float* src = which == 0 ? Am + r * kGP + 32 * hf : Tm + r * kGP + 64 + 32 * hf;
+        const float sc = pow2i(-(which == 0 ? eA : e2));
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          // rows 0..63 take zeros (their products are not read; T is zero there anyway)
+          const float4 x0 = r >= 64 ? *reinterpret_cast<const float4*>(src + 8 * q8) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 x1v =
+              r >= 64 ? *reinterpret_cast<const float4*>(src + 8 * q8 + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float v8[8] = {x0.x, x0.y, x0.z, x0.w, x1v.x, x1v.y, x1v.z, x1v.w};
+          uint4 h4, l4;
+          split8(v8, sc, h4, l4);
+          hi[4 * q8] = h4.x; hi[4 * q8 + 1] = h4.y; hi[4 * q8 + 2] = h4.z; hi[4 * q8 + 3] = h4.w;
+          lo[4 * q8] = l4.x; lo[4 * q8 + 1] = l4.y; lo[4 * q8 + 2] = l4.z; lo[4 * q8 + 3] = l4.w;
+        }
+        const uint32_t tb = (which == 0 ? tA : tW) + lane_off;
+        ptx::tmem_st16(tb + 16 * hf, hi);
+        ptx::tmem_st16(tb + 32 + 16 * hf, lo);
+      }
+      // T11 row kb, columns 16 qb .. 16 qb + 15 (chunks 2 qb, 2 qb + 1) -> B hi, lo
+      const float sc1 = pow2i(-e1);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const float* src = Tm + kb * kGP + 16 * qb + 8 * h2;
+        const float4 x0 = *reinterpret_cast<const float4*>(src);
+        const float4 x1v = *reinterpret_cast<const float4*>(src + 4);
+        const float v8[8] = {x0.x, x0.y, x0.z, x0.w, x1v.x, x1v.y, x1v.z, x1v.w};
+        uint4 h4, l4;
+        split8(v8, sc1, h4, l4);
+        const int off = kb * 128 + (((2 * qb + h2) ^ (kb & 7)) << 4);
+        *reinterpret_cast<uint4*>(BHI + off) = h4;
+        *reinterpret_cast<uint4*>(BLO + off) = l4;
+      }
+      ptx::tmem_st_wait();
+      ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    ok = __syncthreads_and(ok);
+    const uint32_t id64 = ptx::idesc_f16_f32(128, 64, 0, 1);
+    const uint32_t b0 = ptx::smem_u32(RV);
+    auto issue = [&](uint32_t dcol, uint32_t acol) {  // D (+)= A (TMEM hi/lo) B (smem hi/lo)
+      ptx::tc_fence_after();
+      const uint32_t ao[3] = {0, 32, 0}, bo[3] = {0, 0, 8192};
+#pragma unroll
+      for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::umma_f16_tmem_a(dcol, acol + ao[pass] + kk * 8, ptx::smem_desc_sw128(b0 + bo[pass] + kk * 2048, 1024, 1024),
+                               id64, pass > 0 || kk > 0);
+      ptx::umma_commit(&bar_d);
+    };
+    if (ok && tid == 0) {
+      issue(tA + 64, tA);  // X' = A[:, 0:64] T11
+      ++d_issued;
+    }
+    if (ok) {
+      ok = wait_bar(&bar_d, 0);
+      if (!ok) atomicExch(p.status, kStatusTimeout);
+    }
+    ok = __syncthreads_and(ok);
+    // X (rows 64..127 of X', lanes 64..127): its maximum, then hi, lo as B (row r - 64)
+    float xv[32];
+    float mX = 0.f;
+    if (ok && r >= 64) {
+      ptx::tc_fence_after();
+      ptx::tmem_ld32(tA + 64 + lane_off + 32 * hf, xv);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mX = fmaxf(mX, fabsf(xv[j]));
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) mX = fmaxf(mX, __shfl_xor_sync(0xffffffffu, mX, off));
+    if (lane == 0) s_m3[warp][0] = mX;
+    __syncthreads();
+    float xX = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) xX = fmaxf(xX, s_m3[w][0]);
+    const int eX = f16_exp(xX);
+    if (ok && r >= 64) {
+      const float scx = pow2i(-eX);
+      const int k = r - 64;
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const float v8[8] = {xv[8 * q8], xv[8 * q8 + 1], xv[8 * q8 + 2], xv[8 * q8 + 3],
+                             xv[8 * q8 + 4], xv[8 * q8 + 5], xv[8 * q8 + 6], xv[8 * q8 + 7]};
+        uint4 h4, l4;
+        split8(v8, scx, h4, l4);
+        const int off = k * 128 + (((4 * hf + q8) ^ (k & 7)) << 4);
+        *reinterpret_cast<uint4*>(BHI + off) = h4;
+        *reinterpret_cast<uint4*>(BLO + off) = l4;
+      }
+      ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    ok = __syncthreads_and(ok);
+    if (ok && tid == 0) {
+      issue(tW + 64, tW);  // T21' = T[:, 64:128] X
+      ++d_issued;
+    }
+    if (ok) {
+      ok = wait_bar(&bar_d, 1);
+      if (!ok) atomicExch(p.status, kStatusTimeout);
+    }
+    ok = __syncthreads_and(ok);
+    // T21 = -T21' 2^(e2 + eX + eA + e1): rows 64..127, columns 0..63 of T
+    if (ok && r >= 64) {
+      ptx::tc_fence_after();
+      float y[32];
+      ptx::tmem_ld32(tW + 64 + lane_off + 32 * hf, y);
+      ptx::tmem_ld_wait();
+      const float sc = -pow2s(e2 + eX) * pow2s(eA + e1);
+      float* dst = Tm + r * kGP + 32 * hf;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(dst + j) = make_float4(sc * y[j], sc * y[j + 1], sc * y[j + 2], sc * y[j + 3]);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+  }
   // T's tile scale (the maximum over its elements; those of K and V came with the A
   // phase): every thread keeps half of its row r (columns 64 hf ..) in registers, so that
   // T's hi and lo parts can go over T itself.  Meanwhile diag(beta 2^g) K -> fp16 hi, lo
@@ -504,6 +681,7 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
     wait_bar(&bar_ld, 0);
     if (a_issued) wait_bar(&bar_a, 0);
+    if (d_issued) wait_bar(&bar_d, (d_issued - 1) & 1);
     if (w_issued) wait_bar(&bar_w, 0);
   }
   ptx::tc_fence_before();
