@@ -406,11 +406,10 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
       x2 = fmaxf(x2, s_m3[w][2]);
     }
     const int eA = f16_exp(xA), e1 = f16_exp(x1), e2 = f16_exp(x2);
-    if (ok) {
-      // A[r, 32 hf ..] -> TMEM columns 16 hf .. (hi: tA + 0..31, lo: tA + 32..63); the
-      // same for T[r, 64 + 32 hf ..] at tW
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
+    // A[r, 32 hf ..] (which 0) or T[r, 64 + 32 hf ..] (which 1) -> fp16 hi, lo in TMEM
+    // columns 16 hf .. of tA (hi: + 0..31, lo: + 32..63) or of tW
+    auto a_operand = [&](int which) {
+      {
         const float* src = which == 0 ? Am + r * kGP + 32 * hf : Tm + r * kGP + 64 + 32 * hf;
         const float sc = pow2i(-(which == 0 ? eA : e2));
         uint32_t hi[16], lo[16];
@@ -430,6 +429,9 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
         ptx::tmem_st16(tb + 16 * hf, hi);
         ptx::tmem_st16(tb + 32 + 16 * hf, lo);
       }
+    };
+    if (ok) {
+      a_operand(0);
       // T11 row kb, columns 16 qb .. 16 qb + 15 (chunks 2 qb, 2 qb + 1) -> B hi, lo
       const float sc1 = pow2i(-e1);
 #pragma unroll
@@ -466,30 +468,23 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
       issue(tA + 64, tA);  // X' = A[:, 0:64] T11
       ++d_issued;
     }
-    if (ok) {
+    if (ok) {  // T22's operand while the product runs (tW is not touched by it)
+      a_operand(1);
+      ptx::tmem_st_wait();
       ok = wait_bar(&bar_d, 0);
       if (!ok) atomicExch(p.status, kStatusTimeout);
     }
+    ptx::tc_fence_before();
     ok = __syncthreads_and(ok);
-    // X (rows 64..127 of X', lanes 64..127): its maximum, then hi, lo as B (row r - 64)
-    float xv[32];
-    float mX = 0.f;
+    // X (rows 64..127 of X', lanes 64..127) -> hi, lo as B (row r - 64), with the scale of
+    // a bound: |X'| <= 64 max|A op| max|T11 op| (a few binades above the maximum at most;
+    // fp16 keeps 29 binades below 2^15 in its normal range)
+    const int eX = f16_exp(64.f * (xA * pow2i(-eA)) * (x1 * pow2i(-e1)));
     if (ok && r >= 64) {
+      float xv[32];
       ptx::tc_fence_after();
       ptx::tmem_ld32(tA + 64 + lane_off + 32 * hf, xv);
       ptx::tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) mX = fmaxf(mX, fabsf(xv[j]));
-    }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) mX = fmaxf(mX, __shfl_xor_sync(0xffffffffu, mX, off));
-    if (lane == 0) s_m3[warp][0] = mX;
-    __syncthreads();
-    float xX = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) xX = fmaxf(xX, s_m3[w][0]);
-    const int eX = f16_exp(xX);
-    if (ok && r >= 64) {
       const float scx = pow2i(-eX);
       const int k = r - 64;
 #pragma unroll
