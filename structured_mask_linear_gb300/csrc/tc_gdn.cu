@@ -614,27 +614,12 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   const float sw = pow2s(et + ek), su = pow2s(et + ev);
   // Every thread takes half of its row r: W's d_k columns 64 hf .. 64 hf + 63 (the box hf of
   // the operand layout) and U_loc's d_v columns 32 hf .. 32 hf + 31.
-  float mw = 0.f;
+  // W's scale from a bound, with no pass over W: |W| <= 128 max|T| max|diag(beta 2^g) K|
+  // (at most a few binades above W's maximum; fp16 keeps 29 below 2^15 in its normal range)
+  const float xk = fmaxf(fmaxf(s_kv[0][0], s_kv[1][0]), fmaxf(s_kv[2][0], s_kv[3][0]));
+  const int ew = f16_exp(128.f * mxt * xk);
   if (ok) {
     ptx::tc_fence_after();
-#pragma unroll 1
-    for (int c0 = 0; c0 < 64; c0 += 32) {
-      float y[32];
-      ptx::tmem_ld32(tW + lane_off + hf * 64 + c0, y);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) mw = fmaxf(mw, fabsf(y[j]));
-    }
-  }
-#pragma unroll
-  for (int off = 16; off; off >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
-  if (lane == 0) s_red[warp] = mw;
-  __syncthreads();
-  float mwa = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) mwa = fmaxf(mwa, s_red[w]);
-  const int ew = f16_exp(sw * mwa);
-  if (ok) {
     const float sc = sw * pow2i(-ew);
 #pragma unroll 1
     for (int c0 = 0; c0 < 64; c0 += 32) {
