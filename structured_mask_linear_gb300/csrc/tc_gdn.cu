@@ -50,6 +50,11 @@ __device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1
                : "memory");
 }
 
+// L2 prefetch of a contiguous range (16-byte aligned address, size a multiple of 16)
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // component i (0..3, known at compile time after unrolling) of a float4
 __device__ __forceinline__ float f4_at(const float4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -743,6 +748,11 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_consta
       ptx::mbar_arrive_expect_tx(&bar_w[(c + 1) & 1], 65536);
       ptx::bulk_load(RWb + ((c + 1) & 1) * 65536, xc + kGdnChunkBytes, 65536, &bar_w[(c + 1) & 1]);
       ++w_issued;
+      // the next chunk's U_loc, g and scale word, and its K tile, into L2: their loads come
+      // one chunk later, on this CTA's serial path
+      bulk_prefetch_l2(xc + kGdnChunkBytes + kGdnOffU, 32768 + 512 + 16);
+      tma_prefetch_4d(&mapK, 0, g, (c + 1) * kTile, b);
+      tma_prefetch_4d(&mapK, 64, g, (c + 1) * kTile, b);
     }
     const int tokr = c * kTile + r;  // this thread's token (rows of u, Z)
     // this thread's half of U_loc row r, and g
