@@ -12,7 +12,8 @@ namespace {
 // as in gdn.cu: u = U_loc - W S per chunk, T = (I + diag(beta) A)^-1, A = (K Kᵀ) ⊙
 // 2^(g_t - g_s) strictly lower, U_loc = T diag(beta) V, W = T diag(beta 2^g) K).
 //
-// tc_gdn_local, one CTA per (b, h, chunk), 256 threads, one CTA per SM:
+// tc_gdn_local, 256 threads, one persistent CTA per SM walking the (b, h, chunk) items
+// (the next chunk's K and V copied in while this one finishes); per chunk:
 //   K Kᵀ on tcgen05 from the bf16 keys (exact products, fp32 sums); A in fp32 in shared
 //   memory (meanwhile the other four warps take the K and V tile maxima and split
 //   diag(beta) V); T's 16 x 16 diagonal blocks by substitution in registers, then the
@@ -34,7 +35,7 @@ struct TcGdnParams {
   const float* a;
   const float* beta;
   uint8_t* xw;  // (B*H, T/128, kGdnChunkBytes)
-  int pf_stride;  // tc_gdn_local: the CTA this far ahead (the SM count) gets its tiles prefetched
+  int pf_stride;  // the SM count (tc_gdn_local: its grid, one persistent CTA per SM; 0: unknown)
   int b0;         // tc_gdn_pass: first batch element of this launch (CTA x: (b0 + x / H, x % H))
   void* u;        // (B, T, H, d_v) bf16: the transformed values (tc_gdn_pass)
   unsigned* status;
@@ -182,39 +183,55 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
   const int r = tid & 127, rot = r & 7;
   const int nch = p.T >> 7;
-  const int lin = blockIdx.x;
-  const int h = lin % p.H;
-  const int c = (lin / p.H) % nch;
-  const int b = lin / (p.H * nch);
-  const int g = h / p.hpg;
-  const long long t0 = (long long)c * kTile;
-  const size_t row = (size_t)b * p.T + t0 + r;
+  const int total = p.B * p.H * nch;  // chunks: lin = (b nch + c) H + h
+  // K and V of chunk lin into RK, RV (bar_ld)
+  auto load_kv = [&](int lin) {
+    const int h = lin % p.H, c = (lin / p.H) % nch, b = lin / (p.H * nch), g = h / p.hpg;
+    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
+    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, c * kTile, b);
+    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, c * kTile, b);
+    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, c * kTile, b);
+  };
+  // a and beta of row r of chunk lin
+  auto row_of = [&](int lin) {
+    const int h = lin % p.H, c = (lin / p.H) % nch, b = lin / (p.H * nch);
+    return ((size_t)b * p.T + (size_t)c * kTile + r) * p.H + h;
+  };
   if (tid == 0) {
     ptx::mbar_init(&bar_ld, 1);
     ptx::mbar_init(&bar_a, 1);
     ptx::mbar_init(&bar_w, 1);
     ptx::mbar_init(&bar_d, 1);
     ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(&bar_ld, 32768 + 16384);
-    ptx::tma_load_4d(RK, &mapK, &bar_ld, 0, g, (int)t0, b);
-    ptx::tma_load_4d(RK + 16384, &mapK, &bar_ld, 64, g, (int)t0, b);
-    ptx::tma_load_4d(RV, &mapV, &bar_ld, 0, h, (int)t0, b);
-    // One CTA per SM: the CTA that will most likely run next on this SM (one SM count
-    // ahead) finds its K and V tiles in L2.
-    const int l2 = lin + p.pf_stride;
-    if (p.pf_stride > 0 && l2 < (int)gridDim.x) {
-      const int h2 = l2 % p.H, c2 = (l2 / p.H) % nch, b2 = l2 / (p.H * nch), g2 = h2 / p.hpg;
-      tma_prefetch_4d(&mapK, 0, g2, c2 * kTile, b2);
-      tma_prefetch_4d(&mapK, 64, g2, c2 * kTile, b2);
-      tma_prefetch_4d(&mapV, 0, h2, c2 * kTile, b2);
-    }
+    load_kv(blockIdx.x);
   }
   if (warp == 0) {
     ptx::tmem_alloc(&tmem_base, 256);
     ptx::tmem_relinquish();
   }
+  float a_nx = p.a[row_of(blockIdx.x)], b_nx = tid < 128 ? p.beta[row_of(blockIdx.x)] : 0.f;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  // A persistent CTA per SM walks chunks lin = blockIdx.x, + gridDim.x, ...; the next
+  // chunk's K and V are copied into RK and RV as soon as this chunk has read them (after
+  // K's split), and its a and beta are loaded then too.  Barrier phases: bar_ld, bar_a and
+  // bar_w complete once per chunk (parity it & 1), bar_d twice (parities 0, 1).
+  bool ok = true;
+  int ld_issued = 1;                 // K/V copies issued (tid 0); copy j completes phase j & 1
+  // MMAs of the chunk in progress (cleared once a chunk has completed), for the final waits
+  bool a_issued = false, w_issued = false;
+  int d_issued = 0;
+  int it = 0, ph = 0;
+  for (int lin = blockIdx.x; ok && lin < total; lin += gridDim.x, ++it) {
+  const int h = lin % p.H;
+  const int c = (lin / p.H) % nch;
+  const int b = lin / (p.H * nch);
+  ph = it & 1;
   // chunk-local log2 decay cumsum (both halves of the block compute it)
-  float gt = log2f(p.a[row * p.H + h]);
+  float gt = log2f(a_nx);
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const float y = __shfl_up_sync(0xffffffffu, gt, off);
@@ -225,19 +242,18 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   __syncthreads();
   ptx::tc_fence_after();
   for (int w = 0; w < quad; ++w) gt += s_red[w];
-  const uint32_t tbase = tmem_base;
-  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const uint32_t tA = tbase, tW = tbase + 128, tU = tbase;
   if (tid < 128) {
-    const float bt = p.beta[row * p.H + h];
+    const float bt = b_nx;
     gs[r] = gt;
     bs[r] = bt;
     fk[r] = bt * exp2f(gt);
   }
-  bool ok = wait_bar(&bar_ld, 0);
+  ok = wait_bar(&bar_ld, ph);
   if (!ok) atomicExch(p.status, kStatusTimeout);
   ok = __syncthreads_and(ok);
-  if (ok && tid == 0) {  // K Kᵀ: M = N = 128 tokens, K = 128 d_k, bf16, both K-major
+  if (!ok) break;
+  if (tid == 0) {  // K Kᵀ: M = N = 128 tokens, K = 128 d_k, bf16, both K-major
     ptx::tc_fence_after();
     const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, 0, 0);
     const uint32_t k0 = ptx::smem_u32(RK);
@@ -249,10 +265,10 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
     }
     ptx::umma_commit(&bar_a);
   }
-  const bool a_issued = ok;
+  a_issued = true;
   if (tid < 128) b8[r] = exp2f(gs[r | 7] - gt);  // decay from key r to the end of its 8-block
   if (ok) {
-    ok = wait_bar(&bar_a, 0);
+    ok = wait_bar(&bar_a, ph);
     if (!ok) atomicExch(p.status, kStatusTimeout);
   }
   ok = __syncthreads_and(ok);
@@ -367,7 +383,6 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   // scale (hi hi + lo hi + hi lo, about 22 significant bits).  Thread (r, hf) holds row r,
   // K columns 32 hf .. 32 hf + 31 of the A operands; B rows are 64 d_k-wide, 128-byte
   // swizzled.
-  int d_issued = 0;
   {
     const int hf = tid >> 7;
     uint8_t* BHI = RV;           // B operand, hi (64 rows x 128 B)
@@ -561,7 +576,17 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
 #pragma unroll
   for (int off = 16; off; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
   if (lane == 0) s_mx[warp] = mt;
-  __syncthreads();  // also: every thread has read its part of T
+  __syncthreads();  // also: every thread has read its part of T, and RK, RV are free
+  const int nx = lin + gridDim.x;
+  if (nx < total) {  // the next chunk's K, V (into the buffers read for the last time above), a, beta
+    if (ok && tid == 0) {
+      ptx::fence_proxy_async_smem();
+      load_kv(nx);
+      ++ld_issued;
+    }
+    a_nx = p.a[row_of(nx)];
+    if (tid < 128) b_nx = p.beta[row_of(nx)];
+  }
   float mxt = 0.f;
 #pragma unroll
   for (int w = 0; w < 8; ++w) mxt = fmaxf(mxt, s_mx[w]);
@@ -605,17 +630,18 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
       }
     ptx::umma_commit(&bar_w);
   }
-  const bool w_issued = ok;
+  w_issued = ok;
   if (ok) {
-    ok = wait_bar(&bar_w, 0);
+    ok = wait_bar(&bar_w, ph);
     if (!ok) atomicExch(p.status, kStatusTimeout);
   }
   ok = __all_sync(0xffffffffu, ok);
   // W: its tile maximum, then hi and lo fp16 of W 2^-ew in the operand layout; U_loc, g.
-  // The chunk's workspace record is put together in shared memory (free: the products
-  // have read their operands), in its global layout, then copied out by all threads with
-  // consecutive 16-byte stores.
-  uint8_t* dst = smem;
+  // The chunk's workspace record is put together in shared memory from T's space on (T's
+  // and V's parts and the small tables, all read for the last time by the products; RK and
+  // RV hold the next chunk's K and V by now), in its global layout, then copied out by all
+  // threads with consecutive 16-byte stores.
+  uint8_t* dst = reinterpret_cast<uint8_t*>(Tm);
   const float sw = pow2s(et + ek), su = pow2s(et + ev);
   // Every thread takes half of its row r: W's d_k columns 64 hf .. 64 hf + 63 (the box hf of
   // the operand layout) and U_loc's d_v columns 32 hf .. 32 hf + 31.
@@ -660,14 +686,21 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   ok = __syncthreads_and(ok);  // the record is complete
   if (ok) {
     uint4* gdst = reinterpret_cast<uint4*>(p.xw + ((size_t)(b * p.H + h) * nch + c) * kGdnChunkBytes);
-    const uint4* ssrc = reinterpret_cast<const uint4*>(smem);
+    const uint4* ssrc = reinterpret_cast<const uint4*>(dst);
     for (int i = tid; i < (int)(kGdnChunkBytes / 16); i += 256) gdst[i] = ssrc[i];
   }
+  ptx::tc_fence_before();
+  __syncthreads();  // the record and TMEM are read before the next chunk writes them
+  if (ok) {
+    a_issued = w_issued = false;
+    d_issued = 0;
+  }
+  }
   if (tid == 0) {  // bounded: let this CTA's copies and MMAs land before TMEM goes
-    wait_bar(&bar_ld, 0);
-    if (a_issued) wait_bar(&bar_a, 0);
+    wait_bar(&bar_ld, (ld_issued - 1) & 1);
+    if (a_issued) wait_bar(&bar_a, ph);
     if (d_issued) wait_bar(&bar_d, (d_issued - 1) & 1);
-    if (w_issued) wait_bar(&bar_w, 0);
+    if (w_issued) wait_bar(&bar_w, ph);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -980,7 +1013,10 @@ cudaError_t launch_tc_gdn_local(const ll_shape& s, const void* k, const void* v,
   if (!tc_gdn_params(s, k, v, a, beta, u, ws, status, &mK, &mV, &p)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_gdn_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGdnL);
   if (e != cudaSuccess) return e;
-  tc_gdn_local_kernel<<<(unsigned)((size_t)s.batch * s.heads * (s.T / kTile)), 256, kSmemGdnL, st>>>(mK, mV, p);
+  // persistent: one CTA per SM (its shared memory allows no more), chunks in turn
+  const size_t total = (size_t)s.batch * s.heads * (s.T / kTile);
+  const unsigned grid = (unsigned)(p.pf_stride > 0 && (size_t)p.pf_stride < total ? p.pf_stride : total);
+  tc_gdn_local_kernel<<<grid, 256, kSmemGdnL, st>>>(mK, mV, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   return cudaSuccess;
