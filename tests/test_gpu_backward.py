@@ -4,7 +4,7 @@ CPU tests.  Called through the C ABI.
 
 The bar is the forward's: relative L2 <= 1e-2 and max |err| <= 5e-2 RMS per gradient,
 the cast of dq, dk, dv to the input dtype charged at half an ulp.  Cases: fp32 and
-bf16, grouped and ungrouped heads, chunk counts that are not powers of two, every chunk
+bf16, one, two and four heads per Q/K group, chunk counts that are not powers of two, every chunk
 length, slow decay (all levels live) and a one-chunk sequence.  bf16 with d_k = 128,
 d_v = 64, T % 128 == 0 and chunk >= 64 takes the tensor-core kernel for the pairs inside
 128-token tiles (T = 1024 and 640 here, the decay cases too); the others the CUDA-core one.
@@ -59,6 +59,15 @@ def test_bf16_grouped(sml, T, chunk):
 def test_bf16_decays(sml, decay):
     w = workload("small", batch=2, heads=2, T=1024, levels=levels_for(1024), decay=decay)
     _check(sml, w, make_inputs(w, "cpu", seed=33), 64, decay)
+
+
+@pytest.mark.parametrize("hpg", [1, 4])
+def test_bf16_group_sizes(sml, hpg):
+    """The tensor-core path with one and four heads per Q/K group (the pages workload has
+    two): dq and dk are the sums over each group's heads."""
+    w = workload("small", batch=1, heads=4, heads_per_group=hpg, T=1024, levels=levels_for(1024),
+                 decay="slow")
+    _check(sml, w, make_inputs(w, "cpu", seed=35), 64, f"hpg={hpg}")
 
 
 def test_ungrouped_small_dims(sml):
