@@ -5,7 +5,8 @@ pinned to the dense matrix recurrence in the CPU tests), through the C ABI.
 Keys are L2-normalised per token, as the model does, and beta = sigmoid(z).  Cases: the
 fp32 generic path, the bf16 tensor-core path, a length that is not a multiple of the
 tile, chunk 16, slow and mamba2 decays, more than one batch element on the tensor-core
-path (the last element's state pass and forward run on a second stream); beta = 0 must
+path (the last element's state pass and forward run on a second stream), and more
+chunks than SMs (the chunk kernel's persistent CTAs take several each); beta = 0 must
 give exactly zero.
 """
 import pytest
@@ -53,6 +54,7 @@ def _run(sml, w, x, beta, chunk):
     ("small", dict(batch=1, heads=4, T=1024, decay="slow"), 64),
     ("small", dict(batch=1, heads=4, T=1024, decay="mamba2"), 64),
     ("small", dict(batch=3, heads=4, T=1024), 64),            # batch split over two streams
+    ("small", dict(batch=2, heads=16, T=1024), 64),           # 256 chunks: persistent CTAs take two
 ])
 def test_gdn_matches_oracle(sml, name, kw, chunk):
     if "T" in kw:
