@@ -26,7 +26,8 @@ namespace {
 // ---------------------------------------------------------------------------------
 // Workspace per (b, h, chunk): W hi, W lo (fp16, 16 KB boxes of 64 d_k columns with the
 // 128-byte swizzle), U_loc (128 x d_v fp32; in each half row of 32 values, 16-byte chunk j
-// stored at j ^ (row & 7)), g (128 fp32), W's scale exponent.
+// stored at j ^ (row & 7)), g (128 fp32), W's scale exponent, then the fp16 scale exponent
+// of the chunk's keys (from their maximum |k|; tc_gdn_pass converts K with it).
 constexpr int kGdnOffU = 65536, kGdnOffG = 65536 + 32768, kGdnOffE = kGdnOffG + 512;
 constexpr size_t kGdnChunkBytes = 99328;
 
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
   __shared__ uint32_t tmem_base;
   __shared__ float s_red[8];
   __shared__ float s_mx[8];
-  __shared__ float s_kv[4][2];
+  __shared__ float s_kv[4][3];
   __shared__ float s_m3[8][3];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
@@ -325,15 +326,18 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
                        *reinterpret_cast<const uint4*>(RK + 16384 + off));
         m1 = absmax_u4(m1, *reinterpret_cast<const uint4*>(RV + off));
       }
-      float mk = bf16x2_maxhalf(m0) * fabsf(fk[r]), mv = bf16x2_maxhalf(m1) * fabsf(bs[r]);
+      float kr = bf16x2_maxhalf(m0);
+      float mk = kr * fabsf(fk[r]), mv = bf16x2_maxhalf(m1) * fabsf(bs[r]);
 #pragma unroll
       for (int off = 16; off; off >>= 1) {
         mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
         mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+        kr = fmaxf(kr, __shfl_xor_sync(0xffffffffu, kr, off));
       }
       if (lane == 0) {
         s_kv[warp - 4][0] = mk;
         s_kv[warp - 4][1] = mv;
+        s_kv[warp - 4][2] = kr;
       }
       ptx::named_bar_sync(1, 128);
       const int ev = f16_exp(fmaxf(fmaxf(s_kv[0][1], s_kv[1][1]), fmaxf(s_kv[2][1], s_kv[3][1])));
@@ -681,7 +685,11 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
             make_float4(su * y[4 * j], su * y[4 * j + 1], su * y[4 * j + 2], su * y[4 * j + 3]);
     }
     if (hf == 0) reinterpret_cast<float*>(dst + kGdnOffG)[r] = gt;
-    if (tid == 0) *reinterpret_cast<int*>(dst + kGdnOffE) = ew;
+    if (tid == 0) {
+      *reinterpret_cast<int*>(dst + kGdnOffE) = ew;
+      *reinterpret_cast<int*>(dst + kGdnOffE + 4) =
+          f16_exp(fmaxf(fmaxf(s_kv[0][2], s_kv[1][2]), fmaxf(s_kv[2][2], s_kv[3][2])));
+    }
   }
   ok = __syncthreads_and(ok);  // the record is complete
   if (ok) {
@@ -713,7 +721,8 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_local_kernel(const __grid_const
 //   u = U_loc - Z, written in bf16; ũ = 2^(g_end - g) u -> fp16 hi, lo; K -> fp16;
 //   Ŝ <- Ŝ 2^(g_end + sigma - sigma') in TMEM, then Ŝ += Kᵀ (ũ hi + ũ lo) with
 //   sigma' = the scales of K and ũ.  W (hi and lo) is copied one chunk ahead, K by TMA
-//   behind the product W S.
+//   behind the product W S; K's fp16 scale comes with the chunk's record, so each thread
+//   converts its row of K while W S runs.
 constexpr int kSmemGdnP = 2 * 65536 + 3 * 32768 + 1024;
 
 __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_constant__ CUtensorMap mapK,
@@ -803,6 +812,7 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_consta
       if (tid < 128) sg[r] = reinterpret_cast<const float*>(xc + kGdnOffG)[r];
     }
     const int ew = *reinterpret_cast<const int*>(xc + kGdnOffE);
+    const int ek = *reinterpret_cast<const int*>(xc + kGdnOffE + 4);
     // Ŝ (lane r = d_k row), with the fp16 scale of its running bound (no block maximum)
     float sv[32];
     ptx::tc_fence_after();
@@ -845,9 +855,25 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_consta
         atomicExch(p.status, kStatusTimeout);
       }
     }
+    // K of this chunk (by TMA, issued after the last chunk's Kᵀ ũ): this thread's half row
+    // to fp16 2^-ek in place, while W S runs
+    uint8_t* krow = RK + hf * 16384 + r * 128;
+    const bool okk = wait_bar(&bar_k, c & 1);
+    if (okk) {
+      if (tid == 0) ++k_done;
+      const float sk = pow2i(-ek);
+      const __nv_bfloat162 k2 = __floats2bfloat162_rn(sk, sk);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint4* x = reinterpret_cast<uint4*>(krow + ((cc ^ rot) << 4));
+        *x = bf16x8_to_f16x8(*x, k2);
+      }
+    } else {
+      atomicExch(p.status, kStatusTimeout);
+    }
     bool okz = wait_bar(&bar_z, c & 1);
     if (!okz) atomicExch(p.status, kStatusTimeout);
-    okz = __syncthreads_and(okz);
+    okz = __syncthreads_and(okz && okk);
     if (okz) ++z_done;
     if (!okz) {
       ok = false;
@@ -876,41 +902,16 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_consta
 #pragma unroll
       for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
     }
-    // K of this chunk (by TMA, behind W S): tile maximum
-    bool okk = true;
-    if (tid == 0) {
-      okk = wait_bar(&bar_k, c & 1);
-      if (okk) ++k_done;
-      else atomicExch(p.status, kStatusTimeout);
-    }
-    okk = __syncthreads_and(okk);
-    if (!okk) {
-      ok = false;
-      break;
-    }
-    uint8_t* krow = RK + hf * 16384 + r * 128;  // this thread's box of key row r
-    uint32_t mk = 0u;
+    // ũ's tile maximum
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) mk = absmax_u4(mk, *reinterpret_cast<const uint4*>(krow + ((cc ^ rot) << 4)));
-    float fk = bf16x2_maxhalf(mk);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
-      fk = fmaxf(fk, __shfl_xor_sync(0xffffffffu, fk, off));
-    }
-    if (lane == 0) {
-      s_mx[warp][0] = mu;
-      s_mx[warp][1] = fk;
-    }
+    for (int off = 16; off; off >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
+    if (lane == 0) s_mx[warp][0] = mu;
     __syncthreads();
-    float mxu = 0.f, mxk = 0.f;
+    float mxu = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      mxu = fmaxf(mxu, s_mx[w][0]);
-      mxk = fmaxf(mxk, s_mx[w][1]);
-    }
-    const int eu = f16_exp(mxu), ek = f16_exp(mxk);
-    {  // ũ 2^-eu -> hi, lo (row r = token, d_v columns 32 hf ..); K -> fp16 2^-ek in place
+    for (int w = 0; w < 8; ++w) mxu = fmaxf(mxu, s_mx[w][0]);
+    const int eu = f16_exp(mxu);
+    {  // ũ 2^-eu -> hi, lo (row r = token, d_v columns 32 hf ..)
       const float sc = pow2i(-eu);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
@@ -921,13 +922,6 @@ __global__ void __launch_bounds__(256, 1) tc_gdn_pass_kernel(const __grid_consta
         const int off = r * 128 + (((4 * hf + q4) ^ rot) << 4);
         *reinterpret_cast<uint4*>(RU + off) = hi;
         *reinterpret_cast<uint4*>(RU + 16384 + off) = lo;
-      }
-      const float sk = pow2i(-ek);
-      const __nv_bfloat162 k2 = __floats2bfloat162_rn(sk, sk);
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint4* x = reinterpret_cast<uint4*>(krow + ((cc ^ rot) << 4));
-        *x = bf16x8_to_f16x8(*x, k2);
       }
     }
     // Ŝ <- Ŝ 2^(g_end + sigma - (ek + eu)) (the new scale of the state)
