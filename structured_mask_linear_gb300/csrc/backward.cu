@@ -554,9 +554,19 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
   const int tc_base = p.M > 1 ? p.blk_off[1] : 0, tc_slots = p.nblk - tc_base;
   int tc_dual_off[32];
   for (int m = 0; m < 32; ++m) tc_dual_off[m] = m + 1 < p.M ? p.blk_off[m + 1] - tc_base : 0;  // chunk level m + 1
-  const size_t nslot_zero = (size_t)BH * (bp.tc ? tc_slots : p.nblk);
-  if ((e = cudaMemsetAsync(x.ws + bp.off_dual, 0, sizeof(float) * nslot_zero * dk * dv, st)) != cudaSuccess)
-    return e;
+  // The duals start at zero, except, on the tensor-core path with an even tile count, those
+  // of the tile nodes (tile level 0, the first slots of each (b, h)): each has one reader
+  // tile, whose tc_bwd_q CTA stores it.
+  const size_t S = (size_t)dk * dv * sizeof(float);
+  const size_t n0 = bp.tc && bp.tp.NT % 2 == 0 && bp.tp.MT > 1 ? (size_t)tc_dual_off[1] : 0;
+  if (n0 > 0) {
+    if ((e = cudaMemset2DAsync(x.ws + bp.off_dual + n0 * S, tc_slots * S, 0, (tc_slots - n0) * S, BH, st)) !=
+        cudaSuccess)
+      return e;
+  } else {
+    const size_t nslot_zero = (size_t)BH * (bp.tc ? tc_slots : p.nblk);
+    if ((e = cudaMemsetAsync(x.ws + bp.off_dual, 0, nslot_zero * S, st)) != cudaSuccess) return e;
+  }
   // the pairs inside 128-token tiles (two 64-token chunks) on the tensor cores where the
   // shape allows; the inter-chunk kernels then start at chunk level 1, and the query side
   // of those levels runs on the tensor cores over the forward's tree of tile nodes

@@ -791,9 +791,16 @@ __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant_
       ptx::tmem_ld_wait();
       const int nd = (u >> m) - 1;  // even
       float* dst = p.dual + (((size_t)bh * p.nslots + p.dual_off[m] + (nd >> 1)) * kDk + r) * kDv + hf * 32;
+      if (m == 0) {  // a tile node's dual has one reader tile, this one: stored, not added
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        atomicAdd(reinterpret_cast<float4*>(dst + j), make_float4(su * y[j], su * y[j + 1], su * y[j + 2], su * y[j + 3]));
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(dst + j) = make_float4(su * y[j], su * y[j + 1], su * y[j + 2], su * y[j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          atomicAdd(reinterpret_cast<float4*>(dst + j),
+                    make_float4(su * y[j], su * y[j + 1], su * y[j + 2], su * y[j + 3]));
+      }
     }
     D += sNode[i][1];
     if (i + 1 < nlev) {  // diag(w) dO of the next level (its MMA has read this one)
