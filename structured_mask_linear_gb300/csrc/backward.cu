@@ -555,8 +555,8 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
   int tc_dual_off[32];
   for (int m = 0; m < 32; ++m) tc_dual_off[m] = m + 1 < p.M ? p.blk_off[m + 1] - tc_base : 0;  // chunk level m + 1
   // The duals start at zero, except, on the tensor-core path with an even tile count, those
-  // of the tile nodes (tile level 0, the first slots of each (b, h)): each has one reader
-  // tile, whose tc_bwd_q CTA stores it.
+  // of the tile nodes (tile level 0, the first n0 slots of each (b, h)): each has one reader
+  // tile, whose tc_bwd_q CTA publishes it as an fp16 image straight away.
   const size_t S = (size_t)dk * dv * sizeof(float);
   const size_t n0 = bp.tc && bp.tp.NT % 2 == 0 && bp.tp.MT > 1 ? (size_t)tc_dual_off[1] : 0;
   if (n0 > 0) {
@@ -598,7 +598,9 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
   if (tc) {
     if ((e = launch_tc_bwd_q(bp.tp, x.q, x.dO, x.a, x.lam, x.ws + bp.off_tc, reinterpret_cast<float*>(x.ws + bp.off_dq),
                              x.dlam, reinterpret_cast<float*>(x.ws + bp.off_dual), tc_dual_off, tc_slots,
-                             reinterpret_cast<float*>(x.ws + bp.off_cu) + (size_t)p.B * p.T * p.H, fa.status,
+                             reinterpret_cast<float*>(x.ws + bp.off_cu) + (size_t)p.B * p.T * p.H,
+                             n0 > 0 ? reinterpret_cast<uint8_t*>(x.ws + bp.off_dimg) : nullptr,
+                             n0 > 0 ? reinterpret_cast<unsigned*>(x.ws + bp.off_dmeta) : nullptr, fa.status,
                              st)) != cudaSuccess)
       return e;
   } else {
@@ -610,7 +612,7 @@ cudaError_t run_bwd(const ll_shape& s, const BwdPlan& bp, const BwdArgs& x, cons
     if ((e = launch_tc_bwd_kv(bp.tp, x.k, x.v, x.a, x.ws + bp.off_tc, reinterpret_cast<const float*>(x.ws + bp.off_dual),
                               reinterpret_cast<uint8_t*>(x.ws + bp.off_dimg),
                               reinterpret_cast<unsigned*>(x.ws + bp.off_dmeta),
-                              reinterpret_cast<double*>(x.ws + bp.off_P), tc_dual_off, tc_slots,
+                              reinterpret_cast<double*>(x.ws + bp.off_P), tc_dual_off, tc_slots, (int)n0,
                               reinterpret_cast<float*>(x.ws + bp.off_dk), reinterpret_cast<float*>(x.ws + bp.off_dv), x.dv,
                               reinterpret_cast<float*>(x.ws + bp.off_cu), fa.status, st)) != cudaSuccess)
       return e;

@@ -143,19 +143,24 @@ cudaError_t launch_tc_export_only(const TcPlan& p, const FwdArgs& a, cudaStream_
 size_t tc_prefix_bytes(const TcPlan& p, int npre);
 // Backward, query side of the inter-tile levels on the tensor cores: adds into dq32,
 // assigns dlambda levels >= 8 of the set bits, adds the nodes' duals (dual slot of the
-// even node (m, i): dual_off[m] + i / 2, nslots per (b, h); dual zero before the first call),
-// and adds sum_m lambda_t^(8+m) dlambda_t^(8+m) into ru (B, T, H) of the tiles it runs.
+// even node (m, i): dual_off[m] + i / 2, nslots per (b, h); dual zero before the first call,
+// except the tile nodes' (m = 0), which their one reader tile stores), and adds
+// sum_m lambda_t^(8+m) dlambda_t^(8+m) into ru (B, T, H) of the tiles it runs.  With dimg0
+// and dmeta0 given, the tile nodes' duals go straight to their fp16 images and scale
+// exponents there (the layout tc_dual_publish writes) instead of to dual.
 cudaError_t launch_tc_bwd_q(const TcPlan& p, const void* q, const void* dO, const float* a, const float* lam,
                             const char* tree_ws, float* dq32, float* dlam, float* dual, const int* dual_off,
-                            int nslots, float* ru, unsigned* status, cudaStream_t st);
+                            int nslots, float* ru, uint8_t* dimg0, unsigned* dmeta0, unsigned* status,
+                            cudaStream_t st);
 // Backward, key side of the inter-tile levels on the tensor cores: the tile-decay running
-// sums (fp64, (B*H, NT+1) in P), the duals as fp16 images (dimg: 16 KB per slot, dmeta: 4
-// u32 per slot), then adds into dk32, writes dv_out (bf16, (B, T, H, d_v)) as dv32 (the
+// sums (fp64, (B*H, NT+1) in P), the duals of slots n0.. of each (b, h) as fp16 images
+// (dimg: 16 KB per slot, dmeta: 4 u32 per slot; slots below n0 are published by
+// launch_tc_bwd_q), then adds into dk32, writes dv_out (bf16, (B, T, H, d_v)) as dv32 (the
 // in-tile part) plus its own part, and adds v_s . (its part of dv_s) into cu.
 cudaError_t launch_tc_bwd_kv(const TcPlan& p, const void* k, const void* v, const float* a, const char* tree_ws,
                              const float* dual, uint8_t* dimg, unsigned* dmeta, double* P, const int* dual_off,
-                             int nslots, float* dk32, float* dv32, void* dv_out, float* cu, unsigned* status,
-                             cudaStream_t st);
+                             int nslots, int n0, float* dk32, float* dv32, void* dv_out, float* cu,
+                             unsigned* status, cudaStream_t st);
 // Backward: the in-tile pairs (levels 0..7) on the tensor cores, for tc_supported shapes;
 // assigns the fp32 per-head dq, dk, dv buffers, dlambda (levels >= 8 zeroed) and cu, the
 // column sums C_s of the in-tile pair terms, followed in the same buffer by R_t = sum over

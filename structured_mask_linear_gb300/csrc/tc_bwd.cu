@@ -531,6 +531,10 @@ struct TcBwdQParams {
   float* dlam;
   float* dual;        // (B*H, nslots, d_k, d_v) fp32, zero on entry
   float* ru;          // (B, T, H): R_t, to which the inter-tile levels' lambda dlambda is added
+  // non-null: a tile node's dual (one reader tile, this one) goes straight to its fp16
+  // image (dimg: 16 KB per slot) and scale exponent (dmeta[slot * kMeta + 1]), not to dual
+  uint8_t* dimg;
+  unsigned* dmeta;
   unsigned* status;
 };
 
@@ -556,6 +560,7 @@ __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant_
   __shared__ float s_mx[8][2];
   __shared__ unsigned s_lmax[32];
   __shared__ float sNode[32][2];  // per level index: scale exponent (bits), log2 decay
+  __shared__ float s_dmx[8];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = tid & 127, hf = tid >> 7, quad = warp & 3, rot = r & 7;
@@ -790,8 +795,37 @@ __global__ void __launch_bounds__(256, 2) tc_bwd_q_kernel(const __grid_constant_
       ptx::tmem_ld32(tU + lane_off + hf * 32, y);
       ptx::tmem_ld_wait();
       const int nd = (u >> m) - 1;  // even
-      float* dst = p.dual + (((size_t)bh * p.nslots + p.dual_off[m] + (nd >> 1)) * kDk + r) * kDv + hf * 32;
-      if (m == 0) {  // a tile node's dual has one reader tile, this one: stored, not added
+      const size_t slot = (size_t)bh * p.nslots + p.dual_off[m] + (nd >> 1);
+      float* dst = p.dual + (slot * kDk + r) * kDv + hf * 32;
+      if (m == 0 && p.dimg) {  // a tile node's dual, complete here: its fp16 image and scale
+        float mx = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          y[j] *= su;
+          mx = fmaxf(mx, fabsf(y[j]));
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) s_dmx[warp] = mx;
+        __syncthreads();
+        float bm = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) bm = fmaxf(bm, s_dmx[w]);
+        const int e = f16_exp(bm);
+        const float sc = pow2i(-e);
+        uint8_t* im = p.dimg + slot * kImgBytes + r * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {  // columns 32 hf + 8 q4 ..: the row's 16-byte chunk 4 hf + q4
+          const float* x = y + 8 * q4;
+          *reinterpret_cast<uint4*>(im + (((4 * hf + q4) ^ rot) << 4)) =
+              make_uint4(pack_h2(x[0] * sc, x[1] * sc), pack_h2(x[2] * sc, x[3] * sc), pack_h2(x[4] * sc, x[5] * sc),
+                         pack_h2(x[6] * sc, x[7] * sc));
+        }
+        if (tid == 0) {
+          p.dmeta[slot * kMeta + 1] = (unsigned)e;
+          p.dmeta[slot * kMeta + 2] = __float_as_uint(0.f);
+        }
+      } else if (m == 0) {  // a tile node's dual has one reader tile, this one: stored, not added
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
           *reinterpret_cast<float4*>(dst + j) = make_float4(su * y[j], su * y[j + 1], su * y[j + 2], su * y[j + 3]);
@@ -893,11 +927,13 @@ __global__ void __launch_bounds__(256) tc_tile_prefix_kernel(const unsigned* met
 // scale, as a node is published.  The threads read the slot in consecutive 16-byte pieces
 // (thread i: pieces i, i + 128, ...), not a row each, so that every warp load is four whole
 // 128-byte lines; each piece is half of a 16-byte chunk of the image.
-__global__ void __launch_bounds__(128) tc_dual_publish_kernel(const float* dual, uint8_t* img, unsigned* meta) {
+__global__ void __launch_bounds__(128) tc_dual_publish_kernel(const float* dual, uint8_t* img, unsigned* meta,
+                                                              int nslots, int n0) {
   __shared__ __align__(1024) uint8_t stage[kImgBytes];
   __shared__ float2 s_red2[4];
   const int tid = threadIdx.x;
-  const size_t slot = blockIdx.x;
+  // slots n0 .. nslots - 1 of each (b, h) (those below n0 were published by tc_bwd_q)
+  const size_t slot = (size_t)(blockIdx.x / (nslots - n0)) * nslots + n0 + blockIdx.x % (nslots - n0);
   const float4* src = reinterpret_cast<const float4*>(dual + slot * kDk * kDv);
   constexpr int kPieces = kDk * kDv / 4 / 128;  // 16 per thread
   float4 v[kPieces];
@@ -1276,7 +1312,8 @@ cudaError_t launch_tc_bwd_intra(const ll_shape& s, const void* q, const void* k,
 
 cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, const float* a, const float* lam,
                             const char* tree_ws, float* dq32, float* dlam, float* dual, const int* dual_off,
-                            int nslots, float* ru, unsigned* status, cudaStream_t st) {
+                            int nslots, float* ru, uint8_t* dimg0, unsigned* dmeta0, unsigned* status,
+                            cudaStream_t st) {
   CUtensorMap mQ, mD, mDQ;
   if (!make_map(&mQ, q, kDk, tp.G, tp.T, tp.B) || !make_map(&mD, dO, kDv, tp.H, tp.T, tp.B) ||
       !make_map_f32(&mDQ, dq32, kDk, tp.H, tp.T, tp.B))
@@ -1303,6 +1340,8 @@ cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, con
   p.dlam = dlam;
   p.dual = dual;
   p.ru = ru;
+  p.dimg = dimg0;
+  p.dmeta = dmeta0;
   p.status = status;
   const int smem = bwdq_smem_bytes(bit_length(tp.NT - 1));
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1315,15 +1354,16 @@ cudaError_t launch_tc_bwd_q(const TcPlan& tp, const void* q, const void* dO, con
 
 cudaError_t launch_tc_bwd_kv(const TcPlan& tp, const void* k, const void* v, const float* a, const char* tree_ws,
                              const float* dual, uint8_t* dimg, unsigned* dmeta, double* P, const int* dual_off,
-                             int nslots, float* dk32, float* dv32, void* dv_out, float* cu, unsigned* status,
-                             cudaStream_t st) {
+                             int nslots, int n0, float* dk32, float* dv32, void* dv_out, float* cu,
+                             unsigned* status, cudaStream_t st) {
   const unsigned BH = (unsigned)(tp.B * tp.H);
   tc_tile_prefix_kernel<<<BH, 256, 0, st>>>(reinterpret_cast<const unsigned*>(tree_ws + tp.off_meta), tp.nnodes,
                                             tp.NT, P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   note_launch();
-  tc_dual_publish_kernel<<<(unsigned)((size_t)BH * nslots), 128, 0, st>>>(dual, dimg, dmeta);
+  if (n0 < 0 || n0 >= nslots) return cudaErrorInvalidValue;
+  tc_dual_publish_kernel<<<(unsigned)((size_t)BH * (nslots - n0)), 128, 0, st>>>(dual, dimg, dmeta, nslots, n0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   note_launch();
   CUtensorMap mK, mV, mDK, mDV, mDVO;
